@@ -1,0 +1,374 @@
+"""CPU oracle for the OCP-MX training MLP -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never links or
+calls it, and it never imports the product package.
+
+What it computes, and from which passage (web pages cited by title):
+
+* Element codecs, exact RCEIL E8M0 scales, the blocked scale layout, packing
+  and the 32-point Hadamard rotation live in ``mx_oracle.c`` (plain C,
+  float64), wrapped here.  See that file's header for the readings it fixes.
+* GEMMs are float64 matrix products of the *dequantized* operands
+  (torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP fwd/bwd and wgrad
+  group gemm", shared-infrastructure commit: ragged grouped GEMM where each
+  128-row-aligned segment uses its expert's weights; ragged-K wgrad where an
+  expert with zero tokens gets a zero gradient).
+* SwiGLU: h = g * sigmoid(g) * u with z = [g | u] the concatenated FC1
+  halves, sigmoid = 1/(1+exp(-x)) (same PR, correctness-first kernels
+  commit); dSwiGLU is its derivative, taken from the BF16-saved z.
+* tanh-GELU MLP with bias added to the fp32 accumulator before one rounding
+  (Primus PR #1064 "feat(mxfp6): MXFP6 (E2M3) Flux linears, a fused MLP, and
+  the MLPerf recipe", fused-MLP and bias-in-epilogue commits).
+
+Where floating point decides a quantized code inside a fused epilogue, the
+oracle rounds the float64 value to fp32 first -- the arithmetic type the
+epilogue quantizes from -- and then quantizes exactly.
+"""
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+E4M3, E2M3, E2M1 = 0, 1, 2
+FMT_NAMES = {E4M3: "e4m3", E2M3: "e2m3", E2M1: "e2m1"}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        dp = ctypes.POINTER(ctypes.c_double)
+        fp = ctypes.POINTER(ctypes.c_float)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        i64 = ctypes.c_int64
+        L.orc_decode.restype = ctypes.c_double
+        L.orc_decode.argtypes = [ctypes.c_uint8, ctypes.c_int]
+        L.orc_encode.restype = ctypes.c_uint8
+        L.orc_encode.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.orc_fmt_max.restype = ctypes.c_double
+        L.orc_fmt_max.argtypes = [ctypes.c_int]
+        L.orc_fmt_bits.restype = ctypes.c_int
+        L.orc_fmt_bits.argtypes = [ctypes.c_int]
+        L.orc_scale_exp.restype = ctypes.c_int
+        L.orc_scale_exp.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.orc_scale_byte.restype = ctypes.c_uint8
+        L.orc_scale_byte.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.orc_amax.restype = ctypes.c_double
+        L.orc_amax.argtypes = [dp, i64]
+        L.orc_quantize_block.restype = ctypes.c_uint8
+        L.orc_quantize_block.argtypes = [dp, ctypes.c_int, u8p]
+        L.orc_scale_bytes.restype = i64
+        L.orc_scale_bytes.argtypes = [i64, i64]
+        L.orc_blocked_offset.restype = i64
+        L.orc_blocked_offset.argtypes = [i64, i64, i64]
+        L.orc_payload_row_bytes.restype = i64
+        L.orc_payload_row_bytes.argtypes = [i64, ctypes.c_int]
+        L.orc_pack_row.argtypes = [u8p, i64, ctypes.c_int, u8p]
+        L.orc_unpack_row.argtypes = [u8p, i64, ctypes.c_int, u8p]
+        L.orc_hadamard32_f32.argtypes = [fp]
+        L.orc_hadamard32_f64.argtypes = [dp, dp]
+        L.orc_bf16_to_f64.restype = ctypes.c_double
+        L.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        L.orc_f64_to_bf16.restype = ctypes.c_uint16
+        L.orc_f64_to_bf16.argtypes = [ctypes.c_double]
+        L.orc_quantize_rows.argtypes = [dp, i64, i64, ctypes.c_int, ctypes.c_int, u8p, u8p]
+        L.orc_dequantize_rows.argtypes = [u8p, u8p, i64, i64, ctypes.c_int, dp]
+        L.orc_bf16_to_f64_array.argtypes = [u16p, i64, dp]
+        L.orc_f64_to_bf16_array.argtypes = [dp, i64, u16p]
+        L.orc_round_f32_array.argtypes = [dp, i64, dp]
+        _lib = L
+    return _lib
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+# --------------------------------------------------------------------------
+# Scalar codecs
+# --------------------------------------------------------------------------
+
+def encode(v, fmt):
+    return int(lib().orc_encode(float(v), fmt))
+
+
+def decode(code, fmt):
+    return float(lib().orc_decode(int(code), fmt))
+
+
+def fmt_max(fmt):
+    return float(lib().orc_fmt_max(fmt))
+
+
+def scale_exp(amax, fmt):
+    return int(lib().orc_scale_exp(float(amax), fmt))
+
+
+def scale_byte(amax, fmt):
+    return int(lib().orc_scale_byte(float(amax), fmt))
+
+
+def quantize_block(x, fmt):
+    """One block of 32 float64 values -> (scale byte, 32 unpacked codes)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    assert x.shape == (32,)
+    codes = np.zeros(32, dtype=np.uint8)
+    sb = lib().orc_quantize_block(_ptr(x, ctypes.c_double), fmt, _ptr(codes, ctypes.c_uint8))
+    return int(sb), codes
+
+
+def blocked_offset(r, c, scale_cols):
+    return int(lib().orc_blocked_offset(r, c, scale_cols))
+
+
+def scale_bytes(rows, scale_cols):
+    return int(lib().orc_scale_bytes(rows, scale_cols))
+
+
+def payload_row_bytes(cols, fmt):
+    return int(lib().orc_payload_row_bytes(cols, fmt))
+
+
+def hadamard32_f32(v):
+    v = np.array(v, dtype=np.float32).copy()
+    lib().orc_hadamard32_f32(_ptr(v, ctypes.c_float))
+    return v
+
+
+def hadamard32_f64(v):
+    x = np.ascontiguousarray(v, dtype=np.float64)
+    y = np.zeros(32, dtype=np.float64)
+    lib().orc_hadamard32_f64(_ptr(x, ctypes.c_double), _ptr(y, ctypes.c_double))
+    return y
+
+
+# --------------------------------------------------------------------------
+# Array conversions
+# --------------------------------------------------------------------------
+
+def bf16_to_f64(bits):
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float64)
+    lib().orc_bf16_to_f64_array(_ptr(bits, ctypes.c_uint16), bits.size, _ptr(out, ctypes.c_double))
+    return out
+
+
+def f64_to_bf16(x):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_f64_to_bf16_array(_ptr(x, ctypes.c_double), x.size, _ptr(out, ctypes.c_uint16))
+    return out
+
+
+def round_f32(x):
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.float64)
+    lib().orc_round_f32_array(_ptr(x, ctypes.c_double), x.size, _ptr(out, ctypes.c_double))
+    return out
+
+
+# --------------------------------------------------------------------------
+# Whole-tensor quantization
+# --------------------------------------------------------------------------
+
+def quantize_rows(x, fmt, hadamard=False):
+    """Rowwise 1x32 quantization of float64 [rows, cols].
+
+    Returns (payload uint8 [rows, payload_row_bytes], scales uint8 blocked)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    payload = np.zeros((rows, payload_row_bytes(cols, fmt)), dtype=np.uint8)
+    scales = np.zeros(scale_bytes(rows, cols // 32), dtype=np.uint8)
+    lib().orc_quantize_rows(_ptr(x, ctypes.c_double), rows, cols, fmt, 1 if hadamard else 0,
+                            _ptr(payload, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return payload, scales
+
+
+def quantize_cols(x, fmt, hadamard=False):
+    """Columnwise 32x1 quantization of [rows, cols]: blocks of 32 rows, stored
+    as the rowwise quantization of the transpose, payload [cols, rows]."""
+    return quantize_rows(np.ascontiguousarray(np.asarray(x, dtype=np.float64).T), fmt, hadamard)
+
+
+def dequantize_rows(payload, scales, rows, cols, fmt):
+    payload = np.ascontiguousarray(payload, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    out = np.empty((rows, cols), dtype=np.float64)
+    lib().orc_dequantize_rows(_ptr(payload, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8),
+                              rows, cols, fmt, _ptr(out, ctypes.c_double))
+    return out
+
+
+def blocked_index(rows, scale_cols):
+    """int64 [rows, scale_cols] array of blocked-layout byte offsets."""
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    c = np.arange(scale_cols, dtype=np.int64)[None, :]
+    cpad = (scale_cols + 3) // 4 * 4
+    # same closed form as orc_blocked_offset, vectorised; tests check they agree
+    return ((r // 128) * (cpad // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (c % 4)
+
+
+def scales_to_matrix(scales, rows, scale_cols):
+    """Blocked scale bytes -> logical [rows, scale_cols] matrix."""
+    return np.asarray(scales, dtype=np.uint8)[blocked_index(rows, scale_cols)]
+
+
+def quantize_bf16(x_bits, fmt, row=True, col=True, hadamard=False):
+    """Quantize a BF16 tensor [R, C] (or a batch [B, R, C]) in one or both
+    orientations.  Column outputs are per batch entry: payload [B, C, R']."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    batched = x_bits.ndim == 3
+    xb = x_bits if batched else x_bits[None]
+    out = {"row_payload": [], "row_scales": [], "col_payload": [], "col_scales": []}
+    for b in range(xb.shape[0]):
+        x = bf16_to_f64(xb[b])
+        if row:
+            p, s = quantize_rows(x, fmt, hadamard)
+            out["row_payload"].append(p)
+            out["row_scales"].append(s)
+        if col:
+            p, s = quantize_cols(x, fmt, hadamard)
+            out["col_payload"].append(p)
+            out["col_scales"].append(s)
+    res = {}
+    for k, v in out.items():
+        if v:
+            res[k] = np.stack(v) if batched else v[0]
+    return res
+
+
+def colsum(x):
+    """Per-column sum over rows of a float64 [rows, cols] array (bias gradient)."""
+    return np.asarray(x, dtype=np.float64).sum(axis=0)
+
+
+# --------------------------------------------------------------------------
+# GEMMs on dequantized operands (float64)
+# --------------------------------------------------------------------------
+
+def segments(offsets):
+    """Cumulative end offsets -> list of (start, end)."""
+    out, start = [], 0
+    for end in np.asarray(offsets, dtype=np.int64).tolist():
+        out.append((start, int(end)))
+        start = int(end)
+    return out
+
+
+def grouped_gemm(a, b, offsets):
+    """out[r, n] = sum_k a[r, k] * b[g, n, k] for r in expert g's segment.
+
+    a float64 [R, K]; b float64 [G, N, K]; rows past offsets[-1] are NaN
+    (never produced)."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    out = np.full((a.shape[0], b.shape[1]), np.nan)
+    for g, (s, e) in enumerate(segments(offsets)):
+        if e > s:
+            out[s:e] = a[s:e] @ b[g].T
+    return out
+
+
+def wgrad(a_col, b_col, offsets):
+    """dW[g, n, k] = sum over r in segment g of a_col[n, r] * b_col[k, r].
+
+    a_col float64 [N, R], b_col float64 [K, R] (columnwise operands stored
+    transposed).  An empty segment gives an exactly zero slice."""
+    a_col = np.asarray(a_col, dtype=np.float64)
+    b_col = np.asarray(b_col, dtype=np.float64)
+    segs = segments(offsets)
+    out = np.zeros((len(segs), a_col.shape[0], b_col.shape[0]))
+    for g, (s, e) in enumerate(segs):
+        if e > s:
+            out[g] = a_col[:, s:e] @ b_col[:, s:e].T
+    return out
+
+
+# --------------------------------------------------------------------------
+# Activations (float64)
+# --------------------------------------------------------------------------
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-np.asarray(x, dtype=np.float64)))
+
+
+def swiglu(g, u):
+    return g * sigmoid(g) * u
+
+
+def dswiglu(dh, g, u):
+    s = sigmoid(g)
+    dg = dh * u * s * (1.0 + g * (1.0 - s))
+    du = dh * g * s
+    return dg, du
+
+
+_GELU_C = math.sqrt(2.0 / math.pi)
+
+
+def gelu_tanh(x):
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(_GELU_C * (x + 0.044715 * x ** 3)))
+
+
+def dgelu_tanh(x):
+    x = np.asarray(x, dtype=np.float64)
+    t = np.tanh(_GELU_C * (x + 0.044715 * x ** 3))
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * _GELU_C * (1.0 + 3 * 0.044715 * x * x)
+
+
+# --------------------------------------------------------------------------
+# Fused stages: what each library call computes
+# --------------------------------------------------------------------------
+
+def _active_rows(offsets):
+    return int(np.asarray(offsets, dtype=np.int64)[-1]) if len(offsets) else 0
+
+
+def swiglu_fwd(x_deq, w1_deq, offsets, fmt=E4M3):
+    """FC1 grouped GEMM + SwiGLU + dual requant + BF16 pre-activation save.
+
+    x_deq float64 [R, D] (dequantized rowwise X), w1_deq float64 [G, 2F, D].
+    Returns z (float64), z_bf16 (uint16 bits), h (fp32-rounded float64),
+    h_row (payload, scales) over the active rows, h_col (payload, scales) of
+    [F, A] where A = offsets[-1]."""
+    A = _active_rows(offsets)
+    z = grouped_gemm(x_deq, w1_deq, offsets)
+    F = z.shape[1] // 2
+    za = z[:A]
+    h = round_f32(swiglu(za[:, :F], za[:, F:]))
+    return {
+        "z": z,
+        "z_bf16": f64_to_bf16(za),
+        "h": h,
+        "h_row": quantize_rows(h, fmt),
+        "h_col": quantize_cols(h, fmt),
+    }
+
+
+def dswiglu_bwd(dy_deq, w2t_deq, z_bf16, offsets, fmt=E4M3):
+    """FC2 dgrad grouped GEMM + dSwiGLU from the BF16-saved z + dual requant.
+
+    dy_deq float64 [R, D]; w2t_deq float64 [G, F, D]; z_bf16 uint16 [>=A, 2F].
+    Returns dh (float64), dz = [dg | du] (fp32-rounded), dz_row, dz_col."""
+    A = _active_rows(offsets)
+    dh = grouped_gemm(dy_deq, w2t_deq, offsets)[:A]
+    z = bf16_to_f64(np.asarray(z_bf16)[:A])
+    F = dh.shape[1]
+    dg, du = dswiglu(dh, z[:, :F], z[:, F:])
+    dz = round_f32(np.concatenate([dg, du], axis=1))
+    return {"dh": dh, "dz": dz, "dz_row": quantize_rows(dz, fmt), "dz_col": quantize_cols(dz, fmt)}
+
+
+def bf16_out(x):
+    """float64 -> BF16 bits -> float64 (the value a BF16 output holds)."""
+    return bf16_to_f64(f64_to_bf16(x))

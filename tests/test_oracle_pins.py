@@ -1,0 +1,378 @@
+"""Pins for the CPU oracle against things other than itself.
+
+Each test checks the oracle against a fixed external fact: hand-derived
+codes (tests/golden), the library casts the pages say the E4M3 bytes match,
+a bit-level closed form of RCEIL, brute force over every BF16 pattern,
+algebraic identities of the Hadamard rotation, finite-difference derivatives
+and exact rational GEMMs on tiny inputs.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+FMT = {"e4m3": O.E4M3, "e2m3": O.E2M3, "e2m1": O.E2M1}
+
+
+def _golden(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        rows.append((parts[0], parts[1], parts[2]))
+    return rows
+
+
+def all_bf16_values():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    return bits, W.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ---------------------------------------------------------------- codecs
+
+@pytest.mark.parametrize("fmt,value,code", _golden("element_codes.txt"))
+def test_hand_derived_codes(fmt, value, code):
+    assert O.encode(float(value), FMT[fmt]) == int(code, 16)
+
+
+@pytest.mark.parametrize("fmt,amax,byte", _golden("rceil_scales.txt"))
+def test_hand_derived_rceil(fmt, amax, byte):
+    assert O.scale_byte(float(amax), FMT[fmt]) == int(byte)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_every_code_round_trips(fmt):
+    nbits = {O.E4M3: 8, O.E2M3: 6, O.E2M1: 4}[fmt]
+    for c in range(1 << nbits):
+        v = O.decode(c, fmt)
+        if math.isnan(v):
+            assert fmt == O.E4M3 and (c & 0x7F) == 0x7F
+            continue
+        assert O.encode(v, fmt) == c, (fmt, c, v)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_every_midpoint_rounds_to_even_code(fmt):
+    nbits = {O.E4M3: 8, O.E2M3: 6, O.E2M1: 4}[fmt]
+    vals = [O.decode(c, fmt) for c in range(1 << (nbits - 1))]
+    vals = [v for v in vals if not math.isnan(v)]
+    for c in range(len(vals) - 1):
+        mid = 0.5 * (vals[c] + vals[c + 1])
+        want = c if c % 2 == 0 else c + 1
+        assert O.encode(mid, fmt) == want
+        assert O.encode(-mid, fmt) == want | (1 << (nbits - 1))
+
+
+def test_e4m3_matches_torch_cast_on_every_in_range_bf16():
+    """The pages state the f32->E4M3 conversion is byte-identical to torch's
+    cast; torch's cast is round-to-nearest-even and does not saturate, so
+    the comparison covers every finite BF16 value with |v| <= 448."""
+    torch = pytest.importorskip("torch")
+    bits, vals = all_bf16_values()
+    ok = np.isfinite(vals) & (np.abs(vals) <= 448)
+    v = vals[ok]
+    ref = torch.tensor(v, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = np.array([O.encode(x, O.E4M3) for x in v], dtype=np.uint8)
+    assert np.array_equal(mine, ref)
+
+
+@pytest.mark.parametrize("fmt,name", [(O.E2M3, "float6_e2m3fn"), (O.E2M1, "float4_e2m1fn")])
+def test_fp6_fp4_match_ml_dtypes_on_in_range_bf16(fmt, name):
+    ml = pytest.importorskip("ml_dtypes")
+    bits, vals = all_bf16_values()
+    emax = O.fmt_max(fmt)
+    ok = np.isfinite(vals) & (np.abs(vals) <= emax)
+    v = vals[ok]
+    ref = v.astype(getattr(ml, name)).view(np.uint8)
+    mine = np.array([O.encode(x, fmt) for x in v], dtype=np.uint8)
+    assert np.array_equal(mine, ref)
+
+
+# ---------------------------------------------------------------- RCEIL
+
+def _rceil_from_bits(a, fmt):
+    """Closed form on the bit fields: a = 1.m_a * 2^E_a, emax = 1.m_x * 2^E_x
+    gives e = E_a - E_x + (m_a > m_x)."""
+    m_a, e_a = math.frexp(a)          # a = m_a * 2^e_a, m_a in [0.5, 1)
+    m_x, e_x = math.frexp(O.fmt_max(fmt))
+    return (e_a - e_x) + (1 if m_a > m_x else 0)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_rceil_equals_bit_closed_form_on_every_bf16(fmt):
+    _, vals = all_bf16_values()
+    a = np.abs(vals[np.isfinite(vals) & (vals != 0)])
+    a = np.unique(a)
+    for x in a:
+        assert O.scale_exp(x, fmt) == _rceil_from_bits(float(x), fmt)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_scaled_block_never_exceeds_element_max(fmt):
+    """RCEIL is round-up, so |x / 2^e| <= emax for every element of a block."""
+    rng = np.random.default_rng(1)
+    emax = O.fmt_max(fmt)
+    for _ in range(300):
+        x = W.bf16_bits_to_f32(W.to_bf16_bits(
+            (rng.standard_t(3, 32) * 2.0 ** rng.uniform(-60, 60)).astype(np.float32))).astype(np.float64)
+        sb, codes = O.quantize_block(x, fmt)
+        e = sb - 127
+        assert np.all(np.abs(x) * 2.0 ** (-e) <= emax)
+        assert np.max(np.abs(x)) * 2.0 ** (-(e - 1)) > emax or e == -127
+        dec = np.array([O.decode(c, fmt) for c in codes])
+        assert np.all(np.abs(dec) <= emax)
+
+
+def test_specials_policy():
+    z = np.zeros(32)
+    sb, codes = O.quantize_block(z, O.E4M3)
+    assert sb == 0x00 and np.all(codes == 0)
+    nz = -np.zeros(32)
+    sb, codes = O.quantize_block(nz, O.E4M3)
+    assert sb == 0x00 and np.all(codes == 0x80)
+    x = np.ones(32)
+    x[5] = np.nan                       # NaN propagates through the amax
+    sb, codes = O.quantize_block(x, O.E4M3)
+    assert sb == 0xFF and np.all(codes == 0x7F)
+    sb, codes = O.quantize_block(x, O.E2M1)
+    assert sb == 0xFF and np.all(codes == 0)
+    x = np.ones(32)
+    x[3] = np.inf
+    x[4] = -np.inf
+    sb, codes = O.quantize_block(x, O.E4M3)
+    assert sb == 0xFE and codes[3] == 0x7E and codes[4] == 0xFE and codes[0] == 0x00
+
+
+def test_every_bf16_pattern_as_one_element_block():
+    """Each BF16 value as the lone nonzero of a block: the scaled value lies
+    in (emax/2, emax], so the code is in the top binade and decodes back
+    within half an ulp of the format."""
+    bits, vals = all_bf16_values()
+    for fmt in (O.E4M3, O.E2M3, O.E2M1):
+        emax = O.fmt_max(fmt)
+        for v in vals[np.isfinite(vals) & (vals != 0)][::7]:
+            blk = np.zeros(32)
+            blk[0] = v
+            sb, codes = O.quantize_block(blk, fmt)
+            e = sb - 127
+            if e <= -127 or e >= 127:
+                continue
+            s = abs(v) * 2.0 ** -e
+            assert emax / 2 < s <= emax
+            d = abs(O.decode(codes[0], fmt))
+            ulp = {O.E4M3: 2.0 ** (8 - 3), O.E2M3: 2.0 ** (2 - 3), O.E2M1: 2.0 ** (2 - 1)}[fmt]
+            assert abs(d - s) <= ulp / 2
+
+
+# ---------------------------------------------------------------- layout
+
+def test_blocked_layout_is_a_bijection_with_512_byte_k_stride():
+    for rows, sc in [(128, 4), (256, 8), (384, 7), (96, 2), (1000, 13)]:
+        idx = O.blocked_index(rows, sc)
+        total = O.scale_bytes(rows, sc)
+        assert total == ((rows + 127) // 128 * 128) * ((sc + 3) // 4 * 4)
+        assert len(np.unique(idx)) == idx.size and idx.max() < total
+        # same closed form from C and numpy
+        for r in range(0, rows, 37):
+            for c in range(sc):
+                assert O.blocked_offset(r, c, sc) == idx[r, c]
+        # the K stride between consecutive 4-scale groups is 512 bytes in every row block
+        if sc > 4:
+            d = idx[:, 4:] - idx[:, :-4]
+            assert np.all(d == 512)
+
+
+def test_public_scale_factor_tile_example():
+    """The 128x4 scale-factor tile: row r of a 128-row block lives at byte
+    (r%32)*16 + (r//32)*4 + k inside its 512-byte chunk."""
+    assert O.blocked_offset(0, 0, 4) == 0
+    assert O.blocked_offset(1, 0, 4) == 16
+    assert O.blocked_offset(32, 0, 4) == 4
+    assert O.blocked_offset(33, 3, 4) == 16 + 4 + 3
+    assert O.blocked_offset(127, 3, 4) == 31 * 16 + 3 * 4 + 3
+    assert O.blocked_offset(128, 0, 8) == 1024
+    assert O.blocked_offset(0, 4, 8) == 512
+
+
+def _per_group_colwise_offsets(C, offsets):
+    """Per-group ("K-groups") blocking of columnwise scales [C, R/32]: each
+    expert's segment blocked as its own matrix, the matrices concatenated."""
+    R = int(offsets[-1])
+    out = np.zeros((C, R // 32), dtype=np.int64)
+    base = 0
+    for (s, e) in O.segments(offsets):
+        sc = (e - s) // 32
+        if sc:
+            out[:, s // 32:e // 32] = base + O.blocked_index(C, sc)
+            base += O.scale_bytes(C, sc)
+    return out
+
+
+@pytest.mark.parametrize("C", [32, 64, 128, 160, 256, 768])
+def test_colwise_encodings_coincide_iff_n_le_128(C):
+    offsets = np.array([256, 256, 640, 1024])
+    whole = O.blocked_index(C, 1024 // 32)
+    per_group = _per_group_colwise_offsets(C, offsets)
+    assert whole.size == per_group.size
+    if C <= 128:
+        assert np.array_equal(whole, per_group)
+    else:
+        assert not np.array_equal(whole, per_group)
+
+
+@pytest.mark.parametrize("fmt", [O.E2M3, O.E2M1])
+def test_pack_bit_order(fmt):
+    codes = np.arange(64, dtype=np.uint8) & (0x3F if fmt == O.E2M3 else 0xF)
+    x = np.array([O.decode(c, fmt) for c in codes[:32]] * 2, dtype=np.float64).reshape(1, 64)
+    # scale 2^0 needs an element at emax: codes include the max code
+    p, s = O.quantize_rows(x, fmt)
+    if fmt == O.E2M1:
+        assert p[0, 0] == (codes[0] | (codes[1] << 4)) and p.shape == (1, 32)
+    else:
+        b = int(p[0, 0]) | (int(p[0, 1]) << 8) | (int(p[0, 2]) << 16)
+        assert [(b >> (6 * j)) & 0x3F for j in range(4)] == list(codes[:4]) and p.shape == (1, 48)
+
+
+# ---------------------------------------------------------------- Hadamard
+
+def test_hadamard_algebra():
+    H = np.stack([O.hadamard32_f64(np.eye(32)[i]) for i in range(32)]) * math.sqrt(32)
+    assert np.allclose(np.rint(H), H, atol=1e-12)
+    H = np.rint(H)
+    assert np.array_equal(H @ H.T, 32 * np.eye(32))
+    assert np.all(np.abs(H) == 1)
+    # Sylvester order: H[i, j] = (-1)^popcount(i & j)
+    for i in range(32):
+        for j in range(32):
+            assert H[i, j] == (-1) ** bin(i & j).count("1")
+    rng = np.random.default_rng(3)
+    a, b = rng.standard_normal((4, 32)), rng.standard_normal((5, 32))
+    ah = np.stack([O.hadamard32_f64(r) for r in a])
+    bh = np.stack([O.hadamard32_f64(r) for r in b])
+    assert np.allclose(ah @ bh.T, a @ b.T, rtol=1e-12, atol=1e-12)
+    x = rng.standard_normal(32).astype(np.float32)
+    f32 = O.hadamard32_f32(x)
+    assert np.allclose(f32, O.hadamard32_f64(x.astype(np.float64)), rtol=1e-5, atol=1e-6)
+    one_hot = np.zeros(32, dtype=np.float32)
+    one_hot[7] = 1.0
+    assert np.allclose(np.abs(O.hadamard32_f32(one_hot)), 1 / math.sqrt(32), rtol=1e-7)
+
+
+# ---------------------------------------------------------------- BF16
+
+def test_bf16_rounding_matches_torch_on_float32_inputs():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    u = rng.integers(0, 1 << 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    f = u.view(np.float32)
+    f = f[np.isfinite(f)]
+    edge = np.array([0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 3.3895314e38, 3.4e38,
+                     1e-40, -1e-45], dtype=np.float32)
+    f = np.concatenate([f, edge])
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mine = O.f64_to_bf16(f.astype(np.float64))
+    assert np.array_equal(mine, ref)
+
+
+def test_bf16_sgd_step_is_inert_without_fp32_master():
+    """A BF16 weight plus an update ~7e-6 of its size rounds back to itself
+    (BF16 resolves ~8e-3 relative); an FP32 master copy accumulates it
+    (Primus PR #1064, first commit, on test quality)."""
+    rng = np.random.default_rng(7)
+    w = O.bf16_out(rng.standard_normal(4096) * 0.02)
+    upd = 7e-6 * w
+    assert np.array_equal(O.bf16_out(w + upd), w)
+    master = w.astype(np.float32)
+    for _ in range(2000):
+        master = (master + upd.astype(np.float32)).astype(np.float32)
+    assert not np.array_equal(O.bf16_out(master.astype(np.float64)), w)
+
+
+# ---------------------------------------------------------------- GEMMs
+
+def _frac_matmul(a, b):
+    return [[sum((Fraction(a[i][k]) * Fraction(b[j][k]) for k in range(len(a[0]))), Fraction(0))
+             for j in range(len(b))] for i in range(len(a))]
+
+
+def test_grouped_gemm_exact_rational_small():
+    rng = np.random.default_rng(11)
+    x = W.bf16_bits_to_f32(W.normal_bf16(rng, (96, 64))).astype(np.float64)
+    w = W.bf16_bits_to_f32(W.normal_bf16(rng, (3, 8, 64))).astype(np.float64)
+    xp, xs = O.quantize_rows(x, O.E4M3)
+    xd = O.dequantize_rows(xp, xs, 96, 64, O.E4M3)
+    wd = np.stack([O.dequantize_rows(*O.quantize_rows(w[g], O.E4M3), 8, 64, O.E4M3) for g in range(3)])
+    offsets = np.array([32, 32, 64])        # expert 1 empty, rows 64.. inactive
+    out = O.grouped_gemm(xd, wd, offsets)
+    for g, (s, e) in enumerate(O.segments(offsets)):
+        if e > s:
+            exact = _frac_matmul(xd[s:e].tolist(), wd[g].tolist())
+            assert np.array_equal(out[s:e], np.array([[float(v) for v in row] for row in exact]))
+    assert np.all(np.isnan(out[64:]))
+
+
+def test_wgrad_zero_token_expert_and_exact_small():
+    rng = np.random.default_rng(12)
+    a = rng.integers(-3, 4, size=(16, 256)).astype(np.float64)
+    b = rng.integers(-3, 4, size=(8, 256)).astype(np.float64)
+    offsets = np.array([128, 128, 256])
+    dw = O.wgrad(a, b, offsets)
+    assert np.array_equal(dw[1], np.zeros((16, 8)))
+    exact0 = _frac_matmul(a[:, :128].tolist(), b[:, :128].tolist())
+    assert np.array_equal(dw[0], np.array([[float(v) for v in r] for r in exact0]))
+    exact2 = _frac_matmul(a[:, 128:].tolist(), b[:, 128:].tolist())
+    assert np.array_equal(dw[2], np.array([[float(v) for v in r] for r in exact2]))
+
+
+def test_dequantize_error_is_within_half_ulp_of_the_block():
+    rng = np.random.default_rng(13)
+    x = W.bf16_bits_to_f32(W.normal_bf16(rng, (64, 256))).astype(np.float64) * 3.7
+    for fmt, mbits in ((O.E4M3, 3), (O.E2M3, 3), (O.E2M1, 1)):
+        p, s = O.quantize_rows(x, fmt)
+        d = O.dequantize_rows(p, s, 64, 256, fmt)
+        sm = O.scales_to_matrix(s, 64, 8)
+        scale = np.repeat(2.0 ** (sm.astype(np.float64) - 127), 32, axis=1)
+        emax = O.fmt_max(fmt)
+        # top-binade ulp of the format times the block scale bounds the error
+        ulp_top = 2.0 ** (math.floor(math.log2(emax)) - mbits) * scale
+        assert np.all(np.abs(d - x) <= ulp_top / 2 + 1e-300)
+
+
+# ---------------------------------------------------------------- activations
+
+def test_dswiglu_is_the_derivative_of_swiglu():
+    rng = np.random.default_rng(17)
+    g = rng.standard_normal(200) * 3
+    u = rng.standard_normal(200)
+    dh = rng.standard_normal(200)
+    dg, du = O.dswiglu(dh, g, u)
+    eps = 1e-6
+    fd_g = (O.swiglu(g + eps, u) - O.swiglu(g - eps, u)) / (2 * eps)
+    fd_u = (O.swiglu(g, u + eps) - O.swiglu(g, u - eps)) / (2 * eps)
+    assert np.allclose(dg, dh * fd_g, rtol=1e-6, atol=1e-8)
+    assert np.allclose(du, dh * fd_u, rtol=1e-6, atol=1e-8)
+
+
+def test_gelu_tanh_and_its_derivative():
+    x = np.linspace(-8, 8, 2001)
+    erf_gelu = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in x])
+    assert np.max(np.abs(O.gelu_tanh(x) - erf_gelu)) < 1e-3
+    eps = 1e-6
+    fd = (O.gelu_tanh(x + eps) - O.gelu_tanh(x - eps)) / (2 * eps)
+    assert np.allclose(O.dgelu_tanh(x), fd, rtol=1e-6, atol=1e-8)
+    assert O.gelu_tanh(np.array([0.0]))[0] == 0.0
+
+
+def test_saturated_gate_gives_exact_product():
+    """Gate >= 32 makes sigmoid round to 1.0 in fp32, so h = g*u exactly."""
+    g = np.array([32.0, 40.0, 64.0, 100.0])
+    u = np.array([1.5, -2.0, 0.25, 3.0])
+    assert np.array_equal(O.round_f32(O.swiglu(g, u)), g * u)
