@@ -1,0 +1,276 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) OCP-MX training-MLP library.
+ *
+ * The hot path of a microscaling (MX) mixture-of-experts / dense MLP
+ * training step: block-of-32 quantization with E8M0 round-up scales, ragged
+ * grouped block-scaled GEMMs on the 5th-generation tensor core with fused
+ * SwiGLU / dSwiGLU epilogues that requantize from on-chip memory, and the
+ * ragged-K weight-gradient GEMM.
+ *
+ * Sources (web pages, cited by title and passage):
+ *   [MXFP8-PR]  torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP
+ *               fwd/bwd and wgrad group gemm" -- shared-infrastructure commit,
+ *               correctness-first kernels commit, cudnn-fe ops commit,
+ *               validation-memoization commit, hardening commit.
+ *   [MXFP6-PR]  Primus PR #1064 "feat(mxfp6): MXFP6 (E2M3) Flux linears, a
+ *               fused MLP, and the MLPerf recipe" -- first commit, fused-MLP
+ *               commit, bias commits.
+ *   [MXFP4-guide] ROCm Primus guide "MXFP4 training for Flux models",
+ *               Overview.
+ *
+ * Common conventions
+ *   - Every pointer named *_dev or held in an mx_tensor_t is DEVICE memory of
+ *     the current CUDA device; nothing here allocates or frees device memory.
+ *     The caller owns every input, output and workspace buffer.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  No call synchronises the host except
+ *     mx_get_device_status and, when the environment variable
+ *     MX_VALIDATE_OFFSETS=1 is set, the offsets value check ([MXFP8-PR]
+ *     cudnn-fe ops commit: opt-in value checks that need a sync).
+ *   - Errors: arguments are validated on the host before anything is
+ *     launched.  On failure nothing is launched, the call returns a status
+ *     and mx_last_error() returns a message naming the argument (per calling
+ *     thread).  There is no fallback path: an unsupported combination is an
+ *     error, never a slower route.
+ *   - Device: compute capability 10.3 (GB300) only; anything else returns
+ *     MX_ERR_UNSUPPORTED_DEVICE.
+ *   - All device pointers must be 16-byte aligned ([MXFP8-PR] hardening
+ *     commit: 16-byte data_ptr gate).
+ */
+#ifndef MX_H_
+#define MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MX_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+typedef struct CUstream_st *mx_stream_t; /* identical to cudaStream_t */
+
+/* Element formats ([MXFP8-PR]: E4M3; [MXFP6-PR]: E2M3; [MXFP4-guide]: E2M1).
+ * Payload packing: E4M3 one byte per element; E2M3 four elements per three
+ * bytes, element i at bits [6i, 6i+6) of the little-endian 24-bit group;
+ * E2M1 two per byte, even element in the low nibble. */
+typedef enum { MX_E4M3 = 0, MX_E2M3 = 1, MX_E2M1 = 2 } mx_fmt_t;
+
+typedef enum {
+  MX_OK = 0,
+  MX_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, G == 0, ... */
+  MX_ERR_SHAPE = 2,              /* dimension not a required multiple / mismatched */
+  MX_ERR_ALIGNMENT = 3,          /* pointer or leading dimension not 16-byte aligned */
+  MX_ERR_OFFSETS = 4,            /* offsets failed the opt-in value check */
+  MX_ERR_UNSUPPORTED_DEVICE = 5, /* not a compute capability 10.3 device */
+  MX_ERR_CUDA = 6,               /* a CUDA runtime / driver call failed */
+  MX_ERR_DEVICE_TIMEOUT = 7,     /* a bounded on-device wait expired (see mx_get_device_status) */
+  MX_ERR_WORKSPACE = 8,          /* workspace missing or too small */
+  MX_ERR_NOT_SUPPORTED = 9       /* valid request outside what this build implements */
+} mx_status_t;
+
+/* A quantized MX tensor: logical [rows, cols], blocks of 32 run along cols.
+ *   data   packed payload, row-major, mx_payload_bytes(rows, cols, fmt) bytes
+ *   scale  E8M0 block scales (byte b = 2^(b-127), 0xFF = NaN block) in the
+ *          blocked layout: scale (r, c) of the [rows, cols/32] scale matrix
+ *          sits at ((r/128)*ceil(cols/128) + c/4)*512 + (r%32)*16 +
+ *          ((r%128)/32)*4 + c%4, padding bytes zero; mx_scale_bytes() bytes.
+ *          ([MXFP8-PR] shared-infrastructure commit: tcgen05 blocked-scale
+ *          indexing with a constant 512-byte K stride per 128-row block.)
+ *   hadamard  nonzero if each block carries the 32-point rotation.
+ * A "columnwise" (32x1) quantization of a [R, C] tensor is stored as the
+ * rowwise quantization of its transpose: an mx_tensor_t of shape [C, R]
+ * whose scales are blocked over the whole [C, R/32] scale matrix
+ * ([MXFP8-PR] shared-infrastructure commit: whole-matrix columnwise scales). */
+typedef struct {
+  void *data;
+  uint8_t *scale;
+  int64_t rows, cols;
+  int32_t fmt;
+  int32_t hadamard;
+} mx_tensor_t;
+
+/* mx_quantize flags */
+enum { MX_ROWWISE = 1, MX_COLWISE = 2, MX_HADAMARD = 4, MX_COLSUM = 8 };
+
+MX_API int mx_abi_version(void);
+MX_API const char *mx_last_error(void);
+MX_API const char *mx_status_string(mx_status_t status);
+
+/* Sizes (bytes) of the payload and blocked scales of a [rows, cols] tensor. */
+MX_API size_t mx_payload_bytes(int64_t rows, int64_t cols, int32_t fmt);
+MX_API size_t mx_scale_bytes(int64_t rows, int64_t cols);
+/* Workspace mx_quantize needs for `flags` on one [rows, cols] input. */
+MX_API size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, uint32_t flags);
+
+/*
+ * mx_quantize -- BF16 -> MX, rowwise and/or columnwise, in one pass.
+ * [MXFP8-PR] shared-infrastructure commit (RCEIL E8M0, NaN-propagating
+ * amax, rowwise 1x32 / columnwise 32x1); [MXFP6-PR] first and bias commits
+ * (Hadamard folded into the packer; per-column sums for the bias gradient).
+ *
+ *   x_bf16     device BF16 [batch, rows, cols], row stride `ld` elements
+ *              (ld >= cols, ld % 8 == 0); batches contiguous (stride rows*ld)
+ *   fmt        element format
+ *   flags      MX_ROWWISE | MX_COLWISE (at least one), optionally
+ *              MX_HADAMARD (rotate each 32-block before quantizing) and
+ *              MX_COLSUM (fp32 sum over rows of each column, of the
+ *              unrotated input; needs MX_COLWISE and batch == 1)
+ *   out_row    MX_ROWWISE: tensor [batch*rows, cols] of format fmt
+ *   out_col    MX_COLWISE: tensor [batch*cols, rows] (per batch entry the
+ *              transpose's rowwise quantization)
+ *   colsum     MX_COLSUM: device fp32 [cols]
+ *   workspace  MX_COLSUM: >= mx_quantize_workspace_bytes(rows, cols, flags)
+ * Each 32-block's scale is the smallest power of two 2^e with
+ * amax <= emax * 2^e (emax = 448 / 7.5 / 6); elements are x * 2^-e rounded
+ * to nearest-even and saturated; amax == 0 -> 0x00, amax == Inf -> 0xFE,
+ * NaN in the block -> 0xFF with every element code NaN (E4M3 0x7F) or +0.
+ * Shapes: cols % 32 == 0; MX_COLWISE also rows % 32 == 0; batch > 1 needs
+ * rows % 128 == 0 and cols % 128 == 0.  rows == 0: MX_OK, nothing launched.
+ */
+MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                        int32_t fmt, uint32_t flags, const mx_tensor_t *out_row, const mx_tensor_t *out_col,
+                        float *colsum, void *workspace, size_t workspace_bytes, mx_stream_t stream);
+
+/*
+ * Offsets (all grouped calls): device int32 [G], cumulative END offsets of
+ * each expert's row segment, nondecreasing, each a multiple of 128,
+ * offsets[G-1] <= R.  Rows in [offsets[G-1], R) are neither read nor
+ * written (caller-allocated outputs keep their contents there).  An empty
+ * segment is allowed.  ([MXFP8-PR] shared-infrastructure commit: per-expert
+ * row counts are multiples of 128, so no tile straddles an expert and the
+ * expert of a tile follows from its row base; cudnn-fe ops commit: rows past
+ * offsets[-1] are untouched in caller-allocated outputs.)  Values are not
+ * checked on the host unless MX_VALIDATE_OFFSETS=1; the kernels skip a tile
+ * whose segment is malformed and report MX_ERR_OFFSETS through
+ * mx_get_device_status.  G == 0 is MX_ERR_INVALID_ARG.
+ */
+
+/*
+ * mx_grouped_gemm -- out[r, n] = sum_k A[r, k] * B[g(r)][n, k] in fp32,
+ * stored as BF16 (round to nearest even).  The plain grouped GEMM on
+ * prequantized operands (FC2 forward, FC1 dgrad; [MXFP8-PR] cudnn-fe ops
+ * commit, grouped mm with b [G, N, K] blocked along K).
+ *   a         [R, K] rowwise MX (blocks along K)
+ *   b         [G*N, K] rowwise MX; expert g owns rows [g*N, (g+1)*N)
+ *   out_bf16  device BF16 [R, ld_out], ld_out >= N, ld_out % 8 == 0
+ * K % 128 == 0, N % 128 == 0, same format and rotation on both operands.
+ */
+MX_API mx_status_t mx_grouped_gemm(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G, const int32_t *offsets_dev,
+                            void *out_bf16, int64_t ld_out, mx_stream_t stream);
+
+/*
+ * mx_grouped_gemm_swiglu_fwd -- FC1 of the expert MLP with the SwiGLU
+ * epilogue ([MXFP8-PR] correctness-first kernels commit: FC1 ragged grouped
+ * GEMM + SwiGLU + dual 1x32 / 32x1 MXFP8 RCEIL quantization + BF16
+ * pre-activation save, one launch).
+ *   x_row     [R, D] rowwise E4M3
+ *   w1_row    [G*2F, D] rowwise E4M3: expert g's rows [g*2F, g*2F+F) are the
+ *             gate projection, [g*2F+F, (g+1)*2F) the up projection
+ *   z_bf16    out, device BF16 [R, 2F] = [gate | up] pre-activation
+ *   h_row     out, [R, F] rowwise E4M3 of h = gate * sigmoid(gate) * up
+ *   h_col     out, [F, R] columnwise E4M3 of h
+ * D % 128 == 0, F % 128 == 0, R % 128 == 0.  h is computed in fp32 from the
+ * fp32 accumulators; sigmoid(x) = 1 / (1 + exp(-x)).
+ */
+MX_API mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t *x_row, const mx_tensor_t *w1_row, int32_t G,
+                                       const int32_t *offsets_dev, const mx_tensor_t *h_row,
+                                       const mx_tensor_t *h_col, void *z_bf16, mx_stream_t stream);
+
+/*
+ * mx_grouped_gemm_dswiglu_bwd -- FC2 dgrad with the dSwiGLU epilogue
+ * ([MXFP8-PR] correctness-first kernels commit: FC2 dgrad grouped GEMM +
+ * dSwiGLU + dual quantization, one launch).
+ *   dy_row    [R, D] rowwise E4M3 of the output gradient
+ *   w2t_row   [G*F, D] rowwise E4M3 of each expert's W2^T (W2 is [D, F])
+ *   z_bf16    device BF16 [R, 2F], the saved pre-activation
+ *   dz_row    out, [R, 2F] rowwise E4M3 of dz = [dg | du]
+ *   dz_col    out, [2F, R] columnwise E4M3 of dz
+ * with dh = dY W2: dg = dh*u*s*(1 + g*(1-s)), du = dh*g*s, s = sigmoid(g),
+ * g and u read from the BF16 z.  D % 128 == 0, F % 128 == 0, R % 128 == 0.
+ */
+MX_API mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t *dy_row, const mx_tensor_t *w2t_row,
+                                        const void *z_bf16, int32_t G, const int32_t *offsets_dev,
+                                        const mx_tensor_t *dz_row, const mx_tensor_t *dz_col,
+                                        mx_stream_t stream);
+
+/*
+ * mx_grouped_gemm_wgrad -- ragged-K weight gradient, BF16 out ([MXFP8-PR]
+ * correctness-first kernels commit: generic ragged-K grouped wgrad, BF16
+ * out; shared-infrastructure commit: zero-token experts give zeros).
+ *   a_col     [N, R] columnwise operand (e.g. dY: [D, R])
+ *   b_col     [K, R] columnwise operand (e.g. h: [F, R])
+ *   out_bf16  device BF16 [G, N, K]: out[g, n, k] = sum over rows r of
+ *             segment g of a_col[n, r] * b_col[k, r]; an empty segment
+ *             writes exact zeros
+ * N % 128 == 0, K % 128 == 0, R % 128 == 0.
+ */
+MX_API mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
+                                  const int32_t *offsets_dev, void *out_bf16, mx_stream_t stream);
+
+/* Activation of mx_mlp_fwd_bwd. */
+typedef enum { MX_ACT_SWIGLU = 0, MX_ACT_GELU_TANH = 1 } mx_act_t;
+
+/*
+ * Arguments of the whole MLP step.  BF16 inputs / outputs, device memory.
+ *   x   [R, D]        dy  [R, D]       y  out [R, D]     dx out [R, D]
+ *   SwiGLU: w1 [G, 2F, D] (gate rows then up rows per expert), w2 [G, D, F],
+ *           dw1 out [G, 2F, D], dw2 out [G, D, F]; b1, b2, db1, db2 unused.
+ *   workspace  >= mx_mlp_workspace_bytes(args); holds every quantized
+ *              operand and the saved pre-activation between the stages.
+ */
+typedef struct {
+  int32_t act;
+  int32_t fmt;
+  int32_t hadamard;
+  int32_t G;
+  int64_t R, D, F;
+  const int32_t *offsets;
+  const void *x, *w1, *w2, *dy, *b1, *b2;
+  void *y, *dx, *dw1, *dw2;
+  float *db1, *db2;
+  void *workspace;
+  size_t workspace_bytes;
+} mx_mlp_args_t;
+
+MX_API size_t mx_mlp_workspace_bytes(const mx_mlp_args_t *args);
+
+/*
+ * mx_mlp_fwd_bwd -- one training step of the MX MLP on one stream:
+ * quantize X, W1, W2 (rowwise and per-expert columnwise); FC1 + SwiGLU
+ * (mx_grouped_gemm_swiglu_fwd); FC2 (mx_grouped_gemm); quantize dY; FC2
+ * dgrad + dSwiGLU (mx_grouped_gemm_dswiglu_bwd); FC1 dgrad
+ * (mx_grouped_gemm); dW2 and dW1 (mx_grouped_gemm_wgrad).  9 launches.
+ * ([MXFP8-PR] cudnn-fe ops commit: the four ops of the routed-expert MLP;
+ * [MXFP6-PR] fused-MLP commit: owning fc1 -> activation -> fc2 in one unit.)
+ */
+MX_API mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t *args, mx_stream_t stream);
+
+/*
+ * mx_get_device_status -- synchronise `stream`, then report and clear the
+ * device-side status words: MX_ERR_DEVICE_TIMEOUT if a bounded wait inside
+ * a kernel expired (the kernel unwound; its outputs are undefined),
+ * MX_ERR_OFFSETS if a kernel saw a malformed offsets segment, else MX_OK.
+ */
+MX_API mx_status_t mx_get_device_status(mx_stream_t stream);
+
+/*
+ * mx_selftest_bounded_wait -- launch a kernel whose wait nothing completes;
+ * it gives up after `budget_ns` and records the timeout, so the next
+ * mx_get_device_status returns MX_ERR_DEVICE_TIMEOUT.  Exercises the
+ * timeout path without hanging or faulting the device.
+ */
+MX_API mx_status_t mx_selftest_bounded_wait(uint64_t budget_ns, mx_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H_ */

@@ -1,0 +1,259 @@
+"""Thin Python binding of the GB300 MX training-MLP library (``include/mx.h``).
+
+Argument marshalling only: every function here checks nothing the C layer
+does not, computes nothing, and calls exactly one C-ABI entry point of the
+same name (``mx_mlp_fwd_bwd`` launches the whole step).  PyTorch supplies
+device memory (output buffers are ``torch.empty`` allocations when the
+caller passes none) and the current CUDA stream.
+
+There is no fallback: if the shared library is missing or fails to load,
+``load()`` raises and nothing runs.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmxgb300.so")
+
+E4M3, E2M3, E2M1 = 0, 1, 2
+ROWWISE, COLWISE, HADAMARD, COLSUM = 1, 2, 4, 8
+ACT_SWIGLU, ACT_GELU_TANH = 0, 1
+
+STATUS = {
+    0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_SHAPE", 3: "MX_ERR_ALIGNMENT", 4: "MX_ERR_OFFSETS",
+    5: "MX_ERR_UNSUPPORTED_DEVICE", 6: "MX_ERR_CUDA", 7: "MX_ERR_DEVICE_TIMEOUT", 8: "MX_ERR_WORKSPACE",
+    9: "MX_ERR_NOT_SUPPORTED",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+# Every symbol include/mx.h declares.
+ABI_SYMBOLS = (
+    "mx_abi_version", "mx_last_error", "mx_status_string", "mx_payload_bytes", "mx_scale_bytes",
+    "mx_quantize_workspace_bytes", "mx_quantize", "mx_grouped_gemm", "mx_grouped_gemm_swiglu_fwd",
+    "mx_grouped_gemm_dswiglu_bwd", "mx_grouped_gemm_wgrad", "mx_mlp_workspace_bytes", "mx_mlp_fwd_bwd",
+    "mx_get_device_status", "mx_selftest_bounded_wait",
+)
+
+
+class MXError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__("%s: %s" % (self.name, message))
+
+
+class MxTensorStruct(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("fmt", ctypes.c_int32), ("hadamard", ctypes.c_int32)]
+
+
+class MlpArgsStruct(ctypes.Structure):
+    _fields_ = [("act", ctypes.c_int32), ("fmt", ctypes.c_int32), ("hadamard", ctypes.c_int32),
+                ("G", ctypes.c_int32), ("R", ctypes.c_int64), ("D", ctypes.c_int64), ("F", ctypes.c_int64),
+                ("offsets", ctypes.c_void_p), ("x", ctypes.c_void_p), ("w1", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("dy", ctypes.c_void_p), ("b1", ctypes.c_void_p),
+                ("b2", ctypes.c_void_p), ("y", ctypes.c_void_p), ("dx", ctypes.c_void_p),
+                ("dw1", ctypes.c_void_p), ("dw2", ctypes.c_void_p), ("db1", ctypes.c_void_p),
+                ("db2", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def load(path=None):
+    """Load the CUDA library (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("MX CUDA library not built at %s (run __graft_entry__.build())" % path)
+    L = ctypes.CDLL(path)
+    vp, i64, i32, u32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+    tp = ctypes.POINTER(MxTensorStruct)
+    sig = {
+        "mx_abi_version": (ctypes.c_int, []),
+        "mx_last_error": (ctypes.c_char_p, []),
+        "mx_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "mx_payload_bytes": (sz, [i64, i64, i32]),
+        "mx_scale_bytes": (sz, [i64, i64]),
+        "mx_quantize_workspace_bytes": (sz, [i64, i64, u32]),
+        "mx_quantize": (ctypes.c_int, [vp, i64, i64, i64, i64, i32, u32, tp, tp, vp, vp, sz, vp]),
+        "mx_grouped_gemm": (ctypes.c_int, [tp, tp, i32, vp, vp, i64, vp]),
+        "mx_grouped_gemm_swiglu_fwd": (ctypes.c_int, [tp, tp, i32, vp, tp, tp, vp, vp]),
+        "mx_grouped_gemm_dswiglu_bwd": (ctypes.c_int, [tp, tp, vp, i32, vp, tp, tp, vp]),
+        "mx_grouped_gemm_wgrad": (ctypes.c_int, [tp, tp, i32, vp, vp, vp]),
+        "mx_mlp_workspace_bytes": (sz, [ctypes.POINTER(MlpArgsStruct)]),
+        "mx_mlp_fwd_bwd": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp]),
+        "mx_get_device_status": (ctypes.c_int, [vp]),
+        "mx_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status):
+    if status != 0:
+        raise MXError(status, load().mx_last_error().decode())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+# --------------------------------------------------------------------------
+# Quantized tensors
+# --------------------------------------------------------------------------
+
+def payload_bytes(rows, cols, fmt):
+    return int(load().mx_payload_bytes(rows, cols, fmt))
+
+
+def scale_bytes(rows, cols):
+    return int(load().mx_scale_bytes(rows, cols))
+
+
+class MX:
+    """A quantized MX tensor [rows, cols] (blocks along cols) in torch buffers."""
+
+    def __init__(self, rows, cols, fmt=E4M3, hadamard=False, device="cuda", data=None, scale=None):
+        import torch
+        self.rows, self.cols, self.fmt, self.hadamard = int(rows), int(cols), int(fmt), bool(hadamard)
+        rb = payload_bytes(1, cols, fmt)
+        self.data = data if data is not None else torch.empty((rows, rb), dtype=torch.uint8, device=device)
+        self.scale = scale if scale is not None else torch.empty(scale_bytes(rows, cols), dtype=torch.uint8,
+                                                                 device=device)
+
+    def struct(self):
+        return MxTensorStruct(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.cols, self.fmt,
+                              1 if self.hadamard else 0)
+
+
+def _s(m):
+    return None if m is None else ctypes.byref(m.struct())
+
+
+# --------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# --------------------------------------------------------------------------
+
+def mx_quantize(x, fmt=E4M3, rowwise=True, colwise=True, hadamard=False, colsum=False, out_row=None,
+                out_col=None, colsum_out=None, workspace=None, stream=None):
+    """x: BF16 [rows, cols] or [batch, rows, cols] on the GPU.  Returns
+    (out_row [batch*rows, cols], out_col [batch*cols, rows], colsum [cols])."""
+    import torch
+    assert x.dtype == torch.bfloat16
+    batch = x.shape[0] if x.dim() == 3 else 1
+    rows, cols = x.shape[-2], x.shape[-1]
+    ld = x.stride(-2)
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (HADAMARD if hadamard else 0) | \
+            (COLSUM if colsum else 0)
+    if rowwise and out_row is None:
+        out_row = MX(batch * rows, cols, fmt, hadamard, x.device)
+    if colwise and out_col is None:
+        out_col = MX(batch * cols, rows, fmt, hadamard, x.device)
+    ws_bytes = 0
+    if colsum:
+        if colsum_out is None:
+            colsum_out = torch.empty(cols, dtype=torch.float32, device=x.device)
+        ws_bytes = int(load().mx_quantize_workspace_bytes(rows, cols, flags))
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=x.device)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(load().mx_quantize(_ptr(x), batch, rows, cols, ld, fmt, flags, _s(out_row) if rowwise else None,
+                              _s(out_col) if colwise else None, _ptr(colsum_out) if colsum else None,
+                              _ptr(workspace) if colsum else None, ws_bytes, _stream(stream)))
+    return out_row, out_col, colsum_out
+
+
+def mx_grouped_gemm(a, b, G, offsets, out=None, ld_out=None, stream=None):
+    import torch
+    N = b.rows // G if G else 0
+    if out is None:
+        out = torch.empty((a.rows, N), dtype=torch.bfloat16, device=a.data.device)
+    ld = ld_out if ld_out is not None else out.stride(0)
+    _check(load().mx_grouped_gemm(_s(a), _s(b), G, _ptr(offsets), _ptr(out), ld, _stream(stream)))
+    return out
+
+
+def mx_grouped_gemm_swiglu_fwd(x_row, w1_row, G, offsets, h_row=None, h_col=None, z=None, stream=None):
+    import torch
+    R = x_row.rows
+    F = w1_row.rows // (2 * G)
+    dev = x_row.data.device
+    if h_row is None:
+        h_row = MX(R, F, E4M3, False, dev)
+    if h_col is None:
+        h_col = MX(F, R, E4M3, False, dev)
+    if z is None:
+        z = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    _check(load().mx_grouped_gemm_swiglu_fwd(_s(x_row), _s(w1_row), G, _ptr(offsets), _s(h_row), _s(h_col),
+                                             _ptr(z), _stream(stream)))
+    return z, h_row, h_col
+
+
+def mx_grouped_gemm_dswiglu_bwd(dy_row, w2t_row, z, G, offsets, dz_row=None, dz_col=None, stream=None):
+    R = dy_row.rows
+    F = w2t_row.rows // G
+    dev = dy_row.data.device
+    if dz_row is None:
+        dz_row = MX(R, 2 * F, E4M3, False, dev)
+    if dz_col is None:
+        dz_col = MX(2 * F, R, E4M3, False, dev)
+    _check(load().mx_grouped_gemm_dswiglu_bwd(_s(dy_row), _s(w2t_row), _ptr(z), G, _ptr(offsets), _s(dz_row),
+                                              _s(dz_col), _stream(stream)))
+    return dz_row, dz_col
+
+
+def mx_grouped_gemm_wgrad(a_col, b_col, G, offsets, out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((G, a_col.rows, b_col.rows), dtype=torch.bfloat16, device=a_col.data.device)
+    _check(load().mx_grouped_gemm_wgrad(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(out), _stream(stream)))
+    return out
+
+
+def mlp_args(x, w1, w2, dy, offsets, G, F, y, dx, dw1, dw2, workspace=None, act=ACT_SWIGLU, fmt=E4M3,
+             hadamard=False, b1=None, b2=None, db1=None, db2=None):
+    R, D = x.shape
+    a = MlpArgsStruct()
+    a.act, a.fmt, a.hadamard, a.G = act, fmt, 1 if hadamard else 0, G
+    a.R, a.D, a.F = R, D, F
+    for name, t in (("offsets", offsets), ("x", x), ("w1", w1), ("w2", w2), ("dy", dy), ("b1", b1), ("b2", b2),
+                    ("y", y), ("dx", dx), ("dw1", dw1), ("dw2", dw2), ("db1", db1), ("db2", db2)):
+        setattr(a, name, None if t is None else t.data_ptr())
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def mx_mlp_workspace_bytes(args):
+    return int(load().mx_mlp_workspace_bytes(ctypes.byref(args)))
+
+
+def mx_mlp_fwd_bwd(args, stream=None):
+    _check(load().mx_mlp_fwd_bwd(ctypes.byref(args), _stream(stream)))
+
+
+def mx_get_device_status(stream=None):
+    """Synchronise and return the device status name ('MX_OK' or an error)."""
+    return STATUS.get(int(load().mx_get_device_status(_stream(stream))), "unknown")
+
+
+def mx_selftest_bounded_wait(budget_ns, stream=None):
+    _check(load().mx_selftest_bounded_wait(int(budget_ns), _stream(stream)))
+
+
+def mx_last_error():
+    return load().mx_last_error().decode()

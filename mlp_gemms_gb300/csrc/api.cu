@@ -1,0 +1,565 @@
+// C ABI of the MX training-MLP library: host-side validation, TMA tensor
+// maps, launch configuration and the MLP step.  Nothing here allocates
+// device memory; every buffer belongs to the caller.
+//
+// torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP fwd/bwd and wgrad
+// group gemm": cudnn-fe ops commit (two-tier validation: always-on metadata
+// checks plus opt-in value checks of the offsets that need a sync) and the
+// hardening commit (int32 element-index guards, 16-byte pointer gate, G == 0
+// rejected, R == 0 returns early without a launch).
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mx.h"
+#include "mx_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mx_status_t fail(mx_status_t st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+mx_status_t fail(mx_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+mx_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define MX_CHECK(cond, st, ...) \
+  do {                          \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- device properties --------------------------------------------------
+
+struct DevInfo {
+  bool known = false;
+  int major = 0, minor = 0, sms = 0;
+};
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+mx_status_t device_info(DevInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MX_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.known) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    d.known = true;
+  }
+  *out = d;
+  if (d.major != 10 || d.minor != 3)
+    return fail(MX_ERR_UNSUPPORTED_DEVICE, "device %d has compute capability %d.%d; this library runs on 10.3 only",
+                dev, d.major, d.minor);
+  return MX_OK;
+}
+
+// ---- TMA tensor maps ----------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+mx_status_t get_encoder() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  return MX_OK;
+}
+
+// 2-D byte tensor [rows, row_bytes], box 128 bytes x 128 rows, 128-byte swizzle.
+mx_status_t make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MX_OK;
+}
+
+// ---- argument checks ----------------------------------------------------
+
+mx_status_t check_tensor(const mx_tensor_t* t, const char* name, int64_t rows, int64_t cols, int fmt, int had) {
+  MX_CHECK(t != nullptr, MX_ERR_INVALID_ARG, "%s is NULL", name);
+  MX_CHECK(t->rows == rows && t->cols == cols, MX_ERR_SHAPE, "%s is [%lld, %lld], expected [%lld, %lld]", name,
+           (long long)t->rows, (long long)t->cols, (long long)rows, (long long)cols);
+  if (rows == 0 || cols == 0) return MX_OK;  // empty: no storage to check
+  MX_CHECK(t->data != nullptr && t->scale != nullptr, MX_ERR_INVALID_ARG, "%s has a NULL data or scale pointer", name);
+  MX_CHECK(t->fmt == fmt, MX_ERR_INVALID_ARG, "%s has format %d, expected %d", name, t->fmt, fmt);
+  MX_CHECK((t->hadamard != 0) == (had != 0), MX_ERR_INVALID_ARG, "%s rotation flag %d, expected %d", name,
+           t->hadamard, had);
+  MX_CHECK(aligned16(t->data) && aligned16(t->scale), MX_ERR_ALIGNMENT, "%s pointers must be 16-byte aligned", name);
+  return MX_OK;
+}
+
+mx_status_t check_gemm_operand(const mx_tensor_t* t, const char* name) {
+  MX_CHECK(t != nullptr, MX_ERR_INVALID_ARG, "%s is NULL", name);
+  MX_CHECK(t->rows >= 0 && t->cols > 0, MX_ERR_SHAPE, "%s has shape [%lld, %lld]", name, (long long)t->rows,
+           (long long)t->cols);
+  if (t->rows > 0) {
+    MX_CHECK(t->data != nullptr && t->scale != nullptr, MX_ERR_INVALID_ARG, "%s has a NULL data or scale pointer",
+             name);
+    MX_CHECK(aligned16(t->data) && aligned16(t->scale), MX_ERR_ALIGNMENT, "%s pointers must be 16-byte aligned",
+             name);
+  }
+  MX_CHECK(t->fmt == MX_E4M3, MX_ERR_NOT_SUPPORTED, "%s: the grouped GEMMs take E4M3 operands in this build", name);
+  MX_CHECK(t->hadamard == 0, MX_ERR_NOT_SUPPORTED, "%s: rotated operands are not supported by the grouped GEMMs", name);
+  MX_CHECK(t->rows < (1ll << 31) && t->cols < (1ll << 31), MX_ERR_SHAPE, "%s exceeds the int32 coordinate range", name);
+  return MX_OK;
+}
+
+bool env_validate_offsets() {
+  const char* v = getenv("MX_VALIDATE_OFFSETS");
+  return v && v[0] == '1';
+}
+
+// Opt-in value check of the offsets (synchronises the stream).
+mx_status_t validate_offsets_values(const int32_t* offsets_dev, int G, int64_t R, cudaStream_t s) {
+  std::vector<int32_t> h((size_t)G);
+  cudaError_t e = cudaMemcpyAsync(h.data(), offsets_dev, sizeof(int32_t) * (size_t)G, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading offsets");
+  int64_t prev = 0;
+  for (int g = 0; g < G; g++) {
+    MX_CHECK(h[g] % 128 == 0, MX_ERR_OFFSETS, "offsets[%d] = %d is not a multiple of 128", g, h[g]);
+    MX_CHECK(h[g] >= prev, MX_ERR_OFFSETS, "offsets[%d] = %d decreases (previous %lld)", g, h[g], (long long)prev);
+    prev = h[g];
+  }
+  MX_CHECK(prev <= R, MX_ERR_OFFSETS, "offsets[G-1] = %lld exceeds R = %lld", (long long)prev, (long long)R);
+  return MX_OK;
+}
+
+mx_status_t check_offsets(const int32_t* offsets, int32_t G, int64_t R, cudaStream_t s) {
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  MX_CHECK(offsets != nullptr, MX_ERR_INVALID_ARG, "offsets is NULL");
+  MX_CHECK((reinterpret_cast<uintptr_t>(offsets) & 3u) == 0, MX_ERR_ALIGNMENT, "offsets must be 4-byte aligned");
+  if (env_validate_offsets()) return validate_offsets_values(offsets, G, R, s);
+  return MX_OK;
+}
+
+mx_status_t run_gemm(const mx::GemmParams& p, const void* a_data, int64_t a_rows, int64_t a_row_bytes,
+                     const void* b_data, int64_t b_rows, int64_t b_row_bytes, int bn, cudaStream_t s,
+                     const DevInfo& dev) {
+  CUtensorMap ta, tb;
+  mx_status_t st = make_tmap(&ta, a_data, a_rows, a_row_bytes);
+  if (st != MX_OK) return st;
+  if ((st = make_tmap(&tb, b_data, b_rows, b_row_bytes)) != MX_OK) return st;
+  cudaError_t e = mx::launch_gemm(p, ta, tb, bn, s, dev.sms);
+  if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+  return MX_OK;
+}
+
+mx::GemmParams base_params() {
+  mx::GemmParams p;
+  memset(&p, 0, sizeof(p));
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mx_abi_version(void) { return MX_ABI_VERSION; }
+
+const char* mx_last_error(void) { return g_last_error.c_str(); }
+
+const char* mx_status_string(mx_status_t st) {
+  switch (st) {
+    case MX_OK: return "ok";
+    case MX_ERR_INVALID_ARG: return "invalid argument";
+    case MX_ERR_SHAPE: return "bad shape";
+    case MX_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case MX_ERR_OFFSETS: return "malformed offsets";
+    case MX_ERR_UNSUPPORTED_DEVICE: return "unsupported device";
+    case MX_ERR_CUDA: return "CUDA error";
+    case MX_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MX_ERR_WORKSPACE: return "workspace too small";
+    case MX_ERR_NOT_SUPPORTED: return "not supported";
+  }
+  return "unknown status";
+}
+
+size_t mx_payload_bytes(int64_t rows, int64_t cols, int32_t fmt) {
+  if (rows < 0 || cols < 0 || fmt < 0 || fmt > 2) return 0;
+  return (size_t)(rows * mx::payload_row_bytes(cols, fmt));
+}
+
+size_t mx_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return mx::scale_bytes(rows, cols / 32);
+}
+
+size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, uint32_t flags) {
+  if (!(flags & MX_COLSUM) || rows <= 0 || cols <= 0) return 0;
+  return (size_t)((rows + 127) / 128) * (size_t)cols * sizeof(float);
+}
+
+mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                        uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col, float* colsum,
+                        void* workspace, size_t workspace_bytes, mx_stream_t stream) {
+  MX_CHECK(fmt >= MX_E4M3 && fmt <= MX_E2M1, MX_ERR_INVALID_ARG, "fmt = %d is not an MX element format", fmt);
+  MX_CHECK((flags & ~0xFu) == 0, MX_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  MX_CHECK(flags & (MX_ROWWISE | MX_COLWISE), MX_ERR_INVALID_ARG, "neither MX_ROWWISE nor MX_COLWISE requested");
+  MX_CHECK(batch >= 1, MX_ERR_SHAPE, "batch = %lld", (long long)batch);
+  MX_CHECK(rows >= 0 && cols > 0, MX_ERR_SHAPE, "shape [%lld, %lld]", (long long)rows, (long long)cols);
+  MX_CHECK(cols % 32 == 0, MX_ERR_SHAPE, "cols = %lld is not a multiple of 32", (long long)cols);
+  MX_CHECK(!(flags & MX_COLWISE) || rows % 32 == 0, MX_ERR_SHAPE, "columnwise needs rows %% 32 == 0 (rows = %lld)",
+           (long long)rows);
+  MX_CHECK(batch == 1 || (rows % 128 == 0 && cols % 128 == 0), MX_ERR_SHAPE,
+           "batched quantization needs rows and cols multiples of 128");
+  MX_CHECK(ld >= cols && ld % 8 == 0, MX_ERR_ALIGNMENT, "ld = %lld must be >= cols and a multiple of 8",
+           (long long)ld);
+  MX_CHECK(rows == 0 || x_bf16 != nullptr, MX_ERR_INVALID_ARG, "x is NULL");
+  MX_CHECK(aligned16(x_bf16), MX_ERR_ALIGNMENT, "x must be 16-byte aligned");
+  MX_CHECK(rows * ld * batch < (1ll << 40), MX_ERR_SHAPE, "input too large");
+  const int had = (flags & MX_HADAMARD) ? 1 : 0;
+  mx_status_t st;
+  if (flags & MX_ROWWISE) {
+    if ((st = check_tensor(out_row, "out_row", batch * rows, cols, fmt, had)) != MX_OK) return st;
+  }
+  if (flags & MX_COLWISE) {
+    if ((st = check_tensor(out_col, "out_col", batch * cols, rows, fmt, had)) != MX_OK) return st;
+  }
+  if (flags & MX_COLSUM) {
+    MX_CHECK(flags & MX_COLWISE, MX_ERR_INVALID_ARG, "MX_COLSUM needs MX_COLWISE");
+    MX_CHECK(batch == 1, MX_ERR_INVALID_ARG, "MX_COLSUM needs batch == 1");
+    MX_CHECK(colsum != nullptr && aligned16(colsum), MX_ERR_INVALID_ARG, "colsum must be a 16-byte aligned pointer");
+    MX_CHECK(workspace != nullptr && aligned16(workspace) &&
+                 workspace_bytes >= mx_quantize_workspace_bytes(rows, cols, flags),
+             MX_ERR_WORKSPACE, "MX_COLSUM needs %zu bytes of 16-byte aligned workspace",
+             mx_quantize_workspace_bytes(rows, cols, flags));
+  }
+  if (rows == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::QuantLaunch q;
+  q.x = x_bf16;
+  q.batch = batch; q.rows = rows; q.cols = cols; q.ld = ld;
+  q.fmt = fmt; q.hadamard = had;
+  q.row_data = (flags & MX_ROWWISE) ? static_cast<uint8_t*>(out_row->data) : nullptr;
+  q.row_scale = (flags & MX_ROWWISE) ? out_row->scale : nullptr;
+  q.col_data = (flags & MX_COLWISE) ? static_cast<uint8_t*>(out_col->data) : nullptr;
+  q.col_scale = (flags & MX_COLWISE) ? out_col->scale : nullptr;
+  q.colsum_partials = (flags & MX_COLSUM) ? static_cast<float*>(workspace) : nullptr;
+  q.colsum = colsum;
+  cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return MX_OK;
+}
+
+mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                            void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
+  if ((st = check_gemm_operand(b, "b")) != MX_OK) return st;
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  MX_CHECK(a->cols == b->cols, MX_ERR_SHAPE, "a has K = %lld, b has K = %lld", (long long)a->cols, (long long)b->cols);
+  const int64_t K = a->cols, R = a->rows;
+  MX_CHECK(K % 128 == 0, MX_ERR_SHAPE, "K = %lld is not a multiple of 128", (long long)K);
+  MX_CHECK(b->rows % G == 0, MX_ERR_SHAPE, "b has %lld rows, not a multiple of G = %d", (long long)b->rows, G);
+  const int64_t N = b->rows / G;
+  MX_CHECK(N > 0 && N % 128 == 0, MX_ERR_SHAPE, "N = %lld per expert is not a positive multiple of 128", (long long)N);
+  MX_CHECK(out_bf16 != nullptr && aligned16(out_bf16), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
+  MX_CHECK(ld_out >= N && ld_out % 8 == 0, MX_ERR_ALIGNMENT, "ld_out = %lld must be >= N and a multiple of 8",
+           (long long)ld_out);
+  MX_CHECK(R * ld_out < (1ll << 40), MX_ERR_SHAPE, "output too large");
+  if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
+  if (R == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  const int bn = (N % 256 == 0) ? 256 : 128;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_GROUPED;
+  p.epi = mx::EPI_BF16;
+  p.G = G;
+  p.offsets = offsets_dev;
+  p.R = R; p.K = K; p.Nb = N;
+  p.a_type = 0; p.b_type = 0;
+  p.sfa = a->scale; p.sfb = b->scale;
+  p.sfa_kchunks = (K / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)((R + 127) / 128);
+  p.n_tiles = (int)(N / bn);
+  p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+  p.out = static_cast<uint16_t*>(out_bf16);
+  p.out_ld = ld_out;
+  return run_gemm(p, a->data, R, K, b->data, b->rows, K, bn, s, dev);
+}
+
+mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
+                                       const int32_t* offsets_dev, const mx_tensor_t* h_row,
+                                       const mx_tensor_t* h_col, void* z_bf16, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(x_row, "x_row")) != MX_OK) return st;
+  if ((st = check_gemm_operand(w1_row, "w1_row")) != MX_OK) return st;
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  const int64_t R = x_row->rows, D = x_row->cols;
+  MX_CHECK(w1_row->cols == D, MX_ERR_SHAPE, "w1_row has K = %lld, x_row has %lld", (long long)w1_row->cols,
+           (long long)D);
+  MX_CHECK(D % 128 == 0, MX_ERR_SHAPE, "D = %lld is not a multiple of 128", (long long)D);
+  MX_CHECK(R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)R);
+  MX_CHECK(w1_row->rows % (2ll * G) == 0, MX_ERR_SHAPE, "w1_row rows %lld is not 2F*G", (long long)w1_row->rows);
+  const int64_t F = w1_row->rows / (2ll * G);
+  MX_CHECK(F > 0 && F % 128 == 0, MX_ERR_SHAPE, "F = %lld is not a positive multiple of 128", (long long)F);
+  if ((st = check_tensor(h_row, "h_row", R, F, MX_E4M3, 0)) != MX_OK) return st;
+  if ((st = check_tensor(h_col, "h_col", F, R, MX_E4M3, 0)) != MX_OK) return st;
+  MX_CHECK(z_bf16 != nullptr && aligned16(z_bf16), MX_ERR_ALIGNMENT, "z must be a 16-byte aligned pointer");
+  MX_CHECK(R * 2 * F < (1ll << 40), MX_ERR_SHAPE, "output too large");
+  if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
+  if (R == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_GROUPED;
+  p.epi = mx::EPI_SWIGLU;
+  p.G = G; p.offsets = offsets_dev;
+  p.R = R; p.K = D; p.Nb = 2 * F; p.F = F;
+  p.sfa = x_row->scale; p.sfb = w1_row->scale;
+  p.sfa_kchunks = (D / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)(R / 128);
+  p.n_tiles = (int)(F / 128);
+  p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+  p.z = static_cast<uint16_t*>(z_bf16);
+  p.q_row = static_cast<uint8_t*>(h_row->data); p.q_row_scale = h_row->scale;
+  p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
+  p.q_cols = F;
+  return run_gemm(p, x_row->data, R, D, w1_row->data, w1_row->rows, D, 256, s, dev);
+}
+
+mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
+                                        int32_t G, const int32_t* offsets_dev, const mx_tensor_t* dz_row,
+                                        const mx_tensor_t* dz_col, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(dy_row, "dy_row")) != MX_OK) return st;
+  if ((st = check_gemm_operand(w2t_row, "w2t_row")) != MX_OK) return st;
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  const int64_t R = dy_row->rows, D = dy_row->cols;
+  MX_CHECK(w2t_row->cols == D, MX_ERR_SHAPE, "w2t_row has K = %lld, dy_row has %lld", (long long)w2t_row->cols,
+           (long long)D);
+  MX_CHECK(D % 128 == 0, MX_ERR_SHAPE, "D = %lld is not a multiple of 128", (long long)D);
+  MX_CHECK(R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)R);
+  MX_CHECK(w2t_row->rows % G == 0, MX_ERR_SHAPE, "w2t_row rows %lld is not F*G", (long long)w2t_row->rows);
+  const int64_t F = w2t_row->rows / G;
+  MX_CHECK(F > 0 && F % 128 == 0, MX_ERR_SHAPE, "F = %lld is not a positive multiple of 128", (long long)F);
+  if ((st = check_tensor(dz_row, "dz_row", R, 2 * F, MX_E4M3, 0)) != MX_OK) return st;
+  if ((st = check_tensor(dz_col, "dz_col", 2 * F, R, MX_E4M3, 0)) != MX_OK) return st;
+  MX_CHECK(z_bf16 != nullptr && aligned16(z_bf16), MX_ERR_ALIGNMENT, "z must be a 16-byte aligned pointer");
+  MX_CHECK(R * 2 * F < (1ll << 40), MX_ERR_SHAPE, "output too large");
+  if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
+  if (R == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_GROUPED;
+  p.epi = mx::EPI_DSWIGLU;
+  p.G = G; p.offsets = offsets_dev;
+  p.R = R; p.K = D; p.Nb = F; p.F = F;
+  p.sfa = dy_row->scale; p.sfb = w2t_row->scale;
+  p.sfa_kchunks = (D / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)(R / 128);
+  p.n_tiles = (int)(F / 128);
+  p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+  p.z = static_cast<uint16_t*>(const_cast<void*>(z_bf16));
+  p.q_row = static_cast<uint8_t*>(dz_row->data); p.q_row_scale = dz_row->scale;
+  p.q_col = static_cast<uint8_t*>(dz_col->data); p.q_col_scale = dz_col->scale;
+  p.q_cols = 2 * F;
+  return run_gemm(p, dy_row->data, R, D, w2t_row->data, w2t_row->rows, D, 128, s, dev);
+}
+
+mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
+                                  const int32_t* offsets_dev, void* out_bf16, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(a_col, "a_col")) != MX_OK) return st;
+  if ((st = check_gemm_operand(b_col, "b_col")) != MX_OK) return st;
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  const int64_t N = a_col->rows, K = b_col->rows, R = a_col->cols;
+  MX_CHECK(b_col->cols == R, MX_ERR_SHAPE, "a_col has R = %lld, b_col has %lld", (long long)R,
+           (long long)b_col->cols);
+  MX_CHECK(R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)R);
+  MX_CHECK(N > 0 && N % 128 == 0, MX_ERR_SHAPE, "N = %lld is not a positive multiple of 128", (long long)N);
+  MX_CHECK(K > 0 && K % 128 == 0, MX_ERR_SHAPE, "K = %lld is not a positive multiple of 128", (long long)K);
+  MX_CHECK(out_bf16 != nullptr && aligned16(out_bf16), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
+  MX_CHECK((int64_t)G * N * K < (1ll << 40), MX_ERR_SHAPE, "output too large");
+  if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  const int bn = (K % 256 == 0) ? 256 : 128;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_WGRAD;
+  p.epi = mx::EPI_BF16;
+  p.G = G; p.offsets = offsets_dev;
+  p.R = R; p.K = R; p.Nb = K; p.Mw = N;
+  p.sfa = a_col->scale; p.sfb = b_col->scale;
+  p.sfa_kchunks = (R / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)(N / 128);
+  p.n_tiles = (int)(K / bn);
+  p.num_tiles = (int64_t)G * p.m_tiles * p.n_tiles;
+  p.out = static_cast<uint16_t*>(out_bf16);
+  p.out_ld = K;
+  return run_gemm(p, a_col->data, N, R, b_col->data, K, R, bn, s, dev);
+}
+
+// ---- the MLP step -------------------------------------------------------
+
+namespace {
+
+struct MlpLayout {
+  size_t total = 0;
+  struct Slot { size_t data, scale; int64_t rows, cols; };
+  Slot x_row, x_col, w1_row, w1t_row, w2_row, w2t_row, h_row, h_col, dy_row, dy_col, dz_row, dz_col;
+  size_t z;
+};
+
+size_t align_up(size_t x) { return (x + 255) / 256 * 256; }
+
+MlpLayout mlp_layout(const mx_mlp_args_t* a) {
+  MlpLayout L;
+  size_t off = 0;
+  auto slot = [&](int64_t rows, int64_t cols) {
+    MlpLayout::Slot s;
+    s.rows = rows; s.cols = cols;
+    s.data = off; off = align_up(off + (size_t)rows * (size_t)cols);
+    s.scale = off; off = align_up(off + mx::scale_bytes(rows, cols / 32));
+    return s;
+  };
+  const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
+  L.x_row = slot(R, D);
+  L.x_col = slot(D, R);
+  L.w1_row = slot(G * 2 * F, D);
+  L.w1t_row = slot(G * D, 2 * F);
+  L.w2_row = slot(G * D, F);
+  L.w2t_row = slot(G * F, D);
+  L.h_row = slot(R, F);
+  L.h_col = slot(F, R);
+  L.dy_row = slot(R, D);
+  L.dy_col = slot(D, R);
+  L.dz_row = slot(R, 2 * F);
+  L.dz_col = slot(2 * F, R);
+  L.z = off; off = align_up(off + (size_t)R * 2 * (size_t)F * 2);
+  L.total = off;
+  return L;
+}
+
+mx_tensor_t view(const mx_mlp_args_t* a, const MlpLayout::Slot& s) {
+  mx_tensor_t t;
+  uint8_t* base = static_cast<uint8_t*>(a->workspace);
+  t.data = base + s.data;
+  t.scale = base + s.scale;
+  t.rows = s.rows; t.cols = s.cols;
+  t.fmt = MX_E4M3; t.hadamard = 0;
+  return t;
+}
+
+}  // namespace
+
+size_t mx_mlp_workspace_bytes(const mx_mlp_args_t* args) {
+  if (!args || args->R < 0 || args->D <= 0 || args->F <= 0 || args->G <= 0) return 0;
+  return mlp_layout(args).total;
+}
+
+mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
+  MX_CHECK(a != nullptr, MX_ERR_INVALID_ARG, "args is NULL");
+  MX_CHECK(a->act == MX_ACT_SWIGLU, MX_ERR_NOT_SUPPORTED, "activation %d is not supported by this build", a->act);
+  MX_CHECK(a->fmt == MX_E4M3 && a->hadamard == 0, MX_ERR_NOT_SUPPORTED,
+           "the SwiGLU step runs on unrotated E4M3 operands");
+  MX_CHECK(a->G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", a->G);
+  MX_CHECK(a->R >= 0 && a->R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)a->R);
+  MX_CHECK(a->D > 0 && a->D % 128 == 0, MX_ERR_SHAPE, "D = %lld is not a positive multiple of 128", (long long)a->D);
+  MX_CHECK(a->F > 0 && a->F % 128 == 0, MX_ERR_SHAPE, "F = %lld is not a positive multiple of 128", (long long)a->F);
+  const void* ptrs[] = {a->x, a->w1, a->w2, a->dy, a->y, a->dx, a->dw1, a->dw2, a->workspace};
+  const char* names[] = {"x", "w1", "w2", "dy", "y", "dx", "dw1", "dw2", "workspace"};
+  for (int i = 0; i < 9; i++) {
+    MX_CHECK(ptrs[i] != nullptr, MX_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    MX_CHECK(aligned16(ptrs[i]), MX_ERR_ALIGNMENT, "%s must be 16-byte aligned", names[i]);
+  }
+  const MlpLayout L = mlp_layout(a);
+  MX_CHECK(a->workspace_bytes >= L.total, MX_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
+           a->workspace_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_offsets(a->offsets, a->G, a->R, s)) != MX_OK) return st;
+  if (a->R == 0) return MX_OK;
+  const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
+  mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
+  mx_tensor_t w1_row = view(a, L.w1_row), w1t_row = view(a, L.w1t_row);
+  mx_tensor_t w2_row = view(a, L.w2_row), w2t_row = view(a, L.w2t_row);
+  mx_tensor_t h_row = view(a, L.h_row), h_col = view(a, L.h_col);
+  mx_tensor_t dy_row = view(a, L.dy_row), dy_col = view(a, L.dy_col);
+  mx_tensor_t dz_row = view(a, L.dz_row), dz_col = view(a, L.dz_col);
+  void* z = static_cast<uint8_t*>(a->workspace) + L.z;
+  const uint32_t both = MX_ROWWISE | MX_COLWISE;
+  if ((st = mx_quantize(a->x, 1, R, D, D, MX_E4M3, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w1, G, 2 * F, D, D, MX_E4M3, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w2, G, D, F, F, MX_E4M3, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_swiglu_fwd(&x_row, &w1_row, a->G, a->offsets, &h_row, &h_col, z, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->dy, 1, R, D, D, MX_E4M3, both, &dy_row, &dy_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_dswiglu_bwd(&dy_row, &w2t_row, z, a->G, a->offsets, &dz_row, &dz_col, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_wgrad(&dy_col, &h_col, a->G, a->offsets, a->dw2, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_wgrad(&dz_col, &x_col, a->G, a->offsets, a->dw1, stream)) != MX_OK) return st;
+  return MX_OK;
+}
+
+mx_status_t mx_get_device_status(mx_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned word = 0;
+  if ((e = mx::read_gemm_status(&word)) != cudaSuccess) return cuda_fail(e, "reading device status");
+  if ((e = mx::reset_gemm_status()) != cudaSuccess) return cuda_fail(e, "clearing device status");
+  if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
+  if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
+  return MX_OK;
+}
+
+mx_status_t mx_selftest_bounded_wait(uint64_t budget_ns, mx_stream_t stream) {
+  DevInfo dev;
+  mx_status_t st = device_info(&dev);
+  if (st != MX_OK) return st;
+  MX_CHECK(budget_ns > 0 && budget_ns <= 2000000000ull, MX_ERR_INVALID_ARG, "budget must be in (0, 2 s]");
+  cudaError_t e = mx::launch_wait_selftest(budget_ns, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return MX_OK;
+}
+
+}  // extern "C"

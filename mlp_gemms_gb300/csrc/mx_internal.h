@@ -1,0 +1,67 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+inline int64_t round_up_i64(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline size_t scale_bytes(int64_t rows, int64_t scale_cols) {
+  return (size_t)(round_up_i64(rows, 128) * round_up_i64(scale_cols, 4));
+}
+inline int64_t payload_row_bytes(int64_t cols, int fmt) {
+  return fmt == 0 ? cols : (fmt == 1 ? cols / 4 * 3 : cols / 2);
+}
+
+struct QuantLaunch {
+  const void* x;
+  int64_t batch, rows, cols, ld;
+  int fmt, hadamard;
+  uint8_t* row_data;   // null: no rowwise output
+  uint8_t* row_scale;
+  uint8_t* col_data;   // null: no columnwise output
+  uint8_t* col_scale;
+  float* colsum_partials;  // null: no column sums
+  float* colsum;
+};
+cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
+
+enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };
+enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+
+// Everything a grouped-GEMM launch needs besides the two tensor maps.
+struct GemmParams {
+  int mode, epi;
+  int G;
+  const int32_t* offsets;   // device [G], cumulative segment ends
+  int64_t R;                // rows of A (grouped) / reduction extent (wgrad)
+  int64_t K;                // reduction length (grouped; multiple of 128)
+  int64_t Nb;               // B rows per expert (grouped) / B rows total (wgrad)
+  int64_t Mw;               // rows of A (wgrad)
+  int64_t F;                // SwiGLU FFN width (FC1 out = 2F)
+  int a_type, b_type;       // MMA element types (E4M3 = 0, E2M3 = 3, E2M1 = 5)
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int64_t sfa_kchunks, sfb_kchunks;  // 512-byte chunks per 128-row block
+  int m_tiles, n_tiles;
+  int64_t num_tiles;
+  // epilogue outputs
+  uint16_t* out;            // BF16 [rows, out_ld]
+  int64_t out_ld;
+  uint16_t* z;              // SwiGLU: BF16 pre-activation save [R, 2F]; dSwiGLU: its input
+  uint8_t* q_row;           // requantized rowwise payload [R, C] (E4M3)
+  uint8_t* q_row_scale;
+  uint8_t* q_col;           // requantized columnwise payload [C, R] (E4M3)
+  uint8_t* q_col_scale;
+  int64_t q_cols;           // C: F (SwiGLU) or 2F (dSwiGLU)
+};
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, int bn,
+                        cudaStream_t s, int num_sms);
+cudaError_t read_gemm_status(unsigned* out);
+cudaError_t reset_gemm_status();
+cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t s);
+
+}  // namespace mx

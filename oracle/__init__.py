@@ -372,3 +372,111 @@ def dswiglu_bwd(dy_deq, w2t_deq, z_bf16, offsets, fmt=E4M3):
 def bf16_out(x):
     """float64 -> BF16 bits -> float64 (the value a BF16 output holds)."""
     return bf16_to_f64(f64_to_bf16(x))
+
+
+def quantize_experts_cols(w_bits, fmt=E4M3):
+    """Per-expert columnwise quantization of BF16 weights [G, N, K]: each
+    expert's transpose [K, N] rowwise; returns (payload [G*K, N'], scales of
+    the stacked [G*K, N/32] matrix, blocked per expert)."""
+    w_bits = np.asarray(w_bits, dtype=np.uint16)
+    ps, ss = [], []
+    for g in range(w_bits.shape[0]):
+        p, s = quantize_cols(bf16_to_f64(w_bits[g]), fmt)
+        ps.append(p)
+        ss.append(s)
+    return np.concatenate(ps), np.concatenate(ss)
+
+
+def quantize_experts_rows(w_bits, fmt=E4M3):
+    w_bits = np.asarray(w_bits, dtype=np.uint16)
+    G, N, K = w_bits.shape
+    return quantize_rows(bf16_to_f64(w_bits.reshape(G * N, K)), fmt)
+
+
+def mlp_fwd_bwd_swiglu(x_bits, w1_bits, w2_bits, dy_bits, offsets, fmt=E4M3):
+    """The whole MX SwiGLU expert-MLP step, stage by stage, each stage on the
+    oracle's own quantization of its inputs.
+
+    x [R, D], w1 [G, 2F, D], w2 [G, D, F], dy [R, D] as BF16 bits.  Returns a
+    dict with every intermediate and the BF16-rounded outputs y, dx [R, D],
+    dw1 [G, 2F, D], dw2 [G, D, F] (float64 values of the BF16 results)."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    G, F2, D = np.asarray(w1_bits).shape
+    F = F2 // 2
+    R = x_bits.shape[0]
+    A = _active_rows(offsets)
+    x = bf16_to_f64(x_bits)
+    dy = bf16_to_f64(dy_bits)
+    x_row = quantize_rows(x, fmt)
+    x_col = quantize_cols(x[:A], fmt)
+    w1_row = quantize_experts_rows(w1_bits, fmt)
+    w1t_row = quantize_experts_cols(w1_bits, fmt)
+    w2_row = quantize_experts_rows(w2_bits, fmt)
+    w2t_row = quantize_experts_cols(w2_bits, fmt)
+    dq = lambda t, rows, cols: dequantize_rows(t[0], t[1], rows, cols, fmt)
+    xq = dq(x_row, R, D)
+    w1q = dq(w1_row, G * 2 * F, D).reshape(G, 2 * F, D)
+    w1tq = dq(w1t_row, G * D, 2 * F).reshape(G, D, 2 * F)
+    w2q = dq(w2_row, G * D, F).reshape(G, D, F)
+    w2tq = dq(w2t_row, G * F, D).reshape(G, F, D)
+    fwd = swiglu_fwd(xq, w1q, offsets, fmt)
+    hq = dq(fwd["h_row"], A, F)
+    y = grouped_gemm(np.concatenate([hq, np.zeros((R - A, F))]), w2q, offsets)
+    dy_row = quantize_rows(dy, fmt)
+    dy_col = quantize_cols(dy[:A], fmt)
+    dyq = dq(dy_row, R, D)
+    bwd = dswiglu_bwd(dyq, w2tq, fwd["z_bf16"], offsets, fmt)
+    dzq = dq(bwd["dz_row"], A, 2 * F)
+    dx = grouped_gemm(np.concatenate([dzq, np.zeros((R - A, 2 * F))]), w1tq, offsets)
+    dyc = dq(dy_col, D, A)
+    hc = dq(fwd["h_col"], F, A)
+    dzc = dq(bwd["dz_col"], 2 * F, A)
+    xc = dq(x_col, D, A)
+    dw2 = wgrad(dyc, hc, offsets)
+    dw1 = wgrad(dzc, xc, offsets)
+    return {
+        "x_row": x_row, "x_col": x_col, "w1_row": w1_row, "w1t_row": w1t_row, "w2_row": w2_row,
+        "w2t_row": w2t_row, "dy_row": dy_row, "dy_col": dy_col, "fwd": fwd, "bwd": bwd,
+        "y": bf16_out(y[:A]), "dx": bf16_out(dx[:A]), "dw1": bf16_out(dw1), "dw2": bf16_out(dw2),
+        "y_f64": y[:A], "dx_f64": dx[:A], "dw1_f64": dw1, "dw2_f64": dw2,
+    }
+
+
+def mlp_fwd_bwd_swiglu_unquantized(x_bits, w1_bits, w2_bits, dy_bits, offsets):
+    """The same step in float64 with no quantization at all (the reference
+    the quantized chain's SQNR is measured against)."""
+    x = bf16_to_f64(x_bits)
+    dy = bf16_to_f64(dy_bits)
+    w1 = bf16_to_f64(w1_bits)
+    w2 = bf16_to_f64(w2_bits)
+    A = _active_rows(offsets)
+    F = w1.shape[1] // 2
+    z = grouped_gemm(x, w1, offsets)[:A]
+    g, u = z[:, :F], z[:, F:]
+    h = swiglu(g, u)
+    R = x.shape[0]
+    hp = np.concatenate([h, np.zeros((R - A, F))])
+    y = grouped_gemm(hp, w2, offsets)[:A]
+    dh = grouped_gemm(dy, np.transpose(w2, (0, 2, 1)), offsets)[:A]
+    dg, du = dswiglu(dh, g, u)
+    dz = np.concatenate([dg, du], axis=1)
+    dzp = np.concatenate([dz, np.zeros((R - A, 2 * F))])
+    dx = grouped_gemm(dzp, np.transpose(w1, (0, 2, 1)), offsets)[:A]
+    dw2 = wgrad(dy[:A].T, h.T, offsets)
+    dw1 = wgrad(dz.T, x[:A].T, offsets)
+    return {"z": z, "h": h, "y": y, "dx": dx, "dw1": dw1, "dw2": dw2}
+
+
+def sqnr_db(ref, test):
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.asarray(test, dtype=np.float64) - ref
+    return 10.0 * np.log10(np.sum(ref * ref) / max(np.sum(err * err), 1e-300))
+
+
+def within_tolerance(test, ref):
+    """|test - ref| <= 2^-8 |ref| + 2^-14 rms(row of ref), elementwise."""
+    ref = np.asarray(ref, dtype=np.float64)
+    test = np.asarray(test, dtype=np.float64)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * rms
+    return np.abs(test - ref) <= bound

@@ -1,0 +1,258 @@
+"""Grouped-GEMM parity: the CUDA GEMMs and fused epilogues against the
+oracle, stage by stage, on operands quantized identically on both sides
+(the quantizer's bit-exactness is asserted first)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from helpers import assert_quant_equal, bf16_cpu, mx_bytes, requant_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant_both(mx, bits, row=True, col=False):
+    """GPU and oracle rowwise (and columnwise) quantization; asserts equality."""
+    x = to_dev(bits)
+    r, c, _ = mx.mx_quantize(x, O.E4M3, row, col)
+    ref = O.quantize_bf16(bits, O.E4M3, row, col)
+    rows, cols = bits.shape[-2], bits.shape[-1]
+    batch = bits.shape[0] if bits.ndim == 3 else 1
+    if row:
+        assert_quant_equal(r, (ref["row_payload"].reshape(-1, ref["row_payload"].shape[-1]),
+                               ref["row_scales"].reshape(-1)), batch * rows, cols // 32, "row")
+    if col:
+        assert_quant_equal(c, (ref["col_payload"].reshape(-1, ref["col_payload"].shape[-1]),
+                               ref["col_scales"].reshape(-1)), batch * cols, rows // 32, "col")
+    return r, c, ref
+
+
+def _deq(ref_key_payload, ref_key_scales, rows, cols):
+    return O.dequantize_rows(ref_key_payload.reshape(rows, -1), ref_key_scales.reshape(-1), rows, cols, O.E4M3)
+
+
+def _offsets(counts):
+    return W.offsets_from_counts(counts)
+
+
+def test_pr_ref_single_gemm(cuda_lib):
+    """Single expert, X, W [256, 256] ~ N(0, 1): Y = X W^T in BF16."""
+    import torch
+    xb, wb = W.pr_ref(256)
+    xr, _, xref = _quant_both(cuda_lib, xb)
+    wr, _, wref = _quant_both(cuda_lib, wb)
+    offs = torch.tensor([256], dtype=torch.int32, device="cuda")
+    y = cuda_lib.mx_grouped_gemm(xr, wr, 1, offs)
+    ref = _deq(xref["row_payload"], xref["row_scales"], 256, 256) @ \
+        _deq(wref["row_payload"], wref["row_scales"], 256, 256).T
+    got = bf16_cpu(y)
+    assert O.within_tolerance(got, ref).all()
+    # exact: BF16 of the exact product is what a correct fp32 accumulation rounds to, almost everywhere
+    assert np.mean(got == O.bf16_out(ref)) > 0.99
+
+
+@pytest.mark.parametrize("N", [512, 384])
+def test_grouped_gemm_ragged(cuda_lib, N):
+    """4 experts (one empty), K = 1024 (pipeline wraps), ragged inactive tail
+    rows poisoned with NaN must stay untouched."""
+    import torch
+    G, K, R = 4, 1024, 1152
+    counts = [384, 0, 256, 384]          # 1024 active rows, 128-row tail
+    offsets = _offsets(counts)
+    rng = np.random.default_rng(21)
+    ab = W.normal_bf16(rng, (R, K))
+    bb = W.normal_bf16(rng, (G, N, K), std=0.02)
+    ar, _, aref = _quant_both(cuda_lib, ab)
+    br, _, bref = _quant_both(cuda_lib, bb)
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm(ar, br, G, torch.from_numpy(offsets).cuda(), out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    a = _deq(aref["row_payload"], aref["row_scales"], R, K)
+    b = _deq(bref["row_payload"], bref["row_scales"], G * N, K).reshape(G, N, K)
+    ref = O.grouped_gemm(a, b, offsets)
+    got = bf16_cpu(out)
+    A = int(offsets[-1])
+    assert O.within_tolerance(got[:A], ref[:A]).all()
+    assert np.all(np.isnan(got[A:])), "inactive tail rows were written"
+
+
+def test_wgrad_ragged_with_zero_token_expert(cuda_lib):
+    import torch
+    G, N, K, R = 4, 256, 384, 1152
+    counts = [256, 0, 512, 256]
+    offsets = _offsets(counts)
+    A = int(offsets[-1])
+    rng = np.random.default_rng(22)
+    a_bits = W.normal_bf16(rng, (R, N), std=1e-3)   # e.g. dY [R, D]
+    b_bits = W.normal_bf16(rng, (R, K))             # e.g. h  [R, F]
+    _, ac, aref = _quant_both(cuda_lib, a_bits, row=False, col=True)
+    _, bc, bref = _quant_both(cuda_lib, b_bits, row=False, col=True)
+    out = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad(ac, bc, G, torch.from_numpy(offsets).cuda(), out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    a_col = _deq(aref["col_payload"], aref["col_scales"], N, R)
+    b_col = _deq(bref["col_payload"], bref["col_scales"], K, R)
+    ref = O.wgrad(a_col, b_col, offsets)
+    got = bf16_cpu(out)
+    assert np.all(got[1] == 0.0), "zero-token expert must give an exactly zero slice"
+    assert O.within_tolerance(got, ref).all()
+
+
+def _moe_small(seed=0):
+    G, D, F, R = 4, 1024, 384, 1152
+    counts = [384, 0, 256, 384]
+    inp = W.moe_inputs(G, D, F, R, seed=seed)
+    return G, D, F, R, _offsets(counts), inp
+
+
+def test_swiglu_fwd_random(cuda_lib):
+    import torch
+    G, D, F, R, offsets, inp = _moe_small()
+    A = int(offsets[-1])
+    xr, _, xref = _quant_both(cuda_lib, inp["x"])
+    wr, _, wref = _quant_both(cuda_lib, inp["w1"])
+    z = torch.full((R, 2 * F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    z, h_row, h_col = cuda_lib.mx_grouped_gemm_swiglu_fwd(xr, wr, G, torch.from_numpy(offsets).cuda(), z=z)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    x = _deq(xref["row_payload"], xref["row_scales"], R, D)
+    w = _deq(wref["row_payload"], wref["row_scales"], G * 2 * F, D).reshape(G, 2 * F, D)
+    ref = O.swiglu_fwd(x, w, offsets)
+    zg = bf16_cpu(z)
+    assert O.within_tolerance(zg[:A], ref["z"][:A]).all()
+    assert np.all(np.isnan(zg[A:])), "inactive tail of z was written"
+    hp, hs = mx_bytes(h_row)
+    requant_close((hp[:A], hs), ref["h_row"], A, F)
+    cp, cs = mx_bytes(h_col)
+    # compare the active columns of h_col [F, R] through the logical scale matrix
+    got = O.dequantize_rows(cp, cs, F, R, O.E4M3)[:, :A]
+    want = O.dequantize_rows(*ref["h_col"], F, A, O.E4M3)
+    scale = np.repeat(2.0 ** (O.scales_to_matrix(cs, F, R // 32)[:, :A // 32].astype(np.float64) - 127), 32, axis=1)
+    assert np.all(np.abs(got - want) <= scale * 32.0)
+    assert np.mean(cp[:, :A] != ref["h_col"][0]) < 1e-2
+
+
+def test_swiglu_fwd_exact_product_bit_exact(cuda_lib):
+    """Small-integer operands make every product and partial sum exact in
+    fp32 and the gate >= 64 saturates sigmoid to 1.0, so h = g*u exactly and
+    the requantized bytes must match the oracle bit for bit."""
+    import torch
+    G, D, F, R = 2, 256, 128, 512
+    rng = np.random.default_rng(31)
+    x = rng.integers(1, 3, size=(R, D)).astype(np.float32)                 # 1 or 2
+    w1 = np.zeros((G, 2 * F, D), dtype=np.float32)
+    w1[:, :F, :64] = 1.0                                                     # gate = sum of 64 x's >= 64
+    w1[:, F:, :] = rng.integers(-1, 2, size=(G, F, D)).astype(np.float32)   # up in [-512, 512]
+    xb, w1b = W.to_bf16_bits(x), W.to_bf16_bits(w1)
+    offsets = np.array([256, 512], dtype=np.int32)
+    xr, _, xref = _quant_both(cuda_lib, xb)
+    wr, _, wref = _quant_both(cuda_lib, w1b)
+    z, h_row, h_col = cuda_lib.mx_grouped_gemm_swiglu_fwd(xr, wr, G, torch.from_numpy(offsets).cuda())
+    xd = _deq(xref["row_payload"], xref["row_scales"], R, D)
+    wd = _deq(wref["row_payload"], wref["row_scales"], G * 2 * F, D).reshape(G, 2 * F, D)
+    assert np.array_equal(xd, x) and np.array_equal(wd, w1)   # exact operands
+    ref = O.swiglu_fwd(xd, wd, offsets)
+    assert np.array_equal(bf16_cpu(z), O.bf16_out(ref["z"]))
+    assert_quant_equal(h_row, ref["h_row"], R, F // 32, "h_row")
+    assert_quant_equal(h_col, ref["h_col"], F, R // 32, "h_col")
+
+
+def test_dswiglu_bwd_random(cuda_lib):
+    import torch
+    G, D, F, R, offsets, inp = _moe_small(seed=1)
+    A = int(offsets[-1])
+    dyr, _, dyref = _quant_both(cuda_lib, inp["dy"])
+    w2t_bits = np.ascontiguousarray(np.transpose(inp["w2"], (0, 2, 1)))   # [G, F, D]
+    w2tr, _, wref = _quant_both(cuda_lib, w2t_bits)
+    zb = W.normal_bf16(np.random.default_rng(5), (R, 2 * F), std=2.0)
+    dz_row, dz_col = cuda_lib.mx_grouped_gemm_dswiglu_bwd(dyr, w2tr, to_dev(zb), G,
+                                                          torch.from_numpy(offsets).cuda())
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    dy = _deq(dyref["row_payload"], dyref["row_scales"], R, D)
+    w2t = _deq(wref["row_payload"], wref["row_scales"], G * F, D).reshape(G, F, D)
+    ref = O.dswiglu_bwd(dy, w2t, zb, offsets)
+    rp, rs = mx_bytes(dz_row)
+    requant_close((rp[:A], rs), ref["dz_row"], A, 2 * F)
+    cp, cs = mx_bytes(dz_col)
+    got = O.dequantize_rows(cp, cs, 2 * F, R, O.E4M3)[:, :A]
+    want = O.dequantize_rows(*ref["dz_col"], 2 * F, A, O.E4M3)
+    scale = np.repeat(2.0 ** (O.scales_to_matrix(cs, 2 * F, R // 32)[:, :A // 32].astype(np.float64) - 127), 32,
+                      axis=1)
+    assert np.all(np.abs(got - want) <= scale * 32.0)
+    assert np.mean(cp[:, :A] != ref["dz_col"][0]) < 1e-2
+
+
+def test_dswiglu_bwd_exact_product_bit_exact(cuda_lib):
+    """Saturated gates (g >= 64: sigmoid = 1 exactly) and small-integer dY,
+    W2 make dg = dh*u and du = dh*g exact: bytes must match bit for bit."""
+    import torch
+    G, D, F, R = 2, 256, 128, 512
+    rng = np.random.default_rng(32)
+    dy = rng.integers(-2, 3, size=(R, D)).astype(np.float32)
+    w2t = rng.integers(-1, 2, size=(G, F, D)).astype(np.float32)
+    z = np.concatenate([rng.integers(64, 128, size=(R, F)), rng.integers(-8, 9, size=(R, F))], axis=1)
+    dyb, w2tb, zb = W.to_bf16_bits(dy), W.to_bf16_bits(w2t), W.to_bf16_bits(z.astype(np.float32))
+    offsets = np.array([128, 512], dtype=np.int32)
+    dyr, _, dyref = _quant_both(cuda_lib, dyb)
+    w2tr, _, wref = _quant_both(cuda_lib, w2tb)
+    dz_row, dz_col = cuda_lib.mx_grouped_gemm_dswiglu_bwd(dyr, w2tr, to_dev(zb), G,
+                                                          torch.from_numpy(offsets).cuda())
+    dyd = _deq(dyref["row_payload"], dyref["row_scales"], R, D)
+    w2td = _deq(wref["row_payload"], wref["row_scales"], G * F, D).reshape(G, F, D)
+    assert np.array_equal(dyd, dy) and np.array_equal(w2td, w2t)
+    ref = O.dswiglu_bwd(dyd, w2td, zb, offsets)
+    assert_quant_equal(dz_row, ref["dz_row"], R, 2 * F // 32, "dz_row")
+    assert_quant_equal(dz_col, ref["dz_col"], 2 * F, R // 32, "dz_col")
+
+
+def test_mlp_step_against_oracle_chain(cuda_lib):
+    import torch
+    G, D, F, R, offsets, inp = _moe_small(seed=2)
+    A = int(offsets[-1])
+    t = {k: to_dev(v) for k, v in inp.items()}
+    dev = "cuda"
+    out = {"y": torch.full((R, D), float("nan"), dtype=torch.bfloat16, device=dev),
+           "dx": torch.full((R, D), float("nan"), dtype=torch.bfloat16, device=dev),
+           "dw1": torch.empty((G, 2 * F, D), dtype=torch.bfloat16, device=dev),
+           "dw2": torch.empty((G, D, F), dtype=torch.bfloat16, device=dev)}
+    offs = torch.from_numpy(offsets).cuda()
+    args = cuda_lib.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], offs, G, F, out["y"], out["dx"], out["dw1"],
+                             out["dw2"])
+    ws = torch.empty(cuda_lib.mx_mlp_workspace_bytes(args), dtype=torch.uint8, device=dev)
+    args = cuda_lib.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], offs, G, F, out["y"], out["dx"], out["dw1"],
+                             out["dw2"], workspace=ws)
+    cuda_lib.mx_mlp_fwd_bwd(args)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    ref = O.mlp_fwd_bwd_swiglu(inp["x"], inp["w1"], inp["w2"], inp["dy"], offsets)
+    unq = O.mlp_fwd_bwd_swiglu_unquantized(inp["x"], inp["w1"], inp["w2"], inp["dy"], offsets)
+    got = {k: bf16_cpu(v) for k, v in out.items()}
+    assert np.all(np.isnan(got["y"][A:])) and np.all(np.isnan(got["dx"][A:]))
+    assert np.all(got["dw1"][1] == 0) and np.all(got["dw2"][1] == 0)
+    for k in ("y", "dx", "dw1", "dw2"):
+        g = got[k][:A] if k in ("y", "dx") else got[k]
+        s_orc = O.sqnr_db(ref[k + "_f64"], g)
+        s_unq = O.sqnr_db(unq[k], g)
+        assert s_orc > 35.0, (k, s_orc)
+        assert s_unq > 17.0, (k, s_unq)   # MXFP8 chain band of the pages minus 6 dB
+    # run-to-run bitwise determinism
+    first = {k: v.clone() for k, v in out.items()}
+    cuda_lib.mx_mlp_fwd_bwd(args)
+    for k in out:
+        assert torch.equal(torch.nan_to_num(first[k]), torch.nan_to_num(out[k])), k
+
+
+def test_bounded_wait_reports_timeout(cuda_lib):
+    cuda_lib.mx_selftest_bounded_wait(50_000_000)   # 50 ms, nothing will arrive
+    assert cuda_lib.mx_get_device_status() == "MX_ERR_DEVICE_TIMEOUT"
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+
+
+def test_r_zero_and_g_zero(cuda_lib):
+    import torch
+    a = cuda_lib.MX(0, 256)
+    b = cuda_lib.MX(256, 256)
+    offs = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm(a, b, 1, offs, out=out, ld_out=256)
+    with pytest.raises(cuda_lib.MXError) as e:
+        cuda_lib.mx_grouped_gemm(a, b, 0, offs, out=out, ld_out=256)
+    assert e.value.name == "MX_ERR_INVALID_ARG"
