@@ -1,0 +1,447 @@
+"""Benchmark of the MX expert-MLP training step on GB300.
+
+One step = one pass of the whole hot path through the library's public C
+ABI: quantize X, W1, W2 (rowwise + per-expert columnwise MXFP8), FC1 grouped
+GEMM + SwiGLU + dual requant, FC2 grouped GEMM, quantize dY, FC2 dgrad +
+dSwiGLU + dual requant, FC1 dgrad, and the two ragged-K weight gradients.
+
+Workload: 128 experts, hidden 2048, expert FFN 768, 262144 routed rows
+(32768 tokens x top-8) with Zipf(1.1) per-expert row counts in multiples of
+128 (8 experts empty); BF16 X ~ N(0,1), W ~ N(0,0.02), dY ~ N(0,1e-3).
+Work per step: 18*R*D*F = 7.42 TFLOP.  Inputs (>= 403 MB each) are larger
+than the 129 MB L2, so no flush is needed between steps.
+
+JSON line fields beyond the common contract:
+  roofline      the step's dominant kernel: FLOP per launch / its mean
+                CUDA-event duration inside the timed steps, against the
+                measured dense peak (MEASURED_PEAKS.json bf16 x 2 for MXFP8)
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+  stages        per-kernel mean times and rates
+  quantizer     the standalone quantizer workload (8192 x 7168 BF16, both
+                orientations) in GB/s, L2 flushed between iterations
+
+--impl reference times the CPU oracle (the reference arm of this build).
+With torchrun (N > 1) every rank runs an independent replica (weak
+scaling); rank 0 prints the line, time is the max over ranks.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "grouped MX MLP fwd+bwd TFLOP/s and % of GB300 dense FP8 peak; quantizer HBM GB/s"
+SHAPE = dict(G=128, D=2048, F=768, R=262144)
+WORKLOAD = "moe_mlp_fwd_bwd_mxfp8 G=128 D=2048 F=768 R=262144 (32768 tok x top-8) zipf1.1"
+QUANT_GB = 238.6e6  # algorithmic bytes of the quantizer workload: 2 B in + 2 x (1 + 1/32) B out per element
+
+
+def step_flops(G, D, F, R):
+    return 18.0 * R * D * F
+
+
+def stage_flops(D, F, R):
+    return {"fc1_swiglu": 4.0 * R * D * F, "fc2": 2.0 * R * D * F, "fc2_dgrad_dswiglu": 2.0 * R * D * F,
+            "fc1_dgrad": 4.0 * R * D * F, "wgrad_dw2": 2.0 * R * D * F, "wgrad_dw1": 4.0 * R * D * F}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# --------------------------------------------------------------------------
+
+def oracle_sample(seconds_hint=20.0):
+    """Time the CPU oracle's full MLP chain on a bounded sample of the
+    workload: experts of the even-routing layout (2048 rows each, D=2048,
+    F=768), as many as fit in ~seconds_hint.  Returns (TFLOP/s, desc, cores)."""
+    import oracle as O
+    import workloads as W
+    D, F = SHAPE["D"], SHAPE["F"]
+    rows = 2048
+    done_flops, t_total, n = 0.0, 0.0, 0
+    while n == 0 or (t_total < seconds_hint and n < 8):
+        inp = W.moe_inputs(1, D, F, rows, seed=n)
+        offsets = np.array([rows], dtype=np.int32)
+        t0 = time.perf_counter()
+        O.mlp_fwd_bwd_swiglu(inp["x"], inp["w1"], inp["w2"], inp["dy"], offsets)
+        t_total += time.perf_counter() - t0
+        done_flops += step_flops(1, D, F, rows)
+        n += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = "%d expert(s) x %d rows, D=%d, F=%d: the oracle's whole fwd+bwd chain (%.1f s)" % (n, rows, D, F,
+                                                                                           t_total)
+    return done_flops / t_total / 1e12, desc, cores
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    tflops = []
+    for _ in range(args.warmup):
+        oracle_sample(seconds_hint=2.0)
+    desc, cores = "", 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, desc, cores = oracle_sample(seconds_hint=5.0)
+        tflops.append(v)
+    wall = time.perf_counter() - t0
+    value = float(np.mean(tflops))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import mlp_gemms_gb300 as mx
+    import workloads as W
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or world > 1:
+        from mlp_gemms_gb300 import build as _b
+        if rank == 0:
+            _b.build()
+    barrier(world)
+    mx.load()
+
+    G, D, F, R = SHAPE["G"], SHAPE["D"], SHAPE["F"], SHAPE["R"]
+    offsets_np = W.zipf_offsets(G, R)
+    offs = torch.from_numpy(offsets_np).to(dev)
+    inp = W.moe_inputs_device(G, D, F, R, seed=rank, device=dev)
+    out = {"y": torch.empty((R, D), dtype=torch.bfloat16, device=dev),
+           "dx": torch.empty((R, D), dtype=torch.bfloat16, device=dev),
+           "dw1": torch.empty((G, 2 * F, D), dtype=torch.bfloat16, device=dev),
+           "dw2": torch.empty((G, D, F), dtype=torch.bfloat16, device=dev)}
+    args0 = mx.mlp_args(inp["x"], inp["w1"], inp["w2"], inp["dy"], offs, G, F, out["y"], out["dx"], out["dw1"],
+                        out["dw2"])
+    ws = torch.empty(mx.mx_mlp_workspace_bytes(args0), dtype=torch.uint8, device=dev)
+    margs = mx.mlp_args(inp["x"], inp["w1"], inp["w2"], inp["dy"], offs, G, F, out["y"], out["dx"], out["dw1"],
+                        out["dw2"], workspace=ws)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- value: whole steps through mx_mlp_fwd_bwd, inputs resident ----
+    for _ in range(args.warmup):
+        mx.mx_mlp_fwd_bwd(margs)
+    torch.cuda.synchronize(dev)
+    if mx.mx_get_device_status() != "MX_OK":
+        raise RuntimeError("device status after warm-up: " + mx.mx_last_error())
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            mx.mx_mlp_fwd_bwd(margs)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    ms_step = ms_total / args.steps
+    flops = step_flops(G, D, F, R)
+    value = flops * world / (ms_step * 1e-3) / 1e12
+    launches_per_step = 9
+
+    # ---- per-kernel times: the same stages through their entry points ----
+    stages = stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, args.steps, dev)
+
+    # ---- e2e: host buffers, copies inside the timed region ----
+    e2e = end_to_end(mx, torch, inp, offs, G, D, F, R, max(2, min(args.steps, 5)), dev, world)
+
+    # ---- standalone quantizer workload ----
+    quant = quantizer_rate(mx, torch, dev)
+    status = mx.mx_get_device_status()
+    if status != "MX_OK":
+        raise RuntimeError("device status: " + status)
+
+    peaks, peak_kind = measured_peaks()
+    # the dominant kernel of the step: largest share of the step's time
+    dom = max(stages, key=lambda k: stages[k]["ms"] * stages[k]["launches"])
+    sf = stage_flops(D, F, R)
+    peak_fp8 = 2.0 * peaks["bf16_tflops_sustained"]   # MXFP8 dense = 2 x bf16 dense (nominal ratio)
+    achieved = sf[dom] / (stages[dom]["ms"] * 1e-3) / 1e12 if dom in sf else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp8-e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (no flush)",
+                   "flop_per_step": flops, "frac_of_fp8_peak": value / world / peak_fp8,
+                   "peak_fp8_tflops": peak_fp8, "peak_kind": peak_kind + " (bf16 sustained x 2)"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_fp8,
+                     "unit": "TFLOP/s", "frac": (achieved / peak_fp8) if achieved else None, "traffic": None},
+        "stages": stages,
+        "quantizer": quant,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, cores = oracle_sample(seconds_hint=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev):
+    """Mean CUDA-event duration of each kernel of the step, launched through
+    the stage entry points in the order the step uses (events on the
+    launching stream between launches)."""
+    stream = torch.cuda.current_stream(dev)
+    qx = (mx.MX(R, D), mx.MX(D, R))
+    qw1 = (mx.MX(G * 2 * F, D), mx.MX(G * D, 2 * F))
+    qw2 = (mx.MX(G * D, F), mx.MX(G * F, D))
+    qdy = (mx.MX(R, D), mx.MX(D, R))
+    h = (mx.MX(R, F), mx.MX(F, R))
+    dz = (mx.MX(R, 2 * F), mx.MX(2 * F, R))
+    z = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    names = ["quant_x", "quant_w1", "quant_w2", "fc1_swiglu", "fc2", "quant_dy", "fc2_dgrad_dswiglu", "fc1_dgrad",
+             "wgrad_dw2", "wgrad_dw1"]
+    calls = [
+        lambda: mx.mx_quantize(inp["x"], 0, True, True, out_row=qx[0], out_col=qx[1]),
+        lambda: mx.mx_quantize(inp["w1"], 0, True, True, out_row=qw1[0], out_col=qw1[1]),
+        lambda: mx.mx_quantize(inp["w2"], 0, True, True, out_row=qw2[0], out_col=qw2[1]),
+        lambda: mx.mx_grouped_gemm_swiglu_fwd(qx[0], qw1[0], G, offs, h[0], h[1], z),
+        lambda: mx.mx_grouped_gemm(h[0], qw2[0], G, offs, out=out["y"]),
+        lambda: mx.mx_quantize(inp["dy"], 0, True, True, out_row=qdy[0], out_col=qdy[1]),
+        lambda: mx.mx_grouped_gemm_dswiglu_bwd(qdy[0], qw2[1], z, G, offs, dz[0], dz[1]),
+        lambda: mx.mx_grouped_gemm(dz[0], qw1[1], G, offs, out=out["dx"]),
+        lambda: mx.mx_grouped_gemm_wgrad(qdy[1], h[1], G, offs, out=out["dw2"]),
+        lambda: mx.mx_grouped_gemm_wgrad(dz[1], qx[1], G, offs, out=out["dw1"]),
+    ]
+    for _ in range(2):
+        for c in calls:
+            c()
+    torch.cuda.synchronize(dev)
+    n = max(3, min(steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(n)]
+    for i in range(n):
+        evs[i][0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            evs[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    sf = stage_flops(D, F, R)
+    qbytes = {"quant_x": 2 * R * D * (2 + 2 * (1 + 1 / 32)) / 2, "quant_dy": 2 * R * D * (2 + 2 * (1 + 1 / 32)) / 2,
+              "quant_w1": G * 2 * F * D * (2 + 2 * (1 + 1 / 32)), "quant_w2": G * D * F * (2 + 2 * (1 + 1 / 32))}
+    res = {}
+    for j, name in enumerate(names):
+        t = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n)]
+        ms = float(np.mean(t))
+        d = {"ms": ms, "launches": 1}
+        if name in sf:
+            d["tflops"] = sf[name] / (ms * 1e-3) / 1e12
+        if name in qbytes:
+            d["gbs"] = qbytes[name] / (ms * 1e-3) / 1e9
+        res[name] = d
+    return res
+
+
+def end_to_end(mx, torch, inp, offs, G, D, F, R, steps, dev, world):
+    """Same step through mx_mlp_fwd_bwd from pinned host buffers: each step
+    copies its inputs host->device and its results device->host."""
+    host_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
+    for k, v in inp.items():
+        host_in[k].copy_(v)
+    host_off = torch.empty(offs.shape, dtype=offs.dtype, pin_memory=True)
+    host_off.copy_(offs)
+    shapes = {"y": (R, D), "dx": (R, D), "dw1": (G, 2 * F, D), "dw2": (G, D, F)}
+    host_out = {k: torch.empty(s, dtype=torch.bfloat16, pin_memory=True) for k, s in shapes.items()}
+    d_in = {k: torch.empty_like(v) for k, v in inp.items()}
+    d_off = torch.empty_like(offs)
+    d_out = {k: torch.empty(s, dtype=torch.bfloat16, device=dev) for k, s in shapes.items()}
+    a0 = mx.mlp_args(d_in["x"], d_in["w1"], d_in["w2"], d_in["dy"], d_off, G, F, d_out["y"], d_out["dx"],
+                     d_out["dw1"], d_out["dw2"])
+    ws = torch.empty(mx.mx_mlp_workspace_bytes(a0), dtype=torch.uint8, device=dev)
+    margs = mx.mlp_args(d_in["x"], d_in["w1"], d_in["w2"], d_in["dy"], d_off, G, F, d_out["y"], d_out["dx"],
+                        d_out["dw1"], d_out["dw2"], workspace=ws)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values()) + host_off.numel() * 4
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k in host_in:
+            d_in[k].copy_(host_in[k], non_blocking=True)
+        d_off.copy_(host_off, non_blocking=True)
+        mx.mx_mlp_fwd_bwd(margs)
+        for k in host_out:
+            host_out[k].copy_(d_out[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize(dev)
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev) / steps
+    del ws, d_in, d_out
+    torch.cuda.empty_cache()
+    return {"value": step_flops(G, D, F, R) * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+
+
+def quantizer_rate(mx, torch, dev):
+    """The standalone quantizer workload: 8192 x 7168 BF16 -> MXFP8 rowwise
+    and columnwise; the 117 MB input fits in L2, so a 512 MB buffer is
+    written between iterations to flush it."""
+    import workloads as W
+    bits = W.quantizer_input(**W.QUANT_SHAPE) if os.environ.get("MX_BENCH_QUANT_SPECIALS") else None
+    rows, cols = W.QUANT_SHAPE["rows"], W.QUANT_SHAPE["cols"]
+    if bits is None:
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        x = torch.randn((rows, cols), generator=g, device=dev).to(torch.bfloat16)
+    else:
+        x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    r, c = mx.MX(rows, cols), mx.MX(cols, rows)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+    ts = []
+    for _ in range(20):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    ms = float(np.mean(ts))
+    peaks, kind = measured_peaks()
+    gbs = QUANT_GB / (ms * 1e-3) / 1e9
+    return {"workload": "8192x7168 bf16 -> mxfp8 row+col", "us": ms * 1e3, "gbs": gbs,
+            "frac_of_hbm": gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"], "peak_kind": kind,
+            "l2": "flushed (512 MB write) between iterations"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

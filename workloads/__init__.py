@@ -168,3 +168,19 @@ def dense_inputs(M, D, H, seed=0):
 MOE_SHAPE = dict(G=128, D=2048, F=768, R=262144)
 DENSE_SHAPE = dict(M=16384, D=3072, H=12288)
 QUANT_SHAPE = dict(rows=8192, cols=7168)
+
+
+def moe_inputs_device(G, D, F, R, seed=0, dy_seed=2, device="cuda"):
+    """Full-size MoE inputs drawn on the GPU (same distributions as
+    ``moe_inputs``; torch's seeded device generator, so the values differ
+    from the numpy draw).  Used where drawing ~1.7e9 normals on the host
+    would dominate the run."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn((R, D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    w1 = (torch.randn((G, 2 * F, D), generator=g, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn((G, D, F), generator=g, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    g.manual_seed(dy_seed)
+    dy = (torch.randn((R, D), generator=g, device=device, dtype=torch.float32) * 1e-3).to(torch.bfloat16)
+    return {"x": x, "w1": w1, "w2": w2, "dy": dy}
