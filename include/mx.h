@@ -144,7 +144,8 @@ MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, 
  * each expert's row segment, nondecreasing, each a multiple of 128,
  * offsets[G-1] <= R.  Rows in [offsets[G-1], R) are neither read nor
  * written (caller-allocated outputs keep their contents there).  An empty
- * segment is allowed.  ([MXFP8-PR] shared-infrastructure commit: per-expert
+ * segment is allowed; with G == 1 a NULL offsets means one segment of all R
+ * rows.  ([MXFP8-PR] shared-infrastructure commit: per-expert
  * row counts are multiples of 128, so no tile straddles an expert and the
  * expert of a tile follows from its row base; cudnn-fe ops commit: rows past
  * offsets[-1] are untouched in caller-allocated outputs.)  Values are not
@@ -214,6 +215,44 @@ MX_API mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t *dy_row, const 
  */
 MX_API mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
                                   const int32_t *offsets_dev, void *out_bf16, mx_stream_t stream);
+
+/*
+ * Dense (single-segment) calls of the MXFP6 Flux-style MLP ([MXFP6-PR]
+ * fused-MLP commit: one unit owns fc1 -> activation -> fc2, the packer takes
+ * the activation as an epilogue in the forward and its derivative in the
+ * backward, the pre-activation gradient is never assembled in BF16, the bias
+ * gradient comes back as a per-column sum; bias commits: the bias is added in
+ * the fp32 accumulator before one rounding).  M, K and the output width are
+ * multiples of 128; operands of any MX format, both operands alike.
+ */
+
+/* out[m, n] = sum_k A[m, k] B[n, k] + bias[n] (fp32), stored as BF16.
+ *   a [M, K], b [N, K] rowwise MX; bias_bf16 device BF16 [N] or NULL. */
+MX_API mx_status_t mx_gemm_bias(const mx_tensor_t *a, const mx_tensor_t *b, const void *bias_bf16, void *out_bf16,
+                                int64_t ld_out, mx_stream_t stream);
+
+/* FC1 forward with the tanh-GELU epilogue.
+ *   x_row [M, D], w1_row [H, D] rowwise MX; b1_bf16 device BF16 [H] or NULL
+ *   pre_bf16  out, device BF16 [M, H] = x W1^T + b1 (the saved pre-activation)
+ *   act_row   out, [M, H] rowwise MX of act = gelu_tanh(pre) (fp32 pre)
+ *   act_col   out, [H, M] columnwise MX of act
+ * act_row / act_col: format E4M3 or E2M3, same format and rotation flag on
+ * both; with the rotation, each 32-block is rotated before packing. */
+MX_API mx_status_t mx_gemm_gelu_fwd(const mx_tensor_t *x_row, const mx_tensor_t *w1_row, const void *b1_bf16,
+                                    void *pre_bf16, const mx_tensor_t *act_row, const mx_tensor_t *act_col,
+                                    mx_stream_t stream);
+
+/* FC2 dgrad with the dGELU epilogue.
+ *   dy_row [M, D] rowwise MX; w2t_row [H, D] rowwise MX of W2^T (W2 [D, H])
+ *   pre_bf16  device BF16 [M, H] from mx_gemm_gelu_fwd
+ *   dpre_row  out, [M, H] rowwise MX of dpre = (dY W2) * gelu_tanh'(pre)
+ *   dpre_col  out, [H, M] columnwise MX of dpre
+ *   db1       out, device fp32 [H] = sum over rows of dpre (fixed order)
+ *   workspace >= mx_gemm_dgelu_workspace_bytes(M, H), 16-byte aligned */
+MX_API size_t mx_gemm_dgelu_workspace_bytes(int64_t M, int64_t H);
+MX_API mx_status_t mx_gemm_dgelu_bwd(const mx_tensor_t *dy_row, const mx_tensor_t *w2t_row, const void *pre_bf16,
+                                     const mx_tensor_t *dpre_row, const mx_tensor_t *dpre_col, float *db1,
+                                     void *workspace, size_t workspace_bytes, mx_stream_t stream);
 
 /* Activation of mx_mlp_fwd_bwd. */
 typedef enum { MX_ACT_SWIGLU = 0, MX_ACT_GELU_TANH = 1 } mx_act_t;

@@ -31,7 +31,8 @@ ABI_SYMBOLS = (
     "mx_abi_version", "mx_last_error", "mx_status_string", "mx_payload_bytes", "mx_scale_bytes",
     "mx_quantize_workspace_bytes", "mx_quantize", "mx_grouped_gemm", "mx_grouped_gemm_swiglu_fwd",
     "mx_grouped_gemm_dswiglu_bwd", "mx_grouped_gemm_wgrad", "mx_mlp_workspace_bytes", "mx_mlp_fwd_bwd",
-    "mx_get_device_status", "mx_selftest_bounded_wait",
+    "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
+    "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd",
 )
 
 
@@ -87,6 +88,10 @@ def load(path=None):
         "mx_mlp_fwd_bwd": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp]),
         "mx_get_device_status": (ctypes.c_int, [vp]),
         "mx_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
+        "mx_gemm_bias": (ctypes.c_int, [tp, tp, vp, vp, i64, vp]),
+        "mx_gemm_gelu_fwd": (ctypes.c_int, [tp, tp, vp, vp, tp, tp, vp]),
+        "mx_gemm_dgelu_workspace_bytes": (sz, [i64, i64]),
+        "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -221,6 +226,53 @@ def mx_grouped_gemm_wgrad(a_col, b_col, G, offsets, out=None, stream=None):
         out = torch.empty((G, a_col.rows, b_col.rows), dtype=torch.bfloat16, device=a_col.data.device)
     _check(load().mx_grouped_gemm_wgrad(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(out), _stream(stream)))
     return out
+
+
+def mx_gemm_bias(a, b, bias=None, out=None, ld_out=None, stream=None):
+    import torch
+    if out is None:
+        out = torch.empty((a.rows, b.rows), dtype=torch.bfloat16, device=a.data.device)
+    ld = ld_out if ld_out is not None else out.stride(0)
+    _check(load().mx_gemm_bias(_s(a), _s(b), _ptr(bias), _ptr(out), ld, _stream(stream)))
+    return out
+
+
+def mx_gemm_gelu_fwd(x_row, w1_row, b1=None, pre=None, act_row=None, act_col=None, fmt=E2M3, hadamard=True,
+                     stream=None):
+    import torch
+    M, H = x_row.rows, w1_row.rows
+    dev = x_row.data.device
+    if pre is None:
+        pre = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    if act_row is None:
+        act_row = MX(M, H, fmt, hadamard, dev)
+    if act_col is None:
+        act_col = MX(H, M, fmt, hadamard, dev)
+    _check(load().mx_gemm_gelu_fwd(_s(x_row), _s(w1_row), _ptr(b1), _ptr(pre), _s(act_row), _s(act_col),
+                                   _stream(stream)))
+    return pre, act_row, act_col
+
+
+def mx_gemm_dgelu_workspace_bytes(M, H):
+    return int(load().mx_gemm_dgelu_workspace_bytes(M, H))
+
+
+def mx_gemm_dgelu_bwd(dy_row, w2t_row, pre, dpre_row=None, dpre_col=None, db1=None, workspace=None, fmt=E2M3,
+                      hadamard=True, stream=None):
+    import torch
+    M, H = dy_row.rows, w2t_row.rows
+    dev = dy_row.data.device
+    if dpre_row is None:
+        dpre_row = MX(M, H, fmt, hadamard, dev)
+    if dpre_col is None:
+        dpre_col = MX(H, M, fmt, hadamard, dev)
+    if db1 is None:
+        db1 = torch.empty(H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(mx_gemm_dgelu_workspace_bytes(M, H), 16), dtype=torch.uint8, device=dev)
+    _check(load().mx_gemm_dgelu_bwd(_s(dy_row), _s(w2t_row), _ptr(pre), _s(dpre_row), _s(dpre_col), _ptr(db1),
+                                    _ptr(workspace), workspace.numel(), _stream(stream)))
+    return dpre_row, dpre_col, db1
 
 
 def mlp_args(x, w1, w2, dy, offsets, G, F, y, dx, dw1, dw2, workspace=None, act=ACT_SWIGLU, fmt=E4M3,

@@ -95,20 +95,29 @@ mx_status_t get_encoder() {
   return MX_OK;
 }
 
-// 2-D byte tensor [rows, row_bytes], box 128 bytes x 128 rows, 128-byte swizzle.
-mx_status_t make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+// 2-D MX payload [rows, K elements] as a TMA tensor, box 128 elements x 128
+// rows with the 128-byte swizzle.  E4M3 is plain bytes; E2M3 and E2M1 use
+// the packed sub-byte types, which expand each 16-element group into a
+// 16-byte shared-memory slot -- the operand form the block-scaled MMA reads.
+mx_status_t make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int fmt) {
   mx_status_t st = get_encoder();
   if (st != MX_OK) return st;
-  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  CUtensorMapDataType dt = fmt == MX_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                           : (fmt == MX_E2M3 ? CU_TENSOR_MAP_DATA_TYPE_16U6_ALIGN16B
+                                             : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B);
+  cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)mx::payload_row_bytes(k, fmt)};
   cuuint32_t box[2] = {128, 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return MX_OK;
 }
+
+// tcgen05 .kind::mxf8f6f4 element type code of an MX format.
+int mma_type(int fmt) { return fmt == MX_E4M3 ? 0 : (fmt == MX_E2M3 ? 3 : 5); }
 
 // ---- argument checks ----------------------------------------------------
 
@@ -135,9 +144,19 @@ mx_status_t check_gemm_operand(const mx_tensor_t* t, const char* name) {
     MX_CHECK(aligned16(t->data) && aligned16(t->scale), MX_ERR_ALIGNMENT, "%s pointers must be 16-byte aligned",
              name);
   }
-  MX_CHECK(t->fmt == MX_E4M3, MX_ERR_NOT_SUPPORTED, "%s: the grouped GEMMs take E4M3 operands in this build", name);
-  MX_CHECK(t->hadamard == 0, MX_ERR_NOT_SUPPORTED, "%s: rotated operands are not supported by the grouped GEMMs", name);
+  MX_CHECK(t->fmt >= MX_E4M3 && t->fmt <= MX_E2M1, MX_ERR_INVALID_ARG, "%s has format %d", name, t->fmt);
+  // the packed sub-byte tensor-map types need 32-byte aligned rows
+  MX_CHECK(t->fmt == MX_E4M3 || (reinterpret_cast<uintptr_t>(t->data) & 31u) == 0, MX_ERR_ALIGNMENT,
+           "%s: E2M3/E2M1 payload must be 32-byte aligned", name);
   MX_CHECK(t->rows < (1ll << 31) && t->cols < (1ll << 31), MX_ERR_SHAPE, "%s exceeds the int32 coordinate range", name);
+  return MX_OK;
+}
+
+mx_status_t check_pair(const mx_tensor_t* a, const mx_tensor_t* b, const char* an, const char* bn) {
+  MX_CHECK(a->fmt == b->fmt, MX_ERR_INVALID_ARG, "%s and %s have different formats (%d, %d)", an, bn, a->fmt, b->fmt);
+  MX_CHECK((a->hadamard != 0) == (b->hadamard != 0), MX_ERR_INVALID_ARG,
+           "%s and %s must both carry the rotation or neither", an, bn);
+  MX_CHECK(a->fmt == MX_E4M3 || a->cols % 128 == 0, MX_ERR_SHAPE, "packed operands need K %% 128 == 0");
   return MX_OK;
 }
 
@@ -164,19 +183,19 @@ mx_status_t validate_offsets_values(const int32_t* offsets_dev, int G, int64_t R
 
 mx_status_t check_offsets(const int32_t* offsets, int32_t G, int64_t R, cudaStream_t s) {
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  if (offsets == nullptr && G == 1) return MX_OK;  // one segment of all rows
   MX_CHECK(offsets != nullptr, MX_ERR_INVALID_ARG, "offsets is NULL");
   MX_CHECK((reinterpret_cast<uintptr_t>(offsets) & 3u) == 0, MX_ERR_ALIGNMENT, "offsets must be 4-byte aligned");
   if (env_validate_offsets()) return validate_offsets_values(offsets, G, R, s);
   return MX_OK;
 }
 
-mx_status_t run_gemm(const mx::GemmParams& p, const void* a_data, int64_t a_rows, int64_t a_row_bytes,
-                     const void* b_data, int64_t b_rows, int64_t b_row_bytes, int bn, cudaStream_t s,
+mx_status_t run_gemm(const mx::GemmParams& p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
                      const DevInfo& dev) {
   CUtensorMap ta, tb;
-  mx_status_t st = make_tmap(&ta, a_data, a_rows, a_row_bytes);
+  mx_status_t st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt);
   if (st != MX_OK) return st;
-  if ((st = make_tmap(&tb, b_data, b_rows, b_row_bytes)) != MX_OK) return st;
+  if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
   cudaError_t e = mx::launch_gemm(p, ta, tb, bn, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
   return MX_OK;
@@ -286,6 +305,7 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   mx_status_t st;
   if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
   if ((st = check_gemm_operand(b, "b")) != MX_OK) return st;
+  if ((st = check_pair(a, b, "a", "b")) != MX_OK) return st;
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
   MX_CHECK(a->cols == b->cols, MX_ERR_SHAPE, "a has K = %lld, b has K = %lld", (long long)a->cols, (long long)b->cols);
   const int64_t K = a->cols, R = a->rows;
@@ -308,7 +328,7 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   p.G = G;
   p.offsets = offsets_dev;
   p.R = R; p.K = K; p.Nb = N;
-  p.a_type = 0; p.b_type = 0;
+  p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
   p.sfa = a->scale; p.sfb = b->scale;
   p.sfa_kchunks = (K / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
@@ -317,7 +337,7 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = ld_out;
-  return run_gemm(p, a->data, R, K, b->data, b->rows, K, bn, s, dev);
+  return run_gemm(p, a, b, bn, s, dev);
 }
 
 mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
@@ -327,6 +347,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   mx_status_t st;
   if ((st = check_gemm_operand(x_row, "x_row")) != MX_OK) return st;
   if ((st = check_gemm_operand(w1_row, "w1_row")) != MX_OK) return st;
+  if ((st = check_pair(x_row, w1_row, "x_row", "w1_row")) != MX_OK) return st;
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
   const int64_t R = x_row->rows, D = x_row->cols;
   MX_CHECK(w1_row->cols == D, MX_ERR_SHAPE, "w1_row has K = %lld, x_row has %lld", (long long)w1_row->cols,
@@ -349,6 +370,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   p.epi = mx::EPI_SWIGLU;
   p.G = G; p.offsets = offsets_dev;
   p.R = R; p.K = D; p.Nb = 2 * F; p.F = F;
+  p.a_type = mma_type(x_row->fmt); p.b_type = mma_type(w1_row->fmt);
   p.sfa = x_row->scale; p.sfb = w1_row->scale;
   p.sfa_kchunks = (D / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
@@ -359,7 +381,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   p.q_row = static_cast<uint8_t*>(h_row->data); p.q_row_scale = h_row->scale;
   p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
   p.q_cols = F;
-  return run_gemm(p, x_row->data, R, D, w1_row->data, w1_row->rows, D, 256, s, dev);
+  return run_gemm(p, x_row, w1_row, 256, s, dev);
 }
 
 mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
@@ -369,6 +391,7 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   mx_status_t st;
   if ((st = check_gemm_operand(dy_row, "dy_row")) != MX_OK) return st;
   if ((st = check_gemm_operand(w2t_row, "w2t_row")) != MX_OK) return st;
+  if ((st = check_pair(dy_row, w2t_row, "dy_row", "w2t_row")) != MX_OK) return st;
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
   const int64_t R = dy_row->rows, D = dy_row->cols;
   MX_CHECK(w2t_row->cols == D, MX_ERR_SHAPE, "w2t_row has K = %lld, dy_row has %lld", (long long)w2t_row->cols,
@@ -391,6 +414,7 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   p.epi = mx::EPI_DSWIGLU;
   p.G = G; p.offsets = offsets_dev;
   p.R = R; p.K = D; p.Nb = F; p.F = F;
+  p.a_type = mma_type(dy_row->fmt); p.b_type = mma_type(w2t_row->fmt);
   p.sfa = dy_row->scale; p.sfb = w2t_row->scale;
   p.sfa_kchunks = (D / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
@@ -401,7 +425,7 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   p.q_row = static_cast<uint8_t*>(dz_row->data); p.q_row_scale = dz_row->scale;
   p.q_col = static_cast<uint8_t*>(dz_col->data); p.q_col_scale = dz_col->scale;
   p.q_cols = 2 * F;
-  return run_gemm(p, dy_row->data, R, D, w2t_row->data, w2t_row->rows, D, 128, s, dev);
+  return run_gemm(p, dy_row, w2t_row, 128, s, dev);
 }
 
 mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
@@ -410,6 +434,7 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   mx_status_t st;
   if ((st = check_gemm_operand(a_col, "a_col")) != MX_OK) return st;
   if ((st = check_gemm_operand(b_col, "b_col")) != MX_OK) return st;
+  if ((st = check_pair(a_col, b_col, "a_col", "b_col")) != MX_OK) return st;
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
   const int64_t N = a_col->rows, K = b_col->rows, R = a_col->cols;
   MX_CHECK(b_col->cols == R, MX_ERR_SHAPE, "a_col has R = %lld, b_col has %lld", (long long)R,
@@ -428,6 +453,7 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   p.epi = mx::EPI_BF16;
   p.G = G; p.offsets = offsets_dev;
   p.R = R; p.K = R; p.Nb = K; p.Mw = N;
+  p.a_type = mma_type(a_col->fmt); p.b_type = mma_type(b_col->fmt);
   p.sfa = a_col->scale; p.sfb = b_col->scale;
   p.sfa_kchunks = (R / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
@@ -436,18 +462,151 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   p.num_tiles = (int64_t)G * p.m_tiles * p.n_tiles;
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = K;
-  return run_gemm(p, a_col->data, N, R, b_col->data, K, R, bn, s, dev);
+  return run_gemm(p, a_col, b_col, bn, s, dev);
+}
+
+mx_status_t mx_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, const void* bias_bf16, void* out_bf16,
+                         int64_t ld_out, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
+  if ((st = check_gemm_operand(b, "b")) != MX_OK) return st;
+  if ((st = check_pair(a, b, "a", "b")) != MX_OK) return st;
+  const int64_t M = a->rows, K = a->cols, N = b->rows;
+  MX_CHECK(b->cols == K, MX_ERR_SHAPE, "a has K = %lld, b has K = %lld", (long long)K, (long long)b->cols);
+  MX_CHECK(K % 128 == 0 && M % 128 == 0 && N > 0 && N % 128 == 0, MX_ERR_SHAPE,
+           "M = %lld, N = %lld, K = %lld must be multiples of 128", (long long)M, (long long)N, (long long)K);
+  MX_CHECK(out_bf16 != nullptr && aligned16(out_bf16), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
+  MX_CHECK(bias_bf16 == nullptr || aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be 16-byte aligned");
+  MX_CHECK(ld_out >= N && ld_out % 8 == 0, MX_ERR_ALIGNMENT, "ld_out = %lld must be >= N and a multiple of 8",
+           (long long)ld_out);
+  if (M == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  const int bn = (N % 256 == 0) ? 256 : 128;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_GROUPED;
+  p.epi = mx::EPI_BF16;
+  p.G = 1; p.offsets = nullptr;
+  p.R = M; p.K = K; p.Nb = N;
+  p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
+  p.sfa = a->scale; p.sfb = b->scale;
+  p.sfa_kchunks = (K / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)(M / 128);
+  p.n_tiles = (int)(N / bn);
+  p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+  p.out = static_cast<uint16_t*>(out_bf16);
+  p.out_ld = ld_out;
+  p.bias = static_cast<const uint16_t*>(bias_bf16);
+  return run_gemm(p, a, b, bn, s, dev);
+}
+
+namespace {
+
+// Shared set-up of the two dense fused epilogues: A [M, K], B [H, K],
+// requant outputs q_row [M, H] and q_col [H, M] of one format and rotation.
+mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, const void* bias_bf16, void* pre_bf16,
+                        const mx_tensor_t* q_row, const mx_tensor_t* q_col, float* partials, cudaStream_t s,
+                        int64_t* M_out, int64_t* H_out) {
+  mx_status_t st;
+  const char* an = epi == mx::EPI_GELU ? "x_row" : "dy_row";
+  const char* bn = epi == mx::EPI_GELU ? "w1_row" : "w2t_row";
+  if ((st = check_gemm_operand(a, an)) != MX_OK) return st;
+  if ((st = check_gemm_operand(b, bn)) != MX_OK) return st;
+  if ((st = check_pair(a, b, an, bn)) != MX_OK) return st;
+  const int64_t M = a->rows, K = a->cols, H = b->rows;
+  *M_out = M;
+  *H_out = H;
+  MX_CHECK(b->cols == K, MX_ERR_SHAPE, "%s has K = %lld, %s has K = %lld", an, (long long)K, bn, (long long)b->cols);
+  MX_CHECK(M % 128 == 0 && K % 128 == 0 && H > 0 && H % 128 == 0, MX_ERR_SHAPE,
+           "M = %lld, H = %lld, K = %lld must be multiples of 128", (long long)M, (long long)H, (long long)K);
+  MX_CHECK(q_row != nullptr && q_col != nullptr, MX_ERR_INVALID_ARG, "requant outputs are NULL");
+  MX_CHECK(q_row->fmt == MX_E4M3 || q_row->fmt == MX_E2M3, MX_ERR_NOT_SUPPORTED,
+           "the dense epilogues requantize to E4M3 or E2M3");
+  if ((st = check_tensor(q_row, epi == mx::EPI_GELU ? "act_row" : "dpre_row", M, H, q_row->fmt, q_row->hadamard)) != MX_OK)
+    return st;
+  if ((st = check_tensor(q_col, epi == mx::EPI_GELU ? "act_col" : "dpre_col", H, M, q_row->fmt, q_row->hadamard)) != MX_OK)
+    return st;
+  MX_CHECK(pre_bf16 != nullptr && aligned16(pre_bf16), MX_ERR_ALIGNMENT, "pre must be a 16-byte aligned pointer");
+  MX_CHECK(bias_bf16 == nullptr || aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be 16-byte aligned");
+  if (M == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::GemmParams p = base_params();
+  p.mode = mx::MODE_GROUPED;
+  p.epi = epi;
+  p.G = 1; p.offsets = nullptr;
+  p.R = M; p.K = K; p.Nb = H;
+  p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
+  p.sfa = a->scale; p.sfb = b->scale;
+  p.sfa_kchunks = (K / 32 + 3) / 4;
+  p.sfb_kchunks = p.sfa_kchunks;
+  p.m_tiles = (int)(M / 128);
+  p.n_tiles = (int)(H / 128);
+  p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
+  p.z = static_cast<uint16_t*>(pre_bf16);
+  p.q_row = static_cast<uint8_t*>(q_row->data); p.q_row_scale = q_row->scale;
+  p.q_col = static_cast<uint8_t*>(q_col->data); p.q_col_scale = q_col->scale;
+  p.q_cols = H;
+  p.q_row_ld = mx::payload_row_bytes(H, q_row->fmt);
+  p.q_col_ld = mx::payload_row_bytes(M, q_row->fmt);
+  p.q_fmt = q_row->fmt;
+  p.q_had = q_row->hadamard ? 1 : 0;
+  p.bias = static_cast<const uint16_t*>(bias_bf16);
+  p.colsum_partials = partials;
+  CUtensorMap ta, tb;
+  if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
+  if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
+  cudaError_t e = mx::launch_gemm_dense(p, ta, tb, s, dev.sms);
+  if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
+  return MX_OK;
+}
+
+}  // namespace
+
+mx_status_t mx_gemm_gelu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, const void* b1_bf16,
+                             void* pre_bf16, const mx_tensor_t* act_row, const mx_tensor_t* act_col,
+                             mx_stream_t stream) {
+  int64_t M, H;
+  return dense_fused(mx::EPI_GELU, x_row, w1_row, b1_bf16, pre_bf16, act_row, act_col, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), &M, &H);
+}
+
+size_t mx_gemm_dgelu_workspace_bytes(int64_t M, int64_t H) {
+  if (M <= 0 || H <= 0) return 0;
+  return (size_t)((M + 127) / 128) * (size_t)H * sizeof(float);
+}
+
+mx_status_t mx_gemm_dgelu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* pre_bf16,
+                              const mx_tensor_t* dpre_row, const mx_tensor_t* dpre_col, float* db1, void* workspace,
+                              size_t workspace_bytes, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  MX_CHECK(dy_row != nullptr && w2t_row != nullptr, MX_ERR_INVALID_ARG, "operands are NULL");
+  const int64_t M0 = dy_row->rows, H0 = w2t_row->rows;
+  MX_CHECK(db1 != nullptr && aligned16(db1), MX_ERR_INVALID_ARG, "db1 must be a 16-byte aligned pointer");
+  MX_CHECK(workspace != nullptr && aligned16(workspace) && workspace_bytes >= mx_gemm_dgelu_workspace_bytes(M0, H0),
+           MX_ERR_WORKSPACE, "needs %zu bytes of 16-byte aligned workspace", mx_gemm_dgelu_workspace_bytes(M0, H0));
+  int64_t M, H;
+  mx_status_t st = dense_fused(mx::EPI_DGELU, dy_row, w2t_row, nullptr, const_cast<void*>(pre_bf16), dpre_row,
+                               dpre_col, static_cast<float*>(workspace), s, &M, &H);
+  if (st != MX_OK || M == 0) return st;
+  cudaError_t e = mx::launch_colsum_reduce(static_cast<const float*>(workspace), M / 128, H, db1, s);
+  if (e != cudaSuccess) return cuda_fail(e, "column-sum reduce launch");
+  return MX_OK;
 }
 
 // ---- the MLP step -------------------------------------------------------
 
 namespace {
 
+// Workspace of one MLP step: every quantized operand between the stages,
+// the BF16 pre-activation and (GELU) the column-sum partials.
 struct MlpLayout {
   size_t total = 0;
   struct Slot { size_t data, scale; int64_t rows, cols; };
   Slot x_row, x_col, w1_row, w1t_row, w2_row, w2t_row, h_row, h_col, dy_row, dy_col, dz_row, dz_col;
-  size_t z;
+  size_t z, part_dy, part_dz;
 };
 
 size_t align_up(size_t x) { return (x + 255) / 256 * 256; }
@@ -455,27 +614,35 @@ size_t align_up(size_t x) { return (x + 255) / 256 * 256; }
 MlpLayout mlp_layout(const mx_mlp_args_t* a) {
   MlpLayout L;
   size_t off = 0;
+  const int fmt = a->fmt;
   auto slot = [&](int64_t rows, int64_t cols) {
     MlpLayout::Slot s;
     s.rows = rows; s.cols = cols;
-    s.data = off; off = align_up(off + (size_t)rows * (size_t)cols);
+    s.data = off; off = align_up(off + (size_t)rows * (size_t)mx::payload_row_bytes(cols, fmt));
     s.scale = off; off = align_up(off + mx::scale_bytes(rows, cols / 32));
     return s;
   };
   const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
+  const bool glu = a->act == MX_ACT_SWIGLU;
+  const int64_t F1 = glu ? 2 * F : F;  // FC1 output width
   L.x_row = slot(R, D);
   L.x_col = slot(D, R);
-  L.w1_row = slot(G * 2 * F, D);
-  L.w1t_row = slot(G * D, 2 * F);
+  L.w1_row = slot(G * F1, D);
+  L.w1t_row = slot(G * D, F1);
   L.w2_row = slot(G * D, F);
   L.w2t_row = slot(G * F, D);
   L.h_row = slot(R, F);
   L.h_col = slot(F, R);
   L.dy_row = slot(R, D);
   L.dy_col = slot(D, R);
-  L.dz_row = slot(R, 2 * F);
-  L.dz_col = slot(2 * F, R);
-  L.z = off; off = align_up(off + (size_t)R * 2 * (size_t)F * 2);
+  L.dz_row = slot(R, F1);
+  L.dz_col = slot(F1, R);
+  L.z = off; off = align_up(off + (size_t)R * (size_t)F1 * 2);
+  L.part_dy = L.part_dz = off;
+  if (!glu) {
+    L.part_dy = off; off = align_up(off + (size_t)((R + 127) / 128) * (size_t)D * 4);
+    L.part_dz = off; off = align_up(off + (size_t)((R + 127) / 128) * (size_t)F * 4);
+  }
   L.total = off;
   return L;
 }
@@ -486,22 +653,84 @@ mx_tensor_t view(const mx_mlp_args_t* a, const MlpLayout::Slot& s) {
   t.data = base + s.data;
   t.scale = base + s.scale;
   t.rows = s.rows; t.cols = s.cols;
-  t.fmt = MX_E4M3; t.hadamard = 0;
+  t.fmt = a->fmt; t.hadamard = a->hadamard ? 1 : 0;
   return t;
+}
+
+mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream) {
+  const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
+  mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
+  mx_tensor_t w1_row = view(a, L.w1_row), w1t_row = view(a, L.w1t_row);
+  mx_tensor_t w2_row = view(a, L.w2_row), w2t_row = view(a, L.w2t_row);
+  mx_tensor_t h_row = view(a, L.h_row), h_col = view(a, L.h_col);
+  mx_tensor_t dy_row = view(a, L.dy_row), dy_col = view(a, L.dy_col);
+  mx_tensor_t dz_row = view(a, L.dz_row), dz_col = view(a, L.dz_col);
+  void* z = static_cast<uint8_t*>(a->workspace) + L.z;
+  const uint32_t both = MX_ROWWISE | MX_COLWISE;
+  mx_status_t st;
+  if ((st = mx_quantize(a->x, 1, R, D, D, MX_E4M3, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w1, G, 2 * F, D, D, MX_E4M3, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w2, G, D, F, F, MX_E4M3, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_swiglu_fwd(&x_row, &w1_row, a->G, a->offsets, &h_row, &h_col, z, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->dy, 1, R, D, D, MX_E4M3, both, &dy_row, &dy_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_dswiglu_bwd(&dy_row, &w2t_row, z, a->G, a->offsets, &dz_row, &dz_col, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_wgrad(&dy_col, &h_col, a->G, a->offsets, a->dw2, stream)) != MX_OK) return st;
+  return mx_grouped_gemm_wgrad(&dz_col, &x_col, a->G, a->offsets, a->dw1, stream);
+}
+
+// Dense GELU step ([MXFP6-PR] fused-MLP commit): 12 launches.
+mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream) {
+  const int64_t M = a->R, D = a->D, H = a->F;
+  const int fmt = a->fmt;
+  const uint32_t both = MX_ROWWISE | MX_COLWISE | (a->hadamard ? MX_HADAMARD : 0);
+  mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
+  mx_tensor_t w1_row = view(a, L.w1_row), w1t_row = view(a, L.w1t_row);
+  mx_tensor_t w2_row = view(a, L.w2_row), w2t_row = view(a, L.w2t_row);
+  mx_tensor_t act_row = view(a, L.h_row), act_col = view(a, L.h_col);
+  mx_tensor_t dy_row = view(a, L.dy_row), dy_col = view(a, L.dy_col);
+  mx_tensor_t dpre_row = view(a, L.dz_row), dpre_col = view(a, L.dz_col);
+  uint8_t* base = static_cast<uint8_t*>(a->workspace);
+  void* pre = base + L.z;
+  const size_t part_dy_bytes = (size_t)((M + 127) / 128) * (size_t)D * 4;
+  const size_t part_dz_bytes = (size_t)((M + 127) / 128) * (size_t)H * 4;
+  mx_status_t st;
+  if ((st = mx_quantize(a->x, 1, M, D, D, fmt, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w1, 1, H, D, D, fmt, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->w2, 1, D, H, H, fmt, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  if ((st = mx_gemm_gelu_fwd(&x_row, &w1_row, a->b1, pre, &act_row, &act_col, stream)) != MX_OK) return st;
+  if ((st = mx_gemm_bias(&act_row, &w2_row, a->b2, a->y, D, stream)) != MX_OK) return st;
+  if ((st = mx_quantize(a->dy, 1, M, D, D, fmt, both | MX_COLSUM, &dy_row, &dy_col, a->db2, base + L.part_dy,
+                        part_dy_bytes, stream)) != MX_OK)
+    return st;
+  if ((st = mx_gemm_dgelu_bwd(&dy_row, &w2t_row, pre, &dpre_row, &dpre_col, a->db1, base + L.part_dz,
+                              part_dz_bytes, stream)) != MX_OK)
+    return st;
+  if ((st = mx_grouped_gemm(&dpre_row, &w1t_row, 1, nullptr, a->dx, D, stream)) != MX_OK) return st;
+  if ((st = mx_grouped_gemm_wgrad(&dy_col, &act_col, 1, nullptr, a->dw2, stream)) != MX_OK) return st;
+  return mx_grouped_gemm_wgrad(&dpre_col, &x_col, 1, nullptr, a->dw1, stream);
 }
 
 }  // namespace
 
 size_t mx_mlp_workspace_bytes(const mx_mlp_args_t* args) {
   if (!args || args->R < 0 || args->D <= 0 || args->F <= 0 || args->G <= 0) return 0;
+  if (args->fmt < MX_E4M3 || args->fmt > MX_E2M1) return 0;
   return mlp_layout(args).total;
 }
 
 mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
   MX_CHECK(a != nullptr, MX_ERR_INVALID_ARG, "args is NULL");
-  MX_CHECK(a->act == MX_ACT_SWIGLU, MX_ERR_NOT_SUPPORTED, "activation %d is not supported by this build", a->act);
-  MX_CHECK(a->fmt == MX_E4M3 && a->hadamard == 0, MX_ERR_NOT_SUPPORTED,
-           "the SwiGLU step runs on unrotated E4M3 operands");
+  MX_CHECK(a->act == MX_ACT_SWIGLU || a->act == MX_ACT_GELU_TANH, MX_ERR_INVALID_ARG, "activation %d", a->act);
+  if (a->act == MX_ACT_SWIGLU) {
+    MX_CHECK(a->fmt == MX_E4M3 && a->hadamard == 0, MX_ERR_NOT_SUPPORTED,
+             "the SwiGLU expert step runs on unrotated E4M3 operands");
+  } else {
+    MX_CHECK(a->fmt == MX_E4M3 || a->fmt == MX_E2M3, MX_ERR_NOT_SUPPORTED, "the GELU step runs on E4M3 or E2M3");
+    MX_CHECK(a->G == 1, MX_ERR_NOT_SUPPORTED, "the GELU step is dense (G == 1)");
+    MX_CHECK(a->db1 != nullptr && a->db2 != nullptr, MX_ERR_INVALID_ARG, "db1 and db2 are required");
+  }
   MX_CHECK(a->G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", a->G);
   MX_CHECK(a->R >= 0 && a->R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)a->R);
   MX_CHECK(a->D > 0 && a->D % 128 == 0, MX_ERR_SHAPE, "D = %lld is not a positive multiple of 128", (long long)a->D);
@@ -519,34 +748,18 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
   mx_status_t st;
   if ((st = check_offsets(a->offsets, a->G, a->R, s)) != MX_OK) return st;
   if (a->R == 0) return MX_OK;
-  const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
-  mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
-  mx_tensor_t w1_row = view(a, L.w1_row), w1t_row = view(a, L.w1t_row);
-  mx_tensor_t w2_row = view(a, L.w2_row), w2t_row = view(a, L.w2t_row);
-  mx_tensor_t h_row = view(a, L.h_row), h_col = view(a, L.h_col);
-  mx_tensor_t dy_row = view(a, L.dy_row), dy_col = view(a, L.dy_col);
-  mx_tensor_t dz_row = view(a, L.dz_row), dz_col = view(a, L.dz_col);
-  void* z = static_cast<uint8_t*>(a->workspace) + L.z;
-  const uint32_t both = MX_ROWWISE | MX_COLWISE;
-  if ((st = mx_quantize(a->x, 1, R, D, D, MX_E4M3, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
-  if ((st = mx_quantize(a->w1, G, 2 * F, D, D, MX_E4M3, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
-  if ((st = mx_quantize(a->w2, G, D, F, F, MX_E4M3, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm_swiglu_fwd(&x_row, &w1_row, a->G, a->offsets, &h_row, &h_col, z, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
-  if ((st = mx_quantize(a->dy, 1, R, D, D, MX_E4M3, both, &dy_row, &dy_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm_dswiglu_bwd(&dy_row, &w2t_row, z, a->G, a->offsets, &dz_row, &dz_col, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm_wgrad(&dy_col, &h_col, a->G, a->offsets, a->dw2, stream)) != MX_OK) return st;
-  if ((st = mx_grouped_gemm_wgrad(&dz_col, &x_col, a->G, a->offsets, a->dw1, stream)) != MX_OK) return st;
-  return MX_OK;
+  return a->act == MX_ACT_SWIGLU ? mlp_swiglu(a, L, stream) : mlp_gelu(a, L, stream);
 }
 
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned word = 0;
-  if ((e = mx::read_gemm_status(&word)) != cudaSuccess) return cuda_fail(e, "reading device status");
-  if ((e = mx::reset_gemm_status()) != cudaSuccess) return cuda_fail(e, "clearing device status");
+  unsigned word = 0, dense = 0;
+  if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess)
+    return cuda_fail(e, "reading device status");
+  if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess)
+    return cuda_fail(e, "clearing device status");
+  word |= dense;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
   return MX_OK;

@@ -1,0 +1,751 @@
+// The grouped block-scaled GEMM kernel template on the 5th-generation tensor core, with
+// fused epilogues: BF16 store, SwiGLU forward (BF16 pre-activation save +
+// dual-orientation MXFP8 requant) and dSwiGLU backward (dual requant of dz).
+//
+// torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP fwd/bwd and wgrad
+// group gemm":
+//   * shared-infrastructure commit: per-expert row counts are multiples of
+//     128 so no tile straddles an expert; the expert of a tile is found from
+//     its integer row base, with no per-group tensor-map updates; the
+//     blocked scale layout has a constant 512-byte K stride per 128-row
+//     block, so the scale chunk of (row block, K block) is one address;
+//   * correctness-first kernels commit: FC1 grouped GEMM + SwiGLU + dual
+//     (1x32 rowwise, 32x1 columnwise) MXFP8 RCEIL quantization + BF16
+//     pre-activation save in one launch; FC2 dgrad + dSwiGLU + dual
+//     quantization in one launch; ragged-K wgrad with BF16 output where a
+//     zero-token expert gets zeros.
+//
+// Kernel organisation (one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: A/B tiles (128-byte swizzled, K-major) and the
+//               512-byte scale chunks into a ring of shared-memory stages;
+//   warp 1      owns tensor memory; one lane copies each stage's scale
+//               chunks into tensor memory (tcgen05.cp 32x128b.warpx4) and
+//               issues tcgen05.mma .kind::mxf8f6f4.block_scale (M=128, N=BN,
+//               K=32 per instruction, fp32 accumulators in tensor memory);
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
+//               32*(w%4)..+31, two warps per lane quarter split the
+//               columns), then the fused math and stores.
+// With BN = 256 there is one accumulator buffer; the epilogue copies it to
+// registers and releases it before its math, so the next tile's MMAs run
+// under the epilogue.  With BN = 128 two accumulator buffers alternate.
+// Every wait is bounded in time; on expiry the kernel records a device
+// status bit and unwinds without leaving copies or MMAs in flight.
+#pragma once
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+
+// One status word per translation unit that instantiates the kernel.
+static __device__ unsigned g_gemm_status = 0;
+
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_THREADS = 256;
+constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 5;
+  static constexpr int ACC = BN == 256 ? 1 : 2;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int SF_BYTES = 512 + (BN / 128) * 512;
+  static constexpr int SF_COLS = 4 + 4 * (BN / 128);
+  static constexpr uint32_t TX = A_BYTES + B_BYTES + SF_BYTES;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_TB = OFF_SF + STAGES * SF_BYTES;  // 8 x 2 KB transpose buffers
+  static constexpr int OFF_CHUNK = OFF_TB + 8 * 2048;        // scale chunks + column-sum partials
+  static constexpr int OFF_BAR = OFF_CHUNK + 4096;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;    // + slack for 1024-byte alignment
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t SF_TMEM_BASE = 256;
+  static_assert(ACC * BN <= 256, "accumulators live in tensor-memory columns 0..255");
+  static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "scale slots must fit");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+struct Tile {
+  int active;
+  int g;
+  int64_t m0, n0;
+  int64_t kbeg;
+  int nk;
+};
+
+__device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
+
+// Tile t -> (expert, row base, column base, K range).  Grouped: tiles are
+// row-block-major over all R rows; the expert is the segment holding the
+// row base.  Wgrad: tiles are expert-major; K runs over the expert's rows.
+template <int NT, int MODE>
+__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report) {
+  Tile T;
+  T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0;
+  if (MODE == MODE_GROUPED) {
+    int64_t mt = t / p.n_tiles, nt = t % p.n_tiles;
+    T.m0 = mt * 128;
+    T.n0 = nt * NT;
+    // no offsets: one dense segment of all R rows
+    int64_t total = p.offsets ? ldg_i32(p.offsets + p.G - 1) : p.R;
+    if (T.m0 >= total) return T;  // inactive tail
+    int lo = 0, hi = p.G - 1;
+    while (lo < hi) {
+      int mid = (lo + hi) >> 1;
+      if ((int64_t)ldg_i32(p.offsets + mid) > T.m0) hi = mid; else lo = mid + 1;
+    }
+    int64_t end = p.offsets ? ldg_i32(p.offsets + lo) : p.R;
+    int64_t start = lo ? ldg_i32(p.offsets + lo - 1) : 0;
+    bool bad = (start & 127) || (end & 127) || start > T.m0 || end <= T.m0 || end > p.R || total > p.R;
+    if (bad) {
+      if (report) atomicOr(&g_gemm_status, DEV_BAD_OFFSETS);
+      return T;
+    }
+    T.g = lo;
+    T.nk = (int)(p.K / 128);
+    T.active = 1;
+  } else {
+    int64_t per_g = (int64_t)p.m_tiles * p.n_tiles;
+    T.g = (int)(t / per_g);
+    int64_t rem = t % per_g;
+    T.m0 = (rem / p.n_tiles) * 128;
+    T.n0 = (rem % p.n_tiles) * NT;
+    int64_t end = p.offsets ? ldg_i32(p.offsets + T.g) : p.R;
+    int64_t start = T.g ? ldg_i32(p.offsets + T.g - 1) : 0;
+    bool bad = (start & 127) || (end & 127) || end < start || end > p.R || start < 0;
+    if (bad && report) atomicOr(&g_gemm_status, DEV_BAD_OFFSETS);
+    T.kbeg = bad ? 0 : start;
+    T.nk = bad ? 0 : (int)((end - start) / 128);
+    T.active = 1;
+  }
+  return T;
+}
+
+// ---- epilogue helpers --------------------------------------------------
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+// Rowwise E4M3 requant of 32 fp32 values held by one thread.
+__device__ __forceinline__ uint32_t row_quant_store_e4m3(float (&v)[32], uint8_t* dst) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; i++) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  uint32_t sb = rceil_scale_byte<E4M3>(amax);
+  uint32_t w[8];
+  quantize_block_words<E4M3>(v, sb, w);
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return sb;
+}
+
+// Columnwise E4M3 requant of two columns whose 32-row block is spread over
+// the warp's lanes (lane = row): warp-wide integer max of |bits| gives each
+// column's amax; both codes go to the transpose buffer tb[col][lane].
+__device__ __forceinline__ void col_quant_pair_e4m3(float v0, float v1, uint8_t* tb_col0, uint8_t* tb_col1,
+                                                    uint32_t& sb0, uint32_t& sb1, int lane) {
+  uint32_t a0 = __reduce_max_sync(0xffffffffu, __float_as_uint(v0) & 0x7FFFFFFFu);
+  uint32_t a1 = __reduce_max_sync(0xffffffffu, __float_as_uint(v1) & 0x7FFFFFFFu);
+  sb0 = rceil_scale_byte<E4M3>(a0);
+  sb1 = rceil_scale_byte<E4M3>(a1);
+  uint32_t c = cvt_e4m3x2(v0 * inv_scale_from_byte(sb0), v1 * inv_scale_from_byte(sb1));
+  uint32_t c0 = sb0 == 0xFFu ? 0x7Fu : (c & 0xFFu);
+  uint32_t c1 = sb1 == 0xFFu ? 0x7Fu : (c >> 8);
+  tb_col0[lane] = (uint8_t)c0;
+  tb_col1[lane] = (uint8_t)c1;
+}
+
+__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint8_t* chunk, int lane) {
+  reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(chunk)[lane];
+}
+
+// Generic requant helpers (element format QF, optional 32-point rotation).
+
+// tanh-GELU and its derivative in fp32 (Primus PR #1064 "feat(mxfp6): MXFP6
+// (E2M3) Flux linears, a fused MLP, and the MLPerf recipe": the fused MLP's
+// tanh GELU epilogue and its derivative as the backward prologue).
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float u = k0 * (x + 0.044715f * x * x * x);
+  return 0.5f * x * (1.0f + tanhf(u));
+}
+__device__ __forceinline__ float dgelu_tanh_f(float x) {
+  const float k0 = 0.7978845608028654f;
+  const float x2 = x * x;
+  const float t = tanhf(k0 * (x + 0.044715f * x2 * x));
+  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x2);
+}
+
+// Rowwise requant of 32 fp32 values held by one thread (rotated first if QH).
+template <int QF, bool QH>
+__device__ __forceinline__ uint32_t row_quant_store(float (&v)[32], uint8_t* dst) {
+  if constexpr (QH) hadamard32(v);
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 32; i++) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  const uint32_t sb = rceil_scale_byte<QF>(amax);
+  uint32_t w[8];
+  quantize_block_words<QF>(v, sb, w);
+  if constexpr (QF == E4M3) {
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else if constexpr (QF == E2M1) {
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    reinterpret_cast<uint2*>(dst)[0] = make_uint2(w[0], w[1]);
+    reinterpret_cast<uint2*>(dst)[1] = make_uint2(w[2], w[3]);
+    reinterpret_cast<uint2*>(dst)[2] = make_uint2(w[4], w[5]);
+  }
+  return sb;
+}
+
+// Columnwise requant of one column whose 32-row block is spread over the
+// warp (lane = row): optional rotation across the lanes (the same five
+// butterfly stages, partner lane = lane ^ stride), warp-wide amax, and this
+// lane's code into the transpose buffer.  Returns the block's scale byte.
+template <int QF, bool QH>
+__device__ __forceinline__ uint32_t col_quant_one(float v, uint8_t* tb_col, int lane) {
+  if constexpr (QH) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, h);
+      v = (lane & h) ? __fsub_rn(o, v) : __fadd_rn(v, o);
+    }
+    v = __fmul_rn(v, __uint_as_float(0x3E3504F3u));
+  }
+  const uint32_t a = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7FFFFFFFu);
+  const uint32_t sb = rceil_scale_byte<QF>(a);
+  uint32_t code;
+  if (sb == 0xFFu) {
+    code = QF == E4M3 ? 0x7Fu : 0u;
+  } else {
+    const float sv = v * inv_scale_from_byte(sb);
+    if constexpr (QF == E4M3) code = cvt_e4m3x2(sv, 0.f) & 0xFFu;
+    else if constexpr (QF == E2M3) code = cvt_e2m3x2(sv, 0.f) & 0x3Fu;
+    else code = cvt_e2m1x2(sv, 0.f) & 0xFu;
+  }
+  tb_col[lane] = (uint8_t)code;
+  return sb;
+}
+
+// Pack the 32 one-byte codes of a column block (shared memory) into the
+// payload format and store them.
+template <int QF>
+__device__ __forceinline__ void store_col_codes(const uint8_t* codes, uint8_t* dst) {
+  const uint4 a = reinterpret_cast<const uint4*>(codes)[0];
+  const uint4 b = reinterpret_cast<const uint4*>(codes)[1];
+  if constexpr (QF == E4M3) {
+    reinterpret_cast<uint4*>(dst)[0] = a;
+    reinterpret_cast<uint4*>(dst)[1] = b;
+  } else {
+    const uint32_t cw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};  // 4 codes per word
+    if constexpr (QF == E2M3) {
+      uint32_t g[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++)
+        g[i] = (cw[i] & 0x3Fu) | (((cw[i] >> 8) & 0x3Fu) << 6) | (((cw[i] >> 16) & 0x3Fu) << 12) |
+               (((cw[i] >> 24) & 0x3Fu) << 18);
+      uint2* d = reinterpret_cast<uint2*>(dst);
+      d[0] = make_uint2(g[0] | (g[1] << 24), (g[1] >> 8) | (g[2] << 16));
+      d[1] = make_uint2((g[2] >> 16) | (g[3] << 8), g[4] | (g[5] << 24));
+      d[2] = make_uint2((g[5] >> 8) | (g[6] << 16), (g[6] >> 16) | (g[7] << 8));
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const uint32_t lo = cw[2 * i], hi = cw[2 * i + 1];
+        w[i] = (lo & 0xFu) | ((lo >> 4) & 0xF0u) | ((lo >> 8) & 0xF00u) | ((lo >> 12) & 0xF000u) |
+               ((hi & 0xFu) << 16) | (((hi >> 8) & 0xFu) << 20) | (((hi >> 16) & 0xFu) << 24) |
+               (((hi >> 24) & 0xFu) << 28);
+      }
+      reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// ---- the kernel ---------------------------------------------------------
+
+template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+  using C = Cfg<BN>;
+  constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  uint8_t* sSF = smem + C::OFF_SF;
+  uint8_t* sTB = smem + C::OFF_TB;
+  uint8_t* sChunk = smem + C::OFF_CHUNK;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + C::ACC;
+  uint64_t* final_bar = acc_empty + C::ACC;
+  uint64_t* epi_bar = final_bar + 1;  // the 8 epilogue warps' own barrier
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 8); }
+    mbar_init(final_bar, 1);
+    mbar_init(epi_bar, 8);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) { prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); }
+  if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_first();
+      const uint64_t pol_b = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed_parity[C::STAGES];
+      for (int s = 0; s < C::STAGES; s++) armed_parity[s] = -1;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        Tile T = get_tile<NT, MODE>(p, t, false);
+        if (!T.active || T.nk == 0) continue;
+        int64_t brow[2];
+        if (EPI == EPI_SWIGLU) {
+          brow[0] = (int64_t)T.g * 2 * p.F + T.n0;
+          brow[1] = brow[0] + p.F;
+        } else if (MODE == MODE_GROUPED) {
+          brow[0] = (int64_t)T.g * p.Nb + T.n0;
+          brow[1] = brow[0] + 128;
+        } else {
+          brow[0] = T.n0;
+          brow[1] = T.n0 + 128;
+        }
+        for (int kb = 0; kb < T.nk; kb++) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[stage], C::TX);
+          armed_parity[stage] = (int)phase;
+          const int64_t kc = T.kbeg / 128 + kb;
+          const int kx = (int)(kc * 128);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmA, kx, (int)T.m0, &full[stage], pol_a);
+#pragma unroll
+          for (int i = 0; i < BN / 128; i++)
+            tma_load_2d(sB + stage * C::B_BYTES + i * 16384, &tmB, kx, (int)brow[i], &full[stage], pol_b);
+          uint8_t* sf = sSF + stage * C::SF_BYTES;
+          bulk_load(sf, p.sfa + ((T.m0 >> 7) * p.sfa_kchunks + kc) * 512, 512, &full[stage]);
+#pragma unroll
+          for (int i = 0; i < BN / 128; i++)
+            bulk_load(sf + 512 + i * 512, p.sfb + ((brow[i] >> 7) * p.sfb_kchunks + kc) * 512, 512, &full[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Every copy this thread issued must have landed before the CTA exits
+      // (also after an abort: the drain ignores the abort flag, not the clock).
+      volatile int no_abort = 0;
+      for (int s = 0; s < C::STAGES; s++)
+        if (armed_parity[s] >= 0) mbar_wait_bounded(&full[s], (uint32_t)armed_parity[s], &no_abort, WAIT_BUDGET_NS);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        Tile T = get_tile<NT, MODE>(p, t, false);
+        if (!T.active || T.nk == 0) continue;
+        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < T.nk; kb++) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + C::SF_TMEM_BASE + (uint32_t)(stage * C::SF_COLS);
+          const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
+          tc_copy_scales(sf_t, sf_s);
+#pragma unroll
+          for (int i = 0; i < BN / 128; i++) tc_copy_scales(sf_t + 4 + 4 * i, sf_s + 512 + 512 * i);
+          const uint32_t a_s = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_s = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int j = 0; j < 4; j++) {
+            const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
+            const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
+            const uint32_t idesc = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 128, BN, j, j);
+            tc_mma_mx(d_tmem, adesc, bdesc, idesc, sf_t, sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == C::ACC) { acc = 0; acc_phase ^= 1u; }
+      }
+      // No MMA may still be writing tensor memory when it is freed.
+      volatile int no_abort = 0;
+      tc_commit(final_bar);
+      mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;       // 0..7
+    const int q = warp & 3;        // tensor-memory lane quarter
+    const int half = ew >> 2;      // column half
+    uint8_t* tb = sTB + ew * 2048;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t epi_phase = 0;
+    // Barrier among the epilogue warps, bounded like every other wait.
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(epi_bar);
+      bool ok = mbar_wait_bounded(epi_bar, epi_phase, abort_flag, WAIT_BUDGET_NS);
+      epi_phase ^= 1u;
+      return ok;
+    };
+    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      Tile T = get_tile<NT, MODE>(p, t, ew == 0 && lane == 0);
+      if (!T.active) continue;
+      const int64_t row_in_tile = q * 32 + lane;
+      if (T.nk == 0) {
+        if (EPI == EPI_BF16) {  // zero-token expert: an exactly zero gradient slice
+          const int64_t row = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + row_in_tile;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_ld + T.n0 + half * (BN / 2));
+#pragma unroll
+          for (int c = 0; c < BN / 16; c++) dst[c] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, WAIT_BUDGET_NS)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+
+      if constexpr (EPI == EPI_BF16) {
+        constexpr int COLS = BN / 2;
+        uint32_t v[COLS / 32][32];
+#pragma unroll
+        for (int i = 0; i < COLS / 32; i++) tmem_ld32(tbase + half * COLS + 32 * i, v[i]);
+        tmem_wait_ld();
+        if (C::ACC == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+        const int64_t row = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + row_in_tile;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_ld + T.n0 + half * COLS);
+        if (p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
+          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + T.n0 + half * COLS);
+#pragma unroll
+          for (int i = 0; i < COLS / 32; i++) {
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+              const uint4 bw = __ldg(bp + i * 4 + c);
+              const uint32_t b4[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+              for (int k = 0; k < 8; k++) {
+                const float bv = bf16_bits_to_float((k & 1) ? (b4[k >> 1] >> 16) : (b4[k >> 1] & 0xFFFFu));
+                v[i][8 * c + k] = __float_as_uint(__uint_as_float(v[i][8 * c + k]) + bv);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < COLS / 32; i++) {
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            const uint32_t* s = &v[i][8 * c];
+            dst[i * 4 + c] = make_uint4(
+                float2_to_bf16x2(__uint_as_float(s[0]), __uint_as_float(s[1])),
+                float2_to_bf16x2(__uint_as_float(s[2]), __uint_as_float(s[3])),
+                float2_to_bf16x2(__uint_as_float(s[4]), __uint_as_float(s[5])),
+                float2_to_bf16x2(__uint_as_float(s[6]), __uint_as_float(s[7])));
+          }
+        }
+        if (C::ACC == 2) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        // accumulator columns: [0,128) gate of f0..f0+127, [128,256) up
+        uint32_t gv[2][32], uv[2][32];
+        tmem_ld32(tbase + half * 64, gv[0]);
+        tmem_ld32(tbase + half * 64 + 32, gv[1]);
+        tmem_ld32(tbase + 128 + half * 64, uv[0]);
+        tmem_ld32(tbase + 128 + half * 64 + 32, uv[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+
+        const int64_t row = T.m0 + row_in_tile;
+        const int64_t f0 = T.n0;
+        // BF16 pre-activation save: z = [gate | up]
+        uint16_t* zr = p.z + row * (2 * p.F);
+        uint4* zg = reinterpret_cast<uint4*>(zr + f0 + half * 64);
+        uint4* zu = reinterpret_cast<uint4*>(zr + p.F + f0 + half * 64);
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+#pragma unroll
+          for (int c = 0; c < 4; c++) {
+            const uint32_t* s = &gv[i][8 * c];
+            zg[i * 4 + c] = make_uint4(float2_to_bf16x2(__uint_as_float(s[0]), __uint_as_float(s[1])),
+                                       float2_to_bf16x2(__uint_as_float(s[2]), __uint_as_float(s[3])),
+                                       float2_to_bf16x2(__uint_as_float(s[4]), __uint_as_float(s[5])),
+                                       float2_to_bf16x2(__uint_as_float(s[6]), __uint_as_float(s[7])));
+            const uint32_t* u = &uv[i][8 * c];
+            zu[i * 4 + c] = make_uint4(float2_to_bf16x2(__uint_as_float(u[0]), __uint_as_float(u[1])),
+                                       float2_to_bf16x2(__uint_as_float(u[2]), __uint_as_float(u[3])),
+                                       float2_to_bf16x2(__uint_as_float(u[4]), __uint_as_float(u[5])),
+                                       float2_to_bf16x2(__uint_as_float(u[6]), __uint_as_float(u[7])));
+          }
+        }
+        // h = g * sigmoid(g) * u in fp32
+        float h[2][32];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+#pragma unroll
+          for (int j = 0; j < 32; j++) {
+            float g = __uint_as_float(gv[i][j]), u = __uint_as_float(uv[i][j]);
+            h[i][j] = g * sigmoidf_(g) * u;
+          }
+        }
+        uint8_t* chunk_row = sChunk;
+        uint8_t* chunk_col = sChunk + 512;
+        // rowwise: two thread-local 32-column blocks
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+          float tmp[32];
+#pragma unroll
+          for (int j = 0; j < 32; j++) tmp[j] = h[i][j];
+          uint32_t sb = row_quant_store_e4m3(tmp, p.q_row + row * p.q_cols + f0 + half * 64 + 32 * i);
+          chunk_row[lane * 16 + q * 4 + half * 2 + i] = (uint8_t)sb;
+        }
+        // columnwise: 64 columns, each a 32-row block across the warp
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int col = i * 32 + j;  // 0..63 within this thread's half
+            uint32_t sb0, sb1;
+            col_quant_pair_e4m3(h[i][j], h[i][j + 1], tb + col * 32, tb + (col + 1) * 32, sb0, sb1, lane);
+            if (lane == 0) {
+              const int f = half * 64 + col;
+              chunk_col[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb0;
+              chunk_col[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb1;
+            }
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+          const int col = lane + 32 * k;
+          const uint4* s = reinterpret_cast<const uint4*>(tb + col * 32);
+          uint4* d = reinterpret_cast<uint4*>(p.q_col + (f0 + half * 64 + col) * p.R + T.m0 + q * 32);
+          d[0] = s[0];
+          d[1] = s[1];
+        }
+        if (!epi_sync()) break;
+        if (ew == 0) {
+          int64_t ck = (T.m0 >> 7) * ((p.q_cols / 32 + 3) / 4) + (f0 >> 7);
+          store_chunk(p.q_row_scale + ck * 512, chunk_row, lane);
+        } else if (ew == 1) {
+          int64_t ck = (f0 >> 7) * ((p.R / 32 + 3) / 4) + (T.m0 >> 7);
+          store_chunk(p.q_col_scale + ck * 512, chunk_col, lane);
+        }
+        if (!epi_sync()) break;
+      } else if constexpr (EPI == EPI_DSWIGLU) {
+        // accumulator columns [0,128): dh for f0..f0+127
+        const int64_t row = T.m0 + row_in_tile;
+        const int64_t f0 = T.n0;
+        const uint16_t* zr = p.z + row * (2 * p.F);
+        uint8_t* ch_gr = sChunk;
+        uint8_t* ch_ur = sChunk + 512;
+        uint8_t* ch_gc = sChunk + 1024;
+        uint8_t* ch_uc = sChunk + 1536;
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ch++) {
+          const int fc = half * 64 + ch * 32;  // tile-local column of this chunk
+          uint32_t dh[32];
+          tmem_ld32(tbase + fc, dh);
+          uint4 zgw[4], zuw[4];
+          const uint4* zgp = reinterpret_cast<const uint4*>(zr + f0 + fc);
+          const uint4* zup = reinterpret_cast<const uint4*>(zr + p.F + f0 + fc);
+#pragma unroll
+          for (int i = 0; i < 4; i++) { zgw[i] = zgp[i]; zuw[i] = zup[i]; }
+          tmem_wait_ld();
+          float dg[32], du[32];
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const uint32_t gw[4] = {zgw[i].x, zgw[i].y, zgw[i].z, zgw[i].w};
+            const uint32_t uw[4] = {zuw[i].x, zuw[i].y, zuw[i].z, zuw[i].w};
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+              const int j = i * 8 + k;
+              const float g = bf16_bits_to_float((k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu));
+              const float u = bf16_bits_to_float((k & 1) ? (uw[k >> 1] >> 16) : (uw[k >> 1] & 0xFFFFu));
+              const float d = __uint_as_float(dh[j]);
+              const float s = sigmoidf_(g);
+              dg[j] = d * u * s * (1.0f + g * (1.0f - s));
+              du[j] = d * g * s;
+            }
+          }
+          // columnwise first (the rowwise packer scales its input in place)
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            uint32_t sb0, sb1, sb2, sb3;
+            col_quant_pair_e4m3(dg[j], dg[j + 1], tb + j * 32, tb + (j + 1) * 32, sb0, sb1, lane);
+            col_quant_pair_e4m3(du[j], du[j + 1], tb + (32 + j) * 32, tb + (33 + j) * 32, sb2, sb3, lane);
+            if (lane == 0) {
+              const int f = fc + j;
+              ch_gc[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb0;
+              ch_gc[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb1;
+              ch_uc[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb2;
+              ch_uc[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb3;
+            }
+          }
+          __syncwarp();
+          {
+            const uint4* sg = reinterpret_cast<const uint4*>(tb + lane * 32);
+            uint4* dgc = reinterpret_cast<uint4*>(p.q_col + (f0 + fc + lane) * p.R + T.m0 + q * 32);
+            dgc[0] = sg[0];
+            dgc[1] = sg[1];
+            const uint4* su = reinterpret_cast<const uint4*>(tb + (32 + lane) * 32);
+            uint4* duc = reinterpret_cast<uint4*>(p.q_col + (p.F + f0 + fc + lane) * p.R + T.m0 + q * 32);
+            duc[0] = su[0];
+            duc[1] = su[1];
+          }
+          __syncwarp();
+          uint32_t sbg = row_quant_store_e4m3(dg, p.q_row + row * p.q_cols + f0 + fc);
+          uint32_t sbu = row_quant_store_e4m3(du, p.q_row + row * p.q_cols + p.F + f0 + fc);
+          ch_gr[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbg;
+          ch_ur[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbu;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (!epi_sync()) break;
+        {
+          const int64_t rcp = (p.q_cols / 32 + 3) / 4;   // row-scale chunks per 128-row block
+          const int64_t ccp = (p.R / 32 + 3) / 4;        // column-scale chunks per 128-row block
+          if (ew == 0) store_chunk(p.q_row_scale + ((T.m0 >> 7) * rcp + (f0 >> 7)) * 512, ch_gr, lane);
+          else if (ew == 1) store_chunk(p.q_row_scale + ((T.m0 >> 7) * rcp + ((p.F + f0) >> 7)) * 512, ch_ur, lane);
+          else if (ew == 2) store_chunk(p.q_col_scale + ((f0 >> 7) * ccp + (T.m0 >> 7)) * 512, ch_gc, lane);
+          else if (ew == 3) store_chunk(p.q_col_scale + (((p.F + f0) >> 7) * ccp + (T.m0 >> 7)) * 512, ch_uc, lane);
+        }
+        if (!epi_sync()) break;
+      } else if constexpr (EPI == EPI_GELU || EPI == EPI_DGELU) {
+        // Dense MLP epilogues, accumulator columns [0,128) = output columns
+        // n0..n0+127.  GELU: pre = acc + b1 (saved in BF16), act = gelu(pre);
+        // dGELU: dpre = acc * gelu'(pre from the BF16 save), plus per-column
+        // sums of dpre (the bias gradient).  Both requantize rowwise and
+        // columnwise with optional rotation.
+        constexpr int BB = BlockBytes<QF>::value;
+        const int64_t row = T.m0 + row_in_tile;
+        const int64_t n0 = T.n0;
+        uint8_t* ch_row = sChunk;
+        uint8_t* ch_col = sChunk + 512;
+        float* part = reinterpret_cast<float*>(sChunk + 1024);  // [4 lane quarters][128 columns]
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ch++) {
+          const int fc = half * 64 + ch * 32;
+          uint32_t accr[32];
+          tmem_ld32(tbase + fc, accr);
+          float aux[32];  // GELU: bias; dGELU: saved pre-activation
+          if (EPI == EPI_GELU && p.bias == nullptr) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) aux[j] = 0.f;
+          } else {
+            const uint4* src = EPI == EPI_GELU ? reinterpret_cast<const uint4*>(p.bias + n0 + fc)
+                                               : reinterpret_cast<const uint4*>(p.z + row * p.q_cols + n0 + fc);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const uint4 w = EPI == EPI_GELU ? __ldg(src + i) : src[i];
+              const uint32_t w4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int k = 0; k < 8; k++)
+                aux[i * 8 + k] = bf16_bits_to_float((k & 1) ? (w4[k >> 1] >> 16) : (w4[k >> 1] & 0xFFFFu));
+            }
+          }
+          tmem_wait_ld();
+          float val[32];
+          if constexpr (EPI == EPI_GELU) {
+            float pre[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) pre[j] = __uint_as_float(accr[j]) + aux[j];
+            uint4* zd = reinterpret_cast<uint4*>(p.z + row * p.q_cols + n0 + fc);
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+              zd[c] = make_uint4(float2_to_bf16x2(pre[8 * c], pre[8 * c + 1]), float2_to_bf16x2(pre[8 * c + 2], pre[8 * c + 3]),
+                                 float2_to_bf16x2(pre[8 * c + 4], pre[8 * c + 5]), float2_to_bf16x2(pre[8 * c + 6], pre[8 * c + 7]));
+#pragma unroll
+            for (int j = 0; j < 32; j++) val[j] = gelu_tanh_f(pre[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; j++) val[j] = __uint_as_float(accr[j]) * dgelu_tanh_f(aux[j]);
+#pragma unroll
+            for (int j = 0; j < 32; j++) {  // this warp's 32-row column sums, fixed butterfly order
+              float sum = val[j];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+              if (lane == 0) part[q * 128 + fc + j] = sum;
+            }
+          }
+          // columnwise first (the rowwise packer rotates and scales in place)
+#pragma unroll
+          for (int j = 0; j < 32; j++) {
+            const uint32_t sb = col_quant_one<QF, QH>(val[j], tb + j * 32, lane);
+            if (lane == 0) {
+              const int f = fc + j;
+              ch_col[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb;
+            }
+          }
+          __syncwarp();
+          store_col_codes<QF>(tb + lane * 32, p.q_col + (n0 + fc + lane) * p.q_col_ld + (T.m0 + q * 32) / 32 * BB);
+          __syncwarp();
+          const uint32_t sbr = row_quant_store<QF, QH>(val, p.q_row + row * p.q_row_ld + (n0 + fc) / 32 * BB);
+          ch_row[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbr;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (!epi_sync()) break;
+        if (ew == 0) store_chunk(p.q_row_scale + ((T.m0 >> 7) * ((p.q_cols / 32 + 3) / 4) + (n0 >> 7)) * 512, ch_row, lane);
+        else if (ew == 1) store_chunk(p.q_col_scale + ((n0 >> 7) * ((p.R / 32 + 3) / 4) + (T.m0 >> 7)) * 512, ch_col, lane);
+        if constexpr (EPI == EPI_DGELU) {
+          const int c = ew * 32 + lane - 64;  // warps 2..5 of the epilogue: 128 columns
+          if (c >= 0 && c < 128) {
+            float s4 = part[c];
+            s4 += part[128 + c];
+            s4 += part[256 + c];
+            s4 += part[384 + c];
+            p.colsum_partials[(T.m0 >> 7) * p.q_cols + n0 + c] = s4;
+          }
+        }
+        if (!epi_sync()) break;
+      }
+      if (++acc == C::ACC) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_gemm_status, DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<C::TMEM_COLS>(tmem_base);
+  }
+}
+
+}  // namespace mx

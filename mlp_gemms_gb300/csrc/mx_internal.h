@@ -29,7 +29,7 @@ struct QuantLaunch {
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
 
 enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };
-enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2 };
+enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_GELU = 3, EPI_DGELU = 4 };
 
 // Everything a grouped-GEMM launch needs besides the two tensor maps.
 struct GemmParams {
@@ -51,17 +51,26 @@ struct GemmParams {
   uint16_t* out;            // BF16 [rows, out_ld]
   int64_t out_ld;
   uint16_t* z;              // SwiGLU: BF16 pre-activation save [R, 2F]; dSwiGLU: its input
-  uint8_t* q_row;           // requantized rowwise payload [R, C] (E4M3)
+  uint8_t* q_row;           // requantized rowwise payload [R, C]
   uint8_t* q_row_scale;
-  uint8_t* q_col;           // requantized columnwise payload [C, R] (E4M3)
+  uint8_t* q_col;           // requantized columnwise payload [C, R]
   uint8_t* q_col_scale;
-  int64_t q_cols;           // C: F (SwiGLU) or 2F (dSwiGLU)
+  int64_t q_cols;           // C: F (SwiGLU), 2F (dSwiGLU), H (GELU / dGELU)
+  int64_t q_row_ld, q_col_ld;  // payload bytes per row of q_row / q_col
+  int q_fmt, q_had;         // requant element format and rotation (GELU / dGELU)
+  const uint16_t* bias;     // BF16 [N] added to the fp32 accumulator, or null
+  float* colsum_partials;   // dGELU: fp32 [ceil(R/128), C] per-tile column sums
 };
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, int bn,
                         cudaStream_t s, int num_sms);
+cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                              cudaStream_t s, int num_sms);
+cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s);
 cudaError_t read_gemm_status(unsigned* out);
 cudaError_t reset_gemm_status();
+cudaError_t read_dense_status(unsigned* out);
+cudaError_t reset_dense_status();
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t s);
 
 }  // namespace mx

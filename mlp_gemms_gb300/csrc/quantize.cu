@@ -225,6 +225,11 @@ __global__ void colsum_reduce_kernel(const float* __restrict__ partials, int64_t
   out[c] = s;
 }
 
+cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s) {
+  colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(partials, tiles, cols, out);
+  return cudaGetLastError();
+}
+
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
 static cudaError_t launch_q(const QuantParams& p, int batch, cudaStream_t s) {
   int64_t tiles = (int64_t)p.tiles_x * ((p.rows + QT - 1) / QT);

@@ -480,3 +480,65 @@ def within_tolerance(test, ref):
     rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
     bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * rms
     return np.abs(test - ref) <= bound
+
+
+# --------------------------------------------------------------------------
+# Dense MXFP6 + Hadamard + tanh-GELU MLP (Primus PR #1064)
+# --------------------------------------------------------------------------
+
+def gelu_fwd(x_deq, w1_deq, b1, fmt=E2M3, hadamard=True):
+    """FC1 with bias in the accumulator, BF16 pre-activation save, and the
+    tanh-GELU activation packed rowwise [M, H] and columnwise [H, M]."""
+    pre = np.asarray(x_deq) @ np.asarray(w1_deq).T
+    if b1 is not None:
+        pre = pre + np.asarray(b1, dtype=np.float64)[None, :]
+    act = round_f32(gelu_tanh(round_f32(pre)))
+    return {"pre": pre, "pre_bf16": f64_to_bf16(pre), "act": act,
+            "act_row": quantize_rows(act, fmt, hadamard), "act_col": quantize_cols(act, fmt, hadamard)}
+
+
+def dgelu_bwd(dy_deq, w2t_deq, pre_bf16, fmt=E2M3, hadamard=True):
+    """FC2 dgrad with the dGELU epilogue: dpre = (dY W2) * gelu'(pre) from
+    the BF16-saved pre-activation, packed both ways, plus its column sums."""
+    da = np.asarray(dy_deq) @ np.asarray(w2t_deq).T
+    dpre64 = da * dgelu_tanh(bf16_to_f64(pre_bf16))
+    dpre = round_f32(dpre64)
+    return {"da": da, "dpre": dpre, "db1": colsum(dpre64),
+            "dpre_row": quantize_rows(dpre, fmt, hadamard), "dpre_col": quantize_cols(dpre, fmt, hadamard)}
+
+
+def mlp_fwd_bwd_gelu(x_bits, w1_bits, w2_bits, b1_bits, b2_bits, dy_bits, fmt=E2M3, hadamard=True):
+    """The dense MX GELU MLP step, stage by stage on the oracle's own
+    quantization: x [M, D], w1 [H, D], w2 [D, H], b1 [H], b2 [D], dy [M, D]."""
+    x, dy = bf16_to_f64(x_bits), bf16_to_f64(dy_bits)
+    w1, w2 = bf16_to_f64(w1_bits), bf16_to_f64(w2_bits)
+    b1, b2 = bf16_to_f64(b1_bits), bf16_to_f64(b2_bits)
+    M, D = x.shape
+    H = w1.shape[0]
+    dq = lambda t, rows, cols: dequantize_rows(t[0], t[1], rows, cols, fmt)
+    x_row, x_col = quantize_rows(x, fmt, hadamard), quantize_cols(x, fmt, hadamard)
+    w1_row, w1t_row = quantize_rows(w1, fmt, hadamard), quantize_cols(w1, fmt, hadamard)
+    w2_row, w2t_row = quantize_rows(w2, fmt, hadamard), quantize_cols(w2, fmt, hadamard)
+    fwd = gelu_fwd(dq(x_row, M, D), dq(w1_row, H, D), b1, fmt, hadamard)
+    y = dq(fwd["act_row"], M, H) @ dq(w2_row, D, H).T + b2[None, :]
+    dy_row, dy_col = quantize_rows(dy, fmt, hadamard), quantize_cols(dy, fmt, hadamard)
+    db2 = colsum(dy)
+    bwd = dgelu_bwd(dq(dy_row, M, D), dq(w2t_row, H, D), fwd["pre_bf16"], fmt, hadamard)
+    dx = dq(bwd["dpre_row"], M, H) @ dq(w1t_row, D, H).T
+    dw2 = dq(dy_col, D, M) @ dq(fwd["act_col"], H, M).T
+    dw1 = dq(bwd["dpre_col"], H, M) @ dq(x_col, D, M).T
+    return {"x_row": x_row, "x_col": x_col, "w1_row": w1_row, "w1t_row": w1t_row, "w2_row": w2_row,
+            "w2t_row": w2t_row, "dy_row": dy_row, "dy_col": dy_col, "fwd": fwd, "bwd": bwd,
+            "y_f64": y, "dx_f64": dx, "dw1_f64": dw1, "dw2_f64": dw2, "db1": bwd["db1"], "db2": db2}
+
+
+def mlp_fwd_bwd_gelu_unquantized(x_bits, w1_bits, w2_bits, b1_bits, b2_bits, dy_bits):
+    x, dy = bf16_to_f64(x_bits), bf16_to_f64(dy_bits)
+    w1, w2 = bf16_to_f64(w1_bits), bf16_to_f64(w2_bits)
+    b1, b2 = bf16_to_f64(b1_bits), bf16_to_f64(b2_bits)
+    pre = x @ w1.T + b1[None, :]
+    act = gelu_tanh(pre)
+    y = act @ w2.T + b2[None, :]
+    dpre = (dy @ w2) * dgelu_tanh(pre)
+    return {"pre": pre, "y": y, "dx": dpre @ w1, "dw2": dy.T @ act, "dw1": dpre.T @ x,
+            "db1": dpre.sum(0), "db2": dy.sum(0)}

@@ -113,11 +113,13 @@ def test_grouped_gemm_rejections(mx):
     assert _gemm(mx, _t(256, 256), _t(256, 192))[0] == "MX_ERR_SHAPE"          # K mismatch
     assert _gemm(mx, _t(256, 192), _t(256, 192))[0] == "MX_ERR_SHAPE"          # K % 128
     assert _gemm(mx, _t(256, 256), _t(384, 256), G=2)[0] == "MX_ERR_SHAPE"     # N = 192
-    assert _gemm(mx, _t(256, 256, fmt=1), _t(256, 256, fmt=1))[0] == "MX_ERR_NOT_SUPPORTED"
-    assert _gemm(mx, _t(256, 256, had=1), _t(256, 256, had=1))[0] == "MX_ERR_NOT_SUPPORTED"
+    assert _gemm(mx, _t(256, 256, fmt=1), _t(256, 256, fmt=0))[0] == "MX_ERR_INVALID_ARG"   # mixed formats
+    assert _gemm(mx, _t(256, 256, had=1), _t(256, 256))[0] == "MX_ERR_INVALID_ARG"          # rotation on one side
+    assert _gemm(mx, _t(256, 256, fmt=1, data=FAKE + 16), _t(256, 256, fmt=1))[0] == "MX_ERR_ALIGNMENT"
+    assert _gemm(mx, _t(256, 256, fmt=5), _t(256, 256, fmt=5))[0] == "MX_ERR_INVALID_ARG"
     assert _gemm(mx, _t(256, 256), _t(256, 256), out=MISALIGNED)[0] == "MX_ERR_ALIGNMENT"
     assert _gemm(mx, _t(256, 256), _t(256, 256), ld=100)[0] == "MX_ERR_ALIGNMENT"
-    assert _gemm(mx, _t(256, 256), _t(256, 256), offsets=None)[0] == "MX_ERR_INVALID_ARG"
+    assert _gemm(mx, _t(256, 256), _t(512, 256), G=2, offsets=None)[0] == "MX_ERR_INVALID_ARG"
     assert _gemm(mx, _t(256, 256, data=MISALIGNED), _t(256, 256))[0] == "MX_ERR_ALIGNMENT"
 
 

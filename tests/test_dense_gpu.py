@@ -1,0 +1,112 @@
+"""Dense MXFP6 + Hadamard + tanh-GELU stages against the oracle."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from helpers import assert_quant_equal, bf16_cpu, mx_bytes, requant_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _q(mx, bits, fmt, had, row=True, col=True):
+    r, c, _ = mx.mx_quantize(to_dev(bits), fmt, row, col, had)
+    ref = O.quantize_bf16(bits, fmt, row, col, had)
+    rows, cols = bits.shape
+    if row:
+        assert_quant_equal(r, (ref["row_payload"], ref["row_scales"]), rows, cols // 32, "row")
+    if col:
+        assert_quant_equal(c, (ref["col_payload"], ref["col_scales"]), cols, rows // 32, "col")
+    return r, c, ref
+
+
+def _dq(t, rows, cols, fmt):
+    return O.dequantize_rows(t[0], t[1], rows, cols, fmt)
+
+
+@pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E4M3, False)])
+def test_gemm_bias(cuda_lib, fmt, had):
+    rng = np.random.default_rng(50)
+    M, N, K = 256, 384, 512
+    ab, bb = W.normal_bf16(rng, (M, K)), W.normal_bf16(rng, (N, K), std=0.02)
+    bias = W.normal_bf16(rng, (N,), std=0.02)
+    ar, _, aref = _q(cuda_lib, ab, fmt, had, col=False)
+    br, _, bref = _q(cuda_lib, bb, fmt, had, col=False)
+    out = cuda_lib.mx_gemm_bias(ar, br, to_dev(bias))
+    ref = _dq((aref["row_payload"], aref["row_scales"]), M, K, fmt) @ \
+        _dq((bref["row_payload"], bref["row_scales"]), N, K, fmt).T + O.bf16_to_f64(bias)[None, :]
+    assert O.within_tolerance(bf16_cpu(out), ref).all()
+
+
+@pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E2M3, False), (O.E4M3, True)])
+def test_gelu_fwd(cuda_lib, fmt, had):
+    rng = np.random.default_rng(51)
+    M, D, H = 512, 384, 256
+    xb, w1b = W.normal_bf16(rng, (M, D)), W.normal_bf16(rng, (H, D), std=0.05)
+    b1 = W.normal_bf16(rng, (H,), std=0.02)
+    xr, _, xref = _q(cuda_lib, xb, fmt, had, col=False)
+    wr, _, wref = _q(cuda_lib, w1b, fmt, had, col=False)
+    pre, act_row, act_col = cuda_lib.mx_gemm_gelu_fwd(xr, wr, to_dev(b1), fmt=fmt, hadamard=had)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    ref = O.gelu_fwd(_dq((xref["row_payload"], xref["row_scales"]), M, D, fmt),
+                     _dq((wref["row_payload"], wref["row_scales"]), H, D, fmt), O.bf16_to_f64(b1), fmt, had)
+    assert O.within_tolerance(bf16_cpu(pre), ref["pre"]).all()
+    requant_close(mx_bytes(act_row), ref["act_row"], M, H, fmt)
+    requant_close(mx_bytes(act_col), ref["act_col"], H, M, fmt)
+
+
+@pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E4M3, False)])
+def test_dgelu_bwd(cuda_lib, fmt, had):
+    rng = np.random.default_rng(52)
+    M, D, H = 512, 384, 256
+    dyb = W.normal_bf16(rng, (M, D), std=1e-3)
+    w2t = W.normal_bf16(rng, (H, D), std=0.02)
+    pre = W.normal_bf16(rng, (M, H), std=1.5)
+    dyr, _, dyref = _q(cuda_lib, dyb, fmt, had, col=False)
+    wr, _, wref = _q(cuda_lib, w2t, fmt, had, col=False)
+    dpre_row, dpre_col, db1 = cuda_lib.mx_gemm_dgelu_bwd(dyr, wr, to_dev(pre), fmt=fmt, hadamard=had)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    ref = O.dgelu_bwd(_dq((dyref["row_payload"], dyref["row_scales"]), M, D, fmt),
+                      _dq((wref["row_payload"], wref["row_scales"]), H, D, fmt), pre, fmt, had)
+    requant_close(mx_bytes(dpre_row), ref["dpre_row"], M, H, fmt)
+    requant_close(mx_bytes(dpre_col), ref["dpre_col"], H, M, fmt)
+    got = db1.cpu().numpy().astype(np.float64)
+    assert O.within_tolerance(got[None, :], ref["db1"][None, :]).all()
+
+
+def test_dense_gelu_step_against_oracle_chain(cuda_lib):
+    """The dense MXFP6 + Hadamard tanh-GELU MLP step (fwd + bwd, bias
+    gradients) through mx_mlp_fwd_bwd, against the oracle's stage-wise chain
+    and the unquantized float64 chain (the pages' MXFP6 band is ~28 dB)."""
+    import torch
+    M, D, H = 512, 384, 512
+    inp = W.dense_inputs(M, D, H, seed=3)
+    t = {k: to_dev(v) for k, v in inp.items()}
+    dev = "cuda"
+    out = {"y": torch.empty((M, D), dtype=torch.bfloat16, device=dev),
+           "dx": torch.empty((M, D), dtype=torch.bfloat16, device=dev),
+           "dw1": torch.empty((H, D), dtype=torch.bfloat16, device=dev),
+           "dw2": torch.empty((D, H), dtype=torch.bfloat16, device=dev),
+           "db1": torch.empty(H, dtype=torch.float32, device=dev),
+           "db2": torch.empty(D, dtype=torch.float32, device=dev)}
+    kw = dict(act=cuda_lib.ACT_GELU_TANH, fmt=O.E2M3, hadamard=True, b1=t["b1"], b2=t["b2"], db1=out["db1"],
+              db2=out["db2"])
+    args = cuda_lib.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], None, 1, H, out["y"], out["dx"], out["dw1"],
+                             out["dw2"], **kw)
+    ws = torch.empty(cuda_lib.mx_mlp_workspace_bytes(args), dtype=torch.uint8, device=dev)
+    args = cuda_lib.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], None, 1, H, out["y"], out["dx"], out["dw1"],
+                             out["dw2"], workspace=ws, **kw)
+    cuda_lib.mx_mlp_fwd_bwd(args)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    ref = O.mlp_fwd_bwd_gelu(inp["x"], inp["w1"], inp["w2"], inp["b1"], inp["b2"], inp["dy"])
+    unq = O.mlp_fwd_bwd_gelu_unquantized(inp["x"], inp["w1"], inp["w2"], inp["b1"], inp["b2"], inp["dy"])
+    for k in ("y", "dx", "dw1", "dw2"):
+        g = bf16_cpu(out[k])
+        s_orc, s_unq = O.sqnr_db(ref[k + "_f64"], g), O.sqnr_db(unq[k], g)
+        assert s_orc > 30.0, (k, s_orc)
+        assert s_unq > 16.0, (k, s_unq)
+    for k in ("db1", "db2"):
+        g = out[k].cpu().numpy().astype(np.float64)
+        assert O.sqnr_db(ref[k], g) > 30.0, k
+    assert np.all(np.abs(out["db2"].cpu().numpy() - ref["db2"]) <=
+                  2.0 ** -8 * np.abs(ref["db2"]) + 2.0 ** -14 * np.sqrt(np.mean(ref["db2"] ** 2)))

@@ -11,11 +11,11 @@ from helpers import assert_quant_equal, bf16_cpu, mx_bytes, requant_close, to_de
 pytestmark = pytest.mark.gpu
 
 
-def _quant_both(mx, bits, row=True, col=False):
+def _quant_both(mx, bits, row=True, col=False, fmt=O.E4M3, had=False):
     """GPU and oracle rowwise (and columnwise) quantization; asserts equality."""
     x = to_dev(bits)
-    r, c, _ = mx.mx_quantize(x, O.E4M3, row, col)
-    ref = O.quantize_bf16(bits, O.E4M3, row, col)
+    r, c, _ = mx.mx_quantize(x, fmt, row, col, had)
+    ref = O.quantize_bf16(bits, fmt, row, col, had)
     rows, cols = bits.shape[-2], bits.shape[-1]
     batch = bits.shape[0] if bits.ndim == 3 else 1
     if row:
@@ -27,8 +27,8 @@ def _quant_both(mx, bits, row=True, col=False):
     return r, c, ref
 
 
-def _deq(ref_key_payload, ref_key_scales, rows, cols):
-    return O.dequantize_rows(ref_key_payload.reshape(rows, -1), ref_key_scales.reshape(-1), rows, cols, O.E4M3)
+def _deq(ref_key_payload, ref_key_scales, rows, cols, fmt=O.E4M3):
+    return O.dequantize_rows(ref_key_payload.reshape(rows, -1), ref_key_scales.reshape(-1), rows, cols, fmt)
 
 
 def _offsets(counts):
@@ -74,6 +74,32 @@ def test_grouped_gemm_ragged(cuda_lib, N):
     A = int(offsets[-1])
     assert O.within_tolerance(got[:A], ref[:A]).all()
     assert np.all(np.isnan(got[A:])), "inactive tail rows were written"
+
+
+@pytest.mark.parametrize("fmt", [O.E2M3, O.E2M1])
+@pytest.mark.parametrize("had", [False, True])
+def test_grouped_gemm_packed_formats(cuda_lib, fmt, had):
+    """E2M3 / E2M1 operands (packed payload, expanded by the tensor-map
+    types) with and without the 32-point rotation along K."""
+    import torch
+    G, K, N, R = 2, 768, 256, 512
+    offsets = _offsets([256, 256])
+    rng = np.random.default_rng(40 + fmt)
+    ab = W.normal_bf16(rng, (R, K))
+    bb = W.normal_bf16(rng, (G, N, K), std=0.02)
+    ar, _, aref = _quant_both(cuda_lib, ab, fmt=fmt, had=had)
+    br, _, bref = _quant_both(cuda_lib, bb, fmt=fmt, had=had)
+    out = cuda_lib.mx_grouped_gemm(ar, br, G, torch.from_numpy(offsets).cuda())
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    a = _deq(aref["row_payload"], aref["row_scales"], R, K, fmt)
+    b = _deq(bref["row_payload"], bref["row_scales"], G * N, K, fmt).reshape(G, N, K)
+    ref = O.grouped_gemm(a, b, offsets)
+    got = bf16_cpu(out)
+    assert O.within_tolerance(got, ref).all()
+    if had:
+        # the rotation cancels in the product: compare with the unrotated one
+        plain = O.grouped_gemm(O.bf16_to_f64(ab), O.bf16_to_f64(bb), offsets)
+        assert O.sqnr_db(plain, got) > (20.0 if fmt == O.E2M3 else 10.0)
 
 
 def test_wgrad_ragged_with_zero_token_expert(cuda_lib):
