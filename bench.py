@@ -144,14 +144,13 @@ def barrier(world):
 # CPU oracle baseline (bounded sample)
 # --------------------------------------------------------------------------
 
-def oracle_sample(seconds_hint=20.0):
+def oracle_sample(seconds_hint=20.0, rows=2048):
     """Time the CPU oracle's full MLP chain on a bounded sample of the
     workload: experts of the even-routing layout (2048 rows each, D=2048,
     F=768), as many as fit in ~seconds_hint.  Returns (TFLOP/s, desc, cores)."""
     import oracle as O
     import workloads as W
     D, F = SHAPE["D"], SHAPE["F"]
-    rows = 2048
     done_flops, t_total, n = 0.0, 0.0, 0
     while n == 0 or (t_total < seconds_hint and n < 8):
         inp = W.moe_inputs(1, D, F, rows, seed=n)
@@ -172,12 +171,13 @@ def run_reference(args):
     if rank != 0:
         return
     tflops = []
+    # each step: one expert's 512 routed rows through the whole chain (~1 s)
     for _ in range(args.warmup):
-        oracle_sample(seconds_hint=2.0)
+        oracle_sample(seconds_hint=0.0, rows=512)
     desc, cores = "", 0
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, desc, cores = oracle_sample(seconds_hint=5.0)
+        v, desc, cores = oracle_sample(seconds_hint=0.0, rows=512)
         tflops.append(v)
     wall = time.perf_counter() - t0
     value = float(np.mean(tflops))
@@ -426,6 +426,47 @@ def quantizer_rate(mx, torch, dev):
             "l2": "flushed (512 MB write) between iterations"}
 
 
+def ncu_case(name, launches=3):
+    """A small single-kernel case for profiler captures: the named stage on a
+    reduced MoE shape (G=32, R=65536, D=2048, F=768: operands larger than L2,
+    under 1.5 GB on the device), launched `launches` times after one warm-up.
+    'quant' is the standalone quantizer workload (8192 x 7168)."""
+    import torch
+    import mlp_gemms_gb300 as mx
+    import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    mx.load()
+    if name == "quant":
+        x = torch.randn((8192, 7168), device=dev).to(torch.bfloat16)
+        r, c = mx.MX(8192, 7168), mx.MX(7168, 8192)
+        run = lambda: mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+    else:
+        G, D, F, R = 32, 2048, 768, 65536
+        offs = torch.from_numpy(W.even_offsets(G, R)).to(dev)
+        inp = W.moe_inputs_device(G, D, F, R, device=dev)
+        xr, xc, _ = mx.mx_quantize(inp["x"], 0, True, True)
+        w1r, w1t, _ = mx.mx_quantize(inp["w1"], 0, True, True)
+        w2r, w2t, _ = mx.mx_quantize(inp["w2"], 0, True, True)
+        dyr, dyc, _ = mx.mx_quantize(inp["dy"], 0, True, True)
+        z, hr, hc = mx.mx_grouped_gemm_swiglu_fwd(xr, w1r, G, offs)
+        dzr, dzc = mx.mx_grouped_gemm_dswiglu_bwd(dyr, w2t, z, G, offs)
+        y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+        dw1 = torch.empty((G, 2 * F, D), dtype=torch.bfloat16, device=dev)
+        dw2 = torch.empty((G, D, F), dtype=torch.bfloat16, device=dev)
+        run = {"fc1_swiglu": lambda: mx.mx_grouped_gemm_swiglu_fwd(xr, w1r, G, offs, hr, hc, z),
+               "fc2": lambda: mx.mx_grouped_gemm(hr, w2r, G, offs, out=y),
+               "fc2_dgrad_dswiglu": lambda: mx.mx_grouped_gemm_dswiglu_bwd(dyr, w2t, z, G, offs, dzr, dzc),
+               "fc1_dgrad": lambda: mx.mx_grouped_gemm(dzr, w1t, G, offs, out=y),
+               "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad(dyc, hc, G, offs, out=dw2),
+               "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad(dzc, xc, G, offs, out=dw1)}[name]
+    torch.cuda.synchronize(dev)
+    for _ in range(1 + launches):
+        run()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"ncu_case": name, "launches": launches, "status": mx.mx_get_device_status()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -434,7 +475,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", default=None, help="run one small single-kernel case for a profiler capture")
     args = ap.parse_args()
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

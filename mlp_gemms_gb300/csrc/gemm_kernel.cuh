@@ -52,11 +52,12 @@ struct Cfg {
   static constexpr int SF_BYTES = 512 + (BN / 128) * 512;
   static constexpr int SF_COLS = 4 + 4 * (BN / 128);
   static constexpr uint32_t TX = A_BYTES + B_BYTES + SF_BYTES;
+  static constexpr int TB_BYTES = 2304;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_TB = OFF_SF + STAGES * SF_BYTES;  // 8 x 2 KB transpose buffers
-  static constexpr int OFF_CHUNK = OFF_TB + 8 * 2048;        // scale chunks + column-sum partials
+  static constexpr int OFF_TB = OFF_SF + STAGES * SF_BYTES;  // 8 x [32][17] fp32 transpose buffers
+  static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
   static constexpr int OFF_BAR = OFF_CHUNK + 4096;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -141,22 +142,6 @@ __device__ __forceinline__ uint32_t row_quant_store_e4m3(float (&v)[32], uint8_t
   return sb;
 }
 
-// Columnwise E4M3 requant of two columns whose 32-row block is spread over
-// the warp's lanes (lane = row): warp-wide integer max of |bits| gives each
-// column's amax; both codes go to the transpose buffer tb[col][lane].
-__device__ __forceinline__ void col_quant_pair_e4m3(float v0, float v1, uint8_t* tb_col0, uint8_t* tb_col1,
-                                                    uint32_t& sb0, uint32_t& sb1, int lane) {
-  uint32_t a0 = __reduce_max_sync(0xffffffffu, __float_as_uint(v0) & 0x7FFFFFFFu);
-  uint32_t a1 = __reduce_max_sync(0xffffffffu, __float_as_uint(v1) & 0x7FFFFFFFu);
-  sb0 = rceil_scale_byte<E4M3>(a0);
-  sb1 = rceil_scale_byte<E4M3>(a1);
-  uint32_t c = cvt_e4m3x2(v0 * inv_scale_from_byte(sb0), v1 * inv_scale_from_byte(sb1));
-  uint32_t c0 = sb0 == 0xFFu ? 0x7Fu : (c & 0xFFu);
-  uint32_t c1 = sb1 == 0xFFu ? 0x7Fu : (c >> 8);
-  tb_col0[lane] = (uint8_t)c0;
-  tb_col1[lane] = (uint8_t)c1;
-}
-
 __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint8_t* chunk, int lane) {
   reinterpret_cast<uint4*>(dst)[lane] = reinterpret_cast<const uint4*>(chunk)[lane];
 }
@@ -201,67 +186,89 @@ __device__ __forceinline__ uint32_t row_quant_store(float (&v)[32], uint8_t* dst
   return sb;
 }
 
-// Columnwise requant of one column whose 32-row block is spread over the
-// warp (lane = row): optional rotation across the lanes (the same five
-// butterfly stages, partner lane = lane ^ stride), warp-wide amax, and this
-// lane's code into the transpose buffer.  Returns the block's scale byte.
+// Columnwise requant of 16 columns whose 32-row blocks are spread over the
+// warp (lane = row; v = this lane's values of the 16 columns).  The warp
+// transposes them through a padded [32][17] fp32 buffer; lane pair (2c, 2c+1)
+// then owns column c, rows 0..15 and 16..31: optional rotation (stages 1..8
+// inside each lane, stage 16 across the pair), amax over the pair, scale,
+// and 16 packed codes per lane stored straight to the transposed payload.
+// dst(c) is the payload row of column c at this warp's 32-row block;
+// returns nothing, writes column c's scale byte to chunk[(f&31)*16+(f>>5)*4+q]
+// for f = f_local0 + c.
 template <int QF, bool QH>
-__device__ __forceinline__ uint32_t col_quant_one(float v, uint8_t* tb_col, int lane) {
+__device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane, uint8_t* q_col, int64_t col_ld,
+                                            int64_t col0, int64_t row_byte0, uint8_t* chunk, int f_local0, int q) {
+#pragma unroll
+  for (int c = 0; c < 16; c++) buf[lane * 17 + c] = v[c];
+  __syncwarp();
+  const int c = lane >> 1, hh = lane & 1;
+  float x[16];
+#pragma unroll
+  for (int i = 0; i < 16; i++) x[i] = buf[(hh * 16 + i) * 17 + c];
+  __syncwarp();
   if constexpr (QH) {
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v, h);
-      v = (lane & h) ? __fsub_rn(o, v) : __fadd_rn(v, o);
-    }
-    v = __fmul_rn(v, __uint_as_float(0x3E3504F3u));
-  }
-  const uint32_t a = __reduce_max_sync(0xffffffffu, __float_as_uint(v) & 0x7FFFFFFFu);
-  const uint32_t sb = rceil_scale_byte<QF>(a);
-  uint32_t code;
-  if (sb == 0xFFu) {
-    code = QF == E4M3 ? 0x7Fu : 0u;
-  } else {
-    const float sv = v * inv_scale_from_byte(sb);
-    if constexpr (QF == E4M3) code = cvt_e4m3x2(sv, 0.f) & 0xFFu;
-    else if constexpr (QF == E2M3) code = cvt_e2m3x2(sv, 0.f) & 0x3Fu;
-    else code = cvt_e2m1x2(sv, 0.f) & 0xFu;
-  }
-  tb_col[lane] = (uint8_t)code;
-  return sb;
-}
-
-// Pack the 32 one-byte codes of a column block (shared memory) into the
-// payload format and store them.
-template <int QF>
-__device__ __forceinline__ void store_col_codes(const uint8_t* codes, uint8_t* dst) {
-  const uint4 a = reinterpret_cast<const uint4*>(codes)[0];
-  const uint4 b = reinterpret_cast<const uint4*>(codes)[1];
-  if constexpr (QF == E4M3) {
-    reinterpret_cast<uint4*>(dst)[0] = a;
-    reinterpret_cast<uint4*>(dst)[1] = b;
-  } else {
-    const uint32_t cw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};  // 4 codes per word
-    if constexpr (QF == E2M3) {
-      uint32_t g[8];
+    for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
-      for (int i = 0; i < 8; i++)
-        g[i] = (cw[i] & 0x3Fu) | (((cw[i] >> 8) & 0x3Fu) << 6) | (((cw[i] >> 16) & 0x3Fu) << 12) |
-               (((cw[i] >> 24) & 0x3Fu) << 18);
-      uint2* d = reinterpret_cast<uint2*>(dst);
-      d[0] = make_uint2(g[0] | (g[1] << 24), (g[1] >> 8) | (g[2] << 16));
-      d[1] = make_uint2((g[2] >> 16) | (g[3] << 8), g[4] | (g[5] << 24));
-      d[2] = make_uint2((g[5] >> 8) | (g[6] << 16), (g[6] >> 16) | (g[7] << 8));
-    } else {
+      for (int i = 0; i < 16; i++) {
+        if (i & h) continue;
+        const float a = x[i], b = x[i + h];
+        x[i] = __fadd_rn(a, b);
+        x[i + h] = __fsub_rn(a, b);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
+      x[i] = hh ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; i++) x[i] = __fmul_rn(x[i], __uint_as_float(0x3E3504F3u));
+  }
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 16; i++) amax = max(amax, __float_as_uint(x[i]) & 0x7FFFFFFFu);
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const uint32_t sb = rceil_scale_byte<QF>(amax);
+  uint8_t* dst = q_col + (col0 + c) * col_ld + row_byte0 + hh * (BlockBytes<QF>::value / 2);
+  if (sb == 0xFFu) {
+    const uint32_t nw = nan_block_word<QF>();
+    if constexpr (QF == E4M3) reinterpret_cast<uint4*>(dst)[0] = make_uint4(nw, nw, nw, nw);
+    else if constexpr (QF == E2M1) reinterpret_cast<uint2*>(dst)[0] = make_uint2(nw, nw);
+    else { uint32_t* d = reinterpret_cast<uint32_t*>(dst); d[0] = nw; d[1] = nw; d[2] = nw; }
+  } else {
+    const float s = inv_scale_from_byte(sb);
+#pragma unroll
+    for (int i = 0; i < 16; i++) x[i] = x[i] * s;
+    if constexpr (QF == E4M3) {
       uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const uint32_t lo = cw[2 * i], hi = cw[2 * i + 1];
-        w[i] = (lo & 0xFu) | ((lo >> 4) & 0xF0u) | ((lo >> 8) & 0xF00u) | ((lo >> 12) & 0xF000u) |
-               ((hi & 0xFu) << 16) | (((hi >> 8) & 0xFu) << 20) | (((hi >> 16) & 0xFu) << 24) |
-               (((hi >> 24) & 0xFu) << 28);
-      }
+      for (int i = 0; i < 4; i++)
+        w[i] = cvt_e4m3x2(x[4 * i], x[4 * i + 1]) | (cvt_e4m3x2(x[4 * i + 2], x[4 * i + 3]) << 16);
       reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (QF == E2M1) {
+      uint32_t w[2];
+#pragma unroll
+      for (int i = 0; i < 2; i++)
+        w[i] = cvt_e2m1x2(x[8 * i], x[8 * i + 1]) | (cvt_e2m1x2(x[8 * i + 2], x[8 * i + 3]) << 8) |
+               (cvt_e2m1x2(x[8 * i + 4], x[8 * i + 5]) << 16) | (cvt_e2m1x2(x[8 * i + 6], x[8 * i + 7]) << 24);
+      reinterpret_cast<uint2*>(dst)[0] = make_uint2(w[0], w[1]);
+    } else {
+      uint32_t g[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        const uint32_t p0 = cvt_e2m3x2(x[4 * i], x[4 * i + 1]), p1 = cvt_e2m3x2(x[4 * i + 2], x[4 * i + 3]);
+        g[i] = (p0 & 0x3Fu) | (((p0 >> 8) & 0x3Fu) << 6) | ((p1 & 0x3Fu) << 12) | (((p1 >> 8) & 0x3Fu) << 18);
+      }
+      uint32_t* d = reinterpret_cast<uint32_t*>(dst);
+      d[0] = g[0] | (g[1] << 24);
+      d[1] = (g[1] >> 8) | (g[2] << 16);
+      d[2] = (g[2] >> 16) | (g[3] << 8);
     }
+  }
+  if (hh == 0) {
+    const int f = f_local0 + c;
+    chunk[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb;
   }
 }
 
@@ -402,7 +409,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int ew = warp - 2;       // 0..7
     const int q = warp & 3;        // tensor-memory lane quarter
     const int half = ew >> 2;      // column half
-    uint8_t* tb = sTB + ew * 2048;
+    float* tb = reinterpret_cast<float*>(sTB + ew * C::TB_BYTES);
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t epi_phase = 0;
@@ -536,25 +543,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 2; i++) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int col = i * 32 + j;  // 0..63 within this thread's half
-            uint32_t sb0, sb1;
-            col_quant_pair_e4m3(h[i][j], h[i][j + 1], tb + col * 32, tb + (col + 1) * 32, sb0, sb1, lane);
-            if (lane == 0) {
-              const int f = half * 64 + col;
-              chunk_col[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb0;
-              chunk_col[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb1;
-            }
+          for (int k = 0; k < 2; k++) {
+            const int fl = half * 64 + 32 * i + 16 * k;
+            col_quant16<E4M3, false>(&h[i][16 * k], tb, lane, p.q_col, p.R, f0 + fl, T.m0 + q * 32, chunk_col, fl, q);
           }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 2; k++) {
-          const int col = lane + 32 * k;
-          const uint4* s = reinterpret_cast<const uint4*>(tb + col * 32);
-          uint4* d = reinterpret_cast<uint4*>(p.q_col + (f0 + half * 64 + col) * p.R + T.m0 + q * 32);
-          d[0] = s[0];
-          d[1] = s[1];
         }
         if (!epi_sync()) break;
         if (ew == 0) {
@@ -603,30 +595,12 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           // columnwise first (the rowwise packer scales its input in place)
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            uint32_t sb0, sb1, sb2, sb3;
-            col_quant_pair_e4m3(dg[j], dg[j + 1], tb + j * 32, tb + (j + 1) * 32, sb0, sb1, lane);
-            col_quant_pair_e4m3(du[j], du[j + 1], tb + (32 + j) * 32, tb + (33 + j) * 32, sb2, sb3, lane);
-            if (lane == 0) {
-              const int f = fc + j;
-              ch_gc[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb0;
-              ch_gc[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb1;
-              ch_uc[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb2;
-              ch_uc[((f + 1) & 31) * 16 + ((f + 1) >> 5) * 4 + q] = (uint8_t)sb3;
-            }
+          for (int k = 0; k < 2; k++) {
+            col_quant16<E4M3, false>(&dg[16 * k], tb, lane, p.q_col, p.R, f0 + fc + 16 * k, T.m0 + q * 32, ch_gc,
+                                     fc + 16 * k, q);
+            col_quant16<E4M3, false>(&du[16 * k], tb, lane, p.q_col, p.R, p.F + f0 + fc + 16 * k, T.m0 + q * 32,
+                                     ch_uc, fc + 16 * k, q);
           }
-          __syncwarp();
-          {
-            const uint4* sg = reinterpret_cast<const uint4*>(tb + lane * 32);
-            uint4* dgc = reinterpret_cast<uint4*>(p.q_col + (f0 + fc + lane) * p.R + T.m0 + q * 32);
-            dgc[0] = sg[0];
-            dgc[1] = sg[1];
-            const uint4* su = reinterpret_cast<const uint4*>(tb + (32 + lane) * 32);
-            uint4* duc = reinterpret_cast<uint4*>(p.q_col + (p.F + f0 + fc + lane) * p.R + T.m0 + q * 32);
-            duc[0] = su[0];
-            duc[1] = su[1];
-          }
-          __syncwarp();
           uint32_t sbg = row_quant_store_e4m3(dg, p.q_row + row * p.q_cols + f0 + fc);
           uint32_t sbu = row_quant_store_e4m3(du, p.q_row + row * p.q_cols + p.F + f0 + fc);
           ch_gr[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbg;
@@ -704,16 +678,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           // columnwise first (the rowwise packer rotates and scales in place)
 #pragma unroll
-          for (int j = 0; j < 32; j++) {
-            const uint32_t sb = col_quant_one<QF, QH>(val[j], tb + j * 32, lane);
-            if (lane == 0) {
-              const int f = fc + j;
-              ch_col[(f & 31) * 16 + (f >> 5) * 4 + q] = (uint8_t)sb;
-            }
-          }
-          __syncwarp();
-          store_col_codes<QF>(tb + lane * 32, p.q_col + (n0 + fc + lane) * p.q_col_ld + (T.m0 + q * 32) / 32 * BB);
-          __syncwarp();
+          for (int k = 0; k < 2; k++)
+            col_quant16<QF, QH>(&val[16 * k], tb, lane, p.q_col, p.q_col_ld, n0 + fc + 16 * k,
+                                (T.m0 + q * 32) / 32 * BB, ch_col, fc + 16 * k, q);
           const uint32_t sbr = row_quant_store<QF, QH>(val, p.q_row + row * p.q_row_ld + (n0 + fc) / 32 * BB);
           ch_row[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbr;
         }

@@ -54,3 +54,5 @@ def test_reference_arm_sample_is_bounded():
     import bench
     v, desc, cores = bench.oracle_sample(seconds_hint=0.0)
     assert v > 0 and cores >= 1 and "2048 rows" in desc
+    v, desc, cores = bench.oracle_sample(seconds_hint=0.0, rows=512)
+    assert "512 rows" in desc
