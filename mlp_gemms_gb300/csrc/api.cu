@@ -190,8 +190,17 @@ mx_status_t check_offsets(const int32_t* offsets, int32_t G, int64_t R, cudaStre
   return MX_OK;
 }
 
-mx_status_t run_gemm(const mx::GemmParams& p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
+// Bytes one pipeline stage completes on its barrier: the A box (128 rows),
+// the B boxes (bn rows) and the scale chunks.  For the packed sub-byte types
+// the tensor copy counts the packed data, 128 elements a row.
+uint32_t stage_tx_bytes(int fmt, int bn) {
+  const uint32_t row = (uint32_t)mx::payload_row_bytes(128, fmt);
+  return (128u + (uint32_t)bn) * row + 512u + (uint32_t)(bn / 128) * 512u;
+}
+
+mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
                      const DevInfo& dev) {
+  p.tx_bytes = stage_tx_bytes(a->fmt, bn);
   CUtensorMap ta, tb;
   mx_status_t st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt);
   if (st != MX_OK) return st;
@@ -313,7 +322,8 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   MX_CHECK(b->rows % G == 0, MX_ERR_SHAPE, "b has %lld rows, not a multiple of G = %d", (long long)b->rows, G);
   const int64_t N = b->rows / G;
   MX_CHECK(N > 0 && N % 128 == 0, MX_ERR_SHAPE, "N = %lld per expert is not a positive multiple of 128", (long long)N);
-  MX_CHECK(out_bf16 != nullptr && aligned16(out_bf16), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
+  MX_CHECK(R == 0 || (out_bf16 != nullptr && aligned16(out_bf16)), MX_ERR_ALIGNMENT,
+           "out must be a 16-byte aligned pointer");
   MX_CHECK(ld_out >= N && ld_out % 8 == 0, MX_ERR_ALIGNMENT, "ld_out = %lld must be >= N and a multiple of 8",
            (long long)ld_out);
   MX_CHECK(R * ld_out < (1ll << 40), MX_ERR_SHAPE, "output too large");
@@ -555,6 +565,7 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
   p.q_had = q_row->hadamard ? 1 : 0;
   p.bias = static_cast<const uint16_t*>(bias_bf16);
   p.colsum_partials = partials;
+  p.tx_bytes = stage_tx_bytes(a->fmt, 128);
   CUtensorMap ta, tb;
   if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;

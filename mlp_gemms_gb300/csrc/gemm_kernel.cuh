@@ -339,7 +339,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int kb = 0; kb < T.nk; kb++) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], C::TX);
+          mbar_arrive_expect_tx(&full[stage], p.tx_bytes);
           armed_parity[stage] = (int)phase;
           const int64_t kc = T.kbeg / 128 + kb;
           const int kx = (int)(kc * 128);

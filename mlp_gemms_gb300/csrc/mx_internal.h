@@ -42,6 +42,7 @@ struct GemmParams {
   int64_t Mw;               // rows of A (wgrad)
   int64_t F;                // SwiGLU FFN width (FC1 out = 2F)
   int a_type, b_type;       // MMA element types (E4M3 = 0, E2M3 = 3, E2M1 = 5)
+  uint32_t tx_bytes;        // bytes one pipeline stage's copies complete on its barrier
   const uint8_t* sfa;
   const uint8_t* sfb;
   int64_t sfa_kchunks, sfb_kchunks;  // 512-byte chunks per 128-row block
