@@ -116,6 +116,22 @@ mx_status_t make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t k,
   return MX_OK;
 }
 
+// BF16 input [rows, cols] with row stride ld elements, box 64 columns x 128
+// rows (two boxes per 128x128 quantizer tile), 128-byte swizzle.
+mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (input) failed (%d)", (int)r);
+  return MX_OK;
+}
+
 // tcgen05 .kind::mxf8f6f4 element type code of an MX format.
 int mma_type(int fmt) { return fmt == MX_E4M3 ? 0 : (fmt == MX_E2M3 ? 3 : 5); }
 
@@ -272,7 +288,7 @@ mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t
            (long long)ld);
   MX_CHECK(rows == 0 || x_bf16 != nullptr, MX_ERR_INVALID_ARG, "x is NULL");
   MX_CHECK(aligned16(x_bf16), MX_ERR_ALIGNMENT, "x must be 16-byte aligned");
-  MX_CHECK(rows * ld * batch < (1ll << 40), MX_ERR_SHAPE, "input too large");
+  MX_CHECK(rows * ld * batch < (1ll << 40) && rows * batch < (1ll << 31), MX_ERR_SHAPE, "input too large");
   const int had = (flags & MX_HADAMARD) ? 1 : 0;
   mx_status_t st;
   if (flags & MX_ROWWISE) {
@@ -303,6 +319,8 @@ mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t
   q.col_scale = (flags & MX_COLWISE) ? out_col->scale : nullptr;
   q.colsum_partials = (flags & MX_COLSUM) ? static_cast<float*>(workspace) : nullptr;
   q.colsum = colsum;
+  q.num_sms = dev.sms;
+  if ((st = make_tmap_bf16(&q.xmap, x_bf16, batch * rows, cols, ld)) != MX_OK) return st;
   cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return MX_OK;
@@ -765,12 +783,14 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned word = 0, dense = 0;
-  if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess)
+  unsigned word = 0, dense = 0, quant = 0;
+  if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess ||
+      (e = mx::read_quant_status(&quant)) != cudaSuccess)
     return cuda_fail(e, "reading device status");
-  if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess)
+  if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess ||
+      (e = mx::reset_quant_status()) != cudaSuccess)
     return cuda_fail(e, "clearing device status");
-  word |= dense;
+  word |= dense | quant;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
   return MX_OK;

@@ -25,8 +25,12 @@ struct QuantLaunch {
   uint8_t* col_scale;
   float* colsum_partials;  // null: no column sums
   float* colsum;
+  CUtensorMap xmap;        // BF16 [batch*rows, cols], box 64 x 128, 128-byte swizzle
+  int num_sms;
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
+cudaError_t read_quant_status(unsigned* out);
+cudaError_t reset_quant_status();
 
 enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };
 enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_GELU = 3, EPI_DGELU = 4 };

@@ -28,6 +28,8 @@
 
 namespace mx {
 
+__device__ unsigned g_quant_status = 0;
+
 struct QuantParams {
   const uint16_t* x;
   int64_t rows, cols, ld, x_batch_stride;  // elements
@@ -39,10 +41,10 @@ struct QuantParams {
   int64_t col_ld, col_batch_stride, col_scale_batch_stride;  // bytes
   float* colsum_partials;  // [ceil(rows/128), cols] or null
   int tiles_x;             // ceil(cols / 128)
+  int batch;
 };
 
 constexpr int QT = 128;          // tile edge
-constexpr int QPAD = QT + 8;     // smem row pitch in bf16 (272 bytes)
 
 // NaN-propagating amax of 32 BF16 values given as 16 packed pairs: integer
 // max of |bits| (a NaN pattern is larger than every other pattern).
@@ -82,136 +84,184 @@ __device__ __forceinline__ uint32_t quantize32(float (&v)[32], uint32_t amax_bit
   return sb;
 }
 
+// Byte offset of BF16 element (r, c) of a 128x128 tile held as two
+// 128-byte-swizzled TMA boxes of 64 columns: the 16-byte chunk index within
+// each 128-byte row is XORed with (r % 8), so both the row-major 16-byte
+// reads (8 consecutive rows) and the word reads along one row are free of
+// bank conflicts.
+__device__ __forceinline__ uint32_t tile_off(int r, int c) {
+  const int byte = (c & 63) * 2;
+  return (uint32_t)((c >> 6) * 16384 + r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
+}
+
+constexpr int Q_STAGE = 32768;                 // one BF16 tile
+constexpr int Q_SMEM = 2 * Q_STAGE + 2048 + 4096 + 64 + 1024;
+
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
-__global__ void __launch_bounds__(256) quantize_kernel(const QuantParams p) {
-  __shared__ __align__(16) uint16_t tile[QT * QPAD];
-  __shared__ __align__(16) uint8_t sc_row[512];
-  __shared__ __align__(16) uint8_t sc_col[512];
-  __shared__ float part[4][QT];
+__global__ void __launch_bounds__(256, 2)
+quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
+  extern __shared__ uint8_t qsm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sc_all = sm + 2 * Q_STAGE;                                  // [2 parity][row, col][512]
+  float* part_all = reinterpret_cast<float*>(sm + 2 * Q_STAGE + 2048);  // [2 parity][4][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + 2 * Q_STAGE + 2048 + 4096);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.y;
-  const int tx = blockIdx.x % p.tiles_x, ty = blockIdx.x / p.tiles_x;
-  const int64_t r0 = (int64_t)ty * QT, c0 = (int64_t)tx * QT;
-  const int vrows = (int)((p.rows - r0) < QT ? (p.rows - r0) : QT);
-  const int vcols = (int)((p.cols - c0) < QT ? (p.cols - c0) : QT);
-  const uint16_t* xb = p.x + (int64_t)b * p.x_batch_stride;
+  const int64_t tiles_y = (p.rows + QT - 1) / QT;
+  const int64_t per_batch = tiles_y * p.tiles_x;
+  const int64_t total = per_batch * p.batch;
+  const uint64_t budget = 2000000000ull;
 
-  // ---- stage the tile: 16 threads cover one 256-byte row ----
-  {
-    uint4 v[8];
-    const int chunk = tid & 15;
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      int r = i * 16 + (tid >> 4);
-      if (r < vrows && chunk * 8 < vcols) {
-        const uint4* src = reinterpret_cast<const uint4*>(xb + (r0 + r) * p.ld + c0 + chunk * 8);
-        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w) : "l"(src));
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-      int r = i * 16 + (tid >> 4);
-      if (r < vrows && chunk * 8 < vcols) *reinterpret_cast<uint4*>(&tile[r * QPAD + chunk * 8]) = v[i];
-    }
-    for (int i = tid; i < 512 / 4; i += 256) {
-      reinterpret_cast<uint32_t*>(sc_row)[i] = 0u;
-      reinterpret_cast<uint32_t*>(sc_col)[i] = 0u;
-    }
-    if (COLSUM) for (int i = tid; i < 4 * QT; i += 256) (&part[0][0])[i] = 0.f;
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
   }
   __syncthreads();
 
-  // ---- rowwise: blocks of 32 columns ----
-  if constexpr (ROW) {
-    const int r = (warp & 3) * 32 + lane;
+  // tile t -> (batch entry, row base, column base)
+  auto coords = [&](int64_t t, int& b, int64_t& r0, int64_t& c0) {
+    b = (int)(t / per_batch);
+    const int64_t rem = t % per_batch;
+    r0 = (rem / p.tiles_x) * QT;
+    c0 = (rem % p.tiles_x) * QT;
+  };
+  auto issue = [&](int64_t t, int s) {  // thread 0: both 64-column boxes of tile t
+    int b;
+    int64_t r0, c0;
+    coords(t, b, r0, c0);
+    const int gy = (int)(b * p.rows + r0);
+    mbar_arrive_expect_tx(&full[s], Q_STAGE);
+    const uint64_t pol = l2_policy_evict_first();
+    tma_load_2d(sm + s * Q_STAGE, &xmap, (int)c0, gy, &full[s], pol);
+    tma_load_2d(sm + s * Q_STAGE + 16384, &xmap, (int)c0 + 64, gy, &full[s], pol);
+  };
+  if (tid == 0) {
+    if (blockIdx.x < total) issue(blockIdx.x, 0);
+    if (blockIdx.x + gridDim.x < total) issue(blockIdx.x + gridDim.x, 1);
+  }
+
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < total; t += gridDim.x, it++) {
+    const int s = it & 1;
+    if (!mbar_wait_bounded(&full[s], (uint32_t)((it >> 1) & 1), abort_flag, budget)) break;
+    int b;
+    int64_t r0, c0;
+    coords(t, b, r0, c0);
+    const int vrows = (int)((p.rows - r0) < QT ? (p.rows - r0) : QT);
+    const int vcols = (int)((p.cols - c0) < QT ? (p.cols - c0) : QT);
+    const uint8_t* tile = sm + s * Q_STAGE;
+    uint8_t* sc_row = sc_all + s * 1024;
+    uint8_t* sc_col = sc_row + 512;
+    float* part = part_all + s * 512;
+
+    // ---- rowwise: blocks of 32 columns (every chunk slot gets written) ----
+    if constexpr (ROW) {
+      const int r = (warp & 3) * 32 + lane;
 #pragma unroll 1
-    for (int j = 0; j < 2; j++) {
-      const int cb = (warp >> 2) * 2 + j;
-      if (r < vrows && cb * 32 < vcols) {
-        uint32_t wv[16];
-        const uint4* s = reinterpret_cast<const uint4*>(&tile[r * QPAD + cb * 32]);
+      for (int j = 0; j < 2; j++) {
+        const int cb = (warp >> 2) * 2 + j;
+        uint32_t sb = 0;
+        if (r < vrows && cb * 32 < vcols) {
+          uint32_t wv[16];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          uint4 q = s[i];
-          wv[4 * i] = q.x; wv[4 * i + 1] = q.y; wv[4 * i + 2] = q.z; wv[4 * i + 3] = q.w;
-        }
-        uint32_t m2 = amax_bf16_pairs(wv, 16);
-        uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16) << 16;
-        float v[32];
+          for (int k = 0; k < 4; k++) {
+            const uint4 q = *reinterpret_cast<const uint4*>(tile + tile_off(r, cb * 32 + 8 * k));
+            wv[4 * k] = q.x; wv[4 * k + 1] = q.y; wv[4 * k + 2] = q.z; wv[4 * k + 3] = q.w;
+          }
+          const uint32_t m2 = amax_bf16_pairs(wv, 16);
+          const uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+          float v[32];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          v[2 * i] = bf16_bits_to_float(wv[i] & 0xFFFFu);
-          v[2 * i + 1] = bf16_bits_to_float(wv[i] >> 16);
+          for (int i = 0; i < 16; i++) {
+            v[2 * i] = bf16_bits_to_float(wv[i] & 0xFFFFu);
+            v[2 * i + 1] = bf16_bits_to_float(wv[i] >> 16);
+          }
+          uint32_t w[8];
+          sb = quantize32<FMT, HAD>(v, amax, w);
+          uint8_t* dst = p.row_data + (int64_t)b * p.row_batch_stride + (r0 + r) * p.row_ld +
+                         (c0 + cb * 32) / 32 * BlockBytes<FMT>::value;
+          store_block<FMT>(dst, w);
         }
-        uint32_t w[8];
-        uint32_t sb = quantize32<FMT, HAD>(v, amax, w);
-        uint8_t* dst = p.row_data + (int64_t)b * p.row_batch_stride + (r0 + r) * p.row_ld +
-                       (c0 + cb * 32) / 32 * BlockBytes<FMT>::value;
-        store_block<FMT>(dst, w);
         sc_row[(r & 31) * 16 + (r >> 5) * 4 + cb] = (uint8_t)sb;
       }
     }
-  }
 
-  // ---- columnwise: blocks of 32 rows, stored transposed ----
-  if constexpr (COL) {
-    const int cp = (warp & 1) * 32 + lane;  // column pair 0..63
-    const int rb = warp >> 1;               // 32-row block 0..3
-    const int c = 2 * cp;
-    if (c < vcols && rb * 32 < vrows) {
+    // ---- columnwise: blocks of 32 rows, stored transposed ----
+    if constexpr (COL) {
+      const int cp = (warp & 1) * 32 + lane;  // column pair 0..63
+      const int rb = warp >> 1;               // 32-row block 0..3
+      const int c = 2 * cp;
+      const bool valid = c < vcols && rb * 32 < vrows;
       uint32_t wv[32];
+      if (valid) {
 #pragma unroll
-      for (int i = 0; i < 32; i++) wv[i] = *reinterpret_cast<const uint32_t*>(&tile[(rb * 32 + i) * QPAD + c]);
-      uint32_t m2 = amax_bf16_pairs(wv, 32);
+        for (int i = 0; i < 32; i++) wv[i] = *reinterpret_cast<const uint32_t*>(tile + tile_off(rb * 32 + i, c));
+      }
+      const uint32_t m2 = valid ? amax_bf16_pairs(wv, 32) : 0u;
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        float v[32];
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-          v[i] = bf16_bits_to_float(h ? (wv[i] >> 16) : (wv[i] & 0xFFFFu));
-          if (COLSUM) sum += v[i];
-        }
-        if (COLSUM) part[rb][c + h] = sum;
-        uint32_t amax = (h ? (m2 >> 16) : (m2 & 0xFFFFu)) << 16;
-        uint32_t w[8];
-        uint32_t sb = quantize32<FMT, HAD>(v, amax, w);
         const int cc = c + h;
-        uint8_t* dst = p.col_data + (int64_t)b * p.col_batch_stride + (c0 + cc) * p.col_ld +
-                       (r0 + rb * 32) / 32 * BlockBytes<FMT>::value;
-        store_block<FMT>(dst, w);
+        uint32_t sb = 0;
+        float sum = 0.f;
+        if (valid) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            v[i] = bf16_bits_to_float(h ? (wv[i] >> 16) : (wv[i] & 0xFFFFu));
+            if (COLSUM) sum += v[i];
+          }
+          const uint32_t amax = (h ? (m2 >> 16) : (m2 & 0xFFFFu)) << 16;
+          uint32_t w[8];
+          sb = quantize32<FMT, HAD>(v, amax, w);
+          uint8_t* dst = p.col_data + (int64_t)b * p.col_batch_stride + (c0 + cc) * p.col_ld +
+                         (r0 + rb * 32) / 32 * BlockBytes<FMT>::value;
+          store_block<FMT>(dst, w);
+        }
+        if (COLSUM) part[rb * QT + cc] = sum;
         sc_col[(cc & 31) * 16 + (cc >> 5) * 4 + rb] = (uint8_t)sb;
       }
     }
-  }
-  __syncthreads();
+    __syncthreads();  // stage s fully read; chunks and partial sums complete
 
-  // ---- scale chunks (one 512-byte chunk per orientation) and column sums ----
-  if (tid < 32) {
-    if constexpr (ROW) {
-      int64_t sc_cols = p.cols / 32;
-      int64_t chunk = (r0 / 128) * ((sc_cols + 3) / 4) + c0 / 128;
-      uint4* dst = reinterpret_cast<uint4*>(p.row_scale + (int64_t)b * p.row_scale_batch_stride + chunk * 512);
-      dst[tid] = reinterpret_cast<const uint4*>(sc_row)[tid];
+    if (tid == 0 && t + 2 * (int64_t)gridDim.x < total) issue(t + 2 * (int64_t)gridDim.x, s);
+    if (tid < 32) {
+      if constexpr (ROW) {
+        const int64_t chunk = (r0 / 128) * ((p.cols / 32 + 3) / 4) + c0 / 128;
+        reinterpret_cast<uint4*>(p.row_scale + (int64_t)b * p.row_scale_batch_stride + chunk * 512)[tid] =
+            reinterpret_cast<const uint4*>(sc_row)[tid];
+      }
+    } else if (tid < 64) {
+      if constexpr (COL) {
+        const int64_t chunk = (c0 / 128) * ((p.rows / 32 + 3) / 4) + r0 / 128;
+        reinterpret_cast<uint4*>(p.col_scale + (int64_t)b * p.col_scale_batch_stride + chunk * 512)[tid - 32] =
+            reinterpret_cast<const uint4*>(sc_col)[tid - 32];
+      }
     }
-  } else if (tid < 64) {
-    if constexpr (COL) {
-      int64_t sc_cols = p.rows / 32;
-      int64_t chunk = (c0 / 128) * ((sc_cols + 3) / 4) + r0 / 128;
-      uint4* dst = reinterpret_cast<uint4*>(p.col_scale + (int64_t)b * p.col_scale_batch_stride + chunk * 512);
-      dst[tid - 32] = reinterpret_cast<const uint4*>(sc_col)[tid - 32];
+    if constexpr (COLSUM) {
+      if (tid >= 128 && tid - 128 < vcols) {
+        const int c = tid - 128;
+        float sum = part[c];
+        sum += part[QT + c];
+        sum += part[2 * QT + c];
+        sum += part[3 * QT + c];
+        p.colsum_partials[(r0 / 128) * p.cols + c0 + c] = sum;
+      }
     }
   }
-  if constexpr (COLSUM) {
-    if (tid < QT && tid < vcols) {
-      float s = part[0][tid];
-      s += part[1][tid];
-      s += part[2][tid];
-      s += part[3][tid];
-      p.colsum_partials[(r0 / 128) * p.cols + c0 + tid] = s;
+  if (*abort_flag) {
+    // a wait ran out: let every copy this CTA issued land before exiting
+    if (tid == 0) {
+      volatile int no_abort = 0;
+      atomicOr(&g_quant_status, DEV_TIMEOUT);
+      for (int k = 0; k < 2; k++) {
+        const int64_t t = blockIdx.x + (int64_t)(it + k) * gridDim.x;
+        if (t < total) mbar_wait_bounded(&full[(it + k) & 1], (uint32_t)(((it + k) >> 1) & 1), &no_abort, budget);
+      }
     }
+    __syncthreads();
   }
 }
 
@@ -225,30 +275,45 @@ __global__ void colsum_reduce_kernel(const float* __restrict__ partials, int64_t
   out[c] = s;
 }
 
+cudaError_t read_quant_status(unsigned* out) {
+  return cudaMemcpyFromSymbol(out, g_quant_status, sizeof(unsigned));
+}
+cudaError_t reset_quant_status() {
+  unsigned z = 0;
+  return cudaMemcpyToSymbol(g_quant_status, &z, sizeof(unsigned));
+}
+
 cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s) {
   colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, s>>>(partials, tiles, cols, out);
   return cudaGetLastError();
 }
 
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
-static cudaError_t launch_q(const QuantParams& p, int batch, cudaStream_t s) {
-  int64_t tiles = (int64_t)p.tiles_x * ((p.rows + QT - 1) / QT);
-  dim3 grid((unsigned)tiles, (unsigned)batch);
-  quantize_kernel<FMT, HAD, ROW, COL, COLSUM><<<grid, 256, 0, s>>>(p);
+static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStream_t s) {
+  auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int64_t tiles = (int64_t)p.tiles_x * ((p.rows + QT - 1) / QT) * p.batch;
+  const int64_t cap = 2ll * q.num_sms;
+  kern<<<(unsigned)(tiles < cap ? tiles : cap), 256, Q_SMEM, s>>>(q.xmap, p);
   return cudaGetLastError();
 }
 
 template <int FMT, bool HAD>
-static cudaError_t dispatch_orient(const QuantParams& p, int batch, bool row, bool col, bool colsum,
+static cudaError_t dispatch_orient(const QuantLaunch& q, const QuantParams& p, bool row, bool col, bool colsum,
                                    cudaStream_t s) {
   if (colsum) {
-    if (row && col) return launch_q<FMT, HAD, true, true, true>(p, batch, s);
-    if (col) return launch_q<FMT, HAD, false, true, true>(p, batch, s);
+    if (row && col) return launch_q<FMT, HAD, true, true, true>(q, p, s);
+    if (col) return launch_q<FMT, HAD, false, true, true>(q, p, s);
     return cudaErrorInvalidValue;  // column sums come from the columnwise pass
   }
-  if (row && col) return launch_q<FMT, HAD, true, true, false>(p, batch, s);
-  if (row) return launch_q<FMT, HAD, true, false, false>(p, batch, s);
-  return launch_q<FMT, HAD, false, true, false>(p, batch, s);
+  if (row && col) return launch_q<FMT, HAD, true, true, false>(q, p, s);
+  if (row) return launch_q<FMT, HAD, true, false, false>(q, p, s);
+  return launch_q<FMT, HAD, false, true, false>(q, p, s);
 }
 
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s) {
@@ -266,15 +331,16 @@ cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s) {
   p.col_scale_batch_stride = q.col_data ? (int64_t)scale_bytes(q.cols, q.rows / 32) : 0;
   p.colsum_partials = q.colsum_partials;
   p.tiles_x = (int)((q.cols + QT - 1) / QT);
+  p.batch = (int)q.batch;
   const bool row = q.row_data != nullptr, col = q.col_data != nullptr, cs = q.colsum_partials != nullptr;
   cudaError_t e;
   switch (q.fmt * 2 + (q.hadamard ? 1 : 0)) {
-    case 0: e = dispatch_orient<E4M3, false>(p, q.batch, row, col, cs, s); break;
-    case 1: e = dispatch_orient<E4M3, true>(p, q.batch, row, col, cs, s); break;
-    case 2: e = dispatch_orient<E2M3, false>(p, q.batch, row, col, cs, s); break;
-    case 3: e = dispatch_orient<E2M3, true>(p, q.batch, row, col, cs, s); break;
-    case 4: e = dispatch_orient<E2M1, false>(p, q.batch, row, col, cs, s); break;
-    default: e = dispatch_orient<E2M1, true>(p, q.batch, row, col, cs, s); break;
+    case 0: e = dispatch_orient<E4M3, false>(q, p, row, col, cs, s); break;
+    case 1: e = dispatch_orient<E4M3, true>(q, p, row, col, cs, s); break;
+    case 2: e = dispatch_orient<E2M3, false>(q, p, row, col, cs, s); break;
+    case 3: e = dispatch_orient<E2M3, true>(q, p, row, col, cs, s); break;
+    case 4: e = dispatch_orient<E2M1, false>(q, p, row, col, cs, s); break;
+    default: e = dispatch_orient<E2M1, true>(q, p, row, col, cs, s); break;
   }
   if (e != cudaSuccess || !cs) return e;
   int64_t tiles = (q.rows + QT - 1) / QT;
