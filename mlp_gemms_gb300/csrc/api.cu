@@ -132,6 +132,22 @@ mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64
   return MX_OK;
 }
 
+// BF16 output [rows, cols] with row stride ld elements as TMA store
+// target: 32x32 boxes, 64-byte swizzle (matching the epilogue's staging).
+mx_status_t make_tmap_out(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+  return MX_OK;
+}
+
 // tcgen05 .kind::mxf8f6f4 element type code of an MX format.
 int mma_type(int fmt) { return fmt == MX_E4M3 ? 0 : (fmt == MX_E2M3 ? 3 : 5); }
 
@@ -214,14 +230,25 @@ uint32_t stage_tx_bytes(int fmt, int bn) {
   return (128u + (uint32_t)bn) * row + 512u + (uint32_t)(bn / 128) * 512u;
 }
 
+// A BF16 output the epilogue writes with TMA stores (base NULL: none).
+struct OutView {
+  const void* base;
+  int64_t rows, cols, ld;
+};
+
 mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
-                     const DevInfo& dev) {
+                     const DevInfo& dev, OutView out) {
   p.tx_bytes = stage_tx_bytes(a->fmt, bn);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   mx_status_t st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt);
   if (st != MX_OK) return st;
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
-  cudaError_t e = mx::launch_gemm(p, ta, tb, bn, s, dev.sms);
+  if (out.base) {
+    if ((st = make_tmap_out(&to, out.base, out.rows, out.cols, out.ld)) != MX_OK) return st;
+  } else {
+    to = ta;
+  }
+  cudaError_t e = mx::launch_gemm(p, ta, tb, to, bn, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
   return MX_OK;
 }
@@ -365,7 +392,7 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = ld_out;
-  return run_gemm(p, a, b, bn, s, dev);
+  return run_gemm(p, a, b, bn, s, dev, OutView{out_bf16, R, N, ld_out});
 }
 
 mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
@@ -409,7 +436,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   p.q_row = static_cast<uint8_t*>(h_row->data); p.q_row_scale = h_row->scale;
   p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
   p.q_cols = F;
-  return run_gemm(p, x_row, w1_row, 256, s, dev);
+  return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F});
 }
 
 mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
@@ -453,7 +480,7 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   p.q_row = static_cast<uint8_t*>(dz_row->data); p.q_row_scale = dz_row->scale;
   p.q_col = static_cast<uint8_t*>(dz_col->data); p.q_col_scale = dz_col->scale;
   p.q_cols = 2 * F;
-  return run_gemm(p, dy_row, w2t_row, 128, s, dev);
+  return run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0});
 }
 
 mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
@@ -490,7 +517,7 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   p.num_tiles = (int64_t)G * p.m_tiles * p.n_tiles;
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = K;
-  return run_gemm(p, a_col, b_col, bn, s, dev);
+  return run_gemm(p, a_col, b_col, bn, s, dev, OutView{out_bf16, (int64_t)G * N, K, K});
 }
 
 mx_status_t mx_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, const void* bias_bf16, void* out_bf16,
@@ -527,7 +554,7 @@ mx_status_t mx_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, const void*
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = ld_out;
   p.bias = static_cast<const uint16_t*>(bias_bf16);
-  return run_gemm(p, a, b, bn, s, dev);
+  return run_gemm(p, a, b, bn, s, dev, OutView{out_bf16, M, N, ld_out});
 }
 
 namespace {
@@ -584,10 +611,15 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
   p.bias = static_cast<const uint16_t*>(bias_bf16);
   p.colsum_partials = partials;
   p.tx_bytes = stage_tx_bytes(a->fmt, 128);
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to;
   if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
-  cudaError_t e = mx::launch_gemm_dense(p, ta, tb, s, dev.sms);
+  if (epi == mx::EPI_GELU) {
+    if ((st = make_tmap_out(&to, pre_bf16, M, H, H)) != MX_OK) return st;
+  } else {
+    to = ta;
+  }
+  cudaError_t e = mx::launch_gemm_dense(p, ta, tb, to, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
   return MX_OK;
 }

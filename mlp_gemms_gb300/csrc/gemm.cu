@@ -9,7 +9,7 @@ namespace mx {
 
 template <int BN, int EPI, int MODE>
 static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                              cudaStream_t s, int num_sms) {
+                              const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE>;
   constexpr int smem = Cfg<BN>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
@@ -20,20 +20,20 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, NUM_THREADS, smem, s>>>(ta, tb, p);
+  kern<<<(unsigned)grid, NUM_THREADS, smem, s>>>(ta, tb, to, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, int bn,
-                        cudaStream_t s, int num_sms) {
-  if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, s, num_sms);
-  if (p.epi == EPI_DSWIGLU) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, s, num_sms);
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                        int bn, cudaStream_t s, int num_sms) {
+  if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+  if (p.epi == EPI_DSWIGLU) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   if (p.mode == MODE_WGRAD) {
-    if (bn == 128) return launch_one<128, EPI_BF16, MODE_WGRAD>(p, ta, tb, s, num_sms);
-    return launch_one<256, EPI_BF16, MODE_WGRAD>(p, ta, tb, s, num_sms);
+    if (bn == 128) return launch_one<128, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
+    return launch_one<256, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
   }
-  if (bn == 128) return launch_one<128, EPI_BF16, MODE_GROUPED>(p, ta, tb, s, num_sms);
-  return launch_one<256, EPI_BF16, MODE_GROUPED>(p, ta, tb, s, num_sms);
+  if (bn == 128) return launch_one<128, EPI_BF16, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+  return launch_one<256, EPI_BF16, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
 }
 
 cudaError_t read_gemm_status(unsigned* out) {

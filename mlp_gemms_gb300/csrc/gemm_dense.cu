@@ -13,7 +13,7 @@ namespace mx {
 
 template <int EPI, int QF, bool QH>
 static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                                    cudaStream_t s, int num_sms) {
+                                    const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<128, EPI, MODE_GROUPED, QF, QH>;
   constexpr int smem = Cfg<128>::SMEM_BYTES;
   static bool configured = false;
@@ -24,26 +24,26 @@ static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, 
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, NUM_THREADS, smem, s>>>(ta, tb, p);
+  kern<<<(unsigned)grid, NUM_THREADS, smem, s>>>(ta, tb, to, p);
   return cudaGetLastError();
 }
 
 template <int EPI>
-static cudaError_t dispatch_q(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, cudaStream_t s,
-                              int num_sms) {
-  if (p.q_fmt == E2M3 && p.q_had) return launch_dense_one<EPI, E2M3, true>(p, ta, tb, s, num_sms);
-  if (p.q_fmt == E2M3) return launch_dense_one<EPI, E2M3, false>(p, ta, tb, s, num_sms);
-  if (p.q_fmt == E4M3 && p.q_had) return launch_dense_one<EPI, E4M3, true>(p, ta, tb, s, num_sms);
-  if (p.q_fmt == E4M3) return launch_dense_one<EPI, E4M3, false>(p, ta, tb, s, num_sms);
+static cudaError_t dispatch_q(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& to, cudaStream_t s, int num_sms) {
+  if (p.q_fmt == E2M3 && p.q_had) return launch_dense_one<EPI, E2M3, true>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E2M3) return launch_dense_one<EPI, E2M3, false>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E4M3 && p.q_had) return launch_dense_one<EPI, E4M3, true>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E4M3) return launch_dense_one<EPI, E4M3, false>(p, ta, tb, to, s, num_sms);
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, cudaStream_t s,
-                              int num_sms) {
+cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& to, cudaStream_t s, int num_sms) {
   cudaError_t e;
-  if (p.epi == EPI_GELU) return dispatch_q<EPI_GELU>(p, ta, tb, s, num_sms);
+  if (p.epi == EPI_GELU) return dispatch_q<EPI_GELU>(p, ta, tb, to, s, num_sms);
   if (p.epi != EPI_DGELU) return cudaErrorInvalidValue;
-  if ((e = dispatch_q<EPI_DGELU>(p, ta, tb, s, num_sms)) != cudaSuccess) return e;
+  if ((e = dispatch_q<EPI_DGELU>(p, ta, tb, to, s, num_sms)) != cudaSuccess) return e;
   return cudaSuccess;
 }
 

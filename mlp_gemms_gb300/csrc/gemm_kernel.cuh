@@ -52,7 +52,7 @@ struct Cfg {
   static constexpr int SF_BYTES = 512 + (BN / 128) * 512;
   static constexpr int SF_COLS = 4 + 4 * (BN / 128);
   static constexpr uint32_t TX = A_BYTES + B_BYTES + SF_BYTES;
-  static constexpr int TB_BYTES = 2304;
+  static constexpr int TB_BYTES = 2560;  // 512-byte multiple: TMA store swizzle atoms
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
@@ -67,6 +67,7 @@ struct Cfg {
   static_assert(ACC * BN <= 256, "accumulators live in tensor-memory columns 0..255");
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "scale slots must fit");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(OFF_TB % 1024 == 0, "staging buffers must be swizzle-atom aligned");
 };
 
 struct Tile {
@@ -127,7 +128,35 @@ __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool re
 
 // ---- epilogue helpers --------------------------------------------------
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// sigmoid as 1 / (1 + exp(-x)) with the fast exponential and divide
+// intrinsics (exactly 1.0 once exp(-x) vanishes against 1, 0 once it
+// overflows).
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// Convert 32 fp32 values (this lane's row) to BF16 into the warp's staging
+// buffer (row = lane, 64 bytes, 64-byte swizzle) and store the warp's 32x32
+// block with one TMA store.  The caller has made sure the buffer's previous
+// store has been read (bulk_wait_read by lane 0, then __syncwarp).
+__device__ __forceinline__ void store_bf16_block(const float* v, uint8_t* stage, int lane, const CUtensorMap* tm,
+                                                 int64_t col0, int64_t row0) {
+  uint4* row = reinterpret_cast<uint4*>(stage + lane * 64);
+#pragma unroll
+  for (int c = 0; c < 4; c++)
+    row[c ^ ((lane >> 1) & 3)] = make_uint4(float2_to_bf16x2(v[8 * c], v[8 * c + 1]), float2_to_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                            float2_to_bf16x2(v[8 * c + 4], v[8 * c + 5]), float2_to_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm, stage, (int)col0, (int)row0);
+    bulk_commit();
+  }
+}
+
+// Before a warp rewrites its staging buffer: the previous TMA store has read it.
+__device__ __forceinline__ void stage_reuse_wait(int lane) {
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+}
 
 // Rowwise E4M3 requant of 32 fp32 values held by one thread.
 __device__ __forceinline__ uint32_t row_quant_store_e4m3(float (&v)[32], uint8_t* dst) {
@@ -277,7 +306,7 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using C = Cfg<BN>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -306,7 +335,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) { prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); }
+  if (warp == 0 && lane == 0) { prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); prefetch_tensormap(&tmO); }
   if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
   tc_fence_before();
   __syncthreads();
@@ -410,6 +439,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;        // tensor-memory lane quarter
     const int half = ew >> 2;      // column half
     float* tb = reinterpret_cast<float*>(sTB + ew * C::TB_BYTES);
+    uint8_t* tb_bytes = sTB + ew * C::TB_BYTES;
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t epi_phase = 0;
@@ -449,8 +479,6 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
-        const int64_t row = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + row_in_tile;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_ld + T.n0 + half * COLS);
         if (p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
           const uint4* bp = reinterpret_cast<const uint4*>(p.bias + T.n0 + half * COLS);
 #pragma unroll
@@ -467,17 +495,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
           }
         }
+        const int64_t row0 = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + q * 32;
 #pragma unroll
         for (int i = 0; i < COLS / 32; i++) {
-#pragma unroll
-          for (int c = 0; c < 4; c++) {
-            const uint32_t* s = &v[i][8 * c];
-            dst[i * 4 + c] = make_uint4(
-                float2_to_bf16x2(__uint_as_float(s[0]), __uint_as_float(s[1])),
-                float2_to_bf16x2(__uint_as_float(s[2]), __uint_as_float(s[3])),
-                float2_to_bf16x2(__uint_as_float(s[4]), __uint_as_float(s[5])),
-                float2_to_bf16x2(__uint_as_float(s[6]), __uint_as_float(s[7])));
-          }
+          stage_reuse_wait(lane);
+          store_bf16_block(reinterpret_cast<const float*>(v[i]), tb_bytes, lane, &tmO, T.n0 + half * COLS + 32 * i, row0);
         }
         if (C::ACC == 2) {
           tc_fence_before();
@@ -498,26 +520,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
         const int64_t row = T.m0 + row_in_tile;
         const int64_t f0 = T.n0;
-        // BF16 pre-activation save: z = [gate | up]
-        uint16_t* zr = p.z + row * (2 * p.F);
-        uint4* zg = reinterpret_cast<uint4*>(zr + f0 + half * 64);
-        uint4* zu = reinterpret_cast<uint4*>(zr + p.F + f0 + half * 64);
+        // BF16 pre-activation save: z = [gate | up], 32x32 blocks by TMA store
 #pragma unroll
         for (int i = 0; i < 2; i++) {
-#pragma unroll
-          for (int c = 0; c < 4; c++) {
-            const uint32_t* s = &gv[i][8 * c];
-            zg[i * 4 + c] = make_uint4(float2_to_bf16x2(__uint_as_float(s[0]), __uint_as_float(s[1])),
-                                       float2_to_bf16x2(__uint_as_float(s[2]), __uint_as_float(s[3])),
-                                       float2_to_bf16x2(__uint_as_float(s[4]), __uint_as_float(s[5])),
-                                       float2_to_bf16x2(__uint_as_float(s[6]), __uint_as_float(s[7])));
-            const uint32_t* u = &uv[i][8 * c];
-            zu[i * 4 + c] = make_uint4(float2_to_bf16x2(__uint_as_float(u[0]), __uint_as_float(u[1])),
-                                       float2_to_bf16x2(__uint_as_float(u[2]), __uint_as_float(u[3])),
-                                       float2_to_bf16x2(__uint_as_float(u[4]), __uint_as_float(u[5])),
-                                       float2_to_bf16x2(__uint_as_float(u[6]), __uint_as_float(u[7])));
-          }
+          stage_reuse_wait(lane);
+          store_bf16_block(reinterpret_cast<const float*>(gv[i]), tb_bytes, lane, &tmO, f0 + half * 64 + 32 * i,
+                           T.m0 + q * 32);
+          stage_reuse_wait(lane);
+          store_bf16_block(reinterpret_cast<const float*>(uv[i]), tb_bytes, lane, &tmO, p.F + f0 + half * 64 + 32 * i,
+                           T.m0 + q * 32);
         }
+        stage_reuse_wait(lane);  // the transpose buffer is reused below
         // h = g * sigmoid(g) * u in fp32
         float h[2][32];
 #pragma unroll
@@ -658,11 +671,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             float pre[32];
 #pragma unroll
             for (int j = 0; j < 32; j++) pre[j] = __uint_as_float(accr[j]) + aux[j];
-            uint4* zd = reinterpret_cast<uint4*>(p.z + row * p.q_cols + n0 + fc);
-#pragma unroll
-            for (int c = 0; c < 4; c++)
-              zd[c] = make_uint4(float2_to_bf16x2(pre[8 * c], pre[8 * c + 1]), float2_to_bf16x2(pre[8 * c + 2], pre[8 * c + 3]),
-                                 float2_to_bf16x2(pre[8 * c + 4], pre[8 * c + 5]), float2_to_bf16x2(pre[8 * c + 6], pre[8 * c + 7]));
+            stage_reuse_wait(lane);
+            store_bf16_block(pre, tb_bytes, lane, &tmO, n0 + fc, T.m0 + q * 32);
+            stage_reuse_wait(lane);  // the transpose buffer is reused below
 #pragma unroll
             for (int j = 0; j < 32; j++) val[j] = gelu_tanh_f(pre[j]);
           } else {
@@ -704,6 +715,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       if (++acc == C::ACC) { acc = 0; acc_phase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
   }
 
   tc_fence_before();

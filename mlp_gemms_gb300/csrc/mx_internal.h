@@ -67,10 +67,12 @@ struct GemmParams {
   float* colsum_partials;   // dGELU: fp32 [ceil(R/128), C] per-tile column sums
 };
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, int bn,
-                        cudaStream_t s, int num_sms);
+// ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte
+// swizzle) of the epilogue's BF16 output, or any valid map when it has none.
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                        int bn, cudaStream_t s, int num_sms);
 cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                              cudaStream_t s, int num_sms);
+                              const CUtensorMap& to, cudaStream_t s, int num_sms);
 cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s);
 cudaError_t read_gemm_status(unsigned* out);
 cudaError_t reset_gemm_status();
