@@ -140,6 +140,32 @@ MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, 
                         float *colsum, void *workspace, size_t workspace_bytes, mx_stream_t stream);
 
 /*
+ * mx_quantize_colsum_noalloc -- mx_quantize with MX_COLSUM for callers that
+ * cannot allocate device memory: a framework hook that runs under a memory
+ * pool it may not grow, a graph-capture region where allocation is not
+ * allowed, or an embedding that owns all device memory up front.  The
+ * per-tile column-sum partials, which mx_quantize keeps in the caller's
+ * workspace, live here in a fixed scratch array inside this library instead
+ * (MX_NOALLOC_COLSUM_MAX_PARTIALS fp32 values = 8 MiB, held by every GPU that
+ * loads the library until the process exits).  The call allocates nothing.
+ * No passage of the pages corresponds to it: it is a deployment variant.
+ *   Arguments as mx_quantize with batch = 1 and no workspace; flags must
+ *   include MX_COLSUM and MX_COLWISE.
+ *   Limit: ceil(rows / 128) * cols <= MX_NOALLOC_COLSUM_MAX_PARTIALS, else
+ *   MX_ERR_WORKSPACE (use mx_quantize with a workspace).
+ *   The first call on a device looks up the scratch's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   Every call shares the scratch: the partials are fully rewritten by each
+ *   call before they are read, so nothing needs clearing, but calls whose
+ *   execution overlaps on the GPU (different streams, no ordering) race on
+ *   it and must be serialised by the caller.
+ */
+#define MX_NOALLOC_COLSUM_MAX_PARTIALS (1u << 21)
+MX_API mx_status_t mx_quantize_colsum_noalloc(const void *x_bf16, int64_t rows, int64_t cols, int64_t ld,
+                                              int32_t fmt, uint32_t flags, const mx_tensor_t *out_row,
+                                              const mx_tensor_t *out_col, float *colsum, mx_stream_t stream);
+
+/*
  * Offsets (all grouped calls): device int32 [G], cumulative END offsets of
  * each expert's row segment, nondecreasing, each a multiple of 128,
  * offsets[G-1] <= R.  Rows in [offsets[G-1], R) are neither read nor

@@ -32,7 +32,7 @@ ABI_SYMBOLS = (
     "mx_quantize_workspace_bytes", "mx_quantize", "mx_grouped_gemm", "mx_grouped_gemm_swiglu_fwd",
     "mx_grouped_gemm_dswiglu_bwd", "mx_grouped_gemm_wgrad", "mx_mlp_workspace_bytes", "mx_mlp_fwd_bwd",
     "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
-    "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd",
+    "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc",
 )
 
 
@@ -92,6 +92,7 @@ def load(path=None):
         "mx_gemm_gelu_fwd": (ctypes.c_int, [tp, tp, vp, vp, tp, tp, vp]),
         "mx_gemm_dgelu_workspace_bytes": (sz, [i64, i64]),
         "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
+        "mx_quantize_colsum_noalloc": (ctypes.c_int, [vp, i64, i64, i64, i32, u32, tp, tp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -178,6 +179,27 @@ def mx_quantize(x, fmt=E4M3, rowwise=True, colwise=True, hadamard=False, colsum=
     _check(load().mx_quantize(_ptr(x), batch, rows, cols, ld, fmt, flags, _s(out_row) if rowwise else None,
                               _s(out_col) if colwise else None, _ptr(colsum_out) if colsum else None,
                               _ptr(workspace) if colsum else None, ws_bytes, _stream(stream)))
+    return out_row, out_col, colsum_out
+
+
+def mx_quantize_colsum_noalloc(x, fmt=E4M3, rowwise=True, hadamard=False, out_row=None, out_col=None,
+                               colsum_out=None, stream=None):
+    """Quantize a BF16 [rows, cols] tensor columnwise (and rowwise) with the
+    per-column sums, using the library's fixed scratch instead of a
+    workspace: for callers that cannot allocate device memory.  Outputs are
+    allocated here only when the caller passes none."""
+    import torch
+    rows, cols = x.shape
+    flags = COLWISE | COLSUM | (ROWWISE if rowwise else 0) | (HADAMARD if hadamard else 0)
+    if rowwise and out_row is None:
+        out_row = MX(rows, cols, fmt, hadamard, x.device)
+    if out_col is None:
+        out_col = MX(cols, rows, fmt, hadamard, x.device)
+    if colsum_out is None:
+        colsum_out = torch.empty(cols, dtype=torch.float32, device=x.device)
+    _check(load().mx_quantize_colsum_noalloc(_ptr(x), rows, cols, x.stride(0), fmt, flags,
+                                             _s(out_row) if rowwise else None, _s(out_col), _ptr(colsum_out),
+                                             _stream(stream)))
     return out_row, out_col, colsum_out
 
 

@@ -353,6 +353,25 @@ mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t
   return MX_OK;
 }
 
+mx_status_t mx_quantize_colsum_noalloc(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                                       uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col,
+                                       float* colsum, mx_stream_t stream) {
+  MX_CHECK((flags & MX_COLSUM) && (flags & MX_COLWISE), MX_ERR_INVALID_ARG,
+           "mx_quantize_colsum_noalloc computes column sums: flags need MX_COLSUM and MX_COLWISE");
+  MX_CHECK(rows >= 0 && cols > 0, MX_ERR_SHAPE, "shape [%lld, %lld]", (long long)rows, (long long)cols);
+  const size_t need = (size_t)((rows + 127) / 128) * (size_t)cols;
+  MX_CHECK(need <= mx::kNoAllocColsumFloats, MX_ERR_WORKSPACE,
+           "ceil(rows/128) * cols = %zu exceeds the fixed column-sum scratch of %zu values; "
+           "use mx_quantize with a workspace", need, mx::kNoAllocColsumFloats);
+  if (rows == 0) return mx_quantize(x_bf16, 1, rows, cols, ld, fmt, flags, out_row, out_col, colsum, nullptr, 0, stream);
+  float* scratch = nullptr;
+  size_t cap = 0;
+  cudaError_t e = mx::colsum_scratch(&scratch, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "looking up the column-sum scratch");
+  return mx_quantize(x_bf16, 1, rows, cols, ld, fmt, flags, out_row, out_col, colsum, scratch, cap * sizeof(float),
+                     stream);
+}
+
 mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
                             void* out_bf16, int64_t ld_out, mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -30,6 +30,10 @@ struct QuantLaunch {
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
 cudaError_t read_quant_status(unsigned* out);
+// Capacity (fp32 values) of the fixed column-sum scratch and its address on
+// the current device.
+constexpr size_t kNoAllocColsumFloats = size_t(1) << 21;
+cudaError_t colsum_scratch(float** out, size_t* floats);
 cudaError_t reset_quant_status();
 
 enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };

@@ -23,6 +23,8 @@
 // blocked chunk, assembled in shared memory and written with one coalesced
 // store.  Column sums are fp32 per tile ([ceil(rows/128), cols] partials),
 // reduced in a fixed order by a second kernel: deterministic, no atomics.
+#include <mutex>
+
 #include "mx_common.cuh"
 #include "mx_internal.h"
 
@@ -273,6 +275,36 @@ __global__ void colsum_reduce_kernel(const float* __restrict__ partials, int64_t
   float s = 0.f;
   for (int64_t t = 0; t < tiles; t++) s += partials[t * cols + c];
   out[c] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for the column-sum partials of the no-allocation entry point
+// (mx_quantize_colsum_noalloc).  Every GPU that loads this library holds it
+// until the process exits; all calls share it.
+// ---------------------------------------------------------------------------
+
+static __device__ __align__(256) float g_colsum_scratch[kNoAllocColsumFloats];
+
+static std::mutex g_scratch_mu;
+static float* g_scratch_ptr[64] = {};
+
+// Device address of the scratch on the current device, looked up once per
+// device (the array's host-side name is not a device address).
+cudaError_t colsum_scratch(float** out, size_t* floats) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_colsum_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_scratch_ptr[dev];
+  *floats = kNoAllocColsumFloats;
+  return cudaSuccess;
 }
 
 cudaError_t read_quant_status(unsigned* out) {
