@@ -42,6 +42,7 @@ static __device__ unsigned g_gemm_status = 0;
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
+constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
 
 template <int BN>
 struct Cfg {
@@ -61,7 +62,8 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_CHUNK + 4096;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;    // + slack for 1024-byte alignment
+  static constexpr int OFF_ORDER = OFF_MISC + 16;              // wgrad: experts by descending size
+  static constexpr int SMEM_BYTES = OFF_ORDER + 2 * MAX_SORTED_G + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_TMEM_BASE = 256;
   static_assert(ACC * BN <= 256, "accumulators live in tensor-memory columns 0..255");
@@ -84,7 +86,7 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); 
 // row-block-major over all R rows; the expert is the segment holding the
 // row base.  Wgrad: tiles are expert-major; K runs over the expert's rows.
 template <int NT, int MODE>
-__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report) {
+__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
   Tile T;
   T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0;
   if (MODE == MODE_GROUPED) {
@@ -112,6 +114,7 @@ __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool re
   } else {
     int64_t per_g = (int64_t)p.m_tiles * p.n_tiles;
     T.g = (int)(t / per_g);
+    if (order) T.g = order[T.g];
     int64_t rem = t % per_g;
     T.m0 = (rem / p.n_tiles) * 128;
     T.n0 = (rem % p.n_tiles) * NT;
@@ -124,6 +127,21 @@ __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool re
     T.active = 1;
   }
   return T;
+}
+
+// The global tile a CTA handles at its i-th turn.  Grouped: plain round
+// robin (neighbouring CTAs share A rows and B panels in L2).  Wgrad: tiles
+// are laid out expert by expert in descending size order and dealt to the
+// CTAs boustrophedon-wise (forward on even turns, backward on odd), which
+// spreads the long reductions of the largest experts across the grid.
+template <int MODE>
+__device__ __forceinline__ int64_t tile_index(int64_t i) {
+  if (MODE == MODE_WGRAD && (i & 1)) return i * gridDim.x + (gridDim.x - 1 - blockIdx.x);
+  return i * gridDim.x + blockIdx.x;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* ptr) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(ptr));
 }
 
 // ---- epilogue helpers --------------------------------------------------
@@ -341,6 +359,26 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // wgrad: rank the experts by descending row count (ties by index)
+  const uint16_t* order = nullptr;
+  if (MODE == MODE_WGRAD && p.offsets != nullptr && p.G <= MAX_SORTED_G && p.G > 1) {
+    uint16_t* s_order = reinterpret_cast<uint16_t*>(smem + C::OFF_ORDER);
+    auto count = [&](int g) -> int64_t {
+      const int64_t e = ldg_i32(p.offsets + g), b = g ? ldg_i32(p.offsets + g - 1) : 0;
+      return e - b;
+    };
+    for (int g = threadIdx.x; g < p.G; g += blockDim.x) {
+      const int64_t cg = count(g);
+      int rank = 0;
+      for (int h = 0; h < p.G; h++) {
+        const int64_t ch = count(h);
+        rank += (ch > cg || (ch == cg && h < g)) ? 1 : 0;
+      }
+      s_order[rank] = (uint16_t)g;
+    }
+    __syncthreads();
+    order = s_order;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -352,8 +390,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int armed_parity[C::STAGES];
       for (int s = 0; s < C::STAGES; s++) armed_parity[s] = -1;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        Tile T = get_tile<NT, MODE>(p, t, false);
+      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
+        const int64_t t = tile_index<MODE>(i);
+        if (t >= p.num_tiles) continue;
+        Tile T = get_tile<NT, MODE>(p, t, false, order);
         if (!T.active || T.nk == 0) continue;
         int64_t brow[2];
         if (EPI == EPI_SWIGLU) {
@@ -398,8 +438,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        Tile T = get_tile<NT, MODE>(p, t, false);
+      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
+        const int64_t t = tile_index<MODE>(i);
+        if (t >= p.num_tiles) continue;
+        Tile T = get_tile<NT, MODE>(p, t, false, order);
         if (!T.active || T.nk == 0) continue;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
         tc_fence_after();
@@ -451,8 +493,29 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       epi_phase ^= 1u;
       return ok;
     };
-    for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-      Tile T = get_tile<NT, MODE>(p, t, ew == 0 && lane == 0);
+    // dSwiGLU / dGELU read a saved activation per tile: prefetch a tile's
+    // rows into L2 one tile ahead of its epilogue.
+    auto prefetch_aux = [&](int64_t i) {
+      if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_DGELU) {
+        const int64_t t = tile_index<MODE>(i);
+        if (t >= p.num_tiles) return;
+        const Tile U = get_tile<NT, MODE>(p, t, false, order);
+        if (!U.active || U.nk == 0) return;
+        const int64_t r = U.m0 + q * 32 + lane;
+        if (EPI == EPI_DSWIGLU) {
+          prefetch_l2(p.z + r * (2 * p.F) + U.n0 + half * 64);
+          prefetch_l2(p.z + r * (2 * p.F) + p.F + U.n0 + half * 64);
+        } else {
+          prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
+        }
+      }
+    };
+    prefetch_aux(0);
+    for (int64_t i = 0; i * gridDim.x < p.num_tiles; i++) {
+      const int64_t t = tile_index<MODE>(i);
+      if (t >= p.num_tiles) continue;
+      prefetch_aux(i + 1);
+      Tile T = get_tile<NT, MODE>(p, t, ew == 0 && lane == 0, order);
       if (!T.active) continue;
       const int64_t row_in_tile = q * 32 + lane;
       if (T.nk == 0) {

@@ -48,13 +48,25 @@ struct QuantParams {
 
 constexpr int QT = 128;          // tile edge
 
-// NaN-propagating amax of 32 BF16 values given as 16 packed pairs: integer
-// max of |bits| (a NaN pattern is larger than every other pattern).
-__device__ __forceinline__ uint32_t amax_bf16_pairs(const uint32_t* w, int n) {
-  uint32_t m = 0;
+// NaN-propagating amax of BF16 pairs, per 16-bit half: a tree of
+// max.NaN.xorsign.abs.bf16x2 (magnitude max(|a|, |b|), NaN if either is
+// NaN), sign bits cleared at the end; a NaN shows as a pattern above Inf.
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <int N>
+__device__ __forceinline__ uint32_t amax_bf16_pairs(const uint32_t* w) {
+  uint32_t t[N / 2];
 #pragma unroll
-  for (int i = 0; i < n; i++) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-  return m;
+  for (int i = 0; i < N / 2; i++) t[i] = absmax2(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int n = N / 4; n >= 1; n >>= 1) {
+#pragma unroll
+    for (int i = 0; i < n; i++) t[i] = absmax2(t[i], t[i + n]);
+  }
+  return t[0] & 0x7FFF7FFFu;
 }
 
 template <int FMT>
@@ -97,17 +109,18 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 }
 
 constexpr int Q_STAGE = 32768;                 // one BF16 tile
-constexpr int Q_SMEM = 2 * Q_STAGE + 2048 + 4096 + 64 + 1024;
+constexpr int Q_NST = 3;                       // tiles in the load ring
+constexpr int Q_SMEM = Q_NST * Q_STAGE + 2048 + 4096 + 64 + 1024;
 
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
 __global__ void __launch_bounds__(256, 2)
 quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* sc_all = sm + 2 * Q_STAGE;                                  // [2 parity][row, col][512]
-  float* part_all = reinterpret_cast<float*>(sm + 2 * Q_STAGE + 2048);  // [2 parity][4][128]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + 2 * Q_STAGE + 2048 + 4096);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+  uint8_t* sc_all = sm + Q_NST * Q_STAGE;                                  // [2 parity][row, col][512]
+  float* part_all = reinterpret_cast<float*>(sm + Q_NST * Q_STAGE + 2048);  // [2 parity][4][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Q_NST * Q_STAGE + 2048 + 4096);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + Q_NST);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t tiles_y = (p.rows + QT - 1) / QT;
@@ -116,8 +129,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
   const uint64_t budget = 2000000000ull;
 
   if (tid == 0) {
-    mbar_init(&full[0], 1);
-    mbar_init(&full[1], 1);
+    for (int k = 0; k < Q_NST; k++) mbar_init(&full[k], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -141,23 +153,23 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
     tma_load_2d(sm + s * Q_STAGE + 16384, &xmap, (int)c0 + 64, gy, &full[s], pol);
   };
   if (tid == 0) {
-    if (blockIdx.x < total) issue(blockIdx.x, 0);
-    if (blockIdx.x + gridDim.x < total) issue(blockIdx.x + gridDim.x, 1);
+    for (int k = 0; k < Q_NST; k++)
+      if (blockIdx.x + (int64_t)k * gridDim.x < total) issue(blockIdx.x + (int64_t)k * gridDim.x, k);
   }
 
   int it = 0;
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x, it++) {
-    const int s = it & 1;
-    if (!mbar_wait_bounded(&full[s], (uint32_t)((it >> 1) & 1), abort_flag, budget)) break;
+    const int s = it % Q_NST;
+    if (!mbar_wait_bounded(&full[s], (uint32_t)((it / Q_NST) & 1), abort_flag, budget)) break;
     int b;
     int64_t r0, c0;
     coords(t, b, r0, c0);
     const int vrows = (int)((p.rows - r0) < QT ? (p.rows - r0) : QT);
     const int vcols = (int)((p.cols - c0) < QT ? (p.cols - c0) : QT);
     const uint8_t* tile = sm + s * Q_STAGE;
-    uint8_t* sc_row = sc_all + s * 1024;
+    uint8_t* sc_row = sc_all + (it & 1) * 1024;
     uint8_t* sc_col = sc_row + 512;
-    float* part = part_all + s * 512;
+    float* part = part_all + (it & 1) * 512;
 
     // ---- rowwise: blocks of 32 columns (every chunk slot gets written) ----
     if constexpr (ROW) {
@@ -173,7 +185,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
             const uint4 q = *reinterpret_cast<const uint4*>(tile + tile_off(r, cb * 32 + 8 * k));
             wv[4 * k] = q.x; wv[4 * k + 1] = q.y; wv[4 * k + 2] = q.z; wv[4 * k + 3] = q.w;
           }
-          const uint32_t m2 = amax_bf16_pairs(wv, 16);
+          const uint32_t m2 = amax_bf16_pairs<16>(wv);
           const uint32_t amax = max(m2 & 0xFFFFu, m2 >> 16) << 16;
           float v[32];
 #pragma unroll
@@ -202,7 +214,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
 #pragma unroll
         for (int i = 0; i < 32; i++) wv[i] = *reinterpret_cast<const uint32_t*>(tile + tile_off(rb * 32 + i, c));
       }
-      const uint32_t m2 = valid ? amax_bf16_pairs(wv, 32) : 0u;
+      const uint32_t m2 = valid ? amax_bf16_pairs<32>(wv) : 0u;
 #pragma unroll
       for (int h = 0; h < 2; h++) {
         const int cc = c + h;
@@ -228,7 +240,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
     }
     __syncthreads();  // stage s fully read; chunks and partial sums complete
 
-    if (tid == 0 && t + 2 * (int64_t)gridDim.x < total) issue(t + 2 * (int64_t)gridDim.x, s);
+    if (tid == 0 && t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
     if (tid < 32) {
       if constexpr (ROW) {
         const int64_t chunk = (r0 / 128) * ((p.cols / 32 + 3) / 4) + c0 / 128;
@@ -258,9 +270,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
     if (tid == 0) {
       volatile int no_abort = 0;
       atomicOr(&g_quant_status, DEV_TIMEOUT);
-      for (int k = 0; k < 2; k++) {
+      for (int k = 0; k < Q_NST; k++) {
         const int64_t t = blockIdx.x + (int64_t)(it + k) * gridDim.x;
-        if (t < total) mbar_wait_bounded(&full[(it + k) & 1], (uint32_t)(((it + k) >> 1) & 1), &no_abort, budget);
+        if (t < total)
+          mbar_wait_bounded(&full[(it + k) % Q_NST], (uint32_t)(((it + k) / Q_NST) & 1), &no_abort, budget);
       }
     }
     __syncthreads();
