@@ -40,6 +40,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "grouped MX MLP fwd+bwd TFLOP/s and % of GB300 dense FP8 peak; quantizer HBM GB/s"
 SHAPE = dict(G=128, D=2048, F=768, R=262144)
+W_DENSE = dict(M=16384, D=3072, H=12288)
 WORKLOAD = "moe_mlp_fwd_bwd_mxfp8 G=128 D=2048 F=768 R=262144 (32768 tok x top-8) zipf1.1"
 QUANT_GB = 238.6e6  # algorithmic bytes of the quantizer workload: 2 B in + 2 x (1 + 1/32) B out per element
 
@@ -274,8 +275,12 @@ def run_gpu(args):
     # ---- e2e: host buffers, copies inside the timed region ----
     e2e = end_to_end(mx, torch, inp, offs, G, D, F, R, max(2, min(args.steps, 5)), dev, world)
 
-    # ---- standalone quantizer workload ----
+    # ---- standalone quantizer workload; the other configurations ----
     quant = quantizer_rate(mx, torch, dev)
+    del margs, ws, inp, out
+    torch.cuda.empty_cache()
+    dense = dense_step_rate(mx, torch, dev) if not args.no_extra else None
+    fwd_even = moe_forward_even_rate(mx, torch, dev) if not args.no_extra else None
     status = mx.mx_get_device_status()
     if status != "MX_OK":
         raise RuntimeError("device status: " + status)
@@ -320,6 +325,8 @@ def run_gpu(args):
         "roofline": roof,
         "stages": stages,
         "quantizer": quant,
+        "dense_mxfp6_step": dense,
+        "moe_fwd_even_routing": fwd_even,
     }
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(seconds_hint=args.cpu_seconds)
@@ -427,6 +434,85 @@ def end_to_end(mx, torch, inp, offs, G, D, F, R, steps, dev, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
 
 
+def dense_step_rate(mx, torch, dev, steps=5):
+    """The dense MXFP6 + Hadamard tanh-GELU MLP step (M=16384 tokens,
+    hidden 3072, MLP 12288; E2M3 operands rotated along K, bias gradients)
+    through mx_mlp_fwd_bwd: 12*M*D*H FLOP per step."""
+    M, D, H = W_DENSE["M"], W_DENSE["D"], W_DENSE["H"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    t = {"x": (M, D, 1.0), "w1": (H, D, 0.02), "w2": (D, H, 0.02), "b1": (H, 0.02), "b2": (D, 0.02),
+         "dy": (M, D, 1e-3)}
+    inp = {}
+    for k, v in t.items():
+        shape, std = v[:-1], v[-1]
+        inp[k] = (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+    out = {"y": torch.empty((M, D), dtype=torch.bfloat16, device=dev),
+           "dx": torch.empty((M, D), dtype=torch.bfloat16, device=dev),
+           "dw1": torch.empty((H, D), dtype=torch.bfloat16, device=dev),
+           "dw2": torch.empty((D, H), dtype=torch.bfloat16, device=dev),
+           "db1": torch.empty(H, dtype=torch.float32, device=dev),
+           "db2": torch.empty(D, dtype=torch.float32, device=dev)}
+    kw = dict(act=mx.ACT_GELU_TANH, fmt=mx.E2M3, hadamard=True, b1=inp["b1"], b2=inp["b2"], db1=out["db1"],
+              db2=out["db2"])
+    a0 = mx.mlp_args(inp["x"], inp["w1"], inp["w2"], inp["dy"], None, 1, H, out["y"], out["dx"], out["dw1"],
+                     out["dw2"], **kw)
+    ws = torch.empty(mx.mx_mlp_workspace_bytes(a0), dtype=torch.uint8, device=dev)
+    args = mx.mlp_args(inp["x"], inp["w1"], inp["w2"], inp["dy"], None, 1, H, out["y"], out["dx"], out["dw1"],
+                       out["dw2"], workspace=ws, **kw)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        mx.mx_mlp_fwd_bwd(args)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        mx.mx_mlp_fwd_bwd(args)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    flops = 12.0 * M * D * H
+    peaks, _ = measured_peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "dense mxfp6-e2m3 + hadamard tanh-GELU MLP fwd+bwd M=16384 D=3072 H=12288",
+            "ms_per_step": ms, "tflops": tf, "frac_of_fp8_peak": tf / (2.0 * peaks["bf16_tflops"]),
+            "launches_per_step": 12}
+
+
+def moe_forward_even_rate(mx, torch, dev, steps=5):
+    """The forward half (quantize X, W1, W2; FC1 + SwiGLU; FC2) on even
+    routing (2048 rows per expert): 6*R*D*F FLOP."""
+    import workloads as W
+    G, D, F, R = SHAPE["G"], SHAPE["D"], SHAPE["F"], SHAPE["R"]
+    offs = torch.from_numpy(W.even_offsets(G, R)).to(dev)
+    inp = W.moe_inputs_device(G, D, F, R, seed=5, device=dev)
+    qx, qw1, qw2 = mx.MX(R, D), mx.MX(G * 2 * F, D), mx.MX(G * D, F)
+    h = (mx.MX(R, F), mx.MX(F, R))
+    z = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+
+    def fwd():
+        mx.mx_quantize(inp["x"], 0, True, False, out_row=qx)
+        mx.mx_quantize(inp["w1"], 0, True, False, out_row=qw1)
+        mx.mx_quantize(inp["w2"], 0, True, False, out_row=qw2)
+        mx.mx_grouped_gemm_swiglu_fwd(qx, qw1, G, offs, h[0], h[1], z)
+        mx.mx_grouped_gemm(h[0], qw2, G, offs, out=y)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        fwd()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(steps):
+        fwd()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    return {"workload": "moe fwd (quantize + FC1 SwiGLU + FC2), even routing 2048 rows/expert",
+            "ms": ms, "tflops": 6.0 * R * D * F / (ms * 1e-3) / 1e12}
+
+
 def quantizer_rate(mx, torch, dev):
     """The standalone quantizer workload: 8192 x 7168 BF16 -> MXFP8 rowwise
     and columnwise; the 117 MB input fits in L2, so a 512 MB buffer is
@@ -511,6 +597,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the dense and even-routing extra measurements")
     ap.add_argument("--ncu-case", default=None, help="run one small single-kernel case for a profiler capture")
     args = ap.parse_args()
     if args.ncu_case:
