@@ -26,6 +26,8 @@ struct QuantLaunch {
   float* colsum_partials;  // null: no column sums
   float* colsum;
   CUtensorMap xmap;        // BF16 [batch*rows, cols], box 64 x 128, 128-byte swizzle
+  CUtensorMap rowmap;      // E4M3: row payload [batch*rows, cols] bytes, box 128 x 128, 128-byte swizzle
+  CUtensorMap colmap;      // E4M3: col payload [batch*cols, rows] bytes, same boxes
   int num_sms;
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);

@@ -109,17 +109,37 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 }
 
 constexpr int Q_STAGE = 32768;                 // one BF16 tile
-constexpr int Q_NST = 3;                       // tiles in the load ring
-constexpr int Q_SMEM = Q_NST * Q_STAGE + 2048 + 4096 + 64 + 1024;
+
+// E4M3 tiles are staged in shared memory ([128][128] bytes per orientation,
+// 128-byte swizzle) and written with two TMA stores; the packed sub-byte
+// formats store their blocks directly.
+template <int FMT> struct QCfg {
+  static constexpr bool STAGED = FMT == E4M3;
+  static constexpr int NST = STAGED ? 2 : 3;   // tiles in the load ring
+  static constexpr int OFF_OUT = NST * Q_STAGE;
+  static constexpr int OFF_SC = OFF_OUT + (STAGED ? 32768 : 0);
+  static constexpr int SMEM = OFF_SC + 2048 + 4096 + 64 + 1024;
+};
+
+// Byte offset of (row r, byte b) in a [128][128]-byte staging tile with the
+// 128-byte swizzle the TMA store undoes.
+__device__ __forceinline__ uint32_t stage_off(int r, int b) {
+  return (uint32_t)(r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
+}
 
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
 __global__ void __launch_bounds__(256, 2)
-quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
+quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap rowmap,
+                const __grid_constant__ CUtensorMap colmap, const QuantParams p) {
+  using QC = QCfg<FMT>;
+  constexpr int Q_NST = QC::NST;
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* sc_all = sm + Q_NST * Q_STAGE;                                  // [2 parity][row, col][512]
-  float* part_all = reinterpret_cast<float*>(sm + Q_NST * Q_STAGE + 2048);  // [2 parity][4][128]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Q_NST * Q_STAGE + 2048 + 4096);
+  uint8_t* out_row = sm + QC::OFF_OUT;                                    // staged payload tiles
+  uint8_t* out_col = out_row + 16384;
+  uint8_t* sc_all = sm + QC::OFF_SC;                                      // [2 parity][row, col][512]
+  float* part_all = reinterpret_cast<float*>(sm + QC::OFF_SC + 2048);     // [2 parity][4][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + QC::OFF_SC + 2048 + 4096);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + Q_NST);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -167,6 +187,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
     const int vrows = (int)((p.rows - r0) < QT ? (p.rows - r0) : QT);
     const int vcols = (int)((p.cols - c0) < QT ? (p.cols - c0) : QT);
     const uint8_t* tile = sm + s * Q_STAGE;
+    if constexpr (QC::STAGED) {  // the previous tile's TMA stores have read the staging tiles
+      if (tid == 0) bulk_wait_read();
+      __syncthreads();
+    }
     uint8_t* sc_row = sc_all + (it & 1) * 1024;
     uint8_t* sc_col = sc_row + 512;
     float* part = part_all + (it & 1) * 512;
@@ -195,9 +219,14 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
           }
           uint32_t w[8];
           sb = quantize32<FMT, HAD>(v, amax, w);
-          uint8_t* dst = p.row_data + (int64_t)b * p.row_batch_stride + (r0 + r) * p.row_ld +
-                         (c0 + cb * 32) / 32 * BlockBytes<FMT>::value;
-          store_block<FMT>(dst, w);
+          if constexpr (QC::STAGED) {
+            *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            uint8_t* dst = p.row_data + (int64_t)b * p.row_batch_stride + (r0 + r) * p.row_ld +
+                           (c0 + cb * 32) / 32 * BlockBytes<FMT>::value;
+            store_block<FMT>(dst, w);
+          }
         }
         sc_row[(r & 31) * 16 + (r >> 5) * 4 + cb] = (uint8_t)sb;
       }
@@ -230,17 +259,30 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
           const uint32_t amax = (h ? (m2 >> 16) : (m2 & 0xFFFFu)) << 16;
           uint32_t w[8];
           sb = quantize32<FMT, HAD>(v, amax, w);
-          uint8_t* dst = p.col_data + (int64_t)b * p.col_batch_stride + (c0 + cc) * p.col_ld +
-                         (r0 + rb * 32) / 32 * BlockBytes<FMT>::value;
-          store_block<FMT>(dst, w);
+          if constexpr (QC::STAGED) {
+            *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          } else {
+            uint8_t* dst = p.col_data + (int64_t)b * p.col_batch_stride + (c0 + cc) * p.col_ld +
+                           (r0 + rb * 32) / 32 * BlockBytes<FMT>::value;
+            store_block<FMT>(dst, w);
+          }
         }
         if (COLSUM) part[rb * QT + cc] = sum;
         sc_col[(cc & 31) * 16 + (cc >> 5) * 4 + rb] = (uint8_t)sb;
       }
     }
-    __syncthreads();  // stage s fully read; chunks and partial sums complete
+    if constexpr (QC::STAGED) fence_proxy_async_smem();  // staging writes -> visible to the TMA store
+    __syncthreads();  // stage s fully read; staging, chunks and partial sums complete
 
-    if (tid == 0 && t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
+    if (tid == 0) {
+      if constexpr (QC::STAGED) {
+        if constexpr (ROW) tma_store_2d(&rowmap, out_row, (int)c0, (int)(b * p.rows + r0));
+        if constexpr (COL) tma_store_2d(&colmap, out_col, (int)r0, (int)(b * p.cols + c0));
+        bulk_commit();
+      }
+      if (t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
+    }
     if (tid < 32) {
       if constexpr (ROW) {
         const int64_t chunk = (r0 / 128) * ((p.cols / 32 + 3) / 4) + c0 / 128;
@@ -265,6 +307,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantParams p) {
       }
     }
   }
+  if (QC::STAGED && tid == 0) bulk_wait_all();  // this CTA's TMA stores have completed
   if (*abort_flag) {
     // a wait ran out: let every copy this CTA issued land before exiting
     if (tid == 0) {
@@ -336,15 +379,16 @@ cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t c
 template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
 static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStream_t s) {
   auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM>;
+  constexpr int smem = QCfg<FMT>::SMEM;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Q_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int64_t tiles = (int64_t)p.tiles_x * ((p.rows + QT - 1) / QT) * p.batch;
   const int64_t cap = 2ll * q.num_sms;
-  kern<<<(unsigned)(tiles < cap ? tiles : cap), 256, Q_SMEM, s>>>(q.xmap, p);
+  kern<<<(unsigned)(tiles < cap ? tiles : cap), 256, smem, s>>>(q.xmap, q.rowmap, q.colmap, p);
   return cudaGetLastError();
 }
 
