@@ -261,6 +261,8 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
   if (out.base) {
     if ((st = make_tmap_out(&to, out.base, out.rows, out.cols, out.ld)) != MX_OK) return st;
+  } else if (p.epi == mx::EPI_DSWIGLU) {  // the saved z [R, 2F], streamed by the epilogue
+    if ((st = make_tmap_bf16(&to, p.z, p.R, 2 * p.F, 2 * p.F)) != MX_OK) return st;
   } else {
     to = ta;
   }

@@ -11,7 +11,7 @@ template <int BN, int EPI, int MODE>
 static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE>;
-  constexpr int smem = Cfg<BN>::SMEM_BYTES;
+  constexpr int smem = Cfg<BN, EPI == EPI_DSWIGLU>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -20,7 +20,7 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, NUM_THREADS, smem, s>>>(ta, tb, to, p);
+  kern<<<(unsigned)grid, kThreads<EPI>(), smem, s>>>(ta, tb, to, p);
   return cudaGetLastError();
 }
 

@@ -41,12 +41,15 @@ static __device__ unsigned g_gemm_status = 0;
 
 constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
+// Threads of one CTA: the dSwiGLU epilogue adds a warp that streams the saved
+// pre-activation z into shared memory.
+template <int EPI> constexpr int kThreads() { return EPI == EPI_DSWIGLU ? NUM_THREADS + 32 : NUM_THREADS; }
 constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
 
-template <int BN>
+template <int BN, bool ZR = false>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 5;
+  static constexpr int STAGES = BN == 256 ? 4 : (ZR ? 4 : 5);
   static constexpr int ACC = BN == 256 ? 1 : 2;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -57,10 +60,15 @@ struct Cfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_TB = OFF_SF + STAGES * SF_BYTES;  // 8 x [32][17] fp32 transpose buffers
+  // ZR: a ring of two z slots, each [128 rows][64 cols] of gate and of up
+  // (BF16, 128-byte swizzle), one 64-column half of a tile per slot
+  static constexpr int Z_SLOT = 32768;
+  static constexpr int Z_SLOTS = ZR ? 2 : 0;
+  static constexpr int OFF_Z = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
   static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
   static constexpr int OFF_BAR = OFF_CHUNK + 4096;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ORDER = OFF_MISC + 16;              // wgrad: experts by descending size
   static constexpr int SMEM_BYTES = OFF_ORDER + 2 * MAX_SORTED_G + 1024;  // + slack for 1024-byte alignment
@@ -70,6 +78,7 @@ struct Cfg {
   static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "scale slots must fit");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(OFF_TB % 1024 == 0, "staging buffers must be swizzle-atom aligned");
+  static_assert(OFF_Z % 1024 == 0, "z slots must be swizzle-atom aligned");
 };
 
 struct Tile {
@@ -322,10 +331,11 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 // ---- the kernel ---------------------------------------------------------
 
 template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(kThreads<EPI>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
-  using C = Cfg<BN>;
+  constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
+  using C = Cfg<BN, ZR>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -334,12 +344,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint8_t* sSF = smem + C::OFF_SF;
   uint8_t* sTB = smem + C::OFF_TB;
   uint8_t* sChunk = smem + C::OFF_CHUNK;
+  uint8_t* sZ = smem + C::OFF_Z;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::ACC;
   uint64_t* final_bar = acc_empty + C::ACC;
   uint64_t* epi_bar = final_bar + 1;  // the 8 epilogue warps' own barrier
+  uint64_t* z_full = epi_bar + 1;     // ZR: slot loaded
+  uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by all 8 epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -350,6 +363,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 8); }
     mbar_init(final_bar, 1);
     mbar_init(epi_bar, 8);
+    for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], 8); }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -475,6 +489,35 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_commit(final_bar);
       mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ z loader (ZR)
+    // Streams the tile's saved pre-activation, one 64-column half (gate and
+    // up boxes) per slot, in the epilogue's tile order.
+    if (ZR && lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      int zs = 0;
+      uint32_t zph = 0;
+      int armed_parity[2] = {-1, -1};
+      bool ok = true;
+      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
+        const int64_t t = tile_index<MODE>(i);
+        if (t >= p.num_tiles) continue;
+        Tile T = get_tile<NT, MODE>(p, t, false, order);
+        if (!T.active || T.nk == 0) continue;
+        for (int hh = 0; hh < 2; hh++) {
+          if (!mbar_wait_bounded(&z_empty[zs], zph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          mbar_arrive_expect_tx(&z_full[zs], (uint32_t)C::Z_SLOT);
+          armed_parity[zs] = (int)zph;
+          uint8_t* dst = sZ + zs * C::Z_SLOT;
+          tma_load_2d(dst, &tmO, (int)(T.n0 + hh * 64), (int)T.m0, &z_full[zs], pol);
+          tma_load_2d(dst + C::Z_SLOT / 2, &tmO, (int)(p.F + T.n0 + hh * 64), (int)T.m0, &z_full[zs], pol);
+          if (++zs == 2) { zs = 0; zph ^= 1u; }
+        }
+      }
+      volatile int no_abort = 0;
+      for (int z = 0; z < 2; z++)
+        if (armed_parity[z] >= 0) mbar_wait_bounded(&z_full[z], (uint32_t)armed_parity[z], &no_abort, WAIT_BUDGET_NS);
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;       // 0..7
@@ -485,6 +528,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t epi_phase = 0;
+    int zslot = 0;           // ZR: next z slot and its phase
+    uint32_t zphase = 0;
     // Barrier among the epilogue warps, bounded like every other wait.
     auto epi_sync = [&]() -> bool {
       __syncwarp();
@@ -493,21 +538,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       epi_phase ^= 1u;
       return ok;
     };
-    // dSwiGLU / dGELU read a saved activation per tile: prefetch a tile's
-    // rows into L2 one tile ahead of its epilogue.
+    // dGELU reads a saved activation per tile: prefetch a tile's rows into
+    // L2 one tile ahead of its epilogue (dSwiGLU streams z through shared
+    // memory instead).
     auto prefetch_aux = [&](int64_t i) {
-      if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_DGELU) {
+      if constexpr (EPI == EPI_DGELU) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) return;
         const Tile U = get_tile<NT, MODE>(p, t, false, order);
         if (!U.active || U.nk == 0) return;
         const int64_t r = U.m0 + q * 32 + lane;
-        if (EPI == EPI_DSWIGLU) {
-          prefetch_l2(p.z + r * (2 * p.F) + U.n0 + half * 64);
-          prefetch_l2(p.z + r * (2 * p.F) + p.F + U.n0 + half * 64);
-        } else {
-          prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
-        }
+        prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
       }
     };
     prefetch_aux(0);
@@ -634,24 +675,35 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (!epi_sync()) break;
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        // accumulator columns [0,128): dh for f0..f0+127
+        // accumulator columns [0,128): dh for f0..f0+127.  The tile is taken
+        // in two 64-column halves, one z slot each; warp (q, half) handles
+        // columns hh*64 + half*32 .. +31 of half hh for its 32 rows.
         const int64_t row = T.m0 + row_in_tile;
         const int64_t f0 = T.n0;
-        const uint16_t* zr = p.z + row * (2 * p.F);
         uint8_t* ch_gr = sChunk;
         uint8_t* ch_ur = sChunk + 512;
         uint8_t* ch_gc = sChunk + 1024;
         uint8_t* ch_uc = sChunk + 1536;
+        const int zrow = q * 32 + lane;
+        bool zok = true;
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ch++) {
-          const int fc = half * 64 + ch * 32;  // tile-local column of this chunk
+        for (int hh = 0; hh < 2; hh++) {
+          const int fc = hh * 64 + half * 32;  // tile-local column of this chunk
           uint32_t dh[32];
           tmem_ld32(tbase + fc, dh);
+          if (!mbar_wait_bounded(&z_full[zslot], zphase, abort_flag, WAIT_BUDGET_NS)) { zok = false; break; }
+          const uint8_t* grow = sZ + zslot * C::Z_SLOT + zrow * 128;
+          const uint8_t* urow = grow + C::Z_SLOT / 2;
           uint4 zgw[4], zuw[4];
-          const uint4* zgp = reinterpret_cast<const uint4*>(zr + f0 + fc);
-          const uint4* zup = reinterpret_cast<const uint4*>(zr + p.F + f0 + fc);
 #pragma unroll
-          for (int i = 0; i < 4; i++) { zgw[i] = zgp[i]; zuw[i] = zup[i]; }
+          for (int i = 0; i < 4; i++) {
+            const int off = ((half * 4 + i) ^ (zrow & 7)) << 4;  // 128-byte swizzle
+            zgw[i] = *reinterpret_cast<const uint4*>(grow + off);
+            zuw[i] = *reinterpret_cast<const uint4*>(urow + off);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&z_empty[zslot]);
+          if (++zslot == 2) { zslot = 0; zphase ^= 1u; }
           tmem_wait_ld();
           float dg[32], du[32];
 #pragma unroll
@@ -682,6 +734,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ch_gr[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbg;
           ch_ur[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbu;
         }
+        if (!zok) break;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);
