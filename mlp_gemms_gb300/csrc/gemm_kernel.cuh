@@ -187,10 +187,7 @@ __device__ __forceinline__ void stage_reuse_wait(int lane) {
 
 // Rowwise E4M3 requant of 32 fp32 values held by one thread.
 __device__ __forceinline__ uint32_t row_quant_store_e4m3(float (&v)[32], uint8_t* dst) {
-  uint32_t amax = 0;
-#pragma unroll
-  for (int i = 0; i < 32; i++) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-  uint32_t sb = rceil_scale_byte<E4M3>(amax);
+  uint32_t sb = rceil_scale_byte<E4M3>(amax_abs_bits<32>(v));
   uint32_t w[8];
   quantize_block_words<E4M3>(v, sb, w);
   reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -223,10 +220,7 @@ __device__ __forceinline__ float dgelu_tanh_f(float x) {
 template <int QF, bool QH>
 __device__ __forceinline__ uint32_t row_quant_store(float (&v)[32], uint8_t* dst) {
   if constexpr (QH) hadamard32(v);
-  uint32_t amax = 0;
-#pragma unroll
-  for (int i = 0; i < 32; i++) amax = max(amax, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-  const uint32_t sb = rceil_scale_byte<QF>(amax);
+  const uint32_t sb = rceil_scale_byte<QF>(amax_abs_bits<32>(v));
   uint32_t w[8];
   quantize_block_words<QF>(v, sb, w);
   if constexpr (QF == E4M3) {
@@ -281,9 +275,7 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 #pragma unroll
     for (int i = 0; i < 16; i++) x[i] = __fmul_rn(x[i], __uint_as_float(0x3E3504F3u));
   }
-  uint32_t amax = 0;
-#pragma unroll
-  for (int i = 0; i < 16; i++) amax = max(amax, __float_as_uint(x[i]) & 0x7FFFFFFFu);
+  uint32_t amax = amax_abs_bits<16>(x);
   amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   const uint32_t sb = rceil_scale_byte<QF>(amax);
   uint8_t* dst = q_col + (col0 + c) * col_ld + row_byte0 + hh * (BlockBytes<QF>::value / 2);
@@ -293,9 +285,7 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
     else if constexpr (QF == E2M1) reinterpret_cast<uint2*>(dst)[0] = make_uint2(nw, nw);
     else { uint32_t* d = reinterpret_cast<uint32_t*>(dst); d[0] = nw; d[1] = nw; d[2] = nw; }
   } else {
-    const float s = inv_scale_from_byte(sb);
-#pragma unroll
-    for (int i = 0; i < 16; i++) x[i] = x[i] * s;
+    scale_values<16>(x, inv_scale_from_byte(sb));
     if constexpr (QF == E4M3) {
       uint32_t w[4];
 #pragma unroll

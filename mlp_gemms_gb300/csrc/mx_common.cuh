@@ -132,6 +132,42 @@ __device__ __forceinline__ void pack_block(const float (&v)[32], uint32_t (&w)[8
 template <int FMT>
 __device__ __forceinline__ uint32_t nan_block_word() { return FMT == E4M3 ? 0x7F7F7F7Fu : 0u; }
 
+// max(|a|, |b|) in magnitude (the sign bit is meaningless), NaN if either is.
+__device__ __forceinline__ float max_abs_nan(float a, float b) {
+  float d;
+  asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// fp32 bits of max |v[i]| over N values (a power of two), by a pairwise tree;
+// any NaN gives a larger-than-Inf pattern, as rceil_scale_byte expects.
+template <int N>
+__device__ __forceinline__ uint32_t amax_abs_bits(const float* v) {
+  float t[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; i++) t[i] = max_abs_nan(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = N / 4; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; i++) t[i] = max_abs_nan(t[i], t[i + w]);
+  }
+  return __float_as_uint(t[0]) & 0x7FFFFFFFu;
+}
+
+// v[i] *= s for N (even) values, two lanes per instruction (each lane an
+// ordinary round-to-nearest fp32 product).
+template <int N>
+__device__ __forceinline__ void scale_values(float* v, float s) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    uint64_t p, q;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(v[i]), "f"(v[i + 1]));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(q) : "f"(s));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(p) : "l"(q));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v[i]), "=f"(v[i + 1]) : "l"(p));
+  }
+}
+
 // Scale (by 2^-e) and pack one block whose scale byte is `sb`.
 template <int FMT>
 __device__ __forceinline__ void quantize_block_words(float (&v)[32], uint32_t sb, uint32_t (&w)[8]) {
@@ -140,9 +176,7 @@ __device__ __forceinline__ void quantize_block_words(float (&v)[32], uint32_t sb
     for (int i = 0; i < 8; i++) w[i] = nan_block_word<FMT>();
     return;
   }
-  float s = inv_scale_from_byte(sb);
-#pragma unroll
-  for (int i = 0; i < 32; i++) v[i] = v[i] * s;
+  scale_values<32>(v, inv_scale_from_byte(sb));
   pack_block<FMT>(v, w);
 }
 
