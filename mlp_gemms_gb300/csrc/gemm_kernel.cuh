@@ -187,7 +187,7 @@ __device__ __forceinline__ void stage_reuse_wait(int lane) {
 
 // Rowwise E4M3 requant of 32 fp32 values held by one thread.
 __device__ __forceinline__ uint32_t row_quant_store_e4m3(float (&v)[32], uint8_t* dst) {
-  uint32_t sb = rceil_scale_byte<E4M3>(amax_abs_bits<32>(v));
+  uint32_t sb = rceil_scale_byte_sel<E4M3>(amax_abs_bits<32>(v));
   uint32_t w[8];
   quantize_block_words<E4M3>(v, sb, w);
   reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -220,7 +220,7 @@ __device__ __forceinline__ float dgelu_tanh_f(float x) {
 template <int QF, bool QH>
 __device__ __forceinline__ uint32_t row_quant_store(float (&v)[32], uint8_t* dst) {
   if constexpr (QH) hadamard32(v);
-  const uint32_t sb = rceil_scale_byte<QF>(amax_abs_bits<32>(v));
+  const uint32_t sb = rceil_scale_byte_sel<QF>(amax_abs_bits<32>(v));
   uint32_t w[8];
   quantize_block_words<QF>(v, sb, w);
   if constexpr (QF == E4M3) {
@@ -277,7 +277,7 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
   }
   uint32_t amax = amax_abs_bits<16>(x);
   amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  const uint32_t sb = rceil_scale_byte<QF>(amax);
+  const uint32_t sb = rceil_scale_byte_sel<QF>(amax);
   uint8_t* dst = q_col + (col0 + c) * col_ld + row_byte0 + hh * (BlockBytes<QF>::value / 2);
   if (sb == 0xFFu) {
     const uint32_t nw = nan_block_word<QF>();

@@ -58,6 +58,22 @@ __device__ __forceinline__ uint32_t rceil_scale_byte(uint32_t amax_bits) {
   return (uint32_t)(e + 127);
 }
 
+// The same byte as rceil_scale_byte: as a biased byte the scale is the
+// biased exponent field minus E_x plus the carry, clamped to [0, 254].
+// Zero and fp32 subnormals land below 0 for every format here (E_x >= 2),
+// so the clamp gives them byte 0; +Inf gives 0xFE and NaN 0xFF.  Written
+// without branches (selects only).  Measured on GB300: faster in the GEMM
+// epilogues, which interleave many independent blocks per thread; slower
+// in the quantizer kernel, which keeps rceil_scale_byte.
+template <int FMT>
+__device__ __forceinline__ uint32_t rceil_scale_byte_sel(uint32_t amax_bits) {
+  static_assert(FmtMax<FMT>::E >= 2, "zero/subnormal amax must clamp to byte 0");
+  int b = (int)(amax_bits >> 23) - FmtMax<FMT>::E + ((amax_bits & 0x7FFFFFu) > FmtMax<FMT>::M ? 1 : 0);
+  b = b < 0 ? 0 : (b > 254 ? 254 : b);
+  const uint32_t special = amax_bits == 0x7F800000u ? 0xFEu : 0xFFu;
+  return amax_bits >= 0x7F800000u ? special : (uint32_t)b;
+}
+
 // 2^-(b-127) as an fp32 multiplier for scale byte b in [0, 254].
 __device__ __forceinline__ float inv_scale_from_byte(uint32_t b) {
   int neg_e = 127 - (int)b;                    // -e in [-127, 127]
