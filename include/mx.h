@@ -334,6 +334,24 @@ MX_API mx_status_t mx_get_device_status(mx_stream_t stream);
  */
 MX_API mx_status_t mx_selftest_bounded_wait(uint64_t budget_ns, mx_stream_t stream);
 
+/*
+ * mx_debug_tap -- test instrument, not part of the method.  While attached
+ * (tap_f32 != NULL) on the calling host thread, every fused-requant
+ * epilogue (mx_grouped_gemm_swiglu_fwd: h [R, F]; mx_grouped_gemm_dswiglu_bwd:
+ * dz = [dg | du] [R, 2F]; mx_gemm_gelu_fwd: act [M, H]; mx_gemm_dgelu_bwd:
+ * dpre [M, H]) also writes the fp32 values it is about to quantize, row-major,
+ * before any rotation.  Quantizing those values exactly must reproduce the
+ * epilogue's payload and scale bytes bit for bit, which is how the tests
+ * check the fused requant on random data.  Rows of empty tiles are not
+ * written.
+ *   tap_f32  device fp32 buffer of `elems` floats, 16-byte aligned, owned by
+ *            the caller; NULL detaches
+ *   elems    capacity; a fused call whose output is larger fails with
+ *            MX_ERR_SHAPE before launching
+ * Costs one store per value when attached; nothing when detached.
+ */
+MX_API mx_status_t mx_debug_tap(float *tap_f32, int64_t elems);
+
 #ifdef __cplusplus
 }
 #endif

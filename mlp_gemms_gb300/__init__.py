@@ -32,7 +32,7 @@ ABI_SYMBOLS = (
     "mx_quantize_workspace_bytes", "mx_quantize", "mx_grouped_gemm", "mx_grouped_gemm_swiglu_fwd",
     "mx_grouped_gemm_dswiglu_bwd", "mx_grouped_gemm_wgrad", "mx_mlp_workspace_bytes", "mx_mlp_fwd_bwd",
     "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
-    "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc",
+    "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
 )
 
 
@@ -93,6 +93,7 @@ def load(path=None):
         "mx_gemm_dgelu_workspace_bytes": (sz, [i64, i64]),
         "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
         "mx_quantize_colsum_noalloc": (ctypes.c_int, [vp, i64, i64, i64, i32, u32, tp, tp, vp, vp]),
+        "mx_debug_tap": (ctypes.c_int, [vp, i64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -327,6 +328,18 @@ def mx_get_device_status(stream=None):
 
 def mx_selftest_bounded_wait(budget_ns, stream=None):
     _check(load().mx_selftest_bounded_wait(int(budget_ns), _stream(stream)))
+
+
+def mx_debug_tap(tap=None):
+    """Attach (fp32 CUDA tensor) or detach (None) the fused epilogues' test
+    tap on this host thread: they also write their fp32 pre-quantization
+    values into it, row-major [rows, cols] of the requantized output."""
+    if tap is None:
+        _check(load().mx_debug_tap(None, 0))
+        return
+    import torch
+    assert tap.dtype == torch.float32 and tap.is_cuda and tap.is_contiguous()
+    _check(load().mx_debug_tap(tap.data_ptr(), tap.numel()))
 
 
 def mx_last_error():

@@ -246,6 +246,19 @@ uint32_t stage_tx_bytes(int fmt, int bn) {
   return (128u + (uint32_t)bn) * row + 512u + (uint32_t)(bn / 128) * 512u;
 }
 
+// Test instrument (mx_debug_tap): where the fused epilogues also write
+// their fp32 pre-quantization values, per calling thread.
+thread_local float* g_tap = nullptr;
+thread_local int64_t g_tap_elems = 0;
+
+mx_status_t attach_tap(mx::GemmParams* p, int64_t rows, int64_t cols) {
+  if (g_tap == nullptr) return MX_OK;
+  MX_CHECK(g_tap_elems >= rows * cols, MX_ERR_SHAPE, "debug tap holds %lld floats, the epilogue writes %lld",
+           (long long)g_tap_elems, (long long)(rows * cols));
+  p->tap = g_tap;
+  return MX_OK;
+}
+
 // A BF16 output the epilogue writes with TMA stores (base NULL: none).
 struct OutView {
   const void* base;
@@ -480,6 +493,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   p.q_row = static_cast<uint8_t*>(h_row->data); p.q_row_scale = h_row->scale;
   p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
   p.q_cols = F;
+  if ((st = attach_tap(&p, R, F)) != MX_OK) return st;
   return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F});
 }
 
@@ -524,6 +538,7 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   p.q_row = static_cast<uint8_t*>(dz_row->data); p.q_row_scale = dz_row->scale;
   p.q_col = static_cast<uint8_t*>(dz_col->data); p.q_col_scale = dz_col->scale;
   p.q_cols = 2 * F;
+  if ((st = attach_tap(&p, R, 2 * F)) != MX_OK) return st;
   return run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0});
 }
 
@@ -663,6 +678,7 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
   } else {
     to = ta;
   }
+  if ((st = attach_tap(&p, p.R, p.q_cols)) != MX_OK) return st;
   cudaError_t e = mx::launch_gemm_dense(p, ta, tb, to, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
   return MX_OK;
@@ -869,6 +885,14 @@ mx_status_t mx_get_device_status(mx_stream_t stream) {
   word |= dense | quant;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
+  return MX_OK;
+}
+
+mx_status_t mx_debug_tap(float* tap_f32, int64_t elems) {
+  MX_CHECK(tap_f32 == nullptr || (aligned16(tap_f32) && elems >= 0), MX_ERR_ALIGNMENT,
+           "debug tap must be a 16-byte aligned pointer");
+  g_tap = tap_f32;
+  g_tap_elems = tap_f32 ? elems : 0;
   return MX_OK;
 }
 

@@ -7,10 +7,10 @@
 
 namespace mx {
 
-template <int BN, int EPI, int MODE>
+template <int BN, int EPI, int MODE, bool TAP = false>
 static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
-  auto kern = mx_gemm_kernel<BN, EPI, MODE>;
+  auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, TAP>;
   constexpr int smem = Cfg<BN, EPI == EPI_DSWIGLU>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
   if (!configured) {
@@ -27,7 +27,10 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                         int bn, cudaStream_t s, int num_sms) {
   if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
-  if (p.epi == EPI_DSWIGLU) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+  if (p.epi == EPI_DSWIGLU) {
+    if (p.tap != nullptr) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms);
+    return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+  }
   if (p.mode == MODE_WGRAD) {
     if (bn == 128) return launch_one<128, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
     return launch_one<256, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);

@@ -179,6 +179,14 @@ __device__ __forceinline__ void store_bf16_block(const float* v, uint8_t* stage,
   }
 }
 
+// Test instrument: this lane's 32 fp32 pre-quantization values of one row
+// (columns col0..col0+31) into the tap [rows, ld] when one is attached.
+__device__ __forceinline__ void tap_store32(float* tap, int64_t ld, int64_t row, int64_t col0, const float* v) {
+  float4* d = reinterpret_cast<float4*>(tap + row * ld + col0);
+#pragma unroll
+  for (int i = 0; i < 8; i++) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
 // Before a warp rewrites its staging buffer: the previous TMA store has read it.
 __device__ __forceinline__ void stage_reuse_wait(int lane) {
   if (lane == 0) bulk_wait_read();
@@ -320,11 +328,15 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 
 // ---- the kernel ---------------------------------------------------------
 
-template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false>
+// TAP: the dSwiGLU kernel has a separate instantiation that writes the
+// debug tap (its register budget is tight); the other fused epilogues test
+// the tap pointer at run time.
+template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool TAP = false>
 __global__ void __launch_bounds__(kThreads<EPI>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
+  constexpr bool TAP_ON = EPI != EPI_DSWIGLU || TAP;
   using C = Cfg<BN, ZR>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -635,6 +647,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             h[i][j] = g * sigmoidf_(g) * u;
           }
         }
+        if (p.tap != nullptr) {
+#pragma unroll
+          for (int i = 0; i < 2; i++) tap_store32(p.tap, p.q_cols, row, f0 + half * 64 + 32 * i, h[i]);
+        }
         uint8_t* chunk_row = sChunk;
         uint8_t* chunk_col = sChunk + 512;
         // rowwise: two thread-local 32-column blocks
@@ -710,6 +726,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               dg[j] = d * u * s * (1.0f + g * (1.0f - s));
               du[j] = d * g * s;
             }
+          }
+          if (TAP_ON && p.tap != nullptr) {
+            tap_store32(p.tap, p.q_cols, row, f0 + fc, dg);
+            tap_store32(p.tap, p.q_cols, row, p.F + f0 + fc, du);
           }
           // columnwise first (the rowwise packer scales its input in place)
 #pragma unroll
@@ -793,6 +813,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               if (lane == 0) part[q * 128 + fc + j] = sum;
             }
           }
+          if (p.tap != nullptr) tap_store32(p.tap, p.q_cols, row, n0 + fc, val);
           // columnwise first (the rowwise packer rotates and scales in place)
 #pragma unroll
           for (int k = 0; k < 2; k++)

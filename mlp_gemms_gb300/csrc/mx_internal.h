@@ -71,6 +71,7 @@ struct GemmParams {
   int q_fmt, q_had;         // requant element format and rotation (GELU / dGELU)
   const uint16_t* bias;     // BF16 [N] added to the fp32 accumulator, or null
   float* colsum_partials;   // dGELU: fp32 [ceil(R/128), C] per-tile column sums
+  float* tap;               // test instrument: fused epilogues' fp32 pre-quant values [R, C], or null
 };
 
 // ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte

@@ -55,3 +55,36 @@ def requant_close(gpu, ref, rows, cols, fmt=O.E4M3, max_step_frac=1e-2):
     frac = float(np.mean(gp != rp))
     assert frac <= max_step_frac, "requant code mismatch fraction %.4f" % frac
     return frac
+
+
+def assert_tap_requant_exact(gpu_row, gpu_col, tap, rows, cols, R, fmt=O.E4M3, had=False, what="tap"):
+    """The fused epilogue's own fp32 values (the debug tap, [rows, cols])
+    quantized by the oracle must give the epilogue's row and column bytes
+    exactly.  gpu_row is [R, cols] and gpu_col [cols, R] with R >= rows; only
+    the first `rows` rows (a multiple of 128) are compared."""
+    x = np.asarray(tap[:rows], dtype=np.float64)
+    rp, rs = O.quantize_rows(x, fmt, had)
+    gp, gs = mx_bytes(gpu_row)
+    assert np.array_equal(gp[:rows], rp), "%s rowwise payload differs in %d bytes" % (
+        what, int((gp[:rows] != rp).sum()))
+    assert np.array_equal(gs[:rs.size], rs), "%s rowwise scales differ" % what
+    cp_ref, cs_ref = O.quantize_cols(x, fmt, had)
+    cp, cs = mx_bytes(gpu_col)
+    pb = O.payload_row_bytes(rows, fmt)
+    assert np.array_equal(cp[:, :pb], cp_ref), "%s columnwise payload differs in %d bytes" % (
+        what, int((cp[:, :pb] != cp_ref).sum()))
+    got_s = O.scales_to_matrix(cs, cols, R // 32)[:, :rows // 32]
+    assert np.array_equal(got_s, O.scales_to_matrix(cs_ref, cols, rows // 32)), "%s columnwise scales differ" % what
+
+
+def with_tap(mx, rows, cols, fn):
+    """Run fn with a NaN-filled fp32 debug tap [rows, cols] attached; returns
+    (fn's result, the tap as float32 numpy)."""
+    import torch
+    tap = torch.full((rows, cols), float("nan"), dtype=torch.float32, device="cuda")
+    mx.mx_debug_tap(tap)
+    try:
+        out = fn()
+    finally:
+        mx.mx_debug_tap(None)
+    return out, tap.cpu().numpy()

@@ -4,7 +4,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from helpers import assert_quant_equal, bf16_cpu, mx_bytes, requant_close, to_dev
+from helpers import assert_quant_equal, assert_tap_requant_exact, bf16_cpu, mx_bytes, requant_close, to_dev, with_tap
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +72,37 @@ def test_dgelu_bwd(cuda_lib, fmt, had):
     requant_close(mx_bytes(dpre_col), ref["dpre_col"], H, M, fmt)
     got = db1.cpu().numpy().astype(np.float64)
     assert O.within_tolerance(got[None, :], ref["db1"][None, :]).all()
+
+
+@pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E4M3, False)])
+def test_gelu_and_dgelu_tap_requant_bit_exact(cuda_lib, fmt, had):
+    """Random inputs: the GELU activation and the dGELU pre-activation
+    gradient as the epilogues computed them in fp32 (debug tap, before the
+    rotation), quantized by the oracle (its fp32 rotation sequence), give the
+    epilogues' row and column bytes bit for bit."""
+    rng = np.random.default_rng(53)
+    M, D, H = 512, 384, 256
+    xb, w1b = W.normal_bf16(rng, (M, D)), W.normal_bf16(rng, (H, D), std=0.05)
+    b1 = W.normal_bf16(rng, (H,), std=0.02)
+    xr, _, xref = _q(cuda_lib, xb, fmt, had, col=False)
+    wr, _, wref = _q(cuda_lib, w1b, fmt, had, col=False)
+    (pre, act_row, act_col), tap = with_tap(
+        cuda_lib, M, H, lambda: cuda_lib.mx_gemm_gelu_fwd(xr, wr, to_dev(b1), fmt=fmt, hadamard=had))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(act_row, act_col, tap, M, H, M, fmt, had, what="act")
+    ref = O.gelu_fwd(_dq((xref["row_payload"], xref["row_scales"]), M, D, fmt),
+                     _dq((wref["row_payload"], wref["row_scales"]), H, D, fmt), O.bf16_to_f64(b1), fmt, had)
+    assert O.within_tolerance(tap.astype(np.float64), ref["act"]).all()
+
+    dyb = W.normal_bf16(rng, (M, D), std=1e-3)
+    w2t = W.normal_bf16(rng, (H, D), std=0.02)
+    pre_b = W.normal_bf16(rng, (M, H), std=1.5)
+    dyr, _, _ = _q(cuda_lib, dyb, fmt, had, col=False)
+    w2r, _, _ = _q(cuda_lib, w2t, fmt, had, col=False)
+    (dpre_row, dpre_col, _), tap2 = with_tap(
+        cuda_lib, M, H, lambda: cuda_lib.mx_gemm_dgelu_bwd(dyr, w2r, to_dev(pre_b), fmt=fmt, hadamard=had))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(dpre_row, dpre_col, tap2, M, H, M, fmt, had, what="dpre")
 
 
 def test_dense_gelu_step_against_oracle_chain(cuda_lib):

@@ -6,7 +6,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from helpers import assert_quant_equal, bf16_cpu, mx_bytes, requant_close, to_dev
+from helpers import assert_quant_equal, assert_tap_requant_exact, bf16_cpu, mx_bytes, requant_close, to_dev, with_tap
 
 pytestmark = pytest.mark.gpu
 
@@ -228,6 +228,54 @@ def test_dswiglu_bwd_exact_product_bit_exact(cuda_lib):
     ref = O.dswiglu_bwd(dyd, w2td, zb, offsets)
     assert_quant_equal(dz_row, ref["dz_row"], R, 2 * F // 32, "dz_row")
     assert_quant_equal(dz_col, ref["dz_col"], 2 * F, R // 32, "dz_col")
+
+
+def test_swiglu_fwd_tap_requant_bit_exact(cuda_lib):
+    """Random inputs: the epilogue's own fp32 h (debug tap), quantized by the
+    oracle, gives h_row and h_col bit for bit; the tap is the oracle's h
+    within the GEMM tolerance and the inactive tail rows are never written."""
+    import torch
+    G, D, F, R, offsets, inp = _moe_small(seed=3)
+    A = int(offsets[-1])
+    xr, _, xref = _quant_both(cuda_lib, inp["x"])
+    wr, _, wref = _quant_both(cuda_lib, inp["w1"])
+    offs = torch.from_numpy(offsets).cuda()
+    (z, h_row, h_col), tap = with_tap(cuda_lib, R, F, lambda: cuda_lib.mx_grouped_gemm_swiglu_fwd(xr, wr, G, offs))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(h_row, h_col, tap, A, F, R, what="h")
+    assert np.all(np.isnan(tap[A:])), "tail rows of the tap were written"
+    x = _deq(xref["row_payload"], xref["row_scales"], R, D)
+    w = _deq(wref["row_payload"], wref["row_scales"], G * 2 * F, D).reshape(G, 2 * F, D)
+    ref = O.swiglu_fwd(x, w, offsets)
+    assert O.within_tolerance(tap[:A].astype(np.float64), ref["h"]).all()
+
+
+def test_dswiglu_bwd_tap_requant_bit_exact_and_gate_up_swap_fails(cuda_lib):
+    """Random inputs: the epilogue's fp32 dz = [dg | du] (debug tap) quantized
+    by the oracle gives dz_row and dz_col bit for bit, and matches the
+    oracle's dz within tolerance.  Negative control: the oracle with gate and
+    up swapped in z must not match."""
+    import torch
+    G, D, F, R, offsets, inp = _moe_small(seed=4)
+    A = int(offsets[-1])
+    dyr, _, dyref = _quant_both(cuda_lib, inp["dy"])
+    w2t_bits = np.ascontiguousarray(np.transpose(inp["w2"], (0, 2, 1)))
+    w2tr, _, wref = _quant_both(cuda_lib, w2t_bits)
+    zb = W.normal_bf16(np.random.default_rng(6), (R, 2 * F), std=2.0)
+    offs = torch.from_numpy(offsets).cuda()
+    (dz_row, dz_col), tap = with_tap(cuda_lib, R, 2 * F,
+                                     lambda: cuda_lib.mx_grouped_gemm_dswiglu_bwd(dyr, w2tr, to_dev(zb), G, offs))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(dz_row, dz_col, tap, A, 2 * F, R, what="dz")
+    assert np.all(np.isnan(tap[A:]))
+    dy = _deq(dyref["row_payload"], dyref["row_scales"], R, D)
+    w2t = _deq(wref["row_payload"], wref["row_scales"], G * F, D).reshape(G, F, D)
+    ref = O.dswiglu_bwd(dy, w2t, zb, offsets)
+    got = tap[:A].astype(np.float64)
+    assert O.within_tolerance(got, ref["dz"]).all()
+    swapped = np.ascontiguousarray(np.concatenate([zb[:, F:], zb[:, :F]], axis=1))
+    bad = O.dswiglu_bwd(dy, w2t, swapped, offsets)
+    assert np.mean(O.within_tolerance(got, bad["dz"])) < 0.5, "gate/up swap went unnoticed"
 
 
 def test_mlp_step_against_oracle_chain(cuda_lib):

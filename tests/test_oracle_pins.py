@@ -131,6 +131,27 @@ def test_scaled_block_never_exceeds_element_max(fmt):
         assert np.all(np.abs(dec) <= emax)
 
 
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_floor_scale_negative_control(fmt):
+    """Negative control: a FLOOR scale (one below RCEIL whenever amax/emax is
+    not a power of two) must break the round-up invariant on most blocks and
+    give different scale bytes from the oracle's, so a kernel computing FLOOR
+    scales could not pass the byte gates."""
+    rng = np.random.default_rng(11)
+    emax = O.fmt_max(fmt)
+    exceed = differ = 0
+    n = 300
+    for _ in range(n):
+        x = W.bf16_bits_to_f32(W.to_bf16_bits(
+            (rng.standard_normal(32) * 2.0 ** rng.uniform(-20, 20)).astype(np.float32))).astype(np.float64)
+        amax = float(np.max(np.abs(x)))
+        e_rceil = O.scale_byte(amax, fmt) - 127
+        e_floor = e_rceil - (0 if amax == emax * 2.0 ** e_rceil else 1)
+        exceed += bool(amax * 2.0 ** (-e_floor) > emax)
+        differ += e_floor != e_rceil
+    assert exceed > 0.9 * n and differ > 0.9 * n
+
+
 def test_specials_policy():
     z = np.zeros(32)
     sb, codes = O.quantize_block(z, O.E4M3)

@@ -41,6 +41,36 @@ def test_every_bf16_pattern(cuda_lib, fmt):
         assert_quant_equal(xc, (ref["col_payload"], ref["col_scales"]), 256, 8, "col")
 
 
+def test_negative_controls_flipped_byte_and_floor_scales(cuda_lib):
+    """The byte gate must catch one flipped scale byte and one flipped payload
+    byte planted in the oracle's reference, and the GPU's scales must differ
+    from FLOOR scales (derived from the oracle's) on most blocks while
+    equalling RCEIL exactly."""
+    rows, cols = 256, 256
+    bits = W.quantizer_input(rows, cols, seed=9, special_frac=0.0)
+    xr, _, _ = _run(cuda_lib, bits, O.E4M3, True, False)
+    ref = O.quantize_bf16(bits, O.E4M3, True, False)
+    good = (ref["row_payload"], ref["row_scales"])
+    assert_quant_equal(xr, good, rows, cols // 32, "row")
+    bad_scale = ref["row_scales"].copy()
+    bad_scale[O.blocked_offset(5, 3, cols // 32)] ^= 1
+    with pytest.raises(AssertionError):
+        assert_quant_equal(xr, (ref["row_payload"], bad_scale), rows, cols // 32, "row")
+    bad_payload = ref["row_payload"].copy()
+    bad_payload[17, 33] ^= 0x01
+    with pytest.raises(AssertionError):
+        assert_quant_equal(xr, (bad_payload, ref["row_scales"]), rows, cols // 32, "row")
+    x = O.bf16_to_f64(bits)
+    amax = np.max(np.abs(x.reshape(rows, cols // 32, 32)), axis=2)
+    emax = O.fmt_max(O.E4M3)
+    rceil = np.vectorize(lambda a: O.scale_byte(a, O.E4M3))(amax)
+    exact_pow = amax == emax * 2.0 ** (rceil.astype(np.float64) - 127)
+    floor = rceil - (~exact_pow).astype(rceil.dtype)
+    got = O.scales_to_matrix(xr.scale.cpu().numpy(), rows, cols // 32)
+    assert np.array_equal(got, rceil)
+    assert np.mean(got != floor) > 0.9
+
+
 def test_rowwise_only_and_colwise_only(cuda_lib):
     bits = W.quantizer_input(160, 256, seed=5, special_frac=0.01)
     xr, xc, _ = _run(cuda_lib, bits, O.E4M3, True, False)
