@@ -319,6 +319,52 @@ MX_API size_t mx_mlp_workspace_bytes(const mx_mlp_args_t *args);
 MX_API mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t *args, mx_stream_t stream);
 
 /*
+ * Host-buffer pipeline of the step.  A runtime convenience for callers whose
+ * tensors live in host memory; the pages' kernels have no counterpart (they
+ * take device tensors).  Each mx_mlp_pipeline_run enqueues one step of
+ * mx_mlp_fwd_bwd whose inputs (x, w1, w2, dy, the routing offsets, and b1, b2
+ * for GELU) are copied from host memory and whose outputs (y, dx, dw1, dw2,
+ * and db1, db2 for GELU) are copied back, with the two copy directions on
+ * streams of their own: the next step's input copy starts as soon as this
+ * step's only reader of that input has run, an output's copy back starts as
+ * soon as its writer has run, and the next step's writer waits for that copy.
+ * Consecutive runs therefore overlap host traffic in both directions with
+ * the kernels, using one device buffer per tensor.
+ *
+ * mx_mlp_pipeline_create
+ *   dev     device buffers and workspace exactly as for mx_mlp_fwd_bwd
+ *           (validated here; the pointed-to arrays are staging buffers the
+ *           pipeline overwrites; dev->offsets receives each step's routing);
+ *           copied, the caller keeps ownership of every buffer
+ *   stream  the stream the step's kernels run on
+ *   out     receives the pipeline; creates two copy streams and events, no
+ *           device memory
+ * mx_mlp_pipeline_run
+ *   io      host pointers, same shapes and element types as the device
+ *           tensors (BF16, fp32 for db1/db2, int32 offsets [G]); pinned host
+ *           memory is needed for the copies to run asynchronously.  Host
+ *           buffers are read and written after the call returns: keep them
+ *           alive and unchanged (inputs) or unread (outputs) until
+ *           mx_mlp_pipeline_sync.  Returns MX_ERR_INVALID_ARG for a missing
+ *           host buffer, MX_ERR_CUDA if enqueuing failed (later runs then
+ *           fail too).
+ * mx_mlp_pipeline_sync     wait for every enqueued step, copies included
+ * mx_mlp_pipeline_destroy  sync, then release streams and events
+ */
+typedef struct mx_mlp_pipeline mx_mlp_pipeline_t;
+typedef struct {
+  const void *x, *w1, *w2, *dy, *b1, *b2;
+  const int32_t *offsets;
+  void *y, *dx, *dw1, *dw2;
+  float *db1, *db2;
+} mx_mlp_host_io_t;
+
+MX_API mx_status_t mx_mlp_pipeline_create(const mx_mlp_args_t *dev, mx_stream_t stream, mx_mlp_pipeline_t **out);
+MX_API mx_status_t mx_mlp_pipeline_run(mx_mlp_pipeline_t *p, const mx_mlp_host_io_t *io);
+MX_API mx_status_t mx_mlp_pipeline_sync(mx_mlp_pipeline_t *p);
+MX_API void mx_mlp_pipeline_destroy(mx_mlp_pipeline_t *p);
+
+/*
  * mx_get_device_status -- synchronise `stream`, then report and clear the
  * device-side status words: MX_ERR_DEVICE_TIMEOUT if a bounded wait inside
  * a kernel expired (the kernel unwound; its outputs are undefined),

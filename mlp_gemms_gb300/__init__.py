@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "mx_grouped_gemm_dswiglu_bwd", "mx_grouped_gemm_wgrad", "mx_mlp_workspace_bytes", "mx_mlp_fwd_bwd",
     "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
     "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
+    "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
 )
 
 
@@ -56,6 +57,11 @@ class MlpArgsStruct(ctypes.Structure):
                 ("b2", ctypes.c_void_p), ("y", ctypes.c_void_p), ("dx", ctypes.c_void_p),
                 ("dw1", ctypes.c_void_p), ("dw2", ctypes.c_void_p), ("db1", ctypes.c_void_p),
                 ("db2", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class HostIOStruct(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("x", "w1", "w2", "dy", "b1", "b2", "offsets", "y", "dx", "dw1",
+                                               "dw2", "db1", "db2")]
 
 
 _lib = None
@@ -94,6 +100,10 @@ def load(path=None):
         "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
         "mx_quantize_colsum_noalloc": (ctypes.c_int, [vp, i64, i64, i64, i32, u32, tp, tp, vp, vp]),
         "mx_debug_tap": (ctypes.c_int, [vp, i64]),
+        "mx_mlp_pipeline_create": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp, ctypes.POINTER(vp)]),
+        "mx_mlp_pipeline_run": (ctypes.c_int, [vp, ctypes.POINTER(HostIOStruct)]),
+        "mx_mlp_pipeline_sync": (ctypes.c_int, [vp]),
+        "mx_mlp_pipeline_destroy": (None, [vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -319,6 +329,46 @@ def mx_mlp_workspace_bytes(args):
 
 def mx_mlp_fwd_bwd(args, stream=None):
     _check(load().mx_mlp_fwd_bwd(ctypes.byref(args), _stream(stream)))
+
+
+class MlpPipeline:
+    """The step with host-memory inputs and outputs (mx_mlp_pipeline_*).
+
+    dev_args: the device argument block (mlp_args with a workspace) whose
+    buffers the pipeline stages through; the tensors behind it must outlive
+    the pipeline.  run(host) takes CPU tensors (pinned, for overlap) keyed
+    x, w1, w2, dy, offsets, y, dx, dw1, dw2 (and b1, b2, db1, db2 for GELU);
+    they are read and written asynchronously until sync()."""
+
+    def __init__(self, dev_args, stream=None):
+        self._args = dev_args
+        h = ctypes.c_void_p()
+        _check(load().mx_mlp_pipeline_create(ctypes.byref(dev_args), _stream(stream), ctypes.byref(h)))
+        self._h = h
+        self._io = []
+
+    def run(self, host):
+        io = HostIOStruct()
+        for name, _ in HostIOStruct._fields_:
+            t = host.get(name)
+            setattr(io, name, None if t is None else t.data_ptr())
+        self._io.append(io)
+        _check(load().mx_mlp_pipeline_run(self._h, ctypes.byref(io)))
+
+    def sync(self):
+        _check(load().mx_mlp_pipeline_sync(self._h))
+        self._io = []
+
+    def close(self):
+        if self._h is not None:
+            load().mx_mlp_pipeline_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def mx_get_device_status(stream=None):

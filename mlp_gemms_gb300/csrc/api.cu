@@ -41,6 +41,13 @@ mx_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(MX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+}  // namespace
+
+// The thread's last error message, set from other translation units.
+mx_status_t mx::set_error(mx_status_t st, const char* msg) { return fail(st, "%s", msg); }
+
+namespace {
+
 #define MX_CHECK(cond, st, ...) \
   do {                          \
     if (!(cond)) return fail(st, __VA_ARGS__); \
@@ -778,7 +785,15 @@ mx_tensor_t view(const mx_mlp_args_t* a, const MlpLayout::Slot& s) {
   return t;
 }
 
-mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream) {
+// Stage hooks (the host pipeline orders its copies against these points;
+// without hooks the step is the plain chain).
+struct HookCall {
+  const mx::StepHooks* h;
+  void pre(int t) const { if (h) h->before(h->ctx, t); }
+  void post(int t) const { if (h) h->after(h->ctx, t); }
+};
+
+mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream, const mx::StepHooks* hooks) {
   const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
   mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
   mx_tensor_t w1_row = view(a, L.w1_row), w1t_row = view(a, L.w1t_row);
@@ -788,21 +803,39 @@ mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t s
   mx_tensor_t dz_row = view(a, L.dz_row), dz_col = view(a, L.dz_col);
   void* z = static_cast<uint8_t*>(a->workspace) + L.z;
   const uint32_t both = MX_ROWWISE | MX_COLWISE;
+  const HookCall hk{hooks};
   mx_status_t st;
+  hk.pre(mx::T_X);
   if ((st = mx_quantize(a->x, 1, R, D, D, MX_E4M3, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_X);
+  hk.pre(mx::T_W1);
   if ((st = mx_quantize(a->w1, G, 2 * F, D, D, MX_E4M3, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_W1);
+  hk.pre(mx::T_W2);
   if ((st = mx_quantize(a->w2, G, D, F, F, MX_E4M3, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_W2);
   if ((st = mx_grouped_gemm_swiglu_fwd(&x_row, &w1_row, a->G, a->offsets, &h_row, &h_col, z, stream)) != MX_OK) return st;
+  hk.pre(mx::T_Y);
   if ((st = mx_grouped_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
+  hk.post(mx::T_Y);
+  hk.pre(mx::T_DY);
   if ((st = mx_quantize(a->dy, 1, R, D, D, MX_E4M3, both, &dy_row, &dy_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_DY);
   if ((st = mx_grouped_gemm_dswiglu_bwd(&dy_row, &w2t_row, z, a->G, a->offsets, &dz_row, &dz_col, stream)) != MX_OK) return st;
+  hk.pre(mx::T_DX);
   if ((st = mx_grouped_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
+  hk.post(mx::T_DX);
+  hk.pre(mx::T_DW2);
   if ((st = mx_grouped_gemm_wgrad(&dy_col, &h_col, a->G, a->offsets, a->dw2, stream)) != MX_OK) return st;
-  return mx_grouped_gemm_wgrad(&dz_col, &x_col, a->G, a->offsets, a->dw1, stream);
+  hk.post(mx::T_DW2);
+  hk.pre(mx::T_DW1);
+  if ((st = mx_grouped_gemm_wgrad(&dz_col, &x_col, a->G, a->offsets, a->dw1, stream)) != MX_OK) return st;
+  hk.post(mx::T_DW1);
+  return MX_OK;
 }
 
 // Dense GELU step ([MXFP6-PR] fused-MLP commit): 12 launches.
-mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream) {
+mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream, const mx::StepHooks* hooks) {
   const int64_t M = a->R, D = a->D, H = a->F;
   const int fmt = a->fmt;
   const uint32_t both = MX_ROWWISE | MX_COLWISE | (a->hadamard ? MX_HADAMARD : 0);
@@ -816,21 +849,47 @@ mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t str
   void* pre = base + L.z;
   const size_t part_dy_bytes = (size_t)((M + 127) / 128) * (size_t)D * 4;
   const size_t part_dz_bytes = (size_t)((M + 127) / 128) * (size_t)H * 4;
+  const HookCall hk{hooks};
   mx_status_t st;
+  hk.pre(mx::T_X);
   if ((st = mx_quantize(a->x, 1, M, D, D, fmt, both, &x_row, &x_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_X);
+  hk.pre(mx::T_W1);
   if ((st = mx_quantize(a->w1, 1, H, D, D, fmt, both, &w1_row, &w1t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_W1);
+  hk.pre(mx::T_W2);
   if ((st = mx_quantize(a->w2, 1, D, H, H, fmt, both, &w2_row, &w2t_row, nullptr, nullptr, 0, stream)) != MX_OK) return st;
+  hk.post(mx::T_W2);
+  hk.pre(mx::T_B1);
   if ((st = mx_gemm_gelu_fwd(&x_row, &w1_row, a->b1, pre, &act_row, &act_col, stream)) != MX_OK) return st;
+  hk.post(mx::T_B1);
+  hk.pre(mx::T_B2);
+  hk.pre(mx::T_Y);
   if ((st = mx_gemm_bias(&act_row, &w2_row, a->b2, a->y, D, stream)) != MX_OK) return st;
+  hk.post(mx::T_B2);
+  hk.post(mx::T_Y);
+  hk.pre(mx::T_DY);
+  hk.pre(mx::T_DB2);
   if ((st = mx_quantize(a->dy, 1, M, D, D, fmt, both | MX_COLSUM, &dy_row, &dy_col, a->db2, base + L.part_dy,
                         part_dy_bytes, stream)) != MX_OK)
     return st;
+  hk.post(mx::T_DY);
+  hk.post(mx::T_DB2);
+  hk.pre(mx::T_DB1);
   if ((st = mx_gemm_dgelu_bwd(&dy_row, &w2t_row, pre, &dpre_row, &dpre_col, a->db1, base + L.part_dz,
                               part_dz_bytes, stream)) != MX_OK)
     return st;
+  hk.post(mx::T_DB1);
+  hk.pre(mx::T_DX);
   if ((st = mx_grouped_gemm(&dpre_row, &w1t_row, 1, nullptr, a->dx, D, stream)) != MX_OK) return st;
+  hk.post(mx::T_DX);
+  hk.pre(mx::T_DW2);
   if ((st = mx_grouped_gemm_wgrad(&dy_col, &act_col, 1, nullptr, a->dw2, stream)) != MX_OK) return st;
-  return mx_grouped_gemm_wgrad(&dpre_col, &x_col, 1, nullptr, a->dw1, stream);
+  hk.post(mx::T_DW2);
+  hk.pre(mx::T_DW1);
+  if ((st = mx_grouped_gemm_wgrad(&dpre_col, &x_col, 1, nullptr, a->dw1, stream)) != MX_OK) return st;
+  hk.post(mx::T_DW1);
+  return MX_OK;
 }
 
 }  // namespace
@@ -841,7 +900,12 @@ size_t mx_mlp_workspace_bytes(const mx_mlp_args_t* args) {
   return mlp_layout(args).total;
 }
 
-mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
+}  // extern "C"
+
+namespace mx {
+
+// Validation shared by mx_mlp_fwd_bwd and the host pipeline.
+mx_status_t mlp_check(const mx_mlp_args_t* a) {
   MX_CHECK(a != nullptr, MX_ERR_INVALID_ARG, "args is NULL");
   MX_CHECK(a->act == MX_ACT_SWIGLU || a->act == MX_ACT_GELU_TANH, MX_ERR_INVALID_ARG, "activation %d", a->act);
   if (a->act == MX_ACT_SWIGLU) {
@@ -865,12 +929,24 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) {
   const MlpLayout L = mlp_layout(a);
   MX_CHECK(a->workspace_bytes >= L.total, MX_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", L.total,
            a->workspace_bytes);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return MX_OK;
+}
+
+mx_status_t mlp_step(const mx_mlp_args_t* a, mx_stream_t stream, const StepHooks* hooks) {
   mx_status_t st;
+  if ((st = mlp_check(a)) != MX_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if ((st = check_offsets(a->offsets, a->G, a->R, s)) != MX_OK) return st;
   if (a->R == 0) return MX_OK;
-  return a->act == MX_ACT_SWIGLU ? mlp_swiglu(a, L, stream) : mlp_gelu(a, L, stream);
+  const MlpLayout L = mlp_layout(a);
+  return a->act == MX_ACT_SWIGLU ? mlp_swiglu(a, L, stream, hooks) : mlp_gelu(a, L, stream, hooks);
 }
+
+}  // namespace mx
+
+extern "C" {
+
+mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) { return mx::mlp_step(a, stream, nullptr); }
 
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/mx.h"
+
 namespace mx {
 
 inline int64_t round_up_i64(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -86,5 +88,23 @@ cudaError_t reset_gemm_status();
 cudaError_t read_dense_status(unsigned* out);
 cudaError_t reset_dense_status();
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t s);
+
+// The tensors of one MLP step that the host pipeline moves: raw inputs the
+// step reads once (X, W1, W2, dY, b1, b2) and outputs it writes (y, dX, dW1,
+// dW2, db1, db2).
+enum StepTensor { T_X, T_W1, T_W2, T_DY, T_B1, T_B2, T_Y, T_DX, T_DW1, T_DW2, T_DB1, T_DB2, T_COUNT };
+inline bool step_tensor_is_input(int t) { return t <= T_B2; }
+
+// Called on the host while a step is being enqueued: before(t) just before
+// the launch that reads input t or writes output t, after(t) just after it.
+struct StepHooks {
+  void (*before)(void* ctx, int t);
+  void (*after)(void* ctx, int t);
+  void* ctx;
+};
+mx_status_t mlp_check(const mx_mlp_args_t* a);
+// Sets the calling thread's mx_last_error() message; returns st.
+mx_status_t set_error(mx_status_t st, const char* msg);
+mx_status_t mlp_step(const mx_mlp_args_t* a, mx_stream_t stream, const StepHooks* hooks);
 
 }  // namespace mx
