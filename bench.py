@@ -98,21 +98,26 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around the timed region: every
+    sample is time-stamped on arrival, and the summary uses the samples that
+    arrived between mark() and the end of the block (all samples, flagged, if
+    the timed region was shorter than the sampling interval)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, interval_ms=20):
         self.index = index
+        self.interval_ms = interval_ms
         self.proc = None
         self.lines = []
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -121,13 +126,18 @@ class ClockSampler:
         time.sleep(0.25)
         return self
 
+    def mark(self):
+        """Call right before the timed region starts."""
+        self.t_start = time.perf_counter()
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
+        self.t_end = time.perf_counter()
         if self.proc:
-            time.sleep(0.15)
+            time.sleep(0.1)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -135,22 +145,35 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            p = [x.strip() for x in ln.split(",")]
-            if len(p) < 8:
-                continue
-            try:
-                sm.append(float(p[1]))
-                smax = float(p[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, p[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
+
+        def parse(rows):
+            sm, smax, reasons = [], None, set()
+            for _, ln in rows:
+                p = [x.strip() for x in ln.split(",")]
+                if len(p) < 8:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax = float(p[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            return sm, smax, reasons
+
+        lo = self.t_start if self.t_start is not None else 0.0
+        hi = self.t_end if self.t_end is not None else float("inf")
+        inside = [r for r in self.lines if lo <= r[0] <= hi]
+        sm, smax, reasons = parse(inside)
+        window = "timed region"
+        if not sm:
+            sm, smax, reasons = parse(self.lines)
+            window = "around the timed region (it was shorter than the sampling interval)"
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "window": window,
+                "interval_ms": self.interval_ms}
 
 
 def dist_env():
@@ -275,6 +298,7 @@ def run_gpu(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        clk.mark()
         ev0.record(stream)
         for _ in range(args.steps):
             mx.mx_mlp_fwd_bwd(margs)

@@ -56,3 +56,20 @@ def test_reference_arm_sample_is_bounded():
     assert v > 0 and cores >= 1 and "2048 rows" in desc
     v, desc, cores = bench.oracle_sample(seconds_hint=0.0, rows=512)
     assert "512 rows" in desc
+
+
+def test_clock_summary_uses_the_timed_window():
+    """Clock samples are time-stamped: the summary takes those inside the
+    timed region, and falls back to all samples (flagged) when the region
+    was shorter than the sampling interval."""
+    import bench
+    c = bench.ClockSampler(0)
+    c.lines = [(1.0, "0, 2000, 2070, 500, Not Active, Not Active, Not Active, Active"),
+               (5.0, "0, 1900, 2070, 900, Not Active, Not Active, Not Active, Not Active"),
+               (5.5, "0, 1950, 2070, 950, Not Active, Not Active, Not Active, Not Active")]
+    c.t_start, c.t_end = 4.0, 6.0
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1925.0 and s["reasons"] == [] and s["window"] == "timed region"
+    c.t_start, c.t_end = 7.0, 8.0
+    s = c.summary()
+    assert s["samples"] == 3 and "sw_power_cap" in s["reasons"] and s["window"].startswith("around")
