@@ -237,10 +237,34 @@ MX_API mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t *dy_row, const 
  *   out_bf16  device BF16 [G, N, K]: out[g, n, k] = sum over rows r of
  *             segment g of a_col[n, r] * b_col[k, r]; an empty segment
  *             writes exact zeros
- * N % 128 == 0, K % 128 == 0, R % 128 == 0.
+ * N % 128 == 0, K % 128 == 0, R % 128 == 0.  out_bf16 may be the caller's
+ * BF16 main-grad buffer itself: the gradient is stored there with no
+ * separate gradient tensor and no add (Primus PR #1064 "feat(mxfp6): MXFP6
+ * (E2M3) Flux linears, a fused MLP, and the MLPerf recipe", the commit that
+ * writes wgrad into main_grad: a beta = 0 store, one microbatch per step).
  */
 MX_API mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
                                   const int32_t *offsets_dev, void *out_bf16, mx_stream_t stream);
+
+/*
+ * mx_grouped_gemm_wgrad_f32 -- the same weight gradient into a caller's
+ * fp32 gradient buffer (the main-grad of mixed-precision training).  The
+ * page's store overwrites, so it fits one microbatch per optimizer step;
+ * accumulate = 1 is our extension for several microbatches (a beta = 1
+ * variant).
+ *   a_col, b_col, G, offsets_dev   as mx_grouped_gemm_wgrad
+ *   grad_f32    device fp32 [G, N, K], 16-byte aligned
+ *   accumulate  0: grad = a_col^T b_col per expert (an empty segment
+ *               stores zeros); 1: grad += that product, one fp32 rounding
+ *               per element (an empty segment leaves grad unchanged).
+ *               Each element is written by exactly one tile, so the result
+ *               does not depend on scheduling.
+ * Errors: MX_ERR_INVALID_ARG if accumulate is not 0 or 1; otherwise as
+ * mx_grouped_gemm_wgrad.
+ */
+MX_API mx_status_t mx_grouped_gemm_wgrad_f32(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
+                                             const int32_t *offsets_dev, float *grad_f32, int32_t accumulate,
+                                             mx_stream_t stream);
 
 /*
  * Dense (single-segment) calls of the MXFP6 Flux-style MLP ([MXFP6-PR]

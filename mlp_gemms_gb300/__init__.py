@@ -34,6 +34,7 @@ ABI_SYMBOLS = (
     "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
     "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
     "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
+    "mx_grouped_gemm_wgrad_f32",
 )
 
 
@@ -90,6 +91,7 @@ def load(path=None):
         "mx_grouped_gemm_swiglu_fwd": (ctypes.c_int, [tp, tp, i32, vp, tp, tp, vp, vp]),
         "mx_grouped_gemm_dswiglu_bwd": (ctypes.c_int, [tp, tp, vp, i32, vp, tp, tp, vp]),
         "mx_grouped_gemm_wgrad": (ctypes.c_int, [tp, tp, i32, vp, vp, vp]),
+        "mx_grouped_gemm_wgrad_f32": (ctypes.c_int, [tp, tp, i32, vp, vp, i32, vp]),
         "mx_mlp_workspace_bytes": (sz, [ctypes.POINTER(MlpArgsStruct)]),
         "mx_mlp_fwd_bwd": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp]),
         "mx_get_device_status": (ctypes.c_int, [vp]),
@@ -259,6 +261,16 @@ def mx_grouped_gemm_wgrad(a_col, b_col, G, offsets, out=None, stream=None):
         out = torch.empty((G, a_col.rows, b_col.rows), dtype=torch.bfloat16, device=a_col.data.device)
     _check(load().mx_grouped_gemm_wgrad(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(out), _stream(stream)))
     return out
+
+
+def mx_grouped_gemm_wgrad_f32(a_col, b_col, G, offsets, grad, accumulate=False, stream=None):
+    """Weight gradient into the caller's fp32 buffer grad [G, N, K]: stored
+    (accumulate=False) or added to what it holds (accumulate=True)."""
+    import torch
+    assert grad.dtype == torch.float32 and grad.is_contiguous()
+    _check(load().mx_grouped_gemm_wgrad_f32(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(grad),
+                                            1 if accumulate else 0, _stream(stream)))
+    return grad
 
 
 def mx_gemm_bias(a, b, bias=None, out=None, ld_out=None, stream=None):

@@ -155,6 +155,22 @@ mx_status_t make_tmap_out(CUtensorMap* m, const void* base, int64_t rows, int64_
   return MX_OK;
 }
 
+// fp32 output [rows, cols] with row stride ld elements as TMA store or
+// reduce-add target: 16x32 boxes (64-byte rows), 64-byte swizzle.
+mx_status_t make_tmap_out_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (fp32 output) failed (%d)", (int)r);
+  return MX_OK;
+}
+
 // Byte tensor [rows, row_bytes] as a TMA store target: box 128 bytes x 128
 // rows, 128-byte swizzle (the quantizer's staging layout).
 mx_status_t make_tmap_bytes(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
@@ -270,6 +286,7 @@ mx_status_t attach_tap(mx::GemmParams* p, int64_t rows, int64_t cols) {
 struct OutView {
   const void* base;
   int64_t rows, cols, ld;
+  bool f32 = false;  // fp32 elements (EPI_F32) instead of BF16
 };
 
 mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
@@ -280,7 +297,9 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
   if (st != MX_OK) return st;
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
   if (out.base) {
-    if ((st = make_tmap_out(&to, out.base, out.rows, out.cols, out.ld)) != MX_OK) return st;
+    st = out.f32 ? make_tmap_out_f32(&to, out.base, out.rows, out.cols, out.ld)
+                 : make_tmap_out(&to, out.base, out.rows, out.cols, out.ld);
+    if (st != MX_OK) return st;
   } else if (p.epi == mx::EPI_DSWIGLU) {  // the saved z [R, 2F], streamed by the epilogue
     if ((st = make_tmap_bf16(&to, p.z, p.R, 2 * p.F, 2 * p.F)) != MX_OK) return st;
   } else {
@@ -549,8 +568,14 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   return run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0});
 }
 
-mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
-                                  const int32_t* offsets_dev, void* out_bf16, mx_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Ragged-K wgrad into BF16 (EPI_BF16) or into an fp32 gradient buffer
+// (EPI_F32, stored or accumulated).
+mx_status_t wgrad_common(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G, const int32_t* offsets_dev,
+                         void* out, int epi, int accumulate, mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mx_status_t st;
   if ((st = check_gemm_operand(a_col, "a_col")) != MX_OK) return st;
@@ -563,7 +588,7 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   MX_CHECK(R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)R);
   MX_CHECK(N > 0 && N % 128 == 0, MX_ERR_SHAPE, "N = %lld is not a positive multiple of 128", (long long)N);
   MX_CHECK(K > 0 && K % 128 == 0, MX_ERR_SHAPE, "K = %lld is not a positive multiple of 128", (long long)K);
-  MX_CHECK(out_bf16 != nullptr && aligned16(out_bf16), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
+  MX_CHECK(out != nullptr && aligned16(out), MX_ERR_ALIGNMENT, "out must be a 16-byte aligned pointer");
   MX_CHECK((int64_t)G * N * K < (1ll << 40), MX_ERR_SHAPE, "output too large");
   if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
   DevInfo dev;
@@ -571,7 +596,7 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   const int bn = (K % 256 == 0) ? 256 : 128;
   mx::GemmParams p = base_params();
   p.mode = mx::MODE_WGRAD;
-  p.epi = mx::EPI_BF16;
+  p.epi = epi;
   p.G = G; p.offsets = offsets_dev;
   p.R = R; p.K = R; p.Nb = K; p.Mw = N;
   p.a_type = mma_type(a_col->fmt); p.b_type = mma_type(b_col->fmt);
@@ -581,10 +606,32 @@ mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b
   p.m_tiles = (int)(N / 128);
   p.n_tiles = (int)(K / bn);
   p.num_tiles = (int64_t)G * p.m_tiles * p.n_tiles;
-  p.out = static_cast<uint16_t*>(out_bf16);
+  if (epi == mx::EPI_F32) {
+    p.out_f32 = static_cast<float*>(out);
+    p.accumulate = accumulate ? 1 : 0;
+  } else {
+    p.out = static_cast<uint16_t*>(out);
+  }
   p.out_ld = K;
-  return run_gemm(p, a_col, b_col, bn, s, dev, OutView{out_bf16, (int64_t)G * N, K, K});
+  return run_gemm(p, a_col, b_col, bn, s, dev, OutView{out, (int64_t)G * N, K, K, epi == mx::EPI_F32});
 }
+
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
+                                  const int32_t* offsets_dev, void* out_bf16, mx_stream_t stream) {
+  return wgrad_common(a_col, b_col, G, offsets_dev, out_bf16, mx::EPI_BF16, 0, stream);
+}
+
+mx_status_t mx_grouped_gemm_wgrad_f32(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int32_t G,
+                                      const int32_t* offsets_dev, float* grad_f32, int32_t accumulate,
+                                      mx_stream_t stream) {
+  MX_CHECK(accumulate == 0 || accumulate == 1, MX_ERR_INVALID_ARG, "accumulate = %d (0 stores, 1 adds)", accumulate);
+  return wgrad_common(a_col, b_col, G, offsets_dev, grad_f32, mx::EPI_F32, accumulate, stream);
+}
+
 
 mx_status_t mx_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, const void* bias_bf16, void* out_bf16,
                          int64_t ld_out, mx_stream_t stream) {

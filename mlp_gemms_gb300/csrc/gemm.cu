@@ -31,6 +31,11 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtens
     if (p.tap != nullptr) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms);
     return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   }
+  if (p.epi == EPI_F32) {
+    if (p.mode != MODE_WGRAD) return cudaErrorInvalidValue;
+    if (bn == 128) return launch_one<128, EPI_F32, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
+    return launch_one<256, EPI_F32, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
+  }
   if (p.mode == MODE_WGRAD) {
     if (bn == 128) return launch_one<128, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);
     return launch_one<256, EPI_BF16, MODE_WGRAD>(p, ta, tb, to, s, num_sms);

@@ -187,6 +187,25 @@ __device__ __forceinline__ void tap_store32(float* tap, int64_t ld, int64_t row,
   for (int i = 0; i < 8; i++) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
+// fp32 variant: 16 values of this lane's row into the staging buffer (64
+// bytes per row, 64-byte swizzle), then one TMA store (or reduce-add into
+// what the destination holds) of the warp's 32x16 block.
+__device__ __forceinline__ void store_f32_block(const float* v, uint8_t* stage, int lane, const CUtensorMap* tm,
+                                                int64_t col0, int64_t row0, bool add) {
+  uint4* row = reinterpret_cast<uint4*>(stage + lane * 64);
+#pragma unroll
+  for (int c = 0; c < 4; c++)
+    row[c ^ ((lane >> 1) & 3)] = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                            __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (add) tma_reduce_add_2d(tm, stage, (int)col0, (int)row0);
+    else tma_store_2d(tm, stage, (int)col0, (int)row0);
+    bulk_commit();
+  }
+}
+
 // Before a warp rewrites its staging buffer: the previous TMA store has read it.
 __device__ __forceinline__ void stage_reuse_wait(int lane) {
   if (lane == 0) bulk_wait_read();
@@ -567,6 +586,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.out_ld + T.n0 + half * (BN / 2));
 #pragma unroll
           for (int c = 0; c < BN / 16; c++) dst[c] = make_uint4(0, 0, 0, 0);
+        } else if (EPI == EPI_F32 && !p.accumulate) {  // stored zeros; an accumulate adds nothing
+          const int64_t row = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + row_in_tile;
+          uint4* dst = reinterpret_cast<uint4*>(p.out_f32 + row * p.out_ld + T.n0 + half * (BN / 2));
+#pragma unroll
+          for (int c = 0; c < BN / 8; c++) dst[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -606,6 +630,35 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int i = 0; i < COLS / 32; i++) {
           stage_reuse_wait(lane);
           store_bf16_block(reinterpret_cast<const float*>(v[i]), tb_bytes, lane, &tmO, T.n0 + half * COLS + 32 * i, row0);
+        }
+        if (C::ACC == 2) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+      } else if constexpr (EPI == EPI_F32) {
+        // fp32 into the caller's gradient buffer: 32x16 blocks, TMA store
+        // (accumulate = 0) or TMA reduce-add (accumulate = 1)
+        constexpr int COLS = BN / 2;
+        uint32_t v[COLS / 32][32];
+#pragma unroll
+        for (int i = 0; i < COLS / 32; i++) tmem_ld32(tbase + half * COLS + 32 * i, v[i]);
+        tmem_wait_ld();
+        if (C::ACC == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
+        const int64_t row0 = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + q * 32;
+        const bool add = p.accumulate != 0;
+#pragma unroll
+        for (int i = 0; i < COLS / 32; i++) {
+#pragma unroll
+          for (int hh = 0; hh < 2; hh++) {
+            stage_reuse_wait(lane);
+            store_f32_block(reinterpret_cast<const float*>(v[i]) + 16 * hh, tb_bytes, lane, &tmO,
+                            T.n0 + half * COLS + 32 * i + 16 * hh, row0, add);
+          }
         }
         if (C::ACC == 2) {
           tc_fence_before();

@@ -41,7 +41,7 @@ cudaError_t colsum_scratch(float** out, size_t* floats);
 cudaError_t reset_quant_status();
 
 enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };
-enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_GELU = 3, EPI_DGELU = 4 };
+enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_GELU = 3, EPI_DGELU = 4, EPI_F32 = 5 };
 
 // Everything a grouped-GEMM launch needs besides the two tensor maps.
 struct GemmParams {
@@ -74,6 +74,8 @@ struct GemmParams {
   const uint16_t* bias;     // BF16 [N] added to the fp32 accumulator, or null
   float* colsum_partials;   // dGELU: fp32 [ceil(R/128), C] per-tile column sums
   float* tap;               // test instrument: fused epilogues' fp32 pre-quant values [R, C], or null
+  float* out_f32;           // EPI_F32: fp32 gradient buffer [rows, out_ld] (wgrad into main_grad)
+  int accumulate;           // EPI_F32: 0 stores, 1 adds into what out_f32 holds
 };
 
 // ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte

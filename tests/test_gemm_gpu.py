@@ -124,6 +124,54 @@ def test_wgrad_ragged_with_zero_token_expert(cuda_lib):
     assert O.within_tolerance(got, ref).all()
 
 
+@pytest.mark.parametrize("K", [384, 512])
+def test_wgrad_into_fp32_main_grad_store_and_accumulate(cuda_lib, K):
+    """The wgrad written into a caller's fp32 gradient buffer: the store gives
+    the same accumulator the BF16 path rounds (so BF16 of it equals that
+    output bit for bit) and exact zeros for an empty expert; the accumulate
+    adds it with one fp32 rounding, leaves an empty expert's slice untouched,
+    and onto zeros equals the store bit for bit.  K = 384 runs 128-column
+    tiles, K = 512 256-column tiles."""
+    import torch
+    G, N, R = 4, 256, 1152
+    counts = [256, 0, 512, 256]
+    offsets = _offsets(counts)
+    rng = np.random.default_rng(23)
+    a_bits = W.normal_bf16(rng, (R, N), std=1e-3)
+    b_bits = W.normal_bf16(rng, (R, K))
+    _, ac, aref = _quant_both(cuda_lib, a_bits, row=False, col=True)
+    _, bc, bref = _quant_both(cuda_lib, b_bits, row=False, col=True)
+    offs = torch.from_numpy(offsets).cuda()
+    ref = O.wgrad(_deq(aref["col_payload"], aref["col_scales"], N, R),
+                  _deq(bref["col_payload"], bref["col_scales"], K, R), offsets)
+    stored = torch.full((G, N, K), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad_f32(ac, bc, G, offs, stored, accumulate=False)
+    bf = cuda_lib.mx_grouped_gemm_wgrad(ac, bc, G, offs)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    got = stored.cpu().numpy().astype(np.float64)
+    assert np.all(got[1] == 0.0)
+    assert O.within_tolerance(got, ref).all()
+    assert torch.equal(stored.to(torch.bfloat16), bf), "fp32 store and BF16 output disagree"
+    zeros = torch.zeros((G, N, K), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad_f32(ac, bc, G, offs, zeros, accumulate=True)
+    assert torch.equal(zeros, stored), "accumulate onto zeros differs from the store"
+    g0 = torch.from_numpy(rng.standard_normal((G, N, K)).astype(np.float32) * float(np.std(ref))).cuda()
+    acc = g0.clone()
+    cuda_lib.mx_grouped_gemm_wgrad_f32(ac, bc, G, offs, acc, accumulate=True)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    g0n = g0.cpu().numpy().astype(np.float64)
+    a = acc.cpu().numpy().astype(np.float64)
+    assert np.array_equal(a[1], g0n[1]), "an empty expert's slice must stay untouched"
+    # one fp32 rounding of (g0 + fp32 accumulator): within the GEMM tolerance of g0 + ref
+    want = g0n + ref
+    err = np.abs(a - want)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -14 * rms + 2.0 ** -23 * np.abs(want)
+    assert np.all(err <= bound)
+    exact = (g0 + stored).cpu()
+    assert torch.equal(acc.cpu(), exact), "accumulate is not fl32(grad + stored accumulator)"
+
+
 def _moe_small(seed=0):
     G, D, F, R = 4, 1024, 384, 1152
     counts = [384, 0, 256, 384]
