@@ -231,16 +231,29 @@ __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint8_t* chunk, 
 // tanh-GELU and its derivative in fp32 (Primus PR #1064 "feat(mxfp6): MXFP6
 // (E2M3) Flux linears, a fused MLP, and the MLPerf recipe": the fused MLP's
 // tanh GELU epilogue and its derivative as the backward prologue).
-__device__ __forceinline__ float gelu_tanh_f(float x) {
-  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
-  const float u = k0 * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.0f + tanhf(u));
+// With u = sqrt(2/pi) (x + 0.044715 x^3), 0.5 (1 + tanh(u)) = sigma(2u), the
+// logistic function, so gelu(x) = x sigma(2u): one exponential and one
+// reciprocal, and no cancellation in 1 + tanh(u) for negative x.  The
+// derivative is s + x s (1 - s) d(2u)/dx with s = sigma(2u), 1 - s taken as
+// E s (E = exp(-2u)) where s >= 1/2 and as 1 - s below.  The polynomial is
+// evaluated at x clamped to [-100, 100], where the logistic has saturated to
+// 0 or 1 in fp32 anyway, so x^3 cannot overflow.
+__device__ __forceinline__ float gelu_2u_(float x) {
+  const float c1 = 1.5957691216057308f;   // 2 sqrt(2/pi)
+  const float c3 = 0.0713548162726009f;   // 2 sqrt(2/pi) 0.044715
+  const float xc = fminf(fmaxf(x, -100.0f), 100.0f);
+  return xc * fmaf(c3, xc * xc, c1);
 }
+__device__ __forceinline__ float gelu_tanh_f(float x) { return x * sigmoidf_(gelu_2u_(x)); }
 __device__ __forceinline__ float dgelu_tanh_f(float x) {
-  const float k0 = 0.7978845608028654f;
-  const float x2 = x * x;
-  const float t = tanhf(k0 * (x + 0.044715f * x2 * x));
-  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x2);
+  const float c1 = 1.5957691216057308f;
+  const float c3x3 = 0.2140644488178027f;  // 3 * 2 sqrt(2/pi) 0.044715
+  const float v = gelu_2u_(x);
+  const float e = __expf(-v);
+  const float s = __fdividef(1.0f, 1.0f + e);
+  const float oms = v < 0.0f ? 1.0f - s : e * s;
+  const float xc = fminf(fmaxf(x, -100.0f), 100.0f);
+  return fmaf(x * s * oms, fmaf(c3x3, xc * xc, c1), s);
 }
 
 // Rowwise requant of 32 fp32 values held by one thread (rotated first if QH).
@@ -271,10 +284,13 @@ __device__ __forceinline__ uint32_t row_quant_store(float (&v)[32], uint8_t* dst
 // and 16 packed codes per lane stored straight to the transposed payload.
 // dst(c) is the payload row of column c at this warp's 32-row block;
 // returns nothing, writes column c's scale byte to chunk[(f&31)*16+(f>>5)*4+q]
-// for f = f_local0 + c.
+// for f = f_local0 + c.  colsum (optional): column c's sum over the warp's 32
+// rows before any rotation (rows 0..15 and 16..31 each summed in order, then
+// the two halves), written to colsum[c] by the lane pair's first lane.
 template <int QF, bool QH>
 __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane, uint8_t* q_col, int64_t col_ld,
-                                            int64_t col0, int64_t row_byte0, uint8_t* chunk, int f_local0, int q) {
+                                            int64_t col0, int64_t row_byte0, uint8_t* chunk, int f_local0, int q,
+                                            float* colsum = nullptr) {
 #pragma unroll
   for (int c = 0; c < 16; c++) buf[lane * 17 + c] = v[c];
   __syncwarp();
@@ -283,6 +299,13 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 #pragma unroll
   for (int i = 0; i < 16; i++) x[i] = buf[(hh * 16 + i) * 17 + c];
   __syncwarp();
+  if (colsum != nullptr) {
+    float sum = x[0];
+#pragma unroll
+    for (int i = 1; i < 16; i++) sum += x[i];
+    const float other = __shfl_xor_sync(0xffffffffu, sum, 1);
+    if (hh == 0) colsum[c] = sum + other;
+  }
   if constexpr (QH) {
 #pragma unroll
     for (int h = 1; h < 16; h <<= 1) {
@@ -858,20 +881,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           } else {
 #pragma unroll
             for (int j = 0; j < 32; j++) val[j] = __uint_as_float(accr[j]) * dgelu_tanh_f(aux[j]);
-#pragma unroll
-            for (int j = 0; j < 32; j++) {  // this warp's 32-row column sums, fixed butterfly order
-              float sum = val[j];
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-              if (lane == 0) part[q * 128 + fc + j] = sum;
-            }
           }
           if (p.tap != nullptr) tap_store32(p.tap, p.q_cols, row, n0 + fc, val);
           // columnwise first (the rowwise packer rotates and scales in place)
 #pragma unroll
-          for (int k = 0; k < 2; k++)
+          for (int k = 0; k < 2; k++)  // dGELU: this warp's 32-row column sums from the transpose
             col_quant16<QF, QH>(&val[16 * k], tb, lane, p.q_col, p.q_col_ld, n0 + fc + 16 * k,
-                                (T.m0 + q * 32) / 32 * BB, ch_col, fc + 16 * k, q);
+                                (T.m0 + q * 32) / 32 * BB, ch_col, fc + 16 * k, q,
+                                EPI == EPI_DGELU ? part + q * 128 + fc + 16 * k : nullptr);
           const uint32_t sbr = row_quant_store<QF, QH>(val, p.q_row + row * p.q_row_ld + (n0 + fc) / 32 * BB);
           ch_row[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbr;
         }
