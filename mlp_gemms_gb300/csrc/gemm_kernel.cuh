@@ -307,23 +307,13 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
     if (hh == 0) colsum[c] = sum + other;
   }
   if constexpr (QH) {
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 16; i++) {
-        if (i & h) continue;
-        const float a = x[i], b = x[i + h];
-        x[i] = __fadd_rn(a, b);
-        x[i + h] = __fsub_rn(a, b);
-      }
-    }
+    butterfly_stages<16>(x);
 #pragma unroll
     for (int i = 0; i < 16; i++) {
       const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
       x[i] = hh ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
     }
-#pragma unroll
-    for (int i = 0; i < 16; i++) x[i] = __fmul_rn(x[i], __uint_as_float(0x3E3504F3u));
+    scale_values<16>(x, __uint_as_float(0x3E3504F3u));
   }
   uint32_t amax = amax_abs_bits<16>(x);
   amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));

@@ -196,24 +196,47 @@ __device__ __forceinline__ void quantize_block_words(float (&v)[32], uint32_t sb
   pack_block<FMT>(v, w);
 }
 
+// (a0, a1), (b0, b1) -> (a0 + b0, a1 + b1), (a0 - b0, a1 - b1): two
+// butterflies in one packed add and one packed subtract (each lane an
+// ordinary round-to-nearest fp32 operation).
+__device__ __forceinline__ void butterfly_pair(float& a0, float& a1, float& b0, float& b1) {
+  uint64_t A, B, S, D;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(S) : "l"(A), "l"(B));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(D) : "l"(A), "l"(B));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(S));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(b0), "=f"(b1) : "l"(D));
+}
+
+// In-place butterfly stages of stride 1, 2, ..., N/2 over N values
+// (v[i], v[i+h]) -> (v[i] + v[i+h], v[i] - v[i+h]); stride 1 scalar, the
+// wider strides two butterflies at a time.
+template <int N>
+__device__ __forceinline__ void butterfly_stages(float* v) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    const float a = v[i], b = v[i + 1];
+    v[i] = __fadd_rn(a, b);
+    v[i + 1] = __fsub_rn(a, b);
+  }
+#pragma unroll
+  for (int h = 2; h < N; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      if (i & h) continue;
+      butterfly_pair(v[i], v[i + 1], v[i + h], v[i + h + 1]);
+    }
+  }
+}
+
 // In-register 32-point Hadamard: five butterfly stages (stride 1..16), then
 // one multiply by fl32(1/sqrt(32)).  Primus PR #1064 "feat(mxfp6): MXFP6
 // (E2M3) Flux linears, a fused MLP, and the MLPerf recipe", first commit:
 // the rotation folded into the packer.
 __device__ __forceinline__ void hadamard32(float (&v)[32]) {
-#pragma unroll
-  for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 32; i++) {
-      if (i & h) continue;
-      float a = v[i], b = v[i + h];
-      v[i] = __fadd_rn(a, b);
-      v[i + h] = __fsub_rn(a, b);
-    }
-  }
-  const float inv = __uint_as_float(0x3E3504F3u);  // fl32(1/sqrt(32))
-#pragma unroll
-  for (int i = 0; i < 32; i++) v[i] = __fmul_rn(v[i], inv);
+  butterfly_stages<32>(v);
+  scale_values<32>(v, __uint_as_float(0x3E3504F3u));  // fl32(1/sqrt(32))
 }
 
 // Offset of scale (r, c) in the blocked layout of a [rows, scale_cols] scale
