@@ -397,3 +397,37 @@ def test_saturated_gate_gives_exact_product():
     g = np.array([32.0, 40.0, 64.0, 100.0])
     u = np.array([1.5, -2.0, 0.25, 3.0])
     assert np.array_equal(O.round_f32(O.swiglu(g, u)), g * u)
+
+
+def test_routing_probabilities_in_the_swiglu_stages():
+    """The fused activation with routing probabilities: probs = 1 is the plain
+    stage exactly; dz with probs is p_r times dz without (before fp32
+    rounding, so compared in float64 through dswiglu); dprobs is the
+    derivative of sum(dh * h) with respect to p, checked by a central
+    difference of the forward's activation."""
+    rng = np.random.default_rng(41)
+    G, D, F, R = 2, 64, 32, 256
+    offsets = np.array([128, 256], dtype=np.int32)
+    x = rng.standard_normal((R, D))
+    w1 = rng.standard_normal((G, 2 * F, D)) * 0.1
+    dy = rng.standard_normal((R, D)) * 1e-2
+    w2t = rng.standard_normal((G, F, D)) * 0.1
+    probs = rng.uniform(0.05, 1.0, R)
+    plain = O.swiglu_fwd(x, w1, offsets)
+    ones = O.swiglu_fwd(x, w1, offsets, probs=np.ones(R))
+    assert np.array_equal(plain["h"], ones["h"])
+    zb = plain["z_bf16"]
+    b0 = O.dswiglu_bwd(dy, w2t, zb, offsets)
+    b1 = O.dswiglu_bwd(dy, w2t, zb, offsets, probs=np.ones(R))
+    assert np.array_equal(b0["dz"], b1["dz"])
+    bp = O.dswiglu_bwd(dy, w2t, zb, offsets, probs=probs)
+    z = O.bf16_to_f64(zb)
+    dg, du = O.dswiglu(b0["dh"], z[:, :F], z[:, F:])
+    np.testing.assert_allclose(bp["dz"], O.round_f32(np.concatenate([dg, du], axis=1) * probs[:, None]),
+                               rtol=2e-7, atol=0)
+    # dprobs: d/dp_r of sum_f dh[r, f] * act(p)[r, f], act = swiglu(z) * p
+    act = O.swiglu(z[:, :F], z[:, F:])
+    eps = 1e-3
+    fd = (np.sum(b0["dh"] * act * (probs + eps)[:, None], axis=1) -
+          np.sum(b0["dh"] * act * (probs - eps)[:, None], axis=1)) / (2 * eps)
+    np.testing.assert_allclose(bp["dprobs"], fd, rtol=1e-9, atol=1e-15)
