@@ -229,6 +229,33 @@ MX_API mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t *dy_row, const 
                                         mx_stream_t stream);
 
 /*
+ * Routing probabilities fused into the activation (Primus PR #1247
+ * "Qwen3-30B-A3B FP8 on MI355X to 40k tokens/s/GPU": the fused activation
+ * with probabilities, which scales each routed row by its routing weight
+ * before FC2 instead of after it).
+ * mx_grouped_gemm_swiglu_probs_fwd -- mx_grouped_gemm_swiglu_fwd with
+ *   h[r, :] = swiglu(g, u)[r, :] * probs[r] before both requants (z is
+ *   saved unscaled).  probs: device fp32 [R], 16-byte aligned.
+ * mx_grouped_gemm_dswiglu_probs_bwd -- the matching backward: the
+ *   activation gradient is dh * probs[r]; dprobs[r] = sum over f of
+ *   dh[r, f] * swiglu(g, u)[r, f] for the rows of the segments (rows past
+ *   offsets[G-1] untouched), summed in a fixed order (deterministic).
+ *   dprobs: device fp32 [R]; workspace: at least
+ *   mx_dswiglu_probs_workspace_bytes(R, F) bytes for per-tile partial sums.
+ *   Errors as mx_grouped_gemm_dswiglu_bwd, plus MX_ERR_WORKSPACE.
+ */
+MX_API mx_status_t mx_grouped_gemm_swiglu_probs_fwd(const mx_tensor_t *x_row, const mx_tensor_t *w1_row, int32_t G,
+                                                    const int32_t *offsets_dev, const float *probs,
+                                                    const mx_tensor_t *h_row, const mx_tensor_t *h_col,
+                                                    void *z_bf16, mx_stream_t stream);
+MX_API size_t mx_dswiglu_probs_workspace_bytes(int64_t R, int64_t F);
+MX_API mx_status_t mx_grouped_gemm_dswiglu_probs_bwd(const mx_tensor_t *dy_row, const mx_tensor_t *w2t_row,
+                                                     const void *z_bf16, const float *probs, int32_t G,
+                                                     const int32_t *offsets_dev, const mx_tensor_t *dz_row,
+                                                     const mx_tensor_t *dz_col, float *dprobs, void *workspace,
+                                                     size_t workspace_bytes, mx_stream_t stream);
+
+/*
  * mx_grouped_gemm_wgrad -- ragged-K weight gradient, BF16 out ([MXFP8-PR]
  * correctness-first kernels commit: generic ragged-K grouped wgrad, BF16
  * out; shared-infrastructure commit: zero-token experts give zeros).

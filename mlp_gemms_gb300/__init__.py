@@ -34,7 +34,8 @@ ABI_SYMBOLS = (
     "mx_get_device_status", "mx_selftest_bounded_wait", "mx_gemm_bias", "mx_gemm_gelu_fwd",
     "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
     "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
-    "mx_grouped_gemm_wgrad_f32",
+    "mx_grouped_gemm_wgrad_f32", "mx_grouped_gemm_swiglu_probs_fwd", "mx_dswiglu_probs_workspace_bytes",
+    "mx_grouped_gemm_dswiglu_probs_bwd",
 )
 
 
@@ -92,6 +93,9 @@ def load(path=None):
         "mx_grouped_gemm_dswiglu_bwd": (ctypes.c_int, [tp, tp, vp, i32, vp, tp, tp, vp]),
         "mx_grouped_gemm_wgrad": (ctypes.c_int, [tp, tp, i32, vp, vp, vp]),
         "mx_grouped_gemm_wgrad_f32": (ctypes.c_int, [tp, tp, i32, vp, vp, i32, vp]),
+        "mx_grouped_gemm_swiglu_probs_fwd": (ctypes.c_int, [tp, tp, i32, vp, vp, tp, tp, vp, vp]),
+        "mx_dswiglu_probs_workspace_bytes": (sz, [i64, i64]),
+        "mx_grouped_gemm_dswiglu_probs_bwd": (ctypes.c_int, [tp, tp, vp, vp, i32, vp, tp, tp, vp, vp, sz, vp]),
         "mx_mlp_workspace_bytes": (sz, [ctypes.POINTER(MlpArgsStruct)]),
         "mx_mlp_fwd_bwd": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp]),
         "mx_get_device_status": (ctypes.c_int, [vp]),
@@ -240,6 +244,39 @@ def mx_grouped_gemm_swiglu_fwd(x_row, w1_row, G, offsets, h_row=None, h_col=None
     _check(load().mx_grouped_gemm_swiglu_fwd(_s(x_row), _s(w1_row), G, _ptr(offsets), _s(h_row), _s(h_col),
                                              _ptr(z), _stream(stream)))
     return z, h_row, h_col
+
+
+def mx_grouped_gemm_swiglu_probs_fwd(x_row, w1_row, G, offsets, probs, h_row=None, h_col=None, z=None, stream=None):
+    """FC1 + SwiGLU with each routed row's activation scaled by probs [R] (fp32)."""
+    import torch
+    R = x_row.rows
+    F = w1_row.rows // (2 * G)
+    dev = x_row.data.device
+    h_row = h_row if h_row is not None else MX(R, F, E4M3, False, dev)
+    h_col = h_col if h_col is not None else MX(F, R, E4M3, False, dev)
+    z = z if z is not None else torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    _check(load().mx_grouped_gemm_swiglu_probs_fwd(_s(x_row), _s(w1_row), G, _ptr(offsets), _ptr(probs), _s(h_row),
+                                                   _s(h_col), _ptr(z), _stream(stream)))
+    return z, h_row, h_col
+
+
+def mx_grouped_gemm_dswiglu_probs_bwd(dy_row, w2t_row, z, probs, G, offsets, dz_row=None, dz_col=None,
+                                      dprobs=None, workspace=None, stream=None):
+    """The matching backward; returns (dz_row, dz_col, dprobs [R] fp32)."""
+    import torch
+    R = dy_row.rows
+    F = w2t_row.rows // G
+    dev = dy_row.data.device
+    dz_row = dz_row if dz_row is not None else MX(R, 2 * F, E4M3, False, dev)
+    dz_col = dz_col if dz_col is not None else MX(2 * F, R, E4M3, False, dev)
+    dprobs = dprobs if dprobs is not None else torch.empty(R, dtype=torch.float32, device=dev)
+    nbytes = int(load().mx_dswiglu_probs_workspace_bytes(R, F))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check(load().mx_grouped_gemm_dswiglu_probs_bwd(
+        _s(dy_row), _s(w2t_row), _ptr(z), _ptr(probs), G, _ptr(offsets), _s(dz_row), _s(dz_col), _ptr(dprobs),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dz_row, dz_col, dprobs
 
 
 def mx_grouped_gemm_dswiglu_bwd(dy_row, w2t_row, z, G, offsets, dz_row=None, dz_col=None, stream=None):

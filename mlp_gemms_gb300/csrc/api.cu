@@ -478,9 +478,13 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   return run_gemm(p, a, b, bn, s, dev, OutView{out_bf16, R, N, ld_out});
 }
 
-mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
-                                       const int32_t* offsets_dev, const mx_tensor_t* h_row,
-                                       const mx_tensor_t* h_col, void* z_bf16, mx_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+mx_status_t swiglu_fwd_impl(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
+                            const int32_t* offsets_dev, const float* probs, const mx_tensor_t* h_row,
+                            const mx_tensor_t* h_col, void* z_bf16, mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mx_status_t st;
   if ((st = check_gemm_operand(x_row, "x_row")) != MX_OK) return st;
@@ -516,6 +520,7 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   p.n_tiles = (int)(F / 128);
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.z = static_cast<uint16_t*>(z_bf16);
+  p.probs = probs;
   p.q_row = static_cast<uint8_t*>(h_row->data); p.q_row_scale = h_row->scale;
   p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
   p.q_cols = F;
@@ -523,9 +528,32 @@ mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor
   return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F});
 }
 
-mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
-                                        int32_t G, const int32_t* offsets_dev, const mx_tensor_t* dz_row,
-                                        const mx_tensor_t* dz_col, mx_stream_t stream) {
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
+                                       const int32_t* offsets_dev, const mx_tensor_t* h_row,
+                                       const mx_tensor_t* h_col, void* z_bf16, mx_stream_t stream) {
+  return swiglu_fwd_impl(x_row, w1_row, G, offsets_dev, nullptr, h_row, h_col, z_bf16, stream);
+}
+
+mx_status_t mx_grouped_gemm_swiglu_probs_fwd(const mx_tensor_t* x_row, const mx_tensor_t* w1_row, int32_t G,
+                                             const int32_t* offsets_dev, const float* probs,
+                                             const mx_tensor_t* h_row, const mx_tensor_t* h_col, void* z_bf16,
+                                             mx_stream_t stream) {
+  MX_CHECK(probs != nullptr && aligned16(probs), MX_ERR_ALIGNMENT, "probs must be a 16-byte aligned pointer");
+  return swiglu_fwd_impl(x_row, w1_row, G, offsets_dev, probs, h_row, h_col, z_bf16, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
+                             const float* probs, int32_t G, const int32_t* offsets_dev, const mx_tensor_t* dz_row,
+                             const mx_tensor_t* dz_col, float* dprobs, void* workspace, size_t workspace_bytes,
+                             mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mx_status_t st;
   if ((st = check_gemm_operand(dy_row, "dy_row")) != MX_OK) return st;
@@ -565,7 +593,47 @@ mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tens
   p.q_col = static_cast<uint8_t*>(dz_col->data); p.q_col_scale = dz_col->scale;
   p.q_cols = 2 * F;
   if ((st = attach_tap(&p, R, 2 * F)) != MX_OK) return st;
+  if (probs != nullptr) {
+    const int64_t ld = 2 * (F / 128);
+    MX_CHECK(dprobs != nullptr, MX_ERR_INVALID_ARG, "dprobs is NULL");
+    MX_CHECK(workspace != nullptr && aligned16(workspace) && workspace_bytes >= (size_t)(R * ld * 4),
+             MX_ERR_WORKSPACE, "the probabilities' workspace needs %lld bytes", (long long)(R * ld * 4));
+    p.probs = probs;
+    p.dprobs_part = static_cast<float*>(workspace);
+    p.dprobs_ld = ld;
+    if ((st = run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0})) != MX_OK) return st;
+    cudaError_t e = mx::launch_dprobs_reduce(p.dprobs_part, R, ld, offsets_dev, G, dprobs, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dprobs reduction launch");
+    return MX_OK;
+  }
   return run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0});
+}
+
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row, const void* z_bf16,
+                                        int32_t G, const int32_t* offsets_dev, const mx_tensor_t* dz_row,
+                                        const mx_tensor_t* dz_col, mx_stream_t stream) {
+  return dswiglu_bwd_impl(dy_row, w2t_row, z_bf16, nullptr, G, offsets_dev, dz_row, dz_col, nullptr, nullptr, 0,
+                          stream);
+}
+
+size_t mx_dswiglu_probs_workspace_bytes(int64_t R, int64_t F) {
+  if (R < 0 || F <= 0) return 0;
+  return (size_t)R * (size_t)(2 * ((F + 127) / 128)) * 4;
+}
+
+mx_status_t mx_grouped_gemm_dswiglu_probs_bwd(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_row,
+                                              const void* z_bf16, const float* probs, int32_t G,
+                                              const int32_t* offsets_dev, const mx_tensor_t* dz_row,
+                                              const mx_tensor_t* dz_col, float* dprobs, void* workspace,
+                                              size_t workspace_bytes, mx_stream_t stream) {
+  MX_CHECK(probs != nullptr && aligned16(probs), MX_ERR_ALIGNMENT, "probs must be a 16-byte aligned pointer");
+  MX_CHECK(dprobs != nullptr && aligned16(dprobs), MX_ERR_ALIGNMENT, "dprobs must be a 16-byte aligned pointer");
+  return dswiglu_bwd_impl(dy_row, w2t_row, z_bf16, probs, G, offsets_dev, dz_row, dz_col, dprobs, workspace,
+                          workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -7,10 +7,10 @@
 
 namespace mx {
 
-template <int BN, int EPI, int MODE, bool TAP = false>
+template <int BN, int EPI, int MODE, bool EXT = false>
 static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
-  auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, TAP>;
+  auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, EXT>;
   constexpr int smem = Cfg<BN, EPI == EPI_DSWIGLU>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
   if (!configured) {
@@ -28,7 +28,8 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtens
                         int bn, cudaStream_t s, int num_sms) {
   if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   if (p.epi == EPI_DSWIGLU) {
-    if (p.tap != nullptr) return launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms);
+    if (p.tap != nullptr || p.probs != nullptr)
+      return launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms);
     return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   }
   if (p.epi == EPI_F32) {
@@ -42,6 +43,24 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtens
   }
   if (bn == 128) return launch_one<128, EPI_BF16, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   return launch_one<256, EPI_BF16, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+}
+
+__global__ void dprobs_reduce_kernel(const float* __restrict__ part, int64_t R, int64_t ld,
+                                     const int32_t* __restrict__ offsets, int G, float* __restrict__ out) {
+  const int64_t rows = offsets ? (int64_t)__ldg(offsets + G - 1) : R;
+  for (int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; r < rows && r < R;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.0f;
+    for (int64_t k = 0; k < ld; k++) s += part[r * ld + k];
+    out[r] = s;
+  }
+}
+
+cudaError_t launch_dprobs_reduce(const float* part, int64_t R, int64_t ld, const int32_t* offsets, int G,
+                                 float* dprobs, cudaStream_t s) {
+  const int64_t blocks = (R + 255) / 256;
+  dprobs_reduce_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, s>>>(part, R, ld, offsets, G, dprobs);
+  return cudaGetLastError();
 }
 
 cudaError_t read_gemm_status(unsigned* out) {

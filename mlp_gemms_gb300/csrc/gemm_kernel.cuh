@@ -360,15 +360,15 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 
 // ---- the kernel ---------------------------------------------------------
 
-// TAP: the dSwiGLU kernel has a separate instantiation that writes the
-// debug tap (its register budget is tight); the other fused epilogues test
-// the tap pointer at run time.
-template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool TAP = false>
+// EXT: the dSwiGLU kernel has a separate instantiation with its optional
+// extras, the debug tap and the routing probabilities (its register budget is
+// tight); the other fused epilogues test those pointers at run time.
+template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false>
 __global__ void __launch_bounds__(kThreads<EPI>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
-  constexpr bool TAP_ON = EPI != EPI_DSWIGLU || TAP;
+  constexpr bool EXT_ON = EPI != EPI_DSWIGLU || EXT;
   using C = Cfg<BN, ZR>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
@@ -713,6 +713,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             h[i][j] = g * sigmoidf_(g) * u;
           }
         }
+        if (p.probs != nullptr) {  // the routing probability of this row
+          const float prob = __ldg(p.probs + row);
+#pragma unroll
+          for (int i = 0; i < 2; i++) {
+#pragma unroll
+            for (int j = 0; j < 32; j++) h[i][j] *= prob;
+          }
+        }
         if (p.tap != nullptr) {
 #pragma unroll
           for (int i = 0; i < 2; i++) tap_store32(p.tap, p.q_cols, row, f0 + half * 64 + 32 * i, h[i]);
@@ -758,6 +766,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint8_t* ch_uc = sChunk + 1536;
         const int zrow = q * 32 + lane;
         bool zok = true;
+        float dps = 0.0f;  // routing-probability gradient: this row, this warp's 64 columns
+        const float prob = (EXT_ON && p.probs != nullptr) ? __ldg(p.probs + row) : 1.0f;
 #pragma unroll 1
         for (int hh = 0; hh < 2; hh++) {
           const int fc = hh * 64 + half * 32;  // tile-local column of this chunk
@@ -787,13 +797,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const int j = i * 8 + k;
               const float g = bf16_bits_to_float((k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu));
               const float u = bf16_bits_to_float((k & 1) ? (uw[k >> 1] >> 16) : (uw[k >> 1] & 0xFFFFu));
-              const float d = __uint_as_float(dh[j]);
+              float d = __uint_as_float(dh[j]);
               const float s = sigmoidf_(g);
+              if (EXT_ON && p.probs != nullptr) {  // dprobs += dh * swiglu(g, u); then dh * p
+                dps = fmaf(d, g * s * u, dps);
+                d *= prob;
+              }
               dg[j] = d * u * s * (1.0f + g * (1.0f - s));
               du[j] = d * g * s;
             }
           }
-          if (TAP_ON && p.tap != nullptr) {
+          if (EXT_ON && p.tap != nullptr) {
             tap_store32(p.tap, p.q_cols, row, f0 + fc, dg);
             tap_store32(p.tap, p.q_cols, row, p.F + f0 + fc, du);
           }
@@ -811,6 +825,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ch_ur[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbu;
         }
         if (!zok) break;
+        if (EXT_ON && p.probs != nullptr) p.dprobs_part[row * p.dprobs_ld + (f0 >> 7) * 2 + half] = dps;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[acc]);

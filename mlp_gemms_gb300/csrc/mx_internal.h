@@ -76,6 +76,9 @@ struct GemmParams {
   float* tap;               // test instrument: fused epilogues' fp32 pre-quant values [R, C], or null
   float* out_f32;           // EPI_F32: fp32 gradient buffer [rows, out_ld] (wgrad into main_grad)
   int accumulate;           // EPI_F32: 0 stores, 1 adds into what out_f32 holds
+  const float* probs;       // SwiGLU / dSwiGLU: routing probability per row [R], or null
+  float* dprobs_part;       // dSwiGLU with probs: per-row partial sums [R, dprobs_ld]
+  int64_t dprobs_ld;        // 2 per 128-column tile of F
 };
 
 // ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte
@@ -85,6 +88,10 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtens
 cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms);
 cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s);
+// dprobs[r] = sum over k of part[r, k] in order, for the rows of the segments
+// (r < offsets[G-1], or all R rows without offsets); other rows untouched.
+cudaError_t launch_dprobs_reduce(const float* part, int64_t R, int64_t ld, const int32_t* offsets, int G,
+                                 float* dprobs, cudaStream_t s);
 cudaError_t read_gemm_status(unsigned* out);
 cudaError_t reset_gemm_status();
 cudaError_t read_dense_status(unsigned* out);

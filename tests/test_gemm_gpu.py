@@ -326,6 +326,72 @@ def test_dswiglu_bwd_tap_requant_bit_exact_and_gate_up_swap_fails(cuda_lib):
     assert np.mean(O.within_tolerance(got, bad["dz"])) < 0.5, "gate/up swap went unnoticed"
 
 
+def _same_active(a, b, A, cols, R, what):
+    """Two requant outputs agree on the active rows (row orientation [R, cols])
+    or active columns (column orientation [cols, R]); rows and columns past
+    the last segment are never written."""
+    ar, ac = a
+    br, bc = b
+    assert np.array_equal(ar.data.cpu().numpy()[:A], br.data.cpu().numpy()[:A]), what
+    sr = O.scales_to_matrix(ar.scale.cpu().numpy(), R, cols // 32)[:A]
+    assert np.array_equal(sr, O.scales_to_matrix(br.scale.cpu().numpy(), R, cols // 32)[:A]), what
+    assert np.array_equal(ac.data.cpu().numpy()[:, :A], bc.data.cpu().numpy()[:, :A]), what
+    sc = O.scales_to_matrix(ac.scale.cpu().numpy(), cols, R // 32)[:, :A // 32]
+    assert np.array_equal(sc, O.scales_to_matrix(bc.scale.cpu().numpy(), cols, R // 32)[:, :A // 32]), what
+
+
+def test_swiglu_with_routing_probabilities(cuda_lib):
+    """The fused activation with routing probabilities, forward and backward:
+    probs = 1 reproduces the plain kernels' bytes exactly; random probs give
+    requant bytes bit-exact given the epilogue's own fp32 values (debug tap),
+    those values within tolerance of the oracle, and dprobs within tolerance
+    of the oracle's sum_f dh * swiglu(g, u), the same on a second run."""
+    import torch
+    G, D, F, R, offsets, inp = _moe_small(seed=7)
+    A = int(offsets[-1])
+    offs = torch.from_numpy(offsets).cuda()
+    xr, _, xref = _quant_both(cuda_lib, inp["x"])
+    wr, _, wref = _quant_both(cuda_lib, inp["w1"])
+    probs_np = np.random.default_rng(8).uniform(0.05, 1.0, R).astype(np.float32)
+    probs = torch.from_numpy(probs_np).cuda()
+    ones = torch.ones(R, dtype=torch.float32, device="cuda")
+    z0, h0r, h0c = cuda_lib.mx_grouped_gemm_swiglu_fwd(xr, wr, G, offs)
+    z1, h1r, h1c = cuda_lib.mx_grouped_gemm_swiglu_probs_fwd(xr, wr, G, offs, ones)
+    assert torch.equal(z0[:A], z1[:A])
+    _same_active((h0r, h0c), (h1r, h1c), A, F, R, "h with probs = 1")
+    (z, h_row, h_col), tap = with_tap(cuda_lib, R, F,
+                                      lambda: cuda_lib.mx_grouped_gemm_swiglu_probs_fwd(xr, wr, G, offs, probs))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(h_row, h_col, tap, A, F, R, what="h*p")
+    x = _deq(xref["row_payload"], xref["row_scales"], R, D)
+    w = _deq(wref["row_payload"], wref["row_scales"], G * 2 * F, D).reshape(G, 2 * F, D)
+    ref = O.swiglu_fwd(x, w, offsets, probs=probs_np.astype(np.float64))
+    assert O.within_tolerance(tap[:A].astype(np.float64), ref["h"]).all()
+
+    dyr, _, dyref = _quant_both(cuda_lib, inp["dy"])
+    w2t_bits = np.ascontiguousarray(np.transpose(inp["w2"], (0, 2, 1)))
+    w2tr, _, w2ref = _quant_both(cuda_lib, w2t_bits)
+    d0r, d0c = cuda_lib.mx_grouped_gemm_dswiglu_bwd(dyr, w2tr, z, G, offs)
+    d1r, d1c, _ = cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, w2tr, z, ones, G, offs)
+    _same_active((d0r, d0c), (d1r, d1c), A, 2 * F, R, "dz with probs = 1")
+    dprobs0 = torch.full((R,), float("nan"), dtype=torch.float32, device="cuda")
+    (dz_row, dz_col, dprobs), tap2 = with_tap(
+        cuda_lib, R, 2 * F,
+        lambda: cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, w2tr, z, probs, G, offs, dprobs=dprobs0))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert_tap_requant_exact(dz_row, dz_col, tap2, A, 2 * F, R, what="dz with probs")
+    dy = _deq(dyref["row_payload"], dyref["row_scales"], R, D)
+    w2t = _deq(w2ref["row_payload"], w2ref["row_scales"], G * F, D).reshape(G, F, D)
+    zb = z.view(torch.int16).cpu().numpy().view(np.uint16)
+    bref = O.dswiglu_bwd(dy, w2t, zb, offsets, probs=probs_np.astype(np.float64))
+    assert O.within_tolerance(tap2[:A].astype(np.float64), bref["dz"]).all()
+    got = dprobs.cpu().numpy().astype(np.float64)
+    assert np.all(np.isnan(got[A:])), "rows past the segments were written"
+    assert O.within_tolerance(got[None, :A], bref["dprobs"][None, :]).all()
+    again = cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, w2tr, z, probs, G, offs)[2]
+    assert torch.equal(again[:A], dprobs[:A]), "dprobs is not deterministic"
+
+
 def test_mlp_step_against_oracle_chain(cuda_lib):
     import torch
     G, D, F, R, offsets, inp = _moe_small(seed=2)
