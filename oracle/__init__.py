@@ -84,6 +84,14 @@ def lib():
         L.orc_bf16_to_f64_array.argtypes = [u16p, i64, dp]
         L.orc_f64_to_bf16_array.argtypes = [dp, i64, u16p]
         L.orc_round_f32_array.argtypes = [dp, i64, dp]
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        L.orc_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        L.orc_sr_bits.restype = ctypes.c_uint32
+        L.orc_sr_bits.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32]
+        L.orc_encode_sr.restype = ctypes.c_uint8
+        L.orc_encode_sr.argtypes = [ctypes.c_double, ctypes.c_int, ctypes.c_uint32]
+        L.orc_quantize_rows_sr.argtypes = [dp, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+                                           ctypes.c_uint32, u8p, u8p]
         _lib = L
     return _lib
 
@@ -197,6 +205,44 @@ def quantize_cols(x, fmt, hadamard=False):
     """Columnwise 32x1 quantization of [rows, cols]: blocks of 32 rows, stored
     as the rowwise quantization of the transpose, payload [cols, rows]."""
     return quantize_rows(np.ascontiguousarray(np.asarray(x, dtype=np.float64).T), fmt, hadamard)
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 (Salmon et al., SC 2011) of a 4-word counter and a
+    2-word key; returns the 4 output words."""
+    c = (ctypes.c_uint32 * 4)(*counter)
+    k = (ctypes.c_uint32 * 2)(*key)
+    o = (ctypes.c_uint32 * 4)()
+    lib().orc_philox4x32_10(c, k, o)
+    return tuple(int(v) for v in o)
+
+
+def sr_bits(seed, idx, orient):
+    return int(lib().orc_sr_bits(int(seed), int(idx), int(orient)))
+
+
+def encode_sr(v, fmt, u):
+    return int(lib().orc_encode_sr(float(v), fmt, int(u)))
+
+
+def quantize_rows_sr(x, fmt, seed, orient=0, hadamard=False):
+    """quantize_rows with stochastic rounding of the elements (scales stay
+    RCEIL); element (r, c) draws its bits at index r * cols + c of this
+    matrix with the given orientation word."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    payload = np.zeros((rows, payload_row_bytes(cols, fmt)), dtype=np.uint8)
+    scales = np.zeros(scale_bytes(rows, cols // 32), dtype=np.uint8)
+    lib().orc_quantize_rows_sr(_ptr(x, ctypes.c_double), rows, cols, fmt, 1 if hadamard else 0, int(seed),
+                               int(orient), _ptr(payload, ctypes.c_uint8), _ptr(scales, ctypes.c_uint8))
+    return payload, scales
+
+
+def quantize_cols_sr(x, fmt, seed, hadamard=False):
+    """Columnwise quantization with stochastic rounding: the transpose
+    [cols, rows] quantized rowwise with orientation word 1."""
+    return quantize_rows_sr(np.ascontiguousarray(np.asarray(x, dtype=np.float64).T), fmt, seed, 1, hadamard)
 
 
 def dequantize_rows(payload, scales, rows, cols, fmt):

@@ -173,6 +173,95 @@ uint8_t orc_quantize_block(const double *x, int fmt, uint8_t *codes) {
 }
 
 /* ----------------------------------------------------------------------- */
+/* Stochastic rounding of the element step (Primus guide "MXFP4 training    */
+/* for Flux models": optional stochastic rounding of the FP4 gradient        */
+/* quantization).  The pages name the option only; our reading: the scale   */
+/* stays RCEIL, and each scaled element rounds to one of its two grid        */
+/* neighbours, up with probability equal to its fractional position.       */
+/* Random bits: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random */
+/* numbers: as easy as 1, 2, 3", SC 2011), counter-based, keyed by the seed. */
+/* ----------------------------------------------------------------------- */
+
+/* Ten rounds of the Philox 4x32 bijection: two 32x32->64 multiplies per
+ * round, the key bumped by the Weyl constants between rounds. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+    uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    uint32_t n1 = (uint32_t)p1;
+    uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    uint32_t n3 = (uint32_t)p0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The 32 random bits of element `idx` of an output grid: counter
+ * (idx / 4 as two words, orientation, 0), key = the seed's two words, word
+ * idx % 4 of the result. */
+uint32_t orc_sr_bits(uint64_t seed, uint64_t idx, uint32_t orient) {
+  uint64_t n = idx >> 2;
+  uint32_t ctr[4] = {(uint32_t)n, (uint32_t)(n >> 32), orient, 0u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  orc_philox4x32_10(ctr, key, out);
+  return out[idx & 3];
+}
+
+/* Stochastic encode of a scaled value v (an fp32 value): saturating at
+ * +-max, otherwise the upper neighbour when (u >> 8) < frac * 2^24 with
+ * frac = (|v| - lo) / (up - lo), which is exact (the spacing is a power of
+ * two and |v| - lo is exact); the lower neighbour else.  Sign of zero kept;
+ * NaN as orc_encode. */
+uint8_t orc_encode_sr(double v, int fmt, uint32_t u) {
+  orc_init();
+  orc_fmt_desc d = fmt_desc(fmt);
+  int nbits = 1 + d.ebits + d.mbits;
+  uint8_t sign_bit = (uint8_t)(1u << (nbits - 1));
+  if (isnan(v)) return d.has_nan ? (uint8_t)((1 << (nbits - 1)) - 1) : 0;
+  int neg = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  const double *tab = g_tab[fmt];
+  int hi = max_pos_code(fmt);
+  int k;
+  if (a >= tab[hi]) {
+    k = hi;
+  } else {
+    int lo = 0, up = hi;
+    while (up - lo > 1) {
+      int mid = (lo + up) / 2;
+      if (tab[mid] <= a) lo = mid; else up = mid;
+    }
+    double frac = (a - tab[lo]) / (tab[up] - tab[lo]);
+    k = ((double)(u >> 8) < frac * 16777216.0) ? up : lo;
+  }
+  return (uint8_t)(k | (neg ? sign_bit : 0));
+}
+
+/* One block with stochastic rounding: element i of the block is element
+ * idx0 + i of the output grid.  The scaled value is rounded to fp32 first,
+ * as the device's fp32 multiply does. */
+uint8_t orc_quantize_block_sr(const double *x, int fmt, uint64_t seed, uint64_t idx0, uint32_t orient,
+                              uint8_t *codes) {
+  double a = orc_amax(x, 32);
+  uint8_t sb = orc_scale_byte(a, fmt);
+  if (sb == 0xFF) {
+    for (int i = 0; i < 32; i++) codes[i] = orc_encode(NAN, fmt);
+    return sb;
+  }
+  int e = (int)sb - 127;
+  for (int i = 0; i < 32; i++) {
+    double v = (double)(float)ldexp(x[i], -e);
+    codes[i] = orc_encode_sr(v, fmt, orc_sr_bits(seed, idx0 + (uint64_t)i, orient));
+  }
+  return sb;
+}
+
+/* ----------------------------------------------------------------------- */
 /* Blocked ("128x4") scale layout of the tcgen05 block-scaled MMA.          */
 /* [MXFP8-PR] shared-infrastructure commit: tcgen05 blocked-scale indexing, */
 /* constant 512-byte K stride for every 128-row block.                      */
@@ -330,6 +419,37 @@ void orc_quantize_rows(const double *x, int64_t rows, int64_t cols, int fmt, int
         for (int i = 0; i < 32; i++) blk[i] = x[r * cols + b * 32 + i];
       }
       scales[orc_blocked_offset(r, b, sc)] = orc_quantize_block(blk, fmt, codes);
+      memcpy(rowcodes + b * 32, codes, 32);
+    }
+    orc_pack_row(rowcodes, cols, fmt, payload + r * rb);
+  }
+}
+
+/* orc_quantize_rows with stochastic rounding; the element grid is this
+ * [rows, cols] matrix (row-major index r * cols + c), `orient` the fourth
+ * Philox counter word (0 for a rowwise output, 1 for a columnwise one). */
+void orc_quantize_rows_sr(const double *x, int64_t rows, int64_t cols, int fmt, int hadamard, uint64_t seed,
+                          uint32_t orient, uint8_t *payload, uint8_t *scales) {
+  int64_t sc = cols / 32;
+  int64_t rb = orc_payload_row_bytes(cols, fmt);
+  memset(scales, 0, (size_t)orc_scale_bytes(rows, sc));
+  orc_init();
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; r++) {
+    uint8_t codes[32];
+    uint8_t *rowcodes = (uint8_t *)__builtin_alloca((size_t)cols);
+    for (int64_t b = 0; b < sc; b++) {
+      double blk[32];
+      if (hadamard) {
+        float f[32];
+        for (int i = 0; i < 32; i++) f[i] = (float)x[r * cols + b * 32 + i];
+        orc_hadamard32_f32(f);
+        for (int i = 0; i < 32; i++) blk[i] = (double)f[i];
+      } else {
+        for (int i = 0; i < 32; i++) blk[i] = x[r * cols + b * 32 + i];
+      }
+      scales[orc_blocked_offset(r, b, sc)] =
+          orc_quantize_block_sr(blk, fmt, seed, (uint64_t)(r * cols + b * 32), orient, codes);
       memcpy(rowcodes + b * 32, codes, 32);
     }
     orc_pack_row(rowcodes, cols, fmt, payload + r * rb);

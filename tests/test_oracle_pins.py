@@ -431,3 +431,72 @@ def test_routing_probabilities_in_the_swiglu_stages():
     fd = (np.sum(b0["dh"] * act * (probs + eps)[:, None], axis=1) -
           np.sum(b0["dh"] * act * (probs - eps)[:, None], axis=1)) / (2 * eps)
     np.testing.assert_allclose(bp["dprobs"], fd, rtol=1e-9, atol=1e-15)
+
+
+def test_philox_known_answers():
+    """The oracle's Philox4x32-10 against the generator's published
+    known-answer vectors (tests/golden/philox4x32_10_kat.txt)."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
+    n = 0
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        w = [int(t, 16) for t in line.split()]
+        assert O.philox4x32_10(w[0:4], w[4:6]) == tuple(w[6:10])
+        n += 1
+    assert n == 3
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_stochastic_rounding_picks_a_neighbour_without_bias(fmt):
+    """Stochastic encode: always the lower or the upper grid neighbour, grid
+    values and saturated values deterministic, the threshold exactly
+    (u >> 8) < frac * 2^24, and the mean over uniform bits equal to the
+    value within sampling error."""
+    rng = np.random.default_rng(12)
+    emax = O.fmt_max(fmt)
+    grid = sorted({abs(O.decode(c, fmt)) for c in range(1 << O.lib().orc_fmt_bits(fmt))
+                   if not np.isnan(O.decode(c, fmt))})
+    for _ in range(40):
+        i = int(rng.integers(0, len(grid) - 1))
+        lo, up = grid[i], grid[i + 1]
+        frac = float(rng.uniform(0.02, 0.98))
+        v = float(np.float32(lo + frac * (up - lo)))
+        frac = (v - lo) / (up - lo)
+        sign = -1.0 if rng.random() < 0.5 else 1.0
+        us = rng.integers(0, 1 << 32, size=3000, dtype=np.uint64)
+        vals = np.array([O.decode(O.encode_sr(sign * v, fmt, int(u)), fmt) for u in us])
+        assert set(np.abs(vals)) <= {lo, up}
+        p = np.mean(np.abs(vals) == up)
+        assert abs(p - frac) < 5 * np.sqrt(frac * (1 - frac) / len(us)) + 1e-3
+        t = int(np.ceil(frac * 2 ** 24))            # first u24 that rounds down
+        if 0 < t < 2 ** 24:
+            assert abs(O.decode(O.encode_sr(v, fmt, (t - 1) << 8), fmt)) == up
+            assert abs(O.decode(O.encode_sr(v, fmt, t << 8), fmt)) == lo
+    for g in grid:                                   # on the grid: no randomness
+        for u in (0, 0xFFFFFFFF, 0x80000000):
+            assert O.decode(O.encode_sr(g, fmt, u), fmt) == g
+    assert O.decode(O.encode_sr(3 * emax, fmt, 0), fmt) == emax
+    assert O.decode(O.encode_sr(-3 * emax, fmt, 0xFFFFFFFF), fmt) == -emax
+
+
+def test_stochastic_quantize_keeps_rceil_scales_and_is_unbiased():
+    """Stochastic rounding changes the element step only: scales equal the
+    RCEIL ones, and the average of the dequantized blocks over many seeds
+    converges to the scaled input (the round-to-nearest error does not)."""
+    rng = np.random.default_rng(13)
+    x = W.bf16_bits_to_f32(W.to_bf16_bits(rng.standard_normal((32, 64)).astype(np.float32))).astype(np.float64)
+    p0, s0 = O.quantize_rows(x, O.E2M1)
+    acc = np.zeros_like(x)
+    n = 400
+    for seed in range(n):
+        p, s = O.quantize_rows_sr(x, O.E2M1, seed)
+        assert np.array_equal(s, s0)
+        acc += O.dequantize_rows(p, s, 32, 64, O.E2M1)
+    mean = acc / n
+    rn = O.dequantize_rows(p0, s0, 32, 64, O.E2M1)
+    scale = np.repeat(2.0 ** (O.scales_to_matrix(s0, 32, 2).astype(np.float64) - 127), 32, axis=1)
+    err_sr = np.abs(mean - x) / scale
+    err_rn = np.abs(rn - x) / scale
+    assert np.mean(err_sr) < 0.25 * np.mean(err_rn)
+    assert np.max(err_sr) < 0.35                    # a few sampling sigmas of a 2-ulp spacing
