@@ -140,6 +140,29 @@ MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, 
                         float *colsum, void *workspace, size_t workspace_bytes, mx_stream_t stream);
 
 /*
+ * mx_quantize_sr -- mx_quantize with stochastic rounding of the elements,
+ * for gradients in E2M3 or E2M1 (ROCm Primus guide "MXFP4 training for Flux
+ * models", knob semantics: optional stochastic rounding of the FP4 gradient
+ * quantization; the guide names the option only, the rule below is our
+ * reading).  Scales stay RCEIL.  Each scaled element a rounds to the lower
+ * grid neighbour lo or to lo + spacing, the latter when (u >> 8) < frac *
+ * 2^24 with frac = (|a| - lo) / spacing (exact), so E[result] = a; values
+ * on the grid and beyond the largest finite value are deterministic.  u is
+ * the 32-bit word idx % 4 of Philox4x32-10 (Salmon et al., SC 2011) at
+ * counter (idx / 4 as two words, orientation, 0) with key (the seed's two
+ * words), where idx is the element's row-major position in its output grid
+ * ([batch*rows, cols] rowwise, orientation 0; [batch*cols, rows]
+ * columnwise, orientation 1).  Same seed, same bytes.
+ *   seed      the generator key
+ *   other arguments as mx_quantize; flags MX_ROWWISE / MX_COLWISE /
+ *   MX_HADAMARD
+ * Errors as mx_quantize, plus MX_ERR_NOT_SUPPORTED for E4M3 or MX_COLSUM.
+ */
+MX_API mx_status_t mx_quantize_sr(const void *x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
+                                  int32_t fmt, uint32_t flags, uint64_t seed, const mx_tensor_t *out_row,
+                                  const mx_tensor_t *out_col, mx_stream_t stream);
+
+/*
  * mx_quantize_colsum_noalloc -- mx_quantize with MX_COLSUM for callers that
  * cannot allocate device memory: a framework hook that runs under a memory
  * pool it may not grow, a graph-capture region where allocation is not

@@ -35,7 +35,7 @@ ABI_SYMBOLS = (
     "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
     "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
     "mx_grouped_gemm_wgrad_f32", "mx_grouped_gemm_swiglu_probs_fwd", "mx_dswiglu_probs_workspace_bytes",
-    "mx_grouped_gemm_dswiglu_probs_bwd",
+    "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr",
 )
 
 
@@ -105,6 +105,7 @@ def load(path=None):
         "mx_gemm_dgelu_workspace_bytes": (sz, [i64, i64]),
         "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
         "mx_quantize_colsum_noalloc": (ctypes.c_int, [vp, i64, i64, i64, i32, u32, tp, tp, vp, vp]),
+        "mx_quantize_sr": (ctypes.c_int, [vp, i64, i64, i64, i64, i32, u32, ctypes.c_uint64, tp, tp, vp]),
         "mx_debug_tap": (ctypes.c_int, [vp, i64]),
         "mx_mlp_pipeline_create": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp, ctypes.POINTER(vp)]),
         "mx_mlp_pipeline_run": (ctypes.c_int, [vp, ctypes.POINTER(HostIOStruct)]),
@@ -197,6 +198,26 @@ def mx_quantize(x, fmt=E4M3, rowwise=True, colwise=True, hadamard=False, colsum=
                               _s(out_col) if colwise else None, _ptr(colsum_out) if colsum else None,
                               _ptr(workspace) if colsum else None, ws_bytes, _stream(stream)))
     return out_row, out_col, colsum_out
+
+
+def mx_quantize_sr(x, fmt, seed, rowwise=True, colwise=True, hadamard=False, out_row=None, out_col=None,
+                   stream=None):
+    """mx_quantize with stochastic rounding of the elements (E2M3 / E2M1);
+    returns (out_row, out_col)."""
+    import torch
+    assert x.dtype == torch.bfloat16
+    batch = x.shape[0] if x.dim() == 3 else 1
+    rows, cols = x.shape[-2], x.shape[-1]
+    ld = x.stride(-2)
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0) | (HADAMARD if hadamard else 0)
+    if rowwise and out_row is None:
+        out_row = MX(batch * rows, cols, fmt, hadamard, x.device)
+    if colwise and out_col is None:
+        out_col = MX(batch * cols, rows, fmt, hadamard, x.device)
+    _check(load().mx_quantize_sr(x.data_ptr(), batch, rows, cols, ld, fmt, flags, int(seed),
+                                 _s(out_row) if rowwise else None, _s(out_col) if colwise else None,
+                                 _stream(stream)))
+    return out_row, out_col
 
 
 def mx_quantize_colsum_noalloc(x, fmt=E4M3, rowwise=True, hadamard=False, out_row=None, out_col=None,

@@ -355,9 +355,14 @@ size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, uint32_t flags) {
   return (size_t)((rows + 127) / 128) * (size_t)cols * sizeof(float);
 }
 
-mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
-                        uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col, float* colsum,
-                        void* workspace, size_t workspace_bytes, mx_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+mx_status_t quantize_impl(const void* x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                          uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col, float* colsum,
+                          void* workspace, size_t workspace_bytes, bool stochastic, uint64_t seed,
+                          mx_stream_t stream) {
   MX_CHECK(fmt >= MX_E4M3 && fmt <= MX_E2M1, MX_ERR_INVALID_ARG, "fmt = %d is not an MX element format", fmt);
   MX_CHECK((flags & ~0xFu) == 0, MX_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   MX_CHECK(flags & (MX_ROWWISE | MX_COLWISE), MX_ERR_INVALID_ARG, "neither MX_ROWWISE nor MX_COLWISE requested");
@@ -404,6 +409,8 @@ mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t
   q.colsum_partials = (flags & MX_COLSUM) ? static_cast<float*>(workspace) : nullptr;
   q.colsum = colsum;
   q.num_sms = dev.sms;
+  q.stochastic = stochastic;
+  q.seed = seed;
   if ((st = make_tmap_bf16(&q.xmap, x_bf16, batch * rows, cols, ld)) != MX_OK) return st;
   q.rowmap = q.colmap = q.xmap;  // placeholders where no staged store is made
   if (fmt == MX_E4M3 && (flags & MX_ROWWISE)) {
@@ -415,6 +422,27 @@ mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t
   cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return MX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_quantize(const void* x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                        uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col, float* colsum,
+                        void* workspace, size_t workspace_bytes, mx_stream_t stream) {
+  return quantize_impl(x_bf16, batch, rows, cols, ld, fmt, flags, out_row, out_col, colsum, workspace,
+                       workspace_bytes, false, 0, stream);
+}
+
+mx_status_t mx_quantize_sr(const void* x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
+                           uint32_t flags, uint64_t seed, const mx_tensor_t* out_row, const mx_tensor_t* out_col,
+                           mx_stream_t stream) {
+  MX_CHECK(fmt == MX_E2M3 || fmt == MX_E2M1, MX_ERR_NOT_SUPPORTED,
+           "stochastic rounding is built for the E2M3 and E2M1 element formats (fmt = %d)", fmt);
+  MX_CHECK((flags & MX_COLSUM) == 0, MX_ERR_NOT_SUPPORTED, "MX_COLSUM is not combined with stochastic rounding");
+  return quantize_impl(x_bf16, batch, rows, cols, ld, fmt, flags, out_row, out_col, nullptr, nullptr, 0, true, seed,
+                       stream);
 }
 
 mx_status_t mx_quantize_colsum_noalloc(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,

@@ -31,6 +31,8 @@ struct QuantLaunch {
   CUtensorMap rowmap;      // E4M3: row payload [batch*rows, cols] bytes, box 128 x 128, 128-byte swizzle
   CUtensorMap colmap;      // E4M3: col payload [batch*cols, rows] bytes, same boxes
   int num_sms;
+  bool stochastic = false; // stochastic rounding of the elements (E2M3, E2M1)
+  uint64_t seed = 0;       // its generator key
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
 cudaError_t read_quant_status(unsigned* out);

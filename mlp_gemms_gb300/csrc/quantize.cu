@@ -44,6 +44,7 @@ struct QuantParams {
   float* colsum_partials;  // [ceil(rows/128), cols] or null
   int tiles_x;             // ceil(cols / 128)
   int batch;
+  uint64_t seed;           // stochastic rounding: the generator's key
 };
 
 constexpr int QT = 128;          // tile edge
@@ -83,9 +84,80 @@ __device__ __forceinline__ void store_block(uint8_t* dst, const uint32_t (&w)[8]
   }
 }
 
+// ---- stochastic rounding ----------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC 2011): ten rounds of two 32x32->64 multiplies and xors, the
+// key bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                               uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; round++) {
+    if (round > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// Grid of an element format for stochastic rounding: mantissa bits, the
+// smallest normal exponent (the subnormal spacing is 2^(emin - m)) and the
+// largest finite value.
+template <int FMT> struct SrGrid;
+template <> struct SrGrid<E2M3> { static constexpr int M = 3, EMIN = 0; static constexpr float VMAX = 7.5f; };
+template <> struct SrGrid<E2M1> { static constexpr int M = 1, EMIN = 0; static constexpr float VMAX = 6.0f; };
+
+// A scaled value rounded stochastically onto the format's grid: saturating
+// at +-max; otherwise the lower neighbour lo = floor(|a| / spacing) * spacing
+// (spacing = 2^(max(E, emin) - m), E the fp32 exponent of |a|) or lo +
+// spacing, the latter when (u >> 8) < frac * 2^24 with frac = (|a| - lo) /
+// spacing.  Every step is exact in fp32.  The result is on the grid, so the
+// round-to-nearest conversion that follows is exact; the sign (of zero too)
+// is kept.
+template <int FMT>
+__device__ __forceinline__ float sr_round(float a_signed, uint32_t u) {
+  const float a = fabsf(a_signed);
+  if (!(a < SrGrid<FMT>::VMAX)) return copysignf(SrGrid<FMT>::VMAX, a_signed);
+  const int e = (int)(__float_as_uint(a) >> 23) - 127;
+  const int es = (e > SrGrid<FMT>::EMIN ? e : SrGrid<FMT>::EMIN) - SrGrid<FMT>::M;
+  const float sp = __uint_as_float((uint32_t)(es + 127) << 23);      // 2^es, a normal power of two
+  const float isp = __uint_as_float((uint32_t)(127 - es) << 23);     // 2^-es
+  const float lo = floorf(a * isp) * sp;
+  const float frac = (a - lo) * isp;
+  const bool up = (float)(u >> 8) < frac * 16777216.0f;
+  return copysignf(up ? lo + sp : lo, a_signed);
+}
+
+// Stochastic-rounding variant of the block packer: element i of the block is
+// element idx0 + i of its output grid (idx0 a multiple of 32); its bits are
+// word (idx % 4) of Philox at counter (idx / 4, orient, 0), key the seed.
+template <int FMT>
+__device__ __forceinline__ void quantize_block_words_sr(float (&v)[32], uint32_t sb, uint32_t (&w)[8],
+                                                        uint64_t seed, uint64_t idx0, uint32_t orient) {
+  if (sb == 0xFFu) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) w[i] = nan_block_word<FMT>();
+    return;
+  }
+  scale_values<32>(v, inv_scale_from_byte(sb));
+#pragma unroll
+  for (int g = 0; g < 8; g++) {
+    const uint64_t n = (idx0 >> 2) + (uint64_t)g;
+    const uint4 r = philox4x32_10((uint32_t)n, (uint32_t)(n >> 32), orient, 0u, (uint32_t)seed,
+                                  (uint32_t)(seed >> 32));
+    v[4 * g] = sr_round<FMT>(v[4 * g], r.x);
+    v[4 * g + 1] = sr_round<FMT>(v[4 * g + 1], r.y);
+    v[4 * g + 2] = sr_round<FMT>(v[4 * g + 2], r.z);
+    v[4 * g + 3] = sr_round<FMT>(v[4 * g + 3], r.w);
+  }
+  pack_block<FMT>(v, w);
+}
+
 // Quantize 32 fp32 values (rotating first if HAD) and return the scale byte.
-template <int FMT, bool HAD>
-__device__ __forceinline__ uint32_t quantize32(float (&v)[32], uint32_t amax_bits_prerot, uint32_t (&w)[8]) {
+template <int FMT, bool HAD, bool SR = false>
+__device__ __forceinline__ uint32_t quantize32(float (&v)[32], uint32_t amax_bits_prerot, uint32_t (&w)[8],
+                                               uint64_t seed = 0, uint64_t idx0 = 0, uint32_t orient = 0) {
   uint32_t amax_bits = amax_bits_prerot;
   if constexpr (HAD) {
     hadamard32(v);
@@ -94,7 +166,8 @@ __device__ __forceinline__ uint32_t quantize32(float (&v)[32], uint32_t amax_bit
     for (int i = 0; i < 32; i++) amax_bits = max(amax_bits, __float_as_uint(v[i]) & 0x7FFFFFFFu);
   }
   uint32_t sb = rceil_scale_byte<FMT>(amax_bits);
-  quantize_block_words<FMT>(v, sb, w);
+  if constexpr (SR) quantize_block_words_sr<FMT>(v, sb, w, seed, idx0, orient);
+  else quantize_block_words<FMT>(v, sb, w);
   return sb;
 }
 
@@ -127,7 +200,7 @@ __device__ __forceinline__ uint32_t stage_off(int r, int b) {
   return (uint32_t)(r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
 }
 
-template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
+template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false>
 __global__ void __launch_bounds__(256, 2)
 quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap rowmap,
                 const __grid_constant__ CUtensorMap colmap, const QuantParams p) {
@@ -218,7 +291,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             v[2 * i + 1] = bf16_bits_to_float(wv[i] >> 16);
           }
           uint32_t w[8];
-          sb = quantize32<FMT, HAD>(v, amax, w);
+          // stochastic rounding: element index in the rowwise output grid [batch * rows, cols]
+          sb = quantize32<FMT, HAD, SR>(v, amax, w, p.seed,
+                                        (uint64_t)((int64_t)b * p.rows + r0 + r) * (uint64_t)p.cols +
+                                            (uint64_t)(c0 + cb * 32), 0u);
           if constexpr (QC::STAGED) {
             *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -258,7 +334,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           }
           const uint32_t amax = (h ? (m2 >> 16) : (m2 & 0xFFFFu)) << 16;
           uint32_t w[8];
-          sb = quantize32<FMT, HAD>(v, amax, w);
+          // stochastic rounding: element index in the columnwise output grid [batch * cols, rows]
+          sb = quantize32<FMT, HAD, SR>(v, amax, w, p.seed,
+                                        (uint64_t)((int64_t)b * p.cols + c0 + cc) * (uint64_t)p.rows +
+                                            (uint64_t)(r0 + rb * 32), 1u);
           if constexpr (QC::STAGED) {
             *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
             *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -376,9 +455,9 @@ cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t c
   return cudaGetLastError();
 }
 
-template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM>
+template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false>
 static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStream_t s) {
-  auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM>;
+  auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM, SR>;
   constexpr int smem = QCfg<FMT>::SMEM;
   static bool configured = false;
   if (!configured) {
@@ -390,6 +469,14 @@ static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStre
   const int64_t cap = 2ll * q.num_sms;
   kern<<<(unsigned)(tiles < cap ? tiles : cap), 256, smem, s>>>(q.xmap, q.rowmap, q.colmap, p);
   return cudaGetLastError();
+}
+
+template <int FMT, bool HAD>
+static cudaError_t dispatch_orient_sr(const QuantLaunch& q, const QuantParams& p, bool row, bool col,
+                                      cudaStream_t s) {
+  if (row && col) return launch_q<FMT, HAD, true, true, false, true>(q, p, s);
+  if (row) return launch_q<FMT, HAD, true, false, false, true>(q, p, s);
+  return launch_q<FMT, HAD, false, true, false, true>(q, p, s);
 }
 
 template <int FMT, bool HAD>
@@ -421,8 +508,18 @@ cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s) {
   p.colsum_partials = q.colsum_partials;
   p.tiles_x = (int)((q.cols + QT - 1) / QT);
   p.batch = (int)q.batch;
+  p.seed = q.seed;
   const bool row = q.row_data != nullptr, col = q.col_data != nullptr, cs = q.colsum_partials != nullptr;
   cudaError_t e;
+  if (q.stochastic) {  // E2M3 / E2M1 without column sums (checked by the caller)
+    switch (q.fmt * 2 + (q.hadamard ? 1 : 0)) {
+      case 2: return dispatch_orient_sr<E2M3, false>(q, p, row, col, s);
+      case 3: return dispatch_orient_sr<E2M3, true>(q, p, row, col, s);
+      case 4: return dispatch_orient_sr<E2M1, false>(q, p, row, col, s);
+      case 5: return dispatch_orient_sr<E2M1, true>(q, p, row, col, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (q.fmt * 2 + (q.hadamard ? 1 : 0)) {
     case 0: e = dispatch_orient<E4M3, false>(q, p, row, col, cs, s); break;
     case 1: e = dispatch_orient<E4M3, true>(q, p, row, col, cs, s); break;

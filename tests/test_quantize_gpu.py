@@ -138,3 +138,50 @@ def test_quantizer_workload_full_size(cuda_lib):
     ref = O.quantize_bf16(bits, O.E4M3)
     assert_quant_equal(xr, (ref["row_payload"], ref["row_scales"]), 8192, 7168 // 32, "row")
     assert_quant_equal(xc, (ref["col_payload"], ref["col_scales"]), 7168, 8192 // 32, "col")
+
+
+def _oracle_sr(bits, fmt, seed, had):
+    """Oracle stochastic-rounding quantization of BF16 [rows, cols] or
+    [batch, rows, cols]: rowwise over [batch*rows, cols], columnwise over the
+    stacked per-batch transposes [batch*cols, rows]."""
+    x = O.bf16_to_f64(bits)
+    if x.ndim == 2:
+        x = x[None]
+    B, rows, cols = x.shape
+    row = O.quantize_rows_sr(x.reshape(B * rows, cols), fmt, seed, 0, had)
+    col = O.quantize_rows_sr(np.concatenate([x[b].T for b in range(B)], axis=0), fmt, seed, 1, had)
+    return row, col
+
+
+@pytest.mark.parametrize("fmt", [O.E2M3, O.E2M1])
+@pytest.mark.parametrize("had", [False, True])
+@pytest.mark.parametrize("shape", [(256, 256), (96, 160), (2, 128, 256)])
+def test_stochastic_rounding_bytes_match_oracle(cuda_lib, fmt, had, shape):
+    """mx_quantize_sr against the oracle's stochastic rounding (Philox bits per
+    element of each output grid), bit for bit, specials included; a 64-bit
+    seed with high bits set exercises both key words."""
+    if len(shape) == 3:
+        bits = np.stack([W.quantizer_input(shape[1], shape[2], seed=70 + b, special_frac=0.01) for b in range(shape[0])])
+    else:
+        bits = W.quantizer_input(shape[0], shape[1], seed=71, special_frac=0.01)
+    seed = 0x9E3779B97F4A7C15
+    r, c = cuda_lib.mx_quantize_sr(to_dev(bits), fmt, seed, True, shape[-2] % 32 == 0, had)
+    ref_row, ref_col = _oracle_sr(bits, fmt, seed, had)
+    B = shape[0] if len(shape) == 3 else 1
+    rows, cols = shape[-2], shape[-1]
+    assert_quant_equal(r, ref_row, B * rows, cols // 32, "sr row")
+    if rows % 32 == 0:
+        assert_quant_equal(c, ref_col, B * cols, rows // 32, "sr col")
+
+
+def test_stochastic_rounding_seed_dependence(cuda_lib):
+    """Same seed, same bytes; another seed, other bytes (scales unchanged)."""
+    import torch
+    bits = W.quantizer_input(256, 256, seed=72, special_frac=0.0)
+    x = to_dev(bits)
+    a = cuda_lib.mx_quantize_sr(x, O.E2M1, 1)[0]
+    b = cuda_lib.mx_quantize_sr(x, O.E2M1, 1)[0]
+    c = cuda_lib.mx_quantize_sr(x, O.E2M1, 2)[0]
+    assert torch.equal(a.data, b.data) and torch.equal(a.scale, b.scale)
+    assert torch.equal(a.scale, c.scale)
+    assert float((a.data != c.data).float().mean()) > 0.2
