@@ -123,6 +123,22 @@ mx_status_t make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t k,
   return MX_OK;
 }
 
+// Packed E2M1 payload [rows, K elements] as bytes (two elements each) for
+// .kind::mxf4: box 128 bytes (256 elements) x 128 rows, 128-byte swizzle.
+mx_status_t make_tmap_packed(CUtensorMap* m, const void* base, int64_t rows, int64_t k) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (packed E2M1) failed (%d)", (int)r);
+  return MX_OK;
+}
+
 // BF16 input [rows, cols] with row stride ld elements, box 64 columns x 128
 // rows (two boxes per 128x128 quantizer tile), 128-byte swizzle.
 mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
@@ -291,11 +307,17 @@ struct OutView {
 
 mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
                      const DevInfo& dev, OutView out) {
+  // E2M1 operands with a plain epilogue run on .kind::mxf4 from the packed
+  // payload; the fused epilogues keep .kind::mxf8f6f4.
+  p.f4 = (a->fmt == MX_E2M1 && (p.epi == mx::EPI_BF16 || p.epi == mx::EPI_F32)) ? 1 : 0;
   p.tx_bytes = stage_tx_bytes(a->fmt, bn);
   CUtensorMap ta, tb, to;
-  mx_status_t st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt);
+  mx_status_t st = p.f4 ? make_tmap_packed(&ta, a->data, a->rows, a->cols)
+                        : make_tmap(&ta, a->data, a->rows, a->cols, a->fmt);
   if (st != MX_OK) return st;
-  if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
+  if ((st = p.f4 ? make_tmap_packed(&tb, b->data, b->rows, b->cols)
+                 : make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK)
+    return st;
   if (out.base) {
     st = out.f32 ? make_tmap_out_f32(&to, out.base, out.rows, out.cols, out.ld)
                  : make_tmap_out(&to, out.base, out.rows, out.cols, out.ld);
@@ -1094,14 +1116,14 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) { return 
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned word = 0, dense = 0, quant = 0;
+  unsigned word = 0, dense = 0, f4 = 0, quant = 0;
   if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess ||
-      (e = mx::read_quant_status(&quant)) != cudaSuccess)
+      (e = mx::read_f4_status(&f4)) != cudaSuccess || (e = mx::read_quant_status(&quant)) != cudaSuccess)
     return cuda_fail(e, "reading device status");
   if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess ||
-      (e = mx::reset_quant_status()) != cudaSuccess)
+      (e = mx::reset_f4_status()) != cudaSuccess || (e = mx::reset_quant_status()) != cudaSuccess)
     return cuda_fail(e, "clearing device status");
-  word |= dense | quant;
+  word |= dense | f4 | quant;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
   return MX_OK;

@@ -26,6 +26,7 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                         int bn, cudaStream_t s, int num_sms) {
+  if (p.f4) return launch_gemm_f4(p, ta, tb, to, bn, s, num_sms);
   if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   if (p.epi == EPI_DSWIGLU) {
     if (p.tap != nullptr || p.probs != nullptr)

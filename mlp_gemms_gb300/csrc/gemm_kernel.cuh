@@ -21,7 +21,10 @@
 //   warp 1      owns tensor memory; one lane copies each stage's scale
 //               chunks into tensor memory (tcgen05.cp 32x128b.warpx4) and
 //               issues tcgen05.mma .kind::mxf8f6f4.block_scale (M=128, N=BN,
-//               K=32 per instruction, fp32 accumulators in tensor memory);
+//               K=32 per instruction, fp32 accumulators in tensor memory),
+//               or .kind::mxf4 for packed E2M1 operands (F4: K=64 per
+//               instruction, a stage holds 256 K-elements and two scale
+//               chunks per 128-row block);
 //   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
 //               32*(w%4)..+31, two warps per lane quarter split the
 //               columns), then the fused math and stores.
@@ -47,14 +50,18 @@ template <int EPI> constexpr int kThreads() { return EPI == EPI_DSWIGLU ? NUM_TH
 constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
 
-template <int BN, bool ZR = false>
+// F4: packed E2M1 operands on .kind::mxf4.  A stage's 128-byte rows then
+// hold 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
+template <int BN, bool ZR = false, bool F4 = false>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : (ZR ? 4 : 5);
+  static constexpr int KC = F4 ? 2 : 1;
+  static constexpr int STAGES = BN == 256 ? (F4 ? 3 : 4) : (ZR ? 4 : 5);
   static constexpr int ACC = BN == 256 ? 1 : 2;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int SF_BYTES = 512 + (BN / 128) * 512;
-  static constexpr int SF_COLS = 4 + 4 * (BN / 128);
+  static constexpr int SF_A_BYTES = KC * 512;  // A's chunks, then B's (chunk-major)
+  static constexpr int SF_BYTES = KC * (512 + (BN / 128) * 512);
+  static constexpr int SF_COLS = KC * (4 + 4 * (BN / 128));
   static constexpr uint32_t TX = A_BYTES + B_BYTES + SF_BYTES;
   static constexpr int TB_BYTES = 2560;  // 512-byte multiple: TMA store swizzle atoms
   static constexpr int OFF_A = 0;
@@ -86,7 +93,8 @@ struct Tile {
   int g;
   int64_t m0, n0;
   int64_t kbeg;
-  int nk;
+  int nk;  // pipeline stages (K chunks of 128 elements, 256 with F4)
+  int nc;  // K chunks of 128 elements
 };
 
 __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
@@ -94,10 +102,11 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); 
 // Tile t -> (expert, row base, column base, K range).  Grouped: tiles are
 // row-block-major over all R rows; the expert is the segment holding the
 // row base.  Wgrad: tiles are expert-major; K runs over the expert's rows.
+// nk counts K chunks of 128 elements here.
 template <int NT, int MODE>
-__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
+__device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
   Tile T;
-  T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0;
+  T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0; T.nc = 0;
   if (MODE == MODE_GROUPED) {
     int64_t mt = t / p.n_tiles, nt = t % p.n_tiles;
     T.m0 = mt * 128;
@@ -135,6 +144,16 @@ __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool re
     T.nk = bad ? 0 : (int)((end - start) / 128);
     T.active = 1;
   }
+  return T;
+}
+
+// The same with nk in pipeline stages: with F4 a stage covers two chunks
+// and a tile with an odd chunk count ends on a half stage.
+template <int NT, int MODE, bool F4 = false>
+__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
+  Tile T = get_tile_chunks<NT, MODE>(p, t, report, order);
+  T.nc = T.nk;
+  if (F4) T.nk = (T.nc + 1) >> 1;
   return T;
 }
 
@@ -363,13 +382,14 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 // EXT: the dSwiGLU kernel has a separate instantiation with its optional
 // extras, the debug tap and the routing probabilities (its register budget is
 // tight); the other fused epilogues test those pointers at run time.
-template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false>
+template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false, bool F4 = false>
 __global__ void __launch_bounds__(kThreads<EPI>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
   constexpr bool EXT_ON = EPI != EPI_DSWIGLU || EXT;
-  using C = Cfg<BN, ZR>;
+  static_assert(!F4 || (EPI == EPI_BF16 || EPI == EPI_F32), "mxf4 operands: plain epilogues only");
+  using C = Cfg<BN, ZR, F4>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -441,7 +461,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
         if (!T.active || T.nk == 0) continue;
         int64_t brow[2];
         if (EPI == EPI_SWIGLU) {
@@ -456,19 +476,33 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int kb = 0; kb < T.nk; kb++) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], p.tx_bytes);
+          // F4: the stage's first 128-element chunk and how many it holds
+          // (the second half of a tile's last stage may lie past its K range;
+          // its payload is loaded but no MMA reads it, and its scales are not
+          // loaded)
+          const int nch = F4 ? ((2 * kb + 1 < T.nc) ? 2 : 1) : 1;
+          const int64_t kc = T.kbeg / 128 + (F4 ? 2 * kb : kb);
+          const uint32_t tx = F4 ? (uint32_t)(C::A_BYTES + C::B_BYTES + nch * (512 + (BN / 128) * 512))
+                                 : p.tx_bytes;
+          mbar_arrive_expect_tx(&full[stage], tx);
           armed_parity[stage] = (int)phase;
-          const int64_t kc = T.kbeg / 128 + kb;
-          const int kx = (int)(kc * 128);
+          // x coordinate: elements, or bytes of the packed payload with F4
+          const int kx = (int)(F4 ? kc * 64 : kc * 128);
           tma_load_2d(sA + stage * C::A_BYTES, &tmA, kx, (int)T.m0, &full[stage], pol_a);
 #pragma unroll
           for (int i = 0; i < BN / 128; i++)
             tma_load_2d(sB + stage * C::B_BYTES + i * 16384, &tmB, kx, (int)brow[i], &full[stage], pol_b);
           uint8_t* sf = sSF + stage * C::SF_BYTES;
-          bulk_load(sf, p.sfa + ((T.m0 >> 7) * p.sfa_kchunks + kc) * 512, 512, &full[stage]);
 #pragma unroll
-          for (int i = 0; i < BN / 128; i++)
-            bulk_load(sf + 512 + i * 512, p.sfb + ((brow[i] >> 7) * p.sfb_kchunks + kc) * 512, 512, &full[stage]);
+          for (int c = 0; c < C::KC; c++) {
+            if (c < nch) {
+              bulk_load(sf + c * 512, p.sfa + ((T.m0 >> 7) * p.sfa_kchunks + kc + c) * 512, 512, &full[stage]);
+#pragma unroll
+              for (int i = 0; i < BN / 128; i++)
+                bulk_load(sf + C::SF_A_BYTES + (c * (BN / 128) + i) * 512,
+                          p.sfb + ((brow[i] >> 7) * p.sfb_kchunks + kc + c) * 512, 512, &full[stage]);
+            }
+          }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -489,7 +523,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
         if (!T.active || T.nk == 0) continue;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
         tc_fence_after();
@@ -499,17 +533,43 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tc_fence_after();
           const uint32_t sf_t = tmem_base + C::SF_TMEM_BASE + (uint32_t)(stage * C::SF_COLS);
           const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
-          tc_copy_scales(sf_t, sf_s);
-#pragma unroll
-          for (int i = 0; i < BN / 128; i++) tc_copy_scales(sf_t + 4 + 4 * i, sf_s + 512 + 512 * i);
           const uint32_t a_s = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b_s = smem_u32(sB + stage * C::B_BYTES);
+          if constexpr (F4) {
+            // tensor-memory scale columns: A's chunk c at 4c, B's chunk c
+            // (BN/128 row blocks) at 8 + 4c(BN/128)
+            const int nch = (2 * kb + 1 < T.nc) ? 2 : 1;
 #pragma unroll
-          for (int j = 0; j < 4; j++) {
-            const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
-            const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
-            const uint32_t idesc = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 128, BN, j, j);
-            tc_mma_mx(d_tmem, adesc, bdesc, idesc, sf_t, sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+            for (int c = 0; c < 2; c++) {
+              if (c < nch) {
+                tc_copy_scales(sf_t + 4 * c, sf_s + 512 * c);
+#pragma unroll
+                for (int i = 0; i < BN / 128; i++)
+                  tc_copy_scales(sf_t + 8 + 4 * (c * (BN / 128) + i), sf_s + C::SF_A_BYTES + 512 * (c * (BN / 128) + i));
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              if (j < 2 * nch) {
+                const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
+                const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
+                const uint32_t sid = (uint32_t)(j & 1) * 2u;
+                const uint32_t idesc = mma_idesc_mx(MXF4_E2M1, MXF4_E2M1, 128, BN, sid, sid);
+                tc_mma_mxf4(d_tmem, adesc, bdesc, idesc, sf_t + 4 * (j >> 1), sf_t + 8 + 4 * (j >> 1) * (BN / 128),
+                            (kb | j) != 0 ? 1u : 0u);
+              }
+            }
+          } else {
+            tc_copy_scales(sf_t, sf_s);
+#pragma unroll
+            for (int i = 0; i < BN / 128; i++) tc_copy_scales(sf_t + 4 + 4 * i, sf_s + 512 + 512 * i);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              const uint64_t adesc = smem_desc(a_s + 32 * j, 16, 1024, 2);
+              const uint64_t bdesc = smem_desc(b_s + 32 * j, 16, 1024, 2);
+              const uint32_t idesc = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 128, BN, j, j);
+              tc_mma_mx(d_tmem, adesc, bdesc, idesc, sf_t, sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -536,7 +596,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
         if (!T.active || T.nk == 0) continue;
         for (int hh = 0; hh < 2; hh++) {
           if (!mbar_wait_bounded(&z_empty[zs], zph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
@@ -579,7 +639,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if constexpr (EPI == EPI_DGELU) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) return;
-        const Tile U = get_tile<NT, MODE>(p, t, false, order);
+        const Tile U = get_tile<NT, MODE, F4>(p, t, false, order);
         if (!U.active || U.nk == 0) return;
         const int64_t r = U.m0 + q * 32 + lane;
         prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
@@ -590,7 +650,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int64_t t = tile_index<MODE>(i);
       if (t >= p.num_tiles) continue;
       prefetch_aux(i + 1);
-      Tile T = get_tile<NT, MODE>(p, t, ew == 0 && lane == 0, order);
+      Tile T = get_tile<NT, MODE, F4>(p, t, ew == 0 && lane == 0, order);
       if (!T.active) continue;
       const int64_t row_in_tile = q * 32 + lane;
       if (T.nk == 0) {

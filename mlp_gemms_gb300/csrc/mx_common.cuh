@@ -422,6 +422,22 @@ __device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// Element type code of E2M1 in the .kind::mxf4 instruction descriptor.
+constexpr uint32_t MXF4_E2M1 = 1;
+
+// D[tmem] (+)= (A * 2^sfa) (B * 2^sfb)^T for one K=64 step of packed E2M1
+// operands (two elements per byte, 32 bytes of each row), two scale bytes
+// per row: scale IDs 0 and 2 pick the first or second pair of the four
+// bytes a tensor-memory scale word holds.
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

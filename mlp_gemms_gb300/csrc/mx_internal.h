@@ -56,6 +56,7 @@ struct GemmParams {
   int64_t Mw;               // rows of A (wgrad)
   int64_t F;                // SwiGLU FFN width (FC1 out = 2F)
   int a_type, b_type;       // MMA element types (E4M3 = 0, E2M3 = 3, E2M1 = 5)
+  int f4;                   // packed E2M1 operands on .kind::mxf4 (plain epilogues)
   uint32_t tx_bytes;        // bytes one pipeline stage's copies complete on its barrier
   const uint8_t* sfa;
   const uint8_t* sfb;
@@ -98,6 +99,11 @@ cudaError_t read_gemm_status(unsigned* out);
 cudaError_t reset_gemm_status();
 cudaError_t read_dense_status(unsigned* out);
 cudaError_t reset_dense_status();
+// The BF16 / fp32 epilogues on packed E2M1 operands (.kind::mxf4).
+cudaError_t launch_gemm_f4(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
+                           int bn, cudaStream_t s, int num_sms);
+cudaError_t read_f4_status(unsigned* out);
+cudaError_t reset_f4_status();
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t s);
 
 // The tensors of one MLP step that the host pipeline moves: raw inputs the
