@@ -110,23 +110,29 @@ template <> struct SrGrid<E2M1> { static constexpr int M = 1, EMIN = 0; static c
 
 // A scaled value rounded stochastically onto the format's grid: saturating
 // at +-max; otherwise the lower neighbour lo = floor(|a| / spacing) * spacing
-// (spacing = 2^(max(E, emin) - m), E the fp32 exponent of |a|) or lo +
-// spacing, the latter when (u >> 8) < frac * 2^24 with frac = (|a| - lo) /
-// spacing.  Every step is exact in fp32.  The result is on the grid, so the
+// (spacing = 2^es, es = max(E, emin) - m, E the fp32 exponent of |a|) or
+// lo + spacing, the latter when (u >> 8) < frac * 2^24 with frac = (|a| - lo)
+// / spacing.  Evaluated with full-rate operations only, every step exact:
+// lo = (|a| + 2^(es+23)) rounded toward zero, minus 2^(es+23); the
+// comparison as (u >> 8) * 2^(es-24) < |a| - lo, that threshold assembled
+// from the bits of u (2^(es-1) + (bits 8..30) * 2^(es-24), less 2^(es-1)
+// unless bit 31 is set).  The result is on the grid, so the
 // round-to-nearest conversion that follows is exact; the sign (of zero too)
 // is kept.
 template <int FMT>
 __device__ __forceinline__ float sr_round(float a_signed, uint32_t u) {
+  constexpr int M = SrGrid<FMT>::M;
   const float a = fabsf(a_signed);
-  if (!(a < SrGrid<FMT>::VMAX)) return copysignf(SrGrid<FMT>::VMAX, a_signed);
-  const int e = (int)(__float_as_uint(a) >> 23) - 127;
-  const int es = (e > SrGrid<FMT>::EMIN ? e : SrGrid<FMT>::EMIN) - SrGrid<FMT>::M;
-  const float sp = __uint_as_float((uint32_t)(es + 127) << 23);      // 2^es, a normal power of two
-  const float isp = __uint_as_float((uint32_t)(127 - es) << 23);     // 2^-es
-  const float lo = floorf(a * isp) * sp;
-  const float frac = (a - lo) * isp;
-  const bool up = (float)(u >> 8) < frac * 16777216.0f;
-  return copysignf(up ? lo + sp : lo, a_signed);
+  const uint32_t bc = max(__float_as_uint(a) >> 23, (uint32_t)(127 + SrGrid<FMT>::EMIN));  // biased max(E, emin)
+  const float c = __uint_as_float((bc - M + 23) << 23);                  // 2^(es+23)
+  const float lo = __fadd_rz(a, c) - c;
+  const float rem = a - lo;
+  const uint32_t h = (bc - M - 1) << 23;                                 // 2^(es-1)
+  const float hp = __uint_as_float(h | ((u >> 8) & 0x7FFFFFu));
+  const float thr = (u >> 31) ? hp : hp - __uint_as_float(h);
+  const float sp = __uint_as_float((bc - M) << 23);
+  const float r = thr < rem ? lo + sp : lo;
+  return copysignf(a < SrGrid<FMT>::VMAX ? r : SrGrid<FMT>::VMAX, a_signed);
 }
 
 // Stochastic-rounding variant of the block packer: element i of the block is
