@@ -323,6 +323,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     dense = dense_step_rate(mx, torch, dev) if not args.no_extra else None
     fwd_even = moe_forward_even_rate(mx, torch, dev) if not args.no_extra else None
+    variants = variant_rates(mx, torch, dev) if not args.no_extra else None
     status = mx.mx_get_device_status()
     if status != "MX_OK":
         raise RuntimeError("device status: " + status)
@@ -369,6 +370,7 @@ def run_gpu(args):
         "quantizer": quant,
         "dense_mxfp6_step": dense,
         "moe_fwd_even_routing": fwd_even,
+        "variants": variants,
     }
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(seconds_hint=args.cpu_seconds)
@@ -553,6 +555,111 @@ def moe_forward_even_rate(mx, torch, dev, steps=5):
     ms = e0.elapsed_time(e1) / steps
     return {"workload": "moe fwd (quantize + FC1 SwiGLU + FC2), even routing 2048 rows/expert",
             "ms": ms, "tflops": 6.0 * R * D * F / (ms * 1e-3) / 1e12}
+
+
+def _event_mean(torch, stream, dev, fn, reps, before=None):
+    """Mean CUDA-event time of fn over reps launches (before() runs outside
+    the bracket, e.g. an L2 flush)."""
+    ts = []
+    for _ in range(reps):
+        if before is not None:
+            before()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    return float(np.mean(ts))
+
+
+def variant_rates(mx, torch, dev, reps=10):
+    """The optional forms of the stages beside their plain forms, timed the
+    same way: FC1 + SwiGLU and FC2 dgrad + dSwiGLU with routing
+    probabilities (the backward adds its dprobs reduction launch), the dW1
+    weight gradient into an fp32 main-grad buffer (store and accumulate),
+    and the standalone quantizer workload to MXFP4 with round-to-nearest and
+    with stochastic rounding (L2 flushed between iterations)."""
+    import workloads as W
+    G, D, F, R = SHAPE["G"], SHAPE["D"], SHAPE["F"], SHAPE["R"]
+    stream = torch.cuda.current_stream(dev)
+    offs = torch.from_numpy(W.zipf_offsets(G, R)).to(dev)
+    inp = W.moe_inputs_device(G, D, F, R, seed=7, device=dev)
+    qx = (mx.MX(R, D), mx.MX(D, R))
+    qw1 = (mx.MX(G * 2 * F, D), mx.MX(G * D, 2 * F))
+    qw2 = (mx.MX(G * D, F), mx.MX(G * F, D))
+    qdy = (mx.MX(R, D), mx.MX(D, R))
+    for k, q in (("x", qx), ("w1", qw1), ("w2", qw2), ("dy", qdy)):
+        mx.mx_quantize(inp[k], 0, True, True, out_row=q[0], out_col=q[1])
+    del inp
+    h = (mx.MX(R, F), mx.MX(F, R))
+    dz = (mx.MX(R, 2 * F), mx.MX(2 * F, R))
+    z = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    probs = torch.rand(R, generator=g, device=dev)
+    dprobs = torch.empty(R, dtype=torch.float32, device=dev)
+    pws = torch.empty(max(16, int(mx.load().mx_dswiglu_probs_workspace_bytes(R, F))), dtype=torch.uint8, device=dev)
+    dw1 = torch.empty((G, 2 * F, D), dtype=torch.bfloat16, device=dev)
+    dw1_f32 = torch.zeros((G, 2 * F, D), dtype=torch.float32, device=dev)
+    calls = {
+        "fc1_swiglu": lambda: mx.mx_grouped_gemm_swiglu_fwd(qx[0], qw1[0], G, offs, h[0], h[1], z),
+        "fc1_swiglu_probs": lambda: mx.mx_grouped_gemm_swiglu_probs_fwd(qx[0], qw1[0], G, offs, probs, h[0], h[1],
+                                                                       z),
+        "fc2_dgrad_dswiglu": lambda: mx.mx_grouped_gemm_dswiglu_bwd(qdy[0], qw2[1], z, G, offs, dz[0], dz[1]),
+        "fc2_dgrad_dswiglu_probs": lambda: mx.mx_grouped_gemm_dswiglu_probs_bwd(
+            qdy[0], qw2[1], z, probs, G, offs, dz[0], dz[1], dprobs, workspace=pws),
+        "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad(dz[1], qx[1], G, offs, out=dw1),
+        "wgrad_dw1_f32_store": lambda: mx.mx_grouped_gemm_wgrad_f32(dz[1], qx[1], G, offs, dw1_f32, False),
+        "wgrad_dw1_f32_accumulate": lambda: mx.mx_grouped_gemm_wgrad_f32(dz[1], qx[1], G, offs, dw1_f32, True),
+    }
+    for c in calls.values():
+        c()
+        c()
+    torch.cuda.synchronize(dev)
+    sums = {k: 0.0 for k in calls}
+    for _ in range(reps):  # interleaved, so that clock drift hits every form alike
+        for k, c in calls.items():
+            sums[k] += _event_mean(torch, stream, dev, c, 1)
+    sf = stage_flops(D, F, R)
+    res = {}
+    for k, s in sums.items():
+        ms = s / reps
+        base = k.split("_probs")[0].split("_f32")[0]
+        res[k] = {"ms": ms, "tflops": sf[base] / (ms * 1e-3) / 1e12}
+    res["launches"] = {"fc2_dgrad_dswiglu_probs": 2, "others": 1}
+    del qx, qw1, qw2, qdy, h, dz, z, dw1, dw1_f32
+    torch.cuda.empty_cache()
+
+    rows, cols = W.QUANT_SHAPE["rows"], W.QUANT_SHAPE["cols"]
+    x = (torch.randn((rows, cols), generator=g, device=dev)).to(torch.bfloat16)
+    r, c = mx.MX(rows, cols, mx.E2M1), mx.MX(cols, rows, mx.E2M1)
+    rh, ch = mx.MX(rows, cols, mx.E2M1, True), mx.MX(cols, rows, mx.E2M1, True)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    qcalls = {
+        "quant_e2m1_rne": lambda: mx.mx_quantize(x, mx.E2M1, True, True, out_row=r, out_col=c),
+        "quant_e2m1_sr": lambda: mx.mx_quantize_sr(x, mx.E2M1, 1234, True, True, out_row=r, out_col=c),
+        "quant_e2m1_had_rne": lambda: mx.mx_quantize(x, mx.E2M1, True, True, True, out_row=rh, out_col=ch),
+        "quant_e2m1_had_sr": lambda: mx.mx_quantize_sr(x, mx.E2M1, 1234, True, True, True, out_row=rh, out_col=ch),
+    }
+    for qc in qcalls.values():
+        qc()
+    qsums = {k: 0.0 for k in qcalls}
+    for _ in range(reps):
+        for k, qc in qcalls.items():
+            qsums[k] += _event_mean(torch, stream, dev, qc, 1, before=lambda: flush.fill_(1))
+    n = rows * cols
+    qbytes = n * 2 + 2 * n * (0.5 + 1.0 / 32)  # BF16 in; two MXFP4 copies out
+    peaks, _ = measured_peaks()
+    for k, s in qsums.items():
+        ms = s / reps
+        gbs = qbytes / (ms * 1e-3) / 1e9
+        res[k] = {"us": ms * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
+    res["quant_workload"] = "8192x7168 bf16 -> mxfp4 row+col, L2 flushed (512 MB write) between iterations"
+    status = mx.mx_get_device_status()
+    if status != "MX_OK":
+        raise RuntimeError("device status after variants: " + status)
+    return res
 
 
 def quantizer_rate(mx, torch, dev):
