@@ -340,6 +340,78 @@ def wgrad(a_col, b_col, offsets):
 
 
 # --------------------------------------------------------------------------
+# Token permute and un-permute (Primus PR #1247 "Qwen3-30B-A3B FP8 on MI355X
+# to 40k tokens/s/GPU", DeepEP permute section: the dispatched tokens are
+# quantized as part of the permute that hands them to the grouped MLP, and
+# the un-permute's backward hands back the quantized output gradient).
+# Readings where the page is silent: routed rows are grouped by expert in
+# ascending expert order, within an expert in (token, choice) order; every
+# expert's segment is padded with empty rows to a multiple of 128 (the
+# grouped GEMM's segment alignment); an empty row is all zeros.
+# --------------------------------------------------------------------------
+
+def moe_route_index(topk, G, pad=128):
+    """topk int [T, k] expert ids -> (offsets [G] cumulative padded segment
+    ends, src [R] token of each routed row or -1 for a padding row with
+    R = offsets[-1], row_of [T, k] routed row of each (token, choice))."""
+    topk = np.asarray(topk)
+    T, k = topk.shape
+    members = [[] for _ in range(G)]
+    for t in range(T):
+        for j in range(k):
+            e = int(topk[t, j])
+            if not 0 <= e < G:
+                raise ValueError("expert id %d out of range" % e)
+            members[e].append((t, j))
+    offsets = np.zeros(G, dtype=np.int32)
+    src = []
+    row_of = np.full((T, k), -1, dtype=np.int32)
+    for e in range(G):
+        for t, j in members[e]:
+            row_of[t, j] = len(src)
+            src.append(t)
+        while len(src) % pad:
+            src.append(-1)
+        offsets[e] = len(src)
+    return offsets, np.array(src, dtype=np.int32), row_of
+
+
+def permute_rows(x, src):
+    """out[r] = x[src[r]], or a zero row where src[r] < 0 (any dtype; BF16
+    bit patterns give +0.0 rows)."""
+    x = np.asarray(x)
+    src = np.asarray(src)
+    out = np.zeros((len(src),) + x.shape[1:], dtype=x.dtype)
+    for r, t in enumerate(src.tolist()):
+        if t >= 0:
+            out[r] = x[t]
+    return out
+
+
+def permute_quantize(x_bits, src, fmt=E4M3, row=True, col=True):
+    """The quantized permute: the routed rows of BF16 x, quantized in the
+    permuted order (rowwise blocks along D, columnwise blocks of 32 routed
+    rows)."""
+    return quantize_bf16(permute_rows(x_bits, src), fmt, row, col)
+
+
+def unpermute(y, row_of, weights=None):
+    """out[t] = sum over choices j with row_of[t, j] >= 0 of
+    w[t, j] * y[row_of[t, j]] (w = 1 without weights), float64: the
+    combine after the experts, and the backward of the permute."""
+    y = np.asarray(y, dtype=np.float64)
+    row_of = np.asarray(row_of)
+    T, k = row_of.shape
+    out = np.zeros((T,) + y.shape[1:])
+    for t in range(T):
+        for j in range(k):
+            r = int(row_of[t, j])
+            if r >= 0:
+                out[t] += (1.0 if weights is None else float(weights[t, j])) * y[r]
+    return out
+
+
+# --------------------------------------------------------------------------
 # Activations (float64)
 # --------------------------------------------------------------------------
 
