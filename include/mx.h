@@ -17,6 +17,10 @@
  *               commit, bias commits.
  *   [MXFP4-guide] ROCm Primus guide "MXFP4 training for Flux models",
  *               Overview.
+ *   [PERMUTE-PR] Primus PR #1247 "Qwen3-30B-A3B FP8 on MI355X to 40k
+ *               tokens/s/GPU" -- DeepEP permute section (tokens quantized
+ *               as part of the permute; the un-permute's backward returns a
+ *               quantized gradient).
  *
  * Common conventions
  *   - Every pointer named *_dev or held in an mx_tensor_t is DEVICE memory of
@@ -161,6 +165,83 @@ MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, 
 MX_API mx_status_t mx_quantize_sr(const void *x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
                                   int32_t fmt, uint32_t flags, uint64_t seed, const mx_tensor_t *out_row,
                                   const mx_tensor_t *out_col, mx_stream_t stream);
+
+/*
+ * Token permute for the expert MLP ([PERMUTE-PR]).  Routed rows are grouped
+ * by expert, experts ascending; within an expert in (token, choice) order;
+ * each expert's segment is padded with empty rows to a multiple of 128 (the
+ * grouped GEMMs' segment alignment).  An empty row has source -1 and is
+ * all zeros.  Readings of ours where the page is silent: that order, the
+ * padding, and -1 for empty rows.
+ *
+ * mx_moe_route_rows -- the routed-row capacity R_cap to allocate for T
+ * tokens, k choices and G experts: T*k + 127*G rounded up to 128 (every
+ * padded routing fits).  Negative arguments give 0.
+ * mx_moe_route_workspace_bytes -- device workspace of mx_moe_route_index.
+ */
+MX_API int64_t mx_moe_route_rows(int64_t T, int32_t k, int32_t G);
+MX_API size_t mx_moe_route_workspace_bytes(int64_t T, int32_t k, int32_t G);
+
+/*
+ * mx_moe_route_index -- the routing index from the router's choices.
+ *   topk_dev     int32 [T, k]: expert id of each (token, choice), in [0, G)
+ *   offsets_dev  out int32 [G]: cumulative padded segment ends (the grouped
+ *                GEMMs' offsets); offsets[G-1] routed rows are in use
+ *   src_dev      out int32 [R_cap]: source token of each routed row, -1 for
+ *                an empty row (also every row from offsets[G-1] on)
+ *   row_of_dev   out int32 [T, k]: routed row of each (token, choice), -1
+ *                for an out-of-range expert id
+ *   workspace    >= mx_moe_route_workspace_bytes(T, k, G) bytes
+ * Deterministic (a stable counting sort, no order-dependent atomics); four
+ * launches.  Expert ids outside [0, G) are skipped and reported as
+ * MX_ERR_INVALID_ARG by mx_get_device_status.
+ * Errors: MX_ERR_INVALID_ARG (null pointer, k < 1, G < 1 or G > 1024),
+ * MX_ERR_SHAPE (R_cap < mx_moe_route_rows(T, k, G)), MX_ERR_WORKSPACE.
+ */
+MX_API mx_status_t mx_moe_route_index(const int32_t *topk_dev, int64_t T, int32_t k, int32_t G, int32_t *offsets_dev,
+                                      int32_t *src_dev, int64_t R_cap, int32_t *row_of_dev, void *workspace,
+                                      size_t workspace_bytes, mx_stream_t stream);
+
+/*
+ * mx_permute_quantize -- the quantizing permute: routed row r of the output
+ * is the MX quantization of token src[r] of x (a zero row where src[r] <
+ * 0), rowwise and/or columnwise, in one pass over the tokens with no
+ * permuted BF16 copy.  The rowwise bytes equal the gathered rowwise
+ * quantization of the tokens (blocks lie in one row); the columnwise blocks
+ * are 32 consecutive routed rows, as the wgrad needs them.  Used for X
+ * before FC1 and for dY after the un-permute's backward (a gather of the
+ * tokens' gradient with unit weights).
+ *   x_bf16       device BF16 [T, D], row stride ld elements (ld % 8 == 0)
+ *   src_dev      int32 [R_cap] (from mx_moe_route_index)
+ *   offsets_dev  int32 [G]: rows from offsets[G-1] on are not written (NULL:
+ *                all R_cap rows are)
+ *   fmt, flags   element format; MX_ROWWISE and/or MX_COLWISE only
+ *   out_row      MX_ROWWISE: tensor [R_cap, D]
+ *   out_col      MX_COLWISE: tensor [D, R_cap]
+ * Shapes: D % 32 == 0, R_cap % 128 == 0.  A source index >= T is read as an
+ * empty row and reported as MX_ERR_INVALID_ARG by mx_get_device_status.
+ */
+MX_API mx_status_t mx_permute_quantize(const void *x_bf16, int64_t T, int64_t D, int64_t ld, const int32_t *src_dev,
+                                       int64_t R_cap, const int32_t *offsets_dev, int32_t G, int32_t fmt,
+                                       uint32_t flags, const mx_tensor_t *out_row, const mx_tensor_t *out_col,
+                                       mx_stream_t stream);
+
+/*
+ * mx_moe_unpermute -- out[t] = sum over j of w[t, j] * in[row_of[t, j]]
+ * (w = 1 when weights_dev is NULL; choices with row -1 skipped): the
+ * combine of the experts' outputs, and the backward of the permute (dX of
+ * the tokens from dX of the routed rows).  fp32 accumulation in choice
+ * order, one rounding to BF16.
+ *   in_bf16      device BF16 [R, D], contiguous rows
+ *   row_of_dev   int32 [T, k]
+ *   weights_dev  fp32 [T, k] or NULL
+ *   out_bf16     device BF16 [T, D], contiguous rows
+ * Shapes: D % 8 == 0.  A row index >= R is skipped and reported as
+ * MX_ERR_INVALID_ARG by mx_get_device_status.
+ */
+MX_API mx_status_t mx_moe_unpermute(const void *in_bf16, int64_t R, int64_t D, const int32_t *row_of_dev,
+                                    const float *weights_dev, int64_t T, int32_t k, void *out_bf16,
+                                    mx_stream_t stream);
 
 /*
  * mx_quantize_colsum_noalloc -- mx_quantize with MX_COLSUM for callers that

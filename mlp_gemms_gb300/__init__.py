@@ -35,7 +35,8 @@ ABI_SYMBOLS = (
     "mx_gemm_dgelu_workspace_bytes", "mx_gemm_dgelu_bwd", "mx_quantize_colsum_noalloc", "mx_debug_tap",
     "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
     "mx_grouped_gemm_wgrad_f32", "mx_grouped_gemm_swiglu_probs_fwd", "mx_dswiglu_probs_workspace_bytes",
-    "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr",
+    "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr", "mx_moe_route_rows", "mx_moe_route_workspace_bytes",
+    "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute",
 )
 
 
@@ -106,6 +107,11 @@ def load(path=None):
         "mx_gemm_dgelu_bwd": (ctypes.c_int, [tp, tp, vp, tp, tp, vp, vp, sz, vp]),
         "mx_quantize_colsum_noalloc": (ctypes.c_int, [vp, i64, i64, i64, i32, u32, tp, tp, vp, vp]),
         "mx_quantize_sr": (ctypes.c_int, [vp, i64, i64, i64, i64, i32, u32, ctypes.c_uint64, tp, tp, vp]),
+        "mx_moe_route_rows": (i64, [i64, i32, i32]),
+        "mx_moe_route_workspace_bytes": (sz, [i64, i32, i32]),
+        "mx_moe_route_index": (ctypes.c_int, [vp, i64, i32, i32, vp, vp, i64, vp, vp, sz, vp]),
+        "mx_permute_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, i64, vp, i32, i32, u32, tp, tp, vp]),
+        "mx_moe_unpermute": (ctypes.c_int, [vp, i64, i64, vp, vp, i64, i32, vp, vp]),
         "mx_debug_tap": (ctypes.c_int, [vp, i64]),
         "mx_mlp_pipeline_create": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp, ctypes.POINTER(vp)]),
         "mx_mlp_pipeline_run": (ctypes.c_int, [vp, ctypes.POINTER(HostIOStruct)]),
@@ -218,6 +224,62 @@ def mx_quantize_sr(x, fmt, seed, rowwise=True, colwise=True, hadamard=False, out
                                  _s(out_row) if rowwise else None, _s(out_col) if colwise else None,
                                  _stream(stream)))
     return out_row, out_col
+
+
+def mx_moe_route_rows(T, k, G):
+    return int(load().mx_moe_route_rows(T, k, G))
+
+
+def mx_moe_route_index(topk, G, R_cap=None, offsets=None, src=None, row_of=None, workspace=None, stream=None):
+    """topk int32 [T, k] expert ids on the GPU -> (offsets [G], src [R_cap],
+    row_of [T, k]) of the token permute."""
+    import torch
+    assert topk.dtype == torch.int32 and topk.is_contiguous()
+    T, k = topk.shape
+    dev = topk.device
+    R_cap = R_cap if R_cap is not None else mx_moe_route_rows(T, k, G)
+    offsets = offsets if offsets is not None else torch.empty(G, dtype=torch.int32, device=dev)
+    src = src if src is not None else torch.empty(R_cap, dtype=torch.int32, device=dev)
+    row_of = row_of if row_of is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
+    nbytes = int(load().mx_moe_route_workspace_bytes(T, k, G))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    _check(load().mx_moe_route_index(_ptr(topk), T, k, G, _ptr(offsets), _ptr(src), R_cap, _ptr(row_of),
+                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+    return offsets, src, row_of
+
+
+def mx_permute_quantize(x, src, offsets=None, G=0, fmt=E4M3, rowwise=True, colwise=True, out_row=None,
+                        out_col=None, stream=None):
+    """The quantizing permute of BF16 tokens x [T, D] by src [R_cap]:
+    returns (out_row [R_cap, D], out_col [D, R_cap])."""
+    import torch
+    assert x.dtype == torch.bfloat16 and src.dtype == torch.int32
+    T, D = x.shape
+    R_cap = src.numel()
+    if offsets is not None and not G:
+        G = offsets.numel()
+    flags = (ROWWISE if rowwise else 0) | (COLWISE if colwise else 0)
+    if rowwise and out_row is None:
+        out_row = MX(R_cap, D, fmt, False, x.device)
+    if colwise and out_col is None:
+        out_col = MX(D, R_cap, fmt, False, x.device)
+    _check(load().mx_permute_quantize(_ptr(x), T, D, x.stride(0), _ptr(src), R_cap, _ptr(offsets), int(G), fmt, flags,
+                                      _s(out_row) if rowwise else None, _s(out_col) if colwise else None,
+                                      _stream(stream)))
+    return out_row, out_col
+
+
+def mx_moe_unpermute(inp, row_of, weights=None, out=None, stream=None):
+    """out[t] = sum_j w[t, j] * inp[row_of[t, j]] in BF16 (fp32 sums)."""
+    import torch
+    assert inp.dtype == torch.bfloat16 and inp.is_contiguous() and row_of.dtype == torch.int32
+    R, D = inp.shape
+    T, k = row_of.shape
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.bfloat16, device=inp.device)
+    _check(load().mx_moe_unpermute(_ptr(inp), R, D, _ptr(row_of), _ptr(weights), T, k, _ptr(out), _stream(stream)))
+    return out
 
 
 def mx_quantize_colsum_noalloc(x, fmt=E4M3, rowwise=True, hadamard=False, out_row=None, out_col=None,

@@ -467,6 +467,119 @@ mx_status_t mx_quantize_sr(const void* x_bf16, int64_t batch, int64_t rows, int6
                        stream);
 }
 
+int64_t mx_moe_route_rows(int64_t T, int32_t k, int32_t G) {
+  if (T < 0 || k < 0 || G < 0) return 0;
+  return (T * k + 127ll * G + 127) / 128 * 128;
+}
+
+size_t mx_moe_route_workspace_bytes(int64_t T, int32_t k, int32_t G) {
+  if (T < 0 || k < 0 || G < 0) return 0;
+  const int64_t chunks = (T * k + mx::kRouteChunk - 1) / mx::kRouteChunk;
+  return (size_t)(chunks > 0 ? chunks : 1) * (size_t)G * sizeof(int32_t);
+}
+
+mx_status_t mx_moe_route_index(const int32_t* topk_dev, int64_t T, int32_t k, int32_t G, int32_t* offsets_dev,
+                               int32_t* src_dev, int64_t R_cap, int32_t* row_of_dev, void* workspace,
+                               size_t workspace_bytes, mx_stream_t stream) {
+  MX_CHECK(T >= 0 && k >= 1, MX_ERR_INVALID_ARG, "T = %lld, k = %d", (long long)T, k);
+  MX_CHECK(G >= 1 && G <= 1024, MX_ERR_INVALID_ARG, "G = %d is outside [1, 1024]", G);
+  MX_CHECK(T * k < (1ll << 31), MX_ERR_SHAPE, "T * k = %lld exceeds the int32 row range", (long long)(T * k));
+  MX_CHECK(R_cap >= mx_moe_route_rows(T, k, G) && R_cap < (1ll << 31), MX_ERR_SHAPE,
+           "R_cap = %lld; mx_moe_route_rows gives %lld", (long long)R_cap, (long long)mx_moe_route_rows(T, k, G));
+  MX_CHECK(offsets_dev != nullptr && src_dev != nullptr, MX_ERR_INVALID_ARG, "offsets or src is NULL");
+  MX_CHECK(T == 0 || (topk_dev != nullptr && row_of_dev != nullptr), MX_ERR_INVALID_ARG, "topk or row_of is NULL");
+  MX_CHECK(aligned16(topk_dev) && aligned16(offsets_dev) && aligned16(src_dev) && aligned16(row_of_dev),
+           MX_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+  MX_CHECK(workspace != nullptr && aligned16(workspace) && workspace_bytes >= mx_moe_route_workspace_bytes(T, k, G),
+           MX_ERR_WORKSPACE, "mx_moe_route_index needs %zu bytes of 16-byte aligned workspace",
+           mx_moe_route_workspace_bytes(T, k, G));
+  DevInfo dev;
+  mx_status_t st;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  cudaError_t e = mx::launch_route_index(topk_dev, T, k, G, offsets_dev, src_dev, R_cap, row_of_dev,
+                                         static_cast<int32_t*>(workspace), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "routing index launch");
+  return MX_OK;
+}
+
+mx_status_t mx_permute_quantize(const void* x_bf16, int64_t T, int64_t D, int64_t ld, const int32_t* src_dev,
+                                int64_t R_cap, const int32_t* offsets_dev, int32_t G, int32_t fmt, uint32_t flags,
+                                const mx_tensor_t* out_row, const mx_tensor_t* out_col, mx_stream_t stream) {
+  MX_CHECK(fmt >= MX_E4M3 && fmt <= MX_E2M1, MX_ERR_INVALID_ARG, "fmt = %d is not an MX element format", fmt);
+  MX_CHECK((flags & ~(uint32_t)(MX_ROWWISE | MX_COLWISE)) == 0, MX_ERR_NOT_SUPPORTED,
+           "the quantizing permute takes MX_ROWWISE / MX_COLWISE only (flags 0x%x)", flags);
+  MX_CHECK(flags & (MX_ROWWISE | MX_COLWISE), MX_ERR_INVALID_ARG, "neither MX_ROWWISE nor MX_COLWISE requested");
+  MX_CHECK(T >= 0 && D > 0 && D % 32 == 0, MX_ERR_SHAPE, "T = %lld, D = %lld (D %% 32 == 0)", (long long)T,
+           (long long)D);
+  MX_CHECK(R_cap >= 0 && R_cap % 128 == 0 && R_cap < (1ll << 31), MX_ERR_SHAPE,
+           "R_cap = %lld is not a multiple of 128", (long long)R_cap);
+  MX_CHECK(ld >= D && ld % 8 == 0, MX_ERR_ALIGNMENT, "ld = %lld must be >= D and a multiple of 8", (long long)ld);
+  MX_CHECK(T == 0 || x_bf16 != nullptr, MX_ERR_INVALID_ARG, "x is NULL");
+  MX_CHECK(src_dev != nullptr || R_cap == 0, MX_ERR_INVALID_ARG, "src is NULL");
+  MX_CHECK(aligned16(x_bf16) && aligned16(src_dev) && aligned16(offsets_dev), MX_ERR_ALIGNMENT,
+           "pointers must be 16-byte aligned");
+  MX_CHECK(offsets_dev == nullptr || G >= 1, MX_ERR_INVALID_ARG, "G = %d with offsets", G);
+  MX_CHECK(T * ld < (1ll << 40), MX_ERR_SHAPE, "input too large");
+  mx_status_t st;
+  if (flags & MX_ROWWISE) {
+    if ((st = check_tensor(out_row, "out_row", R_cap, D, fmt, 0)) != MX_OK) return st;
+  }
+  if (flags & MX_COLWISE) {
+    if ((st = check_tensor(out_col, "out_col", D, R_cap, fmt, 0)) != MX_OK) return st;
+  }
+  if (R_cap == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::QuantLaunch q;
+  q.x = T > 0 ? x_bf16 : (flags & MX_ROWWISE ? out_row->data : out_col->data);  // never read when T == 0
+  q.batch = 1; q.rows = R_cap; q.cols = D; q.ld = ld;
+  q.fmt = fmt; q.hadamard = 0;
+  q.row_data = (flags & MX_ROWWISE) ? static_cast<uint8_t*>(out_row->data) : nullptr;
+  q.row_scale = (flags & MX_ROWWISE) ? out_row->scale : nullptr;
+  q.col_data = (flags & MX_COLWISE) ? static_cast<uint8_t*>(out_col->data) : nullptr;
+  q.col_scale = (flags & MX_COLWISE) ? out_col->scale : nullptr;
+  q.colsum_partials = nullptr;
+  q.colsum = nullptr;
+  q.num_sms = dev.sms;
+  q.src = src_dev; q.src_rows = T; q.offsets = offsets_dev; q.G = G;
+  // the gather form reads x with plain copies; the map is an unused kernel argument
+  if (T > 0) {
+    if ((st = make_tmap_bf16(&q.xmap, x_bf16, T, D, ld)) != MX_OK) return st;
+  } else if ((st = make_tmap_bytes(&q.xmap, q.row_data ? q.row_data : q.col_data, 128, 128)) != MX_OK) {
+    return st;
+  }
+  q.rowmap = q.colmap = q.xmap;
+  if (fmt == MX_E4M3 && (flags & MX_ROWWISE)) {
+    if ((st = make_tmap_bytes(&q.rowmap, out_row->data, R_cap, D)) != MX_OK) return st;
+  }
+  if (fmt == MX_E4M3 && (flags & MX_COLWISE)) {
+    if ((st = make_tmap_bytes(&q.colmap, out_col->data, D, R_cap)) != MX_OK) return st;
+  }
+  cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantizing permute launch");
+  return MX_OK;
+}
+
+mx_status_t mx_moe_unpermute(const void* in_bf16, int64_t R, int64_t D, const int32_t* row_of_dev,
+                             const float* weights_dev, int64_t T, int32_t k, void* out_bf16, mx_stream_t stream) {
+  MX_CHECK(R >= 0 && T >= 0 && k >= 1, MX_ERR_INVALID_ARG, "R = %lld, T = %lld, k = %d", (long long)R, (long long)T, k);
+  MX_CHECK(D > 0 && D % 8 == 0, MX_ERR_SHAPE, "D = %lld is not a positive multiple of 8", (long long)D);
+  MX_CHECK(T == 0 || (in_bf16 != nullptr || R == 0) && row_of_dev != nullptr && out_bf16 != nullptr,
+           MX_ERR_INVALID_ARG, "in, row_of or out is NULL");
+  MX_CHECK(aligned16(in_bf16) && aligned16(row_of_dev) && aligned16(weights_dev) && aligned16(out_bf16),
+           MX_ERR_ALIGNMENT, "pointers must be 16-byte aligned");
+  MX_CHECK(R * D < (1ll << 40) && T * D < (1ll << 40) && T * k < (1ll << 31), MX_ERR_SHAPE, "input too large");
+  if (T == 0) return MX_OK;
+  DevInfo dev;
+  mx_status_t st;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  cudaError_t e = mx::launch_unpermute(static_cast<const uint16_t*>(in_bf16), R, D, row_of_dev, weights_dev, T, k,
+                                       static_cast<uint16_t*>(out_bf16), dev.sms,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "un-permute launch");
+  return MX_OK;
+}
+
 mx_status_t mx_quantize_colsum_noalloc(const void* x_bf16, int64_t rows, int64_t cols, int64_t ld, int32_t fmt,
                                        uint32_t flags, const mx_tensor_t* out_row, const mx_tensor_t* out_col,
                                        float* colsum, mx_stream_t stream) {
@@ -1116,16 +1229,19 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) { return 
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned word = 0, dense = 0, f4 = 0, quant = 0;
+  unsigned word = 0, dense = 0, f4 = 0, quant = 0, perm = 0;
   if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess ||
-      (e = mx::read_f4_status(&f4)) != cudaSuccess || (e = mx::read_quant_status(&quant)) != cudaSuccess)
+      (e = mx::read_f4_status(&f4)) != cudaSuccess || (e = mx::read_quant_status(&quant)) != cudaSuccess ||
+      (e = mx::read_perm_status(&perm)) != cudaSuccess)
     return cuda_fail(e, "reading device status");
   if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess ||
-      (e = mx::reset_f4_status()) != cudaSuccess || (e = mx::reset_quant_status()) != cudaSuccess)
+      (e = mx::reset_f4_status()) != cudaSuccess || (e = mx::reset_quant_status()) != cudaSuccess ||
+      (e = mx::reset_perm_status()) != cudaSuccess)
     return cuda_fail(e, "clearing device status");
-  word |= dense | f4 | quant;
+  word |= dense | f4 | quant | perm;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
+  if (word & 4u) return fail(MX_ERR_INVALID_ARG, "a routing index (expert id or routed row) was out of range");
   return MX_OK;
 }
 

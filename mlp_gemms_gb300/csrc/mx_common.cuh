@@ -20,8 +20,9 @@ namespace mx {
 enum Fmt : int { E4M3 = 0, E2M3 = 1, E2M1 = 2 };
 
 // Device status words (one set per translation unit that includes this).
-// bit 0: a bounded wait ran out; bit 1: malformed offsets seen on device.
-enum : unsigned { DEV_TIMEOUT = 1u, DEV_BAD_OFFSETS = 2u };
+// bit 0: a bounded wait ran out; bit 1: malformed offsets seen on device;
+// bit 2: a routing index (expert id or source row) out of range.
+enum : unsigned { DEV_TIMEOUT = 1u, DEV_BAD_OFFSETS = 2u, DEV_BAD_INDEX = 4u };
 
 // ---------------------------------------------------------------------------
 // Element formats

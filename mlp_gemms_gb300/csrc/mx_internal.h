@@ -33,6 +33,12 @@ struct QuantLaunch {
   int num_sms;
   bool stochastic = false; // stochastic rounding of the elements (E2M3, E2M1)
   uint64_t seed = 0;       // its generator key
+  // gather (token permute): output row r is x row src[r], zero where
+  // src[r] < 0; rows from offsets[G-1] on are not produced
+  const int32_t* src = nullptr;
+  int64_t src_rows = 0;
+  const int32_t* offsets = nullptr;
+  int G = 0;
 };
 cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s);
 cudaError_t read_quant_status(unsigned* out);
@@ -104,6 +110,15 @@ cudaError_t launch_gemm_f4(const GemmParams& p, const CUtensorMap& ta, const CUt
                            int bn, cudaStream_t s, int num_sms);
 cudaError_t read_f4_status(unsigned* out);
 cudaError_t reset_f4_status();
+// Token permute support (permute.cu).  counts: the workspace, int32
+// [ceil(T*k / 1024), G].
+cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int32_t* offsets, int32_t* src,
+                               int64_t R_cap, int32_t* row_of, int32_t* counts, cudaStream_t s);
+cudaError_t launch_unpermute(const uint16_t* in, int64_t R, int64_t D, const int32_t* row_of, const float* w,
+                             int64_t T, int k, uint16_t* out, int num_sms, cudaStream_t s);
+cudaError_t read_perm_status(unsigned* out);
+cudaError_t reset_perm_status();
+constexpr int kRouteChunk = 1024;
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t s);
 
 // The tensors of one MLP step that the host pipeline moves: raw inputs the

@@ -45,7 +45,25 @@ struct QuantParams {
   int tiles_x;             // ceil(cols / 128)
   int batch;
   uint64_t seed;           // stochastic rounding: the generator's key
+  // gather (token permute): output row r quantizes x row src[r] (a zero row
+  // where src[r] < 0); rows from offsets[G-1] on are not produced
+  const int32_t* src;
+  int64_t src_rows;        // rows of x
+  const int32_t* offsets;
+  int G;
 };
+
+// Non-bulk asynchronous 16-byte copy global -> shared; src_bytes = 0 writes
+// 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on the barrier once this thread's earlier cp.async copies have
+// landed; counts against the barrier's expected arrivals.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 constexpr int QT = 128;          // tile edge
 
@@ -206,7 +224,11 @@ __device__ __forceinline__ uint32_t stage_off(int r, int b) {
   return (uint32_t)(r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
 }
 
-template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false>
+// GATHER: the token-permute form.  Every thread copies 8 of the tile's 2048
+// 16-byte chunks from the routed rows' tokens (cp.async into the same
+// swizzled layout the TMA boxes produce) and arrives on the stage's barrier
+// when they land (expected arrivals: 256).
+template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false, bool GATHER = false>
 __global__ void __launch_bounds__(256, 2)
 quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap rowmap,
                 const __grid_constant__ CUtensorMap colmap, const QuantParams p) {
@@ -222,13 +244,15 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + Q_NST);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t tiles_y = (p.rows + QT - 1) / QT;
+  // gather: only the rows of the routed segments are produced
+  const int64_t rows_out = (GATHER && p.offsets) ? min((int64_t)__ldg(p.offsets + p.G - 1), p.rows) : p.rows;
+  const int64_t tiles_y = (rows_out + QT - 1) / QT;
   const int64_t per_batch = tiles_y * p.tiles_x;
   const int64_t total = per_batch * p.batch;
   const uint64_t budget = 2000000000ull;
 
   if (tid == 0) {
-    for (int k = 0; k < Q_NST; k++) mbar_init(&full[k], 1);
+    for (int k = 0; k < Q_NST; k++) mbar_init(&full[k], GATHER ? 256 : 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -251,7 +275,31 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     tma_load_2d(sm + s * Q_STAGE, &xmap, (int)c0, gy, &full[s], pol);
     tma_load_2d(sm + s * Q_STAGE + 16384, &xmap, (int)c0 + 64, gy, &full[s], pol);
   };
-  if (tid == 0) {
+  auto gather = [&](int64_t t, int s) {  // every thread: 8 chunks of tile t
+    int b;
+    int64_t r0, c0;
+    coords(t, b, r0, c0);
+    uint8_t* dst = sm + s * Q_STAGE;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int id = tid + 256 * j;
+      const int r = id >> 4, c = (id & 15) * 8;
+      const int64_t gr = r0 + r;
+      int64_t tok = gr < p.rows ? (int64_t)__ldg(p.src + gr) : -1;
+      if (tok >= p.src_rows) {
+        atomicOr(&g_quant_status, DEV_BAD_INDEX);
+        tok = -1;
+      }
+      const bool ok = tok >= 0 && c0 + c < p.cols;
+      cp_async16(smem_u32(dst + tile_off(r, c)), ok ? (const void*)(p.x + tok * p.ld + c0 + c) : (const void*)p.x,
+                 ok ? 16u : 0u);
+    }
+    cp_async_arrive_noinc(&full[s]);
+  };
+  if (GATHER) {
+    for (int k = 0; k < Q_NST; k++)
+      if (blockIdx.x + (int64_t)k * gridDim.x < total) gather(blockIdx.x + (int64_t)k * gridDim.x, k);
+  } else if (tid == 0) {
     for (int k = 0; k < Q_NST; k++)
       if (blockIdx.x + (int64_t)k * gridDim.x < total) issue(blockIdx.x + (int64_t)k * gridDim.x, k);
   }
@@ -366,8 +414,9 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         if constexpr (COL) tma_store_2d(&colmap, out_col, (int)r0, (int)(b * p.cols + c0));
         bulk_commit();
       }
-      if (t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
+      if (!GATHER && t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
     }
+    if (GATHER && t + Q_NST * (int64_t)gridDim.x < total) gather(t + Q_NST * (int64_t)gridDim.x, s);
     if (tid < 32) {
       if constexpr (ROW) {
         const int64_t chunk = (r0 / 128) * ((p.cols / 32 + 3) / 4) + c0 / 128;
@@ -393,12 +442,13 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     }
   }
   if (QC::STAGED && tid == 0) bulk_wait_all();  // this CTA's TMA stores have completed
+  if (GATHER) cp_async_wait_all();              // no copy of this thread still in flight
   if (*abort_flag) {
     // a wait ran out: let every copy this CTA issued land before exiting
     if (tid == 0) {
       volatile int no_abort = 0;
       atomicOr(&g_quant_status, DEV_TIMEOUT);
-      for (int k = 0; k < Q_NST; k++) {
+      for (int k = 0; k < (GATHER ? 0 : Q_NST); k++) {
         const int64_t t = blockIdx.x + (int64_t)(it + k) * gridDim.x;
         if (t < total)
           mbar_wait_bounded(&full[(it + k) % Q_NST], (uint32_t)(((it + k) / Q_NST) & 1), &no_abort, budget);
@@ -461,9 +511,9 @@ cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t c
   return cudaGetLastError();
 }
 
-template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false>
+template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false, bool GATHER = false>
 static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStream_t s) {
-  auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM, SR>;
+  auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM, SR, GATHER>;
   constexpr int smem = QCfg<FMT>::SMEM;
   static bool configured = false;
   if (!configured) {
@@ -475,6 +525,14 @@ static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStre
   const int64_t cap = 2ll * q.num_sms;
   kern<<<(unsigned)(tiles < cap ? tiles : cap), 256, smem, s>>>(q.xmap, q.rowmap, q.colmap, p);
   return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t dispatch_orient_gather(const QuantLaunch& q, const QuantParams& p, bool row, bool col,
+                                          cudaStream_t s) {
+  if (row && col) return launch_q<FMT, false, true, true, false, false, true>(q, p, s);
+  if (row) return launch_q<FMT, false, true, false, false, false, true>(q, p, s);
+  return launch_q<FMT, false, false, true, false, false, true>(q, p, s);
 }
 
 template <int FMT, bool HAD>
@@ -515,8 +573,17 @@ cudaError_t launch_quantize(const QuantLaunch& q, cudaStream_t s) {
   p.tiles_x = (int)((q.cols + QT - 1) / QT);
   p.batch = (int)q.batch;
   p.seed = q.seed;
+  p.src = q.src; p.src_rows = q.src_rows; p.offsets = q.offsets; p.G = q.G;
   const bool row = q.row_data != nullptr, col = q.col_data != nullptr, cs = q.colsum_partials != nullptr;
   cudaError_t e;
+  if (q.src) {  // gather (token permute): no rotation, rounding variant or column sums
+    switch (q.fmt) {
+      case E4M3: return dispatch_orient_gather<E4M3>(q, p, row, col, s);
+      case E2M3: return dispatch_orient_gather<E2M3>(q, p, row, col, s);
+      case E2M1: return dispatch_orient_gather<E2M1>(q, p, row, col, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (q.stochastic) {  // E2M3 / E2M1 without column sums (checked by the caller)
     switch (q.fmt * 2 + (q.hadamard ? 1 : 0)) {
       case 2: return dispatch_orient_sr<E2M3, false>(q, p, row, col, s);
