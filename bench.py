@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119454784,
-    "quant_w1": 1573290944,
-    "quant_w2": 755244480,
-    "fc1_swiglu": 2286306112,
-    "fc2": 1447179200,
-    "quant_dy": 2119745536,
-    "fc2_dgrad_dswiglu": 2707057088,
-    "fc1_dgrad": 1867190336,
-    "wgrad_dw2": 1248790784,
-    "wgrad_dw1": 2288578880,
+    "quant_x": 2119431488,
+    "quant_w1": 1573183296,
+    "quant_w2": 755277376,
+    "fc1_swiglu": 2256010816,
+    "fc2": 1444001600,
+    "quant_dy": 2119589632,
+    "fc2_dgrad_dswiglu": 2704789568,
+    "fc1_dgrad": 1864489216,
+    "wgrad_dw2": 1232435328,
+    "wgrad_dw1": 2249464128,
 }
 
 
@@ -324,6 +324,8 @@ def run_gpu(args):
     dense = dense_step_rate(mx, torch, dev) if not args.no_extra else None
     fwd_even = moe_forward_even_rate(mx, torch, dev) if not args.no_extra else None
     variants = variant_rates(mx, torch, dev) if not args.no_extra else None
+    mxfp4 = mxfp4_gemm_rate(mx, torch, dev) if not args.no_extra else None
+    permute = permute_rates(mx, torch, dev) if not args.no_extra else None
     status = mx.mx_get_device_status()
     if status != "MX_OK":
         raise RuntimeError("device status: " + status)
@@ -371,6 +373,8 @@ def run_gpu(args):
         "dense_mxfp6_step": dense,
         "moe_fwd_even_routing": fwd_even,
         "variants": variants,
+        "mxfp4_gemm": mxfp4,
+        "moe_permute": permute,
     }
     if rank == 0 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(seconds_hint=args.cpu_seconds)
@@ -662,6 +666,99 @@ def variant_rates(mx, torch, dev, reps=10):
     return res
 
 
+def mxfp4_gemm_rate(mx, torch, dev, reps=10):
+    """Dense MXFP4 GEMM on the packed-operand tensor-core path: E2M1 operands
+    of the dense MLP's FC1 shape (M=16384 tokens, N=12288, K=3072), BF16 out,
+    inputs larger than L2 (no flush needed)."""
+    M, N, K = W_DENSE["M"], W_DENSE["H"], W_DENSE["D"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    a = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+    b = (torch.randn((N, K), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    ar, _, _ = mx.mx_quantize(a, mx.E2M1, True, False)
+    br, _, _ = mx.mx_quantize(b, mx.E2M1, True, False)
+    del a, b
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        mx.mx_gemm_bias(ar, br, None, out=out)
+    torch.cuda.synchronize(dev)
+    ms = _event_mean(torch, stream, dev, lambda: mx.mx_gemm_bias(ar, br, None, out=out), reps)
+    peaks, kind = measured_peaks()
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    peak_fp4 = 6.0 * peaks["bf16_tflops"]
+    return {"workload": "dense mxfp4-e2m1 GEMM 16384x12288x3072 (tcgen05 kind::mxf4)", "ms": ms, "tflops": tf,
+            "peak_fp4_tflops": peak_fp4, "frac_of_fp4_peak": tf / peak_fp4,
+            "peak_kind": kind + " bf16 burst x 6 (nominal fp4/bf16 ratio)"}
+
+
+def permute_rates(mx, torch, dev, reps=10):
+    """The token permute of the benchmark's routing: 32768 tokens, top-8 of
+    128 experts (Zipf(1.1) popularity, distinct experts per token), hidden
+    2048.  Times the routing index, the quantizing permute (E4M3, both
+    orientations, in permuted order) beside the unfused form (BF16 gather
+    of the routed rows, then the quantizer), and the un-permute (combine)
+    of the routed rows with routing weights.  Algorithmic bytes: tokens read
+    once, outputs written once."""
+    G, D, k = SHAPE["G"], SHAPE["D"], 8
+    T = SHAPE["R"] // k
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    pop = 1.0 / torch.arange(1, G + 1, device=dev, dtype=torch.float32) ** 1.1
+    pop = pop[torch.randperm(G, generator=g, device=dev)]
+    topk = torch.multinomial(pop.expand(T, G), k, replacement=False, generator=g).to(torch.int32).contiguous()
+    x = torch.randn((T, D), generator=g, device=dev).to(torch.bfloat16)
+    R_cap = mx.mx_moe_route_rows(T, k, G)
+    offs = torch.empty(G, dtype=torch.int32, device=dev)
+    src = torch.empty(R_cap, dtype=torch.int32, device=dev)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=dev)
+    ws = torch.empty(max(16, int(mx.load().mx_moe_route_workspace_bytes(T, k, G))), dtype=torch.uint8, device=dev)
+    route = lambda: mx.mx_moe_route_index(topk, G, R_cap, offs, src, row_of, ws)
+    route()
+    torch.cuda.synchronize(dev)
+    R = int(offs[-1].item())
+    qr, qc = mx.MX(R_cap, D), mx.MX(D, R_cap)
+    perm = lambda: mx.mx_permute_quantize(x, src, offs, out_row=qr, out_col=qc)
+    xp = torch.empty((R_cap, D), dtype=torch.bfloat16, device=dev)
+    idx = src.clamp(min=0).long()
+    ur, uc = mx.MX(R_cap, D), mx.MX(D, R_cap)
+
+    def unfused():
+        torch.index_select(x, 0, idx, out=xp)
+        mx.mx_quantize(xp, 0, True, True, out_row=ur, out_col=uc)
+
+    y = torch.randn((R_cap, D), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.rand((T, k), generator=g, device=dev)
+    comb = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    unperm = lambda: mx.mx_moe_unpermute(y, row_of, w, out=comb)
+    stream = torch.cuda.current_stream(dev)
+    for f in (route, perm, unfused, unperm):
+        f()
+    torch.cuda.synchronize(dev)
+    t = {name: 0.0 for name in ("route", "perm", "unfused", "unperm")}
+    for _ in range(reps):
+        for name, f in (("route", route), ("perm", perm), ("unfused", unfused), ("unperm", unperm)):
+            t[name] += _event_mean(torch, stream, dev, f, 1)
+    t = {kk: v / reps for kk, v in t.items()}
+    status = mx.mx_get_device_status()
+    if status != "MX_OK":
+        raise RuntimeError("device status after the permute: " + status)
+    peaks, _ = measured_peaks()
+    q = 1.0 + 1.0 / 32
+    perm_bytes = T * D * 2 + 2 * R * D * q
+    unperm_bytes = T * k * D * 2 + T * D * 2 + T * k * 8
+    return {"workload": "32768 tokens top-8 of 128 experts (zipf1.1), D=2048, routed rows %d" % R,
+            "route_index_us": t["route"] * 1e3,
+            "permute_quantize_us": t["perm"] * 1e3,
+            "permute_quantize_gbs": perm_bytes / (t["perm"] * 1e-3) / 1e9,
+            "permute_quantize_frac_of_hbm": perm_bytes / (t["perm"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "unfused_gather_then_quantize_us": t["unfused"] * 1e3,
+            "unpermute_us": t["unperm"] * 1e3,
+            "unpermute_gbs": unperm_bytes / (t["unperm"] * 1e-3) / 1e9,
+            "algorithmic_bytes": {"permute_quantize": perm_bytes, "unpermute": unperm_bytes},
+            "launches": {"route_index": 3, "permute_quantize": 1, "unpermute": 1}}
+
+
 def quantizer_rate(mx, torch, dev):
     """The standalone quantizer workload: 8192 x 7168 BF16 -> MXFP8 rowwise
     and columnwise; the 117 MB input fits in L2, so a 512 MB buffer is
@@ -701,7 +798,8 @@ def ncu_case(name, launches=3):
     """A small single-kernel case for profiler captures: the named stage on a
     reduced MoE shape (G=32, R=65536, D=2048, F=768: operands larger than L2,
     under 1.5 GB on the device), launched `launches` times after one warm-up.
-    'quant' is the standalone quantizer workload (8192 x 7168)."""
+    'quant' is the standalone quantizer workload (8192 x 7168), 'permute' the
+    quantizing permute of 8192 tokens (top-8 of 128 experts, D = 2048)."""
     import torch
     import mlp_gemms_gb300 as mx
     import workloads as W
@@ -712,6 +810,16 @@ def ncu_case(name, launches=3):
         x = torch.randn((8192, 7168), device=dev).to(torch.bfloat16)
         r, c = mx.MX(8192, 7168), mx.MX(7168, 8192)
         run = lambda: mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+    elif name == "permute":  # 8192 tokens top-8 of 128 experts, D = 2048 (~0.5 GB on the device)
+        T, k, G, D = 8192, 8, 128, 2048
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        pop = 1.0 / torch.arange(1, G + 1, device=dev, dtype=torch.float32) ** 1.1
+        topk = torch.multinomial(pop.expand(T, G), k, replacement=False, generator=g).to(torch.int32).contiguous()
+        x = torch.randn((T, D), generator=g, device=dev).to(torch.bfloat16)
+        offs, src, _ = mx.mx_moe_route_index(topk, G)
+        r, c = mx.MX(src.numel(), D), mx.MX(D, src.numel())
+        run = lambda: mx.mx_permute_quantize(x, src, offs, out_row=r, out_col=c)
     else:
         G, D, F, R = 32, 2048, 768, 65536
         offs = torch.from_numpy(W.even_offsets(G, R)).to(dev)

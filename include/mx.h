@@ -192,7 +192,7 @@ MX_API size_t mx_moe_route_workspace_bytes(int64_t T, int32_t k, int32_t G);
  *   row_of_dev   out int32 [T, k]: routed row of each (token, choice), -1
  *                for an out-of-range expert id
  *   workspace    >= mx_moe_route_workspace_bytes(T, k, G) bytes
- * Deterministic (a stable counting sort, no order-dependent atomics); four
+ * Deterministic (a stable counting sort, no order-dependent atomics); three
  * launches.  Expert ids outside [0, G) are skipped and reported as
  * MX_ERR_INVALID_ARG by mx_get_device_status.
  * Errors: MX_ERR_INVALID_ARG (null pointer, k < 1, G < 1 or G > 1024),

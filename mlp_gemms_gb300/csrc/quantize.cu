@@ -275,30 +275,47 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     tma_load_2d(sm + s * Q_STAGE, &xmap, (int)c0, gy, &full[s], pol);
     tma_load_2d(sm + s * Q_STAGE + 16384, &xmap, (int)c0 + 64, gy, &full[s], pol);
   };
-  auto gather = [&](int64_t t, int s) {  // every thread: 8 chunks of tile t
+  // gather: thread tid copies chunk (tid % 16) of rows tid / 16 + 16 j,
+  // j = 0..7.  The source rows of a tile are read one tile ahead of its
+  // copies, so the index loads' latency hides behind the current tile.
+  auto gather_rows = [&](int64_t t, int32_t (&tok)[8]) {
+    int b;
+    int64_t r0, c0;
+    coords(t, b, r0, c0);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int64_t gr = r0 + (tid >> 4) + 16 * j;
+      tok[j] = gr < p.rows ? __ldg(p.src + gr) : -1;
+    }
+  };
+  auto gather = [&](int64_t t, int s, const int32_t (&tok)[8]) {
     int b;
     int64_t r0, c0;
     coords(t, b, r0, c0);
     uint8_t* dst = sm + s * Q_STAGE;
+    const int c = (tid & 15) * 8;
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-      const int id = tid + 256 * j;
-      const int r = id >> 4, c = (id & 15) * 8;
-      const int64_t gr = r0 + r;
-      int64_t tok = gr < p.rows ? (int64_t)__ldg(p.src + gr) : -1;
-      if (tok >= p.src_rows) {
+      const int r = (tid >> 4) + 16 * j;
+      int64_t tk = tok[j];
+      if (tk >= p.src_rows) {
         atomicOr(&g_quant_status, DEV_BAD_INDEX);
-        tok = -1;
+        tk = -1;
       }
-      const bool ok = tok >= 0 && c0 + c < p.cols;
-      cp_async16(smem_u32(dst + tile_off(r, c)), ok ? (const void*)(p.x + tok * p.ld + c0 + c) : (const void*)p.x,
+      const bool ok = tk >= 0 && c0 + c < p.cols;
+      cp_async16(smem_u32(dst + tile_off(r, c)), ok ? (const void*)(p.x + tk * p.ld + c0 + c) : (const void*)p.x,
                  ok ? 16u : 0u);
     }
     cp_async_arrive_noinc(&full[s]);
   };
+  int32_t next_tok[8];
   if (GATHER) {
-    for (int k = 0; k < Q_NST; k++)
-      if (blockIdx.x + (int64_t)k * gridDim.x < total) gather(blockIdx.x + (int64_t)k * gridDim.x, k);
+    for (int k = 0; k < Q_NST; k++) {
+      if (blockIdx.x + (int64_t)k * gridDim.x < total) {
+        gather_rows(blockIdx.x + (int64_t)k * gridDim.x, next_tok);
+        gather(blockIdx.x + (int64_t)k * gridDim.x, k, next_tok);
+      }
+    }
   } else if (tid == 0) {
     for (int k = 0; k < Q_NST; k++)
       if (blockIdx.x + (int64_t)k * gridDim.x < total) issue(blockIdx.x + (int64_t)k * gridDim.x, k);
@@ -308,6 +325,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
   for (int64_t t = blockIdx.x; t < total; t += gridDim.x, it++) {
     const int s = it % Q_NST;
     if (!mbar_wait_bounded(&full[s], (uint32_t)((it / Q_NST) & 1), abort_flag, budget)) break;
+    if (GATHER && t + Q_NST * (int64_t)gridDim.x < total) gather_rows(t + Q_NST * (int64_t)gridDim.x, next_tok);
     int b;
     int64_t r0, c0;
     coords(t, b, r0, c0);
@@ -416,7 +434,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
       }
       if (!GATHER && t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);
     }
-    if (GATHER && t + Q_NST * (int64_t)gridDim.x < total) gather(t + Q_NST * (int64_t)gridDim.x, s);
+    if (GATHER && t + Q_NST * (int64_t)gridDim.x < total) gather(t + Q_NST * (int64_t)gridDim.x, s, next_tok);
     if (tid < 32) {
       if constexpr (ROW) {
         const int64_t chunk = (r0 / 128) * ((p.cols / 32 + 3) / 4) + c0 / 128;
