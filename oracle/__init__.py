@@ -324,6 +324,20 @@ def grouped_gemm(a, b, offsets):
     return out
 
 
+def grouped_gemm_bias(a, b, bias, offsets):
+    """grouped_gemm plus expert g's bias row on the rows of its segment:
+    out[r, n] = sum_k a[r, k] * b[g, n, k] + bias[g, n] (Primus PR #1064
+    "feat(mxfp6): MXFP6 (E2M3) Flux linears, a fused MLP, and the MLPerf
+    recipe", bias commits: the bias joins the fp32 accumulator before the
+    output's single rounding).  bias float64 [G, N]."""
+    out = grouped_gemm(a, b, offsets)
+    bias = np.asarray(bias, dtype=np.float64)
+    for g, (s, e) in enumerate(segments(offsets)):
+        if e > s:
+            out[s:e] += bias[g][None, :]
+    return out
+
+
 def wgrad(a_col, b_col, offsets):
     """dW[g, n, k] = sum over r in segment g of a_col[n, r] * b_col[k, r].
 

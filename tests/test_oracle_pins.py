@@ -340,6 +340,17 @@ def test_grouped_gemm_exact_rational_small():
     assert np.all(np.isnan(out[64:]))
 
 
+def test_grouped_gemm_bias_exact_small():
+    """Hand-checkable: two experts of one row each, K = 2, N = 2; each row
+    gets its own expert's weights and bias, and bias = 0 is the plain GEMM."""
+    a = np.array([[1.0, 2.0], [3.0, -1.0]])
+    b = np.array([[[1.0, 0.0], [0.0, 1.0]], [[2.0, 1.0], [1.0, -1.0]]])
+    bias = np.array([[0.5, -0.5], [10.0, 20.0]])
+    out = O.grouped_gemm_bias(a, b, bias, np.array([1, 2]))
+    assert out.tolist() == [[1.5, 1.5], [15.0, 24.0]]
+    assert np.array_equal(O.grouped_gemm_bias(a, b, np.zeros((2, 2)), [1, 2]), O.grouped_gemm(a, b, [1, 2]))
+
+
 def test_wgrad_zero_token_expert_and_exact_small():
     rng = np.random.default_rng(12)
     a = rng.integers(-3, 4, size=(16, 256)).astype(np.float64)
