@@ -798,8 +798,10 @@ def ncu_case(name, launches=3):
     """A small single-kernel case for profiler captures: the named stage on a
     reduced MoE shape (G=32, R=65536, D=2048, F=768: operands larger than L2,
     under 1.5 GB on the device), launched `launches` times after one warm-up.
-    'quant' is the standalone quantizer workload (8192 x 7168), 'permute' the
-    quantizing permute of 8192 tokens (top-8 of 128 experts, D = 2048)."""
+    'quant' is the standalone quantizer workload (8192 x 7168) ('quant_sr' /
+    'quant_e2m1' the same to MXFP4 with stochastic / nearest rounding),
+    'permute' the quantizing permute of 8192 tokens (top-8 of 128 experts,
+    D = 2048), 'mxfp4_gemm' a dense E2M1 GEMM 8192 x 12288 x 3072."""
     import torch
     import mlp_gemms_gb300 as mx
     import workloads as W
@@ -810,6 +812,18 @@ def ncu_case(name, launches=3):
         x = torch.randn((8192, 7168), device=dev).to(torch.bfloat16)
         r, c = mx.MX(8192, 7168), mx.MX(7168, 8192)
         run = lambda: mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+    elif name in ("quant_sr", "quant_e2m1"):  # the standalone workload to MXFP4, stochastic / nearest rounding
+        x = torch.randn((8192, 7168), device=dev).to(torch.bfloat16)
+        r, c = mx.MX(8192, 7168, mx.E2M1), mx.MX(7168, 8192, mx.E2M1)
+        run = (lambda: mx.mx_quantize_sr(x, mx.E2M1, 7, True, True, out_row=r, out_col=c)) if name == "quant_sr" \
+            else (lambda: mx.mx_quantize(x, mx.E2M1, True, True, out_row=r, out_col=c))
+    elif name == "mxfp4_gemm":  # dense E2M1 GEMM 8192 x 12288 x 3072 (~0.5 GB on the device)
+        a = torch.randn((8192, 3072), device=dev).to(torch.bfloat16)
+        b = (torch.randn((12288, 3072), device=dev) * 0.02).to(torch.bfloat16)
+        ar, _, _ = mx.mx_quantize(a, mx.E2M1, True, False)
+        br, _, _ = mx.mx_quantize(b, mx.E2M1, True, False)
+        out = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+        run = lambda: mx.mx_gemm_bias(ar, br, None, out=out)
     elif name == "permute":  # 8192 tokens top-8 of 128 experts, D = 2048 (~0.5 GB on the device)
         T, k, G, D = 8192, 8, 128, 2048
         g = torch.Generator(device=dev)

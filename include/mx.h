@@ -298,6 +298,19 @@ MX_API mx_status_t mx_grouped_gemm(const mx_tensor_t *a, const mx_tensor_t *b, i
                             void *out_bf16, int64_t ld_out, mx_stream_t stream);
 
 /*
+ * mx_grouped_gemm_bias -- mx_grouped_gemm with a per-expert bias added to
+ * the fp32 accumulator before the single BF16 rounding ([MXFP6-PR] bias
+ * commits: the bias add belongs in the GEMM's store epilogue; here each
+ * expert has its own row).
+ *   bias_bf16   device BF16 [G, N] (row g for the rows of segment g),
+ *               16-byte aligned
+ * Other arguments, shapes and errors as mx_grouped_gemm.
+ */
+MX_API mx_status_t mx_grouped_gemm_bias(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G,
+                                        const int32_t *offsets_dev, const void *bias_bf16, void *out_bf16,
+                                        int64_t ld_out, mx_stream_t stream);
+
+/*
  * mx_grouped_gemm_swiglu_fwd -- FC1 of the expert MLP with the SwiGLU
  * epilogue ([MXFP8-PR] correctness-first kernels commit: FC1 ragged grouped
  * GEMM + SwiGLU + dual 1x32 / 32x1 MXFP8 RCEIL quantization + BF16

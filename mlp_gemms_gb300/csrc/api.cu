@@ -599,8 +599,14 @@ mx_status_t mx_quantize_colsum_noalloc(const void* x_bf16, int64_t rows, int64_t
                      stream);
 }
 
-mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
-                            void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The BF16-out grouped GEMM, optionally with expert g's bias row
+// bias[g * N .. + N) added to the fp32 accumulator.
+mx_status_t grouped_gemm_impl(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                              const void* bias_bf16, void* out_bf16, int64_t ld_out, mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mx_status_t st;
   if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
@@ -638,7 +644,24 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.out = static_cast<uint16_t*>(out_bf16);
   p.out_ld = ld_out;
+  p.bias = static_cast<const uint16_t*>(bias_bf16);
+  p.bias_ld = N;
   return run_gemm(p, a, b, bn, s, dev, OutView{out_bf16, R, N, ld_out});
+}
+
+}  // namespace
+
+extern "C" {
+
+mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                            void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+  return grouped_gemm_impl(a, b, G, offsets_dev, nullptr, out_bf16, ld_out, stream);
+}
+
+mx_status_t mx_grouped_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                                 const void* bias_bf16, void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+  MX_CHECK(bias_bf16 != nullptr && aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be a 16-byte aligned pointer");
+  return grouped_gemm_impl(a, b, G, offsets_dev, bias_bf16, out_bf16, ld_out, stream);
 }
 
 }  // extern "C"

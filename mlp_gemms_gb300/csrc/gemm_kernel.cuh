@@ -55,7 +55,7 @@ constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts
 template <int BN, bool ZR = false, bool F4 = false>
 struct Cfg {
   static constexpr int KC = F4 ? 2 : 1;
-  static constexpr int STAGES = BN == 256 ? (F4 ? 3 : 4) : (ZR ? 4 : 5);
+  static constexpr int STAGES = BN == 256 ? 4 : (ZR ? 4 : 5);
   static constexpr int ACC = BN == 256 ? 1 : 2;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -63,7 +63,12 @@ struct Cfg {
   static constexpr int SF_BYTES = KC * (512 + (BN / 128) * 512);
   static constexpr int SF_COLS = KC * (4 + 4 * (BN / 128));
   static constexpr uint32_t TX = A_BYTES + B_BYTES + SF_BYTES;
-  static constexpr int TB_BYTES = 2560;  // 512-byte multiple: TMA store swizzle atoms
+  // per-warp staging: a 32x32 BF16 / 32x16 fp32 block (2048 bytes) for the
+  // plain epilogues, the [32][17] fp32 transpose for the requant ones;
+  // 512-byte multiples (TMA store swizzle atoms).  F4 runs plain epilogues
+  // only, and the room goes to a fourth 256-K stage.
+  static constexpr int TB_BYTES = F4 ? 2048 : 2560;
+  static constexpr int CHUNK_BYTES = F4 ? 0 : 4096;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
@@ -74,7 +79,7 @@ struct Cfg {
   static constexpr int OFF_Z = OFF_SF + STAGES * SF_BYTES;
   static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
   static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
-  static constexpr int OFF_BAR = OFF_CHUNK + 4096;
+  static constexpr int OFF_BAR = OFF_CHUNK + CHUNK_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ORDER = OFF_MISC + 16;              // wgrad: experts by descending size
@@ -683,7 +688,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
         if (p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
-          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + T.n0 + half * COLS);
+          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + (int64_t)T.g * p.bias_ld + T.n0 + half * COLS);
 #pragma unroll
           for (int i = 0; i < COLS / 32; i++) {
 #pragma unroll

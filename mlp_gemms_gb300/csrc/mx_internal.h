@@ -81,6 +81,7 @@ struct GemmParams {
   int64_t q_row_ld, q_col_ld;  // payload bytes per row of q_row / q_col
   int q_fmt, q_had;         // requant element format and rotation (GELU / dGELU)
   const uint16_t* bias;     // BF16 [N] added to the fp32 accumulator, or null
+  int64_t bias_ld;          // grouped: elements between experts' bias rows (0: one row for all)
   float* colsum_partials;   // dGELU: fp32 [ceil(R/128), C] per-tile column sums
   float* tap;               // test instrument: fused epilogues' fp32 pre-quant values [R, C], or null
   float* out_f32;           // EPI_F32: fp32 gradient buffer [rows, out_ld] (wgrad into main_grad)

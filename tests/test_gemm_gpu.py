@@ -444,3 +444,30 @@ def test_r_zero_and_g_zero(cuda_lib):
     with pytest.raises(cuda_lib.MXError) as e:
         cuda_lib.mx_grouped_gemm(a, b, 0, offs, out=out, ld_out=256)
     assert e.value.name == "MX_ERR_INVALID_ARG"
+
+
+@pytest.mark.parametrize("fmt,N", [(O.E4M3, 384), (O.E4M3, 512), (O.E2M1, 256)])
+def test_grouped_gemm_per_expert_bias(cuda_lib, fmt, N):
+    """Each segment gets its own expert's bias row in the fp32 accumulator
+    (4 experts, one empty, NaN-poisoned inactive tail untouched); E2M1 runs
+    the kind::mxf4 path.  Small-integer operands and biases make the sums
+    exact, so the BF16 output is compared bit for bit."""
+    import torch
+    G, K, R = 4, 512, 1152
+    offsets = _offsets([384, 0, 256, 384])
+    rng = np.random.default_rng(120 + N + fmt)
+    a = rng.integers(-2, 3, size=(R, K)).astype(np.float32)
+    b = rng.integers(-2, 3, size=(G, N, K)).astype(np.float32)
+    bias = rng.integers(-64, 65, size=(G, N)).astype(np.float32)
+    ar, _, aref = _quant_both(cuda_lib, W.to_bf16_bits(a), fmt=fmt)
+    br, _, bref = _quant_both(cuda_lib, W.to_bf16_bits(b), fmt=fmt)
+    assert np.array_equal(_deq(aref["row_payload"], aref["row_scales"], R, K, fmt), a)
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bias_dev = torch.from_numpy(W.to_bf16_bits(bias).view(np.int16)).cuda().view(torch.bfloat16)
+    cuda_lib.mx_grouped_gemm_bias(ar, br, G, torch.from_numpy(offsets).cuda(), bias_dev, out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    ref = O.grouped_gemm_bias(a.astype(np.float64), b.astype(np.float64), bias.astype(np.float64), offsets)
+    A = int(offsets[-1])
+    got = bf16_cpu(out)
+    assert np.array_equal(got[:A], O.bf16_out(ref[:A]))
+    assert np.all(np.isnan(got[A:]))
