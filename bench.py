@@ -398,6 +398,9 @@ def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev
     h = (mx.MX(R, F), mx.MX(F, R))
     dz = (mx.MX(R, 2 * F), mx.MX(2 * F, R))
     z = torch.empty((R, 2 * F), dtype=torch.bfloat16, device=dev)
+    # the weight gradients with the K-split workspace, as mx_mlp_fwd_bwd runs them
+    split_ws = torch.empty(max(16, mx.mx_grouped_gemm_wgrad_workspace_bytes(D, F, R, G),
+                               mx.mx_grouped_gemm_wgrad_workspace_bytes(2 * F, D, R, G)), dtype=torch.uint8, device=dev)
     names = ["quant_x", "quant_w1", "quant_w2", "fc1_swiglu", "fc2", "quant_dy", "fc2_dgrad_dswiglu", "fc1_dgrad",
              "wgrad_dw2", "wgrad_dw1"]
     calls = [
@@ -409,8 +412,8 @@ def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev
         lambda: mx.mx_quantize(inp["dy"], 0, True, True, out_row=qdy[0], out_col=qdy[1]),
         lambda: mx.mx_grouped_gemm_dswiglu_bwd(qdy[0], qw2[1], z, G, offs, dz[0], dz[1]),
         lambda: mx.mx_grouped_gemm(dz[0], qw1[1], G, offs, out=out["dx"]),
-        lambda: mx.mx_grouped_gemm_wgrad(qdy[1], h[1], G, offs, out=out["dw2"]),
-        lambda: mx.mx_grouped_gemm_wgrad(dz[1], qx[1], G, offs, out=out["dw1"]),
+        lambda: mx.mx_grouped_gemm_wgrad_ws(qdy[1], h[1], G, offs, out=out["dw2"], workspace=split_ws),
+        lambda: mx.mx_grouped_gemm_wgrad_ws(dz[1], qx[1], G, offs, out=out["dw1"], workspace=split_ws),
     ]
     for _ in range(2):
         for c in calls:

@@ -411,6 +411,33 @@ MX_API mx_status_t mx_grouped_gemm_wgrad_f32(const mx_tensor_t *a_col, const mx_
                                              mx_stream_t stream);
 
 /*
+ * K-split of the largest experts' weight gradients (load balance under
+ * skewed routing).  mx_grouped_gemm_wgrad_ws / _f32_ws are
+ * mx_grouped_gemm_wgrad / _f32 with a workspace: experts whose token count
+ * exceeds a split size (chosen from N, K, R and the SM count, in 128-token
+ * chunks) have each output tile's K range cut into parts; every part writes
+ * an fp32 partial tile to the workspace, and the part that completes the
+ * tile's arrival counter sums all parts in part order and stores the tile
+ * (BF16, or fp32 store / accumulate).  Deterministic: the same bits whichever
+ * part finishes last; the sum order differs from the unsplit call's, so the
+ * two agree to fp32 rounding, not bit for bit.  At most 16 experts are
+ * split; with offsets NULL, G == 1, G > 1024 or a NULL workspace nothing is.
+ * mx_grouped_gemm_wgrad_workspace_bytes(N, K, R, G) -- bytes for [N, K]
+ * gradients over R routed rows (0: no split possible); N = a_col rows,
+ * K = b_col rows.  The workspace holds counters the call clears (one
+ * memset per call) and leaves zero.
+ * Errors as mx_grouped_gemm_wgrad / _f32, plus MX_ERR_WORKSPACE when a
+ * non-NULL workspace is smaller than the query's bytes.
+ */
+MX_API size_t mx_grouped_gemm_wgrad_workspace_bytes(int64_t N, int64_t K, int64_t R, int32_t G);
+MX_API mx_status_t mx_grouped_gemm_wgrad_ws(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
+                                            const int32_t *offsets_dev, void *out_bf16, void *workspace,
+                                            size_t workspace_bytes, mx_stream_t stream);
+MX_API mx_status_t mx_grouped_gemm_wgrad_f32_ws(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
+                                                const int32_t *offsets_dev, float *grad_f32, int32_t accumulate,
+                                                void *workspace, size_t workspace_bytes, mx_stream_t stream);
+
+/*
  * Dense (single-segment) calls of the MXFP6 Flux-style MLP ([MXFP6-PR]
  * fused-MLP commit: one unit owns fc1 -> activation -> fc2, the packer takes
  * the activation as an epilogue in the forward and its derivative in the

@@ -37,6 +37,7 @@ ABI_SYMBOLS = (
     "mx_grouped_gemm_wgrad_f32", "mx_grouped_gemm_swiglu_probs_fwd", "mx_dswiglu_probs_workspace_bytes",
     "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr", "mx_moe_route_rows", "mx_moe_route_workspace_bytes",
     "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute", "mx_grouped_gemm_bias",
+    "mx_grouped_gemm_wgrad_workspace_bytes", "mx_grouped_gemm_wgrad_ws", "mx_grouped_gemm_wgrad_f32_ws",
 )
 
 
@@ -113,6 +114,9 @@ def load(path=None):
         "mx_permute_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, i64, vp, i32, i32, u32, tp, tp, vp]),
         "mx_moe_unpermute": (ctypes.c_int, [vp, i64, i64, vp, vp, i64, i32, vp, vp]),
         "mx_grouped_gemm_bias": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, i64, vp]),
+        "mx_grouped_gemm_wgrad_workspace_bytes": (sz, [i64, i64, i64, i32]),
+        "mx_grouped_gemm_wgrad_ws": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, sz, vp]),
+        "mx_grouped_gemm_wgrad_f32_ws": (ctypes.c_int, [tp, tp, i32, vp, vp, i32, vp, sz, vp]),
         "mx_debug_tap": (ctypes.c_int, [vp, i64]),
         "mx_mlp_pipeline_create": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp, ctypes.POINTER(vp)]),
         "mx_mlp_pipeline_run": (ctypes.c_int, [vp, ctypes.POINTER(HostIOStruct)]),
@@ -404,6 +408,39 @@ def mx_grouped_gemm_wgrad_f32(a_col, b_col, G, offsets, grad, accumulate=False, 
     assert grad.dtype == torch.float32 and grad.is_contiguous()
     _check(load().mx_grouped_gemm_wgrad_f32(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(grad),
                                             1 if accumulate else 0, _stream(stream)))
+    return grad
+
+
+def mx_grouped_gemm_wgrad_workspace_bytes(N, K, R, G):
+    return int(load().mx_grouped_gemm_wgrad_workspace_bytes(N, K, R, G))
+
+
+def _wgrad_ws(a_col, b_col, G, workspace):
+    import torch
+    if workspace is None:
+        n = mx_grouped_gemm_wgrad_workspace_bytes(a_col.rows, b_col.rows, a_col.cols, G)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=a_col.data.device)
+    return workspace
+
+
+def mx_grouped_gemm_wgrad_ws(a_col, b_col, G, offsets, out=None, workspace=None, stream=None):
+    """mx_grouped_gemm_wgrad with the largest experts' K range split across
+    CTAs (workspace from mx_grouped_gemm_wgrad_workspace_bytes)."""
+    import torch
+    if out is None:
+        out = torch.empty((G, a_col.rows, b_col.rows), dtype=torch.bfloat16, device=a_col.data.device)
+    ws = _wgrad_ws(a_col, b_col, G, workspace)
+    _check(load().mx_grouped_gemm_wgrad_ws(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(out), _ptr(ws), ws.numel(),
+                                           _stream(stream)))
+    return out
+
+
+def mx_grouped_gemm_wgrad_f32_ws(a_col, b_col, G, offsets, grad, accumulate=False, workspace=None, stream=None):
+    import torch
+    assert grad.dtype == torch.float32 and grad.is_contiguous()
+    ws = _wgrad_ws(a_col, b_col, G, workspace)
+    _check(load().mx_grouped_gemm_wgrad_f32_ws(_s(a_col), _s(b_col), G, _ptr(offsets), _ptr(grad),
+                                               1 if accumulate else 0, _ptr(ws), ws.numel(), _stream(stream)))
     return grad
 
 

@@ -49,6 +49,20 @@ constexpr int EPI_THREADS = 256;
 template <int EPI> constexpr int kThreads() { return EPI == EPI_DSWIGLU ? NUM_THREADS + 32 : NUM_THREADS; }
 constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
+constexpr int MAX_SPLIT = MAX_SPLIT_EXPERTS;  // wgrad: at most this many experts have their K range split
+
+// Wgrad K-splitting of the largest experts (built per CTA in the prologue):
+// ranks 0..n-1 (the largest experts) have parts[j] > 1 parts of at most
+// split_chunks chunks each.  Their parts >= 1 come first in the tile order
+// (xbase[j]: first such tile of rank j), then every expert's part 0 in rank
+// order; sbase[j]: first partial slot of rank j (parts[j] slots per tile).
+struct SplitInfo {
+  int n;
+  int extra_total;
+  int xbase[MAX_SPLIT + 1];
+  int parts[MAX_SPLIT];
+  int sbase[MAX_SPLIT];
+};
 
 // F4: packed E2M1 operands on .kind::mxf4.  A stage's 128-byte rows then
 // hold 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
@@ -83,7 +97,9 @@ struct Cfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ORDER = OFF_MISC + 16;              // wgrad: experts by descending size
-  static constexpr int SMEM_BYTES = OFF_ORDER + 2 * MAX_SORTED_G + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_SPLIT = OFF_ORDER + 2 * MAX_SORTED_G;  // wgrad: SplitInfo
+  static constexpr int SMEM_BYTES = OFF_SPLIT + 256 + 1024;  // + slack for 1024-byte alignment
+  static_assert(sizeof(SplitInfo) <= 256, "split info must fit");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_TMEM_BASE = 256;
   static_assert(ACC * BN <= 256, "accumulators live in tensor-memory columns 0..255");
@@ -100,6 +116,9 @@ struct Tile {
   int64_t kbeg;
   int nk;  // pipeline stages (K chunks of 128 elements, 256 with F4)
   int nc;  // K chunks of 128 elements
+  int parts, part;  // wgrad K-split: parts of this (expert, m, n) tile and which one
+  int64_t slot;     // first partial slot of the tile's parts
+  int cnt;          // its arrival counter
 };
 
 __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
@@ -109,9 +128,11 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); 
 // row base.  Wgrad: tiles are expert-major; K runs over the expert's rows.
 // nk counts K chunks of 128 elements here.
 template <int NT, int MODE>
-__device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
+__device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, bool report, const uint16_t* order,
+                                                const SplitInfo* split) {
   Tile T;
   T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0; T.nc = 0;
+  T.parts = 1; T.part = 0; T.slot = 0; T.cnt = 0;
   if (MODE == MODE_GROUPED) {
     int64_t mt = t / p.n_tiles, nt = t % p.n_tiles;
     T.m0 = mt * 128;
@@ -136,9 +157,27 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
     T.active = 1;
   } else {
     int64_t per_g = (int64_t)p.m_tiles * p.n_tiles;
-    T.g = (int)(t / per_g);
+    int64_t tt = t;
+    int srank = -1;
+    if (split != nullptr && split->n > 0) {
+      if (t < split->extra_total) {  // part >= 1 of a split expert
+        int j = 0;
+        while (j + 1 < split->n && split->xbase[j + 1] <= t) j++;
+        const int64_t local = t - split->xbase[j];
+        T.part = 1 + (int)(local / per_g);
+        tt = (int64_t)j * per_g + local % per_g;
+        srank = j;
+      } else {
+        tt = t - split->extra_total;
+        if (tt / per_g < split->n) srank = (int)(tt / per_g);
+      }
+    }
+    // the tile count has headroom for split parts: past the last expert a
+    // tile is inactive
+    if (tt / per_g >= p.G) return T;
+    T.g = (int)(tt / per_g);
     if (order) T.g = order[T.g];
-    int64_t rem = t % per_g;
+    int64_t rem = tt % per_g;
     T.m0 = (rem / p.n_tiles) * 128;
     T.n0 = (rem % p.n_tiles) * NT;
     int64_t end = p.offsets ? ldg_i32(p.offsets + T.g) : p.R;
@@ -147,6 +186,16 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
     if (bad && report) atomicOr(&g_gemm_status, DEV_BAD_OFFSETS);
     T.kbeg = bad ? 0 : start;
     T.nk = bad ? 0 : (int)((end - start) / 128);
+    if (srank >= 0 && !bad) {  // this part's share of the chunks, balanced
+      T.parts = split->parts[srank];
+      const int lo = (int)((int64_t)T.nk * T.part / T.parts), hi = (int)((int64_t)T.nk * (T.part + 1) / T.parts);
+      T.kbeg = start + 128ll * lo;
+      T.nk = hi - lo;
+      T.slot = (int64_t)split->sbase[srank] + rem * T.parts;
+      T.cnt = (int)((int64_t)srank * per_g + rem);
+    } else {
+      T.part = 0;
+    }
     T.active = 1;
   }
   return T;
@@ -155,8 +204,9 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
 // The same with nk in pipeline stages: with F4 a stage covers two chunks
 // and a tile with an odd chunk count ends on a half stage.
 template <int NT, int MODE, bool F4 = false>
-__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order) {
-  Tile T = get_tile_chunks<NT, MODE>(p, t, report, order);
+__device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order,
+                                         const SplitInfo* split = nullptr) {
+  Tile T = get_tile_chunks<NT, MODE>(p, t, report, order, split);
   T.nc = T.nk;
   if (F4) T.nk = (T.nc + 1) >> 1;
   return T;
@@ -434,6 +484,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem_base = *tmem_slot;
   // wgrad: rank the experts by descending row count (ties by index)
   const uint16_t* order = nullptr;
+  const SplitInfo* split = nullptr;
   if (MODE == MODE_WGRAD && p.offsets != nullptr && p.G <= MAX_SORTED_G && p.G > 1) {
     uint16_t* s_order = reinterpret_cast<uint16_t*>(smem + C::OFF_ORDER);
     auto count = [&](int g) -> int64_t {
@@ -451,6 +502,37 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     __syncthreads();
     order = s_order;
+    if (p.split_chunks > 0) {
+      // the largest experts (ranks 0..) with more than split_min chunks get
+      // ceil(chunks / split_chunks) parts, while the partial slots and
+      // counters the host provided last
+      SplitInfo* si = reinterpret_cast<SplitInfo*>(smem + C::OFF_SPLIT);
+      if (threadIdx.x == 0) {
+        const int64_t per_g = (int64_t)p.m_tiles * p.n_tiles;
+        int n = 0;
+        int64_t x = 0, sb = 0;
+        for (int j = 0; j < p.G && n < MAX_SPLIT; j++) {
+          const int g = s_order[j];
+          const int64_t e = ldg_i32(p.offsets + g), b = g ? ldg_i32(p.offsets + g - 1) : 0;
+          const bool ok = e >= b && ((b | e) & 127) == 0 && e <= p.R;
+          const int64_t nk = ok ? (e - b) / 128 : 0;
+          if (nk <= p.split_min || nk <= p.split_chunks) break;
+          const int parts = (int)((nk + p.split_chunks - 1) / p.split_chunks);
+          if (sb + parts * per_g > p.split_slots || x + (parts - 1) * per_g > p.split_extra) break;
+          si->parts[n] = parts;
+          si->xbase[n] = (int)x;
+          si->sbase[n] = (int)sb;
+          x += (parts - 1) * per_g;
+          sb += parts * per_g;
+          n++;
+        }
+        si->xbase[n] = (int)x;
+        si->n = n;
+        si->extra_total = (int)x;
+      }
+      __syncthreads();
+      split = si;
+    }
   }
 
   if (warp == 0) {
@@ -466,7 +548,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
         int64_t brow[2];
         if (EPI == EPI_SWIGLU) {
@@ -528,7 +610,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
         tc_fence_after();
@@ -601,7 +683,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order);
+        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
         for (int hh = 0; hh < 2; hh++) {
           if (!mbar_wait_bounded(&z_empty[zs], zph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
@@ -637,6 +719,54 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       epi_phase ^= 1u;
       return ok;
     };
+    // Wgrad K-split: this part's fp32 partial (the thread's row, BN/2
+    // columns) goes to its slot; the part whose arrival completes the tile's
+    // counter sums every part's slot in part order (its own from registers)
+    // into v, so the result does not depend on which part finishes last.
+    // A slot is [BN/4 column groups][128 rows] of float4, so a warp's 32 rows
+    // of one group are 512 contiguous bytes.
+    // Returns 1 when v holds the tile's sum, 0 when another part stores it,
+    // -1 when a wait gave up.
+    auto split_reduce = [&](const Tile& T, uint32_t (&v)[BN / 64][32]) -> int {
+      constexpr int COLS = BN / 2;
+      const int64_t row = q * 32 + lane;
+      const int64_t tile_floats = 128ll * BN;
+      // float4 index of (column group grp, this row): grp * 128 + row
+      float4* own = reinterpret_cast<float4*>(p.split_ws + (T.slot + T.part) * tile_floats) + half * (COLS / 4) * 128 + row;
+#pragma unroll
+      for (int i = 0; i < COLS / 32; i++) {
+#pragma unroll
+        for (int c = 0; c < 8; c++)
+          __stcg(own + (i * 8 + c) * 128,
+                 make_float4(__uint_as_float(v[i][4 * c]), __uint_as_float(v[i][4 * c + 1]),
+                             __uint_as_float(v[i][4 * c + 2]), __uint_as_float(v[i][4 * c + 3])));
+      }
+      __threadfence();
+      if (!epi_sync()) return -1;
+      volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+      if (ew == 0 && lane == 0) *flag = atomicAdd(p.split_cnt + T.cnt, 1) == T.parts - 1 ? 1 : 0;
+      if (!epi_sync()) return -1;
+      if (*flag == 0) return 0;
+      __threadfence();
+      const float4* base = reinterpret_cast<const float4*>(p.split_ws + T.slot * tile_floats) + half * (COLS / 4) * 128 + row;
+#pragma unroll
+      for (int i = 0; i < COLS / 32; i++) {
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const float4 mine = make_float4(__uint_as_float(v[i][4 * c]), __uint_as_float(v[i][4 * c + 1]),
+                                          __uint_as_float(v[i][4 * c + 2]), __uint_as_float(v[i][4 * c + 3]));
+          float4 sum = T.part == 0 ? mine : __ldcg(base + (i * 8 + c) * 128);
+          for (int pp = 1; pp < T.parts; pp++) {
+            const float4 x = pp == T.part ? mine : __ldcg(base + pp * (tile_floats / 4) + (i * 8 + c) * 128);
+            sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+          }
+          v[i][4 * c] = __float_as_uint(sum.x); v[i][4 * c + 1] = __float_as_uint(sum.y);
+          v[i][4 * c + 2] = __float_as_uint(sum.z); v[i][4 * c + 3] = __float_as_uint(sum.w);
+        }
+      }
+      if (ew == 0 && lane == 0) p.split_cnt[T.cnt] = 0;  // ready for the next launch
+      return 1;
+    };
     // dGELU reads a saved activation per tile: prefetch a tile's rows into
     // L2 one tile ahead of its epilogue (dSwiGLU streams z through shared
     // memory instead).
@@ -644,7 +774,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if constexpr (EPI == EPI_DGELU) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) return;
-        const Tile U = get_tile<NT, MODE, F4>(p, t, false, order);
+        const Tile U = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!U.active || U.nk == 0) return;
         const int64_t r = U.m0 + q * 32 + lane;
         prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
@@ -655,7 +785,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int64_t t = tile_index<MODE>(i);
       if (t >= p.num_tiles) continue;
       prefetch_aux(i + 1);
-      Tile T = get_tile<NT, MODE, F4>(p, t, ew == 0 && lane == 0, order);
+      Tile T = get_tile<NT, MODE, F4>(p, t, ew == 0 && lane == 0, order, split);
       if (!T.active) continue;
       const int64_t row_in_tile = q * 32 + lane;
       if (T.nk == 0) {
@@ -687,7 +817,19 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
-        if (p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
+        bool store = true;
+        const bool split_tile = MODE == MODE_WGRAD && T.parts > 1;
+        if (split_tile) {
+          if (C::ACC == 2) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const int r = split_reduce(T, v);
+          if (r < 0) break;
+          store = r == 1;
+        }
+        if (store && p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
           const uint4* bp = reinterpret_cast<const uint4*>(p.bias + (int64_t)T.g * p.bias_ld + T.n0 + half * COLS);
 #pragma unroll
           for (int i = 0; i < COLS / 32; i++) {
@@ -704,12 +846,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
         const int64_t row0 = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + q * 32;
+        if (store) {
 #pragma unroll
-        for (int i = 0; i < COLS / 32; i++) {
-          stage_reuse_wait(lane);
-          store_bf16_block(reinterpret_cast<const float*>(v[i]), tb_bytes, lane, &tmO, T.n0 + half * COLS + 32 * i, row0);
+          for (int i = 0; i < COLS / 32; i++) {
+            stage_reuse_wait(lane);
+            store_bf16_block(reinterpret_cast<const float*>(v[i]), tb_bytes, lane, &tmO, T.n0 + half * COLS + 32 * i,
+                             row0);
+          }
         }
-        if (C::ACC == 2) {
+        if (C::ACC == 2 && !split_tile) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -727,18 +872,32 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
+        bool store = true;
+        const bool split_tile = MODE == MODE_WGRAD && T.parts > 1;
+        if (split_tile) {
+          if (C::ACC == 2) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          }
+          const int r = split_reduce(T, v);
+          if (r < 0) break;
+          store = r == 1;
+        }
         const int64_t row0 = (MODE == MODE_WGRAD ? (int64_t)T.g * p.Mw : 0) + T.m0 + q * 32;
         const bool add = p.accumulate != 0;
+        if (store) {
 #pragma unroll
-        for (int i = 0; i < COLS / 32; i++) {
+          for (int i = 0; i < COLS / 32; i++) {
 #pragma unroll
-          for (int hh = 0; hh < 2; hh++) {
-            stage_reuse_wait(lane);
-            store_f32_block(reinterpret_cast<const float*>(v[i]) + 16 * hh, tb_bytes, lane, &tmO,
-                            T.n0 + half * COLS + 32 * i + 16 * hh, row0, add);
+            for (int hh = 0; hh < 2; hh++) {
+              stage_reuse_wait(lane);
+              store_f32_block(reinterpret_cast<const float*>(v[i]) + 16 * hh, tb_bytes, lane, &tmO,
+                              T.n0 + half * COLS + 32 * i + 16 * hh, row0, add);
+            }
           }
         }
-        if (C::ACC == 2) {
+        if (C::ACC == 2 && !split_tile) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);

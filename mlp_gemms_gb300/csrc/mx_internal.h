@@ -49,6 +49,7 @@ cudaError_t colsum_scratch(float** out, size_t* floats);
 cudaError_t reset_quant_status();
 
 enum GemmMode : int { MODE_GROUPED = 0, MODE_WGRAD = 1 };
+constexpr int MAX_SPLIT_EXPERTS = 16;  // wgrad K-split: experts split at most (the kernel's MAX_SPLIT)
 enum GemmEpi : int { EPI_BF16 = 0, EPI_SWIGLU = 1, EPI_DSWIGLU = 2, EPI_GELU = 3, EPI_DGELU = 4, EPI_F32 = 5 };
 
 // Everything a grouped-GEMM launch needs besides the two tensor maps.
@@ -89,6 +90,17 @@ struct GemmParams {
   const float* probs;       // SwiGLU / dSwiGLU: routing probability per row [R], or null
   float* dprobs_part;       // dSwiGLU with probs: per-row partial sums [R, dprobs_ld]
   int64_t dprobs_ld;        // 2 per 128-column tile of F
+  // wgrad K-split of the largest experts (split_chunks = 0: none; an expert
+  // with more than split_min chunks gets parts of at most split_chunks): fp32
+  // partial tiles [128][BN] in split_ws (split_slots of them), one arrival
+  // counter per split tile in split_cnt (zero before the launch, zero after),
+  // at most split_extra extra tiles (the num_tiles headroom)
+  int split_chunks;
+  int split_min;            // experts with more chunks than this are split
+  float* split_ws;
+  int32_t* split_cnt;
+  int64_t split_slots;
+  int64_t split_extra;
 };
 
 // ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte

@@ -153,7 +153,11 @@ def test_mlp_rejections_and_workspace_size(mx):
     # every quantized operand of the step plus the BF16 pre-activation
     R, D, F, G = 262144, 2048, 768, 128
     payload = 2 * R * D + 6 * G * D * F + 2 * R * F + 2 * R * D + 4 * R * F + 4 * R * F
-    assert payload < ws < payload * 1.05
+    # plus the wgrad K-split workspace, shared by dW2 [D, F] and dW1 [2F, D]
+    split = max(mx.mx_grouped_gemm_wgrad_workspace_bytes(D, F, R, G),
+                mx.mx_grouped_gemm_wgrad_workspace_bytes(2 * F, D, R, G))
+    assert 0 < split < 0.1 * payload
+    assert payload + split < ws < (payload + split) * 1.05
     st = mx.load().mx_mlp_fwd_bwd(ctypes.byref(a), None)
     assert mx.STATUS[st] == "MX_ERR_INVALID_ARG"          # NULL tensors
     a.act = 1

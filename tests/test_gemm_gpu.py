@@ -471,3 +471,82 @@ def test_grouped_gemm_per_expert_bias(cuda_lib, fmt, N):
     got = bf16_cpu(out)
     assert np.array_equal(got[:A], O.bf16_out(ref[:A]))
     assert np.all(np.isnan(got[A:]))
+
+
+@pytest.mark.parametrize("fmt,K", [(O.E4M3, 384), (O.E4M3, 512), (O.E2M1, 384)])
+def test_wgrad_k_split_exact_and_deterministic(cuda_lib, fmt, K):
+    """An expert with 20480 tokens (160 chunks of 128) has its K range split
+    into parts reduced by the last part to arrive.  Small-integer operands
+    make every partial sum exact, so BF16 out, the fp32 store and the fp32
+    accumulate must equal the oracle bit for bit (K = 384: 128-column
+    tiles, K = 512: 256-column tiles; E2M1 runs kind::mxf4)."""
+    import torch
+    G, N = 4, 256
+    counts = [20480, 0, 1024, 512]
+    offsets = _offsets(counts)
+    R = int(offsets[-1])
+    rng = np.random.default_rng(130 + K + fmt)
+    a = rng.integers(-2, 3, size=(R, N)).astype(np.float32)
+    b = rng.integers(-2, 3, size=(R, K)).astype(np.float32)
+    _, ac, aref = _quant_both(cuda_lib, W.to_bf16_bits(a), row=False, col=True, fmt=fmt)
+    _, bc, bref = _quant_both(cuda_lib, W.to_bf16_bits(b), row=False, col=True, fmt=fmt)
+    assert cuda_lib.mx_grouped_gemm_wgrad_workspace_bytes(N, K, R, G) > 0
+    offs = torch.from_numpy(offsets).cuda()
+    ref = O.wgrad(a.T.astype(np.float64), b.T.astype(np.float64), offsets)
+    out = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad_ws(ac, bc, G, offs, out=out)
+    st = torch.full((G, N, K), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad_f32_ws(ac, bc, G, offs, st, accumulate=False)
+    g0 = torch.from_numpy(rng.integers(-8, 9, size=(G, N, K)).astype(np.float32)).cuda()
+    acc = g0.clone()
+    cuda_lib.mx_grouped_gemm_wgrad_f32_ws(ac, bc, G, offs, acc, accumulate=True)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert np.array_equal(bf16_cpu(out), O.bf16_out(ref))
+    assert np.array_equal(st.cpu().numpy().astype(np.float64), ref)
+    assert np.array_equal(acc.cpu().numpy().astype(np.float64), g0.cpu().numpy().astype(np.float64) + ref)
+
+
+def test_wgrad_k_split_random_is_deterministic_and_close_to_unsplit(cuda_lib):
+    """Random operands: the split wgrad gives the same bits on every run,
+    agrees with the oracle within the GEMM tolerance, and with the unsplit
+    call to fp32 summation order (BF16 outputs within one BF16 step)."""
+    import torch
+    G, N, K = 4, 256, 512
+    counts = [20480, 0, 1024, 512]
+    offsets = _offsets(counts)
+    R = int(offsets[-1])
+    rng = np.random.default_rng(140)
+    _, ac, aref = _quant_both(cuda_lib, W.normal_bf16(rng, (R, N), std=1e-3), row=False, col=True)
+    _, bc, bref = _quant_both(cuda_lib, W.normal_bf16(rng, (R, K)), row=False, col=True)
+    offs = torch.from_numpy(offsets).cuda()
+    runs = [cuda_lib.mx_grouped_gemm_wgrad_ws(ac, bc, G, offs) for _ in range(3)]
+    plain = cuda_lib.mx_grouped_gemm_wgrad(ac, bc, G, offs)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert all(torch.equal(runs[0], r) for r in runs[1:]), "split wgrad is not deterministic"
+    ref = O.wgrad(_deq(aref["col_payload"], aref["col_scales"], N, R), _deq(bref["col_payload"], bref["col_scales"], K, R),
+                  offsets)
+    got = bf16_cpu(runs[0])
+    assert np.all(got[1] == 0.0)
+    assert O.within_tolerance(got, ref).all()
+    p = bf16_cpu(plain)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    assert np.all(np.abs(got - p) <= 2.0 ** -7 * np.abs(p) + 2.0 ** -14 * rms)
+
+
+def test_wgrad_k_split_writes_nothing_outside_its_output(cuda_lib):
+    """The split wgrad launches headroom tiles for the parts; tiles past the
+    last expert must stay inactive: poisoned guard slices around the output
+    (in one allocation) stay untouched, and an empty expert's slice is zero."""
+    import torch
+    G, N, K = 4, 256, 384
+    offsets = _offsets([20480, 0, 1024, 512])
+    R = int(offsets[-1])
+    rng = np.random.default_rng(150)
+    _, ac, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (R, N), std=1e-3), row=False, col=True)
+    _, bc, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (R, K)), row=False, col=True)
+    buf = torch.full((G + 4, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[2:2 + G]
+    cuda_lib.mx_grouped_gemm_wgrad_ws(ac, bc, G, torch.from_numpy(offsets).cuda(), out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert torch.isnan(buf[:2]).all() and torch.isnan(buf[2 + G:]).all()
+    assert (out[1] == 0).all() and not torch.isnan(out).any()
