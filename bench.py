@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119431488,
-    "quant_w1": 1573183296,
-    "quant_w2": 755277376,
-    "fc1_swiglu": 2256010816,
-    "fc2": 1444001600,
-    "quant_dy": 2119589632,
-    "fc2_dgrad_dswiglu": 2704789568,
-    "fc1_dgrad": 1864489216,
-    "wgrad_dw2": 1232435328,
-    "wgrad_dw1": 2249464128,
+    "quant_x": 2119369472,
+    "quant_w1": 1572993024,
+    "quant_w2": 755268608,
+    "fc1_swiglu": 2292543040,
+    "fc2": 1452804672,
+    "quant_dy": 2119402240,
+    "fc2_dgrad_dswiglu": 2727847616,
+    "fc1_dgrad": 1871048448,
+    "wgrad_dw2": 1273574528,
+    "wgrad_dw1": 2284071744,
 }
 
 

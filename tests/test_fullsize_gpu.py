@@ -125,7 +125,8 @@ def test_dswiglu_full_size_sampled_rows(cuda_lib, routing):
 
 def test_wgrad_full_size_sampled_entries(cuda_lib, routing):
     """dW2[g] = dY_g^T h_g for the largest, a small and an empty expert:
-    sampled entries recomputed from the BF16 columns of the segment."""
+    sampled entries recomputed from the BF16 columns of the segment, for
+    the plain call and the K-split one the step uses."""
     import torch
     counts, offsets, big, empty, small = routing
     dy = _rand_bf16((R, D), 1e-3, 41)
@@ -134,8 +135,9 @@ def test_wgrad_full_size_sampled_entries(cuda_lib, routing):
     _, dyc, _ = cuda_lib.mx_quantize(dy, O.E4M3, False, True)
     _, hc, _ = cuda_lib.mx_quantize(h, O.E4M3, False, True)
     dw = cuda_lib.mx_grouped_gemm_wgrad(dyc, hc, G, offs)
+    dws = cuda_lib.mx_grouped_gemm_wgrad_ws(dyc, hc, G, offs)   # the largest expert's K range split
     assert cuda_lib.mx_get_device_status() == "MX_OK"
-    assert bool((dw[empty] == 0).all())
+    assert bool((dw[empty] == 0).all()) and bool((dws[empty] == 0).all())
     rng = np.random.default_rng(4)
     for g in (big, small):
         s, e = int(offsets[g - 1]) if g else 0, int(offsets[g])
@@ -146,8 +148,9 @@ def test_wgrad_full_size_sampled_entries(cuda_lib, routing):
         aq = O.dequantize_rows(*O.quantize_cols(a, O.E4M3), 8, e - s, O.E4M3)
         bq = O.dequantize_rows(*O.quantize_cols(b, O.E4M3), F, e - s, O.E4M3)
         ref = aq @ bq.T                                                     # 8 full rows of dW2[g]
-        got = bf16_cpu(dw[g][torch.from_numpy(ns).cuda()])
-        assert O.within_tolerance(got, ref).all(), g
+        for out in (dw, dws):
+            got = bf16_cpu(out[g][torch.from_numpy(ns).cuda()])
+            assert O.within_tolerance(got, ref).all(), g
 
 
 def test_mlp_step_full_size_runs_and_is_deterministic(cuda_lib, routing):
