@@ -190,19 +190,25 @@ mx_status_t make_tmap_out_f32(CUtensorMap* m, const void* base, int64_t rows, in
 
 // Byte tensor [rows, row_bytes] as a TMA store target: box 128 bytes x 128
 // rows, 128-byte swizzle (the quantizer's staging layout).
-mx_status_t make_tmap_bytes(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes) {
+mx_status_t make_tmap_bytes(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_bytes) {
   mx_status_t st = get_encoder();
   if (st != MX_OK) return st;
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {(cuuint32_t)box_bytes, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (payload) failed (%d)", (int)r);
   return MX_OK;
 }
+
+// The quantizer stages E4M3 and E2M1 tiles in shared memory and stores
+// them with TMA: box 128 bytes (E4M3, 128 elements) or 64 bytes (E2M1).
+bool staged(int fmt) { return fmt == MX_E4M3 || fmt == MX_E2M1; }
+int staged_box(int fmt) { return fmt == MX_E4M3 ? 128 : 64; }
 
 // tcgen05 .kind::mxf8f6f4 element type code of an MX format.
 int mma_type(int fmt) { return fmt == MX_E4M3 ? 0 : (fmt == MX_E2M3 ? 3 : 5); }
@@ -436,11 +442,15 @@ mx_status_t quantize_impl(const void* x_bf16, int64_t batch, int64_t rows, int64
   q.seed = seed;
   if ((st = make_tmap_bf16(&q.xmap, x_bf16, batch * rows, cols, ld)) != MX_OK) return st;
   q.rowmap = q.colmap = q.xmap;  // placeholders where no staged store is made
-  if (fmt == MX_E4M3 && (flags & MX_ROWWISE)) {
-    if ((st = make_tmap_bytes(&q.rowmap, out_row->data, batch * rows, cols)) != MX_OK) return st;
+  if (staged(fmt) && (flags & MX_ROWWISE)) {
+    if ((st = make_tmap_bytes(&q.rowmap, out_row->data, batch * rows, mx::payload_row_bytes(cols, fmt),
+                              staged_box(fmt))) != MX_OK)
+      return st;
   }
-  if (fmt == MX_E4M3 && (flags & MX_COLWISE)) {
-    if ((st = make_tmap_bytes(&q.colmap, out_col->data, batch * cols, rows)) != MX_OK) return st;
+  if (staged(fmt) && (flags & MX_COLWISE)) {
+    if ((st = make_tmap_bytes(&q.colmap, out_col->data, batch * cols, mx::payload_row_bytes(rows, fmt),
+                              staged_box(fmt))) != MX_OK)
+      return st;
   }
   cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
@@ -546,15 +556,19 @@ mx_status_t mx_permute_quantize(const void* x_bf16, int64_t T, int64_t D, int64_
   // the gather form reads x with plain copies; the map is an unused kernel argument
   if (T > 0) {
     if ((st = make_tmap_bf16(&q.xmap, x_bf16, T, D, ld)) != MX_OK) return st;
-  } else if ((st = make_tmap_bytes(&q.xmap, q.row_data ? q.row_data : q.col_data, 128, 128)) != MX_OK) {
+  } else if ((st = make_tmap_bytes(&q.xmap, q.row_data ? q.row_data : q.col_data, 128, 128, 128)) != MX_OK) {
     return st;
   }
   q.rowmap = q.colmap = q.xmap;
-  if (fmt == MX_E4M3 && (flags & MX_ROWWISE)) {
-    if ((st = make_tmap_bytes(&q.rowmap, out_row->data, R_cap, D)) != MX_OK) return st;
+  if (staged(fmt) && (flags & MX_ROWWISE)) {
+    if ((st = make_tmap_bytes(&q.rowmap, out_row->data, R_cap, mx::payload_row_bytes(D, fmt), staged_box(fmt))) !=
+        MX_OK)
+      return st;
   }
-  if (fmt == MX_E4M3 && (flags & MX_COLWISE)) {
-    if ((st = make_tmap_bytes(&q.colmap, out_col->data, D, R_cap)) != MX_OK) return st;
+  if (staged(fmt) && (flags & MX_COLWISE)) {
+    if ((st = make_tmap_bytes(&q.colmap, out_col->data, D, mx::payload_row_bytes(R_cap, fmt), staged_box(fmt))) !=
+        MX_OK)
+      return st;
   }
   cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantizing permute launch");

@@ -207,21 +207,28 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 
 constexpr int Q_STAGE = 32768;                 // one BF16 tile
 
-// E4M3 tiles are staged in shared memory ([128][128] bytes per orientation,
-// 128-byte swizzle) and written with two TMA stores; the packed sub-byte
-// formats store their blocks directly.
+// E4M3 and E2M1 tiles are staged in shared memory ([128][128] bytes per
+// orientation with the 128-byte swizzle, or [128][64] bytes with the
+// 64-byte swizzle) and written with two TMA stores; E2M3 (24-byte blocks)
+// stores its blocks directly.
 template <int FMT> struct QCfg {
-  static constexpr bool STAGED = FMT == E4M3;
+  static constexpr bool STAGED = FMT == E4M3 || FMT == E2M1;
+  static constexpr int ROW_BYTES = FMT == E4M3 ? 128 : 64;    // staged payload bytes per tile row
+  static constexpr int OUT_BYTES = STAGED ? 128 * ROW_BYTES : 0;  // one orientation
   static constexpr int NST = STAGED ? 2 : 3;   // tiles in the load ring
   static constexpr int OFF_OUT = NST * Q_STAGE;
-  static constexpr int OFF_SC = OFF_OUT + (STAGED ? 32768 : 0);
+  static constexpr int OFF_SC = OFF_OUT + 2 * OUT_BYTES;
   static constexpr int SMEM = OFF_SC + 2048 + 4096 + 64 + 1024;
 };
 
-// Byte offset of (row r, byte b) in a [128][128]-byte staging tile with the
-// 128-byte swizzle the TMA store undoes.
+// Byte offset of (row r, byte b) in a staging tile of 128-byte rows with the
+// 128-byte swizzle, or of 64-byte rows with the 64-byte swizzle, as the TMA
+// store undoes it: the 16-byte chunk index is XORed with (r % 8), or with
+// (r / 2) % 4.
+template <int ROW_BYTES>
 __device__ __forceinline__ uint32_t stage_off(int r, int b) {
-  return (uint32_t)(r * 128 + ((((b >> 4) ^ (r & 7)) << 4) | (b & 15)));
+  const int x = ROW_BYTES == 128 ? (r & 7) : ((r >> 1) & 3);
+  return (uint32_t)(r * ROW_BYTES + ((((b >> 4) ^ x) << 4) | (b & 15)));
 }
 
 // GATHER: the token-permute form.  Every thread copies 8 of the tile's 2048
@@ -237,7 +244,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
   extern __shared__ uint8_t qsm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* out_row = sm + QC::OFF_OUT;                                    // staged payload tiles
-  uint8_t* out_col = out_row + 16384;
+  uint8_t* out_col = out_row + QC::OUT_BYTES;
   uint8_t* sc_all = sm + QC::OFF_SC;                                      // [2 parity][row, col][512]
   float* part_all = reinterpret_cast<float*>(sm + QC::OFF_SC + 2048);     // [2 parity][4][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + QC::OFF_SC + 2048 + 4096);
@@ -367,9 +374,11 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           sb = quantize32<FMT, HAD, SR>(v, amax, w, p.seed,
                                         (uint64_t)((int64_t)b * p.rows + r0 + r) * (uint64_t)p.cols +
                                             (uint64_t)(c0 + cb * 32), 0u);
-          if constexpr (QC::STAGED) {
-            *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(out_row + stage_off(r, cb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          if constexpr (FMT == E4M3) {
+            *reinterpret_cast<uint4*>(out_row + stage_off<128>(r, cb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(out_row + stage_off<128>(r, cb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          } else if constexpr (FMT == E2M1) {
+            *reinterpret_cast<uint4*>(out_row + stage_off<64>(r, cb * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
           } else {
             uint8_t* dst = p.row_data + (int64_t)b * p.row_batch_stride + (r0 + r) * p.row_ld +
                            (c0 + cb * 32) / 32 * BlockBytes<FMT>::value;
@@ -410,9 +419,11 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           sb = quantize32<FMT, HAD, SR>(v, amax, w, p.seed,
                                         (uint64_t)((int64_t)b * p.cols + c0 + cc) * (uint64_t)p.rows +
                                             (uint64_t)(r0 + rb * 32), 1u);
-          if constexpr (QC::STAGED) {
-            *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(out_col + stage_off(cc, rb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          if constexpr (FMT == E4M3) {
+            *reinterpret_cast<uint4*>(out_col + stage_off<128>(cc, rb * 32)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(out_col + stage_off<128>(cc, rb * 32 + 16)) = make_uint4(w[4], w[5], w[6], w[7]);
+          } else if constexpr (FMT == E2M1) {
+            *reinterpret_cast<uint4*>(out_col + stage_off<64>(cc, rb * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
           } else {
             uint8_t* dst = p.col_data + (int64_t)b * p.col_batch_stride + (c0 + cc) * p.col_ld +
                            (r0 + rb * 32) / 32 * BlockBytes<FMT>::value;
@@ -428,8 +439,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 
     if (tid == 0) {
       if constexpr (QC::STAGED) {
-        if constexpr (ROW) tma_store_2d(&rowmap, out_row, (int)c0, (int)(b * p.rows + r0));
-        if constexpr (COL) tma_store_2d(&colmap, out_col, (int)r0, (int)(b * p.cols + c0));
+        // x in payload bytes: one per element (E4M3), one per two (E2M1)
+        constexpr int SH = FMT == E4M3 ? 0 : 1;
+        if constexpr (ROW) tma_store_2d(&rowmap, out_row, (int)(c0 >> SH), (int)(b * p.rows + r0));
+        if constexpr (COL) tma_store_2d(&colmap, out_col, (int)(r0 >> SH), (int)(b * p.cols + c0));
         bulk_commit();
       }
       if (!GATHER && t + Q_NST * (int64_t)gridDim.x < total) issue(t + Q_NST * (int64_t)gridDim.x, s);

@@ -71,13 +71,14 @@ def test_negative_controls_flipped_byte_and_floor_scales(cuda_lib):
     assert np.mean(got != floor) > 0.9
 
 
-def test_rowwise_only_and_colwise_only(cuda_lib):
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1])
+def test_rowwise_only_and_colwise_only(cuda_lib, fmt):
     bits = W.quantizer_input(160, 256, seed=5, special_frac=0.01)
-    xr, xc, _ = _run(cuda_lib, bits, O.E4M3, True, False)
+    xr, xc, _ = _run(cuda_lib, bits, fmt, True, False)
     assert xc is None
-    ref = O.quantize_bf16(bits, O.E4M3, True, True)
+    ref = O.quantize_bf16(bits, fmt, True, True)
     assert_quant_equal(xr, (ref["row_payload"], ref["row_scales"]), 160, 8, "row")
-    xr, xc, _ = _run(cuda_lib, bits, O.E4M3, False, True)
+    xr, xc, _ = _run(cuda_lib, bits, fmt, False, True)
     assert xr is None
     assert_quant_equal(xc, (ref["col_payload"], ref["col_scales"]), 256, 5, "col")
 
@@ -94,7 +95,7 @@ def test_strided_input(cuda_lib):
     assert torch.equal(full, to_dev(bits))
 
 
-@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3])
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
 def test_batched_weights(cuda_lib, fmt):
     """[G, N, K] weights: rowwise of the stack and per-expert columnwise."""
     G, N, K = 3, 256, 384
@@ -129,13 +130,14 @@ def test_rows_zero_is_a_no_op(cuda_lib):
 
 
 @pytest.mark.slow
-def test_quantizer_workload_full_size(cuda_lib):
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M1])
+def test_quantizer_workload_full_size(cuda_lib, fmt):
     """The standalone quantizer workload at full size: 8192 x 7168 BF16,
-    heavy-tailed rows spanning 2^+-20, 0.1 % specials; MXFP8 both
-    orientations, every byte compared."""
+    heavy-tailed rows spanning 2^+-20, 0.1 % specials; MXFP8 and MXFP4,
+    both orientations, every byte compared."""
     bits = W.quantizer_input(**W.QUANT_SHAPE)
-    xr, xc, _ = _run(cuda_lib, bits, O.E4M3)
-    ref = O.quantize_bf16(bits, O.E4M3)
+    xr, xc, _ = _run(cuda_lib, bits, fmt)
+    ref = O.quantize_bf16(bits, fmt)
     assert_quant_equal(xr, (ref["row_payload"], ref["row_scales"]), 8192, 7168 // 32, "row")
     assert_quant_equal(xc, (ref["col_payload"], ref["col_scales"]), 7168, 8192 // 32, "col")
 
