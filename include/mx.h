@@ -507,7 +507,10 @@ MX_API size_t mx_mlp_workspace_bytes(const mx_mlp_args_t *args);
  * quantize X, W1, W2 (rowwise and per-expert columnwise); FC1 + SwiGLU
  * (mx_grouped_gemm_swiglu_fwd); FC2 (mx_grouped_gemm); quantize dY; FC2
  * dgrad + dSwiGLU (mx_grouped_gemm_dswiglu_bwd); FC1 dgrad
- * (mx_grouped_gemm); dW2 and dW1 (mx_grouped_gemm_wgrad).  10 launches.
+ * (mx_grouped_gemm); dW2 and dW1 (mx_grouped_gemm_wgrad_ws: the largest
+ * experts' K range split, with the split workspace inside `workspace`).
+ * 10 kernel launches (plus one small memset of the split counters per
+ * weight gradient when the routing has more than one expert).
  * ([MXFP8-PR] cudnn-fe ops commit: the four ops of the routed-expert MLP;
  * [MXFP6-PR] fused-MLP commit: owning fc1 -> activation -> fc2 in one unit.)
  */
