@@ -525,9 +525,44 @@ def dense_step_rate(mx, torch, dev, steps=5):
     flops = 12.0 * M * D * H
     peaks, _ = measured_peaks()
     tf = flops / (ms * 1e-3) / 1e12
+    # the same stages through their entry points, one at a time
+    f = mx.E2M3
+    q = {k: (mx.MX(r, c, f, True), mx.MX(c, r, f, True)) for k, (r, c) in
+         {"x": (M, D), "w1": (H, D), "w2": (D, H), "dy": (M, D)}.items()}
+    cs = torch.empty(D, dtype=torch.float32, device=dev)
+    cws = torch.empty(max(16, int(mx.load().mx_quantize_workspace_bytes(M, D, mx.ROWWISE | mx.COLWISE | mx.COLSUM))),
+                      dtype=torch.uint8, device=dev)
+    quant = lambda k, colsum=False: mx.mx_quantize(inp[k], f, True, True, True, colsum=colsum, out_row=q[k][0],
+                                                   out_col=q[k][1], colsum_out=cs if colsum else None,
+                                                   workspace=cws if colsum else None)
+    for k in ("x", "w1", "w2"):
+        quant(k)
+    quant("dy", True)
+    pre, ar, ac = mx.mx_gemm_gelu_fwd(q["x"][0], q["w1"][0], inp["b1"])
+    dpr, dpc, db1 = mx.mx_gemm_dgelu_bwd(q["dy"][0], q["w2"][1], pre)
+    calls = {
+        "quant_x": lambda: quant("x"), "quant_w1": lambda: quant("w1"), "quant_w2": lambda: quant("w2"),
+        "fc1_gelu": lambda: mx.mx_gemm_gelu_fwd(q["x"][0], q["w1"][0], inp["b1"], pre, ar, ac),
+        "fc2": lambda: mx.mx_gemm_bias(ar, q["w2"][0], inp["b2"], out=out["y"]),
+        "quant_dy_colsum": lambda: quant("dy", True),
+        "fc2_dgrad_dgelu": lambda: mx.mx_gemm_dgelu_bwd(q["dy"][0], q["w2"][1], pre, dpr, dpc, db1),
+        "fc1_dgrad": lambda: mx.mx_grouped_gemm(dpr, q["w1"][1], 1, None, out=out["dx"]),
+        "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad(q["dy"][1], ac, 1, None, out=out["dw2"]),
+        "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad(dpc, q["x"][1], 1, None, out=out["dw1"]),
+    }
+    for c in calls.values():
+        c()
+    torch.cuda.synchronize(dev)
+    st = {k: 0.0 for k in calls}
+    for _ in range(5):
+        for k, c in calls.items():
+            st[k] += _event_mean(torch, stream, dev, c, 1) / 5
+    gemm = 2.0 * M * D * H
+    stages = {k: {"ms": v, "tflops": gemm / (v * 1e-3) / 1e12} if k[:5] in ("fc1_g", "fc2", "fc2_d", "fc1_d", "wgrad")
+              else {"ms": v} for k, v in st.items()}
     return {"workload": "dense mxfp6-e2m3 + hadamard tanh-GELU MLP fwd+bwd M=16384 D=3072 H=12288",
             "ms_per_step": ms, "tflops": tf, "frac_of_fp8_peak": tf / (2.0 * peaks["bf16_tflops"]),
-            "launches_per_step": 12}
+            "launches_per_step": 12, "stages": stages}
 
 
 def moe_forward_even_rate(mx, torch, dev, steps=5):
