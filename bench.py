@@ -678,6 +678,7 @@ def variant_rates(mx, torch, dev, reps=10):
     r, c = mx.MX(rows, cols, mx.E2M1), mx.MX(cols, rows, mx.E2M1)
     rh, ch = mx.MX(rows, cols, mx.E2M1, True), mx.MX(cols, rows, mx.E2M1, True)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
     qcalls = {
         "quant_e2m1_rne": lambda: mx.mx_quantize(x, mx.E2M1, True, True, out_row=r, out_col=c),
         "quant_e2m1_sr": lambda: mx.mx_quantize_sr(x, mx.E2M1, 1234, True, True, out_row=r, out_col=c),
@@ -689,7 +690,7 @@ def variant_rates(mx, torch, dev, reps=10):
     qsums = {k: 0.0 for k in qcalls}
     for _ in range(reps):
         for k, qc in qcalls.items():
-            qsums[k] += _event_mean(torch, stream, dev, qc, 1, before=lambda: flush.fill_(1))
+            qsums[k] += _event_mean(torch, stream, dev, qc, 1, before=lambda: (flush.fill_(1), clean.max()))
     n = rows * cols
     qbytes = n * 2 + 2 * n * (0.5 + 1.0 / 32)  # BF16 in; two MXFP4 copies out
     peaks, _ = measured_peaks()
@@ -697,7 +698,8 @@ def variant_rates(mx, torch, dev, reps=10):
         ms = s / reps
         gbs = qbytes / (ms * 1e-3) / 1e9
         res[k] = {"us": ms * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
-    res["quant_workload"] = "8192x7168 bf16 -> mxfp4 row+col, L2 flushed (512 MB write) between iterations"
+    res["quant_workload"] = ("8192x7168 bf16 -> mxfp4 row+col, L2 flushed between iterations (512 MB written, then "
+                             "512 MB read)")
     status = mx.mx_get_device_status()
     if status != "MX_OK":
         raise RuntimeError("device status after variants: " + status)
@@ -812,24 +814,33 @@ def quantizer_rate(mx, torch, dev):
         x = torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
     r, c = mx.MX(rows, cols), mx.MX(cols, rows)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(3):
         mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
-    ts = []
-    for _ in range(20):
-        flush.fill_(1)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ts.append(e0.elapsed_time(e1))
-    ms = float(np.mean(ts))
+
+    def timed(after_write_read):
+        ts = []
+        for _ in range(20):
+            flush.fill_(1)
+            if after_write_read:  # evict the flush's dirty lines before the timed launch
+                clean.max()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            mx.mx_quantize(x, 0, True, True, out_row=r, out_col=c)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+
+    ms, ms_dirty = timed(True), timed(False)
     peaks, kind = measured_peaks()
     gbs = QUANT_GB / (ms * 1e-3) / 1e9
     return {"workload": "8192x7168 bf16 -> mxfp8 row+col", "us": ms * 1e3, "gbs": gbs,
             "frac_of_hbm": gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"], "peak_kind": kind,
-            "l2": "flushed (512 MB write) between iterations"}
+            "l2": "flushed between iterations: 512 MB written, then 512 MB read so no dirty line is left",
+            "us_dirty_l2": ms_dirty * 1e3,
+            "note_dirty_l2": "the same with the 512 MB write alone: the launch also writes back the flush's dirty lines"}
 
 
 def ncu_case(name, launches=3):
