@@ -550,3 +550,34 @@ def test_wgrad_k_split_writes_nothing_outside_its_output(cuda_lib):
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     assert torch.isnan(buf[:2]).all() and torch.isnan(buf[2 + G:]).all()
     assert (out[1] == 0).all() and not torch.isnan(out).any()
+
+
+def test_malformed_offsets_reported_on_device_and_opt_in_host_check(cuda_lib, monkeypatch):
+    """Offsets that are not multiples of 128: by default the call launches,
+    the kernels skip the malformed segments (their rows stay untouched) and
+    mx_get_device_status reports MX_ERR_OFFSETS once; with
+    MX_VALIDATE_OFFSETS=1 the host reads the offsets first and returns
+    MX_ERR_OFFSETS without launching."""
+    import torch
+    G, K, N, R = 2, 256, 256, 512
+    rng = np.random.default_rng(160)
+    ar, _, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (R, K)))
+    br, _, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (G, N, K), std=0.02))
+    bad = torch.tensor([100, 256], dtype=torch.int32, device="cuda")
+    out = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm(ar, br, G, bad, out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_ERR_OFFSETS"
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert torch.isnan(out[:256]).all(), "rows of malformed segments were written"
+    monkeypatch.setenv("MX_VALIDATE_OFFSETS", "1")
+    with pytest.raises(cuda_lib.MXError) as e:
+        cuda_lib.mx_grouped_gemm(ar, br, G, bad, out=out)
+    assert e.value.name == "MX_ERR_OFFSETS"
+    dec = torch.tensor([256, 128], dtype=torch.int32, device="cuda")
+    with pytest.raises(cuda_lib.MXError) as e:
+        cuda_lib.mx_grouped_gemm(ar, br, G, dec, out=out)
+    assert e.value.name == "MX_ERR_OFFSETS" and "decreases" in str(e.value)
+    good = torch.tensor([256, 512], dtype=torch.int32, device="cuda")
+    cuda_lib.mx_grouped_gemm(ar, br, G, good, out=out)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert not torch.isnan(out).any()
