@@ -124,7 +124,7 @@ cudaError_t launch_gemm_f4(const GemmParams& p, const CUtensorMap& ta, const CUt
 cudaError_t read_f4_status(unsigned* out);
 cudaError_t reset_f4_status();
 // Token permute support (permute.cu).  counts: the workspace, int32
-// [ceil(T*k / 1024), G].
+// [G, ceil(T*k / 1024)] (expert-major).
 cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int32_t* offsets, int32_t* src,
                                int64_t R_cap, int32_t* row_of, int32_t* counts, cudaStream_t s);
 cudaError_t launch_unpermute(const uint16_t* in, int64_t R, int64_t D, const int32_t* row_of, const float* w,

@@ -20,8 +20,9 @@ static __device__ unsigned g_perm_status = 0;
 
 constexpr int ROUTE_CHUNK = 1024;  // (token, choice) entries per counting chunk
 
-// Pass 1: per-chunk expert histograms, counts[chunk][G].
-__global__ void route_count_kernel(const int32_t* __restrict__ topk, int64_t n, int G, int32_t* __restrict__ counts) {
+// Pass 1: per-chunk expert histograms, expert-major: counts[e][chunk].
+__global__ void route_count_kernel(const int32_t* __restrict__ topk, int64_t n, int G, int nchunks,
+                                   int32_t* __restrict__ counts) {
   extern __shared__ int32_t hist[];
   for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -33,59 +34,96 @@ __global__ void route_count_kernel(const int32_t* __restrict__ topk, int64_t n, 
     else atomicOr(&g_perm_status, DEV_BAD_INDEX);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G; e += blockDim.x) counts[(int64_t)blockIdx.x * G + e] = hist[e];
+  for (int e = threadIdx.x; e < G; e += blockDim.x) counts[(int64_t)e * nchunks + blockIdx.x] = hist[e];
 }
 
-// Pass 2 (one block): per expert, the chunk counts become absolute first
-// rows of each chunk's entries; padded segment ends go to offsets; padding
-// rows and the rows past the last segment get source -1.
+// Pass 2 (one block of 1024 threads): per expert, the chunk counts become
+// absolute first rows of each chunk's entries (a warp scans an expert's
+// chunks 256 at a time, 8 per lane, with a shuffle scan across lanes);
+// padded segment ends go to offsets; padding rows and the rows past the
+// last segment get source -1.
 __global__ void route_scan_kernel(int32_t* __restrict__ counts, int nchunks, int G, int32_t* __restrict__ offsets,
                                   int32_t* __restrict__ src, int64_t R_cap) {
   __shared__ int32_t tot[1024];
+  __shared__ int32_t first[1024];
   __shared__ int32_t end[1024];
-  for (int e = threadIdx.x; e < G; e += blockDim.x) {
-    int32_t run = 0;
-    for (int c = 0; c < nchunks; c++) {
-      const int32_t v = counts[(int64_t)c * G + e];
-      counts[(int64_t)c * G + e] = run;
-      run += v;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  for (int e = warp; e < G; e += nwarps) {
+    int32_t* ce = counts + (int64_t)e * nchunks;
+    int32_t carry = 0;
+    for (int base = 0; base < nchunks; base += 256) {
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const int c = base + lane * 8 + j;
+        v[j] = c < nchunks ? ce[c] : 0;
+      }
+      int32_t run = 0;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const int32_t t = v[j];
+        v[j] = run;
+        run += t;
+      }
+      int32_t incl = run;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const int32_t excl = incl - run;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const int c = base + lane * 8 + j;
+        if (c < nchunks) ce[c] = carry + excl + v[j];
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    tot[e] = run;
+    if (lane == 0) tot[e] = carry;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     int32_t acc = 0;
     for (int e = 0; e < G; e++) {
-      acc += (tot[e] + 127) & ~127;
+      const int32_t padded = (tot[e] + 127) & ~127;
+      first[e] = acc;
+      acc += padded;
       end[e] = acc;
       offsets[e] = acc;
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G; e += blockDim.x) {
-    const int32_t start = end[e] - ((tot[e] + 127) & ~127);
-    for (int c = 0; c < nchunks; c++) counts[(int64_t)c * G + e] += start;
-    for (int32_t r = start + tot[e]; r < end[e]; r++) src[r] = -1;
-  }
+  for (int64_t idx = threadIdx.x; idx < (int64_t)G * nchunks; idx += blockDim.x)
+    counts[idx] += first[idx / nchunks];
+  for (int e = warp; e < G; e += nwarps)
+    for (int32_t r = first[e] + tot[e] + lane; r < end[e]; r += 32) src[r] = -1;
   for (int64_t r = (int64_t)end[G - 1] + threadIdx.x; r < R_cap; r += blockDim.x) src[r] = -1;
 }
 
-// Pass 3: one warp per chunk walks its entries in order, 32 at a time;
-// lanes routed to the same expert take consecutive rows in lane order.
-__global__ void route_scatter_kernel(const int32_t* __restrict__ topk, int64_t n, int k, int G,
+// Pass 3: one warp per chunk walks its entries in order, 32 at a time
+// (all of the chunk's expert ids loaded first); lanes routed to the same
+// expert take consecutive rows in lane order.
+__global__ void route_scatter_kernel(const int32_t* __restrict__ topk, int64_t n, int k, int G, int nchunks,
                                      const int32_t* __restrict__ counts, int32_t* __restrict__ src,
                                      int32_t* __restrict__ row_of) {
   extern __shared__ int32_t next[];
   const int lane = threadIdx.x;
-  for (int e = lane; e < G; e += 32) next[e] = counts[(int64_t)blockIdx.x * G + e];
-  __syncwarp();
+  for (int e = lane; e < G; e += 32) next[e] = counts[(int64_t)e * nchunks + blockIdx.x];
   const int64_t b0 = (int64_t)blockIdx.x * ROUTE_CHUNK;
   const int64_t b1 = b0 + ROUTE_CHUNK < n ? b0 + ROUTE_CHUNK : n;
+  int ev[ROUTE_CHUNK / 32];
+#pragma unroll
+  for (int it = 0; it < ROUTE_CHUNK / 32; it++) {
+    const int64_t i = b0 + it * 32 + lane;
+    ev[it] = i < b1 ? __ldg(topk + i) : -1;
+  }
+  __syncwarp();
   const unsigned below = (1u << lane) - 1u;
-  for (int64_t i0 = b0; i0 < b1; i0 += 32) {
-    const int64_t i = i0 + lane;
+#pragma unroll
+  for (int it = 0; it < ROUTE_CHUNK / 32; it++) {
+    const int64_t i = b0 + it * 32 + lane;
     const bool in = i < b1;
-    const int e = in ? __ldg(topk + i) : -1;
+    const int e = ev[it];
     const bool ok = in && e >= 0 && e < G;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? e : -1) & __ballot_sync(0xFFFFFFFFu, ok);
     int32_t pos = -1;
@@ -106,14 +144,14 @@ cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int
   const int nchunks = (int)((n + ROUTE_CHUNK - 1) / ROUTE_CHUNK);
   const size_t hist = (size_t)G * sizeof(int32_t);
   if (nchunks > 0) {
-    route_count_kernel<<<nchunks, 256, hist, s>>>(topk, n, G, counts);
+    route_count_kernel<<<nchunks, 256, hist, s>>>(topk, n, G, nchunks, counts);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   route_scan_kernel<<<1, 1024, 0, s>>>(counts, nchunks, G, offsets, src, R_cap);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nchunks == 0) return e;
-  route_scatter_kernel<<<nchunks, 32, hist, s>>>(topk, n, k, G, counts, src, row_of);
+  route_scatter_kernel<<<nchunks, 32, hist, s>>>(topk, n, k, G, nchunks, counts, src, row_of);
   return cudaGetLastError();
 }
 

@@ -581,3 +581,28 @@ def test_malformed_offsets_reported_on_device_and_opt_in_host_check(cuda_lib, mo
     cuda_lib.mx_grouped_gemm(ar, br, G, good, out=out)
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     assert not torch.isnan(out).any()
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E2M3, O.E2M1])
+def test_one_hot_probe_tensor_core_reads_our_element_order(cuda_lib, fmt):
+    """Row i of A is one-hot at K position i (i < 256: every position of
+    eight 32-element blocks, both nibbles / all four 6-bit slots of each
+    packed group), B holds distinct small integers; then Y[i, n] must be
+    B[n, i] exactly.  A packing-order or scale-slot mismatch between our
+    payload layout and the tensor core's reading moves values to other K
+    positions and fails here position by position (E2M1 runs kind::mxf4)."""
+    import torch
+    K, N = 256, 256
+    a = np.zeros((256, K), dtype=np.float32)
+    a[np.arange(256), np.arange(256)] = 1.0
+    n_idx, k_idx = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    b = (((n_idx * 5 + k_idx * 3) % 7) - 3).astype(np.float32)          # -3..3, exact in every format
+    ar, _, aref = _quant_both(cuda_lib, W.to_bf16_bits(a), fmt=fmt)
+    br, _, bref = _quant_both(cuda_lib, W.to_bf16_bits(b), fmt=fmt)
+    assert np.array_equal(_deq(aref["row_payload"], aref["row_scales"], 256, K, fmt), a)
+    assert np.array_equal(_deq(bref["row_payload"], bref["row_scales"], N, K, fmt), b)
+    y = cuda_lib.mx_gemm_bias(ar, br, None)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    got = bf16_cpu(y)
+    bad = np.argwhere(got != b.T)
+    assert bad.size == 0, "first wrong (row=K position, n): %s" % bad[:4].tolist()
