@@ -178,3 +178,82 @@ def test_mlp_step_full_size_runs_and_is_deterministic(cuda_lib, routing):
         assert torch.equal(first[k], out[k]), k
         assert bool(torch.isfinite(out[k].float()).all()), k
     assert bool((out["dw1"][empty] == 0).all()) and bool((out["dw2"][empty] == 0).all())
+
+
+def test_swiglu_probs_fwd_bwd_full_size_sampled_rows(cuda_lib, routing):
+    """The routing-probability forms at full size: h = swiglu(z) * p[r]
+    requantized (sampled rows within one step), and the backward's dz =
+    dSwiGLU(dh * p) bytes and dprobs[r] = sum_f dh * swiglu(z) on the same
+    rows (z saved by the forward, so the backward's input is the GPU's own
+    BF16 z, which the oracle reads as given)."""
+    import torch
+    counts, offsets, big, empty, small = routing
+    x = _rand_bf16((R, D), 1.0, 111)
+    w1 = _rand_bf16((G, 2 * F, D), 0.02, 112)
+    dy = _rand_bf16((R, D), 1e-3, 113)
+    w2t = _rand_bf16((G, F, D), 0.02, 114)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(115)
+    probs = torch.rand(R, generator=g, device="cuda") * 0.9 + 0.05
+    offs = torch.from_numpy(offsets).cuda()
+    xr, _, _ = cuda_lib.mx_quantize(x, O.E4M3, True, False)
+    wr, _, _ = cuda_lib.mx_quantize(w1, O.E4M3, True, False)
+    z, h_row, _ = cuda_lib.mx_grouped_gemm_swiglu_probs_fwd(xr, wr, G, offs, probs)
+    dyr, _, _ = cuda_lib.mx_quantize(dy, O.E4M3, True, False)
+    wtr, _, _ = cuda_lib.mx_quantize(w2t, O.E4M3, True, False)
+    dz_row, _, dprobs = cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, wtr, z, probs, G, offs)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    rows = _sample_rows(offsets, [big, small], per=16, seed=5)
+    idx = torch.from_numpy(rows).cuda()
+    p = probs[idx].cpu().numpy().astype(np.float64)
+    hp, dzp = h_row.data[idx].cpu().numpy(), dz_row.data[idx].cpu().numpy()
+    dpg = dprobs[idx].cpu().numpy().astype(np.float64)
+    xb, dyb, zb = _bits(x[idx]), _bits(dy[idx]), _bits(z[idx])
+    for e in sorted({_expert_of(offsets, r) for r in rows}):
+        sel = np.array([_expert_of(offsets, r) == e for r in rows])
+        xq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(xb[sel]), O.E4M3), int(sel.sum()), D, O.E4M3)
+        wq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w1[e])), O.E4M3), 2 * F, D, O.E4M3)
+        zref = xq @ wq.T
+        h = O.round_f32(O.swiglu(zref[:, :F], zref[:, F:]) * p[sel][:, None])
+        assert np.mean(hp[sel] != O.quantize_rows(h, O.E4M3)[0]) < 1e-2
+        dyq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(dyb[sel]), O.E4M3), int(sel.sum()), D, O.E4M3)
+        w2q = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w2t[e])), O.E4M3), F, D, O.E4M3)
+        zf = O.bf16_to_f64(zb[sel])
+        dh = dyq @ w2q.T
+        act = O.swiglu(zf[:, :F], zf[:, F:])
+        dg, du = O.dswiglu(dh * p[sel][:, None], zf[:, :F], zf[:, F:])
+        ref_p, _ = O.quantize_rows(O.round_f32(np.concatenate([dg, du], axis=1)), O.E4M3)
+        assert np.mean(dzp[sel] != ref_p) < 1e-2
+        want = np.sum(dh * act, axis=1)
+        scale = np.sqrt(np.sum((dh * act) ** 2, axis=1)) + 1e-30
+        assert np.all(np.abs(dpg[sel] - want) <= 2.0 ** -8 * np.abs(want) + 2.0 ** -10 * scale), e
+
+
+def test_wgrad_into_fp32_full_size_sampled_entries(cuda_lib, routing):
+    """The fp32 main-grad wgrad at full size (largest expert, K-split form):
+    the store within tolerance of the oracle's entries, the accumulate equal
+    to grad + store bit for bit, an empty expert's slice zero / untouched."""
+    import torch
+    counts, offsets, big, empty, small = routing
+    dy = _rand_bf16((R, D), 1e-3, 121)
+    h = _rand_bf16((R, F), 0.5, 122)
+    offs = torch.from_numpy(offsets).cuda()
+    _, dyc, _ = cuda_lib.mx_quantize(dy, O.E4M3, False, True)
+    _, hc, _ = cuda_lib.mx_quantize(h, O.E4M3, False, True)
+    st = torch.empty((G, D, F), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_grouped_gemm_wgrad_f32_ws(dyc, hc, G, offs, st, accumulate=False)
+    g0 = _rand_bf16((G, D, F), 1e-2, 123).float()
+    acc = g0.clone()
+    cuda_lib.mx_grouped_gemm_wgrad_f32_ws(dyc, hc, G, offs, acc, accumulate=True)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    assert bool((st[empty] == 0).all()) and torch.equal(acc[empty], g0[empty])
+    assert torch.equal(acc, g0 + st), "accumulate is not fl32(grad + the stored sum)"
+    rng = np.random.default_rng(6)
+    s, e = (int(offsets[big - 1]) if big else 0), int(offsets[big])
+    ns, ks = np.sort(rng.choice(D, 8, replace=False)), np.sort(rng.choice(F, 8, replace=False))
+    a = O.bf16_to_f64(_bits(dy[s:e][:, torch.from_numpy(ns).cuda()]))
+    b = O.bf16_to_f64(_bits(h[s:e][:, torch.from_numpy(ks).cuda()]))
+    aq = O.dequantize_rows(*O.quantize_cols(a, O.E4M3), 8, e - s, O.E4M3)
+    bq = O.dequantize_rows(*O.quantize_cols(b, O.E4M3), 8, e - s, O.E4M3)
+    got = st[big][torch.from_numpy(ns).cuda()][:, torch.from_numpy(ks).cuda()].cpu().numpy().astype(np.float64)
+    assert O.within_tolerance(got, aq @ bq.T).all()

@@ -187,3 +187,18 @@ def test_stochastic_rounding_seed_dependence(cuda_lib):
     assert torch.equal(a.data, b.data) and torch.equal(a.scale, b.scale)
     assert torch.equal(a.scale, c.scale)
     assert float((a.data != c.data).float().mean()) > 0.2
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("fmt", [O.E2M1, O.E2M3])
+def test_stochastic_rounding_full_size_workload(cuda_lib, fmt):
+    """Stochastic rounding on the full 8192 x 7168 workload (heavy-tailed
+    rows, 0.1 % specials), both orientations, every byte against the
+    oracle's Philox-driven rounding."""
+    bits = W.quantizer_input(**W.QUANT_SHAPE)
+    r, c = cuda_lib.mx_quantize_sr(to_dev(bits), fmt, 0x5EED, True, True)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    row, col = _oracle_sr(bits, fmt, 0x5EED, False)
+    rows, cols = bits.shape
+    assert_quant_equal(r, row, rows, cols // 32, "row")
+    assert_quant_equal(c, col, cols, rows // 32, "col")
