@@ -543,9 +543,12 @@ MX_API mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t *args, mx_stream_t stream)
  *           memory is needed for the copies to run asynchronously.  Host
  *           buffers are read and written after the call returns: keep them
  *           alive and unchanged (inputs) or unread (outputs) until
- *           mx_mlp_pipeline_sync.  Returns MX_ERR_INVALID_ARG for a missing
- *           host buffer, MX_ERR_CUDA if enqueuing failed (later runs then
- *           fail too).
+ *           mx_mlp_pipeline_sync.  w1, w2, dw1 and dw2 may be NULL: those
+ *           tensors then stay resident in the device buffers (weights the
+ *           caller keeps and updates on the device, gradients it consumes
+ *           there), as in a training loop with the optimizer on the device.
+ *           Returns MX_ERR_INVALID_ARG for another missing host buffer,
+ *           MX_ERR_CUDA if enqueuing failed (later runs then fail too).
  * mx_mlp_pipeline_sync     wait for every enqueued step, copies included
  * mx_mlp_pipeline_destroy  sync, then release streams and events
  */

@@ -128,8 +128,10 @@ mx_status_t mx_mlp_pipeline_run(mx_mlp_pipeline_t* p, const mx_mlp_host_io_t* io
   const mx_mlp_args_t& a = p->dev;
   TensorIO t[mx::T_COUNT];
   step_tensors(a, io, t);
+  // weights and their gradients may stay on the device (no host buffer)
+  auto resident_ok = [](int k) { return k == mx::T_W1 || k == mx::T_W2 || k == mx::T_DW1 || k == mx::T_DW2; };
   for (int k = 0; k < mx::T_COUNT; k++) {
-    if (t[k].dev == nullptr) continue;
+    if (t[k].dev == nullptr || resident_ok(k)) continue;
     if (mx::step_tensor_is_input(k) ? t[k].host_in == nullptr : t[k].host_out == nullptr) {
       char buf[96];
       snprintf(buf, sizeof(buf), "host buffer of step tensor %d is NULL", k);
@@ -142,7 +144,7 @@ mx_status_t mx_mlp_pipeline_run(mx_mlp_pipeline_t* p, const mx_mlp_host_io_t* io
   // host -> device, in the order the step reads them
   const int in_order[] = {mx::T_X, mx::T_W1, mx::T_W2, mx::T_B1, mx::T_B2, mx::T_DY};
   for (int k : in_order) {
-    if (t[k].dev == nullptr) continue;
+    if (t[k].dev == nullptr || t[k].host_in == nullptr) continue;
     note(p, cudaStreamWaitEvent(p->copy_in, p->in_free[k], 0));
     note(p, cudaMemcpyAsync(t[k].dev, t[k].host_in, t[k].bytes, cudaMemcpyHostToDevice, p->copy_in));
     note(p, cudaEventRecord(p->in_ready[k], p->copy_in));
@@ -159,7 +161,7 @@ mx_status_t mx_mlp_pipeline_run(mx_mlp_pipeline_t* p, const mx_mlp_host_io_t* io
   // device -> host, in the order the step writes them
   const int out_order[] = {mx::T_Y, mx::T_DB2, mx::T_DB1, mx::T_DX, mx::T_DW2, mx::T_DW1};
   for (int k : out_order) {
-    if (t[k].dev == nullptr) continue;
+    if (t[k].dev == nullptr || t[k].host_out == nullptr) continue;
     note(p, cudaStreamWaitEvent(p->copy_out, p->out_ready[k], 0));
     note(p, cudaMemcpyAsync(t[k].host_out, t[k].dev, t[k].bytes, cudaMemcpyDeviceToHost, p->copy_out));
     note(p, cudaEventRecord(p->out_done[k], p->copy_out));

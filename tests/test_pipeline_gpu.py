@@ -121,3 +121,54 @@ def test_pipeline_dense_gelu_steps_match_device_step(cuda_lib):
         want = _device_step(cuda_lib, inp, None, 1, H, cuda_lib.ACT_GELU_TANH, cuda_lib.E2M3, True)
         for k in want:
             assert torch.equal(got[i][k], want[k]), (i, k)
+
+
+def test_pipeline_with_resident_weights(cuda_lib):
+    """Weights kept on the device (no w1 / w2 / dw1 / dw2 host buffers): each
+    step's y and dX come back bitwise equal to the device step's, and the
+    last step's weight gradients are left in the device buffers."""
+    import torch
+    mx = cuda_lib
+    G, D, F, R = 4, 1024, 384, 1152
+    raw0 = W.moe_inputs(G, D, F, R, seed=40, dy_seed=41)
+    to_t = lambda v: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).view(torch.bfloat16)
+    weights = {k: to_t(raw0[k]) for k in ("w1", "w2")}
+    steps = []
+    for i, counts in enumerate([[384, 0, 256, 384], [128, 512, 256, 256]]):
+        raw = W.moe_inputs(G, D, F, R, seed=42 + i, dy_seed=50 + i)
+        inp = {k: to_t(raw[k]) for k in ("x", "dy")}
+        inp.update(weights)
+        steps.append((inp, torch.from_numpy(W.offsets_from_counts(counts))))
+    dev = "cuda"
+    dd = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in steps[0][0].items()}
+    dd["w1"].copy_(weights["w1"])
+    dd["w2"].copy_(weights["w2"])
+    dout = {"y": torch.empty((R, D), dtype=torch.bfloat16, device=dev),
+            "dx": torch.empty((R, D), dtype=torch.bfloat16, device=dev),
+            "dw1": torch.empty(weights["w1"].shape, dtype=torch.bfloat16, device=dev),
+            "dw2": torch.empty(weights["w2"].shape, dtype=torch.bfloat16, device=dev)}
+    doff = torch.empty(G, dtype=torch.int32, device=dev)
+    a0 = mx.mlp_args(dd["x"], dd["w1"], dd["w2"], dd["dy"], doff, G, F, dout["y"], dout["dx"], dout["dw1"],
+                     dout["dw2"])
+    ws = torch.empty(mx.mx_mlp_workspace_bytes(a0), dtype=torch.uint8, device=dev)
+    a = mx.mlp_args(dd["x"], dd["w1"], dd["w2"], dd["dy"], doff, G, F, dout["y"], dout["dx"], dout["dw1"],
+                    dout["dw2"], workspace=ws)
+    pipe = mx.MlpPipeline(a)
+    results, keep = [], []
+    for inp, offs in steps:
+        host = {"x": _pinned(inp["x"]), "dy": _pinned(inp["dy"]), "offsets": _pinned(offs)}
+        outs = {k: torch.full((R, D), float("nan"), dtype=torch.bfloat16, pin_memory=True) for k in ("y", "dx")}
+        host.update(outs)
+        pipe.run(host)
+        keep.append(host)
+        results.append(outs)
+    pipe.sync()
+    pipe.close()
+    assert mx.mx_get_device_status() == "MX_OK"
+    for i, (inp, offs) in enumerate(steps):
+        want = _device_step(mx, inp, offs, G, F, mx.ACT_SWIGLU, mx.E4M3, False)
+        A = int(offs[-1])
+        for k in ("y", "dx"):
+            assert torch.equal(results[i][k][:A], want[k][:A]), (i, k)
+    for k in ("dw1", "dw2"):
+        assert torch.equal(dout[k].cpu(), want[k]), k
