@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119369472,
-    "quant_w1": 1572993024,
-    "quant_w2": 755268608,
-    "fc1_swiglu": 2292543040,
-    "fc2": 1452804672,
-    "quant_dy": 2119402240,
-    "fc2_dgrad_dswiglu": 2727847616,
-    "fc1_dgrad": 1871048448,
-    "wgrad_dw2": 1273574528,
-    "wgrad_dw1": 2284071744,
+    "quant_x": 2119296768,
+    "quant_w1": 1573072064,
+    "quant_w2": 755416000,
+    "fc1_swiglu": 2262478784,
+    "fc2": 1449511360,
+    "quant_dy": 2119643328,
+    "fc2_dgrad_dswiglu": 2734874176,
+    "fc1_dgrad": 1869400064,
+    "wgrad_dw2": 1272231360,
+    "wgrad_dw1": 2299763584,
 }
 
 
