@@ -1049,8 +1049,10 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
   p.sfa = a->scale; p.sfb = b->scale;
   p.sfa_kchunks = (K / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
+  // 256-column tiles (the 128x256 MMA) where H allows, else 128
+  const int tile_n = H % 256 == 0 ? 256 : 128;
   p.m_tiles = (int)(M / 128);
-  p.n_tiles = (int)(H / 128);
+  p.n_tiles = (int)(H / tile_n);
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.z = static_cast<uint16_t*>(pre_bf16);
   p.q_row = static_cast<uint8_t*>(q_row->data); p.q_row_scale = q_row->scale;
@@ -1062,7 +1064,7 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
   p.q_had = q_row->hadamard ? 1 : 0;
   p.bias = static_cast<const uint16_t*>(bias_bf16);
   p.colsum_partials = partials;
-  p.tx_bytes = stage_tx_bytes(a->fmt, 128);
+  p.tx_bytes = stage_tx_bytes(a->fmt, tile_n);
   CUtensorMap ta, tb, to;
   if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
   if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
@@ -1072,7 +1074,7 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
     to = ta;
   }
   if ((st = attach_tap(&p, p.R, p.q_cols)) != MX_OK) return st;
-  cudaError_t e = mx::launch_gemm_dense(p, ta, tb, to, s, dev.sms);
+  cudaError_t e = mx::launch_gemm_dense(p, ta, tb, to, tile_n, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
   return MX_OK;
 }

@@ -11,11 +11,11 @@
 
 namespace mx {
 
-template <int EPI, int QF, bool QH>
+template <int BN, int EPI, int QF, bool QH>
 static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                                     const CUtensorMap& to, cudaStream_t s, int num_sms) {
-  auto kern = mx_gemm_kernel<128, EPI, MODE_GROUPED, QF, QH>;
-  constexpr int smem = Cfg<128>::SMEM_BYTES;
+  auto kern = mx_gemm_kernel<BN, EPI, MODE_GROUPED, QF, QH>;
+  constexpr int smem = Cfg<BN, false, false, BN == 256>::SMEM_BYTES;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -28,23 +28,27 @@ static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, 
   return cudaGetLastError();
 }
 
-template <int EPI>
+template <int BN, int EPI>
 static cudaError_t dispatch_q(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
-  if (p.q_fmt == E2M3 && p.q_had) return launch_dense_one<EPI, E2M3, true>(p, ta, tb, to, s, num_sms);
-  if (p.q_fmt == E2M3) return launch_dense_one<EPI, E2M3, false>(p, ta, tb, to, s, num_sms);
-  if (p.q_fmt == E4M3 && p.q_had) return launch_dense_one<EPI, E4M3, true>(p, ta, tb, to, s, num_sms);
-  if (p.q_fmt == E4M3) return launch_dense_one<EPI, E4M3, false>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E2M3 && p.q_had) return launch_dense_one<BN, EPI, E2M3, true>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E2M3) return launch_dense_one<BN, EPI, E2M3, false>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E4M3 && p.q_had) return launch_dense_one<BN, EPI, E4M3, true>(p, ta, tb, to, s, num_sms);
+  if (p.q_fmt == E4M3) return launch_dense_one<BN, EPI, E4M3, false>(p, ta, tb, to, s, num_sms);
   return cudaErrorInvalidValue;
 }
 
+// bn = 256 where the output width allows (the 128x256 MMA, tensor-memory
+// parking in the epilogue), else 128.
 cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                              const CUtensorMap& to, cudaStream_t s, int num_sms) {
-  cudaError_t e;
-  if (p.epi == EPI_GELU) return dispatch_q<EPI_GELU>(p, ta, tb, to, s, num_sms);
-  if (p.epi != EPI_DGELU) return cudaErrorInvalidValue;
-  if ((e = dispatch_q<EPI_DGELU>(p, ta, tb, to, s, num_sms)) != cudaSuccess) return e;
-  return cudaSuccess;
+                              const CUtensorMap& to, int bn, cudaStream_t s, int num_sms) {
+  if (p.epi == EPI_GELU)
+    return bn == 256 ? dispatch_q<256, EPI_GELU>(p, ta, tb, to, s, num_sms)
+                     : dispatch_q<128, EPI_GELU>(p, ta, tb, to, s, num_sms);
+  if (p.epi == EPI_DGELU)
+    return bn == 256 ? dispatch_q<256, EPI_DGELU>(p, ta, tb, to, s, num_sms)
+                     : dispatch_q<128, EPI_DGELU>(p, ta, tb, to, s, num_sms);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t read_dense_status(unsigned* out) {

@@ -66,10 +66,14 @@ struct SplitInfo {
 
 // F4: packed E2M1 operands on .kind::mxf4.  A stage's 128-byte rows then
 // hold 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
-template <int BN, bool ZR = false, bool F4 = false>
+// PK: the dense GELU / dGELU epilogues at BN = 256, which park three of
+// each warp's four 32-column chunks in tensor memory past the scale slots
+// so that the single accumulator is handed back at once; they take three
+// stages for the room their larger scale-chunk and column-sum buffers need.
+template <int BN, bool ZR = false, bool F4 = false, bool PK = false>
 struct Cfg {
   static constexpr int KC = F4 ? 2 : 1;
-  static constexpr int STAGES = BN == 256 ? 4 : (ZR ? 4 : 5);
+  static constexpr int STAGES = BN == 256 ? (PK ? 3 : 4) : (ZR ? 4 : 5);
   static constexpr int ACC = BN == 256 ? 1 : 2;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = BN * 128;
@@ -82,7 +86,9 @@ struct Cfg {
   // 512-byte multiples (TMA store swizzle atoms).  F4 runs plain epilogues
   // only, and the room goes to a fourth 256-K stage.
   static constexpr int TB_BYTES = F4 ? 2048 : 2560;
-  static constexpr int CHUNK_BYTES = F4 ? 0 : 4096;
+  // scale chunks (BN/128 rowwise, BN/128 columnwise, 512 bytes each) and the
+  // dense dGELU column-sum partials [4 lane quarters][BN] fp32
+  static constexpr int CHUNK_BYTES = F4 ? 0 : (PK ? 6144 : 4096);
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
@@ -90,7 +96,7 @@ struct Cfg {
   // (BF16, 128-byte swizzle), one 64-column half of a tile per slot
   static constexpr int Z_SLOT = 32768;
   static constexpr int Z_SLOTS = ZR ? 2 : 0;
-  static constexpr int OFF_Z = OFF_SF + STAGES * SF_BYTES;
+  static constexpr int OFF_Z = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
   static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
   static constexpr int OFF_BAR = OFF_CHUNK + CHUNK_BYTES;
@@ -102,8 +108,10 @@ struct Cfg {
   static_assert(sizeof(SplitInfo) <= 256, "split info must fit");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_TMEM_BASE = 256;
+  static constexpr uint32_t PARK_COL = 320;  // PK: 2 x 96 parked columns
   static_assert(ACC * BN <= 256, "accumulators live in tensor-memory columns 0..255");
-  static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= TMEM_COLS, "scale slots must fit");
+  static_assert(SF_TMEM_BASE + STAGES * SF_COLS <= (PK ? PARK_COL : TMEM_COLS), "scale slots must fit");
+  static_assert(!PK || (BN == 256 && PARK_COL + 192 <= TMEM_COLS), "parked chunks must fit");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(OFF_TB % 1024 == 0, "staging buffers must be swizzle-atom aligned");
   static_assert(OFF_Z % 1024 == 0, "z slots must be swizzle-atom aligned");
@@ -444,7 +452,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
   constexpr bool EXT_ON = EPI != EPI_DSWIGLU || EXT;
   static_assert(!F4 || (EPI == EPI_BF16 || EPI == EPI_F32), "mxf4 operands: plain epilogues only");
-  using C = Cfg<BN, ZR, F4>;
+  constexpr bool PK = BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU);
+  using C = Cfg<BN, ZR, F4, PK>;
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -777,7 +786,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const Tile U = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!U.active || U.nk == 0) return;
         const int64_t r = U.m0 + q * 32 + lane;
-        prefetch_l2(p.z + r * p.q_cols + U.n0 + half * 64);
+        prefetch_l2(p.z + r * p.q_cols + U.n0 + half * (BN / 2));
+        if (BN == 256) prefetch_l2(p.z + r * p.q_cols + U.n0 + half * (BN / 2) + 64);
       }
     };
     prefetch_aux(0);
@@ -1064,22 +1074,46 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (!epi_sync()) break;
       } else if constexpr (EPI == EPI_GELU || EPI == EPI_DGELU) {
-        // Dense MLP epilogues, accumulator columns [0,128) = output columns
-        // n0..n0+127.  GELU: pre = acc + b1 (saved in BF16), act = gelu(pre);
-        // dGELU: dpre = acc * gelu'(pre from the BF16 save), plus per-column
-        // sums of dpre (the bias gradient).  Both requantize rowwise and
-        // columnwise with optional rotation.
+        // Dense MLP epilogues, accumulator columns [0,BN) = output columns
+        // n0..n0+BN-1, warp (q, half) taking its lane quarter's columns
+        // half*BN/2.. in 32-column chunks.  GELU: pre = acc + b1 (saved in
+        // BF16), act = gelu(pre); dGELU: dpre = acc * gelu'(pre from the BF16
+        // save), plus per-column sums of dpre (the bias gradient).  Both
+        // requantize rowwise and columnwise with optional rotation.
         constexpr int BB = BlockBytes<QF>::value;
+        constexpr int NCH = BN / 64;  // chunks per warp
         const int64_t row = T.m0 + row_in_tile;
         const int64_t n0 = T.n0;
-        uint8_t* ch_row = sChunk;
-        uint8_t* ch_col = sChunk + 512;
-        float* part = reinterpret_cast<float*>(sChunk + 1024);  // [4 lane quarters][128 columns]
+        const int c0 = half * (BN / 2);
+        uint8_t* ch_row = sChunk;                   // BN/128 rowwise scale chunks
+        uint8_t* ch_col = sChunk + 4 * BN;          // BN/128 columnwise scale chunks
+        float* part = reinterpret_cast<float*>(sChunk + 8 * BN);  // [4 lane quarters][BN columns]
+        uint32_t accr[32];
+        // PK: chunks 1..3 of the warp go to tensor-memory columns past the
+        // scale slots and chunk 0 to registers; then the accumulator is free
+        // for the next tile's MMAs while this one is requantized.
+        const uint32_t park = tmem_base + ((uint32_t)(q * 32) << 16) + C::PARK_COL + (uint32_t)(half * 96);
+        if constexpr (PK) {
+          uint32_t t1[32], t2[32], t3[32];
+          tmem_ld32(tbase + c0 + 32, t1);
+          tmem_ld32(tbase + c0 + 64, t2);
+          tmem_ld32(tbase + c0 + 96, t3);
+          tmem_wait_ld();
+          tmem_st32(park, t1);
+          tmem_st32(park + 32, t2);
+          tmem_st32(park + 64, t3);
+          tmem_ld32(tbase + c0, accr);
+          tmem_wait_ld();
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
 #pragma unroll 1
-        for (int ch = 0; ch < 2; ch++) {
-          const int fc = half * 64 + ch * 32;
-          uint32_t accr[32];
-          tmem_ld32(tbase + fc, accr);
+        for (int ch = 0; ch < NCH; ch++) {
+          const int fc = c0 + ch * 32;
+          if (!PK) tmem_ld32(tbase + fc, accr);
+          else if (ch > 0) tmem_ld32(park + (uint32_t)(ch - 1) * 32u, accr);
           float aux[32];  // GELU: bias; dGELU: saved pre-activation
           if (EPI == EPI_GELU && p.bias == nullptr) {
 #pragma unroll
@@ -1116,24 +1150,32 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < 2; k++)  // dGELU: this warp's 32-row column sums from the transpose
             col_quant16<QF, QH>(&val[16 * k], tb, lane, p.q_col, p.q_col_ld, n0 + fc + 16 * k,
-                                (T.m0 + q * 32) / 32 * BB, ch_col, fc + 16 * k, q,
-                                EPI == EPI_DGELU ? part + q * 128 + fc + 16 * k : nullptr);
+                                (T.m0 + q * 32) / 32 * BB, ch_col + (fc >> 7) * 512, (fc & 127) + 16 * k, q,
+                                EPI == EPI_DGELU ? part + q * BN + fc + 16 * k : nullptr);
           const uint32_t sbr = row_quant_store<QF, QH>(val, p.q_row + row * p.q_row_ld + (n0 + fc) / 32 * BB);
-          ch_row[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbr;
+          ch_row[(fc >> 7) * 512 + lane * 16 + q * 4 + ((fc >> 5) & 3)] = (uint8_t)sbr;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (!PK) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
         if (!epi_sync()) break;
-        if (ew == 0) store_chunk(p.q_row_scale + ((T.m0 >> 7) * ((p.q_cols / 32 + 3) / 4) + (n0 >> 7)) * 512, ch_row, lane);
-        else if (ew == 1) store_chunk(p.q_col_scale + ((n0 >> 7) * ((p.R / 32 + 3) / 4) + (T.m0 >> 7)) * 512, ch_col, lane);
+        constexpr int NCK = BN / 128;  // scale chunks per orientation
+        if (ew < NCK)
+          store_chunk(p.q_row_scale + ((T.m0 >> 7) * ((p.q_cols / 32 + 3) / 4) + (n0 >> 7) + ew) * 512,
+                      ch_row + ew * 512, lane);
+        else if (ew < 2 * NCK)
+          store_chunk(p.q_col_scale + (((n0 >> 7) + ew - NCK) * ((p.R / 32 + 3) / 4) + (T.m0 >> 7)) * 512,
+                      ch_col + (ew - NCK) * 512, lane);
         if constexpr (EPI == EPI_DGELU) {
-          const int c = ew * 32 + lane - 64;  // warps 2..5 of the epilogue: 128 columns
-          if (c >= 0 && c < 128) {
+          // BN columns: all 8 epilogue warps at BN = 256, warps 2..5 at 128
+          const int c = BN == 256 ? ew * 32 + lane : ew * 32 + lane - 64;
+          if (c >= 0 && c < BN) {
             float s4 = part[c];
-            s4 += part[128 + c];
-            s4 += part[256 + c];
-            s4 += part[384 + c];
+            s4 += part[BN + c];
+            s4 += part[2 * BN + c];
+            s4 += part[3 * BN + c];
             p.colsum_partials[(T.m0 >> 7) * p.q_cols + n0 + c] = s4;
           }
         }

@@ -108,7 +108,7 @@ struct GemmParams {
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                         int bn, cudaStream_t s, int num_sms);
 cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                              const CUtensorMap& to, cudaStream_t s, int num_sms);
+                              const CUtensorMap& to, int bn, cudaStream_t s, int num_sms);
 cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t cols, float* out, cudaStream_t s);
 // dprobs[r] = sum over k of part[r, k] in order, for the rows of the segments
 // (r < offsets[G-1], or all R rows without offsets); other rows untouched.

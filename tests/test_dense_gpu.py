@@ -55,10 +55,11 @@ def test_gelu_fwd(cuda_lib, fmt, had):
     requant_close(mx_bytes(act_col), ref["act_col"], H, M, fmt)
 
 
+@pytest.mark.parametrize("H", [256, 384])
 @pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E4M3, False)])
-def test_dgelu_bwd(cuda_lib, fmt, had):
+def test_dgelu_bwd(cuda_lib, fmt, had, H):
     rng = np.random.default_rng(52)
-    M, D, H = 512, 384, 256
+    M, D = 512, 384
     dyb = W.normal_bf16(rng, (M, D), std=1e-3)
     w2t = W.normal_bf16(rng, (H, D), std=0.02)
     pre = W.normal_bf16(rng, (M, H), std=1.5)
@@ -74,14 +75,17 @@ def test_dgelu_bwd(cuda_lib, fmt, had):
     assert O.within_tolerance(got[None, :], ref["db1"][None, :]).all()
 
 
+@pytest.mark.parametrize("H", [256, 384, 512])
 @pytest.mark.parametrize("fmt,had", [(O.E2M3, True), (O.E4M3, False)])
-def test_gelu_and_dgelu_tap_requant_bit_exact(cuda_lib, fmt, had):
+def test_gelu_and_dgelu_tap_requant_bit_exact(cuda_lib, fmt, had, H):
     """Random inputs: the GELU activation and the dGELU pre-activation
     gradient as the epilogues computed them in fp32 (debug tap, before the
     rotation), quantized by the oracle (its fp32 rotation sequence), give the
-    epilogues' row and column bytes bit for bit."""
+    epilogues' row and column bytes bit for bit.  H = 256 and 512 run the
+    256-column tiles (one and two per row block), H = 384 the 128-column
+    ones."""
     rng = np.random.default_rng(53)
-    M, D, H = 512, 384, 256
+    M, D = 512, 384
     xb, w1b = W.normal_bf16(rng, (M, D)), W.normal_bf16(rng, (H, D), std=0.05)
     b1 = W.normal_bf16(rng, (H,), std=0.02)
     xr, _, xref = _q(cuda_lib, xb, fmt, had, col=False)
