@@ -865,7 +865,11 @@ def ncu_case(name, launches=3):
     'quant' is the standalone quantizer workload (8192 x 7168) ('quant_sr' /
     'quant_e2m1' the same to MXFP4 with stochastic / nearest rounding),
     'permute' the quantizing permute of 8192 tokens (top-8 of 128 experts,
-    D = 2048), 'mxfp4_gemm' a dense E2M1 GEMM 8192 x 12288 x 3072."""
+    D = 2048), 'mxfp4_gemm' a dense E2M1 GEMM 8192 x 12288 x 3072,
+    'dense_gelu' / 'dense_dgelu' the dense MXFP6 + rotation FC1 + GELU and
+    FC2 dgrad + dGELU stages at M = 8192, D = 3072, H = 12288 (the dGELU
+    case on a random saved pre-activation, so its GEMM launches are the only
+    ones)."""
     import torch
     import mlp_gemms_gb300 as mx
     import workloads as W
@@ -888,6 +892,23 @@ def ncu_case(name, launches=3):
         br, _, _ = mx.mx_quantize(b, mx.E2M1, True, False)
         out = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
         run = lambda: mx.mx_gemm_bias(ar, br, None, out=out)
+    elif name in ("dense_gelu", "dense_dgelu"):  # M = 8192, D = 3072, H = 12288 (~0.6 GB on the device)
+        M, D, H = 8192, 3072, 12288
+        g = torch.Generator(device=dev)
+        g.manual_seed(13)
+        a = torch.randn((M, D), generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn((H, D), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        ar, _, _ = mx.mx_quantize(a, mx.E2M3, True, False, True)
+        wr, _, _ = mx.mx_quantize(w, mx.E2M3, True, False, True)
+        pre = (torch.randn((M, H), generator=g, device=dev) * 1.5).to(torch.bfloat16)
+        qr, qc = mx.MX(M, H, mx.E2M3, True, dev), mx.MX(H, M, mx.E2M3, True, dev)
+        if name == "dense_gelu":
+            b1 = (torch.randn((H,), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+            run = lambda: mx.mx_gemm_gelu_fwd(ar, wr, b1, pre=pre, act_row=qr, act_col=qc)
+        else:
+            db1 = torch.empty((H,), dtype=torch.float32, device=dev)
+            ws = torch.empty((mx.mx_gemm_dgelu_workspace_bytes(M, H),), dtype=torch.uint8, device=dev)
+            run = lambda: mx.mx_gemm_dgelu_bwd(ar, wr, pre, dpre_row=qr, dpre_col=qc, db1=db1, workspace=ws)
     elif name == "permute":  # 8192 tokens top-8 of 128 experts, D = 2048 (~0.5 GB on the device)
         T, k, G, D = 8192, 8, 128, 2048
         g = torch.Generator(device=dev)
