@@ -142,15 +142,17 @@ mx_status_t make_tmap_packed(CUtensorMap* m, const void* base, int64_t rows, int
 
 // BF16 input [rows, cols] with row stride ld elements, box 64 columns x 128
 // rows (two boxes per 128x128 quantizer tile), 128-byte swizzle.
-mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                           int box_cols = 64) {
   mx_status_t st = get_encoder();
   if (st != MX_OK) return st;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, 128};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (input) failed (%d)", (int)r);
   return MX_OK;
@@ -329,8 +331,8 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
     st = out.f32 ? make_tmap_out_f32(&to, out.base, out.rows, out.cols, out.ld)
                  : make_tmap_out(&to, out.base, out.rows, out.cols, out.ld);
     if (st != MX_OK) return st;
-  } else if (p.epi == mx::EPI_DSWIGLU) {  // the saved z [R, 2F], streamed by the epilogue
-    if ((st = make_tmap_bf16(&to, p.z, p.R, 2 * p.F, 2 * p.F)) != MX_OK) return st;
+  } else if (p.epi == mx::EPI_DSWIGLU) {  // the saved z [R, 2F], streamed by the epilogue (64 / 32 columns a box)
+    if ((st = make_tmap_bf16(&to, p.z, p.R, 2 * p.F, 2 * p.F, bn == 256 ? 32 : 64)) != MX_OK) return st;
   } else {
     to = ta;
   }
@@ -786,8 +788,10 @@ mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_r
   p.sfa = dy_row->scale; p.sfb = w2t_row->scale;
   p.sfa_kchunks = (D / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
+  // 256-column tiles (the 128x256 MMA) where F allows, else 128
+  const int tile_n = F % 256 == 0 ? 256 : 128;
   p.m_tiles = (int)(R / 128);
-  p.n_tiles = (int)(F / 128);
+  p.n_tiles = (int)(F / tile_n);
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
   p.z = static_cast<uint16_t*>(const_cast<void*>(z_bf16));
   p.q_row = static_cast<uint8_t*>(dz_row->data); p.q_row_scale = dz_row->scale;
@@ -795,19 +799,19 @@ mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_r
   p.q_cols = 2 * F;
   if ((st = attach_tap(&p, R, 2 * F)) != MX_OK) return st;
   if (probs != nullptr) {
-    const int64_t ld = 2 * (F / 128);
+    const int64_t ld = 2 * (F / tile_n);  // one partial per tile and column half
     MX_CHECK(dprobs != nullptr, MX_ERR_INVALID_ARG, "dprobs is NULL");
     MX_CHECK(workspace != nullptr && aligned16(workspace) && workspace_bytes >= (size_t)(R * ld * 4),
              MX_ERR_WORKSPACE, "the probabilities' workspace needs %lld bytes", (long long)(R * ld * 4));
     p.probs = probs;
     p.dprobs_part = static_cast<float*>(workspace);
     p.dprobs_ld = ld;
-    if ((st = run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0})) != MX_OK) return st;
+    if ((st = run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0})) != MX_OK) return st;
     cudaError_t e = mx::launch_dprobs_reduce(p.dprobs_part, R, ld, offsets_dev, G, dprobs, s);
     if (e != cudaSuccess) return cuda_fail(e, "dprobs reduction launch");
     return MX_OK;
   }
-  return run_gemm(p, dy_row, w2t_row, 128, s, dev, OutView{nullptr, 0, 0, 0});
+  return run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0});
 }
 
 }  // namespace

@@ -11,7 +11,7 @@ template <int BN, int EPI, int MODE, bool EXT = false>
 static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, EXT>;
-  constexpr int smem = Cfg<BN, EPI == EPI_DSWIGLU>::SMEM_BYTES;
+  constexpr int smem = KCfg<BN, EPI>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -28,10 +28,13 @@ cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtens
                         int bn, cudaStream_t s, int num_sms) {
   if (p.f4) return launch_gemm_f4(p, ta, tb, to, bn, s, num_sms);
   if (p.epi == EPI_SWIGLU) return launch_one<256, EPI_SWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
-  if (p.epi == EPI_DSWIGLU) {
-    if (p.tap != nullptr || p.probs != nullptr)
-      return launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms);
-    return launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+  if (p.epi == EPI_DSWIGLU) {  // 256-column tiles where F allows (bn), else 128
+    const bool ext = p.tap != nullptr || p.probs != nullptr;
+    if (bn == 256)
+      return ext ? launch_one<256, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms)
+                 : launch_one<256, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
+    return ext ? launch_one<128, EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, to, s, num_sms)
+               : launch_one<128, EPI_DSWIGLU, MODE_GROUPED>(p, ta, tb, to, s, num_sms);
   }
   if (p.epi == EPI_F32) {
     if (p.mode != MODE_WGRAD) return cudaErrorInvalidValue;

@@ -15,7 +15,7 @@ template <int BN, int EPI, int QF, bool QH>
 static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                                     const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE_GROUPED, QF, QH>;
-  constexpr int smem = Cfg<BN, false, false, BN == 256>::SMEM_BYTES;
+  constexpr int smem = KCfg<BN, EPI>::SMEM_BYTES;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -13,7 +13,7 @@ template <int BN, int EPI, int MODE>
 static cudaError_t launch_f4_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                                  const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, false, true>;
-  constexpr int smem = Cfg<BN, false, true>::SMEM_BYTES;
+  constexpr int smem = KCfg<BN, EPI, true>::SMEM_BYTES;
   static bool configured = false;  // per instantiation; attribute set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -66,10 +66,11 @@ struct SplitInfo {
 
 // F4: packed E2M1 operands on .kind::mxf4.  A stage's 128-byte rows then
 // hold 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
-// PK: the dense GELU / dGELU epilogues at BN = 256, which park three of
-// each warp's four 32-column chunks in tensor memory past the scale slots
-// so that the single accumulator is handed back at once; they take three
-// stages for the room their larger scale-chunk and column-sum buffers need.
+// PK: the fused requant epilogues at BN = 256 (dense GELU / dGELU,
+// dSwiGLU), which park three of each warp's four 32-column chunks in tensor
+// memory past the scale slots so that the single accumulator is handed back
+// at once; they take three stages for the room their larger scale-chunk and
+// column-sum buffers (GELU / dGELU) or the z ring (dSwiGLU) need.
 template <int BN, bool ZR = false, bool F4 = false, bool PK = false>
 struct Cfg {
   static constexpr int KC = F4 ? 2 : 1;
@@ -88,14 +89,18 @@ struct Cfg {
   static constexpr int TB_BYTES = F4 ? 2048 : 2560;
   // scale chunks (BN/128 rowwise, BN/128 columnwise, 512 bytes each) and the
   // dense dGELU column-sum partials [4 lane quarters][BN] fp32
-  static constexpr int CHUNK_BYTES = F4 ? 0 : (PK ? 6144 : 4096);
+  static constexpr int CHUNK_BYTES = F4 ? 0 : ((PK && !ZR) ? 6144 : 4096);
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  // ZR: a ring of two z slots, each [128 rows][64 cols] of gate and of up
-  // (BF16, 128-byte swizzle), one 64-column half of a tile per slot
-  static constexpr int Z_SLOT = 32768;
-  static constexpr int Z_SLOTS = ZR ? 2 : 0;
+  // ZR: a ring of z slots, each [128 rows][Z_COLS cols] of gate and of up
+  // (BF16): at BN = 128 two slots of 64 columns (128-byte swizzle), read by
+  // all 8 epilogue warps; at BN = 256 three slots of 32 columns (64-byte
+  // swizzle), each read by the 4 warps of one column half
+  static constexpr int Z_COLS = BN == 256 ? 32 : 64;
+  static constexpr int Z_SLOT = 2 * 128 * Z_COLS * 2;
+  static constexpr int Z_SLOTS = ZR ? (BN == 256 ? 3 : 2) : 0;
+  static constexpr int Z_READERS = BN == 256 ? 4 : 8;
   static constexpr int OFF_Z = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
   static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
@@ -116,6 +121,14 @@ struct Cfg {
   static_assert(OFF_TB % 1024 == 0, "staging buffers must be swizzle-atom aligned");
   static_assert(OFF_Z % 1024 == 0, "z slots must be swizzle-atom aligned");
 };
+
+// The configuration a kernel instantiation uses (launchers size shared
+// memory with the same one).
+template <int BN, int EPI> constexpr bool kParks() {
+  return BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU || EPI == EPI_DSWIGLU);
+}
+template <int BN, int EPI, bool F4 = false>
+using KCfg = Cfg<BN, EPI == EPI_DSWIGLU, F4, kParks<BN, EPI>()>;
 
 struct Tile {
   int active;
@@ -452,8 +465,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
   constexpr bool EXT_ON = EPI != EPI_DSWIGLU || EXT;
   static_assert(!F4 || (EPI == EPI_BF16 || EPI == EPI_F32), "mxf4 operands: plain epilogues only");
-  constexpr bool PK = BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU);
-  using C = Cfg<BN, ZR, F4, PK>;
+  using C = KCfg<BN, EPI, F4>;
+  constexpr bool PK = kParks<BN, EPI>();
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -481,7 +494,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 8); }
     mbar_init(final_bar, 1);
     mbar_init(epi_bar, 8);
-    for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], 8); }
+    for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], C::Z_READERS); }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -681,31 +694,32 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (warp == 10) {
     // ------------------------------------------------------------ z loader (ZR)
-    // Streams the tile's saved pre-activation, one 64-column half (gate and
-    // up boxes) per slot, in the epilogue's tile order.
+    // Streams the tile's saved pre-activation, Z_COLS columns (gate and up
+    // boxes) per slot, in the epilogue's tile order.
     if (ZR && lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       int zs = 0;
       uint32_t zph = 0;
-      int armed_parity[2] = {-1, -1};
+      int armed_parity[C::Z_SLOTS > 0 ? C::Z_SLOTS : 1];
+      for (int z = 0; z < C::Z_SLOTS; z++) armed_parity[z] = -1;
       bool ok = true;
       for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
         const int64_t t = tile_index<MODE>(i);
         if (t >= p.num_tiles) continue;
         Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
-        for (int hh = 0; hh < 2; hh++) {
+        for (int hh = 0; hh < BN / C::Z_COLS; hh++) {
           if (!mbar_wait_bounded(&z_empty[zs], zph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
           mbar_arrive_expect_tx(&z_full[zs], (uint32_t)C::Z_SLOT);
           armed_parity[zs] = (int)zph;
           uint8_t* dst = sZ + zs * C::Z_SLOT;
-          tma_load_2d(dst, &tmO, (int)(T.n0 + hh * 64), (int)T.m0, &z_full[zs], pol);
-          tma_load_2d(dst + C::Z_SLOT / 2, &tmO, (int)(p.F + T.n0 + hh * 64), (int)T.m0, &z_full[zs], pol);
-          if (++zs == 2) { zs = 0; zph ^= 1u; }
+          tma_load_2d(dst, &tmO, (int)(T.n0 + hh * C::Z_COLS), (int)T.m0, &z_full[zs], pol);
+          tma_load_2d(dst + C::Z_SLOT / 2, &tmO, (int)(p.F + T.n0 + hh * C::Z_COLS), (int)T.m0, &z_full[zs], pol);
+          if (++zs == C::Z_SLOTS) { zs = 0; zph ^= 1u; }
         }
       }
       volatile int no_abort = 0;
-      for (int z = 0; z < 2; z++)
+      for (int z = 0; z < C::Z_SLOTS; z++)
         if (armed_parity[z] >= 0) mbar_wait_bounded(&z_full[z], (uint32_t)armed_parity[z], &no_abort, WAIT_BUDGET_NS);
     }
   } else {
@@ -720,6 +734,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t epi_phase = 0;
     int zslot = 0;           // ZR: next z slot and its phase
     uint32_t zphase = 0;
+    uint32_t zt = 0;         // ZR, BN = 256: z slots of the tiles done (8 per tile)
     // Barrier among the epilogue warps, bounded like every other wait.
     auto epi_sync = [&]() -> bool {
       __syncwarp();
@@ -989,37 +1004,76 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         if (!epi_sync()) break;
       } else if constexpr (EPI == EPI_DSWIGLU) {
-        // accumulator columns [0,128): dh for f0..f0+127.  The tile is taken
-        // in two 64-column halves, one z slot each; warp (q, half) handles
-        // columns hh*64 + half*32 .. +31 of half hh for its 32 rows.
+        // accumulator columns [0,BN): dh for f0..f0+BN-1.  Warp (q, half)
+        // takes 32-column chunks j = 0..NST-1 at fc = 64j + 32*half for its
+        // 32 rows.  BN = 128: chunk j is the warp's half of z slot j (two
+        // 64-column slots per tile, every warp reads every slot).  BN = 256:
+        // chunk j is z slot 2j + half of the tile (eight 32-column slots per
+        // tile, a three-slot ring), and chunks 1..3 are parked in tensor
+        // memory at the tile boundary so that the accumulator goes back at
+        // once.
+        constexpr int NST = BN / 64;
+        constexpr int NCK = BN / 128;  // scale chunks per orientation and half of z
         const int64_t row = T.m0 + row_in_tile;
         const int64_t f0 = T.n0;
         uint8_t* ch_gr = sChunk;
-        uint8_t* ch_ur = sChunk + 512;
-        uint8_t* ch_gc = sChunk + 1024;
-        uint8_t* ch_uc = sChunk + 1536;
+        uint8_t* ch_ur = sChunk + 512 * NCK;
+        uint8_t* ch_gc = sChunk + 1024 * NCK;
+        uint8_t* ch_uc = sChunk + 1536 * NCK;
         const int zrow = q * 32 + lane;
         bool zok = true;
-        float dps = 0.0f;  // routing-probability gradient: this row, this warp's 64 columns
+        float dps = 0.0f;  // routing-probability gradient: this row, this warp's columns
         const float prob = (EXT_ON && p.probs != nullptr) ? __ldg(p.probs + row) : 1.0f;
+        uint32_t dh[32];
+        const uint32_t park = tmem_base + ((uint32_t)(q * 32) << 16) + C::PARK_COL + (uint32_t)(half * 96);
+        if constexpr (PK) {
+          uint32_t t1[32], t2[32], t3[32];
+          tmem_ld32(tbase + 64 + half * 32, t1);
+          tmem_ld32(tbase + 128 + half * 32, t2);
+          tmem_ld32(tbase + 192 + half * 32, t3);
+          tmem_wait_ld();
+          tmem_st32(park, t1);
+          tmem_st32(park + 32, t2);
+          tmem_st32(park + 64, t3);
+          tmem_ld32(tbase + half * 32, dh);
+          tmem_wait_ld();
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
 #pragma unroll 1
-        for (int hh = 0; hh < 2; hh++) {
-          const int fc = hh * 64 + half * 32;  // tile-local column of this chunk
-          uint32_t dh[32];
-          tmem_ld32(tbase + fc, dh);
-          if (!mbar_wait_bounded(&z_full[zslot], zphase, abort_flag, WAIT_BUDGET_NS)) { zok = false; break; }
-          const uint8_t* grow = sZ + zslot * C::Z_SLOT + zrow * 128;
+        for (int j = 0; j < NST; j++) {
+          const int fc = 64 * j + 32 * half;  // tile-local column of this chunk
+          int zs;
+          uint32_t zph;
+          if constexpr (PK) {
+            if (j > 0) tmem_ld32(park + (uint32_t)(j - 1) * 32u, dh);
+            const uint32_t zi = zt + 2u * (uint32_t)j + (uint32_t)half;  // slot sequence number
+            zs = (int)(zi % (uint32_t)C::Z_SLOTS);
+            zph = (zi / (uint32_t)C::Z_SLOTS) & 1u;
+          } else {
+            tmem_ld32(tbase + fc, dh);
+            zs = zslot;
+            zph = zphase;
+          }
+          if (!mbar_wait_bounded(&z_full[zs], zph, abort_flag, WAIT_BUDGET_NS)) { zok = false; break; }
+          // this row's 32 gate and 32 up values of the chunk
+          const uint8_t* grow = sZ + zs * C::Z_SLOT + zrow * (2 * C::Z_COLS);
           const uint8_t* urow = grow + C::Z_SLOT / 2;
           uint4 zgw[4], zuw[4];
 #pragma unroll
           for (int i = 0; i < 4; i++) {
-            const int off = ((half * 4 + i) ^ (zrow & 7)) << 4;  // 128-byte swizzle
+            const int off = BN == 256 ? (i ^ ((zrow >> 1) & 3)) << 4           // 64-byte swizzle
+                                      : ((half * 4 + i) ^ (zrow & 7)) << 4;   // 128-byte swizzle
             zgw[i] = *reinterpret_cast<const uint4*>(grow + off);
             zuw[i] = *reinterpret_cast<const uint4*>(urow + off);
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&z_empty[zslot]);
-          if (++zslot == 2) { zslot = 0; zphase ^= 1u; }
+          if (lane == 0) mbar_arrive(&z_empty[zs]);
+          if (!PK) {
+            if (++zslot == C::Z_SLOTS) { zslot = 0; zphase ^= 1u; }
+          }
           tmem_wait_ld();
           float dg[32], du[32];
 #pragma unroll
@@ -1028,17 +1082,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t uw[4] = {zuw[i].x, zuw[i].y, zuw[i].z, zuw[i].w};
 #pragma unroll
             for (int k = 0; k < 8; k++) {
-              const int j = i * 8 + k;
+              const int jj = i * 8 + k;
               const float g = bf16_bits_to_float((k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu));
               const float u = bf16_bits_to_float((k & 1) ? (uw[k >> 1] >> 16) : (uw[k >> 1] & 0xFFFFu));
-              float d = __uint_as_float(dh[j]);
+              float d = __uint_as_float(dh[jj]);
               const float s = sigmoidf_(g);
               if (EXT_ON && p.probs != nullptr) {  // dprobs += dh * swiglu(g, u); then dh * p
                 dps = fmaf(d, g * s * u, dps);
                 d *= prob;
               }
-              dg[j] = d * u * s * (1.0f + g * (1.0f - s));
-              du[j] = d * g * s;
+              dg[jj] = d * u * s * (1.0f + g * (1.0f - s));
+              du[jj] = d * g * s;
             }
           }
           if (EXT_ON && p.tap != nullptr) {
@@ -1048,29 +1102,34 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           // columnwise first (the rowwise packer scales its input in place)
 #pragma unroll
           for (int k = 0; k < 2; k++) {
-            col_quant16<E4M3, false>(&dg[16 * k], tb, lane, p.q_col, p.R, f0 + fc + 16 * k, T.m0 + q * 32, ch_gc,
-                                     fc + 16 * k, q);
+            col_quant16<E4M3, false>(&dg[16 * k], tb, lane, p.q_col, p.R, f0 + fc + 16 * k, T.m0 + q * 32,
+                                     ch_gc + (fc >> 7) * 512, (fc & 127) + 16 * k, q);
             col_quant16<E4M3, false>(&du[16 * k], tb, lane, p.q_col, p.R, p.F + f0 + fc + 16 * k, T.m0 + q * 32,
-                                     ch_uc, fc + 16 * k, q);
+                                     ch_uc + (fc >> 7) * 512, (fc & 127) + 16 * k, q);
           }
           uint32_t sbg = row_quant_store_e4m3(dg, p.q_row + row * p.q_cols + f0 + fc);
           uint32_t sbu = row_quant_store_e4m3(du, p.q_row + row * p.q_cols + p.F + f0 + fc);
-          ch_gr[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbg;
-          ch_ur[lane * 16 + q * 4 + (fc >> 5)] = (uint8_t)sbu;
+          const int cb = (fc >> 7) * 512 + lane * 16 + q * 4 + ((fc >> 5) & 3);
+          ch_gr[cb] = (uint8_t)sbg;
+          ch_ur[cb] = (uint8_t)sbu;
         }
         if (!zok) break;
-        if (EXT_ON && p.probs != nullptr) p.dprobs_part[row * p.dprobs_ld + (f0 >> 7) * 2 + half] = dps;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        if (PK) zt += (uint32_t)(BN / C::Z_COLS);
+        if (EXT_ON && p.probs != nullptr) p.dprobs_part[row * p.dprobs_ld + (f0 / BN) * 2 + half] = dps;
+        if (!PK) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        }
         if (!epi_sync()) break;
-        {
+        if (ew < 4 * NCK) {
           const int64_t rcp = (p.q_cols / 32 + 3) / 4;   // row-scale chunks per 128-row block
           const int64_t ccp = (p.R / 32 + 3) / 4;        // column-scale chunks per 128-row block
-          if (ew == 0) store_chunk(p.q_row_scale + ((T.m0 >> 7) * rcp + (f0 >> 7)) * 512, ch_gr, lane);
-          else if (ew == 1) store_chunk(p.q_row_scale + ((T.m0 >> 7) * rcp + ((p.F + f0) >> 7)) * 512, ch_ur, lane);
-          else if (ew == 2) store_chunk(p.q_col_scale + ((f0 >> 7) * ccp + (T.m0 >> 7)) * 512, ch_gc, lane);
-          else if (ew == 3) store_chunk(p.q_col_scale + (((p.F + f0) >> 7) * ccp + (T.m0 >> 7)) * 512, ch_uc, lane);
+          const int kind = ew / NCK, jc = ew % NCK;      // dg row, du row, dg col, du col
+          const int64_t fb = (((kind & 1) ? p.F : 0) + f0) >> 7;
+          const uint8_t* src = (kind == 0 ? ch_gr : kind == 1 ? ch_ur : kind == 2 ? ch_gc : ch_uc) + jc * 512;
+          if (kind < 2) store_chunk(p.q_row_scale + ((T.m0 >> 7) * rcp + fb + jc) * 512, src, lane);
+          else store_chunk(p.q_col_scale + ((fb + jc) * ccp + (T.m0 >> 7)) * 512, src, lane);
         }
         if (!epi_sync()) break;
       } else if constexpr (EPI == EPI_GELU || EPI == EPI_DGELU) {

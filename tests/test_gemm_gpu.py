@@ -172,8 +172,10 @@ def test_wgrad_into_fp32_main_grad_store_and_accumulate(cuda_lib, K):
     assert torch.equal(acc.cpu(), exact), "accumulate is not fl32(grad + stored accumulator)"
 
 
-def _moe_small(seed=0):
-    G, D, F, R = 4, 1024, 384, 1152
+def _moe_small(seed=0, F=384):
+    """Four experts (one empty), R = 1152 routed rows.  F = 384 runs the
+    dSwiGLU kernel on 128-column tiles, F = 512 on 256-column ones."""
+    G, D, R = 4, 1024, 1152
     counts = [384, 0, 256, 384]
     inp = W.moe_inputs(G, D, F, R, seed=seed)
     return G, D, F, R, _offsets(counts), inp
@@ -298,13 +300,14 @@ def test_swiglu_fwd_tap_requant_bit_exact(cuda_lib):
     assert O.within_tolerance(tap[:A].astype(np.float64), ref["h"]).all()
 
 
-def test_dswiglu_bwd_tap_requant_bit_exact_and_gate_up_swap_fails(cuda_lib):
+@pytest.mark.parametrize("F", [384, 512])
+def test_dswiglu_bwd_tap_requant_bit_exact_and_gate_up_swap_fails(cuda_lib, F):
     """Random inputs: the epilogue's fp32 dz = [dg | du] (debug tap) quantized
     by the oracle gives dz_row and dz_col bit for bit, and matches the
     oracle's dz within tolerance.  Negative control: the oracle with gate and
     up swapped in z must not match."""
     import torch
-    G, D, F, R, offsets, inp = _moe_small(seed=4)
+    G, D, F, R, offsets, inp = _moe_small(seed=4, F=F)
     A = int(offsets[-1])
     dyr, _, dyref = _quant_both(cuda_lib, inp["dy"])
     w2t_bits = np.ascontiguousarray(np.transpose(inp["w2"], (0, 2, 1)))
@@ -340,14 +343,15 @@ def _same_active(a, b, A, cols, R, what):
     assert np.array_equal(sc, O.scales_to_matrix(bc.scale.cpu().numpy(), cols, R // 32)[:, :A // 32]), what
 
 
-def test_swiglu_with_routing_probabilities(cuda_lib):
+@pytest.mark.parametrize("F", [384, 512])
+def test_swiglu_with_routing_probabilities(cuda_lib, F):
     """The fused activation with routing probabilities, forward and backward:
     probs = 1 reproduces the plain kernels' bytes exactly; random probs give
     requant bytes bit-exact given the epilogue's own fp32 values (debug tap),
     those values within tolerance of the oracle, and dprobs within tolerance
     of the oracle's sum_f dh * swiglu(g, u), the same on a second run."""
     import torch
-    G, D, F, R, offsets, inp = _moe_small(seed=7)
+    G, D, F, R, offsets, inp = _moe_small(seed=7, F=F)
     A = int(offsets[-1])
     offs = torch.from_numpy(offsets).cuda()
     xr, _, xref = _quant_both(cuda_lib, inp["x"])
