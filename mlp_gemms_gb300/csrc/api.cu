@@ -140,8 +140,11 @@ mx_status_t make_tmap_packed(CUtensorMap* m, const void* base, int64_t rows, int
   return MX_OK;
 }
 
-// BF16 input [rows, cols] with row stride ld elements, box 64 columns x 128
-// rows (two boxes per 128x128 quantizer tile), 128-byte swizzle.
+// BF16 input [rows, cols] with row stride ld elements: boxes of 64 columns
+// x 128 rows with the 128-byte swizzle (two per 128x128 quantizer tile, or
+// the z slots of the 128-column dSwiGLU tiles), or of 32 columns with the
+// 64-byte swizzle and 64-byte L2 fetches (the 256-column dSwiGLU tiles' z
+// slots).
 mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
                            int box_cols = 64) {
   mx_status_t st = get_encoder();
@@ -153,7 +156,7 @@ mx_status_t make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        box_cols == 32 ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (input) failed (%d)", (int)r);
   return MX_OK;
 }
