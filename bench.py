@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119296768,
-    "quant_w1": 1573072064,
-    "quant_w2": 755416000,
-    "fc1_swiglu": 2262478784,
-    "fc2": 1449511360,
-    "quant_dy": 2119643328,
-    "fc2_dgrad_dswiglu": 2734874176,
-    "fc1_dgrad": 1869400064,
-    "wgrad_dw2": 1272231360,
-    "wgrad_dw1": 2299763584,
+    "quant_x": 2119491712,
+    "quant_w1": 1573200576,
+    "quant_w2": 755411008,
+    "fc1_swiglu": 2276800448,
+    "fc2": 1448628032,
+    "quant_dy": 2119846656,
+    "fc2_dgrad_dswiglu": 2681607936,
+    "fc1_dgrad": 1868923136,
+    "wgrad_dw2": 1268650112,
+    "wgrad_dw1": 2303875008,
 }
 
 
