@@ -561,10 +561,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // A panels are read by the neighbouring CTAs that take the same row
-      // block's other column tiles: normal eviction priority (evict-first
-      // measured 1-2 % slower); B slices, reused by every row block of an
-      // expert, are kept longer
-      const uint64_t pol_a = l2_policy_evict_normal();
+      // block's other column tiles: normal eviction priority for the grouped
+      // GEMMs (FC1 + SwiGLU, FC2, FC1 dgrad 1 % faster than evict-first), but
+      // evict-first where the kernel streams more data past them (dSwiGLU's
+      // z, 3 % slower with normal priority) or reads them once (wgrad); B
+      // slices, reused by every row block of an expert, are kept longer
+      const uint64_t pol_a = (EPI == EPI_DSWIGLU || MODE == MODE_WGRAD) ? l2_policy_evict_first()
+                                                                        : l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
