@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119491712,
-    "quant_w1": 1573200576,
-    "quant_w2": 755411008,
-    "fc1_swiglu": 2276800448,
-    "fc2": 1448628032,
-    "quant_dy": 2119846656,
-    "fc2_dgrad_dswiglu": 2681607936,
-    "fc1_dgrad": 1868923136,
-    "wgrad_dw2": 1268650112,
-    "wgrad_dw1": 2303875008,
+    "quant_x": 2119470464,
+    "quant_w1": 1572995392,
+    "quant_w2": 755100864,
+    "fc1_swiglu": 2121180224,
+    "fc2": 1425125696,
+    "quant_dy": 2119635136,
+    "fc2_dgrad_dswiglu": 2674763456,
+    "fc1_dgrad": 1842516416,
+    "wgrad_dw2": 1276375680,
+    "wgrad_dw1": 2412683648,
 }
 
 
