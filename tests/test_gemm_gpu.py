@@ -300,7 +300,7 @@ def test_swiglu_fwd_tap_requant_bit_exact(cuda_lib):
     assert O.within_tolerance(tap[:A].astype(np.float64), ref["h"]).all()
 
 
-@pytest.mark.parametrize("F", [384, 512])
+@pytest.mark.parametrize("F", [256, 384, 512])
 def test_dswiglu_bwd_tap_requant_bit_exact_and_gate_up_swap_fails(cuda_lib, F):
     """Random inputs: the epilogue's fp32 dz = [dg | du] (debug tap) quantized
     by the oracle gives dz_row and dz_col bit for bit, and matches the
@@ -396,9 +396,12 @@ def test_swiglu_with_routing_probabilities(cuda_lib, F):
     assert torch.equal(again[:A], dprobs[:A]), "dprobs is not deterministic"
 
 
-def test_mlp_step_against_oracle_chain(cuda_lib):
+@pytest.mark.parametrize("F", [384, 512])
+def test_mlp_step_against_oracle_chain(cuda_lib, F):
+    """The whole SwiGLU step through mx_mlp_fwd_bwd against the oracle's
+    chain (F = 512 runs dSwiGLU on 256-column tiles)."""
     import torch
-    G, D, F, R, offsets, inp = _moe_small(seed=2)
+    G, D, F, R, offsets, inp = _moe_small(seed=2, F=F)
     A = int(offsets[-1])
     t = {k: to_dev(v) for k, v in inp.items()}
     dev = "cuda"
