@@ -42,11 +42,18 @@ namespace mx {
 // One status word per translation unit that instantiates the kernel.
 static __device__ unsigned g_gemm_status = 0;
 
-constexpr int NUM_THREADS = 320;
 constexpr int EPI_THREADS = 256;
 // Threads of one CTA: the dSwiGLU epilogue adds a warp that streams the saved
 // pre-activation z into shared memory.
-template <int EPI> constexpr int kThreads() { return EPI == EPI_DSWIGLU ? NUM_THREADS + 32 : NUM_THREADS; }
+// Epilogue warps: two per tensor-memory lane quarter, three for the dense
+// GELU / dGELU epilogues at BN = 256 (the heaviest per output element; their
+// tiles' columns are dealt round-robin to the quarter's warps).
+template <int BN, int EPI> constexpr int kEpiWarps() {
+  return (BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU)) ? 12 : 8;
+}
+template <int BN, int EPI> constexpr int kThreads() {
+  return 64 + 32 * kEpiWarps<BN, EPI>() + (EPI == EPI_DSWIGLU ? 32 : 0);
+}
 constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
 constexpr int MAX_SPLIT = MAX_SPLIT_EXPERTS;  // wgrad: at most this many experts have their K range split
@@ -71,8 +78,9 @@ struct SplitInfo {
 // memory past the scale slots so that the single accumulator is handed back
 // at once; they take three stages for the room their larger scale-chunk and
 // column-sum buffers (GELU / dGELU) or the z ring (dSwiGLU) need.
-template <int BN, bool ZR = false, bool F4 = false, bool PK = false>
+template <int BN, bool ZR = false, bool F4 = false, bool PK = false, int EWARPS = 8>
 struct Cfg {
+  static constexpr int EW = EWARPS;  // epilogue warps
   static constexpr int KC = F4 ? 2 : 1;
   static constexpr int STAGES = BN == 256 ? (PK ? 3 : 4) : (ZR ? 4 : 5);
   static constexpr int ACC = BN == 256 ? 1 : 2;
@@ -103,7 +111,7 @@ struct Cfg {
   static constexpr int Z_READERS = BN == 256 ? 4 : 8;
   static constexpr int OFF_Z = (OFF_SF + STAGES * SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
-  static constexpr int OFF_CHUNK = OFF_TB + 8 * TB_BYTES;    // scale chunks + column-sum partials
+  static constexpr int OFF_CHUNK = OFF_TB + EW * TB_BYTES;   // scale chunks + column-sum partials
   static constexpr int OFF_BAR = OFF_CHUNK + CHUNK_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -128,7 +136,7 @@ template <int BN, int EPI> constexpr bool kParks() {
   return BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU || EPI == EPI_DSWIGLU);
 }
 template <int BN, int EPI, bool F4 = false>
-using KCfg = Cfg<BN, EPI == EPI_DSWIGLU, F4, kParks<BN, EPI>()>;
+using KCfg = Cfg<BN, EPI == EPI_DSWIGLU, F4, kParks<BN, EPI>(), kEpiWarps<BN, EPI>()>;
 
 struct Tile {
   int active;
@@ -459,7 +467,7 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 // extras, the debug tap and the routing probabilities (its register budget is
 // tight); the other fused epilogues test those pointers at run time.
 template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false, bool F4 = false>
-__global__ void __launch_bounds__(kThreads<EPI>(), 1)
+__global__ void __launch_bounds__(kThreads<BN, EPI>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
@@ -481,7 +489,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::ACC;
   uint64_t* final_bar = acc_empty + C::ACC;
-  uint64_t* epi_bar = final_bar + 1;  // the 8 epilogue warps' own barrier
+  uint64_t* epi_bar = final_bar + 1;  // the epilogue warps' own barrier
   uint64_t* z_full = epi_bar + 1;     // ZR: slot loaded
   uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by all 8 epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -491,9 +499,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 8); }
+    for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], C::EW); }
     mbar_init(final_bar, 1);
-    mbar_init(epi_bar, 8);
+    mbar_init(epi_bar, C::EW);
     for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], C::Z_READERS); }
     *abort_flag = 0;
     fence_barrier_init();
@@ -699,7 +707,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_commit(final_bar);
       mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
     }
-  } else if (warp == 10) {
+  } else if (ZR && warp == 2 + C::EW) {
     // ------------------------------------------------------------ z loader (ZR)
     // Streams the tile's saved pre-activation, Z_COLS columns (gate and up
     // boxes) per slot, in the epilogue's tile order.
@@ -731,7 +739,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;       // 0..7
+    const int ew = warp - 2;       // 0..EW-1
     const int q = warp & 3;        // tensor-memory lane quarter
     const int half = ew >> 2;      // column half
     float* tb = reinterpret_cast<float*>(sTB + ew * C::TB_BYTES);
@@ -808,8 +816,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const Tile U = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!U.active || U.nk == 0) return;
         const int64_t r = U.m0 + q * 32 + lane;
-        prefetch_l2(p.z + r * p.q_cols + U.n0 + half * (BN / 2));
-        if (BN == 256) prefetch_l2(p.z + r * p.q_cols + U.n0 + half * (BN / 2) + 64);
+        // the row's BN columns in 128-byte lines, dealt to the quarter's warps
+        for (int l = ew >> 2; l < BN / 64; l += C::EW / 4) prefetch_l2(p.z + r * p.q_cols + U.n0 + 64 * l);
       }
     };
     prefetch_aux(0);
@@ -1141,43 +1149,48 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!epi_sync()) break;
       } else if constexpr (EPI == EPI_GELU || EPI == EPI_DGELU) {
         // Dense MLP epilogues, accumulator columns [0,BN) = output columns
-        // n0..n0+BN-1, warp (q, half) taking its lane quarter's columns
-        // half*BN/2.. in 32-column chunks.  GELU: pre = acc + b1 (saved in
+        // n0..n0+BN-1 in 32-column chunks, chunk c of lane quarter q taken
+        // by the quarter's warp c mod (EW / 4).  GELU: pre = acc + b1 (saved in
         // BF16), act = gelu(pre); dGELU: dpre = acc * gelu'(pre from the BF16
         // save), plus per-column sums of dpre (the bias gradient).  Both
         // requantize rowwise and columnwise with optional rotation.
         constexpr int BB = BlockBytes<QF>::value;
-        constexpr int NCH = BN / 64;  // chunks per warp
+        constexpr int EPQ = C::EW / 4;                     // epilogue warps per lane quarter
+        constexpr int NCHMAX = (BN / 32 + EPQ - 1) / EPQ;  // most 32-column chunks a warp takes
+        const int wq = ew >> 2;                            // this warp's index within its quarter
+        const int nchw = (BN / 32 - wq + EPQ - 1) / EPQ;   // its chunks: wq, wq + EPQ, ... (warp-uniform)
         const int64_t row = T.m0 + row_in_tile;
         const int64_t n0 = T.n0;
-        const int c0 = half * (BN / 2);
         uint8_t* ch_row = sChunk;                   // BN/128 rowwise scale chunks
         uint8_t* ch_col = sChunk + 4 * BN;          // BN/128 columnwise scale chunks
         float* part = reinterpret_cast<float*>(sChunk + 8 * BN);  // [4 lane quarters][BN columns]
         uint32_t accr[32];
-        // PK: chunks 1..3 of the warp go to tensor-memory columns past the
-        // scale slots and chunk 0 to registers; then the accumulator is free
-        // for the next tile's MMAs while this one is requantized.
-        const uint32_t park = tmem_base + ((uint32_t)(q * 32) << 16) + C::PARK_COL + (uint32_t)(half * 96);
+        // PK: the warp's chunks after its first go to tensor-memory columns
+        // past the scale slots and the first to registers; then the
+        // accumulator is free for the next tile's MMAs while this one is
+        // requantized.
+        const uint32_t park =
+            tmem_base + ((uint32_t)(q * 32) << 16) + C::PARK_COL + (uint32_t)(wq * (NCHMAX - 1) * 32);
         if constexpr (PK) {
-          uint32_t t1[32], t2[32], t3[32];
-          tmem_ld32(tbase + c0 + 32, t1);
-          tmem_ld32(tbase + c0 + 64, t2);
-          tmem_ld32(tbase + c0 + 96, t3);
+          static_assert(!PK || C::PARK_COL + EPQ * (NCHMAX - 1) * 32 <= C::TMEM_COLS, "parked chunks must fit");
+          // one chunk at a time through accr (its registers are reused only
+          // after the store has completed)
+#pragma unroll 1
+          for (int k = 1; k < nchw; k++) {
+            tmem_ld32(tbase + 32 * (wq + EPQ * k), accr);
+            tmem_wait_ld();
+            tmem_st32(park + 32 * (k - 1), accr);
+            tmem_wait_st();
+          }
+          tmem_ld32(tbase + 32 * wq, accr);
           tmem_wait_ld();
-          tmem_st32(park, t1);
-          tmem_st32(park + 32, t2);
-          tmem_st32(park + 64, t3);
-          tmem_ld32(tbase + c0, accr);
-          tmem_wait_ld();
-          tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
         }
 #pragma unroll 1
-        for (int ch = 0; ch < NCH; ch++) {
-          const int fc = c0 + ch * 32;
+        for (int ch = 0; ch < nchw; ch++) {
+          const int fc = 32 * (wq + EPQ * ch);
           if (!PK) tmem_ld32(tbase + fc, accr);
           else if (ch > 0) tmem_ld32(park + (uint32_t)(ch - 1) * 32u, accr);
           float aux[32];  // GELU: bias; dGELU: saved pre-activation
