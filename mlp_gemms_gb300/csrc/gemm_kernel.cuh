@@ -25,12 +25,16 @@
 //               or .kind::mxf4 for packed E2M1 operands (F4: K=64 per
 //               instruction, a stage holds 256 K-elements and two scale
 //               chunks per 128-row block);
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (warp w reads lanes
-//               32*(w%4)..+31, two warps per lane quarter split the
-//               columns), then the fused math and stores.
+//   warps 2..    epilogue (8 warps, 12 for the dense GELU / dGELU ones at
+//               BN = 256): tcgen05.ld of the accumulator (warp w reads
+//               lanes 32*(w%4)..+31, the warps of a lane quarter split the
+//               columns), then the fused math and stores; dSwiGLU adds a
+//               loader warp that streams the saved z by TMA.
 // With BN = 256 there is one accumulator buffer; the epilogue copies it to
-// registers and releases it before its math, so the next tile's MMAs run
-// under the epilogue.  With BN = 128 two accumulator buffers alternate.
+// registers (plain, SwiGLU) or parks part of it in unused tensor-memory
+// columns (dSwiGLU, GELU / dGELU) and releases it before its math, so the
+// next tile's MMAs run under the epilogue.  With BN = 128 two accumulator
+// buffers alternate.
 // Every wait is bounded in time; on expiry the kernel records a device
 // status bit and unwinds without leaving copies or MMAs in flight.
 #pragma once
@@ -491,7 +495,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* final_bar = acc_empty + C::ACC;
   uint64_t* epi_bar = final_bar + 1;  // the epilogue warps' own barrier
   uint64_t* z_full = epi_bar + 1;     // ZR: slot loaded
-  uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by all 8 epilogue warps
+  uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by its Z_READERS epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -1248,7 +1252,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           store_chunk(p.q_col_scale + (((n0 >> 7) + ew - NCK) * ((p.R / 32 + 3) / 4) + (T.m0 >> 7)) * 512,
                       ch_col + (ew - NCK) * 512, lane);
         if constexpr (EPI == EPI_DGELU) {
-          // BN columns: all 8 epilogue warps at BN = 256, warps 2..5 at 128
+          // BN columns: epilogue warps 0..7 at BN = 256, 2..5 at 128
           const int c = BN == 256 ? ew * 32 + lane : ew * 32 + lane - 64;
           if (c >= 0 && c < BN) {
             float s4 = part[c];
