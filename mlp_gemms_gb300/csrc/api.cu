@@ -876,7 +876,8 @@ WgradSplit wgrad_split(int64_t N, int64_t K, int64_t R, int num_sms) {
   w.chunks = c < 64 ? 64 : (c > 4096 ? 4096 : c);
   w.extra = w.per_g * (total / w.chunks);
   w.slots = w.per_g * (2 * total / w.chunks);
-  w.cnt_bytes = align_up((size_t)mx::MAX_SPLIT_EXPERTS * (size_t)w.per_g * 4);
+  // the split parts' arrival counters, then the dynamic schedule's tile counter
+  w.cnt_bytes = align_up(((size_t)mx::MAX_SPLIT_EXPERTS * (size_t)w.per_g + 1) * 4);
   w.bytes = w.slots > 0 ? w.cnt_bytes + (size_t)w.slots * 128 * (size_t)w.bn * 4 : 0;
   return w;
 }
@@ -931,6 +932,7 @@ mx_status_t wgrad_common(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int
     p.split_chunks = (int)w.chunks;
     p.split_min = (int)w.trigger;
     p.split_cnt = static_cast<int32_t*>(workspace);
+    p.dyn_ctr = p.split_cnt + (int64_t)mx::MAX_SPLIT_EXPERTS * w.per_g;
     p.split_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.cnt_bytes);
     p.split_slots = w.slots;
     p.split_extra = w.extra;

@@ -117,9 +117,13 @@ struct Cfg {
   static constexpr int OFF_TB = OFF_Z + Z_SLOTS * Z_SLOT;   // 8 x [32][17] fp32 transpose buffers
   static constexpr int OFF_CHUNK = OFF_TB + EW * TB_BYTES;   // scale chunks + column-sum partials
   static constexpr int OFF_BAR = OFF_CHUNK + CHUNK_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS;
+  // wgrad with a workspace: tiles claimed from a global counter reach the
+  // MMA thread and the epilogue through a TQN-entry queue
+  static constexpr int TQN = 4;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS + 2 * TQN;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_ORDER = OFF_MISC + 16;              // wgrad: experts by descending size
+  static constexpr int OFF_TQ = OFF_MISC + 16;                 // TQN int32 tile indices
+  static constexpr int OFF_ORDER = OFF_TQ + 4 * TQN;           // wgrad: experts by descending size
   static constexpr int OFF_SPLIT = OFF_ORDER + 2 * MAX_SORTED_G;  // wgrad: SplitInfo
   static constexpr int SMEM_BYTES = OFF_SPLIT + 256 + 1024;  // + slack for 1024-byte alignment
   static_assert(sizeof(SplitInfo) <= 256, "split info must fit");
@@ -495,11 +499,18 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* final_bar = acc_empty + C::ACC;
   uint64_t* epi_bar = final_bar + 1;  // the epilogue warps' own barrier
   uint64_t* z_full = epi_bar + 1;     // ZR: slot loaded
-  uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by its Z_READERS epilogue warps
+  uint64_t* z_empty = z_full + C::Z_SLOTS;
+  uint64_t* tq_full = z_empty + C::Z_SLOTS;   // dynamic wgrad schedule: queue entry written
+  uint64_t* tq_empty = tq_full + C::TQN;      // ... and read by the MMA thread and every epilogue warp
+  volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + C::OFF_TQ);  // ZR: slot read by its Z_READERS epilogue warps
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // wgrad with a workspace: each CTA's producer claims the next tile (in the
+  // order of get_tile: split parts, then experts by descending size) from a
+  // counter the host zeroes, so tiles go to whichever CTA is free first
+  const bool dyn = MODE == MODE_WGRAD && p.dyn_ctr != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -507,6 +518,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     mbar_init(final_bar, 1);
     mbar_init(epi_bar, C::EW);
     for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], C::Z_READERS); }
+    for (int e = 0; e < C::TQN; e++) { mbar_init(&tq_full[e], 1); mbar_init(&tq_empty[e], 1 + C::EW); }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -586,9 +598,25 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int armed_parity[C::STAGES];
       for (int s = 0; s < C::STAGES; s++) armed_parity[s] = -1;
       bool ok = true;
-      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
-        const int64_t t = tile_index<MODE>(i);
-        if (t >= p.num_tiles) continue;
+      int qi = 0;
+      uint32_t qph = 0;
+      int32_t next = dyn ? atomicAdd(p.dyn_ctr, 1) : 0;
+      for (int64_t i = 0; ok; i++) {
+        int64_t t;
+        if (dyn) {  // claim one tile ahead, queue this one for the MMA thread and the epilogue
+          t = next;
+          const bool end = t >= p.num_tiles;
+          if (!end) next = atomicAdd(p.dyn_ctr, 1);
+          if (!mbar_wait_bounded(&tq_empty[qi], qph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          tq[qi] = end ? -1 : (int32_t)t;
+          mbar_arrive(&tq_full[qi]);
+          if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
+          if (end) break;
+        } else {
+          if (i * gridDim.x >= p.num_tiles) break;
+          t = tile_index<MODE>(i);
+          if (t >= p.num_tiles) continue;
+        }
         Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
         int64_t brow[2];
@@ -648,9 +676,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
-        const int64_t t = tile_index<MODE>(i);
-        if (t >= p.num_tiles) continue;
+      int qi = 0;
+      uint32_t qph = 0;
+      for (int64_t i = 0; ok; i++) {
+        int64_t t;
+        if (dyn) {
+          if (!mbar_wait_bounded(&tq_full[qi], qph, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          t = tq[qi];
+          mbar_arrive(&tq_empty[qi]);
+          if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
+          if (t < 0) break;
+        } else {
+          if (i * gridDim.x >= p.num_tiles) break;
+          t = tile_index<MODE>(i);
+          if (t >= p.num_tiles) continue;
+        }
         Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!T.active || T.nk == 0) continue;
         if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
@@ -825,9 +865,22 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     };
     prefetch_aux(0);
-    for (int64_t i = 0; i * gridDim.x < p.num_tiles; i++) {
-      const int64_t t = tile_index<MODE>(i);
-      if (t >= p.num_tiles) continue;
+    int tqi = 0;
+    uint32_t tqph = 0;
+    for (int64_t i = 0;; i++) {
+      int64_t t;
+      if (dyn) {
+        if (!mbar_wait_bounded(&tq_full[tqi], tqph, abort_flag, WAIT_BUDGET_NS)) break;
+        t = tq[tqi];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tq_empty[tqi]);
+        if (++tqi == C::TQN) { tqi = 0; tqph ^= 1u; }
+        if (t < 0) break;
+      } else {
+        if (i * gridDim.x >= p.num_tiles) break;
+        t = tile_index<MODE>(i);
+        if (t >= p.num_tiles) continue;
+      }
       prefetch_aux(i + 1);
       Tile T = get_tile<NT, MODE, F4>(p, t, ew == 0 && lane == 0, order, split);
       if (!T.active) continue;

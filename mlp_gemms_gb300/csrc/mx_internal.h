@@ -64,6 +64,7 @@ struct GemmParams {
   int64_t F;                // SwiGLU FFN width (FC1 out = 2F)
   int a_type, b_type;       // MMA element types (E4M3 = 0, E2M3 = 3, E2M1 = 5)
   int f4;                   // packed E2M1 operands on .kind::mxf4 (plain epilogues)
+  int32_t* dyn_ctr;         // wgrad: tile counter for the dynamic schedule (zeroed by the host), or null
   uint32_t tx_bytes;        // bytes one pipeline stage's copies complete on its barrier
   const uint8_t* sfa;
   const uint8_t* sfb;
