@@ -59,16 +59,16 @@ def stage_flops(D, F, R):
 # benchmark (four steps averaged) on the kernels as they are now.  An entry
 # goes back to None whenever its kernel changes, until it is captured again.
 MEASURED_TRAFFIC = {
-    "quant_x": 2119470464,
-    "quant_w1": 1572995392,
-    "quant_w2": 755100864,
-    "fc1_swiglu": 2121180224,
-    "fc2": 1425125696,
-    "quant_dy": 2119635136,
-    "fc2_dgrad_dswiglu": 2674763456,
-    "fc1_dgrad": 1842516416,
-    "wgrad_dw2": 1276375680,
-    "wgrad_dw1": 2412683648,
+    "quant_x": 2119435968,
+    "quant_w1": 1573157184,
+    "quant_w2": 755222528,
+    "fc1_swiglu": 2121824960,
+    "fc2": 1423439360,
+    "quant_dy": 2119638336,
+    "fc2_dgrad_dswiglu": 2719386944,
+    "fc1_dgrad": 1840506432,
+    "wgrad_dw2": 1362582208,
+    "wgrad_dw1": 2154535168,
 }
 
 
