@@ -540,6 +540,33 @@ def test_wgrad_k_split_random_is_deterministic_and_close_to_unsplit(cuda_lib):
     assert np.all(np.abs(got - p) <= 2.0 ** -7 * np.abs(p) + 2.0 ** -14 * rms)
 
 
+def test_wgrad_claimed_tiles_equal_dealt_tiles(cuda_lib):
+    """With a workspace the wgrad's CTAs claim tiles from a counter instead
+    of taking a fixed share.  With no expert large enough to be split
+    (64 experts of at most 1024 rows, several empty: over a thousand tiles,
+    several per CTA) every tile is still computed once by one CTA, so the
+    result equals the call without a workspace bit for bit, on every run."""
+    import torch
+    G, N, K = 64, 256, 512
+    rng = np.random.default_rng(160)
+    counts = [int(c) for c in rng.integers(0, 9, size=G) * 128]
+    counts[3] = counts[17] = 0
+    offsets = _offsets(counts)
+    R = int(offsets[-1])
+    _, ac, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (R, N), std=1e-3), row=False, col=True)
+    _, bc, _ = _quant_both(cuda_lib, W.normal_bf16(rng, (R, K)), row=False, col=True)
+    offs = torch.from_numpy(offsets).cuda()
+    plain = cuda_lib.mx_grouped_gemm_wgrad(ac, bc, G, offs)
+    runs = []
+    for _ in range(3):
+        out = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+        runs.append(cuda_lib.mx_grouped_gemm_wgrad_ws(ac, bc, G, offs, out=out))
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    for r in runs:
+        assert torch.equal(r, plain), "claimed tiles differ from dealt tiles"
+    assert (plain[3] == 0).all() and (plain[17] == 0).all()
+
+
 def test_wgrad_k_split_writes_nothing_outside_its_output(cuda_lib):
     """The split wgrad launches headroom tiles for the parts; tiles past the
     last expert must stay inactive: poisoned guard slices around the output
