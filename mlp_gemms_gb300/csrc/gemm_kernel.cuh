@@ -499,10 +499,10 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* final_bar = acc_empty + C::ACC;
   uint64_t* epi_bar = final_bar + 1;  // the epilogue warps' own barrier
   uint64_t* z_full = epi_bar + 1;     // ZR: slot loaded
-  uint64_t* z_empty = z_full + C::Z_SLOTS;
+  uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by its Z_READERS epilogue warps
   uint64_t* tq_full = z_empty + C::Z_SLOTS;   // dynamic wgrad schedule: queue entry written
   uint64_t* tq_empty = tq_full + C::TQN;      // ... and read by the MMA thread and every epilogue warp
-  volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + C::OFF_TQ);  // ZR: slot read by its Z_READERS epilogue warps
+  volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + C::OFF_TQ);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
