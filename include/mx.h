@@ -422,10 +422,16 @@ MX_API mx_status_t mx_grouped_gemm_wgrad_f32(const mx_tensor_t *a_col, const mx_
  * part finishes last; the sum order differs from the unsplit call's, so the
  * two agree to fp32 rounding, not bit for bit.  At most 16 experts are
  * split; with offsets NULL, G == 1, G > 1024 or a NULL workspace nothing is.
+ * In the same cases the CTAs also claim output tiles (split parts first,
+ * then experts by descending token count) from a counter in the workspace
+ * instead of taking a fixed share; each tile is still computed by one CTA,
+ * so with nothing split the result equals mx_grouped_gemm_wgrad's bit for
+ * bit.
  * mx_grouped_gemm_wgrad_workspace_bytes(N, K, R, G) -- bytes for [N, K]
  * gradients over R routed rows (0: no split possible); N = a_col rows,
- * K = b_col rows.  The workspace holds counters the call clears (one
- * memset per call) and leaves zero.
+ * K = b_col rows.  The workspace starts with counters the call clears
+ * itself (one memset per call, before its launch); its contents need no
+ * preparation by the caller.
  * Errors as mx_grouped_gemm_wgrad / _f32, plus MX_ERR_WORKSPACE when a
  * non-NULL workspace is smaller than the query's bytes.
  */
