@@ -932,12 +932,17 @@ def ncu_case(name, launches=3):
         y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
         dw1 = torch.empty((G, 2 * F, D), dtype=torch.bfloat16, device=dev)
         dw2 = torch.empty((G, D, F), dtype=torch.bfloat16, device=dev)
+        ws1 = torch.zeros((max(mx.mx_grouped_gemm_wgrad_workspace_bytes(2 * F, D, R, G), 16),), dtype=torch.uint8,
+                          device=dev)
+        ws2 = torch.zeros((max(mx.mx_grouped_gemm_wgrad_workspace_bytes(D, F, R, G), 16),), dtype=torch.uint8,
+                          device=dev)
         run = {"fc1_swiglu": lambda: mx.mx_grouped_gemm_swiglu_fwd(xr, w1r, G, offs, hr, hc, z),
                "fc2": lambda: mx.mx_grouped_gemm(hr, w2r, G, offs, out=y),
                "fc2_dgrad_dswiglu": lambda: mx.mx_grouped_gemm_dswiglu_bwd(dyr, w2t, z, G, offs, dzr, dzc),
                "fc1_dgrad": lambda: mx.mx_grouped_gemm(dzr, w1t, G, offs, out=y),
-               "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad(dyc, hc, G, offs, out=dw2),
-               "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad(dzc, xc, G, offs, out=dw1)}[name]
+               # the wgrads as the step runs them: with a workspace (claimed tiles, K-split)
+               "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad_ws(dyc, hc, G, offs, out=dw2, workspace=ws2),
+               "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad_ws(dzc, xc, G, offs, out=dw1, workspace=ws1)}[name]
     torch.cuda.synchronize(dev)
     for _ in range(1 + launches):
         run()
