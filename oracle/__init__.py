@@ -593,11 +593,21 @@ def mlp_fwd_bwd_swiglu(x_bits, w1_bits, w2_bits, dy_bits, offsets, fmt=E4M3):
 
 def mlp_fwd_bwd_swiglu_unquantized(x_bits, w1_bits, w2_bits, dy_bits, offsets):
     """The same step in float64 with no quantization at all (the reference
-    the quantized chain's SQNR is measured against)."""
-    x = bf16_to_f64(x_bits)
-    dy = bf16_to_f64(dy_bits)
-    w1 = bf16_to_f64(w1_bits)
-    w2 = bf16_to_f64(w2_bits)
+    the quantized chain's SQNR is measured against), on BF16 inputs."""
+    return mlp_fwd_bwd_swiglu_f64(bf16_to_f64(x_bits), bf16_to_f64(w1_bits), bf16_to_f64(w2_bits),
+                                  bf16_to_f64(dy_bits), offsets)
+
+
+def mlp_fwd_bwd_swiglu_f64(x, w1, w2, dy, offsets):
+    """The unquantized SwiGLU expert-MLP step on float64 arrays: x [R, D],
+    w1 [G, 2F, D], w2 [G, D, F], dy [R, D].  Rows past offsets[-1] take no
+    part.  Forward z = x W1[g]^T, h = swiglu(z), y = h W2[g]^T; backward
+    of the loss sum(y * dy): dh = dy W2[g], dz = dswiglu(dh, z),
+    dx = dz W1[g], dW2[g] = dy_seg^T h_seg, dW1[g] = dz_seg^T x_seg."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    w1 = np.asarray(w1, dtype=np.float64)
+    w2 = np.asarray(w2, dtype=np.float64)
     A = _active_rows(offsets)
     F = w1.shape[1] // 2
     z = grouped_gemm(x, w1, offsets)[:A]
@@ -682,9 +692,21 @@ def mlp_fwd_bwd_gelu(x_bits, w1_bits, w2_bits, b1_bits, b2_bits, dy_bits, fmt=E2
 
 
 def mlp_fwd_bwd_gelu_unquantized(x_bits, w1_bits, w2_bits, b1_bits, b2_bits, dy_bits):
-    x, dy = bf16_to_f64(x_bits), bf16_to_f64(dy_bits)
-    w1, w2 = bf16_to_f64(w1_bits), bf16_to_f64(w2_bits)
-    b1, b2 = bf16_to_f64(b1_bits), bf16_to_f64(b2_bits)
+    """The dense GELU MLP step in float64 with no quantization and no
+    rotation, on BF16 inputs."""
+    return mlp_fwd_bwd_gelu_f64(bf16_to_f64(x_bits), bf16_to_f64(w1_bits), bf16_to_f64(w2_bits),
+                                bf16_to_f64(b1_bits), bf16_to_f64(b2_bits), bf16_to_f64(dy_bits))
+
+
+def mlp_fwd_bwd_gelu_f64(x, w1, w2, b1, b2, dy):
+    """The unquantized dense GELU MLP step on float64 arrays: x [M, D],
+    w1 [H, D], w2 [D, H], b1 [H], b2 [D], dy [M, D].  Forward
+    pre = x W1^T + b1, act = gelu_tanh(pre), y = act W2^T + b2; backward of
+    the loss sum(y * dy): dpre = (dy W2) * gelu'(pre), dx = dpre W1,
+    dW2 = dy^T act, dW1 = dpre^T x, db1 / db2 = column sums of dpre / dy."""
+    x, dy = np.asarray(x, dtype=np.float64), np.asarray(dy, dtype=np.float64)
+    w1, w2 = np.asarray(w1, dtype=np.float64), np.asarray(w2, dtype=np.float64)
+    b1, b2 = np.asarray(b1, dtype=np.float64), np.asarray(b2, dtype=np.float64)
     pre = x @ w1.T + b1[None, :]
     act = gelu_tanh(pre)
     y = act @ w2.T + b2[None, :]
