@@ -137,7 +137,10 @@ MX_API size_t mx_quantize_workspace_bytes(int64_t rows, int64_t cols, uint32_t f
  * to nearest-even and saturated; amax == 0 -> 0x00, amax == Inf -> 0xFE,
  * NaN in the block -> 0xFF with every element code NaN (E4M3 0x7F) or +0.
  * Shapes: cols % 32 == 0; MX_COLWISE also rows % 32 == 0; batch > 1 needs
- * rows % 128 == 0 and cols % 128 == 0.  rows == 0: MX_OK, nothing launched.
+ * rows % 128 == 0 and cols % 128 == 0.  rows == 0: MX_OK; nothing is
+ * quantized, and with MX_COLSUM colsum is set to zero (the sum over no
+ * rows; the workspace may then be NULL).  Sizes past rows * batch < 2^31
+ * or rows * batch * ld < 2^40 elements: MX_ERR_SHAPE.
  */
 MX_API mx_status_t mx_quantize(const void *x_bf16, int64_t batch, int64_t rows, int64_t cols, int64_t ld,
                         int32_t fmt, uint32_t flags, const mx_tensor_t *out_row, const mx_tensor_t *out_col,
@@ -507,6 +510,42 @@ typedef struct {
 } mx_mlp_args_t;
 
 MX_API size_t mx_mlp_workspace_bytes(const mx_mlp_args_t *args);
+
+/*
+ * mx_mlp_workspace_layout -- where mx_mlp_fwd_bwd keeps its intermediates
+ * inside the caller's workspace, so a caller (a test, a debugger) can read
+ * the quantized operands each stage consumed after the step has run.  Not
+ * part of the method: the pages' fused MLP keeps these between its stages
+ * too, but says nothing of where.
+ *   args  as for mx_mlp_workspace_bytes (pointers are not read)
+ *   out   receives, for each quantized tensor, the byte offsets of its
+ *         payload and of its blocked scales from the workspace start and
+ *         its logical [rows, cols] (columnwise tensors are stored as the
+ *         rowwise quantization of the transpose, so rows = the source's
+ *         columns):
+ *           x_row [R, D], x_col [D, R], w1_row [G*F1, D], w1t_row [G*D, F1],
+ *           w2_row [G*D, F], w2t_row [G*F, D], h_row [R, F], h_col [F, R],
+ *           dy_row [R, D], dy_col [D, R], dz_row [R, F1], dz_col [F1, R],
+ *         F1 = 2F for SwiGLU (FC1's gate and up halves), F for GELU (where
+ *         h is the activation and dz the pre-activation gradient);
+ *         z: the BF16 [R, F1] pre-activation (SwiGLU z, GELU pre);
+ *         total: mx_mlp_workspace_bytes(args).
+ * Returns MX_ERR_INVALID_ARG for a NULL pointer or a malformed shape (the
+ * cases where mx_mlp_workspace_bytes returns 0).
+ */
+typedef struct {
+  size_t data, scale;
+  int64_t rows, cols;
+} mx_mlp_slot_t;
+
+typedef struct {
+  mx_mlp_slot_t x_row, x_col, w1_row, w1t_row, w2_row, w2t_row;
+  mx_mlp_slot_t h_row, h_col, dy_row, dy_col, dz_row, dz_col;
+  size_t z;
+  size_t total;
+} mx_mlp_layout_t;
+
+MX_API mx_status_t mx_mlp_workspace_layout(const mx_mlp_args_t *args, mx_mlp_layout_t *out);
 
 /*
  * mx_mlp_fwd_bwd -- one training step of the MX MLP on one stream:

@@ -38,6 +38,7 @@ ABI_SYMBOLS = (
     "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr", "mx_moe_route_rows", "mx_moe_route_workspace_bytes",
     "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute", "mx_grouped_gemm_bias",
     "mx_grouped_gemm_wgrad_workspace_bytes", "mx_grouped_gemm_wgrad_ws", "mx_grouped_gemm_wgrad_f32_ws",
+    "mx_mlp_workspace_layout",
 )
 
 
@@ -61,6 +62,19 @@ class MlpArgsStruct(ctypes.Structure):
                 ("b2", ctypes.c_void_p), ("y", ctypes.c_void_p), ("dx", ctypes.c_void_p),
                 ("dw1", ctypes.c_void_p), ("dw2", ctypes.c_void_p), ("db1", ctypes.c_void_p),
                 ("db2", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class MlpSlotStruct(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_size_t), ("scale", ctypes.c_size_t), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64)]
+
+
+MLP_SLOTS = ("x_row", "x_col", "w1_row", "w1t_row", "w2_row", "w2t_row", "h_row", "h_col", "dy_row", "dy_col",
+             "dz_row", "dz_col")
+
+
+class MlpLayoutStruct(ctypes.Structure):
+    _fields_ = [(n, MlpSlotStruct) for n in MLP_SLOTS] + [("z", ctypes.c_size_t), ("total", ctypes.c_size_t)]
 
 
 class HostIOStruct(ctypes.Structure):
@@ -99,6 +113,7 @@ def load(path=None):
         "mx_dswiglu_probs_workspace_bytes": (sz, [i64, i64]),
         "mx_grouped_gemm_dswiglu_probs_bwd": (ctypes.c_int, [tp, tp, vp, vp, i32, vp, tp, tp, vp, vp, sz, vp]),
         "mx_mlp_workspace_bytes": (sz, [ctypes.POINTER(MlpArgsStruct)]),
+        "mx_mlp_workspace_layout": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), ctypes.POINTER(MlpLayoutStruct)]),
         "mx_mlp_fwd_bwd": (ctypes.c_int, [ctypes.POINTER(MlpArgsStruct), vp]),
         "mx_get_device_status": (ctypes.c_int, [vp]),
         "mx_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint64, vp]),
@@ -508,6 +523,36 @@ def mlp_args(x, w1, w2, dy, offsets, G, F, y, dx, dw1, dw2, workspace=None, act=
 
 def mx_mlp_workspace_bytes(args):
     return int(load().mx_mlp_workspace_bytes(ctypes.byref(args)))
+
+
+def mx_mlp_workspace_layout(args):
+    """{slot: (payload offset, scale offset, rows, cols)} for every quantized
+    tensor of the step, plus "z" (offset of the BF16 pre-activation) and
+    "total" (workspace bytes)."""
+    out = MlpLayoutStruct()
+    _check(load().mx_mlp_workspace_layout(ctypes.byref(args), ctypes.byref(out)))
+    lay = {n: (int(getattr(out, n).data), int(getattr(out, n).scale), int(getattr(out, n).rows),
+               int(getattr(out, n).cols)) for n in MLP_SLOTS}
+    lay["z"] = int(out.z)
+    lay["total"] = int(out.total)
+    return lay
+
+
+def mlp_workspace_views(args, workspace):
+    """The step's intermediates as views into its workspace (uint8 torch
+    tensor): {slot: MX} and "z" (BF16 [R, F1])."""
+    import torch
+    lay = mx_mlp_workspace_layout(args)
+    views = {}
+    for n in MLP_SLOTS:
+        d, sc, rows, cols = lay[n]
+        rb = payload_bytes(1, cols, args.fmt)
+        data = workspace[d:d + rows * rb].view(rows, rb)
+        scale = workspace[sc:sc + scale_bytes(rows, cols)]
+        views[n] = MX(rows, cols, args.fmt, bool(args.hadamard), workspace.device, data=data, scale=scale)
+    f1 = lay["dz_row"][3]
+    views["z"] = workspace[lay["z"]:lay["z"] + args.R * f1 * 2].view(torch.bfloat16).view(args.R, f1)
+    return views
 
 
 def mx_mlp_fwd_bwd(args, stream=None):

@@ -411,7 +411,10 @@ mx_status_t quantize_impl(const void* x_bf16, int64_t batch, int64_t rows, int64
            (long long)ld);
   MX_CHECK(rows == 0 || x_bf16 != nullptr, MX_ERR_INVALID_ARG, "x is NULL");
   MX_CHECK(aligned16(x_bf16), MX_ERR_ALIGNMENT, "x must be 16-byte aligned");
-  MX_CHECK(rows * ld * batch < (1ll << 40) && rows * batch < (1ll << 31), MX_ERR_SHAPE, "input too large");
+  // bound each factor before multiplying, so no product below can overflow
+  MX_CHECK(rows < (1ll << 31) && batch < (1ll << 31) && ld < (1ll << 40), MX_ERR_SHAPE, "input too large");
+  MX_CHECK(rows * batch < (1ll << 31) && (rows == 0 || ld <= ((1ll << 40) - 1) / (rows * batch)), MX_ERR_SHAPE,
+           "input too large");
   const int had = (flags & MX_HADAMARD) ? 1 : 0;
   mx_status_t st;
   if (flags & MX_ROWWISE) {
@@ -424,12 +427,18 @@ mx_status_t quantize_impl(const void* x_bf16, int64_t batch, int64_t rows, int64
     MX_CHECK(flags & MX_COLWISE, MX_ERR_INVALID_ARG, "MX_COLSUM needs MX_COLWISE");
     MX_CHECK(batch == 1, MX_ERR_INVALID_ARG, "MX_COLSUM needs batch == 1");
     MX_CHECK(colsum != nullptr && aligned16(colsum), MX_ERR_INVALID_ARG, "colsum must be a 16-byte aligned pointer");
-    MX_CHECK(workspace != nullptr && aligned16(workspace) &&
-                 workspace_bytes >= mx_quantize_workspace_bytes(rows, cols, flags),
-             MX_ERR_WORKSPACE, "MX_COLSUM needs %zu bytes of 16-byte aligned workspace",
-             mx_quantize_workspace_bytes(rows, cols, flags));
+    const size_t need = mx_quantize_workspace_bytes(rows, cols, flags);
+    MX_CHECK(need == 0 || (workspace != nullptr && aligned16(workspace) && workspace_bytes >= need),
+             MX_ERR_WORKSPACE, "MX_COLSUM needs %zu bytes of 16-byte aligned workspace", need);
   }
-  if (rows == 0) return MX_OK;
+  if (rows == 0) {
+    // no rows: nothing to quantize; each column's sum over zero rows is 0
+    if (flags & MX_COLSUM) {
+      cudaError_t e = cudaMemsetAsync(colsum, 0, (size_t)cols * sizeof(float), reinterpret_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "clearing colsum");
+    }
+    return MX_OK;
+  }
   DevInfo dev;
   if ((st = device_info(&dev)) != MX_OK) return st;
   mx::QuantLaunch q;
@@ -606,11 +615,12 @@ mx_status_t mx_quantize_colsum_noalloc(const void* x_bf16, int64_t rows, int64_t
   MX_CHECK((flags & MX_COLSUM) && (flags & MX_COLWISE), MX_ERR_INVALID_ARG,
            "mx_quantize_colsum_noalloc computes column sums: flags need MX_COLSUM and MX_COLWISE");
   MX_CHECK(rows >= 0 && cols > 0, MX_ERR_SHAPE, "shape [%lld, %lld]", (long long)rows, (long long)cols);
-  const size_t need = (size_t)((rows + 127) / 128) * (size_t)cols;
-  MX_CHECK(need <= mx::kNoAllocColsumFloats, MX_ERR_WORKSPACE,
-           "ceil(rows/128) * cols = %zu exceeds the fixed column-sum scratch of %zu values; "
-           "use mx_quantize with a workspace", need, mx::kNoAllocColsumFloats);
-  if (rows == 0) return mx_quantize(x_bf16, 1, rows, cols, ld, fmt, flags, out_row, out_col, colsum, nullptr, 0, stream);
+  // rows and cols bounded first, so the product cannot wrap past the limit
+  const bool fits = rows <= 128 * (int64_t)mx::kNoAllocColsumFloats && cols <= (int64_t)mx::kNoAllocColsumFloats &&
+                    (size_t)((rows + 127) / 128) * (size_t)cols <= mx::kNoAllocColsumFloats;
+  MX_CHECK(fits, MX_ERR_WORKSPACE,
+           "ceil(rows/128) * cols for [%lld, %lld] exceeds the fixed column-sum scratch of %zu values; "
+           "use mx_quantize with a workspace", (long long)rows, (long long)cols, mx::kNoAllocColsumFloats);
   float* scratch = nullptr;
   size_t cap = 0;
   cudaError_t e = mx::colsum_scratch(&scratch, &cap);
@@ -1309,6 +1319,26 @@ size_t mx_mlp_workspace_bytes(const mx_mlp_args_t* args) {
   if (!args || args->R < 0 || args->D <= 0 || args->F <= 0 || args->G <= 0) return 0;
   if (args->fmt < MX_E4M3 || args->fmt > MX_E2M1) return 0;
   return mlp_layout(args).total;
+}
+
+mx_status_t mx_mlp_workspace_layout(const mx_mlp_args_t* args, mx_mlp_layout_t* out) {
+  MX_CHECK(out != nullptr, MX_ERR_INVALID_ARG, "out is NULL");
+  MX_CHECK(mx_mlp_workspace_bytes(args) > 0, MX_ERR_INVALID_ARG, "args is NULL or describes no valid step");
+  const MlpLayout L = mlp_layout(args);
+  auto put = [](const MlpLayout::Slot& s) {
+    mx_mlp_slot_t o;
+    o.data = s.data; o.scale = s.scale; o.rows = s.rows; o.cols = s.cols;
+    return o;
+  };
+  out->x_row = put(L.x_row); out->x_col = put(L.x_col);
+  out->w1_row = put(L.w1_row); out->w1t_row = put(L.w1t_row);
+  out->w2_row = put(L.w2_row); out->w2t_row = put(L.w2t_row);
+  out->h_row = put(L.h_row); out->h_col = put(L.h_col);
+  out->dy_row = put(L.dy_row); out->dy_col = put(L.dy_col);
+  out->dz_row = put(L.dz_row); out->dz_col = put(L.dz_col);
+  out->z = L.z;
+  out->total = L.total;
+  return MX_OK;
 }
 
 }  // extern "C"

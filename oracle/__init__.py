@@ -254,9 +254,10 @@ def dequantize_rows(payload, scales, rows, cols, fmt):
     return out
 
 
-def blocked_index(rows, scale_cols):
-    """int64 [rows, scale_cols] array of blocked-layout byte offsets."""
-    r = np.arange(rows, dtype=np.int64)[:, None]
+def blocked_index(rows, scale_cols, row_ids=None):
+    """int64 [rows, scale_cols] array of blocked-layout byte offsets (or
+    [len(row_ids), scale_cols] for the given rows only)."""
+    r = (np.arange(rows, dtype=np.int64) if row_ids is None else np.asarray(row_ids, dtype=np.int64))[:, None]
     c = np.arange(scale_cols, dtype=np.int64)[None, :]
     cpad = (scale_cols + 3) // 4 * 4
     # same closed form as orc_blocked_offset, vectorised; tests check they agree

@@ -88,3 +88,52 @@ def with_tap(mx, rows, cols, fn):
     finally:
         mx.mx_debug_tap(None)
     return out, tap.cpu().numpy()
+
+
+def decode_lut(fmt):
+    """float64 value of every unpacked element code of fmt (NaN codes give NaN)."""
+    n = {O.E4M3: 256, O.E2M3: 64, O.E2M1: 16}[fmt]
+    return np.array([O.decode(c, fmt) for c in range(n)])
+
+
+def mx_row_scales(m, rows):
+    """Scale bytes [len(rows), cols/32] of the given rows of an MX tensor
+    (read from its blocked layout)."""
+    import torch
+    off = O.blocked_index(m.rows, m.cols // 32, rows)
+    return m.scale[torch.from_numpy(off.reshape(-1)).to(m.scale.device)].cpu().numpy().reshape(off.shape)
+
+
+def mx_rows_f64(m, rows, lut):
+    """Dequantized rows of an E4M3 MX tensor (one payload byte per element)."""
+    import torch
+    idx = torch.from_numpy(np.asarray(rows, dtype=np.int64)).to(m.data.device)
+    codes = m.data[idx].cpu().numpy()
+    s = mx_row_scales(m, rows).astype(np.float64)
+    return lut[codes] * np.repeat(2.0 ** (s - 127.0), 32, axis=1)
+
+
+def assert_tap_requant_exact_sampled(gpu_row, gpu_col, tap, rows, fmt=O.E4M3, had=False, what="tap"):
+    """Sampled form of assert_tap_requant_exact for full-size outputs: the
+    rowwise payload and scale bytes of `rows`, and the columnwise payload and
+    scale bytes of every 32-row block holding one of them, equal the
+    oracle's quantization of the epilogue's own fp32 values (the tap,
+    a torch tensor [R, C] on the GPU)."""
+    import torch
+    rows = np.asarray(sorted(rows), dtype=np.int64)
+    R, C = tap.shape
+    idx = torch.from_numpy(rows).to(tap.device)
+    t = tap[idx].cpu().numpy().astype(np.float64)
+    rp, rs = O.quantize_rows(t, fmt, had)
+    assert np.array_equal(gpu_row.data[idx].cpu().numpy(), rp), "%s rowwise payload differs" % what
+    assert np.array_equal(mx_row_scales(gpu_row, rows), O.scales_to_matrix(rs, len(rows), C // 32)), \
+        "%s rowwise scales differ" % what
+    pb = O.payload_row_bytes(32, fmt)
+    col_scales = mx_row_scales(gpu_col, np.arange(C))                    # [C, R/32]
+    for b in np.unique(rows // 32):
+        blk = tap[32 * b:32 * b + 32].cpu().numpy().astype(np.float64)  # [32, C]
+        cp, cs = O.quantize_rows(np.ascontiguousarray(blk.T), fmt, had)  # [C, one block]
+        got = gpu_col.data[:, b * pb:(b + 1) * pb].cpu().numpy()
+        assert np.array_equal(got, cp), "%s columnwise payload of rows %d..%d differs" % (what, 32 * b, 32 * b + 31)
+        assert np.array_equal(col_scales[:, b], O.scales_to_matrix(cs, C, 1)[:, 0]), \
+            "%s columnwise scales of rows %d..%d differ" % (what, 32 * b, 32 * b + 31)

@@ -76,6 +76,10 @@ def _quant(mx, **kw):
     (dict(batch=2, rows=96, out_row=None, out_col=None, flags=1), "MX_ERR_SHAPE", "batched"),
     (dict(out_row=None), "MX_ERR_INVALID_ARG", "out_row"),
     (dict(out_col=None), "MX_ERR_INVALID_ARG", "out_col"),
+    # sizes whose element products would overflow 64 bits if multiplied unchecked
+    (dict(rows=1 << 62, ld=1 << 40, flags=1), "MX_ERR_SHAPE", "too large"),
+    (dict(rows=1 << 30, ld=1 << 39, batch=1 << 30, flags=1), "MX_ERR_SHAPE", "too large"),
+    (dict(rows=1 << 20, ld=1 << 21, flags=1), "MX_ERR_SHAPE", "too large"),
 ], ids=lambda v: str(v))
 def test_quantize_rejections(mx, kw, status, word):
     if kw.get("out_row", 1) is None and "flags" in kw:
@@ -163,3 +167,45 @@ def test_mlp_rejections_and_workspace_size(mx):
     a.act = 1
     st = mx.load().mx_mlp_fwd_bwd(ctypes.byref(a), None)
     assert mx.STATUS[st] == "MX_ERR_NOT_SUPPORTED"
+
+
+@pytest.mark.parametrize("act,fmt,G,R,D,F", [(0, 0, 128, 262144, 2048, 768), (0, 0, 2, 512, 256, 128),
+                                             (1, 1, 1, 16384, 3072, 12288)])
+def test_mlp_workspace_layout(mx, act, fmt, G, R, D, F):
+    """The step's workspace layout: every slot sized for its tensor's payload
+    and blocked scales, all slots and the BF16 pre-activation disjoint and
+    16-byte aligned, inside mx_mlp_workspace_bytes."""
+    a = mx.MlpArgsStruct()
+    a.act, a.fmt, a.G, a.R, a.D, a.F = act, fmt, G, R, D, F
+    lay = mx.mx_mlp_workspace_layout(a)
+    assert lay["total"] == mx.mx_mlp_workspace_bytes(a)
+    F1 = 2 * F if act == 0 else F
+    shapes = {"x_row": (R, D), "x_col": (D, R), "w1_row": (G * F1, D), "w1t_row": (G * D, F1),
+              "w2_row": (G * D, F), "w2t_row": (G * F, D), "h_row": (R, F), "h_col": (F, R), "dy_row": (R, D),
+              "dy_col": (D, R), "dz_row": (R, F1), "dz_col": (F1, R)}
+    spans = []
+    for n, (rows, cols) in shapes.items():
+        d, sc, r, c = lay[n]
+        assert (r, c) == (rows, cols), n
+        spans.append((d, d + rows * mx.payload_bytes(1, cols, fmt), n))
+        spans.append((sc, sc + mx.scale_bytes(rows, cols), n + " scales"))
+    spans.append((lay["z"], lay["z"] + R * F1 * 2, "z"))
+    spans.sort()
+    for (s0, e0, n0), (s1, e1, n1) in zip(spans, spans[1:]):
+        assert e0 <= s1, (n0, n1)
+    assert all(s % 16 == 0 for s, _, _ in spans) and spans[-1][1] <= lay["total"]
+    bad = mx.MlpArgsStruct()
+    with pytest.raises(mx.MXError) as e:
+        mx.mx_mlp_workspace_layout(bad)
+    assert e.value.name == "MX_ERR_INVALID_ARG"
+
+
+def test_noalloc_rejects_overflowing_sizes_before_any_device_call(mx):
+    """ceil(rows/128) * cols must not wrap past the scratch limit: huge rows
+    or cols are refused on their own."""
+    L = mx.load()
+    for rows, cols in ((1 << 62, 32), (128, 1 << 62), ((1 << 63) - 1, 1 << 40)):
+        st = L.mx_quantize_colsum_noalloc(FAKE, rows, cols, cols, 0, 2 | 8, None, ctypes.byref(_t(cols, rows)),
+                                          FAKE, None)
+        assert mx.STATUS[st] == "MX_ERR_WORKSPACE", (rows, cols)
+        assert "scratch" in mx.mx_last_error()

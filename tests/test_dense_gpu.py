@@ -139,7 +139,8 @@ def test_dense_gelu_step_against_oracle_chain(cuda_lib):
         g = bf16_cpu(out[k])
         s_orc, s_unq = O.sqnr_db(ref[k + "_f64"], g), O.sqnr_db(unq[k], g)
         assert s_orc > 30.0, (k, s_orc)
-        assert s_unq > 16.0, (k, s_unq)
+        # the Primus PR #1064 page's MXFP6 band (about 28 dB) minus 6 dB
+        assert s_unq > 28.0 - 6.0, (k, s_unq)
     for k in ("db1", "db2"):
         g = out[k].cpu().numpy().astype(np.float64)
         assert O.sqnr_db(ref[k], g) > 30.0, k
