@@ -12,11 +12,9 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
                               const CUtensorMap& to, cudaStream_t s, int num_sms) {
   auto kern = mx_gemm_kernel<BN, EPI, MODE, E4M3, false, EXT>;
   constexpr int smem = KCfg<BN, EPI>::SMEM_BYTES;
-  static bool configured = false;  // per instantiation; attribute set once per process
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  {
+    const cudaError_t e = ensure_smem_attr<mx_gemm_kernel<BN, EPI, MODE, E4M3, false, EXT>>(smem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;

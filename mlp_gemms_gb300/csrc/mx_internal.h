@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/mx.h"
+#include "attr_guard.h"
 
 namespace mx {
 

@@ -546,11 +546,9 @@ template <int FMT, bool HAD, bool ROW, bool COL, bool COLSUM, bool SR = false, b
 static cudaError_t launch_q(const QuantLaunch& q, const QuantParams& p, cudaStream_t s) {
   auto kern = quantize_kernel<FMT, HAD, ROW, COL, COLSUM, SR, GATHER>;
   constexpr int smem = QCfg<FMT>::SMEM;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  {
+    const cudaError_t e = ensure_smem_attr<quantize_kernel<FMT, HAD, ROW, COL, COLSUM, SR, GATHER>>(smem);
     if (e != cudaSuccess) return e;
-    configured = true;
   }
   const int64_t tiles = (int64_t)p.tiles_x * ((p.rows + QT - 1) / QT) * p.batch;
   const int64_t cap = 2ll * q.num_sms;

@@ -36,6 +36,16 @@ def test_noalloc_matches_workspace_variant_on_two_calls(cuda_lib, rows, cols, fm
     assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 2.0 ** -14 * np.sqrt(np.mean(want ** 2)))
 
 
+def test_noalloc_zero_rows_gives_zero_sums(cuda_lib):
+    """No rows: nothing to quantize, and each column's sum over no rows is 0."""
+    import torch
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    cs = torch.full((256,), float("nan"), dtype=torch.float32, device="cuda")
+    _, _, cs = cuda_lib.mx_quantize_colsum_noalloc(x, O.E4M3, True, colsum_out=cs)
+    torch.cuda.synchronize()
+    assert bool((cs == 0).all())
+
+
 def test_noalloc_rejects_sizes_beyond_the_scratch(cuda_lib):
     import torch
     rows, cols = 128 * 65, 32768          # 65 tile rows x 32768 columns > 2^21 partials
