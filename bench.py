@@ -12,11 +12,16 @@ Work per step: 18*R*D*F = 7.42 TFLOP.  Inputs (>= 403 MB each) are larger
 than the 129 MB L2, so no flush is needed between steps.
 
 JSON line fields beyond the common contract:
-  roofline      the step's dominant kernel: FLOP per launch / its mean
-                CUDA-event duration inside the timed steps, against the
-                measured dense peak (MEASURED_PEAKS.json bf16 x 2 for MXFP8)
+  roofline      the step's dominant kernel: FLOP per launch / its median
+                CUDA-event duration over >= 20 steps of its stage, against
+                the measured dense peak (MEASURED_PEAKS.json bf16 x 2 for
+                MXFP8); traffic from a small-case ncu capture, named in
+                traffic_source
+  config        also carries compact copies of the per-stage times, the
+                GEMM-only fraction of the FP8 peak, the standalone quantizer
+                and the dense MXFP6 step
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
-  stages        per-kernel mean times and rates
+  stages        per-kernel median times (>= 20 runs) and rates
   quantizer     the standalone quantizer workload (8192 x 7168 BF16, both
                 orientations) in GB/s, L2 flushed between iterations
 
@@ -55,20 +60,19 @@ def stage_flops(D, F, R):
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
-# each stage at the benchmark shape, from a one-pass ncu launch list of this
-# benchmark (four steps averaged) on the kernels as they are now.  An entry
-# goes back to None whenever its kernel changes, until it is captured again.
-MEASURED_TRAFFIC = {
-    "quant_x": 2119435968,
-    "quant_w1": 1573157184,
-    "quant_w2": 755222528,
-    "fc1_swiglu": 2121824960,
-    "fc2": 1423439360,
-    "quant_dy": 2119638336,
-    "fc2_dgrad_dswiglu": 2719386944,
-    "fc1_dgrad": 1840506432,
-    "wgrad_dw2": 1362582208,
-    "wgrad_dw1": 2154535168,
+# the step's GEMM stages, from single-kernel ncu captures of the G=32,
+# R=65536 case (a quarter of the benchmark's experts and routed rows, so
+# every operand and output is a quarter of a full launch's), multiplied by
+# TRAFFIC_SCALE to a full launch.  Writes still held in the 129 MB L2 when
+# the kernel exits are not counted.  Each entry names the summary of its
+# capture under profiles/; an entry goes back to None whenever its kernel
+# changes, until it is captured again.
+TRAFFIC_SCALE = 4
+SMALL_CASE_TRAFFIC = {
+    "fc1_swiglu": (242.3e6 + 262.5e6, "profiles/fc1_swiglu_gemm_moe_G32_R65536.md"),
+    "fc2_dgrad_dswiglu": (425.2e6 + 152.9e6, "profiles/dswiglu_gemm_moe_G32_R65536.md"),
+    "fc1_dgrad": (207.7e6 + 227.3e6, "profiles/fc1_dgrad_gemm_moe_G32_R65536.md"),
+    "wgrad_dw1": (254.0e6 + 161.7e6, "profiles/wgrad_dw1_moe_G32_R65536.md"),
 }
 
 
@@ -355,7 +359,17 @@ def run_gpu(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_kind"] = peak_kind + (" hbm copy" if roof["bound"] == "hbm" else " bf16 burst x 2")
     roof["launch_ms"] = dd["ms"]
-    roof["traffic"] = MEASURED_TRAFFIC.get(dom)  # bytes per launch, or None if not captured
+    if SMALL_CASE_TRAFFIC.get(dom) is not None:
+        small, src = SMALL_CASE_TRAFFIC[dom]
+        roof["traffic"] = small * TRAFFIC_SCALE
+        roof["traffic_source"] = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the G=32 "
+                                  "R=65536 case (%s), x%d to a full launch; not measured in this run"
+                                  % (src, TRAFFIC_SCALE))
+    else:
+        roof["traffic"] = None
+        roof["traffic_source"] = "not captured on this kernel"
+    gemm_names = ("fc1_swiglu", "fc2", "fc2_dgrad_dswiglu", "fc1_dgrad", "wgrad_dw2", "wgrad_dw1")
+    gemm_ms = sum(stages[k]["ms"] for k in gemm_names)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -363,7 +377,15 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (no flush)",
                    "flop_per_step": flops, "frac_of_fp8_peak": value / world / peak_fp8,
                    "frac_of_fp8_peak_sustained": value / world / peak_fp8_sust,
-                   "peak_fp8_tflops": peak_fp8, "peak_kind": peak_kind + " (bf16 burst x 2)"},
+                   "peak_fp8_tflops": peak_fp8, "peak_kind": peak_kind + " (bf16 burst x 2)",
+                   # compact copies of the per-stage figures (medians of >= 20 CUDA-event runs)
+                   "gemm_only_ms": gemm_ms,
+                   "gemm_only_frac": flops / (gemm_ms * 1e-3) / 1e12 / peak_fp8,
+                   "stage_ms": {k: round(v["ms"], 4) for k, v in stages.items()},
+                   "quantizer_mxfp8_us": round(quant["us"], 2),
+                   "quantizer_mxfp8_frac_of_hbm": round(quant["frac_of_hbm"], 4),
+                   "dense_mxfp6_step_ms": None if dense is None else round(dense["ms_per_step"], 4),
+                   "dense_mxfp6_frac_of_fp8_peak": None if dense is None else round(dense["frac_of_fp8_peak"], 4)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
@@ -387,7 +409,7 @@ def run_gpu(args):
 
 
 def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev):
-    """Mean CUDA-event duration of each kernel of the step, launched through
+    """Median CUDA-event duration (over >= 20 steps) of each kernel of the step, launched through
     the stage entry points in the order the step uses (events on the
     launching stream between launches)."""
     stream = torch.cuda.current_stream(dev)
@@ -419,7 +441,7 @@ def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev
         for c in calls:
             c()
     torch.cuda.synchronize(dev)
-    n = max(3, min(steps, 20))
+    n = max(20, steps)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(n)]
     for i in range(n):
         evs[i][0].record(stream)
@@ -432,7 +454,7 @@ def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev
     res = {}
     for j, name in enumerate(names):
         t = [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n)]
-        ms = float(np.mean(t))
+        ms = float(np.median(t))
         d = {"ms": ms, "launches": 1}
         if name in sf:
             d["tflops"] = sf[name] / (ms * 1e-3) / 1e12
@@ -568,10 +590,11 @@ def dense_step_rate(mx, torch, dev, steps=5):
     for c in calls.values():
         c()
     torch.cuda.synchronize(dev)
-    st = {k: 0.0 for k in calls}
-    for _ in range(5):
+    samples = {k: [] for k in calls}
+    for _ in range(20):  # interleaved rounds, median per stage
         for k, c in calls.items():
-            st[k] += _event_mean(torch, stream, dev, c, 1) / 5
+            samples[k].append(_event_median(torch, stream, dev, c, 1))
+    st = {k: float(np.median(v)) for k, v in samples.items()}
     gemm = 2.0 * M * D * H
     stages = {k: {"ms": v, "tflops": gemm / (v * 1e-3) / 1e12} if k[:5] in ("fc1_g", "fc2", "fc2_d", "fc1_d", "wgrad")
               else {"ms": v} for k, v in st.items()}
@@ -614,8 +637,8 @@ def moe_forward_even_rate(mx, torch, dev, steps=5):
             "ms": ms, "tflops": 6.0 * R * D * F / (ms * 1e-3) / 1e12}
 
 
-def _event_mean(torch, stream, dev, fn, reps, before=None):
-    """Mean CUDA-event time of fn over reps launches (before() runs outside
+def _event_median(torch, stream, dev, fn, reps, before=None):
+    """Median CUDA-event time of fn over reps launches (before() runs outside
     the bracket, e.g. an L2 flush)."""
     ts = []
     for _ in range(reps):
@@ -627,10 +650,10 @@ def _event_mean(torch, stream, dev, fn, reps, before=None):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ts.append(e0.elapsed_time(e1))
-    return float(np.mean(ts))
+    return float(np.median(ts))
 
 
-def variant_rates(mx, torch, dev, reps=10):
+def variant_rates(mx, torch, dev, reps=20):
     """The optional forms of the stages beside their plain forms, timed the
     same way: FC1 + SwiGLU and FC2 dgrad + dSwiGLU with routing
     probabilities (the backward adds its dprobs reduction launch), the dW1
@@ -674,14 +697,14 @@ def variant_rates(mx, torch, dev, reps=10):
         c()
         c()
     torch.cuda.synchronize(dev)
-    sums = {k: 0.0 for k in calls}
+    sums = {k: [] for k in calls}
     for _ in range(reps):  # interleaved, so that clock drift hits every form alike
         for k, c in calls.items():
-            sums[k] += _event_mean(torch, stream, dev, c, 1)
+            sums[k].append(_event_median(torch, stream, dev, c, 1))
     sf = stage_flops(D, F, R)
     res = {}
     for k, s in sums.items():
-        ms = s / reps
+        ms = float(np.median(s))
         base = k.split("_probs")[0].split("_f32")[0]
         res[k] = {"ms": ms, "tflops": sf[base] / (ms * 1e-3) / 1e12}
     res["launches"] = {"fc2_dgrad_dswiglu_probs": 2, "others": 1}
@@ -702,15 +725,15 @@ def variant_rates(mx, torch, dev, reps=10):
     }
     for qc in qcalls.values():
         qc()
-    qsums = {k: 0.0 for k in qcalls}
+    qsums = {k: [] for k in qcalls}
     for _ in range(reps):
         for k, qc in qcalls.items():
-            qsums[k] += _event_mean(torch, stream, dev, qc, 1, before=lambda: (flush.fill_(1), clean.max()))
+            qsums[k].append(_event_median(torch, stream, dev, qc, 1, before=lambda: (flush.fill_(1), clean.max())))
     n = rows * cols
     qbytes = n * 2 + 2 * n * (0.5 + 1.0 / 32)  # BF16 in; two MXFP4 copies out
     peaks, _ = measured_peaks()
     for k, s in qsums.items():
-        ms = s / reps
+        ms = float(np.median(s))
         gbs = qbytes / (ms * 1e-3) / 1e9
         res[k] = {"us": ms * 1e3, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"]}
     res["quant_workload"] = ("8192x7168 bf16 -> mxfp4 row+col, L2 flushed between iterations (512 MB written, then "
@@ -721,7 +744,7 @@ def variant_rates(mx, torch, dev, reps=10):
     return res
 
 
-def mxfp4_gemm_rate(mx, torch, dev, reps=10):
+def mxfp4_gemm_rate(mx, torch, dev, reps=20):
     """Dense MXFP4 GEMM on the packed-operand tensor-core path: E2M1 operands
     of the dense MLP's FC1 shape (M=16384 tokens, N=12288, K=3072), BF16 out,
     inputs larger than L2 (no flush needed)."""
@@ -738,7 +761,7 @@ def mxfp4_gemm_rate(mx, torch, dev, reps=10):
     for _ in range(3):
         mx.mx_gemm_bias(ar, br, None, out=out)
     torch.cuda.synchronize(dev)
-    ms = _event_mean(torch, stream, dev, lambda: mx.mx_gemm_bias(ar, br, None, out=out), reps)
+    ms = _event_median(torch, stream, dev, lambda: mx.mx_gemm_bias(ar, br, None, out=out), reps)
     peaks, kind = measured_peaks()
     tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     peak_fp4 = 6.0 * peaks["bf16_tflops"]
@@ -747,7 +770,7 @@ def mxfp4_gemm_rate(mx, torch, dev, reps=10):
             "peak_kind": kind + " bf16 burst x 6 (nominal fp4/bf16 ratio)"}
 
 
-def permute_rates(mx, torch, dev, reps=10):
+def permute_rates(mx, torch, dev, reps=20):
     """The token permute of the benchmark's routing: 32768 tokens, top-8 of
     128 experts (Zipf(1.1) popularity, distinct experts per token), hidden
     2048.  Times the routing index, the quantizing permute (E4M3, both
@@ -793,7 +816,7 @@ def permute_rates(mx, torch, dev, reps=10):
     t = {name: 0.0 for name in ("route", "perm", "unfused", "unperm")}
     for _ in range(reps):
         for name, f in (("route", route), ("perm", perm), ("unfused", unfused), ("unperm", unperm)):
-            t[name] += _event_mean(torch, stream, dev, f, 1)
+            t[name] += _event_median(torch, stream, dev, f, 1)
     t = {kk: v / reps for kk, v in t.items()}
     status = mx.mx_get_device_status()
     if status != "MX_OK":
@@ -846,7 +869,7 @@ def quantizer_rate(mx, torch, dev):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ts.append(e0.elapsed_time(e1))
-        return float(np.mean(ts))
+        return float(np.median(ts))
 
     ms, ms_dirty = timed(True), timed(False)
     peaks, kind = measured_peaks()
