@@ -69,10 +69,12 @@ def stage_flops(D, F, R):
 # changes, until it is captured again.
 TRAFFIC_SCALE = 4
 SMALL_CASE_TRAFFIC = {
-    "fc1_swiglu": (242.3e6 + 262.5e6, "profiles/fc1_swiglu_gemm_moe_G32_R65536.md"),
-    "fc2_dgrad_dswiglu": (425.2e6 + 152.9e6, "profiles/dswiglu_gemm_moe_G32_R65536.md"),
-    "fc1_dgrad": (207.7e6 + 227.3e6, "profiles/fc1_dgrad_gemm_moe_G32_R65536.md"),
-    "wgrad_dw1": (254.0e6 + 161.7e6, "profiles/wgrad_dw1_moe_G32_R65536.md"),
+    "fc1_swiglu": (242.3e6 + 261.9e6, "profiles/launches_moe_mlp_step.md"),
+    "fc2": (103.9e6 + 217.0e6, "profiles/launches_moe_mlp_step.md"),
+    "fc2_dgrad_dswiglu": (424.6e6 + 153.0e6, "profiles/launches_moe_mlp_step.md"),
+    "fc1_dgrad": (207.7e6 + 227.5e6, "profiles/launches_moe_mlp_step.md"),
+    "wgrad_dw2": (200.1e6 + 58.0e6, "profiles/launches_moe_mlp_step.md"),
+    "wgrad_dw1": (252.5e6 + 161.4e6, "profiles/launches_moe_mlp_step.md"),
 }
 
 
@@ -304,8 +306,10 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         clk.mark()
         ev0.record(stream)
+        h0 = time.perf_counter()
         for _ in range(args.steps):
             mx.mx_mlp_fwd_bwd(margs)
+        host_us_per_step = (time.perf_counter() - h0) * 1e6 / args.steps
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -314,6 +318,9 @@ def run_gpu(args):
     flops = step_flops(G, D, F, R)
     value = flops * world / (ms_step * 1e-3) / 1e12
     launches_per_step = 10  # 4 quantizer + 6 GEMM launches (mx_mlp_fwd_bwd, SwiGLU)
+
+    # ---- the same step replayed from a CUDA graph (no per-launch host work) ----
+    graph_ms = step_graph_ms(mx, torch, margs, dev, args.steps)
 
     # ---- per-kernel times: the same stages through their entry points ----
     stages = stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, args.steps, dev)
@@ -384,6 +391,8 @@ def run_gpu(args):
                    "stage_ms": {k: round(v["ms"], 4) for k, v in stages.items()},
                    "quantizer_mxfp8_us": round(quant["us"], 2),
                    "quantizer_mxfp8_frac_of_hbm": round(quant["frac_of_hbm"], 4),
+                   "step_graph_ms": round(graph_ms, 4),
+                   "host_us_per_step": round(host_us_per_step, 1),
                    "dense_mxfp6_step_ms": None if dense is None else round(dense["ms_per_step"], 4),
                    "dense_mxfp6_frac_of_fp8_peak": None if dense is None else round(dense["frac_of_fp8_peak"], 4)},
         "e2e": e2e,
@@ -406,6 +415,30 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def step_graph_ms(mx, torch, margs, dev, steps):
+    """Mean CUDA-event time of the step replayed from a CUDA graph captured
+    once from mx_mlp_fwd_bwd (the eager steps before have set every kernel's
+    launch attribute)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            mx.mx_mlp_fwd_bwd(margs)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
 
 
 def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev):

@@ -13,6 +13,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_set>
 #include <vector>
 
 #include <cuda.h>
@@ -264,6 +265,37 @@ bool env_validate_offsets() {
   return v && v[0] == '1';
 }
 
+// MX_LOG=1: one line on stderr for each launch configuration the process
+// has not launched before (kernel, epilogue, tile width, shapes, grid), read
+// from the environment once.  The configurations seen are kept in a set of
+// at most 4096 entries (past that, nothing more is printed).
+bool env_log() {
+  static const bool on = [] {
+    const char* v = getenv("MX_LOG");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+void log_config(const char* fmt, ...) {
+  if (!env_log()) return;
+  char line[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(line, sizeof(line), fmt, ap);
+  va_end(ap);
+  static std::mutex mu;
+  static std::unordered_set<std::string> seen;
+  std::lock_guard<std::mutex> lk(mu);
+  if (seen.size() >= 4096 || !seen.insert(line).second) return;
+  fprintf(stderr, "mx: %s\n", line);
+}
+
+const char* epi_name(int epi) {
+  static const char* names[] = {"bf16", "swiglu", "dswiglu", "gelu", "dgelu", "f32"};
+  return (epi >= 0 && epi <= 5) ? names[epi] : "?";
+}
+
 // Opt-in value check of the offsets (synchronises the stream).
 mx_status_t validate_offsets_values(const int32_t* offsets_dev, int G, int64_t R, cudaStream_t s) {
   std::vector<int32_t> h((size_t)G);
@@ -339,6 +371,10 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
   } else {
     to = ta;
   }
+  log_config("gemm %s %s%s BN=%d a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld grid=%lld split=%d",
+             p.mode == mx::MODE_WGRAD ? "wgrad" : "grouped", epi_name(p.epi), p.f4 ? " mxf4" : "", bn, p.a_type,
+             p.b_type, (long long)p.R, (long long)p.K, (long long)p.Nb, p.G, (long long)p.num_tiles,
+             (long long)(p.num_tiles < dev.sms ? p.num_tiles : dev.sms), p.split_chunks > 0 ? 1 : 0);
   cudaError_t e = mx::launch_gemm(p, ta, tb, to, bn, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
   return MX_OK;
@@ -466,6 +502,8 @@ mx_status_t quantize_impl(const void* x_bf16, int64_t batch, int64_t rows, int64
                               staged_box(fmt))) != MX_OK)
       return st;
   }
+  log_config("quantize fmt=%d flags=0x%x%s batch=%lld rows=%lld cols=%lld", fmt, flags, stochastic ? " sr" : "",
+             (long long)batch, (long long)rows, (long long)cols);
   cudaError_t e = mx::launch_quantize(q, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return MX_OK;
@@ -1093,6 +1131,9 @@ mx_status_t dense_fused(int epi, const mx_tensor_t* a, const mx_tensor_t* b, con
     to = ta;
   }
   if ((st = attach_tap(&p, p.R, p.q_cols)) != MX_OK) return st;
+  log_config("gemm dense %s BN=%d a=%d out_fmt=%d rotated=%d M=%lld K=%lld N=%lld tiles=%lld grid=%lld",
+             epi_name(p.epi), tile_n, p.a_type, p.q_fmt, p.q_had, (long long)p.R, (long long)p.K, (long long)p.Nb,
+             (long long)p.num_tiles, (long long)(p.num_tiles < dev.sms ? p.num_tiles : dev.sms));
   cudaError_t e = mx::launch_gemm_dense(p, ta, tb, to, tile_n, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "dense GEMM launch");
   return MX_OK;
