@@ -206,6 +206,21 @@ MX_API mx_status_t mx_moe_route_index(const int32_t *topk_dev, int64_t T, int32_
                                       size_t workspace_bytes, mx_stream_t stream);
 
 /*
+ * mx_moe_route_rows_pad / mx_moe_route_index_pad -- the same with each
+ * expert's segment padded to a multiple of `pad` rows, pad = 128 or 256
+ * (256: the segment alignment the CTA-pair grouped GEMM needs, the torchao
+ * PR #5 page's cudnn-fe ops commit: 256-row alignment for its kernels).
+ * mx_moe_route_rows_pad gives T*k + (pad-1)*G rounded up to pad (0 for a
+ * pad other than 128 or 256); mx_moe_route_index_pad returns
+ * MX_ERR_INVALID_ARG for another pad, else behaves as mx_moe_route_index.
+ */
+MX_API int64_t mx_moe_route_rows_pad(int64_t T, int32_t k, int32_t G, int32_t pad);
+MX_API mx_status_t mx_moe_route_index_pad(const int32_t *topk_dev, int64_t T, int32_t k, int32_t G, int32_t pad,
+                                          int32_t *offsets_dev, int32_t *src_dev, int64_t R_cap,
+                                          int32_t *row_of_dev, void *workspace, size_t workspace_bytes,
+                                          mx_stream_t stream);
+
+/*
  * mx_permute_quantize -- the quantizing permute: routed row r of the output
  * is the MX quantization of token src[r] of x (a zero row where src[r] <
  * 0), rowwise and/or columnwise, in one pass over the tokens with no
@@ -299,6 +314,27 @@ MX_API mx_status_t mx_quantize_colsum_noalloc(const void *x_bf16, int64_t rows, 
  */
 MX_API mx_status_t mx_grouped_gemm(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G, const int32_t *offsets_dev,
                             void *out_bf16, int64_t ld_out, mx_stream_t stream);
+
+/*
+ * mx_grouped_gemm_2sm -- mx_grouped_gemm on CTA pairs: two SMs take a
+ * 256 x 256 output tile with tcgen05 .cta_group::2 MMAs (M = 256), each SM
+ * loading its 128 rows of A and half of the tile's B slice ([MXFP8-PR]
+ * cudnn-fe ops commit: 256-row MMA tiles and 256-row segment alignment).
+ * Same arguments and output as mx_grouped_gemm, with:
+ *   a, b     E4M3 or E2M3 (E2M1: MX_ERR_NOT_SUPPORTED); N = b->rows / G a
+ *            multiple of 256 (else MX_ERR_SHAPE)
+ *   offsets  every segment a multiple of 256 rows (mx_moe_route_index_pad
+ *            with pad 256 builds such a routing); a segment that is not is
+ *            skipped on the device and reported as MX_ERR_OFFSETS by
+ *            mx_get_device_status.  NULL: one segment of all R rows, R a
+ *            multiple of 256.
+ * The products and their fp32 accumulation are those of mx_grouped_gemm
+ * (bit-identical outputs).  The training step uses the single-SM kernel;
+ * this one is measured beside it.
+ */
+MX_API mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G,
+                                       const int32_t *offsets_dev, void *out_bf16, int64_t ld_out,
+                                       mx_stream_t stream);
 
 /*
  * mx_grouped_gemm_bias -- mx_grouped_gemm with a per-expert bias added to

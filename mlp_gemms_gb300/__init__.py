@@ -38,7 +38,7 @@ ABI_SYMBOLS = (
     "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr", "mx_moe_route_rows", "mx_moe_route_workspace_bytes",
     "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute", "mx_grouped_gemm_bias",
     "mx_grouped_gemm_wgrad_workspace_bytes", "mx_grouped_gemm_wgrad_ws", "mx_grouped_gemm_wgrad_f32_ws",
-    "mx_mlp_workspace_layout",
+    "mx_mlp_workspace_layout", "mx_moe_route_rows_pad", "mx_moe_route_index_pad", "mx_grouped_gemm_2sm",
 )
 
 
@@ -105,6 +105,7 @@ def load(path=None):
         "mx_quantize_workspace_bytes": (sz, [i64, i64, u32]),
         "mx_quantize": (ctypes.c_int, [vp, i64, i64, i64, i64, i32, u32, tp, tp, vp, vp, sz, vp]),
         "mx_grouped_gemm": (ctypes.c_int, [tp, tp, i32, vp, vp, i64, vp]),
+        "mx_grouped_gemm_2sm": (ctypes.c_int, [tp, tp, i32, vp, vp, i64, vp]),
         "mx_grouped_gemm_swiglu_fwd": (ctypes.c_int, [tp, tp, i32, vp, tp, tp, vp, vp]),
         "mx_grouped_gemm_dswiglu_bwd": (ctypes.c_int, [tp, tp, vp, i32, vp, tp, tp, vp]),
         "mx_grouped_gemm_wgrad": (ctypes.c_int, [tp, tp, i32, vp, vp, vp]),
@@ -126,6 +127,8 @@ def load(path=None):
         "mx_moe_route_rows": (i64, [i64, i32, i32]),
         "mx_moe_route_workspace_bytes": (sz, [i64, i32, i32]),
         "mx_moe_route_index": (ctypes.c_int, [vp, i64, i32, i32, vp, vp, i64, vp, vp, sz, vp]),
+        "mx_moe_route_rows_pad": (i64, [i64, i32, i32, i32]),
+        "mx_moe_route_index_pad": (ctypes.c_int, [vp, i64, i32, i32, i32, vp, vp, i64, vp, vp, sz, vp]),
         "mx_permute_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, i64, vp, i32, i32, u32, tp, tp, vp]),
         "mx_moe_unpermute": (ctypes.c_int, [vp, i64, i64, vp, vp, i64, i32, vp, vp]),
         "mx_grouped_gemm_bias": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, i64, vp]),
@@ -250,22 +253,24 @@ def mx_moe_route_rows(T, k, G):
     return int(load().mx_moe_route_rows(T, k, G))
 
 
-def mx_moe_route_index(topk, G, R_cap=None, offsets=None, src=None, row_of=None, workspace=None, stream=None):
+def mx_moe_route_index(topk, G, R_cap=None, offsets=None, src=None, row_of=None, workspace=None, stream=None,
+                       pad=128):
     """topk int32 [T, k] expert ids on the GPU -> (offsets [G], src [R_cap],
-    row_of [T, k]) of the token permute."""
+    row_of [T, k]) of the token permute; segments padded to `pad` (128 or
+    256) rows."""
     import torch
     assert topk.dtype == torch.int32 and topk.is_contiguous()
     T, k = topk.shape
     dev = topk.device
-    R_cap = R_cap if R_cap is not None else mx_moe_route_rows(T, k, G)
+    R_cap = R_cap if R_cap is not None else int(load().mx_moe_route_rows_pad(T, k, G, pad))
     offsets = offsets if offsets is not None else torch.empty(G, dtype=torch.int32, device=dev)
     src = src if src is not None else torch.empty(R_cap, dtype=torch.int32, device=dev)
     row_of = row_of if row_of is not None else torch.empty((T, k), dtype=torch.int32, device=dev)
     nbytes = int(load().mx_moe_route_workspace_bytes(T, k, G))
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-    _check(load().mx_moe_route_index(_ptr(topk), T, k, G, _ptr(offsets), _ptr(src), R_cap, _ptr(row_of),
-                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+    _check(load().mx_moe_route_index_pad(_ptr(topk), T, k, G, pad, _ptr(offsets), _ptr(src), R_cap, _ptr(row_of),
+                                          _ptr(workspace), workspace.numel(), _stream(stream)))
     return offsets, src, row_of
 
 
@@ -330,6 +335,17 @@ def mx_grouped_gemm(a, b, G, offsets, out=None, ld_out=None, stream=None):
         out = torch.empty((a.rows, N), dtype=torch.bfloat16, device=a.data.device)
     ld = ld_out if ld_out is not None else out.stride(0)
     _check(load().mx_grouped_gemm(_s(a), _s(b), G, _ptr(offsets), _ptr(out), ld, _stream(stream)))
+    return out
+
+
+def mx_grouped_gemm_2sm(a, b, G, offsets, out=None, ld_out=None, stream=None):
+    """mx_grouped_gemm on CTA pairs (256-row tiles; segments multiples of 256)."""
+    import torch
+    N = b.rows // G if G else 0
+    if out is None:
+        out = torch.empty((a.rows, N), dtype=torch.bfloat16, device=a.data.device)
+    ld = ld_out if ld_out is not None else out.stride(0)
+    _check(load().mx_grouped_gemm_2sm(_s(a), _s(b), G, _ptr(offsets), _ptr(out), ld, _stream(stream)))
     return out
 
 

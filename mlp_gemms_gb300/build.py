@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libmxgb300.so")
-SOURCES = ["quantize.cu", "gemm.cu", "gemm_dense.cu", "gemm_f4.cu", "permute.cu", "api.cu", "pipeline.cu"]
+SOURCES = ["quantize.cu", "gemm.cu", "gemm_dense.cu", "gemm_f4.cu", "gemm_pair.cu", "permute.cu", "api.cu",
+           "pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "--expt-relaxed-constexpr"]

@@ -194,6 +194,25 @@ mx_status_t make_tmap_out_f32(CUtensorMap* m, const void* base, int64_t rows, in
   return MX_OK;
 }
 
+// Blocked scales of a [rows, K] MX tensor as [row blocks][K chunks][512
+// bytes] (64 x 8-byte elements per chunk), boxes of one chunk x `blocks`
+// consecutive row blocks: the CTA-pair GEMM loads a stage's scale chunks
+// with the 2-SM TMA form.
+mx_status_t make_tmap_scales(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int blocks) {
+  mx_status_t st = get_encoder();
+  if (st != MX_OK) return st;
+  const int64_t kchunks = (k / 32 + 3) / 4, rblocks = (rows + 127) / 128;
+  cuuint64_t dims[3] = {64, (cuuint64_t)kchunks, (cuuint64_t)rblocks};
+  cuuint64_t strides[2] = {512, (cuuint64_t)(kchunks * 512)};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)blocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MX_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", (int)r);
+  return MX_OK;
+}
+
 // Byte tensor [rows, row_bytes] as a TMA store target: box 128 bytes x 128
 // rows, 128-byte swizzle (the quantizer's staging layout).
 mx_status_t make_tmap_bytes(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_bytes) {
@@ -530,10 +549,12 @@ mx_status_t mx_quantize_sr(const void* x_bf16, int64_t batch, int64_t rows, int6
                        stream);
 }
 
-int64_t mx_moe_route_rows(int64_t T, int32_t k, int32_t G) {
-  if (T < 0 || k < 0 || G < 0) return 0;
-  return (T * k + 127ll * G + 127) / 128 * 128;
+int64_t mx_moe_route_rows_pad(int64_t T, int32_t k, int32_t G, int32_t pad) {
+  if (T < 0 || k < 0 || G < 0 || (pad != 128 && pad != 256)) return 0;
+  return (T * k + (int64_t)(pad - 1) * G + pad - 1) / pad * pad;
 }
+
+int64_t mx_moe_route_rows(int64_t T, int32_t k, int32_t G) { return mx_moe_route_rows_pad(T, k, G, 128); }
 
 size_t mx_moe_route_workspace_bytes(int64_t T, int32_t k, int32_t G) {
   if (T < 0 || k < 0 || G < 0) return 0;
@@ -544,11 +565,20 @@ size_t mx_moe_route_workspace_bytes(int64_t T, int32_t k, int32_t G) {
 mx_status_t mx_moe_route_index(const int32_t* topk_dev, int64_t T, int32_t k, int32_t G, int32_t* offsets_dev,
                                int32_t* src_dev, int64_t R_cap, int32_t* row_of_dev, void* workspace,
                                size_t workspace_bytes, mx_stream_t stream) {
+  return mx_moe_route_index_pad(topk_dev, T, k, G, 128, offsets_dev, src_dev, R_cap, row_of_dev, workspace,
+                                workspace_bytes, stream);
+}
+
+mx_status_t mx_moe_route_index_pad(const int32_t* topk_dev, int64_t T, int32_t k, int32_t G, int32_t pad,
+                                   int32_t* offsets_dev, int32_t* src_dev, int64_t R_cap, int32_t* row_of_dev,
+                                   void* workspace, size_t workspace_bytes, mx_stream_t stream) {
+  MX_CHECK(pad == 128 || pad == 256, MX_ERR_INVALID_ARG, "pad = %d; segments are padded to 128 or 256 rows", pad);
   MX_CHECK(T >= 0 && k >= 1, MX_ERR_INVALID_ARG, "T = %lld, k = %d", (long long)T, k);
   MX_CHECK(G >= 1 && G <= 1024, MX_ERR_INVALID_ARG, "G = %d is outside [1, 1024]", G);
   MX_CHECK(T * k < (1ll << 31), MX_ERR_SHAPE, "T * k = %lld exceeds the int32 row range", (long long)(T * k));
-  MX_CHECK(R_cap >= mx_moe_route_rows(T, k, G) && R_cap < (1ll << 31), MX_ERR_SHAPE,
-           "R_cap = %lld; mx_moe_route_rows gives %lld", (long long)R_cap, (long long)mx_moe_route_rows(T, k, G));
+  MX_CHECK(R_cap >= mx_moe_route_rows_pad(T, k, G, pad) && R_cap < (1ll << 31), MX_ERR_SHAPE,
+           "R_cap = %lld; mx_moe_route_rows_pad gives %lld", (long long)R_cap,
+           (long long)mx_moe_route_rows_pad(T, k, G, pad));
   MX_CHECK(offsets_dev != nullptr && src_dev != nullptr, MX_ERR_INVALID_ARG, "offsets or src is NULL");
   MX_CHECK(T == 0 || (topk_dev != nullptr && row_of_dev != nullptr), MX_ERR_INVALID_ARG, "topk or row_of is NULL");
   MX_CHECK(aligned16(topk_dev) && aligned16(offsets_dev) && aligned16(src_dev) && aligned16(row_of_dev),
@@ -560,7 +590,7 @@ mx_status_t mx_moe_route_index(const int32_t* topk_dev, int64_t T, int32_t k, in
   mx_status_t st;
   if ((st = device_info(&dev)) != MX_OK) return st;
   cudaError_t e = mx::launch_route_index(topk_dev, T, k, G, offsets_dev, src_dev, R_cap, row_of_dev,
-                                         static_cast<int32_t*>(workspace), reinterpret_cast<cudaStream_t>(stream));
+                                         static_cast<int32_t*>(workspace), pad, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "routing index launch");
   return MX_OK;
 }
@@ -724,6 +754,54 @@ extern "C" {
 mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
                             void* out_bf16, int64_t ld_out, mx_stream_t stream) {
   return grouped_gemm_impl(a, b, G, offsets_dev, nullptr, out_bf16, ld_out, stream);
+}
+
+mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                                void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mx_status_t st;
+  if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
+  if ((st = check_gemm_operand(b, "b")) != MX_OK) return st;
+  if ((st = check_pair(a, b, "a", "b")) != MX_OK) return st;
+  MX_CHECK(a->fmt != MX_E2M1, MX_ERR_NOT_SUPPORTED, "the CTA-pair GEMM runs E4M3 and E2M3 operands");
+  MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
+  MX_CHECK(a->cols == b->cols, MX_ERR_SHAPE, "a has K = %lld, b has K = %lld", (long long)a->cols, (long long)b->cols);
+  const int64_t K = a->cols, R = a->rows;
+  MX_CHECK(K % 128 == 0, MX_ERR_SHAPE, "K = %lld is not a multiple of 128", (long long)K);
+  MX_CHECK(b->rows % G == 0, MX_ERR_SHAPE, "b has %lld rows, not a multiple of G = %d", (long long)b->rows, G);
+  const int64_t N = b->rows / G;
+  MX_CHECK(N > 0 && N % 256 == 0, MX_ERR_SHAPE, "N = %lld per expert is not a positive multiple of 256",
+           (long long)N);
+  MX_CHECK(offsets_dev != nullptr || R % 256 == 0, MX_ERR_SHAPE,
+           "without offsets R = %lld must be a multiple of 256", (long long)R);
+  MX_CHECK(R == 0 || (out_bf16 != nullptr && aligned16(out_bf16)), MX_ERR_ALIGNMENT,
+           "out must be a 16-byte aligned pointer");
+  MX_CHECK(ld_out >= N && ld_out % 8 == 0, MX_ERR_ALIGNMENT, "ld_out = %lld must be >= N and a multiple of 8",
+           (long long)ld_out);
+  MX_CHECK(R * ld_out < (1ll << 40), MX_ERR_SHAPE, "output too large");
+  if ((st = check_offsets(offsets_dev, G, R, s)) != MX_OK) return st;
+  if (R == 0) return MX_OK;
+  DevInfo dev;
+  if ((st = device_info(&dev)) != MX_OK) return st;
+  mx::PairParams p;
+  memset(&p, 0, sizeof(p));
+  p.G = G; p.offsets = offsets_dev;
+  p.R = R; p.K = K; p.Nb = N;
+  p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
+  p.n_tiles = N / 256;
+  p.num_tiles = (R + 255) / 256 * p.n_tiles;
+  p.tx_bytes = stage_tx_bytes(a->fmt, 128) + 512u;  // 128 A rows, 128 B rows, A's chunk and both B chunks
+  CUtensorMap ta, tb, tsa, tsb, to;
+  if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
+  if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
+  if ((st = make_tmap_scales(&tsa, a->scale, a->rows, K, 1)) != MX_OK) return st;
+  if ((st = make_tmap_scales(&tsb, b->scale, b->rows, K, 2)) != MX_OK) return st;
+  if ((st = make_tmap_out(&to, out_bf16, R, N, ld_out)) != MX_OK) return st;
+  log_config("gemm pair bf16 BN=256 a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld", p.a_type, p.b_type,
+             (long long)R, (long long)K, (long long)N, G, (long long)p.num_tiles);
+  cudaError_t e = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, to, s, dev.sms);
+  if (e != cudaSuccess) return cuda_fail(e, "CTA-pair GEMM launch");
+  return MX_OK;
 }
 
 mx_status_t mx_grouped_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
@@ -1433,16 +1511,16 @@ mx_status_t mx_mlp_fwd_bwd(const mx_mlp_args_t* a, mx_stream_t stream) { return 
 mx_status_t mx_get_device_status(mx_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  unsigned word = 0, dense = 0, f4 = 0, quant = 0, perm = 0;
+  unsigned word = 0, dense = 0, f4 = 0, quant = 0, perm = 0, pairs = 0;
   if ((e = mx::read_gemm_status(&word)) != cudaSuccess || (e = mx::read_dense_status(&dense)) != cudaSuccess ||
       (e = mx::read_f4_status(&f4)) != cudaSuccess || (e = mx::read_quant_status(&quant)) != cudaSuccess ||
-      (e = mx::read_perm_status(&perm)) != cudaSuccess)
+      (e = mx::read_perm_status(&perm)) != cudaSuccess || (e = mx::read_pair_status(&pairs)) != cudaSuccess)
     return cuda_fail(e, "reading device status");
   if ((e = mx::reset_gemm_status()) != cudaSuccess || (e = mx::reset_dense_status()) != cudaSuccess ||
       (e = mx::reset_f4_status()) != cudaSuccess || (e = mx::reset_quant_status()) != cudaSuccess ||
-      (e = mx::reset_perm_status()) != cudaSuccess)
+      (e = mx::reset_perm_status()) != cudaSuccess || (e = mx::reset_pair_status()) != cudaSuccess)
     return cuda_fail(e, "clearing device status");
-  word |= dense | f4 | quant | perm;
+  word |= dense | f4 | quant | perm | pairs;
   if (word & 1u) return fail(MX_ERR_DEVICE_TIMEOUT, "a bounded device-side wait expired");
   if (word & 2u) return fail(MX_ERR_OFFSETS, "a kernel saw a malformed offsets segment");
   if (word & 4u) return fail(MX_ERR_INVALID_ARG, "a routing index (expert id or routed row) was out of range");

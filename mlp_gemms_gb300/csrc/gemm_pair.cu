@@ -1,0 +1,324 @@
+// The grouped block-scaled GEMM on CTA pairs (tcgen05 .cta_group::2), BF16
+// out: y[r, :] = A[r, :] B[g]^T for the rows r of expert g's segment.
+//
+// torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP fwd/bwd and wgrad
+// group gemm", cudnn-fe ops commit: its kernels take 256-row MMA tiles on
+// two SMs and need every expert's segment to be a multiple of 256 rows.
+//
+// A pair of CTAs (a cluster of two) takes a 256 x 256 output tile: each CTA
+// loads its own 128 rows of A and its own half (128 rows) of the tile's B
+// slice, plus the scale chunks of its A rows and of all 256 B rows, by 2-SM
+// TMA loads whose bytes are all counted on the leader CTA's stage barrier.
+// The leader's MMA thread issues tcgen05.mma .cta_group::2 (M = 256, N = 256,
+// K = 32), each CTA's tensor memory holding its 128 x 256 fp32 accumulator,
+// and its commits arrive on both CTAs' barriers.  Each CTA's eight epilogue
+// warps read their accumulator, hand it back to the leader (a remote arrive
+// on the leader's barrier) and store BF16 by TMA.  Tensor memory is
+// allocated by both CTAs collectively (.cta_group::2 returns the same
+// columns in both, checked on the device before this kernel was written).
+// Every wait is bounded; on expiry the CTA records a device status bit and
+// unwinds.  No TMA multicast.
+#include "gemm_kernel.cuh"
+
+namespace mx {
+
+static __device__ unsigned g_pair_status = 0;
+
+namespace pair {
+constexpr int ST = 6;                                 // 33.5 KB stages
+constexpr int A_BYTES = 16384, B_BYTES = 16384, SF_BYTES = 1536;
+constexpr int OFF_B = ST * A_BYTES;
+constexpr int OFF_SF = OFF_B + ST * B_BYTES;
+constexpr int OFF_BAR = OFF_SF + ST * SF_BYTES;
+constexpr int NUM_BARS = 2 * ST + 3;                  // full, empty, acc_full, acc_empty, final
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;      // tmem slot, abort flag
+constexpr int OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;  // eight 2 KB staging buffers
+constexpr int SMEM = OFF_STG + 8 * 2048 + 1024;       // + slack for 1024-byte alignment
+constexpr int THREADS = 320;                          // producer, MMA, 8 epilogue warps
+constexpr uint32_t SF_TMEM = 256;                     // scale slots after the accumulator
+static_assert(SMEM <= 232448, "shared memory per CTA");
+static_assert(SF_TMEM + ST * 12 <= 512, "scale slots must fit");
+}  // namespace pair
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The leader CTA's (rank 0) shared::cluster address of a local shared address.
+__device__ __forceinline__ uint32_t leader_addr(const void* p) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bounded wait with cluster-scope acquire (the barrier's arrivals come from
+// both CTAs of the pair).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (true) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    if (ok) return true;
+    if ((++n & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) { *abort_flag = 1; return false; }
+    }
+  }
+}
+__device__ __forceinline__ void arrive_on_leader(uint32_t bar_cl) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cl) : "memory");
+}
+// 2-SM TMA loads: destination in this CTA's shared memory, completion bytes
+// counted on the (leader's) barrier at shared::cluster address bar_cl.
+__device__ __forceinline__ void tma2_load_2d(void* dst, const CUtensorMap* m, int c0, int c1, uint32_t bar_cl,
+                                             uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+               " [%0], [%1, {%2, %3}], [%4], %5;"
+               :: "r"(smem_u32(dst)), "l"(m), "r"(c0), "r"(c1), "r"(bar_cl), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma2_load_3d(void* dst, const CUtensorMap* m, int c0, int c1, int c2, uint32_t bar_cl) {
+  asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+               " [%0], [%1, {%2, %3, %4}], [%5];"
+               :: "r"(smem_u32(dst)), "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cl) : "memory");
+}
+__device__ __forceinline__ void tc2_copy_scales(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc2_mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                           uint32_t sfb, uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
+// Arrive on the barrier at this shared offset in both CTAs once every
+// tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void tc2_commit_both(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+               :: "r"(smem_u32(bar)), "h"((uint16_t)3) : "memory");
+}
+__device__ __forceinline__ void tc2_commit_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+struct PairTile {
+  int active, g;
+  int64_t m0, n0;
+};
+
+// Pair tile t -> (expert, row base of the 256-row block, column base).  The
+// expert is the segment holding the row base; a segment that is not a
+// multiple of 256 rows (or runs past R) makes the tile inactive and, when
+// `report`, sets the malformed-offsets status bit.
+__device__ __forceinline__ PairTile get_pair_tile(const PairParams& p, int64_t t, bool report) {
+  PairTile T;
+  T.active = 0; T.g = 0;
+  T.m0 = (t / p.n_tiles) * 256;
+  T.n0 = (t % p.n_tiles) * 256;
+  const int64_t total = p.offsets ? ldg_i32(p.offsets + p.G - 1) : p.R;
+  if (T.m0 >= total) return T;
+  int lo = 0;
+  if (p.offsets) {
+    int hi = p.G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)ldg_i32(p.offsets + mid) > T.m0) hi = mid; else lo = mid + 1;
+    }
+  }
+  const int64_t end = p.offsets ? ldg_i32(p.offsets + lo) : p.R;
+  const int64_t start = (p.offsets && lo) ? ldg_i32(p.offsets + lo - 1) : 0;
+  if ((start & 255) || (end & 255) || start > T.m0 || end <= T.m0 || end > p.R || total > p.R) {
+    if (report) atomicOr(&g_pair_status, DEV_BAD_OFFSETS);
+    return T;
+  }
+  T.g = lo;
+  T.active = 1;
+  return T;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
+mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                    const __grid_constant__ CUtensorMap tmO, const PairParams p) {
+  using namespace pair;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // leader's: both CTAs' bytes of a stage
+  uint64_t* empty = full + ST;                                   // both CTAs: the stage's MMAs are done
+  uint64_t* acc_full = empty + ST;                               // both CTAs: the tile's MMAs are done
+  uint64_t* acc_empty = acc_full + 1;                            // leader's: 16 epilogue warps have read
+  uint64_t* final_bar = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 16);
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); prefetch_tensormap(&tmSA); prefetch_tensormap(&tmSB);
+    prefetch_tensormap(&tmO);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(smem_u32(tmem_slot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive or copy
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int64_t pidx = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int nk = (int)(p.K / 128);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_a = l2_policy_evict_normal(), pol_b = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[ST];
+      for (int s = 0; s < ST; s++) armed[s] = -1;
+      bool ok = true;
+      for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
+        const PairTile T = get_pair_tile(p, t, false);
+        if (!T.active) continue;
+        const int64_t brow = (int64_t)T.g * p.Nb + T.n0;
+        for (int kb = 0; kb < nk; kb++) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          const uint32_t fb = leader_addr(&full[stage]);
+          if (leader) {
+            mbar_arrive_expect_tx(&full[stage], 2u * p.tx_bytes);
+            armed[stage] = (int)phase;
+          }
+          tma2_load_2d(smem + stage * A_BYTES, &tmA, kb * 128, (int)(T.m0 + 128 * rank), fb, pol_a);
+          tma2_load_2d(smem + OFF_B + stage * B_BYTES, &tmB, kb * 128, (int)(brow + 128 * rank), fb, pol_b);
+          uint8_t* sf = smem + OFF_SF + stage * SF_BYTES;
+          tma2_load_3d(sf, &tmSA, 0, kb, (int)((T.m0 >> 7) + rank), fb);
+          tma2_load_3d(sf + 512, &tmSB, 0, kb, (int)(brow >> 7), fb);
+          if (++stage == ST) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // The leader's stage barriers count both CTAs' copies: every copy has
+      // landed once they complete (the drain ignores the abort flag).
+      if (leader) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < ST; s++)
+          if (armed[s] >= 0) mbar_wait_bounded(&full[s], (uint32_t)armed[s], &no_abort, WAIT_BUDGET_NS);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && leader) {
+      const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, 2);
+      const uint64_t sf_desc0 = smem_desc(smem_u32(smem + OFF_SF), 0, 128, 0);
+      const uint32_t idesc0 = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 256, 256, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
+        const PairTile T = get_pair_tile(p, t, false);
+        if (!T.active) continue;
+        if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < nk; kb++) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + SF_TMEM + (uint32_t)(stage * 12);
+          const uint64_t sd = sf_desc0 + (uint64_t)((stage * SF_BYTES) >> 4);
+          tc2_copy_scales(sf_t, sd);                   // A's 128 rows (each CTA its own)
+          tc2_copy_scales(sf_t + 4, sd + (512 >> 4));  // B rows 0..127 of the tile
+          tc2_copy_scales(sf_t + 8, sd + (1024 >> 4)); // B rows 128..255
+          const uint64_t ad = a_desc0 + (uint64_t)((stage * A_BYTES) >> 4);
+          const uint64_t bd = b_desc0 + (uint64_t)((stage * B_BYTES) >> 4);
+#pragma unroll
+          for (int j = 0; j < 4; j++)
+            tc2_mma_mx(tmem_base, ad + 2 * j, bd + 2 * j, idesc0 | ((uint32_t)j << 4) | ((uint32_t)j << 29), sf_t,
+                       sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+          tc2_commit_both(&empty[stage]);
+          if (++stage == ST) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc2_commit_both(acc_full);
+        acc_phase ^= 1u;
+      }
+      if (!ok) *abort_flag = 1;
+      // No MMA may still be writing either CTA's tensor memory when it is freed.
+      volatile int no_abort = 0;
+      tc2_commit_local(final_bar);
+      mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;            // tensor-memory lane quarter
+    const int half = (warp - 2) >> 2;  // column half of the 256-column tile
+    uint8_t* stg = smem + OFF_STG + (warp - 2) * 2048;
+    const uint32_t acc_empty_cl = leader_addr(acc_empty);
+    const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
+    uint32_t acc_phase = 0;
+    for (int64_t t = pidx; t < p.num_tiles; t += npairs) {
+      const PairTile T = get_pair_tile(p, t, leader && warp == 2 && lane == 0);
+      if (!T.active) continue;
+      if (!mbar_wait_bounded(acc_full, acc_phase, abort_flag, WAIT_BUDGET_NS)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; c++) tmem_ld32(tbase + 32 * c, v[c]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_on_leader(acc_empty_cl);
+      const int64_t row0 = T.m0 + 128 * rank + q * 32;
+#pragma unroll
+      for (int c = 0; c < 4; c++) {
+        stage_reuse_wait(lane);
+        store_bf16_block(reinterpret_cast<const float*>(v[c]), stg, lane, &tmO, T.n0 + half * 128 + 32 * c, row0);
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_pair_status, DEV_TIMEOUT);
+  cluster_sync_all();  // neither CTA frees tensor memory or exits while the other still uses the pair
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, 512;" :: "r"(tmem_base) : "memory");
+  cluster_sync_all();
+}
+
+cudaError_t launch_gemm_pair(const PairParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                             const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to, cudaStream_t s,
+                             int num_sms) {
+  {
+    const cudaError_t e = ensure_smem_attr<mx_gemm_pair_kernel>(pair::SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  int64_t pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
+  if (pairs < 1) pairs = 1;
+  mx_gemm_pair_kernel<<<(unsigned)(2 * pairs), pair::THREADS, pair::SMEM, s>>>(ta, tb, tsa, tsb, to, p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_pair_status(unsigned* out) { return cudaMemcpyFromSymbol(out, g_pair_status, sizeof(unsigned)); }
+cudaError_t reset_pair_status() {
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_pair_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace mx

@@ -116,6 +116,21 @@ cudaError_t launch_colsum_reduce(const float* partials, int64_t tiles, int64_t c
 // (r < offsets[G-1], or all R rows without offsets); other rows untouched.
 cudaError_t launch_dprobs_reduce(const float* part, int64_t R, int64_t ld, const int32_t* offsets, int G,
                                  float* dprobs, cudaStream_t s);
+// The CTA-pair grouped GEMM (gemm_pair.cu): 256 x 256 tiles on two SMs,
+// BF16 out through a [R, Nb] tensor map; segments multiples of 256 rows.
+struct PairParams {
+  int G;
+  const int32_t* offsets;  // device [G], cumulative segment ends (NULL: one segment of R rows)
+  int64_t R, K, Nb;        // A [R, K], B [G * Nb, K]
+  int a_type, b_type;      // MMA element types
+  int64_t n_tiles, num_tiles;  // 256-column tiles per row block; pair tiles in all
+  uint32_t tx_bytes;       // one CTA's bytes per stage (A and B boxes, scale chunks)
+};
+cudaError_t launch_gemm_pair(const PairParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                             const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to, cudaStream_t s,
+                             int num_sms);
+cudaError_t read_pair_status(unsigned* out);
+cudaError_t reset_pair_status();
 cudaError_t read_gemm_status(unsigned* out);
 cudaError_t reset_gemm_status();
 cudaError_t read_dense_status(unsigned* out);
@@ -128,7 +143,7 @@ cudaError_t reset_f4_status();
 // Token permute support (permute.cu).  counts: the workspace, int32
 // [G, ceil(T*k / 1024)] (expert-major).
 cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int32_t* offsets, int32_t* src,
-                               int64_t R_cap, int32_t* row_of, int32_t* counts, cudaStream_t s);
+                               int64_t R_cap, int32_t* row_of, int32_t* counts, int32_t pad, cudaStream_t s);
 cudaError_t launch_unpermute(const uint16_t* in, int64_t R, int64_t D, const int32_t* row_of, const float* w,
                              int64_t T, int k, uint16_t* out, int num_sms, cudaStream_t s);
 cudaError_t read_perm_status(unsigned* out);

@@ -1,5 +1,5 @@
 // Token permute support for the expert MLP: the routing index (top-k expert
-// ids -> 128-row padded expert segments, the source token of every routed
+// ids -> 128- (or 256-) row padded expert segments, the source token of every routed
 // row and the routed row of every (token, choice)) and the un-permute (the
 // weighted sum of a token's routed rows).  Primus PR #1247 "Qwen3-30B-A3B
 // FP8 on MI355X to 40k tokens/s/GPU", DeepEP permute section: the permute
@@ -9,7 +9,7 @@
 //
 // Order of the routed rows: experts ascending; within an expert, (token,
 // choice) ascending; each segment padded with empty rows (source -1) to a
-// multiple of 128.  Built as a stable counting sort with no floating point
+// multiple of 128 (256 for the CTA-pair GEMM).  Built as a stable counting sort with no floating point
 // and no order-dependent atomics, so the index is deterministic.
 #include "mx_common.cuh"
 #include "mx_internal.h"
@@ -43,7 +43,7 @@ __global__ void route_count_kernel(const int32_t* __restrict__ topk, int64_t n, 
 // padded segment ends go to offsets; padding rows and the rows past the
 // last segment get source -1.
 __global__ void route_scan_kernel(int32_t* __restrict__ counts, int nchunks, int G, int32_t* __restrict__ offsets,
-                                  int32_t* __restrict__ src, int64_t R_cap) {
+                                  int32_t* __restrict__ src, int64_t R_cap, int32_t pad) {
   __shared__ int32_t tot[1024];
   __shared__ int32_t first[1024];
   __shared__ int32_t end[1024];
@@ -85,7 +85,7 @@ __global__ void route_scan_kernel(int32_t* __restrict__ counts, int nchunks, int
   if (threadIdx.x == 0) {
     int32_t acc = 0;
     for (int e = 0; e < G; e++) {
-      const int32_t padded = (tot[e] + 127) & ~127;
+      const int32_t padded = (tot[e] + pad - 1) / pad * pad;
       first[e] = acc;
       acc += padded;
       end[e] = acc;
@@ -139,7 +139,7 @@ __global__ void route_scatter_kernel(const int32_t* __restrict__ topk, int64_t n
 }
 
 cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int32_t* offsets, int32_t* src,
-                               int64_t R_cap, int32_t* row_of, int32_t* counts, cudaStream_t s) {
+                               int64_t R_cap, int32_t* row_of, int32_t* counts, int32_t pad, cudaStream_t s) {
   const int64_t n = T * k;
   const int nchunks = (int)((n + ROUTE_CHUNK - 1) / ROUTE_CHUNK);
   const size_t hist = (size_t)G * sizeof(int32_t);
@@ -148,7 +148,7 @@ cudaError_t launch_route_index(const int32_t* topk, int64_t T, int k, int G, int
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  route_scan_kernel<<<1, 1024, 0, s>>>(counts, nchunks, G, offsets, src, R_cap);
+  route_scan_kernel<<<1, 1024, 0, s>>>(counts, nchunks, G, offsets, src, R_cap, pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nchunks == 0) return e;
   route_scatter_kernel<<<nchunks, 32, hist, s>>>(topk, n, k, G, nchunks, counts, src, row_of);

@@ -209,3 +209,19 @@ def test_noalloc_rejects_overflowing_sizes_before_any_device_call(mx):
                                           FAKE, None)
         assert mx.STATUS[st] == "MX_ERR_WORKSPACE", (rows, cols)
         assert "scratch" in mx.mx_last_error()
+
+
+def test_pair_gemm_rejections(mx):
+    """mx_grouped_gemm_2sm: host checks before any device work."""
+    L = mx.load()
+    a, b = _t(512, 256), _t(384, 256)
+    st = L.mx_grouped_gemm_2sm(ctypes.byref(a), ctypes.byref(b), 1, FAKE, FAKE, 384, None)
+    assert mx.STATUS[st] == "MX_ERR_SHAPE" and "256" in mx.mx_last_error()
+    a4, b4 = _t(512, 256, fmt=2), _t(512, 256, fmt=2)
+    st = L.mx_grouped_gemm_2sm(ctypes.byref(a4), ctypes.byref(b4), 1, FAKE, FAKE, 512, None)
+    assert mx.STATUS[st] == "MX_ERR_NOT_SUPPORTED"
+    a3, b3 = _t(384, 256), _t(256, 256)
+    st = L.mx_grouped_gemm_2sm(ctypes.byref(a3), ctypes.byref(b3), 1, None, FAKE, 256, None)
+    assert mx.STATUS[st] == "MX_ERR_SHAPE" and "without offsets" in mx.mx_last_error()
+    assert L.mx_moe_route_rows_pad(100, 8, 4, 256) == (800 + 255 * 4 + 255) // 256 * 256
+    assert L.mx_moe_route_rows_pad(100, 8, 4, 200) == 0
