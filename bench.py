@@ -336,6 +336,7 @@ def run_gpu(args):
     fwd_even = moe_forward_even_rate(mx, torch, dev) if not args.no_extra else None
     variants = variant_rates(mx, torch, dev) if not args.no_extra else None
     mxfp4 = mxfp4_gemm_rate(mx, torch, dev) if not args.no_extra else None
+    pairs = pair_gemm_rates(mx, torch, dev) if not args.no_extra else None
     permute = permute_rates(mx, torch, dev) if not args.no_extra else None
     status = mx.mx_get_device_status()
     if status != "MX_OK":
@@ -392,6 +393,8 @@ def run_gpu(args):
                    "quantizer_mxfp8_us": round(quant["us"], 2),
                    "quantizer_mxfp8_frac_of_hbm": round(quant["frac_of_hbm"], 4),
                    "step_graph_ms": round(graph_ms, 4),
+                   "pair_gemm_ms": None if pairs is None else {k: round(v["ms"], 4) for k, v in pairs.items()
+                                                               if isinstance(v, dict)},
                    "host_us_per_step": round(host_us_per_step, 1),
                    "dense_mxfp6_step_ms": None if dense is None else round(dense["ms_per_step"], 4),
                    "dense_mxfp6_frac_of_fp8_peak": None if dense is None else round(dense["frac_of_fp8_peak"], 4)},
@@ -405,6 +408,7 @@ def run_gpu(args):
         "moe_fwd_even_routing": fwd_even,
         "variants": variants,
         "mxfp4_gemm": mxfp4,
+        "pair_gemm": pairs,
         "moe_permute": permute,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -774,6 +778,48 @@ def variant_rates(mx, torch, dev, reps=20):
     status = mx.mx_get_device_status()
     if status != "MX_OK":
         raise RuntimeError("device status after variants: " + status)
+    return res
+
+
+def pair_gemm_rates(mx, torch, dev, reps=20):
+    """The plain grouped GEMMs of the step (FC2: y = h W2[g]^T, FC1 dgrad:
+    dX = dz W1[g]) at the MoE shape on Zipf(1.1) routing counted in 256-row
+    tiles (every segment a multiple of 256), through the single-SM kernel
+    and through the CTA-pair kernel (mx_grouped_gemm_2sm) on the same
+    operands: median CUDA-event times of interleaved launches."""
+    import workloads as W
+    G, D, F, R = SHAPE["G"], SHAPE["D"], SHAPE["F"], SHAPE["R"]
+    offs = torch.from_numpy(W.offsets_from_counts(W.zipf_counts(G, R, tile=256))).to(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    rnd = lambda shape, std: (torch.randn(shape, generator=g, device=dev) * std).to(torch.bfloat16)
+    hr, _, _ = mx.mx_quantize(rnd((R, F), 0.5), mx.E4M3, True, False)
+    w2r, _, _ = mx.mx_quantize(rnd((G, D, F), 0.02), mx.E4M3, True, False)
+    dzr, _, _ = mx.mx_quantize(rnd((R, 2 * F), 1e-3), mx.E4M3, True, False)
+    w1tr, _, _ = mx.mx_quantize(rnd((G, D, 2 * F), 0.02), mx.E4M3, True, False)
+    out = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    calls = {
+        "fc2": lambda: mx.mx_grouped_gemm(hr, w2r, G, offs, out=out),
+        "fc2_2sm": lambda: mx.mx_grouped_gemm_2sm(hr, w2r, G, offs, out=out),
+        "fc1_dgrad": lambda: mx.mx_grouped_gemm(dzr, w1tr, G, offs, out=out),
+        "fc1_dgrad_2sm": lambda: mx.mx_grouped_gemm_2sm(dzr, w1tr, G, offs, out=out),
+    }
+    stream = torch.cuda.current_stream(dev)
+    for c in calls.values():
+        c()
+    torch.cuda.synchronize(dev)
+    samples = {k: [] for k in calls}
+    for _ in range(reps):
+        for k, c in calls.items():
+            samples[k].append(_event_median(torch, stream, dev, c, 1))
+    status = mx.mx_get_device_status()
+    if status != "MX_OK":
+        raise RuntimeError("device status after the pair GEMMs: " + status)
+    sf = stage_flops(D, F, R)
+    res = {"workload": "MoE shape, Zipf(1.1) routing in 256-row tiles; single-SM vs CTA-pair kernel"}
+    for k, v in samples.items():
+        ms = float(np.median(v))
+        res[k] = {"ms": ms, "tflops": sf[k.replace("_2sm", "")] / (ms * 1e-3) / 1e12}
     return res
 
 
