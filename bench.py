@@ -837,15 +837,29 @@ def mxfp4_gemm_rate(mx, torch, dev, reps=20):
     del a, b
     out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    single = lambda: mx.mx_gemm_bias(ar, br, None, out=out)
+    pair = lambda: mx.mx_grouped_gemm_2sm(ar, br, 1, None, out=out)   # the same product on CTA pairs
     for _ in range(3):
-        mx.mx_gemm_bias(ar, br, None, out=out)
+        single()
+        pair()
     torch.cuda.synchronize(dev)
-    ms = _event_median(torch, stream, dev, lambda: mx.mx_gemm_bias(ar, br, None, out=out), reps)
+    ts = {"single": [], "pair": []}
+    for _ in range(reps):
+        ts["single"].append(_event_median(torch, stream, dev, single, 1))
+        ts["pair"].append(_event_median(torch, stream, dev, pair, 1))
+    status = mx.mx_get_device_status()
+    if status != "MX_OK":
+        raise RuntimeError("device status after the MXFP4 GEMMs: " + status)
     peaks, kind = measured_peaks()
-    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     peak_fp4 = 6.0 * peaks["bf16_tflops"]
+    ms = float(np.median(ts["single"]))
+    ms2 = float(np.median(ts["pair"]))
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    tf2 = 2.0 * M * N * K / (ms2 * 1e-3) / 1e12
     return {"workload": "dense mxfp4-e2m1 GEMM 16384x12288x3072 (tcgen05 kind::mxf4)", "ms": ms, "tflops": tf,
             "peak_fp4_tflops": peak_fp4, "frac_of_fp4_peak": tf / peak_fp4,
+            "pair": {"ms": ms2, "tflops": tf2, "frac_of_fp4_peak": tf2 / peak_fp4,
+                     "kernel": "mx_grouped_gemm_2sm (tcgen05 .cta_group::2 .kind::mxf4, 256x256 tiles)"},
             "peak_kind": kind + " bf16 burst x 6 (nominal fp4/bf16 ratio)"}
 
 
@@ -967,7 +981,8 @@ def ncu_case(name, launches=3):
     'quant' is the standalone quantizer workload (8192 x 7168) ('quant_sr' /
     'quant_e2m1' the same to MXFP4 with stochastic / nearest rounding),
     'permute' the quantizing permute of 8192 tokens (top-8 of 128 experts,
-    D = 2048), 'mxfp4_gemm' a dense E2M1 GEMM 8192 x 12288 x 3072,
+    D = 2048), 'mxfp4_gemm' a dense E2M1 GEMM 8192 x 12288 x 3072 ('mxfp4_gemm_2sm'
+    the same on CTA pairs),
     'dense_gelu' / 'dense_dgelu' the dense MXFP6 + rotation FC1 + GELU and
     FC2 dgrad + dGELU stages at M = 8192, D = 3072, H = 12288 (the dGELU
     case on a random saved pre-activation, so its GEMM launches are the only
@@ -987,13 +1002,14 @@ def ncu_case(name, launches=3):
         r, c = mx.MX(8192, 7168, mx.E2M1), mx.MX(7168, 8192, mx.E2M1)
         run = (lambda: mx.mx_quantize_sr(x, mx.E2M1, 7, True, True, out_row=r, out_col=c)) if name == "quant_sr" \
             else (lambda: mx.mx_quantize(x, mx.E2M1, True, True, out_row=r, out_col=c))
-    elif name == "mxfp4_gemm":  # dense E2M1 GEMM 8192 x 12288 x 3072 (~0.5 GB on the device)
+    elif name in ("mxfp4_gemm", "mxfp4_gemm_2sm"):  # dense E2M1 GEMM 8192 x 12288 x 3072 (~0.5 GB on the device)
         a = torch.randn((8192, 3072), device=dev).to(torch.bfloat16)
         b = (torch.randn((12288, 3072), device=dev) * 0.02).to(torch.bfloat16)
         ar, _, _ = mx.mx_quantize(a, mx.E2M1, True, False)
         br, _, _ = mx.mx_quantize(b, mx.E2M1, True, False)
         out = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
-        run = lambda: mx.mx_gemm_bias(ar, br, None, out=out)
+        run = (lambda: mx.mx_gemm_bias(ar, br, None, out=out)) if name == "mxfp4_gemm" \
+            else (lambda: mx.mx_grouped_gemm_2sm(ar, br, 1, None, out=out))
     elif name in ("dense_gelu", "dense_dgelu"):  # M = 8192, D = 3072, H = 12288 (~0.6 GB on the device)
         M, D, H = 8192, 3072, 12288
         g = torch.Generator(device=dev)

@@ -321,8 +321,11 @@ MX_API mx_status_t mx_grouped_gemm(const mx_tensor_t *a, const mx_tensor_t *b, i
  * loading its 128 rows of A and half of the tile's B slice ([MXFP8-PR]
  * cudnn-fe ops commit: 256-row MMA tiles and 256-row segment alignment).
  * Same arguments and output as mx_grouped_gemm, with:
- *   a, b     E4M3 or E2M3 (E2M1: MX_ERR_NOT_SUPPORTED); N = b->rows / G a
- *            multiple of 256 (else MX_ERR_SHAPE)
+ *   a, b     E4M3, E2M3 (.kind::mxf8f6f4, K = 32 per MMA) or packed E2M1
+ *            (.kind::mxf4, K = 64 per MMA; ROCm Primus guide "MXFP4
+ *            training for Flux models", backends section: FP4 GEMMs at
+ *            twice the FP8 rate); N = b->rows / G a multiple of 256 (else
+ *            MX_ERR_SHAPE)
  *   offsets  every segment a multiple of 256 rows (mx_moe_route_index_pad
  *            with pad 256 builds such a routing); a segment that is not is
  *            skipped on the device and reported as MX_ERR_OFFSETS by

@@ -195,16 +195,16 @@ mx_status_t make_tmap_out_f32(CUtensorMap* m, const void* base, int64_t rows, in
 }
 
 // Blocked scales of a [rows, K] MX tensor as [row blocks][K chunks][512
-// bytes] (64 x 8-byte elements per chunk), boxes of one chunk x `blocks`
-// consecutive row blocks: the CTA-pair GEMM loads a stage's scale chunks
-// with the 2-SM TMA form.
-mx_status_t make_tmap_scales(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int blocks) {
+// bytes] (64 x 8-byte elements per chunk), boxes of `chunks` consecutive
+// chunks x `blocks` consecutive row blocks: the CTA-pair GEMM loads a
+// stage's scale chunks with the 2-SM TMA form.
+mx_status_t make_tmap_scales(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int blocks, int chunks) {
   mx_status_t st = get_encoder();
   if (st != MX_OK) return st;
   const int64_t kchunks = (k / 32 + 3) / 4, rblocks = (rows + 127) / 128;
   cuuint64_t dims[3] = {64, (cuuint64_t)kchunks, (cuuint64_t)rblocks};
   cuuint64_t strides[2] = {512, (cuuint64_t)(kchunks * 512)};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)blocks};
+  cuuint32_t box[3] = {64, (cuuint32_t)chunks, (cuuint32_t)blocks};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -763,7 +763,6 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
   if ((st = check_gemm_operand(b, "b")) != MX_OK) return st;
   if ((st = check_pair(a, b, "a", "b")) != MX_OK) return st;
-  MX_CHECK(a->fmt != MX_E2M1, MX_ERR_NOT_SUPPORTED, "the CTA-pair GEMM runs E4M3 and E2M3 operands");
   MX_CHECK(G >= 1, MX_ERR_INVALID_ARG, "G = %d; at least one expert is required", G);
   MX_CHECK(a->cols == b->cols, MX_ERR_SHAPE, "a has K = %lld, b has K = %lld", (long long)a->cols, (long long)b->cols);
   const int64_t K = a->cols, R = a->rows;
@@ -790,15 +789,25 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
   p.n_tiles = N / 256;
   p.num_tiles = (R + 255) / 256 * p.n_tiles;
-  p.tx_bytes = stage_tx_bytes(a->fmt, 128) + 512u;  // 128 A rows, 128 B rows, A's chunk and both B chunks
+  // E2M1 runs on .kind::mxf4 from the packed payload: a stage is 128 bytes
+  // (256 elements) of each row and two scale chunks, every box counted whole
+  // (past K it is zero-filled).
+  p.f4 = a->fmt == MX_E2M1 ? 1 : 0;
+  const int kc = p.f4 ? 2 : 1;
+  // one CTA's stage: 128 A rows, 128 B rows, A's chunks and both B row blocks' chunks
+  p.tx_bytes = p.f4 ? 2u * 16384u + 3u * 1024u : stage_tx_bytes(a->fmt, 128) + 512u;
   CUtensorMap ta, tb, tsa, tsb, to;
-  if ((st = make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK) return st;
-  if ((st = make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK) return st;
-  if ((st = make_tmap_scales(&tsa, a->scale, a->rows, K, 1)) != MX_OK) return st;
-  if ((st = make_tmap_scales(&tsb, b->scale, b->rows, K, 2)) != MX_OK) return st;
+  if ((st = p.f4 ? make_tmap_packed(&ta, a->data, a->rows, a->cols)
+                 : make_tmap(&ta, a->data, a->rows, a->cols, a->fmt)) != MX_OK)
+    return st;
+  if ((st = p.f4 ? make_tmap_packed(&tb, b->data, b->rows, b->cols)
+                 : make_tmap(&tb, b->data, b->rows, b->cols, b->fmt)) != MX_OK)
+    return st;
+  if ((st = make_tmap_scales(&tsa, a->scale, a->rows, K, 1, kc)) != MX_OK) return st;
+  if ((st = make_tmap_scales(&tsb, b->scale, b->rows, K, 2, kc)) != MX_OK) return st;
   if ((st = make_tmap_out(&to, out_bf16, R, N, ld_out)) != MX_OK) return st;
-  log_config("gemm pair bf16 BN=256 a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld", p.a_type, p.b_type,
-             (long long)R, (long long)K, (long long)N, G, (long long)p.num_tiles);
+  log_config("gemm pair bf16 BN=256%s a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld", p.f4 ? " mxf4" : "",
+             p.a_type, p.b_type, (long long)R, (long long)K, (long long)N, G, (long long)p.num_tiles);
   cudaError_t e = mx::launch_gemm_pair(p, ta, tb, tsa, tsb, to, s, dev.sms);
   if (e != cudaSuccess) return cuda_fail(e, "CTA-pair GEMM launch");
   return MX_OK;

@@ -10,7 +10,9 @@
 // slice, plus the scale chunks of its A rows and of all 256 B rows, by 2-SM
 // TMA loads whose bytes are all counted on the leader CTA's stage barrier.
 // The leader's MMA thread issues tcgen05.mma .cta_group::2 (M = 256, N = 256,
-// K = 32), each CTA's tensor memory holding its 128 x 256 fp32 accumulator,
+// K = 32 on .kind::mxf8f6f4; K = 64 on .kind::mxf4 for packed E2M1 operands,
+// whose stages hold 256 K-elements and two scale chunks), each CTA's tensor
+// memory holding its 128 x 256 fp32 accumulator,
 // and its commits arrive on both CTAs' barriers.  Each CTA's eight epilogue
 // warps read their accumulator, hand it back to the leader (the peer's by
 // one remote arrive on the leader's barrier) and store BF16 by TMA.  Tensor memory is
@@ -25,19 +27,27 @@ namespace mx {
 static __device__ unsigned g_pair_status = 0;
 
 namespace pair {
-constexpr int ST = 6;                                 // 33.5 KB stages
-constexpr int A_BYTES = 16384, B_BYTES = 16384, SF_BYTES = 1536;
-constexpr int OFF_B = ST * A_BYTES;
-constexpr int OFF_SF = OFF_B + ST * B_BYTES;
-constexpr int OFF_BAR = OFF_SF + ST * SF_BYTES;
-constexpr int NUM_BARS = 2 * ST + 4;                  // full, empty, acc_full, acc_empty, final, peer_read
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;      // tmem slot, abort flag
-constexpr int OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;  // eight 2 KB staging buffers
-constexpr int SMEM = OFF_STG + 8 * 2048 + 1024;       // + slack for 1024-byte alignment
 constexpr int THREADS = 320;                          // producer, MMA, 8 epilogue warps
 constexpr uint32_t SF_TMEM = 256;                     // scale slots after the accumulator
-static_assert(SMEM <= 232448, "shared memory per CTA");
-static_assert(SF_TMEM + ST * 12 <= 512, "scale slots must fit");
+// F4: packed E2M1 operands on .kind::mxf4 -- a stage's 128-byte rows hold
+// 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
+template <bool F4> struct PCfg {
+  static constexpr int KC = F4 ? 2 : 1;
+  static constexpr int ST = F4 ? 5 : 6;               // 33.5 KB (35 KB with F4) stages
+  static constexpr int A_BYTES = 16384, B_BYTES = 16384;
+  // A's KC chunks, then B's two row blocks of KC chunks each
+  static constexpr int SF_BYTES = KC * 1536;
+  static constexpr int SF_COLS = KC * 12;             // tensor-memory columns of a stage's scales
+  static constexpr int OFF_B = ST * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + ST * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + ST * SF_BYTES;
+  static constexpr int NUM_BARS = 2 * ST + 4;         // full, empty, acc_full, acc_empty, final, peer_read
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem slot, abort flag
+  static constexpr int OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;  // eight 2 KB staging buffers
+  static constexpr int SMEM = OFF_STG + 8 * 2048 + 1024;  // + slack for 1024-byte alignment
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(SF_TMEM + ST * SF_COLS <= 512, "scale slots must fit");
+};
 }  // namespace pair
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -96,6 +106,12 @@ __device__ __forceinline__ void tc2_mma_mx(uint32_t d, uint64_t a, uint64_t b, u
                "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
                :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
+__device__ __forceinline__ void tc2_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                             uint32_t sfb, uint32_t accumulate) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
 // Arrive on the barrier at this shared offset in both CTAs once every
 // tcgen05 operation this thread issued has completed.
 __device__ __forceinline__ void tc2_commit_both(uint64_t* bar) {
@@ -142,21 +158,26 @@ __device__ __forceinline__ PairTile get_pair_tile(const PairParams& p, int64_t t
   return T;
 }
 
+template <bool F4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
 mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                     const __grid_constant__ CUtensorMap tmO, const PairParams p) {
   using namespace pair;
+  using C = PCfg<F4>;
+  constexpr int ST = C::ST, KC = C::KC;
+  constexpr int A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, SF_BYTES = C::SF_BYTES;
+  constexpr int OFF_B = C::OFF_B, OFF_SF = C::OFF_SF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // leader's: both CTAs' bytes of a stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // leader's: both CTAs' bytes of a stage
   uint64_t* empty = full + ST;                                   // both CTAs: the stage's MMAs are done
   uint64_t* acc_full = empty + ST;                               // both CTAs: the tile's MMAs are done
   uint64_t* acc_empty = acc_full + 1;   // leader's: its 8 epilogue warps and the peer's hand-off have read
   uint64_t* final_bar = acc_empty + 1;
   uint64_t* peer_read = final_bar + 1;  // peer's: its 8 epilogue warps have read their accumulator
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,7 +205,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int64_t pidx = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int nk = (int)(p.K / 128);
+  const int nc = (int)(p.K / 128);        // 128-K scale chunks
+  const int nk = (nc + KC - 1) / KC;     // stages per tile
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -206,11 +228,14 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_arrive_expect_tx(&full[stage], 2u * p.tx_bytes);
             armed[stage] = (int)phase;
           }
+          // x: 128 elements (F4: 128 bytes = 256 packed elements) per stage.
+          // F4's last stage of an odd chunk count reads its second half past
+          // K: zero-filled and counted like the rest of the box, read by no MMA.
           tma2_load_2d(smem + stage * A_BYTES, &tmA, kb * 128, (int)(T.m0 + 128 * rank), fb, pol_a);
           tma2_load_2d(smem + OFF_B + stage * B_BYTES, &tmB, kb * 128, (int)(brow + 128 * rank), fb, pol_b);
           uint8_t* sf = smem + OFF_SF + stage * SF_BYTES;
-          tma2_load_3d(sf, &tmSA, 0, kb, (int)((T.m0 >> 7) + rank), fb);
-          tma2_load_3d(sf + 512, &tmSB, 0, kb, (int)(brow >> 7), fb);
+          tma2_load_3d(sf, &tmSA, 0, kb * KC, (int)((T.m0 >> 7) + rank), fb);
+          tma2_load_3d(sf + KC * 512, &tmSB, 0, kb * KC, (int)(brow >> 7), fb);
           if (++stage == ST) { stage = 0; phase ^= 1u; }
         }
       }
@@ -228,7 +253,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, 2);
       const uint64_t sf_desc0 = smem_desc(smem_u32(smem + OFF_SF), 0, 128, 0);
-      const uint32_t idesc0 = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 256, 256, 0, 0);
+      const uint32_t idesc0 = F4 ? mma_idesc_mx(MXF4_E2M1, MXF4_E2M1, 256, 256, 0, 0)
+                                 : mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 256, 256, 0, 0);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -240,17 +266,41 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int kb = 0; kb < nk; kb++) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sf_t = tmem_base + SF_TMEM + (uint32_t)(stage * 12);
+          const uint32_t sf_t = tmem_base + SF_TMEM + (uint32_t)(stage * C::SF_COLS);
           const uint64_t sd = sf_desc0 + (uint64_t)((stage * SF_BYTES) >> 4);
-          tc2_copy_scales(sf_t, sd);                   // A's 128 rows (each CTA its own)
-          tc2_copy_scales(sf_t + 4, sd + (512 >> 4));  // B rows 0..127 of the tile
-          tc2_copy_scales(sf_t + 8, sd + (1024 >> 4)); // B rows 128..255
           const uint64_t ad = a_desc0 + (uint64_t)((stage * A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + (uint64_t)((stage * B_BYTES) >> 4);
+          if constexpr (F4) {
+            // tensor-memory scale columns: A's chunk c at 4c (each CTA its
+            // own rows), B's chunk c of row block i at 8 + 8c + 4i; shared
+            // memory holds A's chunks, then B's row blocks of two chunks
+            const int nch = (2 * kb + 1 < nc) ? 2 : 1;
 #pragma unroll
-          for (int j = 0; j < 4; j++)
-            tc2_mma_mx(tmem_base, ad + 2 * j, bd + 2 * j, idesc0 | ((uint32_t)j << 4) | ((uint32_t)j << 29), sf_t,
-                       sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+            for (int c = 0; c < 2; c++) {
+              if (c < nch) {
+                tc2_copy_scales(sf_t + 4 * c, sd + (uint64_t)((512 * c) >> 4));
+#pragma unroll
+                for (int i = 0; i < 2; i++)
+                  tc2_copy_scales(sf_t + 8 + 8 * c + 4 * i, sd + (uint64_t)((1024 + 512 * (2 * i + c)) >> 4));
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+              if (j < 2 * nch) {  // K = 64 per MMA; scale IDs 0 and 2 pick the chunk's byte pair
+                const uint32_t sid = (uint32_t)(j & 1) * 2u;
+                tc2_mma_mxf4(tmem_base, ad + 2 * j, bd + 2 * j, idesc0 | (sid << 4) | (sid << 29),
+                             sf_t + 4 * (j >> 1), sf_t + 8 + 8 * (j >> 1), (kb | j) != 0 ? 1u : 0u);
+              }
+            }
+          } else {
+            tc2_copy_scales(sf_t, sd);                   // A's 128 rows (each CTA its own)
+            tc2_copy_scales(sf_t + 4, sd + (512 >> 4));  // B rows 0..127 of the tile
+            tc2_copy_scales(sf_t + 8, sd + (1024 >> 4)); // B rows 128..255
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+              tc2_mma_mx(tmem_base, ad + 2 * j, bd + 2 * j, idesc0 | ((uint32_t)j << 4) | ((uint32_t)j << 29), sf_t,
+                         sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+          }
           tc2_commit_both(&empty[stage]);
           if (++stage == ST) { stage = 0; phase ^= 1u; }
         }
@@ -268,7 +318,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;            // tensor-memory lane quarter
     const int half = (warp - 2) >> 2;  // column half of the 256-column tile
-    uint8_t* stg = smem + OFF_STG + (warp - 2) * 2048;
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * 2048;
     const uint32_t acc_empty_cl = leader_addr(acc_empty);
     const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
     uint32_t acc_phase = 0, peer_phase = 0;
@@ -321,13 +371,19 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 cudaError_t launch_gemm_pair(const PairParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                              const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to, cudaStream_t s,
                              int num_sms) {
-  {
-    const cudaError_t e = ensure_smem_attr<mx_gemm_pair_kernel>(pair::SMEM);
-    if (e != cudaSuccess) return e;
-  }
   int64_t pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
   if (pairs < 1) pairs = 1;
-  mx_gemm_pair_kernel<<<(unsigned)(2 * pairs), pair::THREADS, pair::SMEM, s>>>(ta, tb, tsa, tsb, to, p);
+  if (p.f4) {
+    constexpr int smem = pair::PCfg<true>::SMEM;
+    const cudaError_t e = ensure_smem_attr<mx_gemm_pair_kernel<true>>(smem);
+    if (e != cudaSuccess) return e;
+    mx_gemm_pair_kernel<true><<<(unsigned)(2 * pairs), pair::THREADS, smem, s>>>(ta, tb, tsa, tsb, to, p);
+  } else {
+    constexpr int smem = pair::PCfg<false>::SMEM;
+    const cudaError_t e = ensure_smem_attr<mx_gemm_pair_kernel<false>>(smem);
+    if (e != cudaSuccess) return e;
+    mx_gemm_pair_kernel<false><<<(unsigned)(2 * pairs), pair::THREADS, smem, s>>>(ta, tb, tsa, tsb, to, p);
+  }
   return cudaGetLastError();
 }
 

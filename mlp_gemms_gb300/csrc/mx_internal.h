@@ -125,6 +125,7 @@ struct PairParams {
   int a_type, b_type;      // MMA element types
   int64_t n_tiles, num_tiles;  // 256-column tiles per row block; pair tiles in all
   uint32_t tx_bytes;       // one CTA's bytes per stage (A and B boxes, scale chunks)
+  int f4;                  // packed E2M1 operands on .kind::mxf4 (256 K-elements a stage)
 };
 cudaError_t launch_gemm_pair(const PairParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                              const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to, cudaStream_t s,

@@ -136,3 +136,54 @@ def test_route_index_pads_to_256(cuda_lib):
     assert np.all(src.cpu().numpy()[R:] == -1)
     assert np.array_equal(row_of.cpu().numpy(), o_row)
     assert np.all(o_offs % 256 == 0)
+
+
+def test_pair_gemm_e2m1_exact_products(cuda_lib):
+    """Packed E2M1 operands on .kind::mxf4: integers in [-3, 3] times powers
+    of two quantize exactly to E2M1 and every partial sum is exact in fp32,
+    so the BF16 output equals the oracle's exact product rounded once, and
+    the single-SM kernel's bit for bit."""
+    import torch
+    mx = cuda_lib
+    G, N, K, R = 2, 256, 768, 512
+    offsets = W.offsets_from_counts([256, 256])
+    rng = np.random.default_rng(11)
+    a = rng.integers(-3, 4, size=(R, K)).astype(np.float32) * np.float32(2.0 ** -3)
+    b = rng.integers(-3, 4, size=(G, N, K)).astype(np.float32) * np.float32(2.0 ** 2)
+    ar, aref = _quant(mx, W.to_bf16_bits(a), O.E2M1)
+    br, bref = _quant(mx, W.to_bf16_bits(b), O.E2M1)
+    offs = torch.from_numpy(offsets).cuda()
+    pair = mx.mx_grouped_gemm_2sm(ar, br, G, offs)
+    single = mx.mx_grouped_gemm(ar, br, G, offs)
+    torch.cuda.synchronize()
+    assert mx.mx_get_device_status() == "MX_OK"
+    ref = O.grouped_gemm(_deq(aref, R, K, O.E2M1), _deq(bref, G * N, K, O.E2M1).reshape(G, N, K), offsets)
+    assert np.array_equal(bf16_cpu(pair), O.bf16_out(ref))
+    assert torch.equal(pair, single)
+
+
+@pytest.mark.parametrize("K", [640, 1024])
+def test_pair_gemm_e2m1_ragged(cuda_lib, K):
+    """E2M1 on random operands: segments of 512, 0 and 256 rows with a
+    NaN-poisoned inactive tail; K = 640 ends on half a stage (five 128-K
+    chunks), K = 1024 wraps the five-stage ring.  Bit-identical to the
+    single-SM .kind::mxf4 kernel and within tolerance of the oracle."""
+    import torch
+    mx = cuda_lib
+    G, N, R = 3, 512, 1024
+    offsets = W.offsets_from_counts([512, 0, 256])
+    A = int(offsets[-1])
+    rng = np.random.default_rng(K)
+    ar, aref = _quant(mx, W.normal_bf16(rng, (R, K)), O.E2M1)
+    br, bref = _quant(mx, W.normal_bf16(rng, (G, N, K), std=0.02), O.E2M1)
+    offs = torch.from_numpy(offsets).cuda()
+    pair = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.mx_grouped_gemm_2sm(ar, br, G, offs, out=pair)
+    single = mx.mx_grouped_gemm(ar, br, G, offs)
+    torch.cuda.synchronize()
+    assert mx.mx_get_device_status() == "MX_OK"
+    assert torch.equal(pair[:A], single[:A]), "pair and single-SM products differ"
+    got = bf16_cpu(pair)
+    ref = O.grouped_gemm(_deq(aref, R, K, O.E2M1), _deq(bref, G * N, K, O.E2M1).reshape(G, N, K), offsets)
+    assert O.within_tolerance(got[:A], ref[:A]).all()
+    assert np.all(np.isnan(got[A:])), "inactive tail rows were written"
