@@ -986,7 +986,7 @@ def ncu_case(name, launches=3):
     'dense_gelu' / 'dense_dgelu' the dense MXFP6 + rotation FC1 + GELU and
     FC2 dgrad + dGELU stages at M = 8192, D = 3072, H = 12288 (the dGELU
     case on a random saved pre-activation, so its GEMM launches are the only
-    ones)."""
+    ones); 'fc2_2sm' / 'fc1_dgrad_2sm' the plain MoE GEMMs on CTA pairs."""
     import torch
     import mlp_gemms_gb300 as mx
     import workloads as W
@@ -1058,6 +1058,9 @@ def ncu_case(name, launches=3):
                "fc2": lambda: mx.mx_grouped_gemm(hr, w2r, G, offs, out=y),
                "fc2_dgrad_dswiglu": lambda: mx.mx_grouped_gemm_dswiglu_bwd(dyr, w2t, z, G, offs, dzr, dzc),
                "fc1_dgrad": lambda: mx.mx_grouped_gemm(dzr, w1t, G, offs, out=y),
+               # the plain GEMMs on CTA pairs (even routing: 2048-row segments, multiples of 256)
+               "fc2_2sm": lambda: mx.mx_grouped_gemm_2sm(hr, w2r, G, offs, out=y),
+               "fc1_dgrad_2sm": lambda: mx.mx_grouped_gemm_2sm(dzr, w1t, G, offs, out=y),
                # the wgrads as the step runs them: with a workspace (claimed tiles, K-split)
                "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad_ws(dyc, hc, G, offs, out=dw2, workspace=ws2),
                "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad_ws(dzc, xc, G, offs, out=dw1, workspace=ws1)}[name]
