@@ -13,7 +13,11 @@
 // K = 32 on .kind::mxf8f6f4; K = 64 on .kind::mxf4 for packed E2M1 operands,
 // whose stages hold 256 K-elements and two scale chunks), each CTA's tensor
 // memory holding its 128 x 256 fp32 accumulator,
-// and its commits arrive on both CTAs' barriers.  Each CTA's eight epilogue
+// and its commits arrive on both CTAs' barriers.  A warp of the leader of
+// its own copies each stage's scale chunks into both CTAs' tensor memory
+// (tcgen05.cp .cta_group::2) and signals the MMA thread, which then issues
+// only MMAs (with the copies inline the issuing thread, feeding two SMs'
+// tensor cores, was the limit).  Each CTA's eight epilogue
 // warps read their accumulator, hand it back to the leader (the peer's by
 // one remote arrive on the leader's barrier) and store BF16 by TMA.  Tensor memory is
 // allocated by both CTAs collectively (.cta_group::2 returns the same
@@ -27,7 +31,8 @@ namespace mx {
 static __device__ unsigned g_pair_status = 0;
 
 namespace pair {
-constexpr int THREADS = 320;                          // producer, MMA, 8 epilogue warps
+constexpr int THREADS = 352;                          // producer, MMA, 8 epilogue warps, scale copies
+constexpr int SCALE_WARP = 10;
 constexpr uint32_t SF_TMEM = 256;                     // scale slots after the accumulator
 // F4: packed E2M1 operands on .kind::mxf4 -- a stage's 128-byte rows hold
 // 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
@@ -41,7 +46,8 @@ template <bool F4> struct PCfg {
   static constexpr int OFF_B = ST * A_BYTES;
   static constexpr int OFF_SF = OFF_B + ST * B_BYTES;
   static constexpr int OFF_BAR = OFF_SF + ST * SF_BYTES;
-  static constexpr int NUM_BARS = 2 * ST + 4;         // full, empty, acc_full, acc_empty, final, peer_read
+  // full, empty, acc_full, acc_empty, final, peer_read, sf_ready[ST], sf_final
+  static constexpr int NUM_BARS = 3 * ST + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem slot, abort flag
   static constexpr int OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;  // eight 2 KB staging buffers
   static constexpr int SMEM = OFF_STG + 8 * 2048 + 1024;  // + slack for 1024-byte alignment
@@ -176,6 +182,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   uint64_t* acc_empty = acc_full + 1;   // leader's: its 8 epilogue warps and the peer's hand-off have read
   uint64_t* final_bar = acc_empty + 1;
   uint64_t* peer_read = final_bar + 1;  // peer's: its 8 epilogue warps have read their accumulator
+  uint64_t* sf_ready = peer_read + 1;   // leader's: the stage's scales are in both CTAs' tensor memory
+  uint64_t* sf_final = sf_ready + ST;   // leader's: every scale copy has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const uint32_t rank = cluster_rank();
@@ -188,6 +196,8 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     mbar_init(acc_empty, 9);
     mbar_init(final_bar, 1);
     mbar_init(peer_read, 8);
+    for (int s2 = 0; s2 < ST; s2++) mbar_init(&sf_ready[s2], 1);
+    mbar_init(sf_final, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -252,7 +262,6 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (lane == 0 && leader) {
       const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(smem_u32(smem + OFF_B), 16, 1024, 2);
-      const uint64_t sf_desc0 = smem_desc(smem_u32(smem + OFF_SF), 0, 128, 0);
       const uint32_t idesc0 = F4 ? mma_idesc_mx(MXF4_E2M1, MXF4_E2M1, 256, 256, 0, 0)
                                  : mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 256, 256, 0, 0);
       int stage = 0;
@@ -264,26 +273,14 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < nk; kb++) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          // the stage's operands have landed and its scales are in tensor memory
+          if (!mbar_wait_bounded(&sf_ready[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sf_t = tmem_base + SF_TMEM + (uint32_t)(stage * C::SF_COLS);
-          const uint64_t sd = sf_desc0 + (uint64_t)((stage * SF_BYTES) >> 4);
           const uint64_t ad = a_desc0 + (uint64_t)((stage * A_BYTES) >> 4);
           const uint64_t bd = b_desc0 + (uint64_t)((stage * B_BYTES) >> 4);
           if constexpr (F4) {
-            // tensor-memory scale columns: A's chunk c at 4c (each CTA its
-            // own rows), B's chunk c of row block i at 8 + 8c + 4i; shared
-            // memory holds A's chunks, then B's row blocks of two chunks
             const int nch = (2 * kb + 1 < nc) ? 2 : 1;
-#pragma unroll
-            for (int c = 0; c < 2; c++) {
-              if (c < nch) {
-                tc2_copy_scales(sf_t + 4 * c, sd + (uint64_t)((512 * c) >> 4));
-#pragma unroll
-                for (int i = 0; i < 2; i++)
-                  tc2_copy_scales(sf_t + 8 + 8 * c + 4 * i, sd + (uint64_t)((1024 + 512 * (2 * i + c)) >> 4));
-              }
-            }
 #pragma unroll
             for (int j = 0; j < 4; j++) {
               if (j < 2 * nch) {  // K = 64 per MMA; scale IDs 0 and 2 pick the chunk's byte pair
@@ -293,9 +290,6 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               }
             }
           } else {
-            tc2_copy_scales(sf_t, sd);                   // A's 128 rows (each CTA its own)
-            tc2_copy_scales(sf_t + 4, sd + (512 >> 4));  // B rows 0..127 of the tile
-            tc2_copy_scales(sf_t + 8, sd + (1024 >> 4)); // B rows 128..255
 #pragma unroll
             for (int j = 0; j < 4; j++)
               tc2_mma_mx(tmem_base, ad + 2 * j, bd + 2 * j, idesc0 | ((uint32_t)j << 4) | ((uint32_t)j << 29), sf_t,
@@ -313,6 +307,54 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       volatile int no_abort = 0;
       tc2_commit_local(final_bar);
       mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
+    }
+  } else if (warp == SCALE_WARP) {
+    // ------------------------------------------------------------ scale copies (leader)
+    // In the MMA thread's stage order: wait for the stage's bytes (both
+    // CTAs'), copy its scale chunks into both CTAs' tensor memory and signal
+    // sf_ready once the copies have completed.  A slot is rewritten only after
+    // the producers refilled its stage, i.e. after the MMAs that read it.
+    if (lane == 0 && leader) {
+      const uint64_t sf_desc0 = smem_desc(smem_u32(smem + OFF_SF), 0, 128, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
+        const PairTile T = get_pair_tile(p, t, false);
+        if (!T.active) continue;
+        for (int kb = 0; kb < nk; kb++) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + SF_TMEM + (uint32_t)(stage * C::SF_COLS);
+          const uint64_t sd = sf_desc0 + (uint64_t)((stage * SF_BYTES) >> 4);
+          if constexpr (F4) {
+            // A's chunk c at column 4c (each CTA its own rows), B's chunk c of
+            // row block i at 8 + 8c + 4i; shared memory holds A's chunks, then
+            // B's row blocks of two chunks
+            const int nch = (2 * kb + 1 < nc) ? 2 : 1;
+#pragma unroll
+            for (int c = 0; c < 2; c++) {
+              if (c < nch) {
+                tc2_copy_scales(sf_t + 4 * c, sd + (uint64_t)((512 * c) >> 4));
+#pragma unroll
+                for (int i = 0; i < 2; i++)
+                  tc2_copy_scales(sf_t + 8 + 8 * c + 4 * i, sd + (uint64_t)((1024 + 512 * (2 * i + c)) >> 4));
+              }
+            }
+          } else {
+            tc2_copy_scales(sf_t, sd);                   // A's 128 rows (each CTA its own)
+            tc2_copy_scales(sf_t + 4, sd + (512 >> 4));  // B rows 0..127 of the tile
+            tc2_copy_scales(sf_t + 8, sd + (1024 >> 4)); // B rows 128..255
+          }
+          tc2_commit_local(&sf_ready[stage]);
+          if (++stage == ST) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // No copy may still be writing either CTA's tensor memory when it is freed.
+      volatile int no_abort = 0;
+      tc2_commit_local(sf_final);
+      mbar_wait_bounded(sf_final, 0, &no_abort, WAIT_BUDGET_NS);
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
