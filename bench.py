@@ -467,10 +467,10 @@ def stage_breakdown(mx, torch, margs, inp, offs, out, ws, G, D, F, R, steps, dev
         lambda: mx.mx_quantize(inp["w1"], 0, True, True, out_row=qw1[0], out_col=qw1[1]),
         lambda: mx.mx_quantize(inp["w2"], 0, True, True, out_row=qw2[0], out_col=qw2[1]),
         lambda: mx.mx_grouped_gemm_swiglu_fwd(qx[0], qw1[0], G, offs, h[0], h[1], z),
-        lambda: mx.mx_grouped_gemm(h[0], qw2[0], G, offs, out=out["y"]),
+        lambda: mx.mx_grouped_gemm_2sm(h[0], qw2[0], G, offs, out=out["y"]),   # as the step runs it (CTA pairs)
         lambda: mx.mx_quantize(inp["dy"], 0, True, True, out_row=qdy[0], out_col=qdy[1]),
         lambda: mx.mx_grouped_gemm_dswiglu_bwd(qdy[0], qw2[1], z, G, offs, dz[0], dz[1]),
-        lambda: mx.mx_grouped_gemm(dz[0], qw1[1], G, offs, out=out["dx"]),
+        lambda: mx.mx_grouped_gemm_2sm(dz[0], qw1[1], G, offs, out=out["dx"]),
         lambda: mx.mx_grouped_gemm_wgrad_ws(qdy[1], h[1], G, offs, out=out["dw2"], workspace=split_ws),
         lambda: mx.mx_grouped_gemm_wgrad_ws(dz[1], qx[1], G, offs, out=out["dw1"], workspace=split_ws),
     ]

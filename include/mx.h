@@ -326,14 +326,17 @@ MX_API mx_status_t mx_grouped_gemm(const mx_tensor_t *a, const mx_tensor_t *b, i
  *            training for Flux models", backends section: FP4 GEMMs at
  *            twice the FP8 rate); N = b->rows / G a multiple of 256 (else
  *            MX_ERR_SHAPE)
- *   offsets  every segment a multiple of 256 rows (mx_moe_route_index_pad
- *            with pad 256 builds such a routing); a segment that is not is
+ *   offsets  segments multiples of 128 rows, as for mx_grouped_gemm; each
+ *            expert's rows are taken in 256-row tiles, and an expert with an
+ *            odd number of 128-row blocks computes its last tile's upper
+ *            half and discards it (no wasted half with 256-row segments:
+ *            mx_moe_route_index_pad with pad 256).  A malformed segment is
  *            skipped on the device and reported as MX_ERR_OFFSETS by
- *            mx_get_device_status.  NULL: one segment of all R rows, R a
- *            multiple of 256.
+ *            mx_get_device_status.  G <= 1024 (else MX_ERR_NOT_SUPPORTED).
+ *            NULL: one segment of all R rows.
  * The products and their fp32 accumulation are those of mx_grouped_gemm
- * (bit-identical outputs).  The training step uses the single-SM kernel;
- * this one is measured beside it.
+ * (bit-identical outputs).  A warp of the leader CTA copies each stage's
+ * scale chunks into tensor memory, so the MMA thread issues only MMAs.
  */
 MX_API mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G,
                                        const int32_t *offsets_dev, void *out_bf16, int64_t ld_out,

@@ -771,8 +771,8 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   const int64_t N = b->rows / G;
   MX_CHECK(N > 0 && N % 256 == 0, MX_ERR_SHAPE, "N = %lld per expert is not a positive multiple of 256",
            (long long)N);
-  MX_CHECK(offsets_dev != nullptr || R % 256 == 0, MX_ERR_SHAPE,
-           "without offsets R = %lld must be a multiple of 256", (long long)R);
+  MX_CHECK(R % 128 == 0, MX_ERR_SHAPE, "R = %lld is not a multiple of 128", (long long)R);
+  MX_CHECK(G <= 1024, MX_ERR_NOT_SUPPORTED, "G = %d; the CTA-pair GEMM takes at most 1024 experts", G);
   MX_CHECK(R == 0 || (out_bf16 != nullptr && aligned16(out_bf16)), MX_ERR_ALIGNMENT,
            "out must be a 16-byte aligned pointer");
   MX_CHECK(ld_out >= N && ld_out % 8 == 0, MX_ERR_ALIGNMENT, "ld_out = %lld must be >= N and a multiple of 8",
@@ -788,7 +788,9 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   p.R = R; p.K = K; p.Nb = N;
   p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
   p.n_tiles = N / 256;
-  p.num_tiles = (R + 255) / 256 * p.n_tiles;
+  // 256-row tiles per expert segment: at most R / 256 plus one half-filled
+  // tile for every expert with an odd number of 128-row blocks
+  p.num_tiles = ((R + 255) / 256 + (offsets_dev ? (G + 1) / 2 : 0)) * p.n_tiles;
   // E2M1 runs on .kind::mxf4 from the packed payload: a stage is 128 bytes
   // (256 elements) of each row and two scale chunks, every box counted whole
   // (past K it is zero-filled).
@@ -1337,6 +1339,16 @@ struct HookCall {
   void post(int t) const { if (h) h->after(h->ctx, t); }
 };
 
+// The step's plain grouped GEMMs (FC2, FC1 dgrad): on CTA pairs when the
+// output width is a multiple of 256 (3-13 % faster than one SM per tile),
+// else on the single-SM kernel; the outputs are the same bit for bit.
+mx_status_t plain_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets, void* out,
+                       int64_t ld, mx_stream_t stream) {
+  const int64_t N = G > 0 ? b->rows / G : 0;
+  if (N > 0 && N % 256 == 0 && G <= 1024) return mx_grouped_gemm_2sm(a, b, G, offsets, out, ld, stream);
+  return mx_grouped_gemm(a, b, G, offsets, out, ld, stream);
+}
+
 mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t stream, const mx::StepHooks* hooks) {
   const int64_t R = a->R, D = a->D, F = a->F, G = a->G;
   mx_tensor_t x_row = view(a, L.x_row), x_col = view(a, L.x_col);
@@ -1360,14 +1372,14 @@ mx_status_t mlp_swiglu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t s
   hk.post(mx::T_W2);
   if ((st = mx_grouped_gemm_swiglu_fwd(&x_row, &w1_row, a->G, a->offsets, &h_row, &h_col, z, stream)) != MX_OK) return st;
   hk.pre(mx::T_Y);
-  if ((st = mx_grouped_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
+  if ((st = plain_gemm(&h_row, &w2_row, a->G, a->offsets, a->y, D, stream)) != MX_OK) return st;
   hk.post(mx::T_Y);
   hk.pre(mx::T_DY);
   if ((st = mx_quantize(a->dy, 1, R, D, D, MX_E4M3, both, &dy_row, &dy_col, nullptr, nullptr, 0, stream)) != MX_OK) return st;
   hk.post(mx::T_DY);
   if ((st = mx_grouped_gemm_dswiglu_bwd(&dy_row, &w2t_row, z, a->G, a->offsets, &dz_row, &dz_col, stream)) != MX_OK) return st;
   hk.pre(mx::T_DX);
-  if ((st = mx_grouped_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
+  if ((st = plain_gemm(&dz_row, &w1t_row, a->G, a->offsets, a->dx, D, stream)) != MX_OK) return st;
   hk.post(mx::T_DX);
   hk.pre(mx::T_DW2);
   void* split_ws = L.split_bytes ? static_cast<uint8_t*>(a->workspace) + L.split : nullptr;

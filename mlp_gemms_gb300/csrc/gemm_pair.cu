@@ -34,6 +34,7 @@ namespace pair {
 constexpr int THREADS = 352;                          // producer, MMA, 8 epilogue warps, scale copies
 constexpr int SCALE_WARP = 10;
 constexpr uint32_t SF_TMEM = 256;                     // scale slots after the accumulator
+constexpr int MAX_PAIR_G = 1024;                      // experts the row-tile table holds
 // F4: packed E2M1 operands on .kind::mxf4 -- a stage's 128-byte rows hold
 // 256 K-elements, i.e. KC = 2 scale chunks per 128-row block.
 template <bool F4> struct PCfg {
@@ -50,7 +51,8 @@ template <bool F4> struct PCfg {
   static constexpr int NUM_BARS = 3 * ST + 5;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem slot, abort flag
   static constexpr int OFF_STG = (OFF_MISC + 64 + 1023) / 1024 * 1024;  // eight 2 KB staging buffers
-  static constexpr int SMEM = OFF_STG + 8 * 2048 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_PREF = OFF_STG + 8 * 2048;     // pair row tiles before expert g, g = 0..G
+  static constexpr int SMEM = OFF_PREF + 4 * (MAX_PAIR_G + 1) + 1024;  // + slack for 1024-byte alignment
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(SF_TMEM + ST * SF_COLS <= 512, "scale slots must fit");
 };
@@ -132,34 +134,59 @@ __device__ __forceinline__ void tc2_commit_local(uint64_t* bar) {
 struct PairTile {
   int active, g;
   int64_t m0, n0;
+  int upper;  // the tile's rows m0 + 128 .. m0 + 255 belong to its expert
 };
 
-// Pair tile t -> (expert, row base of the 256-row block, column base).  The
-// expert is the segment holding the row base; a segment that is not a
-// multiple of 256 rows (or runs past R) makes the tile inactive and, when
-// `report`, sets the malformed-offsets status bit.
-__device__ __forceinline__ PairTile get_pair_tile(const PairParams& p, int64_t t, bool report) {
-  PairTile T;
-  T.active = 0; T.g = 0;
-  T.m0 = (t / p.n_tiles) * 256;
-  T.n0 = (t % p.n_tiles) * 256;
-  const int64_t total = p.offsets ? ldg_i32(p.offsets + p.G - 1) : p.R;
-  if (T.m0 >= total) return T;
-  int lo = 0;
-  if (p.offsets) {
-    int hi = p.G - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if ((int64_t)ldg_i32(p.offsets + mid) > T.m0) hi = mid; else lo = mid + 1;
+// Row tiles of 256 per expert segment (segments are multiples of 128 rows;
+// an odd number of 128-row blocks leaves the last tile's upper half past the
+// segment: computed, not stored).  pref[g] = row tiles of experts 0..g-1,
+// built in shared memory by warp 0 with a running warp scan; a malformed
+// segment (not a multiple of 128 rows, decreasing, or past R) gets no tiles
+// and, when `report`, sets the malformed-offsets status bit.
+__device__ __forceinline__ void build_pair_prefix(const PairParams& p, int32_t* pref, int lane, bool report) {
+  int32_t run = 0;
+  if (lane == 0) pref[0] = 0;
+  bool bad = false;
+  for (int base = 0; base < p.G; base += 32) {
+    const int g = base + lane;
+    int32_t cnt = 0;
+    if (g < p.G) {
+      const int64_t end = p.offsets ? ldg_i32(p.offsets + g) : p.R;
+      const int64_t start = (p.offsets && g) ? ldg_i32(p.offsets + g - 1) : 0;
+      if ((start & 127) || (end & 127) || end < start || end > p.R) bad = true;
+      else cnt = (int32_t)((end - start + 255) / 256);
     }
+    int32_t v = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += u;
+    }
+    if (g < p.G) pref[g + 1] = run + v;
+    run += __shfl_sync(0xffffffffu, v, 31);
   }
-  const int64_t end = p.offsets ? ldg_i32(p.offsets + lo) : p.R;
+  if (report && __any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&g_pair_status, DEV_BAD_OFFSETS);
+}
+
+// Pair tile t -> (expert, row base of its 256-row tile, column base): row
+// tile mt = t / n_tiles in expert order (pref), column tile t % n_tiles.
+__device__ __forceinline__ PairTile get_pair_tile(const PairParams& p, const int32_t* pref, int64_t t) {
+  PairTile T;
+  T.active = 0; T.g = 0; T.upper = 0;
+  const int64_t mt = t / p.n_tiles;
+  T.n0 = (t % p.n_tiles) * 256;
+  T.m0 = 0;
+  if (mt >= pref[p.G]) return T;
+  int lo = 0, hi = p.G - 1;  // the expert g with pref[g] <= mt < pref[g + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)pref[mid] <= mt) lo = mid; else hi = mid - 1;
+  }
   const int64_t start = (p.offsets && lo) ? ldg_i32(p.offsets + lo - 1) : 0;
-  if ((start & 255) || (end & 255) || start > T.m0 || end <= T.m0 || end > p.R || total > p.R) {
-    if (report) atomicOr(&g_pair_status, DEV_BAD_OFFSETS);
-    return T;
-  }
+  const int64_t end = p.offsets ? ldg_i32(p.offsets + lo) : p.R;
   T.g = lo;
+  T.m0 = start + 256 * (mt - pref[lo]);
+  T.upper = T.m0 + 128 < end ? 1 : 0;
   T.active = 1;
   return T;
 }
@@ -210,8 +237,10 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + C::OFF_PREF);
+  if (warp == 0) build_pair_prefix(p, pref, lane, leader);
   tc_fence_before();
-  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive or copy
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive or copy; pref is built
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int64_t pidx = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -228,7 +257,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       for (int s = 0; s < ST; s++) armed[s] = -1;
       bool ok = true;
       for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
-        const PairTile T = get_pair_tile(p, t, false);
+        const PairTile T = get_pair_tile(p, pref, t);
         if (!T.active) continue;
         const int64_t brow = (int64_t)T.g * p.Nb + T.n0;
         for (int kb = 0; kb < nk; kb++) {
@@ -268,7 +297,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
-        const PairTile T = get_pair_tile(p, t, false);
+        const PairTile T = get_pair_tile(p, pref, t);
         if (!T.active) continue;
         if (!mbar_wait_cluster(acc_empty, acc_phase ^ 1u, abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -320,7 +349,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = pidx; t < p.num_tiles && ok; t += npairs) {
-        const PairTile T = get_pair_tile(p, t, false);
+        const PairTile T = get_pair_tile(p, pref, t);
         if (!T.active) continue;
         for (int kb = 0; kb < nk; kb++) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
@@ -365,7 +394,7 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128);
     uint32_t acc_phase = 0, peer_phase = 0;
     for (int64_t t = pidx; t < p.num_tiles; t += npairs) {
-      const PairTile T = get_pair_tile(p, t, leader && warp == 2 && lane == 0);
+      const PairTile T = get_pair_tile(p, pref, t);
       if (!T.active) continue;
       if (!mbar_wait_bounded(acc_full, acc_phase, abort_flag, WAIT_BUDGET_NS)) break;
       acc_phase ^= 1u;
@@ -392,10 +421,12 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
       }
       const int64_t row0 = T.m0 + 128 * rank + q * 32;
+      if (leader || T.upper) {  // an upper half past the expert's segment is not stored
 #pragma unroll
-      for (int c = 0; c < 4; c++) {
-        stage_reuse_wait(lane);
-        store_bf16_block(reinterpret_cast<const float*>(v[c]), stg, lane, &tmO, T.n0 + half * 128 + 32 * c, row0);
+        for (int c = 0; c < 4; c++) {
+          stage_reuse_wait(lane);
+          store_bf16_block(reinterpret_cast<const float*>(v[c]), stg, lane, &tmO, T.n0 + half * 128 + 32 * c, row0);
+        }
       }
     }
     if (lane == 0) bulk_wait_all();  // this warp's TMA stores have landed

@@ -220,8 +220,11 @@ def test_pair_gemm_rejections(mx):
     a4, b4 = _t(512, 256, fmt=2), _t(512, 256)   # packed E2M1 against E4M3: .kind::mxf4 takes E2M1 on both
     st = L.mx_grouped_gemm_2sm(ctypes.byref(a4), ctypes.byref(b4), 1, FAKE, FAKE, 512, None)
     assert mx.STATUS[st] == "MX_ERR_INVALID_ARG" and "different formats" in mx.mx_last_error()
-    a3, b3 = _t(384, 256), _t(256, 256)
+    a3, b3 = _t(320, 256), _t(256, 256)
     st = L.mx_grouped_gemm_2sm(ctypes.byref(a3), ctypes.byref(b3), 1, None, FAKE, 256, None)
-    assert mx.STATUS[st] == "MX_ERR_SHAPE" and "without offsets" in mx.mx_last_error()
+    assert mx.STATUS[st] == "MX_ERR_SHAPE" and "multiple of 128" in mx.mx_last_error()
+    a5, b5 = _t(512, 256), _t(1025 * 256, 256)
+    st = L.mx_grouped_gemm_2sm(ctypes.byref(a5), ctypes.byref(b5), 1025, FAKE, FAKE, 256, None)
+    assert mx.STATUS[st] == "MX_ERR_NOT_SUPPORTED" and "1024" in mx.mx_last_error()
     assert L.mx_moe_route_rows_pad(100, 8, 4, 256) == (800 + 255 * 4 + 255) // 256 * 256
     assert L.mx_moe_route_rows_pad(100, 8, 4, 200) == 0

@@ -29,14 +29,17 @@ def _deq(ref, rows, cols, fmt=O.E4M3):
     return O.dequantize_rows(ref["row_payload"].reshape(rows, -1), ref["row_scales"].reshape(-1), rows, cols, fmt)
 
 
-@pytest.mark.parametrize("N,K", [(512, 1024), (256, 768)])
-def test_pair_gemm_equals_single_sm_and_oracle(cuda_lib, N, K):
-    """4 experts with segments of 512, 0, 256 and 768 rows and a 256-row
-    inactive tail poisoned with NaN (K = 1024 wraps the six-stage ring)."""
+@pytest.mark.parametrize("N,K,counts", [(512, 1024, [512, 0, 256, 768]), (256, 768, [512, 0, 256, 768]),
+                                         (512, 768, [384, 128, 0, 640])])
+def test_pair_gemm_equals_single_sm_and_oracle(cuda_lib, N, K, counts):
+    """4 experts with a 256-row inactive tail poisoned with NaN (K = 1024
+    wraps the six-stage ring); segments of 256-row multiples, or of odd
+    128-row block counts (384, 128, 640: each expert's last 256-row tile
+    computes an upper half past its segment, which must not be stored)."""
     import torch
     mx = cuda_lib
     G, R = 4, 1792
-    offsets = W.offsets_from_counts([512, 0, 256, 768])
+    offsets = W.offsets_from_counts(counts)
     A = int(offsets[-1])
     rng = np.random.default_rng(51 + N)
     ab = W.normal_bf16(rng, (R, K))
@@ -98,14 +101,15 @@ def test_pair_gemm_dense_e2m3(cuda_lib, had):
     assert O.within_tolerance(bf16_cpu(pair), ref).all()
 
 
-def test_pair_gemm_reports_segments_not_256_aligned(cuda_lib):
-    """Segments of 128-row multiples that are not 256-row multiples: their
-    tiles are skipped on the device (output untouched) and the call's status
-    reads MX_ERR_OFFSETS; the aligned ones are computed."""
+def test_pair_gemm_reports_malformed_segments(cuda_lib):
+    """A segment that is not a multiple of 128 rows (and every segment after
+    it that starts off the grid) is skipped on the device, its rows left
+    untouched, and the call's status reads MX_ERR_OFFSETS; the well-formed
+    expert before it is computed."""
     import torch
     mx = cuda_lib
     G, N, K, R = 3, 256, 256, 768
-    offsets = W.offsets_from_counts([256, 128, 384])   # expert 0 aligned; 1 and 2 are not
+    offsets = np.array([256, 456, 640], dtype=np.int32)   # expert 1 ends, expert 2 starts, off the grid
     rng = np.random.default_rng(3)
     ar, _ = _quant(mx, W.normal_bf16(rng, (R, K)))
     br, _ = _quant(mx, W.normal_bf16(rng, (G, N, K), std=0.02))
@@ -113,7 +117,9 @@ def test_pair_gemm_reports_segments_not_256_aligned(cuda_lib):
     mx.mx_grouped_gemm_2sm(ar, br, G, torch.from_numpy(offsets).cuda(), out=out)
     assert mx.mx_get_device_status() == "MX_ERR_OFFSETS"
     assert mx.mx_get_device_status() == "MX_OK"
-    single = mx.mx_grouped_gemm(ar, br, G, torch.from_numpy(offsets).cuda())
+    good = W.offsets_from_counts([256, 0, 0])
+    single = mx.mx_grouped_gemm(ar, br, G, torch.from_numpy(good).cuda())
+    torch.cuda.synchronize()
     assert torch.equal(out[:256], single[:256])
     assert bool(torch.isnan(out[256:].float()).all())
 
@@ -162,16 +168,17 @@ def test_pair_gemm_e2m1_exact_products(cuda_lib):
     assert torch.equal(pair, single)
 
 
-@pytest.mark.parametrize("K", [640, 1024])
-def test_pair_gemm_e2m1_ragged(cuda_lib, K):
-    """E2M1 on random operands: segments of 512, 0 and 256 rows with a
-    NaN-poisoned inactive tail; K = 640 ends on half a stage (five 128-K
-    chunks), K = 1024 wraps the five-stage ring.  Bit-identical to the
-    single-SM .kind::mxf4 kernel and within tolerance of the oracle."""
+@pytest.mark.parametrize("K,counts", [(640, [512, 0, 256]), (1024, [512, 0, 256]), (640, [128, 0, 640])])
+def test_pair_gemm_e2m1_ragged(cuda_lib, K, counts):
+    """E2M1 on random operands with a NaN-poisoned inactive tail; K = 640
+    ends on half a stage (five 128-K chunks), K = 1024 wraps the five-stage
+    ring; segments of 256-row multiples or of odd 128-row block counts.
+    Bit-identical to the single-SM .kind::mxf4 kernel and within tolerance
+    of the oracle."""
     import torch
     mx = cuda_lib
     G, N, R = 3, 512, 1024
-    offsets = W.offsets_from_counts([512, 0, 256])
+    offsets = W.offsets_from_counts(counts)
     A = int(offsets[-1])
     rng = np.random.default_rng(K)
     ar, aref = _quant(mx, W.normal_bf16(rng, (R, K)), O.E2M1)
