@@ -617,12 +617,13 @@ def dense_step_rate(mx, torch, dev, steps=5):
     calls = {
         "quant_x": lambda: quant("x"), "quant_w1": lambda: quant("w1"), "quant_w2": lambda: quant("w2"),
         "fc1_gelu": lambda: mx.mx_gemm_gelu_fwd(q["x"][0], q["w1"][0], inp["b1"], pre, ar, ac),
-        "fc2": lambda: mx.mx_gemm_bias(ar, q["w2"][0], inp["b2"], out=out["y"]),
+        # the plain GEMMs as the step runs them: on CTA pairs
+        "fc2": lambda: mx.mx_grouped_gemm_bias_2sm(ar, q["w2"][0], 1, None, inp["b2"], out=out["y"]),
         "quant_dy_colsum": lambda: quant("dy", True),
         "fc2_dgrad_dgelu": lambda: mx.mx_gemm_dgelu_bwd(q["dy"][0], q["w2"][1], pre, dpr, dpc, db1),
-        "fc1_dgrad": lambda: mx.mx_grouped_gemm(dpr, q["w1"][1], 1, None, out=out["dx"]),
-        "wgrad_dw2": lambda: mx.mx_grouped_gemm_wgrad(q["dy"][1], ac, 1, None, out=out["dw2"]),
-        "wgrad_dw1": lambda: mx.mx_grouped_gemm_wgrad(dpc, q["x"][1], 1, None, out=out["dw1"]),
+        "fc1_dgrad": lambda: mx.mx_grouped_gemm_2sm(dpr, q["w1"][1], 1, None, out=out["dx"]),
+        "wgrad_dw2": lambda: mx.mx_grouped_gemm_2sm(q["dy"][1], ac, 1, None, out=out["dw2"]),
+        "wgrad_dw1": lambda: mx.mx_grouped_gemm_2sm(dpc, q["x"][1], 1, None, out=out["dw1"]),
     }
     for c in calls.values():
         c()
@@ -657,7 +658,7 @@ def moe_forward_even_rate(mx, torch, dev, steps=5):
         mx.mx_quantize(inp["w1"], 0, True, False, out_row=qw1)
         mx.mx_quantize(inp["w2"], 0, True, False, out_row=qw2)
         mx.mx_grouped_gemm_swiglu_fwd(qx, qw1, G, offs, h[0], h[1], z)
-        mx.mx_grouped_gemm(h[0], qw2, G, offs, out=y)
+        mx.mx_grouped_gemm_2sm(h[0], qw2, G, offs, out=y)   # as the step runs FC2
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(3):

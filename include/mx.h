@@ -356,6 +356,17 @@ MX_API mx_status_t mx_grouped_gemm_bias(const mx_tensor_t *a, const mx_tensor_t 
                                         int64_t ld_out, mx_stream_t stream);
 
 /*
+ * mx_grouped_gemm_bias_2sm -- mx_grouped_gemm_bias on CTA pairs: the bias
+ * row of the expert added to the fp32 accumulator before the single BF16
+ * rounding, as in mx_grouped_gemm_bias (bit-identical outputs); shapes,
+ * offsets and errors as mx_grouped_gemm_2sm.
+ *   bias_bf16   device BF16 [G, N], 16-byte aligned
+ */
+MX_API mx_status_t mx_grouped_gemm_bias_2sm(const mx_tensor_t *a, const mx_tensor_t *b, int32_t G,
+                                            const int32_t *offsets_dev, const void *bias_bf16, void *out_bf16,
+                                            int64_t ld_out, mx_stream_t stream);
+
+/*
  * mx_grouped_gemm_swiglu_fwd -- FC1 of the expert MLP with the SwiGLU
  * epilogue ([MXFP8-PR] correctness-first kernels commit: FC1 ragged grouped
  * GEMM + SwiGLU + dual 1x32 / 32x1 MXFP8 RCEIL quantization + BF16

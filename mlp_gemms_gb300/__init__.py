@@ -36,7 +36,7 @@ ABI_SYMBOLS = (
     "mx_mlp_pipeline_create", "mx_mlp_pipeline_run", "mx_mlp_pipeline_sync", "mx_mlp_pipeline_destroy",
     "mx_grouped_gemm_wgrad_f32", "mx_grouped_gemm_swiglu_probs_fwd", "mx_dswiglu_probs_workspace_bytes",
     "mx_grouped_gemm_dswiglu_probs_bwd", "mx_quantize_sr", "mx_moe_route_rows", "mx_moe_route_workspace_bytes",
-    "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute", "mx_grouped_gemm_bias",
+    "mx_moe_route_index", "mx_permute_quantize", "mx_moe_unpermute", "mx_grouped_gemm_bias", "mx_grouped_gemm_bias_2sm",
     "mx_grouped_gemm_wgrad_workspace_bytes", "mx_grouped_gemm_wgrad_ws", "mx_grouped_gemm_wgrad_f32_ws",
     "mx_mlp_workspace_layout", "mx_moe_route_rows_pad", "mx_moe_route_index_pad", "mx_grouped_gemm_2sm",
 )
@@ -132,6 +132,7 @@ def load(path=None):
         "mx_permute_quantize": (ctypes.c_int, [vp, i64, i64, i64, vp, i64, vp, i32, i32, u32, tp, tp, vp]),
         "mx_moe_unpermute": (ctypes.c_int, [vp, i64, i64, vp, vp, i64, i32, vp, vp]),
         "mx_grouped_gemm_bias": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, i64, vp]),
+        "mx_grouped_gemm_bias_2sm": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, i64, vp]),
         "mx_grouped_gemm_wgrad_workspace_bytes": (sz, [i64, i64, i64, i32]),
         "mx_grouped_gemm_wgrad_ws": (ctypes.c_int, [tp, tp, i32, vp, vp, vp, sz, vp]),
         "mx_grouped_gemm_wgrad_f32_ws": (ctypes.c_int, [tp, tp, i32, vp, vp, i32, vp, sz, vp]),
@@ -346,6 +347,19 @@ def mx_grouped_gemm_2sm(a, b, G, offsets, out=None, ld_out=None, stream=None):
         out = torch.empty((a.rows, N), dtype=torch.bfloat16, device=a.data.device)
     ld = ld_out if ld_out is not None else out.stride(0)
     _check(load().mx_grouped_gemm_2sm(_s(a), _s(b), G, _ptr(offsets), _ptr(out), ld, _stream(stream)))
+    return out
+
+
+def mx_grouped_gemm_bias_2sm(a, b, G, offsets, bias, out=None, ld_out=None, stream=None):
+    """mx_grouped_gemm_bias on CTA pairs."""
+    import torch
+    N = b.rows // G if G else 0
+    assert bias.dtype == torch.bfloat16 and bias.is_contiguous()
+    if out is None:
+        out = torch.empty((a.rows, N), dtype=torch.bfloat16, device=a.data.device)
+    ld = ld_out if ld_out is not None else out.stride(0)
+    _check(load().mx_grouped_gemm_bias_2sm(_s(a), _s(b), G, _ptr(offsets), _ptr(bias), _ptr(out), ld,
+                                           _stream(stream)))
     return out
 
 

@@ -749,6 +749,12 @@ mx_status_t grouped_gemm_impl(const mx_tensor_t* a, const mx_tensor_t* b, int32_
 
 }  // namespace
 
+namespace {
+mx_status_t pair_gemm_impl(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                           const void* bias_bf16, int64_t bias_ld, void* out_bf16, int64_t ld_out,
+                           mx_stream_t stream);
+}  // namespace
+
 extern "C" {
 
 mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
@@ -758,6 +764,18 @@ mx_status_t mx_grouped_gemm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t 
 
 mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
                                 void* out_bf16, int64_t ld_out, mx_stream_t stream) {
+  return pair_gemm_impl(a, b, G, offsets_dev, nullptr, 0, out_bf16, ld_out, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The CTA-pair grouped GEMM with an optional BF16 bias ([G, N] rows bias_ld
+// apart, or one row of N with bias_ld 0) added before the single rounding.
+mx_status_t pair_gemm_impl(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
+                           const void* bias_bf16, int64_t bias_ld, void* out_bf16, int64_t ld_out,
+                           mx_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mx_status_t st;
   if ((st = check_gemm_operand(a, "a")) != MX_OK) return st;
@@ -784,9 +802,12 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   if ((st = device_info(&dev)) != MX_OK) return st;
   mx::PairParams p;
   memset(&p, 0, sizeof(p));
+  MX_CHECK(bias_bf16 == nullptr || aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be a 16-byte aligned pointer");
   p.G = G; p.offsets = offsets_dev;
   p.R = R; p.K = K; p.Nb = N;
   p.a_type = mma_type(a->fmt); p.b_type = mma_type(b->fmt);
+  p.bias = static_cast<const uint16_t*>(bias_bf16);
+  p.bias_ld = bias_ld;
   p.n_tiles = N / 256;
   // 256-row tiles per expert segment: at most R / 256 plus one half-filled
   // tile for every expert with an odd number of 128-row blocks
@@ -815,10 +836,22 @@ mx_status_t mx_grouped_gemm_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int3
   return MX_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
 mx_status_t mx_grouped_gemm_bias(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G, const int32_t* offsets_dev,
                                  const void* bias_bf16, void* out_bf16, int64_t ld_out, mx_stream_t stream) {
   MX_CHECK(bias_bf16 != nullptr && aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be a 16-byte aligned pointer");
   return grouped_gemm_impl(a, b, G, offsets_dev, bias_bf16, out_bf16, ld_out, stream);
+}
+
+mx_status_t mx_grouped_gemm_bias_2sm(const mx_tensor_t* a, const mx_tensor_t* b, int32_t G,
+                                     const int32_t* offsets_dev, const void* bias_bf16, void* out_bf16,
+                                     int64_t ld_out, mx_stream_t stream) {
+  MX_CHECK(bias_bf16 != nullptr && aligned16(bias_bf16), MX_ERR_ALIGNMENT, "bias must be a 16-byte aligned pointer");
+  MX_CHECK(a != nullptr && b != nullptr && G >= 1, MX_ERR_INVALID_ARG, "a, b and G >= 1 are required");
+  return pair_gemm_impl(a, b, G, offsets_dev, bias_bf16, b->rows / G, out_bf16, ld_out, stream);
 }
 
 }  // extern "C"
@@ -1426,7 +1459,9 @@ mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t str
   hk.post(mx::T_B1);
   hk.pre(mx::T_B2);
   hk.pre(mx::T_Y);
-  if ((st = mx_gemm_bias(&act_row, &w2_row, a->b2, a->y, D, stream)) != MX_OK) return st;
+  if ((st = D % 256 == 0 ? pair_gemm_impl(&act_row, &w2_row, 1, nullptr, a->b2, 0, a->y, D, stream)
+                          : mx_gemm_bias(&act_row, &w2_row, a->b2, a->y, D, stream)) != MX_OK)
+    return st;
   hk.post(mx::T_B2);
   hk.post(mx::T_Y);
   hk.pre(mx::T_DY);
@@ -1442,13 +1477,20 @@ mx_status_t mlp_gelu(const mx_mlp_args_t* a, const MlpLayout& L, mx_stream_t str
     return st;
   hk.post(mx::T_DB1);
   hk.pre(mx::T_DX);
-  if ((st = mx_grouped_gemm(&dpre_row, &w1t_row, 1, nullptr, a->dx, D, stream)) != MX_OK) return st;
+  if ((st = plain_gemm(&dpre_row, &w1t_row, 1, nullptr, a->dx, D, stream)) != MX_OK) return st;
   hk.post(mx::T_DX);
   hk.pre(mx::T_DW2);
-  if ((st = mx_grouped_gemm_wgrad(&dy_col, &act_col, 1, nullptr, a->dw2, stream)) != MX_OK) return st;
+  // dense weight gradients: the same K order as the wgrad kernel's, as plain
+  // GEMMs on CTA pairs where the widths allow (dW2 [D, H] = dY^T act, dW1
+  // [H, D] = dpre^T X over the M tokens)
+  if ((st = H % 256 == 0 ? plain_gemm(&dy_col, &act_col, 1, nullptr, a->dw2, H, stream)
+                         : mx_grouped_gemm_wgrad(&dy_col, &act_col, 1, nullptr, a->dw2, stream)) != MX_OK)
+    return st;
   hk.post(mx::T_DW2);
   hk.pre(mx::T_DW1);
-  if ((st = mx_grouped_gemm_wgrad(&dpre_col, &x_col, 1, nullptr, a->dw1, stream)) != MX_OK) return st;
+  if ((st = D % 256 == 0 ? plain_gemm(&dpre_col, &x_col, 1, nullptr, a->dw1, D, stream)
+                         : mx_grouped_gemm_wgrad(&dpre_col, &x_col, 1, nullptr, a->dw1, stream)) != MX_OK)
+    return st;
   hk.post(mx::T_DW1);
   return MX_OK;
 }

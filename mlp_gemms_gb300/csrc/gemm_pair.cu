@@ -420,6 +420,22 @@ mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (lane == 0) arrive_on_leader(acc_empty_cl);
         }
       }
+      if (p.bias != nullptr) {  // bias added to the fp32 accumulator: one rounding
+        const uint4* bp = reinterpret_cast<const uint4*>(p.bias + (int64_t)T.g * p.bias_ld + T.n0 + half * 128);
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+#pragma unroll
+          for (int w = 0; w < 4; w++) {
+            const uint4 bw = __ldg(bp + c * 4 + w);
+            const uint32_t b4[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+              const float bv = bf16_bits_to_float((k & 1) ? (b4[k >> 1] >> 16) : (b4[k >> 1] & 0xFFFFu));
+              v[c][8 * w + k] = __float_as_uint(__uint_as_float(v[c][8 * w + k]) + bv);
+            }
+          }
+        }
+      }
       const int64_t row0 = T.m0 + 128 * rank + q * 32;
       if (leader || T.upper) {  // an upper half past the expert's segment is not stored
 #pragma unroll

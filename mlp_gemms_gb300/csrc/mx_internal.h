@@ -126,6 +126,8 @@ struct PairParams {
   int64_t n_tiles, num_tiles;  // 256-column tiles per row block; pair tiles in all
   uint32_t tx_bytes;       // one CTA's bytes per stage (A and B boxes, scale chunks)
   int f4;                  // packed E2M1 operands on .kind::mxf4 (256 K-elements a stage)
+  const uint16_t* bias;    // BF16 bias added to the fp32 accumulator before the rounding, or null
+  int64_t bias_ld;         // elements between experts' bias rows (0: one row for all)
 };
 cudaError_t launch_gemm_pair(const PairParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                              const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to, cudaStream_t s,

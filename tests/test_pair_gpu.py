@@ -194,3 +194,27 @@ def test_pair_gemm_e2m1_ragged(cuda_lib, K, counts):
     ref = O.grouped_gemm(_deq(aref, R, K, O.E2M1), _deq(bref, G * N, K, O.E2M1).reshape(G, N, K), offsets)
     assert O.within_tolerance(got[:A], ref[:A]).all()
     assert np.all(np.isnan(got[A:])), "inactive tail rows were written"
+
+
+@pytest.mark.parametrize("fmt,had,counts", [(O.E4M3, False, [384, 0, 256]), (O.E2M3, True, [256, 128, 256])])
+def test_pair_gemm_bias_equals_single_sm(cuda_lib, fmt, had, counts):
+    """The bias epilogue on CTA pairs (each expert's BF16 bias row added to
+    the fp32 accumulator before the one rounding) equals the single-SM bias
+    epilogue bit for bit, rows past the segments untouched."""
+    import torch
+    mx = cuda_lib
+    G, N, K, R = 3, 512, 768, 1024
+    offsets = W.offsets_from_counts(counts)
+    A = int(offsets[-1])
+    rng = np.random.default_rng(29)
+    ar, _ = _quant(mx, W.normal_bf16(rng, (R, K)), fmt, had)
+    br, _ = _quant(mx, W.normal_bf16(rng, (G, N, K), std=0.02), fmt, had)
+    bias = to_dev(W.normal_bf16(rng, (G, N), std=0.5))
+    offs = torch.from_numpy(offsets).cuda()
+    pair = torch.full((R, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mx.mx_grouped_gemm_bias_2sm(ar, br, G, offs, bias, out=pair)
+    single = mx.mx_grouped_gemm_bias(ar, br, G, offs, bias)
+    torch.cuda.synchronize()
+    assert mx.mx_get_device_status() == "MX_OK"
+    assert torch.equal(pair[:A], single[:A])
+    assert bool(torch.isnan(pair[A:].float()).all())
