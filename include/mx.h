@@ -378,7 +378,10 @@ MX_API mx_status_t mx_grouped_gemm_bias_2sm(const mx_tensor_t *a, const mx_tenso
  *   h_row     out, [R, F] rowwise E4M3 of h = gate * sigmoid(gate) * up
  *   h_col     out, [F, R] columnwise E4M3 of h
  * D % 128 == 0, F % 128 == 0, R % 128 == 0.  h is computed in fp32 from the
- * fp32 accumulators; sigmoid(x) = 1 / (1 + exp(-x)).
+ * fp32 accumulators; sigmoid(x) = 1 / (1 + exp(-x)).  Runs on CTA pairs
+ * (256-row tiles per expert, tcgen05 .cta_group::2) for G <= 1024 unless the
+ * environment holds MX_FUSED_PAIRS=0 (one SM per 128-row tile); the output
+ * bytes are the same either way.
  */
 MX_API mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t *x_row, const mx_tensor_t *w1_row, int32_t G,
                                        const int32_t *offsets_dev, const mx_tensor_t *h_row,
@@ -395,6 +398,9 @@ MX_API mx_status_t mx_grouped_gemm_swiglu_fwd(const mx_tensor_t *x_row, const mx
  *   dz_col    out, [2F, R] columnwise E4M3 of dz
  * with dh = dY W2: dg = dh*u*s*(1 + g*(1-s)), du = dh*g*s, s = sigmoid(g),
  * g and u read from the BF16 z.  D % 128 == 0, F % 128 == 0, R % 128 == 0.
+ * With MX_FUSED_PAIRS=1 in the environment and F % 256 == 0 it runs on CTA
+ * pairs (its epilogue, not its mainloop, is the limit, so by default it
+ * takes one SM per tile); the output bytes are the same either way.
  */
 MX_API mx_status_t mx_grouped_gemm_dswiglu_bwd(const mx_tensor_t *dy_row, const mx_tensor_t *w2t_row,
                                         const void *z_bf16, int32_t G, const int32_t *offsets_dev,

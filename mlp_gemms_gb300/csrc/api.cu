@@ -368,8 +368,20 @@ struct OutView {
   bool f32 = false;  // fp32 elements (EPI_F32) instead of BF16
 };
 
+// Which fused epilogues run on CTA pairs (the outputs are the same bit for
+// bit either way).  By default the SwiGLU forward (4 % faster on pairs: its
+// mainloop is the limit) and not the dSwiGLU backward (5 % slower on pairs:
+// its epilogue is the limit); MX_FUSED_PAIRS=0 keeps both on one SM per
+// tile, MX_FUSED_PAIRS=1 puts both on pairs.  Read at every call.
+bool fused_pairs_enabled(int epi) {
+  const char* v = getenv("MX_FUSED_PAIRS");
+  if (v && v[0] == '0') return false;
+  if (v && v[0] == '1') return true;
+  return epi == mx::EPI_SWIGLU;
+}
+
 mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
-                     const DevInfo& dev, OutView out) {
+                     const DevInfo& dev, OutView out, bool pair = false) {
   // E2M1 operands with a plain epilogue run on .kind::mxf4 from the packed
   // payload; the fused epilogues keep .kind::mxf8f6f4.
   p.f4 = (a->fmt == MX_E2M1 && (p.epi == mx::EPI_BF16 || p.epi == mx::EPI_F32)) ? 1 : 0;
@@ -389,6 +401,22 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
     if ((st = make_tmap_bf16(&to, p.z, p.R, 2 * p.F, 2 * p.F, bn == 256 ? 32 : 64)) != MX_OK) return st;
   } else {
     to = ta;
+  }
+  if (pair) {
+    // CTA pairs: 256-row tiles per expert segment (the last one of an odd
+    // 128-row block count half computed past the segment), each CTA staging
+    // its 128 A rows, one 128-row block of B and the scale chunks of its A
+    // rows and of both B blocks
+    p.tx_bytes = stage_tx_bytes(a->fmt, 128) + 512u;
+    p.num_tiles = ((p.R + 255) / 256 + (p.offsets ? (p.G + 1) / 2 : 0)) * p.n_tiles;
+    CUtensorMap tsa, tsb;
+    if ((st = make_tmap_scales(&tsa, a->scale, a->rows, a->cols, 1, 1)) != MX_OK) return st;
+    if ((st = make_tmap_scales(&tsb, b->scale, b->rows, b->cols, 1, 1)) != MX_OK) return st;
+    log_config("gemm pair %s BN=256 a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld", epi_name(p.epi), p.a_type,
+               p.b_type, (long long)p.R, (long long)p.K, (long long)p.Nb, p.G, (long long)p.num_tiles);
+    cudaError_t e = mx::launch_gemm_pair_fused(p, ta, tb, tsa, tsb, to, s, dev.sms);
+    if (e != cudaSuccess) return cuda_fail(e, "CTA-pair fused GEMM launch");
+    return MX_OK;
   }
   log_config("gemm %s %s%s BN=%d a=%d b=%d R=%lld K=%lld N=%lld G=%d tiles=%lld grid=%lld split=%d",
              p.mode == mx::MODE_WGRAD ? "wgrad" : "grouped", epi_name(p.epi), p.f4 ? " mxf4" : "", bn, p.a_type,
@@ -901,7 +929,8 @@ mx_status_t swiglu_fwd_impl(const mx_tensor_t* x_row, const mx_tensor_t* w1_row,
   p.q_col = static_cast<uint8_t*>(h_col->data); p.q_col_scale = h_col->scale;
   p.q_cols = F;
   if ((st = attach_tap(&p, R, F)) != MX_OK) return st;
-  return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F});
+  return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F},
+                  fused_pairs_enabled(mx::EPI_SWIGLU) && G <= mx::MAX_PAIR_G_HOST);
 }
 
 }  // namespace
@@ -963,6 +992,7 @@ mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_r
   p.sfb_kchunks = p.sfa_kchunks;
   // 256-column tiles (the 128x256 MMA) where F allows, else 128
   const int tile_n = F % 256 == 0 ? 256 : 128;
+  const bool pair = tile_n == 256 && fused_pairs_enabled(mx::EPI_DSWIGLU) && G <= mx::MAX_PAIR_G_HOST;
   p.m_tiles = (int)(R / 128);
   p.n_tiles = (int)(F / tile_n);
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
@@ -979,12 +1009,12 @@ mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_r
     p.probs = probs;
     p.dprobs_part = static_cast<float*>(workspace);
     p.dprobs_ld = ld;
-    if ((st = run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0})) != MX_OK) return st;
+    if ((st = run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0}, pair)) != MX_OK) return st;
     cudaError_t e = mx::launch_dprobs_reduce(p.dprobs_part, R, ld, offsets_dev, G, dprobs, s);
     if (e != cudaSuccess) return cuda_fail(e, "dprobs reduction launch");
     return MX_OK;
   }
-  return run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0});
+  return run_gemm(p, dy_row, w2t_row, tile_n, s, dev, OutView{nullptr, 0, 0, 0}, pair);
 }
 
 }  // namespace

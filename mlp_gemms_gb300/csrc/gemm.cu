@@ -18,8 +18,48 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads<BN, EPI>(), smem, s>>>(ta, tb, to, p);
+  kern<<<(unsigned)grid, kThreads<BN, EPI>(), smem, s>>>(ta, tb, to, ta, tb, p);
   return cudaGetLastError();
+}
+
+// The fused SwiGLU / dSwiGLU epilogues on CTA pairs (256-row tiles, two SMs
+// per tile): clusters of two CTAs, one pair per two SMs.
+template <int EPI, bool EXT>
+static cudaError_t launch_pair_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                                   const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to,
+                                   cudaStream_t s, int num_sms) {
+  constexpr int smem = KCfg<256, EPI, false, true>::SMEM_BYTES;
+  {
+    const cudaError_t e = ensure_smem_attr<mx_gemm_kernel<256, EPI, MODE_GROUPED, E4M3, false, EXT, false, true>>(smem);
+    if (e != cudaSuccess) return e;
+  }
+  int64_t pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(kThreads<256, EPI, true>(), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<256, EPI, MODE_GROUPED, E4M3, false, EXT, false, true>, ta, tb, to,
+                            tsa, tsb, p);
+}
+
+cudaError_t launch_gemm_pair_fused(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                                   const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to,
+                                   cudaStream_t s, int num_sms) {
+  const bool ext = p.tap != nullptr || p.probs != nullptr;
+  if (p.epi == EPI_SWIGLU) return launch_pair_one<EPI_SWIGLU, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+  if (p.epi == EPI_DSWIGLU)
+    return ext ? launch_pair_one<EPI_DSWIGLU, true>(p, ta, tb, tsa, tsb, to, s, num_sms)
+               : launch_pair_one<EPI_DSWIGLU, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,

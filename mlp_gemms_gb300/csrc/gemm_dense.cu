@@ -22,7 +22,7 @@ static cudaError_t launch_dense_one(const GemmParams& p, const CUtensorMap& ta, 
   }
   int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   if (grid < 1) grid = 1;
-  kern<<<(unsigned)grid, kThreads<BN, EPI>(), smem, s>>>(ta, tb, to, p);
+  kern<<<(unsigned)grid, kThreads<BN, EPI>(), smem, s>>>(ta, tb, to, ta, tb, p);
   return cudaGetLastError();
 }
 

@@ -40,6 +40,7 @@
 #pragma once
 #include "mx_common.cuh"
 #include "mx_internal.h"
+#include "pair_common.cuh"
 
 namespace mx {
 
@@ -55,10 +56,12 @@ constexpr int EPI_THREADS = 256;
 template <int BN, int EPI> constexpr int kEpiWarps() {
   return (BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU)) ? 12 : 8;
 }
-template <int BN, int EPI> constexpr int kThreads() {
-  return 64 + 32 * kEpiWarps<BN, EPI>() + (EPI == EPI_DSWIGLU ? 32 : 0);
+// PAIR (CTA pairs, tcgen05 .cta_group::2): one more warp copies each
+// stage's scale chunks into both CTAs' tensor memory, so that the leader's
+// MMA thread issues only MMAs.
+template <int BN, int EPI, bool PAIR = false> constexpr int kThreads() {
+  return 64 + 32 * kEpiWarps<BN, EPI>() + (EPI == EPI_DSWIGLU ? 32 : 0) + (PAIR ? 32 : 0);
 }
-constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 constexpr int MAX_SORTED_G = 1024;  // wgrad schedules at most this many experts by size
 constexpr int MAX_SPLIT = MAX_SPLIT_EXPERTS;  // wgrad: at most this many experts have their K range split
 
@@ -82,14 +85,16 @@ struct SplitInfo {
 // memory past the scale slots so that the single accumulator is handed back
 // at once; they take three stages for the room their larger scale-chunk and
 // column-sum buffers (GELU / dGELU) or the z ring (dSwiGLU) need.
-template <int BN, bool ZR = false, bool F4 = false, bool PK = false, int EWARPS = 8>
+// PAIR: each CTA of a pair stages its own 128 rows of A and half (BN / 2
+// rows) of the tile's B slice, so a stage is 33.5 KB and more of them fit.
+template <int BN, bool ZR = false, bool F4 = false, bool PK = false, int EWARPS = 8, bool PAIR = false>
 struct Cfg {
   static constexpr int EW = EWARPS;  // epilogue warps
   static constexpr int KC = F4 ? 2 : 1;
-  static constexpr int STAGES = BN == 256 ? (PK ? 3 : 4) : (ZR ? 4 : 5);
+  static constexpr int STAGES = PAIR ? (PK ? 4 : 5) : (BN == 256 ? (PK ? 3 : 4) : (ZR ? 4 : 5));
   static constexpr int ACC = BN == 256 ? 1 : 2;
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * 128;
   static constexpr int SF_A_BYTES = KC * 512;  // A's chunks, then B's (chunk-major)
   static constexpr int SF_BYTES = KC * (512 + (BN / 128) * 512);
   static constexpr int SF_COLS = KC * (4 + 4 * (BN / 128));
@@ -120,12 +125,15 @@ struct Cfg {
   // wgrad with a workspace: tiles claimed from a global counter reach the
   // MMA thread and the epilogue through a TQN-entry queue
   static constexpr int TQN = 4;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS + 2 * TQN;
+  // PAIR adds peer_read, sf_ready[STAGES] and sf_final
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 2 + 2 * Z_SLOTS + 2 * TQN + (PAIR ? STAGES + 2 : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TQ = OFF_MISC + 16;                 // TQN int32 tile indices
   static constexpr int OFF_ORDER = OFF_TQ + 4 * TQN;           // wgrad: experts by descending size
   static constexpr int OFF_SPLIT = OFF_ORDER + 2 * MAX_SORTED_G;  // wgrad: SplitInfo
-  static constexpr int SMEM_BYTES = OFF_SPLIT + 256 + 1024;  // + slack for 1024-byte alignment
+  static constexpr int OFF_PREF = OFF_SPLIT + 256;             // PAIR: 256-row tiles before each expert
+  static constexpr int SMEM_BYTES = OFF_PREF + (PAIR ? 4 * (MAX_PAIR_G + 1) : 0) + 1024;  // + alignment slack
+  static_assert(MAX_PAIR_G == MAX_PAIR_G_HOST, "row-tile table size");
   static_assert(sizeof(SplitInfo) <= 256, "split info must fit");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t SF_TMEM_BASE = 256;
@@ -143,8 +151,8 @@ struct Cfg {
 template <int BN, int EPI> constexpr bool kParks() {
   return BN == 256 && (EPI == EPI_GELU || EPI == EPI_DGELU || EPI == EPI_DSWIGLU);
 }
-template <int BN, int EPI, bool F4 = false>
-using KCfg = Cfg<BN, EPI == EPI_DSWIGLU, F4, kParks<BN, EPI>(), kEpiWarps<BN, EPI>()>;
+template <int BN, int EPI, bool F4 = false, bool PAIR = false>
+using KCfg = Cfg<BN, EPI == EPI_DSWIGLU, F4, kParks<BN, EPI>(), kEpiWarps<BN, EPI>(), PAIR>;
 
 struct Tile {
   int active;
@@ -156,6 +164,7 @@ struct Tile {
   int parts, part;  // wgrad K-split: parts of this (expert, m, n) tile and which one
   int64_t slot;     // first partial slot of the tile's parts
   int cnt;          // its arrival counter
+  int upper;        // PAIR: the 256-row tile's upper 128 rows lie in its expert's segment
 };
 
 __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); }
@@ -169,7 +178,7 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
                                                 const SplitInfo* split) {
   Tile T;
   T.active = 0; T.g = 0; T.m0 = 0; T.n0 = 0; T.kbeg = 0; T.nk = 0; T.nc = 0;
-  T.parts = 1; T.part = 0; T.slot = 0; T.cnt = 0;
+  T.parts = 1; T.part = 0; T.slot = 0; T.cnt = 0; T.upper = 1;
   if (MODE == MODE_GROUPED) {
     int64_t mt = t / p.n_tiles, nt = t % p.n_tiles;
     T.m0 = mt * 128;
@@ -249,6 +258,27 @@ __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool re
   return T;
 }
 
+// get_tile, or with PAIR (grouped only) the 256-row tile of pair tile t:
+// row tile t / n_tiles in expert order (the pref table), column tile
+// t % n_tiles; m0 is the pair's row base (each CTA adds 128 x its rank).
+template <int NT, int MODE, bool F4, bool PAIR>
+__device__ __forceinline__ Tile get_tile_x(const GemmParams& p, int64_t t, bool report, const uint16_t* order,
+                                           const SplitInfo* split, const int32_t* pref) {
+  if constexpr (!PAIR) {
+    return get_tile<NT, MODE, F4>(p, t, report, order, split);
+  } else {
+    Tile T;
+    T.active = 0; T.g = 0; T.m0 = 0; T.n0 = (t % p.n_tiles) * NT; T.kbeg = 0; T.nk = 0; T.nc = 0;
+    T.parts = 1; T.part = 0; T.slot = 0; T.cnt = 0; T.upper = 0;
+    if (pair_row_tile(p.offsets, p.G, p.R, pref, t / p.n_tiles, &T.g, &T.m0, &T.upper)) {
+      T.nk = (int)(p.K / 128);
+      T.nc = T.nk;
+      T.active = 1;
+    }
+    return T;
+  }
+}
+
 // The global tile a CTA handles at its i-th turn.  Grouped: plain round
 // robin (neighbouring CTAs share A rows and B panels in L2).  Wgrad: tiles
 // are laid out expert by expert in descending size order and dealt to the
@@ -259,6 +289,18 @@ __device__ __forceinline__ int64_t tile_index(int64_t i) {
   if (MODE == MODE_WGRAD && (i & 1)) return i * gridDim.x + (gridDim.x - 1 - blockIdx.x);
   return i * gridDim.x + blockIdx.x;
 }
+
+// With PAIR both CTAs of a cluster take the same tiles: pair p = blockIdx / 2
+// of gridDim / 2 takes tiles p, p + gridDim / 2, ...
+template <bool PAIR>
+__device__ __forceinline__ int64_t tile_slots() { return PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x; }
+
+template <int MODE, bool PAIR>
+__device__ __forceinline__ int64_t tile_index_x(int64_t i) {
+  if constexpr (PAIR) return i * (int64_t)(gridDim.x >> 1) + (int64_t)(blockIdx.x >> 1);
+  return tile_index<MODE>(i);
+}
+
 
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" :: "l"(ptr));
@@ -474,15 +516,20 @@ __device__ __forceinline__ void col_quant16(const float* v, float* buf, int lane
 // EXT: the dSwiGLU kernel has a separate instantiation with its optional
 // extras, the debug tap and the routing probabilities (its register budget is
 // tight); the other fused epilogues test those pointers at run time.
-template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false, bool F4 = false>
-__global__ void __launch_bounds__(kThreads<BN, EPI>(), 1)
+template <int BN, int EPI, int MODE, int QF = E4M3, bool QH = false, bool EXT = false, bool F4 = false,
+          bool PAIR = false>
+__global__ void __launch_bounds__(kThreads<BN, EPI, PAIR>(), 1)
 mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmSA,
+               const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
   constexpr bool ZR = EPI == EPI_DSWIGLU;  // z streamed by TMA (tmO maps the BF16 z [R, 2F])
   constexpr bool EXT_ON = EPI != EPI_DSWIGLU || EXT;
   static_assert(!F4 || (EPI == EPI_BF16 || EPI == EPI_F32), "mxf4 operands: plain epilogues only");
-  using C = KCfg<BN, EPI, F4>;
+  using C = KCfg<BN, EPI, F4, PAIR>;
   constexpr bool PK = kParks<BN, EPI>();
+  // PAIR: clusters of two CTAs on 256-row tiles (grouped, BN = 256, FP8/FP6
+  // operands); tmSA / tmSB map the operands' blocked scales for the 2-SM loads
+  static_assert(!PAIR || (MODE == MODE_GROUPED && BN == 256 && !F4), "CTA pairs: grouped 256-column tiles");
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -502,11 +549,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* z_empty = z_full + C::Z_SLOTS;  // ZR: slot read by its Z_READERS epilogue warps
   uint64_t* tq_full = z_empty + C::Z_SLOTS;   // dynamic wgrad schedule: queue entry written
   uint64_t* tq_empty = tq_full + C::TQN;      // ... and read by the MMA thread and every epilogue warp
+  uint64_t* peer_read = tq_empty + C::TQN;    // PAIR, peer: its epilogue warps have read the accumulator
+  uint64_t* sf_ready = peer_read + 1;         // PAIR, leader: the stage's scales are in tensor memory
+  uint64_t* sf_final = sf_ready + C::STAGES;  // PAIR, leader: every scale copy has completed
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + C::OFF_PREF);  // PAIR: 256-row tiles before each expert
   volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + C::OFF_TQ);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;  // PAIR: 0 = leader (issues the MMAs), 1 = peer
+  const bool leader = rank == 0;
   // wgrad with a workspace: each CTA's producer claims the next tile (in the
   // order of get_tile: split parts, then experts by descending size) from a
   // counter the host zeroes, so tiles go to whichever CTA is free first
@@ -514,7 +567,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], C::EW); }
+    // PAIR: the leader's accumulator is handed back by its own epilogue
+    // warps plus one arrival from the peer
+    for (int a = 0; a < C::ACC; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], C::EW + (PAIR ? 1 : 0)); }
+    if (PAIR) {
+      mbar_init(peer_read, C::EW);
+      for (int s = 0; s < C::STAGES; s++) mbar_init(&sf_ready[s], 1);
+      mbar_init(sf_final, 1);
+    }
     mbar_init(final_bar, 1);
     mbar_init(epi_bar, C::EW);
     for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], C::Z_READERS); }
@@ -522,11 +582,28 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) { prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); prefetch_tensormap(&tmO); }
-  if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA); prefetch_tensormap(&tmB); prefetch_tensormap(&tmO);
+    if (PAIR) { prefetch_tensormap(&tmSA); prefetch_tensormap(&tmSB); }
+  }
+  if constexpr (PAIR) {
+    // tensor memory allocated by both CTAs of the pair at once (each gets the
+    // same columns); the row-tile table built before the pair meets
+    if (warp == 1) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                   :: "r"(smem_u32(tmem_slot)), "n"(C::TMEM_COLS) : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0) build_pair_prefix(p.offsets, p.G, p.R, pref, lane, leader ? &g_gemm_status : nullptr);
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs' barriers initialised before any remote arrival or 2-SM copy
+    tc_fence_after();
+  } else {
+    if (warp == 1) tmem_alloc<C::TMEM_COLS>(tmem_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   const uint32_t tmem_base = *tmem_slot;
   // wgrad: rank the experts by descending row count (ties by index)
   const uint16_t* order = nullptr;
@@ -613,12 +690,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
           if (end) break;
         } else {
-          if (i * gridDim.x >= p.num_tiles) break;
-          t = tile_index<MODE>(i);
+          if (i * tile_slots<PAIR>() >= p.num_tiles) break;
+          t = tile_index_x<MODE, PAIR>(i);
           if (t >= p.num_tiles) continue;
         }
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
+        Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, false, order, split, pref);
         if (!T.active || T.nk == 0) continue;
+        if (PAIR) T.m0 += 128 * rank;  // this CTA's 128 rows of the pair's 256
         int64_t brow[2];
         if (EPI == EPI_SWIGLU) {
           brow[0] = (int64_t)T.g * 2 * p.F + T.n0;
@@ -640,10 +718,29 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int64_t kc = T.kbeg / 128 + (F4 ? 2 * kb : kb);
           const uint32_t tx = F4 ? (uint32_t)(C::A_BYTES + C::B_BYTES + nch * (512 + (BN / 128) * 512))
                                  : p.tx_bytes;
-          mbar_arrive_expect_tx(&full[stage], tx);
-          armed_parity[stage] = (int)phase;
           // x coordinate: elements, or bytes of the packed payload with F4
           const int kx = (int)(F4 ? kc * 64 : kc * 128);
+          if constexpr (PAIR) {
+            // 2-SM loads: each CTA its 128 rows of A, its 128-row block of
+            // the tile's B slice and every scale chunk its tensor memory
+            // needs (its A rows', both B blocks'), all counted on the
+            // leader's barrier, which expects both CTAs' bytes
+            const uint32_t fb = leader_addr(&full[stage]);
+            if (leader) {
+              mbar_arrive_expect_tx(&full[stage], 2u * tx);
+              armed_parity[stage] = (int)phase;
+            }
+            tma2_load_2d(sA + stage * C::A_BYTES, &tmA, kx, (int)T.m0, fb, pol_a);
+            tma2_load_2d(sB + stage * C::B_BYTES, &tmB, kx, (int)brow[rank], fb, pol_b);
+            uint8_t* sf = sSF + stage * C::SF_BYTES;
+            tma2_load_3d(sf, &tmSA, 0, (int)kc, (int)(T.m0 >> 7), fb);
+            tma2_load_3d(sf + 512, &tmSB, 0, (int)kc, (int)(brow[0] >> 7), fb);
+            tma2_load_3d(sf + 1024, &tmSB, 0, (int)kc, (int)(brow[1] >> 7), fb);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            continue;
+          }
+          mbar_arrive_expect_tx(&full[stage], tx);
+          armed_parity[stage] = (int)phase;
           tma_load_2d(sA + stage * C::A_BYTES, &tmA, kx, (int)T.m0, &full[stage], pol_a);
 #pragma unroll
           for (int i = 0; i < BN / 128; i++)
@@ -670,7 +767,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (PAIR: the leader's, for both CTAs, M = 256)
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -687,18 +785,40 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
           if (t < 0) break;
         } else {
-          if (i * gridDim.x >= p.num_tiles) break;
-          t = tile_index<MODE>(i);
+          if (i * tile_slots<PAIR>() >= p.num_tiles) break;
+          t = tile_index_x<MODE, PAIR>(i);
           if (t >= p.num_tiles) continue;
         }
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
+        Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, false, order, split, pref);
         if (!T.active || T.nk == 0) continue;
-        if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+        // PAIR: the peer's hand-back arrives across the cluster (acquire at cluster scope)
+        if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1u, abort_flag)
+                   : mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, abort_flag, WAIT_BUDGET_NS))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < T.nk; kb++) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          // PAIR: the scale warp has seen the stage's bytes land and copied its scales
+          if (!mbar_wait_bounded(PAIR ? &sf_ready[stage] : &full[stage], phase, abort_flag, WAIT_BUDGET_NS)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
+          if constexpr (PAIR) {
+            const uint32_t sf_t = tmem_base + C::SF_TMEM_BASE + (uint32_t)(stage * C::SF_COLS);
+            const uint64_t ad = smem_desc(smem_u32(sA + stage * C::A_BYTES), 16, 1024, 2);
+            const uint64_t bd = smem_desc(smem_u32(sB + stage * C::B_BYTES), 16, 1024, 2);
+            const uint32_t idesc0 = mma_idesc_mx((uint32_t)p.a_type, (uint32_t)p.b_type, 256, BN, 0, 0);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+              tc2_mma_mx(d_tmem, ad + 2 * j, bd + 2 * j, idesc0 | ((uint32_t)j << 4) | ((uint32_t)j << 29), sf_t,
+                         sf_t + 4, (kb | j) != 0 ? 1u : 0u);
+            tc2_commit_both(&empty[stage]);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           const uint32_t sf_t = tmem_base + C::SF_TMEM_BASE + (uint32_t)(stage * C::SF_COLS);
           const uint32_t sf_s = smem_u32(sSF + stage * C::SF_BYTES);
           const uint32_t a_s = smem_u32(sA + stage * C::A_BYTES);
@@ -743,13 +863,51 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(&acc_full[acc]);
+        if (PAIR) tc2_commit_both(&acc_full[acc]);
+        else tc_commit(&acc_full[acc]);
         if (++acc == C::ACC) { acc = 0; acc_phase ^= 1u; }
       }
+      if (PAIR && !ok) *abort_flag = 1;
       // No MMA may still be writing tensor memory when it is freed.
       volatile int no_abort = 0;
-      tc_commit(final_bar);
+      if (PAIR) tc2_commit_local(final_bar);
+      else tc_commit(final_bar);
       mbar_wait_bounded(final_bar, 0, &no_abort, WAIT_BUDGET_NS);
+    }
+  } else if (PAIR && warp == kThreads<BN, EPI, PAIR>() / 32 - 1) {
+    // ------------------------------------------------------------ scale copies (PAIR, leader)
+    // In the MMA thread's stage order: wait for the stage's bytes (both
+    // CTAs'), copy its three scale chunks into both CTAs' tensor memory
+    // (tcgen05.cp .cta_group::2) and signal sf_ready once they completed.  A
+    // slot is rewritten only after the producers refilled its stage, i.e.
+    // after the MMAs that read it.
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t i = 0; ok; i++) {
+        if (i * tile_slots<PAIR>() >= p.num_tiles) break;
+        const int64_t t = tile_index_x<MODE, PAIR>(i);
+        if (t >= p.num_tiles) continue;
+        const Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, false, order, split, pref);
+        if (!T.active || T.nk == 0) continue;
+        for (int kb = 0; kb < T.nk; kb++) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sf_t = tmem_base + C::SF_TMEM_BASE + (uint32_t)(stage * C::SF_COLS);
+          const uint64_t sd = smem_desc(smem_u32(sSF + stage * C::SF_BYTES), 0, 128, 0);
+          tc2_copy_scales(sf_t, sd);                    // A's 128 rows (each CTA its own)
+          tc2_copy_scales(sf_t + 4, sd + (512 >> 4));   // B block 0
+          tc2_copy_scales(sf_t + 8, sd + (1024 >> 4));  // B block 1
+          tc2_commit_local(&sf_ready[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      // No copy may still be writing either CTA's tensor memory when it is freed.
+      volatile int no_abort = 0;
+      tc2_commit_local(sf_final);
+      mbar_wait_bounded(sf_final, 0, &no_abort, WAIT_BUDGET_NS);
     }
   } else if (ZR && warp == 2 + C::EW) {
     // ------------------------------------------------------------ z loader (ZR)
@@ -762,11 +920,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int armed_parity[C::Z_SLOTS > 0 ? C::Z_SLOTS : 1];
       for (int z = 0; z < C::Z_SLOTS; z++) armed_parity[z] = -1;
       bool ok = true;
-      for (int64_t i = 0; i * gridDim.x < p.num_tiles && ok; i++) {
-        const int64_t t = tile_index<MODE>(i);
+      for (int64_t i = 0; i * tile_slots<PAIR>() < p.num_tiles && ok; i++) {
+        const int64_t t = tile_index_x<MODE, PAIR>(i);
         if (t >= p.num_tiles) continue;
-        Tile T = get_tile<NT, MODE, F4>(p, t, false, order, split);
+        Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, false, order, split, pref);
         if (!T.active || T.nk == 0) continue;
+        if (PAIR && rank && !T.upper) continue;  // the epilogue skips a half past its segment
+        if (PAIR) T.m0 += 128 * rank;
         for (int hh = 0; hh < BN / C::Z_COLS; hh++) {
           if (!mbar_wait_bounded(&z_empty[zs], zph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
           mbar_arrive_expect_tx(&z_full[zs], (uint32_t)C::Z_SLOT);
@@ -794,6 +954,24 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int zslot = 0;           // ZR: next z slot and its phase
     uint32_t zphase = 0;
     uint32_t zt = 0;         // ZR, BN = 256: z slots of the tiles done (8 per tile)
+    // Hand accumulator a back to the MMA thread (after tc_fence_before and
+    // __syncwarp).  PAIR: the leader's warps arrive on its barrier; the
+    // peer's warps meet on their own and one of them then arrives across the
+    // pair (release at cluster scope), one remote message per tile.
+    uint32_t peer_phase = 0;
+    const uint32_t acc_empty_cl = PAIR ? leader_addr(acc_empty) : 0u;
+    auto release_acc = [&](int a) {
+      if (!PAIR || leader) {
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+      } else {
+        if (lane == 0) mbar_arrive(peer_read);
+        if (ew == 0) {
+          mbar_wait_bounded(peer_read, peer_phase, abort_flag, WAIT_BUDGET_NS);
+          peer_phase ^= 1u;
+          if (lane == 0) arrive_on_leader(acc_empty_cl);
+        }
+      }
+    };
     // Barrier among the epilogue warps, bounded like every other wait.
     auto epi_sync = [&]() -> bool {
       __syncwarp();
@@ -855,7 +1033,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // memory instead).
     auto prefetch_aux = [&](int64_t i) {
       if constexpr (EPI == EPI_DGELU) {
-        const int64_t t = tile_index<MODE>(i);
+        const int64_t t = tile_index_x<MODE, PAIR>(i);
         if (t >= p.num_tiles) return;
         const Tile U = get_tile<NT, MODE, F4>(p, t, false, order, split);
         if (!U.active || U.nk == 0) return;
@@ -877,13 +1055,15 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (++tqi == C::TQN) { tqi = 0; tqph ^= 1u; }
         if (t < 0) break;
       } else {
-        if (i * gridDim.x >= p.num_tiles) break;
-        t = tile_index<MODE>(i);
+        if (i * tile_slots<PAIR>() >= p.num_tiles) break;
+        t = tile_index_x<MODE, PAIR>(i);
         if (t >= p.num_tiles) continue;
       }
       prefetch_aux(i + 1);
-      Tile T = get_tile<NT, MODE, F4>(p, t, ew == 0 && lane == 0, order, split);
+      Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, ew == 0 && lane == 0, order, split, pref);
       if (!T.active) continue;
+      const bool dead = PAIR && rank && !T.upper;  // PAIR: an upper half past its expert's segment
+      if (PAIR) T.m0 += 128 * rank;                // this CTA's 128 rows of the pair's 256
       const int64_t row_in_tile = q * 32 + lane;
       if (T.nk == 0) {
         if (EPI == EPI_BF16) {  // zero-token expert: an exactly zero gradient slice
@@ -902,6 +1082,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, WAIT_BUDGET_NS)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (dead) {  // computed by the pair's MMAs, not stored
+        tc_fence_before();
+        __syncwarp();
+        release_acc(acc);
+        if (++acc == C::ACC) { acc = 0; acc_phase ^= 1u; }
+        continue;
+      }
 
       if constexpr (EPI == EPI_BF16) {
         constexpr int COLS = BN / 2;
@@ -912,7 +1099,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (C::ACC == 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
         bool store = true;
         const bool split_tile = MODE == MODE_WGRAD && T.parts > 1;
@@ -920,7 +1107,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (C::ACC == 2) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            release_acc(acc);
           }
           const int r = split_reduce(T, v);
           if (r < 0) break;
@@ -954,7 +1141,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (C::ACC == 2 && !split_tile) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
       } else if constexpr (EPI == EPI_F32) {
         // fp32 into the caller's gradient buffer: 32x16 blocks, TMA store
@@ -967,7 +1154,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (C::ACC == 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
         bool store = true;
         const bool split_tile = MODE == MODE_WGRAD && T.parts > 1;
@@ -975,7 +1162,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (C::ACC == 2) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            release_acc(acc);
           }
           const int r = split_reduce(T, v);
           if (r < 0) break;
@@ -997,7 +1184,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (C::ACC == 2 && !split_tile) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
         // accumulator columns: [0,128) gate of f0..f0+127, [128,256) up
@@ -1009,7 +1196,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[acc]);
+        release_acc(acc);
 
         const int64_t row = T.m0 + row_in_tile;
         const int64_t f0 = T.n0;
@@ -1112,7 +1299,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
 #pragma unroll 1
         for (int j = 0; j < NST; j++) {
@@ -1191,7 +1378,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!PK) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
         if (!epi_sync()) break;
         if (ew < 4 * NCK) {
@@ -1243,7 +1430,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tmem_wait_ld();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
 #pragma unroll 1
         for (int ch = 0; ch < nchw; ch++) {
@@ -1294,7 +1481,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!PK) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          release_acc(acc);
         }
         if (!epi_sync()) break;
         constexpr int NCK = BN / 128;  // scale chunks per orientation
@@ -1325,7 +1512,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) atomicOr(&g_gemm_status, DEV_TIMEOUT);
-  if (warp == 1) {
+  if constexpr (PAIR) {
+    cluster_sync_all();  // neither CTA frees tensor memory or exits while the other still uses the pair
+    tc_fence_after();
+    if (warp == 1)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "n"(C::TMEM_COLS)
+                   : "memory");
+    cluster_sync_all();
+  } else if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<C::TMEM_COLS>(tmem_base);
   }

@@ -23,6 +23,8 @@ enum Fmt : int { E4M3 = 0, E2M3 = 1, E2M1 = 2 };
 // bit 0: a bounded wait ran out; bit 1: malformed offsets seen on device;
 // bit 2: a routing index (expert id or source row) out of range.
 enum : unsigned { DEV_TIMEOUT = 1u, DEV_BAD_OFFSETS = 2u, DEV_BAD_INDEX = 4u };
+// Longest any bounded device-side wait spins before it gives up.
+constexpr uint64_t WAIT_BUDGET_NS = 2000000000ull;
 
 // ---------------------------------------------------------------------------
 // Element formats

@@ -107,6 +107,16 @@ struct GemmParams {
 
 // ta, tb: operand maps; to: the BF16 output map (32x32 boxes, 64-byte
 // swizzle) of the epilogue's BF16 output, or any valid map when it has none.
+// Experts the CTA-pair kernels' row-tile table holds (their device constant
+// MAX_PAIR_G).
+constexpr int MAX_PAIR_G_HOST = 1024;
+
+// The SwiGLU forward / dSwiGLU backward on CTA pairs: tsa / tsb map the
+// operands' blocked scales ([row blocks][K chunks][512 B], boxes of one
+// chunk of one row block) for the 2-SM scale loads.
+cudaError_t launch_gemm_pair_fused(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                                   const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to,
+                                   cudaStream_t s, int num_sms);
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to,
                         int bn, cudaStream_t s, int num_sms);
 cudaError_t launch_gemm_dense(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
