@@ -448,6 +448,9 @@ MX_API mx_status_t mx_grouped_gemm_dswiglu_probs_bwd(const mx_tensor_t *dy_row, 
  * separate gradient tensor and no add (Primus PR #1064 "feat(mxfp6): MXFP6
  * (E2M3) Flux linears, a fused MLP, and the MLPerf recipe", the commit that
  * writes wgrad into main_grad: a beta = 0 store, one microbatch per step).
+ * With MX_FUSED_PAIRS=1 in the environment and N, K multiples of 256 (this
+ * and the other weight-gradient calls) it runs on CTA pairs; the output
+ * bytes are the same either way.
  */
 MX_API mx_status_t mx_grouped_gemm_wgrad(const mx_tensor_t *a_col, const mx_tensor_t *b_col, int32_t G,
                                   const int32_t *offsets_dev, void *out_bf16, mx_stream_t stream);

@@ -368,16 +368,19 @@ struct OutView {
   bool f32 = false;  // fp32 elements (EPI_F32) instead of BF16
 };
 
-// Which fused epilogues run on CTA pairs (the outputs are the same bit for
-// bit either way).  By default the SwiGLU forward (4 % faster on pairs: its
-// mainloop is the limit) and not the dSwiGLU backward (5 % slower on pairs:
-// its epilogue is the limit); MX_FUSED_PAIRS=0 keeps both on one SM per
-// tile, MX_FUSED_PAIRS=1 puts both on pairs.  Read at every call.
-bool fused_pairs_enabled(int epi) {
+// Which fused-epilogue and weight-gradient launches run on CTA pairs (the
+// outputs are the same bit for bit either way).  By default only the SwiGLU
+// forward (0.73 -> 0.69-0.70 ms: its mainloop is the limit); the dSwiGLU
+// backward is bound by its epilogue (0.63 on one SM per tile, 0.66 on
+// pairs) and the weight gradients lose on pairs (dW1 0.70 -> 0.75 ms: half
+// as many units of twice the work for the claimed-tile balance under the
+// skewed routing).  MX_FUSED_PAIRS=0 keeps all on one SM per tile,
+// MX_FUSED_PAIRS=1 puts all on pairs.  Read at every call.
+bool fused_pairs_enabled(bool by_default) {
   const char* v = getenv("MX_FUSED_PAIRS");
   if (v && v[0] == '0') return false;
   if (v && v[0] == '1') return true;
-  return epi == mx::EPI_SWIGLU;
+  return by_default;
 }
 
 mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* b, int bn, cudaStream_t s,
@@ -408,7 +411,7 @@ mx_status_t run_gemm(mx::GemmParams p, const mx_tensor_t* a, const mx_tensor_t* 
     // its 128 A rows, one 128-row block of B and the scale chunks of its A
     // rows and of both B blocks
     p.tx_bytes = stage_tx_bytes(a->fmt, 128) + 512u;
-    p.num_tiles = ((p.R + 255) / 256 + (p.offsets ? (p.G + 1) / 2 : 0)) * p.n_tiles;
+    if (p.mode == mx::MODE_GROUPED) p.num_tiles = ((p.R + 255) / 256 + (p.offsets ? (p.G + 1) / 2 : 0)) * p.n_tiles;
     CUtensorMap tsa, tsb;
     if ((st = make_tmap_scales(&tsa, a->scale, a->rows, a->cols, 1, 1)) != MX_OK) return st;
     if ((st = make_tmap_scales(&tsb, b->scale, b->rows, b->cols, 1, 1)) != MX_OK) return st;
@@ -930,7 +933,7 @@ mx_status_t swiglu_fwd_impl(const mx_tensor_t* x_row, const mx_tensor_t* w1_row,
   p.q_cols = F;
   if ((st = attach_tap(&p, R, F)) != MX_OK) return st;
   return run_gemm(p, x_row, w1_row, 256, s, dev, OutView{z_bf16, R, 2 * F, 2 * F},
-                  fused_pairs_enabled(mx::EPI_SWIGLU) && G <= mx::MAX_PAIR_G_HOST);
+                  fused_pairs_enabled(true) && G <= mx::MAX_PAIR_G_HOST);
 }
 
 }  // namespace
@@ -992,7 +995,7 @@ mx_status_t dswiglu_bwd_impl(const mx_tensor_t* dy_row, const mx_tensor_t* w2t_r
   p.sfb_kchunks = p.sfa_kchunks;
   // 256-column tiles (the 128x256 MMA) where F allows, else 128
   const int tile_n = F % 256 == 0 ? 256 : 128;
-  const bool pair = tile_n == 256 && fused_pairs_enabled(mx::EPI_DSWIGLU) && G <= mx::MAX_PAIR_G_HOST;
+  const bool pair = tile_n == 256 && fused_pairs_enabled(false) && G <= mx::MAX_PAIR_G_HOST;
   p.m_tiles = (int)(R / 128);
   p.n_tiles = (int)(F / tile_n);
   p.num_tiles = (int64_t)p.m_tiles * p.n_tiles;
@@ -1103,6 +1106,8 @@ mx_status_t wgrad_common(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int
   DevInfo dev;
   if ((st = device_info(&dev)) != MX_OK) return st;
   const int bn = (K % 256 == 0) ? 256 : 128;
+  // CTA pairs on 256 x 256 tiles where the weight's rows and columns allow
+  const bool pair = bn == 256 && N % 256 == 0 && a_col->fmt != MX_E2M1 && fused_pairs_enabled(false);
   mx::GemmParams p = base_params();
   p.mode = mx::MODE_WGRAD;
   p.epi = epi;
@@ -1112,7 +1117,7 @@ mx_status_t wgrad_common(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int
   p.sfa = a_col->scale; p.sfb = b_col->scale;
   p.sfa_kchunks = (R / 32 + 3) / 4;
   p.sfb_kchunks = p.sfa_kchunks;
-  p.m_tiles = (int)(N / 128);
+  p.m_tiles = (int)(N / (pair ? 256 : 128));
   p.n_tiles = (int)(K / bn);
   p.num_tiles = (int64_t)G * p.m_tiles * p.n_tiles;
   if (epi == mx::EPI_F32) {
@@ -1135,12 +1140,14 @@ mx_status_t wgrad_common(const mx_tensor_t* a_col, const mx_tensor_t* b_col, int
     p.dyn_ctr = p.split_cnt + (int64_t)mx::MAX_SPLIT_EXPERTS * w.per_g;
     p.split_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + w.cnt_bytes);
     p.split_slots = w.slots;
-    p.split_extra = w.extra;
-    p.num_tiles += w.extra;
+    // pairs: the extra tiles (and the kernel's slots) count 256-row tiles,
+    // half as many; the workspace's slots and counters are the same bytes
+    p.split_extra = pair ? w.extra / 2 : w.extra;
+    p.num_tiles += p.split_extra;
     cudaError_t e = cudaMemsetAsync(workspace, 0, w.cnt_bytes, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the split counters");
   }
-  return run_gemm(p, a_col, b_col, bn, s, dev, OutView{out, (int64_t)G * N, K, K, epi == mx::EPI_F32});
+  return run_gemm(p, a_col, b_col, bn, s, dev, OutView{out, (int64_t)G * N, K, K, epi == mx::EPI_F32}, pair);
 }
 
 }  // namespace

@@ -24,13 +24,13 @@ static cudaError_t launch_one(const GemmParams& p, const CUtensorMap& ta, const 
 
 // The fused SwiGLU / dSwiGLU epilogues on CTA pairs (256-row tiles, two SMs
 // per tile): clusters of two CTAs, one pair per two SMs.
-template <int EPI, bool EXT>
+template <int EPI, int MODE, bool EXT>
 static cudaError_t launch_pair_one(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                                    const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to,
                                    cudaStream_t s, int num_sms) {
   constexpr int smem = KCfg<256, EPI, false, true>::SMEM_BYTES;
   {
-    const cudaError_t e = ensure_smem_attr<mx_gemm_kernel<256, EPI, MODE_GROUPED, E4M3, false, EXT, false, true>>(smem);
+    const cudaError_t e = ensure_smem_attr<mx_gemm_kernel<256, EPI, MODE, E4M3, false, EXT, false, true>>(smem);
     if (e != cudaSuccess) return e;
   }
   int64_t pairs = p.num_tiles < num_sms / 2 ? p.num_tiles : num_sms / 2;
@@ -47,18 +47,23 @@ static cudaError_t launch_pair_one(const GemmParams& p, const CUtensorMap& ta, c
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<256, EPI, MODE_GROUPED, E4M3, false, EXT, false, true>, ta, tb, to,
-                            tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<256, EPI, MODE, E4M3, false, EXT, false, true>, ta, tb, to, tsa,
+                            tsb, p);
 }
 
 cudaError_t launch_gemm_pair_fused(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                                    const CUtensorMap& tsa, const CUtensorMap& tsb, const CUtensorMap& to,
                                    cudaStream_t s, int num_sms) {
   const bool ext = p.tap != nullptr || p.probs != nullptr;
-  if (p.epi == EPI_SWIGLU) return launch_pair_one<EPI_SWIGLU, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+  if (p.mode == MODE_WGRAD) {
+    if (p.epi == EPI_F32) return launch_pair_one<EPI_F32, MODE_WGRAD, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+    if (p.epi == EPI_BF16) return launch_pair_one<EPI_BF16, MODE_WGRAD, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+    return cudaErrorInvalidValue;
+  }
+  if (p.epi == EPI_SWIGLU) return launch_pair_one<EPI_SWIGLU, MODE_GROUPED, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
   if (p.epi == EPI_DSWIGLU)
-    return ext ? launch_pair_one<EPI_DSWIGLU, true>(p, ta, tb, tsa, tsb, to, s, num_sms)
-               : launch_pair_one<EPI_DSWIGLU, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
+    return ext ? launch_pair_one<EPI_DSWIGLU, MODE_GROUPED, true>(p, ta, tb, tsa, tsb, to, s, num_sms)
+               : launch_pair_one<EPI_DSWIGLU, MODE_GROUPED, false>(p, ta, tb, tsa, tsb, to, s, num_sms);
   return cudaErrorInvalidValue;
 }
 

@@ -173,7 +173,7 @@ __device__ __forceinline__ int32_t ldg_i32(const int32_t* p) { return __ldg(p); 
 // row-block-major over all R rows; the expert is the segment holding the
 // row base.  Wgrad: tiles are expert-major; K runs over the expert's rows.
 // nk counts K chunks of 128 elements here.
-template <int NT, int MODE>
+template <int NT, int MODE, int MT = 128>
 __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, bool report, const uint16_t* order,
                                                 const SplitInfo* split) {
   Tile T;
@@ -224,7 +224,7 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
     T.g = (int)(tt / per_g);
     if (order) T.g = order[T.g];
     int64_t rem = tt % per_g;
-    T.m0 = (rem / p.n_tiles) * 128;
+    T.m0 = (rem / p.n_tiles) * MT;  // MT: 256-row tiles for CTA pairs
     T.n0 = (rem % p.n_tiles) * NT;
     int64_t end = p.offsets ? ldg_i32(p.offsets + T.g) : p.R;
     int64_t start = T.g ? ldg_i32(p.offsets + T.g - 1) : 0;
@@ -249,10 +249,10 @@ __device__ __forceinline__ Tile get_tile_chunks(const GemmParams& p, int64_t t, 
 
 // The same with nk in pipeline stages: with F4 a stage covers two chunks
 // and a tile with an odd chunk count ends on a half stage.
-template <int NT, int MODE, bool F4 = false>
+template <int NT, int MODE, bool F4 = false, int MT = 128>
 __device__ __forceinline__ Tile get_tile(const GemmParams& p, int64_t t, bool report, const uint16_t* order,
                                          const SplitInfo* split = nullptr) {
-  Tile T = get_tile_chunks<NT, MODE>(p, t, report, order, split);
+  Tile T = get_tile_chunks<NT, MODE, MT>(p, t, report, order, split);
   T.nc = T.nk;
   if (F4) T.nk = (T.nc + 1) >> 1;
   return T;
@@ -266,6 +266,10 @@ __device__ __forceinline__ Tile get_tile_x(const GemmParams& p, int64_t t, bool 
                                            const SplitInfo* split, const int32_t* pref) {
   if constexpr (!PAIR) {
     return get_tile<NT, MODE, F4>(p, t, report, order, split);
+  } else if constexpr (MODE == MODE_WGRAD) {
+    // wgrad: the weight rows in 256-row tiles (p.m_tiles of them), the rest
+    // as for one SM per tile
+    return get_tile<NT, MODE, F4, 256>(p, t, report, order, split);
   } else {
     Tile T;
     T.active = 0; T.g = 0; T.m0 = 0; T.n0 = (t % p.n_tiles) * NT; T.kbeg = 0; T.nk = 0; T.nc = 0;
@@ -297,7 +301,11 @@ __device__ __forceinline__ int64_t tile_slots() { return PAIR ? (int64_t)(gridDi
 
 template <int MODE, bool PAIR>
 __device__ __forceinline__ int64_t tile_index_x(int64_t i) {
-  if constexpr (PAIR) return i * (int64_t)(gridDim.x >> 1) + (int64_t)(blockIdx.x >> 1);
+  if constexpr (PAIR) {
+    const int64_t np = gridDim.x >> 1, pi = blockIdx.x >> 1;
+    if (MODE == MODE_WGRAD && (i & 1)) return i * np + (np - 1 - pi);  // boustrophedon, as for one SM
+    return i * np + pi;
+  }
   return tile_index<MODE>(i);
 }
 
@@ -529,7 +537,7 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   constexpr bool PK = kParks<BN, EPI>();
   // PAIR: clusters of two CTAs on 256-row tiles (grouped, BN = 256, FP8/FP6
   // operands); tmSA / tmSB map the operands' blocked scales for the 2-SM loads
-  static_assert(!PAIR || (MODE == MODE_GROUPED && BN == 256 && !F4), "CTA pairs: grouped 256-column tiles");
+  static_assert(!PAIR || (BN == 256 && !F4), "CTA pairs: 256-column tiles of FP8 / FP6 operands");
   constexpr int NT = (EPI == EPI_SWIGLU) ? 128 : BN;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -578,7 +586,13 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     mbar_init(final_bar, 1);
     mbar_init(epi_bar, C::EW);
     for (int z = 0; z < C::Z_SLOTS; z++) { mbar_init(&z_full[z], 1); mbar_init(&z_empty[z], C::Z_READERS); }
-    for (int e = 0; e < C::TQN; e++) { mbar_init(&tq_full[e], 1); mbar_init(&tq_empty[e], 1 + C::EW); }
+    // tile queue: read by the MMA thread and every epilogue warp; with PAIR
+    // the leader's entries are also read by its scale-copy warp and by the
+    // peer's producer and epilogue warps, which arrive across the pair
+    for (int e = 0; e < C::TQN; e++) {
+      mbar_init(&tq_full[e], 1);
+      mbar_init(&tq_empty[e], PAIR ? 3 + 2 * C::EW : 1 + C::EW);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -641,7 +655,8 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const int64_t nk = ok ? (e - b) / 128 : 0;
           if (nk <= p.split_min || nk <= p.split_chunks) break;
           const int parts = (int)((nk + p.split_chunks - 1) / p.split_chunks);
-          if (sb + parts * per_g > p.split_slots || x + (parts - 1) * per_g > p.split_extra) break;
+          // PAIR: every pair-tile slot is two 128-row slots
+          if ((PAIR ? 2 : 1) * (sb + parts * per_g) > p.split_slots || x + (parts - 1) * per_g > p.split_extra) break;
           si->parts[n] = parts;
           si->xbase[n] = (int)x;
           si->sbase[n] = (int)sb;
@@ -677,16 +692,31 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool ok = true;
       int qi = 0;
       uint32_t qph = 0;
-      int32_t next = dyn ? atomicAdd(p.dyn_ctr, 1) : 0;
+      int32_t next = (dyn && leader) ? atomicAdd(p.dyn_ctr, 1) : 0;
       for (int64_t i = 0; ok; i++) {
         int64_t t;
-        if (dyn) {  // claim one tile ahead, queue this one for the MMA thread and the epilogue
+        if (dyn && PAIR && !leader) {  // the peer takes the tiles its leader claimed
+          if (!mbar_wait_cluster(&tq_full[qi], qph, abort_flag)) { ok = false; break; }
+          t = tq[qi];
+          arrive_on_leader(leader_addr(&tq_empty[qi]));
+          if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
+          if (t < 0) break;
+        } else if (dyn) {  // claim one tile ahead, queue this one for the MMA thread and the epilogue
           t = next;
           const bool end = t >= p.num_tiles;
           if (!end) next = atomicAdd(p.dyn_ctr, 1);
-          if (!mbar_wait_bounded(&tq_empty[qi], qph ^ 1u, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
-          tq[qi] = end ? -1 : (int32_t)t;
+          if (!(PAIR ? mbar_wait_cluster(&tq_empty[qi], qph ^ 1u, abort_flag)
+                     : mbar_wait_bounded(&tq_empty[qi], qph ^ 1u, abort_flag, WAIT_BUDGET_NS))) {
+            ok = false;
+            break;
+          }
+          const int32_t v = end ? -1 : (int32_t)t;
+          tq[qi] = v;
           mbar_arrive(&tq_full[qi]);
+          if (PAIR) {  // the same entry in the peer's queue
+            st_cluster_u32(peer_addr((const void*)&tq[qi]), (uint32_t)v);
+            arrive_on_leader(peer_addr(&tq_full[qi]));
+          }
           if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
           if (end) break;
         } else {
@@ -885,10 +915,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int qi = 0;
+      uint32_t qph = 0;
       for (int64_t i = 0; ok; i++) {
-        if (i * tile_slots<PAIR>() >= p.num_tiles) break;
-        const int64_t t = tile_index_x<MODE, PAIR>(i);
-        if (t >= p.num_tiles) continue;
+        int64_t t;
+        if (dyn) {  // the claimed tiles, in queue order
+          if (!mbar_wait_bounded(&tq_full[qi], qph, abort_flag, WAIT_BUDGET_NS)) { ok = false; break; }
+          t = tq[qi];
+          mbar_arrive(&tq_empty[qi]);
+          if (++qi == C::TQN) { qi = 0; qph ^= 1u; }
+          if (t < 0) break;
+        } else {
+          if (i * tile_slots<PAIR>() >= p.num_tiles) break;
+          t = tile_index_x<MODE, PAIR>(i);
+          if (t >= p.num_tiles) continue;
+        }
         const Tile T = get_tile_x<NT, MODE, F4, PAIR>(p, t, false, order, split, pref);
         if (!T.active || T.nk == 0) continue;
         for (int kb = 0; kb < T.nk; kb++) {
@@ -992,8 +1033,16 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       constexpr int COLS = BN / 2;
       const int64_t row = q * 32 + lane;
       const int64_t tile_floats = 128ll * BN;
+      // PAIR: each CTA's 128 rows of a pair tile are a sub-tile of their
+      // own: part k of this CTA's rows in slot 2 (slot + k) + rank, its
+      // arrival counter at 2 cnt + rank (the workspace holds as many slots
+      // and counters as for one SM per 128-row tile)
+      const int64_t sl0 = PAIR ? 2 * T.slot + rank : T.slot;  // part 0's slot
+      const int64_t sstride = PAIR ? 2 : 1;                     // slots between parts
+      const int64_t cnt = PAIR ? 2 * (int64_t)T.cnt + rank : (int64_t)T.cnt;
       // float4 index of (column group grp, this row): grp * 128 + row
-      float4* own = reinterpret_cast<float4*>(p.split_ws + (T.slot + T.part) * tile_floats) + half * (COLS / 4) * 128 + row;
+      float4* own = reinterpret_cast<float4*>(p.split_ws + (sl0 + sstride * T.part) * tile_floats) +
+                    half * (COLS / 4) * 128 + row;
 #pragma unroll
       for (int i = 0; i < COLS / 32; i++) {
 #pragma unroll
@@ -1005,11 +1054,11 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       __threadfence();
       if (!epi_sync()) return -1;
       volatile int* flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-      if (ew == 0 && lane == 0) *flag = atomicAdd(p.split_cnt + T.cnt, 1) == T.parts - 1 ? 1 : 0;
+      if (ew == 0 && lane == 0) *flag = atomicAdd(p.split_cnt + cnt, 1) == T.parts - 1 ? 1 : 0;
       if (!epi_sync()) return -1;
       if (*flag == 0) return 0;
       __threadfence();
-      const float4* base = reinterpret_cast<const float4*>(p.split_ws + T.slot * tile_floats) + half * (COLS / 4) * 128 + row;
+      const float4* base = reinterpret_cast<const float4*>(p.split_ws + sl0 * tile_floats) + half * (COLS / 4) * 128 + row;
 #pragma unroll
       for (int i = 0; i < COLS / 32; i++) {
 #pragma unroll
@@ -1018,14 +1067,14 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                           __uint_as_float(v[i][4 * c + 2]), __uint_as_float(v[i][4 * c + 3]));
           float4 sum = T.part == 0 ? mine : __ldcg(base + (i * 8 + c) * 128);
           for (int pp = 1; pp < T.parts; pp++) {
-            const float4 x = pp == T.part ? mine : __ldcg(base + pp * (tile_floats / 4) + (i * 8 + c) * 128);
+            const float4 x = pp == T.part ? mine : __ldcg(base + pp * sstride * (tile_floats / 4) + (i * 8 + c) * 128);
             sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
           }
           v[i][4 * c] = __float_as_uint(sum.x); v[i][4 * c + 1] = __float_as_uint(sum.y);
           v[i][4 * c + 2] = __float_as_uint(sum.z); v[i][4 * c + 3] = __float_as_uint(sum.w);
         }
       }
-      if (ew == 0 && lane == 0) p.split_cnt[T.cnt] = 0;  // ready for the next launch
+      if (ew == 0 && lane == 0) p.split_cnt[cnt] = 0;  // ready for the next launch
       return 1;
     };
     // dGELU reads a saved activation per tile: prefetch a tile's rows into
@@ -1048,10 +1097,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int64_t i = 0;; i++) {
       int64_t t;
       if (dyn) {
-        if (!mbar_wait_bounded(&tq_full[tqi], tqph, abort_flag, WAIT_BUDGET_NS)) break;
+        // PAIR peer: the entry was written across the pair, and its slot is
+        // handed back to the leader's producer across the pair
+        if (!(PAIR && !leader ? mbar_wait_cluster(&tq_full[tqi], tqph, abort_flag)
+                              : mbar_wait_bounded(&tq_full[tqi], tqph, abort_flag, WAIT_BUDGET_NS)))
+          break;
         t = tq[tqi];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tq_empty[tqi]);
+        if (lane == 0) {
+          if (PAIR && !leader) arrive_on_leader(leader_addr(&tq_empty[tqi]));
+          else mbar_arrive(&tq_empty[tqi]);
+        }
         if (++tqi == C::TQN) { tqi = 0; tqph ^= 1u; }
         if (t < 0) break;
       } else {

@@ -42,6 +42,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
   }
 }
+// The peer CTA's (rank 1) shared::cluster address of a local shared address.
+__device__ __forceinline__ uint32_t peer_addr(const void* p) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 1;" : "=r"(r) : "r"(smem_u32(p)));
+  return r;
+}
+// A 32-bit store into the shared memory of a CTA of the cluster.
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr_cl, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr_cl), "r"(v) : "memory");
+}
 __device__ __forceinline__ void arrive_on_leader(uint32_t bar_cl) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar_cl) : "memory");
 }

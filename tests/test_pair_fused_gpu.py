@@ -1,14 +1,15 @@
-"""The fused SwiGLU forward and dSwiGLU backward on CTA pairs.
+"""The fused SwiGLU forward, dSwiGLU backward and ragged-K weight gradient
+on CTA pairs.
 
-MX_FUSED_PAIRS=1 runs both fused epilogues on CTA pairs (256-row tiles,
-.cta_group::2 MMAs; by default only the SwiGLU forward), MX_FUSED_PAIRS=0
-keeps both on one SM per tile.
-The two are the same K order of block-scaled MMAs into fp32 and the same
-epilogue code, so every output byte must agree: the requantized payloads and
-scales of both orientations, the BF16 pre-activation save, the routing
-probability gradient -- including segments with an odd number of 128-row
-blocks, whose last 256-row tile computes an upper half that must not be
-stored, and a poisoned inactive tail."""
+MX_FUSED_PAIRS=1 runs all three on CTA pairs (256-row tiles, .cta_group::2
+MMAs; by default only the SwiGLU forward), MX_FUSED_PAIRS=0 keeps all on one
+SM per tile.  The two are the same K order of block-scaled MMAs into fp32
+and the same epilogue code, so every output byte must agree: the requantized
+payloads and scales of both orientations, the BF16 pre-activation save, the
+routing-probability gradient, the weight gradients (split or not) --
+including segments with an odd number of 128-row blocks, whose last 256-row
+tile computes an upper half that must not be stored, and a poisoned
+inactive tail."""
 import numpy as np
 import pytest
 
@@ -97,3 +98,53 @@ def test_fused_pairs_equal_single_sm(cuda_lib, monkeypatch, F, counts, use_probs
     bs = _bwd(mx, G, R, F, offs, dyr, w2t, fs[4], probs, use_probs)
     _equal(fp, fs, ["h_row", "h_row scales", "h_col", "h_col scales", "z"])
     _equal(bp, bs, ["dz_row", "dz_row scales", "dz_col", "dz_col scales", "dprobs"])
+
+
+@pytest.mark.parametrize("counts,ws,f32", [
+    ([384, 0, 1920, 128, 640], False, False),   # one SM per tile's dealt order vs the pairs' (static)
+    ([384, 0, 1920, 128, 640], True, False),    # claimed tiles and the largest expert's K range split
+    ([256, 2816, 0, 512], True, True),          # fp32 store into main_grad, split
+])
+def test_wgrad_pairs_equal_single_sm(cuda_lib, monkeypatch, counts, ws, f32):
+    """The ragged-K weight gradient on CTA pairs (256 x 256 tiles of the
+    weight, the claimed-tile queue shared across the pair, each CTA's K-split
+    partials in slots of their own) equals one SM per tile byte for byte,
+    zero-token experts included."""
+    import torch
+    mx = cuda_lib
+    G = len(counts)
+    offsets = W.offsets_from_counts(counts)
+    R = int(offsets[-1]) + 128
+    N, K = 512, 768   # dW rows (a_col) and columns (b_col)
+    rng = np.random.default_rng(len(counts) * 7 + (1 if ws else 0))
+    a = to_dev(W.normal_bf16(rng, (R, N), std=1e-3))
+    b = to_dev(W.normal_bf16(rng, (R, K)))
+    _, a_col, _ = mx.mx_quantize(a, mx.E4M3, False, True)
+    _, b_col, _ = mx.mx_quantize(b, mx.E4M3, False, True)
+    offs = torch.from_numpy(offsets).cuda()
+
+    def run():
+        if f32:
+            out = torch.full((G, N, K), float("nan"), dtype=torch.float32, device="cuda")
+            if ws:
+                mx.mx_grouped_gemm_wgrad_f32_ws(a_col, b_col, G, offs, out)
+            else:
+                mx.mx_grouped_gemm_wgrad_f32(a_col, b_col, G, offs, out)
+        else:
+            out = torch.full((G, N, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+            if ws:
+                mx.mx_grouped_gemm_wgrad_ws(a_col, b_col, G, offs, out=out)
+            else:
+                mx.mx_grouped_gemm_wgrad(a_col, b_col, G, offs, out=out)
+        torch.cuda.synchronize()
+        assert mx.mx_get_device_status() == "MX_OK"
+        return out
+
+    monkeypatch.setenv("MX_FUSED_PAIRS", "1")
+    pair = run()
+    monkeypatch.setenv("MX_FUSED_PAIRS", "0")
+    single = run()
+    _equal([pair], [single], ["dW"])
+    empty = [g for g, c in enumerate(counts) if c == 0]
+    for g in empty:   # a zero-token expert's slice is exactly zero
+        assert bool((pair[g] == 0).all())
