@@ -69,12 +69,12 @@ def stage_flops(D, F, R):
 # changes, until it is captured again.
 TRAFFIC_SCALE = 4
 SMALL_CASE_TRAFFIC = {
-    "fc1_swiglu": (242.3e6 + 261.9e6, "profiles/launches_moe_mlp_step.md"),
-    "fc2": (103.9e6 + 217.0e6, "profiles/launches_moe_mlp_step.md"),
-    "fc2_dgrad_dswiglu": (424.6e6 + 153.0e6, "profiles/launches_moe_mlp_step.md"),
-    "fc1_dgrad": (207.7e6 + 227.5e6, "profiles/launches_moe_mlp_step.md"),
-    "wgrad_dw2": (200.1e6 + 58.0e6, "profiles/launches_moe_mlp_step.md"),
-    "wgrad_dw1": (252.5e6 + 161.4e6, "profiles/launches_moe_mlp_step.md"),
+    "fc1_swiglu": (242.4e6 + 264.6e6, "profiles/launches_moe_mlp_step.md"),
+    "fc2": (103.9e6 + 217.5e6, "profiles/launches_moe_mlp_step.md"),
+    "fc2_dgrad_dswiglu": (423.4e6 + 153.0e6, "profiles/launches_moe_mlp_step.md"),
+    "fc1_dgrad": (207.7e6 + 228.7e6, "profiles/launches_moe_mlp_step.md"),
+    "wgrad_dw2": (198.0e6 + 56.6e6, "profiles/launches_moe_mlp_step.md"),
+    "wgrad_dw1": (253.0e6 + 161.6e6, "profiles/launches_moe_mlp_step.md"),
 }
 
 
