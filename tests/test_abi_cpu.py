@@ -226,5 +226,15 @@ def test_pair_gemm_rejections(mx):
     a5, b5 = _t(512, 256), _t(1025 * 256, 256)
     st = L.mx_grouped_gemm_2sm(ctypes.byref(a5), ctypes.byref(b5), 1025, FAKE, FAKE, 256, None)
     assert mx.STATUS[st] == "MX_ERR_NOT_SUPPORTED" and "1024" in mx.mx_last_error()
+    # the pair bias form: a bias is required, 16-byte aligned, and at least one expert
+    st = L.mx_grouped_gemm_bias_2sm(ctypes.byref(_t(512, 256)), ctypes.byref(_t(512, 256)), 1, FAKE, None, FAKE,
+                                    512, None)
+    assert mx.STATUS[st] == "MX_ERR_ALIGNMENT" and "bias" in mx.mx_last_error()
+    st = L.mx_grouped_gemm_bias_2sm(ctypes.byref(_t(512, 256)), ctypes.byref(_t(512, 256)), 1, FAKE, FAKE + 8, FAKE,
+                                    512, None)
+    assert mx.STATUS[st] == "MX_ERR_ALIGNMENT"
+    st = L.mx_grouped_gemm_bias_2sm(ctypes.byref(_t(512, 256)), ctypes.byref(_t(512, 256)), 0, FAKE, FAKE, FAKE,
+                                    512, None)
+    assert mx.STATUS[st] == "MX_ERR_INVALID_ARG"
     assert L.mx_moe_route_rows_pad(100, 8, 4, 256) == (800 + 255 * 4 + 255) // 256 * 256
     assert L.mx_moe_route_rows_pad(100, 8, 4, 200) == 0
