@@ -296,11 +296,13 @@ def test_mlp_step_full_size_sampled_parity(cuda_lib, routing):
 
 
 def test_swiglu_probs_fwd_bwd_full_size_sampled_rows(cuda_lib, routing):
-    """The routing-probability forms at full size: h = swiglu(z) * p[r]
-    requantized (sampled rows within one step), and the backward's dz =
-    dSwiGLU(dh * p) bytes and dprobs[r] = sum_f dh * swiglu(z) on the same
-    rows (z saved by the forward, so the backward's input is the GPU's own
-    BF16 z, which the oracle reads as given)."""
+    """The routing-probability forms at full size with the debug tap
+    attached: the forward's fp32 h = swiglu(z) * p[r] and the backward's fp32
+    dz = dSwiGLU(dh * p) within tolerance of the oracle on sampled rows, both
+    requantized orientations (payload and scale bytes) equal to the oracle's
+    quantization of those fp32 values, and dprobs[r] = sum_f dh * swiglu(z)
+    on the same rows (z saved by the forward, so the backward's input is the
+    GPU's own BF16 z, which the oracle reads as given)."""
     import torch
     counts, offsets, big, empty, small = routing
     x = _rand_bf16((R, D), 1.0, 111)
@@ -313,15 +315,26 @@ def test_swiglu_probs_fwd_bwd_full_size_sampled_rows(cuda_lib, routing):
     offs = torch.from_numpy(offsets).cuda()
     xr, _, _ = cuda_lib.mx_quantize(x, O.E4M3, True, False)
     wr, _, _ = cuda_lib.mx_quantize(w1, O.E4M3, True, False)
-    z, h_row, _ = cuda_lib.mx_grouped_gemm_swiglu_probs_fwd(xr, wr, G, offs, probs)
+    tap_h = torch.full((R, F), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_debug_tap(tap_h)
+    try:
+        z, h_row, h_col = cuda_lib.mx_grouped_gemm_swiglu_probs_fwd(xr, wr, G, offs, probs)
+    finally:
+        cuda_lib.mx_debug_tap(None)
     dyr, _, _ = cuda_lib.mx_quantize(dy, O.E4M3, True, False)
     wtr, _, _ = cuda_lib.mx_quantize(w2t, O.E4M3, True, False)
-    dz_row, _, dprobs = cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, wtr, z, probs, G, offs)
+    tap_dz = torch.full((R, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_debug_tap(tap_dz)
+    try:
+        dz_row, dz_col, dprobs = cuda_lib.mx_grouped_gemm_dswiglu_probs_bwd(dyr, wtr, z, probs, G, offs)
+    finally:
+        cuda_lib.mx_debug_tap(None)
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     rows = _sample_rows(offsets, [big, small], per=16, seed=5)
     idx = torch.from_numpy(rows).cuda()
     p = probs[idx].cpu().numpy().astype(np.float64)
-    hp, dzp = h_row.data[idx].cpu().numpy(), dz_row.data[idx].cpu().numpy()
+    hg = tap_h[idx].cpu().numpy().astype(np.float64)
+    dzg = tap_dz[idx].cpu().numpy().astype(np.float64)
     dpg = dprobs[idx].cpu().numpy().astype(np.float64)
     xb, dyb, zb = _bits(x[idx]), _bits(dy[idx]), _bits(z[idx])
     for e in sorted({_expert_of(offsets, r) for r in rows}):
@@ -330,18 +343,19 @@ def test_swiglu_probs_fwd_bwd_full_size_sampled_rows(cuda_lib, routing):
         wq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w1[e])), O.E4M3), 2 * F, D, O.E4M3)
         zref = xq @ wq.T
         h = O.round_f32(O.swiglu(zref[:, :F], zref[:, F:]) * p[sel][:, None])
-        assert np.mean(hp[sel] != O.quantize_rows(h, O.E4M3)[0]) < 1e-2
+        assert O.within_tolerance(hg[sel], h).all(), e
         dyq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(dyb[sel]), O.E4M3), int(sel.sum()), D, O.E4M3)
         w2q = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w2t[e])), O.E4M3), F, D, O.E4M3)
         zf = O.bf16_to_f64(zb[sel])
         dh = dyq @ w2q.T
         act = O.swiglu(zf[:, :F], zf[:, F:])
         dg, du = O.dswiglu(dh * p[sel][:, None], zf[:, :F], zf[:, F:])
-        ref_p, _ = O.quantize_rows(O.round_f32(np.concatenate([dg, du], axis=1)), O.E4M3)
-        assert np.mean(dzp[sel] != ref_p) < 1e-2
+        assert O.within_tolerance(dzg[sel], O.round_f32(np.concatenate([dg, du], axis=1))).all(), e
         want = np.sum(dh * act, axis=1)
         # dprobs is one vector: the tolerance's "row" is the sampled vector
         assert O.within_tolerance(dpg[sel][None, :], want[None, :]).all(), e
+    assert_tap_requant_exact_sampled(h_row, h_col, tap_h, rows, what="h * p")
+    assert_tap_requant_exact_sampled(dz_row, dz_col, tap_dz, rows, what="dSwiGLU(dh * p)")
 
 
 def test_wgrad_into_fp32_full_size_sampled_entries(cuda_lib, routing):
