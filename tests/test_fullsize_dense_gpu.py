@@ -56,39 +56,79 @@ def _sub_row(mx_t, rows, cols, fmt=E2M3):
     return pay, blocked
 
 
+def _tapped(cuda_lib, fn):
+    """Run fn with a NaN-filled fp32 debug tap [M, H] attached; returns
+    (fn's result, the tap on the GPU)."""
+    import torch
+    tap = torch.full((M, H), float("nan"), dtype=torch.float32, device="cuda")
+    cuda_lib.mx_debug_tap(tap)
+    try:
+        out = fn()
+    finally:
+        cuda_lib.mx_debug_tap(None)
+    return out, tap
+
+
+def _assert_tap_exact_blocks(tap, gpu_row, gpu_col, what):
+    """The epilogue's own fp32 values on the sampled blocks (the tap, before
+    the rotation), quantized by the oracle with the Hadamard rotation, give
+    the sampled rowwise and columnwise payload and scale bytes exactly (the
+    samples are whole 32-row and 32-column blocks)."""
+    t = tap[_idx(ROWS)][:, _idx(COLS)].cpu().numpy().astype(np.float64)
+    rp, rs = O.quantize_rows(t, E2M3, True)
+    gp, gs = _sub_row(gpu_row, ROWS, COLS)
+    assert np.array_equal(gp, rp), "%s rowwise payload differs in %d bytes" % (what, int((gp != rp).sum()))
+    assert np.array_equal(gs, rs), "%s rowwise scales differ" % what
+    cp, cs = O.quantize_rows(np.ascontiguousarray(t.T), E2M3, True)
+    gp, gs = _sub_row(gpu_col, COLS, ROWS)
+    assert np.array_equal(gp, cp), "%s columnwise payload differs in %d bytes" % (what, int((gp != cp).sum()))
+    assert np.array_equal(gs, cs), "%s columnwise scales differ" % what
+
+
 def test_dense_fc1_gelu_full_size_sampled_blocks(cuda_lib):
-    """pre = x W1^T + b1 (BF16) within tolerance; act = gelu(pre) packed
-    rowwise and columnwise within one quantization step, on 64 x 64 samples."""
+    """pre = x W1^T + b1 (BF16) within tolerance; the epilogue's fp32 act =
+    gelu(pre) (debug tap) within tolerance of the oracle, and act packed
+    rowwise and columnwise byte-equal to the oracle's quantization of those
+    fp32 values (rotation included), on 64 x 64 samples; the packed bytes
+    also within one quantization step of the oracle's own act."""
     x = _rand_bf16((M, D), 1.0, 71)
     w1 = _rand_bf16((H, D), 0.02, 72)
     b1 = _rand_bf16((H,), 0.02, 73)
     xr, _, _ = cuda_lib.mx_quantize(x, E2M3, True, False, True)
     wr, _, _ = cuda_lib.mx_quantize(w1, E2M3, True, False, True)
-    pre, act_row, act_col = cuda_lib.mx_gemm_gelu_fwd(xr, wr, b1)
+    (pre, act_row, act_col), tap = _tapped(cuda_lib, lambda: cuda_lib.mx_gemm_gelu_fwd(xr, wr, b1))
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     xq = _deq_rows(O.bf16_to_f64(_bits(x[_idx(ROWS)])))
     wq = _deq_rows(O.bf16_to_f64(_bits(w1[_idx(COLS)])))
     ref = O.gelu_fwd(xq, wq, O.bf16_to_f64(_bits(b1))[COLS], E2M3, True)
     got = bf16_cpu(pre[_idx(ROWS)][:, _idx(COLS)])
     assert O.within_tolerance(got, ref["pre"]).all()
+    t = tap[_idx(ROWS)][:, _idx(COLS)].cpu().numpy().astype(np.float64)
+    assert O.within_tolerance(t, ref["act"]).all()
+    _assert_tap_exact_blocks(tap, act_row, act_col, "act")
     requant_close(_sub_row(act_row, ROWS, COLS), ref["act_row"], len(ROWS), len(COLS), E2M3)
     requant_close(_sub_row(act_col, COLS, ROWS), ref["act_col"], len(COLS), len(ROWS), E2M3)
 
 
 def test_dense_dgelu_full_size_sampled_blocks(cuda_lib):
-    """dpre = (dY W2) * gelu'(pre) from the BF16 save, packed both ways, on
-    64 x 64 samples (W2's columnwise quantization gives the W2^T operand)."""
+    """dpre = (dY W2) * gelu'(pre) from the BF16 save: the epilogue's fp32
+    dpre (debug tap) within tolerance of the oracle and packed both ways
+    byte-equal to the oracle's quantization of it, on 64 x 64 samples (W2's
+    columnwise quantization gives the W2^T operand)."""
     dy = _rand_bf16((M, D), 1e-3, 81)
     w2 = _rand_bf16((D, H), 0.02, 82)
     pre = _rand_bf16((M, H), 1.5, 83)
     dyr, _, _ = cuda_lib.mx_quantize(dy, E2M3, True, False, True)
     _, w2t, _ = cuda_lib.mx_quantize(w2, E2M3, False, True, True)
-    dpre_row, dpre_col, _ = cuda_lib.mx_gemm_dgelu_bwd(dyr, w2t, pre)
+    (dpre_row, dpre_col, _), tap = _tapped(cuda_lib, lambda: cuda_lib.mx_gemm_dgelu_bwd(dyr, w2t, pre))
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     dyq = _deq_rows(O.bf16_to_f64(_bits(dy[_idx(ROWS)])))
     w2tq = _deq_rows(O.bf16_to_f64(_bits(w2[:, _idx(COLS)])).T.copy())
     pre_s = _bits(pre[_idx(ROWS)][:, _idx(COLS)])
     ref = O.dgelu_bwd(dyq, w2tq, pre_s, E2M3, True)
+    t = tap[_idx(ROWS)][:, _idx(COLS)].cpu().numpy().astype(np.float64)
+    assert O.within_tolerance(t, ref["dpre"]).all()
+    _assert_tap_exact_blocks(tap, dpre_row, dpre_col, "dpre")
     requant_close(_sub_row(dpre_row, ROWS, COLS), ref["dpre_row"], len(ROWS), len(COLS), E2M3)
     requant_close(_sub_row(dpre_col, COLS, ROWS), ref["dpre_col"], len(COLS), len(ROWS), E2M3)
 
