@@ -152,14 +152,21 @@ def test_dense_wgrad_full_size_sampled_entries(cuda_lib):
 
 def test_mxfp4_gemm_full_size_sampled_blocks(cuda_lib):
     """The dense MXFP4 GEMM of the benchmark (16384 x 12288 x 3072, E2M1 on
-    tcgen05 kind::mxf4) on a 64 x 64 sample of the output."""
+    tcgen05 kind::mxf4) on a 64 x 64 sample of the output, from both the
+    single-SM kernel and the CTA-pair kernel the benchmark's MXFP4 figure
+    times; the two outputs are also equal byte for byte in full."""
+    import torch
     a = _rand_bf16((M, D), 1.0, 101)
     b = _rand_bf16((H, D), 0.02, 102)
     ar, _, _ = cuda_lib.mx_quantize(a, O.E2M1, True, False)
     br, _, _ = cuda_lib.mx_quantize(b, O.E2M1, True, False)
     out = cuda_lib.mx_gemm_bias(ar, br, None)
+    pair = torch.full((M, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm_2sm(ar, br, 1, None, out=pair)
     assert cuda_lib.mx_get_device_status() == "MX_OK"
     aq = _deq_rows(O.bf16_to_f64(_bits(a[_idx(ROWS)])), O.E2M1, False)
     bq = _deq_rows(O.bf16_to_f64(_bits(b[_idx(COLS)])), O.E2M1, False)
-    got = bf16_cpu(out[_idx(ROWS)][:, _idx(COLS)])
-    assert O.within_tolerance(got, aq @ bq.T).all()
+    for o in (out, pair):
+        got = bf16_cpu(o[_idx(ROWS)][:, _idx(COLS)])
+        assert O.within_tolerance(got, aq @ bq.T).all()
+    assert torch.equal(out.view(torch.int16), pair.view(torch.int16))

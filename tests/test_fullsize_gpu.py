@@ -89,6 +89,9 @@ def test_fc1_swiglu_full_size_sampled_rows(cuda_lib, routing):
 
 
 def test_fc2_full_size_sampled_rows(cuda_lib, routing):
+    """FC2 at full size on one SM per tile and on CTA pairs: the two outputs
+    byte-equal, and sampled rows of the largest and a small expert within
+    tolerance of the oracle."""
     import torch
     counts, offsets, big, empty, small = routing
     h = _rand_bf16((R, F), 0.5, 21)
@@ -98,14 +101,21 @@ def test_fc2_full_size_sampled_rows(cuda_lib, routing):
     w2r, _, _ = cuda_lib.mx_quantize(w2, O.E4M3, True, False)
     y = torch.full((R, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     cuda_lib.mx_grouped_gemm(hr, w2r, G, offs, out=y)
+    # the same product on CTA pairs (the kernel the step runs FC2 on)
+    y2 = torch.full((R, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cuda_lib.mx_grouped_gemm_2sm(hr, w2r, G, offs, out=y2)
+    assert cuda_lib.mx_get_device_status() == "MX_OK"
+    A = int(offsets[-1])
+    assert torch.equal(y[:A].view(torch.int16), y2[:A].view(torch.int16))
     rows = _sample_rows(offsets, [big, small], seed=1)
-    yg = bf16_cpu(y[torch.from_numpy(rows).cuda()])
     hb = _bits(h[torch.from_numpy(rows).cuda()])
-    for g in sorted({_expert_of(offsets, r) for r in rows}):
-        sel = np.array([_expert_of(offsets, r) == g for r in rows])
-        hq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(hb[sel]), O.E4M3), int(sel.sum()), F, O.E4M3)
-        wq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w2[g])), O.E4M3), D, F, O.E4M3)
-        assert O.within_tolerance(yg[sel], hq @ wq.T).all(), g
+    for out in (y, y2):
+        yg = bf16_cpu(out[torch.from_numpy(rows).cuda()])
+        for g in sorted({_expert_of(offsets, r) for r in rows}):
+            sel = np.array([_expert_of(offsets, r) == g for r in rows])
+            hq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(hb[sel]), O.E4M3), int(sel.sum()), F, O.E4M3)
+            wq = O.dequantize_rows(*O.quantize_rows(O.bf16_to_f64(_bits(w2[g])), O.E4M3), D, F, O.E4M3)
+            assert O.within_tolerance(yg[sel], hq @ wq.T).all(), g
 
 
 def test_dswiglu_full_size_sampled_rows(cuda_lib, routing):
