@@ -264,8 +264,8 @@ MX_API mx_status_t mx_moe_unpermute(const void *in_bf16, int64_t R, int64_t D, c
 /*
  * mx_quantize_colsum_noalloc -- mx_quantize with MX_COLSUM for callers that
  * cannot allocate device memory: a framework hook that runs under a memory
- * pool it may not grow, a graph-capture region where allocation is not
- * allowed, or an embedding that owns all device memory up front.  The
+ * pool it may not grow, or an embedding that owns all device memory up
+ * front.  The
  * per-tile column-sum partials, which mx_quantize keeps in the caller's
  * workspace, live here in a fixed scratch array inside this library instead
  * (MX_NOALLOC_COLSUM_MAX_PARTIALS fp32 values = 8 MiB, held by every GPU that
@@ -276,7 +276,7 @@ MX_API mx_status_t mx_moe_unpermute(const void *in_bf16, int64_t R, int64_t D, c
  *   Limit: ceil(rows / 128) * cols <= MX_NOALLOC_COLSUM_MAX_PARTIALS, else
  *   MX_ERR_WORKSPACE (use mx_quantize with a workspace).
  *   The first call on a device looks up the scratch's device address
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   (cudaGetSymbolAddress, a host-side query), later calls reuse it.
  *   Every call shares the scratch: the partials are fully rewritten by each
  *   call before they are read, so nothing needs clearing, but calls whose
  *   execution overlaps on the GPU (different streams, no ordering) race on

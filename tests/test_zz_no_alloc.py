@@ -1,7 +1,7 @@
 """The no-allocation column-sum quantizer (mx_quantize_colsum_noalloc).
 
 Some callers cannot allocate device memory at the point where they quantize
-(a fixed memory pool, a capture region, an embedding that owns all memory):
+(a fixed memory pool, an embedding that owns all memory):
 this entry point keeps its column-sum partials in a fixed scratch array
 inside the library.  Its results must equal the workspace variant's, call
 after call, since every call shares and rewrites the same scratch.
