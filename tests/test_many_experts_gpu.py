@@ -146,3 +146,32 @@ def test_many_experts_wgrad(cuda_lib, G):
     active = np.flatnonzero(counts)
     assert O.within_tolerance(got[active], ref[active]).all()
     assert (got[np.flatnonzero(counts == 0)] == 0).all(), "an empty expert's slice is not zero"
+
+
+@pytest.mark.parametrize("G", [1024, 1100])
+def test_many_experts_dswiglu_bwd(cuda_lib, G):
+    """FC2 dgrad + dSwiGLU over G experts (one SM per tile, 128-column tiles
+    at F = 128): the epilogue's fp32 dz (debug tap) within tolerance of the
+    oracle's dSwiGLU of the exact dh and the saved z, and both requantized
+    orientations equal to the oracle's quantization of those fp32 values."""
+    import torch
+    counts, offsets, R = _routing(G, seed=G + 6)
+    D, F = 128, 128
+    rng = np.random.default_rng(G + 7)
+    dyb = W.normal_bf16(rng, (R, D), std=1e-3)
+    w2tb = W.normal_bf16(rng, (G, F, D), std=0.02)
+    zb = W.normal_bf16(rng, (R, 2 * F), std=2.0)
+    dyr, dyd = _quant_rows(cuda_lib, dyb)
+    w2tr, w2td = _quant_rows(cuda_lib, w2tb)
+    offs = torch.from_numpy(offsets).cuda()
+    A = int(offsets[-1])
+
+    def run():
+        dz_row, dz_col = cuda_lib.mx_grouped_gemm_dswiglu_bwd(dyr, w2tr, to_dev(zb), G, offs)
+        assert cuda_lib.mx_get_device_status() == "MX_OK"
+        return dz_row, dz_col
+
+    (dz_row, dz_col), tap = with_tap(cuda_lib, R, 2 * F, run)
+    ref = O.dswiglu_bwd(dyd, w2td, zb, offsets)
+    assert O.within_tolerance(tap[:A], ref["dz"]).all()
+    assert_tap_requant_exact(dz_row, dz_col, tap, A, 2 * F, R, what="dz")
