@@ -198,3 +198,44 @@ def test_gelu_step_elementwise(cuda_lib, H):
     _close(bf16_cpu(out["dx"]), _deq(V["dz_row"], fmt) @ _deq(V["w1t_row"], fmt).T, "dx")
     _close(bf16_cpu(out["dw2"]), _deq(V["dy_col"], fmt) @ _deq(V["h_col"], fmt).T, "dw2")
     _close(bf16_cpu(out["dw1"]), _deq(V["dz_col"], fmt) @ _deq(V["x_col"], fmt).T, "dw1")
+
+
+@pytest.mark.parametrize("counts", [[0, 0, 0, 0], [0, 1024, 0, 0]])
+def test_swiglu_step_degenerate_routing(cuda_lib, counts):
+    """No routed rows at all (every expert empty, R rows of inactive tail),
+    and every routed row on one expert: the step runs clean; with no rows
+    y and dX stay untouched and both weight gradients are exactly zero; with
+    one expert the other experts' gradient slices are exactly zero and the
+    busy expert's dW2 is held to the oracle on the step's own operands."""
+    import torch
+    mx = cuda_lib
+    G, D, F, R = 4, 512, 256, 1152
+    offsets = _offsets(counts)
+    A = int(offsets[-1])
+    inp = W.moe_inputs(G, D, F, R, seed=23)
+    t = {k: to_dev(v) for k, v in inp.items()}
+    out = {"y": torch.full((R, D), float("nan"), dtype=torch.bfloat16, device="cuda"),
+           "dx": torch.full((R, D), float("nan"), dtype=torch.bfloat16, device="cuda"),
+           "dw1": torch.full((G, 2 * F, D), float("nan"), dtype=torch.bfloat16, device="cuda"),
+           "dw2": torch.full((G, D, F), float("nan"), dtype=torch.bfloat16, device="cuda")}
+    offs = torch.from_numpy(offsets).cuda()
+    a0 = mx.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], offs, G, F, out["y"], out["dx"], out["dw1"], out["dw2"])
+    ws = torch.zeros(mx.mx_mlp_workspace_bytes(a0), dtype=torch.uint8, device="cuda")
+    args = mx.mlp_args(t["x"], t["w1"], t["w2"], t["dy"], offs, G, F, out["y"], out["dx"], out["dw1"],
+                       out["dw2"], workspace=ws)
+    mx.mx_mlp_fwd_bwd(args)
+    assert mx.mx_get_device_status() == "MX_OK"
+    y, dx = bf16_cpu(out["y"]), bf16_cpu(out["dx"])
+    assert np.isnan(y[A:]).all() and np.isnan(dx[A:]).all(), "rows past the routed segments were written"
+    assert np.isfinite(y[:A]).all() and np.isfinite(dx[:A]).all()
+    dw1, dw2 = bf16_cpu(out["dw1"]), bf16_cpu(out["dw2"])
+    for g in range(G):
+        if counts[g] == 0:
+            assert (dw1[g] == 0).all() and (dw2[g] == 0).all(), "empty expert %d" % g
+    if A:
+        g = int(np.flatnonzero(counts)[0])
+        V = mx.mlp_workspace_views(args, ws)
+        E = O.E4M3
+        dyc = _deq(V["dy_col"], E)[:, :A]   # [D, A]
+        hc = _deq(V["h_col"], E)[:, :A]     # [F, A]
+        _close(dw2[g], dyc @ hc.T, "dW2 of the busy expert")
