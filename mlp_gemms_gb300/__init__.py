@@ -340,7 +340,8 @@ def mx_grouped_gemm(a, b, G, offsets, out=None, ld_out=None, stream=None):
 
 
 def mx_grouped_gemm_2sm(a, b, G, offsets, out=None, ld_out=None, stream=None):
-    """mx_grouped_gemm on CTA pairs (256-row tiles; segments multiples of 256)."""
+    """mx_grouped_gemm on CTA pairs (256-row tiles; segments multiples of
+    128, a 128-row remainder's upper half computed and not stored)."""
     import torch
     N = b.rows // G if G else 0
     if out is None:

@@ -4,6 +4,8 @@
 // torchao PR #5 "MXFP8 cudnn-fe Swiglu fused Grouped MLP fwd/bwd and wgrad
 // group gemm", cudnn-fe ops commit: its kernels take 256-row MMA tiles on
 // two SMs and need every expert's segment to be a multiple of 256 rows.
+// This one takes 128-row segments too: an expert with an odd number of
+// 128-row blocks computes its last tile's upper half and does not store it.
 //
 // A pair of CTAs (a cluster of two) takes a 256 x 256 output tile: each CTA
 // loads its own 128 rows of A and its own half (128 rows) of the tile's B
